@@ -1,0 +1,359 @@
+"""Pins of the float64 oracle against facts fixed outside the oracle itself.
+
+Each test checks the oracle against one of: values the pages print (tests/golden/),
+hand-derived arithmetic on exactly representable inputs, the closed form of
+Newton-Schulz on a matrix with a known SVD, brute-force pure-Python loops on tiny
+shapes, algebraic identities (gram form == standard form), or special cases.
+No expected value here comes from the CUDA path.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- constants (pages)
+
+def test_coefficients_match_pages():
+    g = _golden("pages_constants.json")
+    c = g["ns_coefficients"]
+    assert (oracle.NS_A, oracle.NS_B, oracle.NS_C) == (c["a"], c["b"], c["c"])
+    assert oracle.NS_STEPS == c["steps"]
+    assert set(oracle.NS_METHODS) == set(g["ns_methods"]["methods"])
+    assert oracle.muon_ref.NS_METHOD_DEFAULT == g["ns_methods"]["default"]
+    d = g["muon_defaults"]
+    assert oracle.muon_ref.MUON_LR_DEFAULT == d["lr"]
+    assert oracle.muon_ref.MUON_MOMENTUM_DEFAULT == d["momentum"]
+    a = g["adam_defaults"]
+    assert oracle.muon_ref.ADAM_LR_DEFAULT == a["lr"]
+    assert list(oracle.muon_ref.ADAM_BETAS_DEFAULT) == a["betas"]
+    assert oracle.muon_ref.ADAM_EPS_DEFAULT == a["eps"]
+
+
+# ---------------------------------------------------------------- routing
+
+def test_routing_cases_from_prose():
+    cases = _golden("routing_cases.json")["cases"]
+    for name, ndim, expected, why in cases:
+        assert oracle.route(name, ndim) is expected, (name, ndim, why)
+
+
+def test_matrix_view_shape():
+    assert oracle.matrix_view_shape((6, 4)) == (6, 4)
+    assert oracle.matrix_view_shape((8, 3, 3, 2)) == (8, 18)
+    with pytest.raises(ValueError):
+        oracle.matrix_view_shape((5,))
+
+
+# ---------------------------------------------------------------- packing (hand values)
+
+def test_pack_offsets_by_hand():
+    # 2x3 = 6 elements at 0, next start rounds 6 up to 64; 4x4 = 16 at 64 ends at 80 ->
+    # 128; 1x65 at 128 ends at 193 -> total rounds to 256.
+    offs, total = oracle.pack_offsets([(2, 3), (4, 4), (1, 65)], align=64)
+    assert offs == [0, 64, 128] and total == 256
+    offs, total = oracle.pack_offsets([(2, 3), (4, 4), (1, 65)], align=1)
+    assert offs == [0, 6, 22] and total == 87
+    offs, total = oracle.pack_offsets([(8, 8)], align=64)
+    assert offs == [0] and total == 64
+    with pytest.raises(ValueError):
+        oracle.pack_offsets([(0, 3)])
+
+
+# ---------------------------------------------------------------- momentum (hand values)
+
+def test_momentum_by_hand():
+    g = np.array([1.0, -2.0, 0.5, 0.0])
+    m = np.array([0.5, 0.25, -1.0, 2.0])
+    mu = 0.5
+    # M_new = mu*M + G = [1.25, -1.875, 0.0, 1.0]
+    # Nesterov U = G + mu*M_new = [1.625, -2.9375, 0.5, 0.5]; plain U = M_new
+    m_new, u = oracle.momentum_update(g, m, mu, nesterov=True)
+    assert np.array_equal(m_new, [1.25, -1.875, 0.0, 1.0])
+    assert np.array_equal(u, [1.625, -2.9375, 0.5, 0.5])
+    m_new2, u2 = oracle.momentum_update(g, m, mu, nesterov=False)
+    assert np.array_equal(m_new2, m_new) and np.array_equal(u2, m_new)
+
+
+def test_normalize_by_hand():
+    u = np.array([[3.0, 0.0], [0.0, 4.0]])
+    x = oracle.frobenius_normalize(u, eps=0.0)
+    assert np.array_equal(x, u / 5.0)
+    x = oracle.frobenius_normalize(np.zeros((2, 2)), eps=1e-7)
+    assert np.array_equal(x, np.zeros((2, 2)))
+
+
+# ---------------------------------------------------------------- scalar polynomial
+
+def test_scalar_polynomial_by_hand():
+    # p(1) = a + b + c = 3.4445 - 4.7750 + 2.0315 = 0.701
+    assert oracle.ns_poly(1.0) == pytest.approx(0.701, abs=1e-15)
+    # p(0.5) = 1.72225 - 0.596875 + 0.063484375 = 1.188859375
+    assert oracle.ns_poly(0.5) == pytest.approx(1.188859375, abs=1e-15)
+    assert oracle.ns_poly(0.0) == 0.0
+    xs = np.linspace(-1, 1, 11)
+    assert np.allclose(oracle.ns_poly(-xs), -oracle.ns_poly(xs))
+    # composition: p5(1) = p(p(p(p(0.701))))
+    y = 1.0
+    for _ in range(5):
+        y = 3.4445 * y - 4.7750 * y ** 3 + 2.0315 * y ** 5
+    assert oracle.ns_poly_iterated(1.0) == pytest.approx(y, abs=1e-15)
+
+
+def test_iterated_polynomial_band():
+    # Singular values in [0.01, 1] land in a band around 1 after five steps: the
+    # iteration's purpose (orthogonalisation up to a bounded spread).
+    xs = np.linspace(0.01, 1.0, 2000)
+    ys = oracle.ns_poly_iterated(xs)
+    assert ys.min() > 0.68 and ys.max() < 1.14
+
+
+# ---------------------------------------------------------------- NS closed form via SVD
+
+def _known_svd(m, n, sigmas, seed):
+    rng = np.random.default_rng(seed)
+    uu, _ = np.linalg.qr(rng.standard_normal((m, m)))
+    vv, _ = np.linalg.qr(rng.standard_normal((n, m)))
+    return uu, np.asarray(sigmas, dtype=np.float64), vv
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+@pytest.mark.parametrize("m,n", [(4, 4), (5, 9), (16, 40), (32, 32)])
+def test_ns_closed_form(method, m, n):
+    # For X = U diag(s) V^T every step maps singular values through p and keeps the
+    # singular vectors; so NS(X) = U diag(p^5(s)) V^T.
+    rng = np.random.default_rng(m * 100 + n)
+    sig = np.sort(rng.uniform(0.02, 1.0, m))[::-1] * np.logspace(0, -2, m)
+    uu, s, vv = _known_svd(m, n, sig, seed=m + n)
+    x = (uu * s) @ vv.T
+    x = x / np.linalg.norm(x)  # singular values now s/||s||
+    s_n = s / np.linalg.norm(s)
+    expected = (uu * oracle.ns_poly_iterated(s_n)) @ vv.T
+    got = oracle.newton_schulz(x, method)
+    assert np.max(np.abs(got - expected)) < 1e-10
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_orthogonalize_closed_form_with_norm(method):
+    # orthogonalize divides by ||U||_F + eps before iterating.
+    m, n = 6, 10
+    uu, s, vv = _known_svd(m, n, [5.0, 3.0, 2.0, 1.0, 0.5, 0.01], seed=7)
+    g = (uu * s) @ vv.T
+    expected = (uu * oracle.ns_poly_iterated(s / (np.linalg.norm(s) + 1e-7))) @ vv.T
+    assert np.max(np.abs(oracle.orthogonalize(g, method) - expected)) < 1e-10
+    # tall input takes the transposed path and comes back in the input's shape
+    got_t = oracle.orthogonalize(g.T, method)
+    assert got_t.shape == (n, m)
+    assert np.max(np.abs(got_t - expected.T)) < 1e-10
+
+
+def test_transpose_rule_is_strict():
+    # square: no transpose; mathematically NS(X) == NS(X^T)^T for square X too, so
+    # check the rule through shapes of a wide and a tall case instead.
+    rng = np.random.default_rng(3)
+    wide = rng.standard_normal((3, 7))
+    tall = wide.T.copy()
+    ow = oracle.orthogonalize(wide, "standard")
+    ot = oracle.orthogonalize(tall, "standard")
+    assert np.max(np.abs(ot - ow.T)) < 1e-12
+
+
+# ---------------------------------------------------------------- special cases
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_zero_gradient(method):
+    o = oracle.orthogonalize(np.zeros((4, 8)), method)
+    assert np.array_equal(o, np.zeros((4, 8)))
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_rank_one(method):
+    rng = np.random.default_rng(11)
+    u = rng.standard_normal(5)
+    v = rng.standard_normal(9)
+    u /= np.linalg.norm(u)
+    v /= np.linalg.norm(v)
+    sigma = 3.7
+    g = sigma * np.outer(u, v)
+    expected = oracle.ns_poly_iterated(sigma / (sigma + 1e-7)) * np.outer(u, v)
+    assert np.max(np.abs(oracle.orthogonalize(g, method) - expected)) < 1e-12
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_orthonormal_rows(method):
+    rng = np.random.default_rng(5)
+    q, _ = np.linalg.qr(rng.standard_normal((12, 4)))
+    rows = q.T  # 4 x 12 with orthonormal rows
+    scale = 2.5
+    g = scale * rows
+    # ||g||_F = scale*sqrt(4): every singular value of X is scale/(2*scale + eps)
+    s = scale / (scale * 2.0 + 1e-7)
+    expected = oracle.ns_poly_iterated(s) * rows
+    assert np.max(np.abs(oracle.orthogonalize(g, method) - expected)) < 1e-12
+
+
+# ---------------------------------------------------------------- gram == standard
+
+@pytest.mark.parametrize("m,n", [(8, 8), (8, 64), (24, 40), (1, 5)])
+def test_gram_equals_standard(m, n):
+    rng = np.random.default_rng(m * 7 + n)
+    x = rng.standard_normal((m, n))
+    x /= np.linalg.norm(x)
+    a = oracle.ns_standard(x)
+    b = oracle.ns_gram(x)
+    assert np.max(np.abs(a - b)) < 1e-10
+
+
+@pytest.mark.parametrize("steps", [1, 2, 3, 7])
+def test_gram_equals_standard_other_step_counts(steps):
+    rng = np.random.default_rng(steps)
+    x = rng.standard_normal((6, 13))
+    x /= np.linalg.norm(x)
+    assert np.max(np.abs(oracle.ns_standard(x, steps) - oracle.ns_gram(x, steps))) < 1e-10
+
+
+# ---------------------------------------------------------------- brute force loops
+
+def _mm(a, b):
+    n, k, m = len(a), len(b), len(b[0])
+    return [[sum(a[i][t] * b[t][j] for t in range(k)) for j in range(m)] for i in range(n)]
+
+
+def _tr(a):
+    return [list(r) for r in zip(*a)]
+
+
+def _brute_ns(x, steps, a, b, c):
+    for _ in range(steps):
+        aa = _mm(x, _tr(x))
+        aa2 = _mm(aa, aa)
+        bb = [[b * aa[i][j] + c * aa2[i][j] for j in range(len(aa))] for i in range(len(aa))]
+        bx = _mm(bb, x)
+        x = [[a * x[i][j] + bx[i][j] for j in range(len(x[0]))] for i in range(len(x))]
+    return x
+
+
+@pytest.mark.parametrize("shape", [(2, 3), (3, 5), (4, 4), (5, 2), (1, 4)])
+def test_brute_force_tiny(shape):
+    rng = np.random.default_rng(sum(shape))
+    g = rng.standard_normal(shape)
+    rows, cols = shape
+    x = g.T if rows > cols else g
+    nrm = math.sqrt(sum(v * v for row in x.tolist() for v in row))
+    xl = [[v / (nrm + 1e-7) for v in row] for row in x.tolist()]
+    o = np.array(_brute_ns(xl, 5, 3.4445, -4.7750, 2.0315))
+    if rows > cols:
+        o = o.T
+    for method in ("standard", "gram"):
+        assert np.max(np.abs(oracle.orthogonalize(g, method) - o)) < 1e-12
+
+
+# ---------------------------------------------------------------- apply (hand values)
+
+def test_apply_by_hand():
+    p = np.array([[1.0, -2.0, 0.5, 4.0]])           # 1 x 4: scale sqrt(max(1, 1/4)) = 1
+    o = np.array([[0.5, 0.25, -1.0, 0.0]])
+    lr, wd = 0.5, 0.5                                # p*(1 - 0.25) - 0.5*o
+    expected = np.array([[0.5, -1.625, 0.875, 3.0]])
+    assert np.array_equal(oracle.apply_update(p, o, lr, wd), expected)
+    # 4 x 1: scale sqrt(4) = 2 -> p*0.75 - 1.0*o
+    expected_t = np.array([[0.25], [-1.75], [1.375], [3.0]])
+    assert np.array_equal(oracle.apply_update(p.T, o.T, lr, wd), expected_t)
+    assert oracle.update_scale(9, 4) == 1.5
+    assert oracle.update_scale(4, 9) == 1.0
+
+
+def test_muon_step_closed_form_row_vector():
+    # one 1x4 gradient [3,0,4,0], M=0, mu=0.5, Nesterov: M_new = g, U = 1.5 g,
+    # ||U|| = 7.5, X has the single singular value 7.5/(7.5+eps) with right vector g/5.
+    g = np.array([[3.0, 0.0, 4.0, 0.0]])
+    p = np.array([[1.0, 1.0, 1.0, 1.0]])
+    m = np.zeros((1, 4))
+    lr, wd = 0.1, 0.2
+    s = oracle.ns_poly_iterated(7.5 / (7.5 + 1e-7))
+    o = s * g / 5.0
+    for method in ("standard", "gram"):
+        (pn,), (mn,), (on,) = oracle.muon_step([g], [p], [m], lr, wd, mu=0.5, method=method)
+        assert np.array_equal(mn, g)
+        assert np.max(np.abs(on - o)) < 1e-14
+        assert np.max(np.abs(pn - (p * (1 - lr * wd) - lr * o))) < 1e-14
+        # tall version: scale 2 and the result is the transpose
+        (pt,), _, (ot,) = oracle.muon_step([g.T], [p.T], [m.T], lr, wd, mu=0.5, method=method)
+        assert np.max(np.abs(ot - o.T)) < 1e-14
+        assert np.max(np.abs(pt - (p.T * (1 - lr * wd) - lr * 2.0 * o.T))) < 1e-14
+
+
+# ---------------------------------------------------------------- AdamW (hand values)
+
+def test_adamw_two_steps_by_hand():
+    lr, b1, b2, eps, wd = 0.5, 0.5, 0.5, 0.0, 0.5
+    p, m, v = np.array([1.0]), np.array([0.0]), np.array([0.0])
+    # step 1, g = 2: m = 1, v = 2; m_hat = 2, v_hat = 4; step = 2/2 = 1
+    # p = 1*(1 - 0.25) - 0.5*1 = 0.25
+    p, m, v = oracle.adamw_step(np.array([2.0]), p, m, v, lr, b1, b2, eps, wd, 1)
+    assert (p[0], m[0], v[0]) == (0.25, 1.0, 2.0)
+    # step 2, g = -2: m = 0.5 - 1 = -0.5, v = 1 + 2 = 3; m_hat = -0.5/0.75 = -2/3,
+    # v_hat = 3/0.75 = 4; step = (-2/3)/2 = -1/3; p = 0.25*0.75 + 0.5/3
+    p, m, v = oracle.adamw_step(np.array([-2.0]), p, m, v, lr, b1, b2, eps, wd, 2)
+    assert m[0] == -0.5 and v[0] == 3.0
+    assert p[0] == pytest.approx(0.1875 + 0.5 / 3.0, abs=1e-15)
+
+
+def test_adamw_eps_outside_sqrt():
+    # with v = 0 the step is m_hat / eps exactly (eps outside the square root)
+    p, m, v = oracle.adamw_step(np.array([0.0]), np.array([0.0]), np.array([1.0]),
+                                np.array([0.0]), 1.0, 0.5, 0.5, 0.25, 0.0, 1)
+    # m = 0.5, m_hat = 1, v_hat = 0 -> step = 1/0.25 = 4
+    assert p[0] == -4.0
+
+
+# ---------------------------------------------------------------- bf16 decode, flops
+
+def test_bf16_decode():
+    bits = np.array([0x3F80, 0xBF80, 0x4049, 0x0000, 0x7F80], dtype=np.uint16)
+    vals = oracle.bf16_bits_to_f64(bits)
+    assert vals[0] == 1.0 and vals[1] == -1.0 and vals[3] == 0.0 and np.isinf(vals[4])
+    assert vals[2] == 3.140625
+
+
+def _count_macs_standard(m, n, steps):
+    macs = 0
+    for _ in range(steps):
+        macs += m * m * n        # X X^T
+        macs += m * m * m        # A A
+        macs += m * m * n        # B X
+    return 2 * macs
+
+
+def test_flop_counts():
+    for m, n in [(2, 3), (128, 4096), (4096, 11008)]:
+        assert oracle.flops_standard(m, n) == _count_macs_standard(m, n, 5)
+    # gram, 5 steps: R0 and Q X0 (m^2 n MACs each); R R x5; H Q x4; H R H = 2 per step x4
+    m, n = 7, 11
+    assert oracle.flops_gram(m, n) == 2 * (2 * m * m * n + (5 + 4 + 8) * m ** 3)
+
+
+# ---------------------------------------------------------------- page arithmetic
+
+def test_page_memory_arithmetic():
+    g = _golden("pages_constants.json")
+    mem = g["memory_per_param_bytes"]
+    w = mem["world"]
+    assert 2 + 2 + 4 + 4 + 4 == mem["no_shard"]
+    assert 2 + 2 + (4 + 4 + 4) / w == mem["zero1"]
+    assert 2 + (2 + 4 + 4 + 4) / w == mem["zero2"]
+    assert (2 + 2 + 4 + 4 + 4) / w == mem["zero3"]
+    d = g["dmuon_z2_example"]
+    assert d["params_muon"] * d["bytes_per_elem"] / d["shards"] / 1e6 == d["per_rank_mb"]
