@@ -1,0 +1,166 @@
+/*
+ * nsmuon.h — C ABI of the GB300 (sm_103a) owner-side Muon optimizer step.
+ *
+ * One shared library, libnsmuon.so.  Every entry point takes plain pointers and sizes;
+ * no framework types cross this boundary.  All device work is launched asynchronously
+ * on the stream the caller passes (NULL = the legacy default stream).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [DSM]  "DeepSpeed 集成 Muon 优化器实战：从正交化原理到 ZeRO 微调配置"
+ *   [DMZ]  "Z2 与 Z3 模式" (DMuon guide)
+ *
+ * Conventions shared by every call
+ *   - Return value: NSM_OK (0) on success, a negative NSM_ERR_* code otherwise.  When
+ *     argument validation fails nothing is launched and nsm_last_error() describes why.
+ *     Kernel launches are asynchronous: a fault inside a kernel surfaces at the next
+ *     synchronising CUDA call, and a bounded wait that expired inside a kernel is
+ *     reported by nsm_device_status().
+ *   - Ownership: the caller owns every buffer (device memory, host tables, workspace,
+ *     stream).  Host tables are read during the call only.  The library keeps a small
+ *     cache of launch plans (tensor maps and work lists, in device memory it allocates
+ *     itself on the first call for a given table/workspace pair); it never frees or
+ *     writes anything the caller owns except the documented outputs and the workspace.
+ *     Because building a plan allocates, the first call for a new table/workspace pair
+ *     should not be made inside CUDA stream capture.
+ *   - Packed layout: a Muon group is one contiguous buffer; matrix i (rows x cols,
+ *     row-major) starts at element offsets[i].  Offsets must be multiples of 8 elements,
+ *     matrices must not overlap, and every base pointer must be 16-byte aligned.
+ *   - shapes is a host array of n pairs {rows, cols} (int32, rows-then-cols).
+ *   - Not thread-safe per workspace: two calls that share a workspace must be ordered
+ *     on one stream.
+ */
+#ifndef NSMUON_H
+#define NSMUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st* nsm_stream_t;
+
+#define NSM_OK             0
+#define NSM_ERR_NULL      -1  /* a required pointer is NULL */
+#define NSM_ERR_SHAPE     -2  /* n <= 0, rows or cols <= 0, or a size overflows */
+#define NSM_ERR_OFFSET    -3  /* offsets overlap, are negative or not increasing */
+#define NSM_ERR_ALIGN     -4  /* pointer or offset misaligned */
+#define NSM_ERR_METHOD    -5  /* unknown ns_method or ns_steps out of [0, 16] */
+#define NSM_ERR_WORKSPACE -6  /* workspace NULL or smaller than muon_workspace_bytes() */
+#define NSM_ERR_CUDA      -7  /* a CUDA runtime/driver call failed */
+#define NSM_ERR_TIMEOUT   -8  /* a bounded in-kernel wait expired (nsm_device_status) */
+#define NSM_ERR_ARG       -9  /* any other invalid argument */
+
+#define NSM_NS_STANDARD 0     /* quintic Newton-Schulz on X, bf16 storage  [DSM §核心算子] */
+#define NSM_NS_GRAM     1     /* gram form on R = X X^T, fp16 storage       [DSM §核心算子] */
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int nsm_version(void);
+
+/* Message of the last failing call on this host thread ("" if none).  The pointer
+ * stays valid until the next library call on the same thread. */
+const char* nsm_last_error(void);
+
+/* Routing rule of [DSM] §use_muon参数打标: returns 1 (Muon group) when ndim >= 2 and the
+ * lower-cased name contains neither "embed" nor "lm_head", 0 (AdamW group) otherwise,
+ * NSM_ERR_NULL if name is NULL.  name: NUL-terminated, ASCII case folding only.
+ * Host-only; touches no GPU. */
+int nsm_route(const char* name, int ndim);
+
+/* Packed-buffer layout of [DMZ] §两种packed buffer生命周期 (one contiguous buffer per
+ * owner): offsets_out[i] = start of matrix i, each rounded up to a multiple of
+ * align_elems (>= 1, a multiple of 8 keeps the buffers usable by muon_step);
+ * *total_out = end of the last matrix rounded up likewise.  offsets_out has n entries
+ * (caller-allocated).  Host-only. */
+int nsm_pack(const int32_t* shapes, int n, int64_t align_elems,
+             int64_t* offsets_out, int64_t* total_out);
+
+/* Bytes of device workspace muon_step / muon_orthogonalize need for this table and
+ * method (independent of offsets).  Returns 0 when the arguments are invalid (the
+ * reason is in nsm_last_error()).  Host-only. */
+size_t muon_workspace_bytes(const int32_t* shapes, int n, int ns_method, int ns_steps);
+
+/* One owner-side Muon step over a packed group ([DSM] §什么是 Muon 优化器？,
+ * §核心算子; [DMZ] §两种packed buffer生命周期), for every matrix i:
+ *     M <- mu*M + G;   U = G + mu*M (nesterov != 0) or U = M (nesterov == 0)
+ *     X = U / (||U||_F + 1e-7), working on U^T when rows > cols
+ *     X <- ns_steps quintic Newton-Schulz steps (a, b, c) = (3.4445, -4.7750, 2.0315)
+ *          in the standard or gram form
+ *     p <- p*(1 - lr*wd) - lr*sqrt(max(1, rows/cols))*O      (O transposed back)
+ *   packed_grads  device, bf16 bits, read only
+ *   packed_params device, fp32, updated in place (the owner's master copy)
+ *   momentum      device, fp32, updated in place
+ *   offsets       host, n int64 element offsets (shared by the three buffers)
+ *   shapes        host, n {rows, cols}
+ *   workspace     device, >= muon_workspace_bytes(shapes, n, ns_method, ns_steps)
+ *                 bytes, 256-byte aligned; overwritten; contents not needed between calls
+ *   stream        stream to launch on
+ * Grads must not alias params or momentum.  Deterministic: identical inputs give
+ * bit-identical outputs, and a matrix's result does not depend on the other matrices
+ * in the table. */
+int muon_step(const void* packed_grads, float* packed_params, float* momentum,
+              const int64_t* offsets, const int32_t* shapes, int n,
+              float lr, float wd, float mu, int ns_method, int ns_steps, int nesterov,
+              void* workspace, size_t workspace_bytes, nsm_stream_t stream);
+
+/* Orthogonalisation only: out_i = NS(in_i / (||in_i||_F + 1e-7)) for every matrix of a
+ * packed bf16 group (the same transpose rule and methods as muon_step).  in_bf16 and
+ * out_bf16 are device bf16 buffers sharing the offsets table; they may not overlap.
+ * Used to check and time the Newton-Schulz chain on its own. */
+int muon_orthogonalize(const void* in_bf16, void* out_bf16,
+                       const int64_t* offsets, const int32_t* shapes, int n,
+                       int ns_method, int ns_steps,
+                       void* workspace, size_t workspace_bytes, nsm_stream_t stream);
+
+/* Fused AdamW step on one flat group ([DSM] §混合优化器的参数组构造: parameters without
+ * use_muon go to AdamW; decoupled decay is the default mode):
+ *     m <- b1*m + (1-b1)*g;  v <- b2*v + (1-b2)*g^2
+ *     p <- p*(1 - lr*wd) - lr * (m/(1-b1^step)) / (sqrt(v/(1-b2^step)) + eps)
+ *   grads bf16 (device, read only); params, exp_avg, exp_avg_sq fp32 (device, updated
+ *   in place); numel >= 0 elements; step >= 1; all pointers 16-byte aligned. */
+int adamw_step(const void* grads, float* params, float* exp_avg, float* exp_avg_sq,
+               int64_t numel, float lr, float beta1, float beta2, float eps, float wd,
+               int step, nsm_stream_t stream);
+
+/* The tensor-core GEMM engine of the Newton-Schulz chain on one problem:
+ *     out = alpha * A . op(B) + beta * aux + diag * I
+ *   A      device, M x K row-major, row stride lda elements
+ *   B      device; b_mn_major == 0: N x K row-major (op(B) = B^T, "K-major"),
+ *          b_mn_major != 0: K x N row-major (op(B) = B, "MN-major"); row stride ldb
+ *   out    device, M x N row-major, row stride ldo (written)
+ *   aux    device, M x N row-major, row stride ldx, or NULL (then beta is ignored)
+ *   fp16   0: every operand is bf16; 1: every operand is fp16.  fp32 accumulation.
+ *   scratch device, >= 1024 bytes, 128-byte aligned (holds the tensor maps of the call)
+ * Row strides must be multiples of 8 elements (>= the row length), pointers 16-byte
+ * aligned, aux must not overlap out.  Exposed so the engine can be checked and timed
+ * on its own; muon_step and muon_orthogonalize use the same kernel. */
+int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
+             const void* aux, int ldx, int M, int N, int K, int b_mn_major, int fp16,
+             float alpha, float beta, float diag, void* scratch, size_t scratch_bytes,
+             nsm_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word that kernels set
+ * when a bounded wait expires.  *status_out = NSM_OK or NSM_ERR_TIMEOUT.  Returns
+ * NSM_ERR_CUDA if the synchronisation itself reports an error. */
+int nsm_device_status(nsm_stream_t stream, int* status_out);
+
+/* Kernel timing for profiling.  While enabled, every Newton-Schulz GEMM launch of
+ * muon_step / muon_orthogonalize is bracketed by CUDA events on the caller's stream.
+ * nsm_timing_read synchronises the recorded events and returns, summed since the last
+ * reset: *gemm_ms (device time of those launches), *gemm_launches, *gemm_flops
+ * (canonical flops they performed).  Any output pointer may be NULL. */
+int nsm_timing_enable(int enable);
+int nsm_timing_read(double* gemm_ms, int64_t* gemm_launches, double* gemm_flops);
+int nsm_timing_reset(void);
+
+/* Number of kernel launches the last successful muon_step / muon_orthogonalize /
+ * adamw_step call made on this host thread. */
+int nsm_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSMUON_H */

@@ -1,0 +1,339 @@
+"""Python binding of libnsmuon.so, the GB300 owner-side Muon optimizer step.
+
+This module only marshals arguments: it turns torch tensors into device pointers and
+host tables into C arrays and calls the C ABI declared in ``include/nsmuon.h``.  Every
+step of the optimizer runs in the library's CUDA kernels; there is no CPU fallback, and
+importing the binding fails loudly when the library has not been built.
+
+Names follow the pages ("DeepSpeed 集成 Muon 优化器实战"): ``ns_method`` is
+``"standard"`` or ``"gram"`` (default ``"gram"``), ``muon_lr`` / ``adam_lr`` override a
+group's ``lr``, the Muon group defaults are lr 0.02 and momentum 0.95, and the Adam group
+defaults are lr 3e-4, betas (0.9, 0.95) and eps 1e-10.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Iterable, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnsmuon.so")
+
+NSM_OK = 0
+NSM_ERR_NULL = -1
+NSM_ERR_SHAPE = -2
+NSM_ERR_OFFSET = -3
+NSM_ERR_ALIGN = -4
+NSM_ERR_METHOD = -5
+NSM_ERR_WORKSPACE = -6
+NSM_ERR_CUDA = -7
+NSM_ERR_TIMEOUT = -8
+NSM_ERR_ARG = -9
+
+NS_METHODS = {"standard": 0, "gram": 1}
+NS_METHOD_DEFAULT = "gram"
+NS_STEPS_DEFAULT = 5
+MUON_LR_DEFAULT = 0.02
+MUON_MOMENTUM_DEFAULT = 0.95
+ADAM_LR_DEFAULT = 3e-4
+ADAM_BETAS_DEFAULT = (0.9, 0.95)
+ADAM_EPS_DEFAULT = 1e-10
+
+_c_i32p = ctypes.POINTER(ctypes.c_int32)
+_c_i64p = ctypes.POINTER(ctypes.c_int64)
+_vp = ctypes.c_void_p
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class NsmError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"nsmuon error {code}: {message}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libnsmuon.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+    L = ctypes.CDLL(LIB_PATH)
+    L.nsm_version.restype = ctypes.c_int
+    L.nsm_last_error.restype = ctypes.c_char_p
+    L.nsm_last_launch_count.restype = ctypes.c_int
+    L.nsm_route.argtypes = [ctypes.c_char_p, ctypes.c_int]
+    L.nsm_route.restype = ctypes.c_int
+    L.nsm_pack.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int64, _c_i64p, _c_i64p]
+    L.nsm_pack.restype = ctypes.c_int
+    L.muon_workspace_bytes.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    L.muon_workspace_bytes.restype = ctypes.c_size_t
+    L.muon_step.argtypes = [_vp, _vp, _vp, _c_i64p, _c_i32p, ctypes.c_int, ctypes.c_float,
+                            ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                            ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+    L.muon_step.restype = ctypes.c_int
+    L.muon_orthogonalize.argtypes = [_vp, _vp, _c_i64p, _c_i32p, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+    L.muon_orthogonalize.restype = ctypes.c_int
+    L.adamw_step.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
+                             ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_int, _vp]
+    L.adamw_step.restype = ctypes.c_int
+    L.nsm_gemm.argtypes = [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
+                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                           ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp,
+                           ctypes.c_size_t, _vp]
+    L.nsm_gemm.restype = ctypes.c_int
+    L.nsm_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
+    L.nsm_device_status.restype = ctypes.c_int
+    L.nsm_timing_enable.argtypes = [ctypes.c_int]
+    L.nsm_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p,
+                                  ctypes.POINTER(ctypes.c_double)]
+    _lib = L
+    return L
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise NsmError(rc, last_error())
+    return rc
+
+
+def last_error() -> str:
+    return lib().nsm_last_error().decode("utf-8", "replace")
+
+
+def version() -> int:
+    return lib().nsm_version()
+
+
+def last_launch_count() -> int:
+    return lib().nsm_last_launch_count()
+
+
+def route(name: str, ndim: int) -> bool:
+    """Muon (True) or AdamW (False) for a named parameter of ``ndim`` dimensions."""
+    return bool(_check(lib().nsm_route(name.encode("utf-8"), int(ndim))))
+
+
+def _shapes_array(shapes: Sequence[Tuple[int, int]]) -> np.ndarray:
+    arr = np.ascontiguousarray(np.asarray(shapes, dtype=np.int32).reshape(-1, 2))
+    return arr
+
+
+def _i32p(a: np.ndarray):
+    return a.ctypes.data_as(_c_i32p)
+
+
+def _i64p(a: np.ndarray):
+    return a.ctypes.data_as(_c_i64p)
+
+
+def pack(shapes: Sequence[Tuple[int, int]], align: int = 64) -> Tuple[np.ndarray, int]:
+    """Offsets (int64 elements) and total length of the packed buffer for ``shapes``."""
+    s = _shapes_array(shapes)
+    n = s.shape[0]
+    offs = np.zeros(n, dtype=np.int64)
+    total = np.zeros(1, dtype=np.int64)
+    _check(lib().nsm_pack(_i32p(s), n, int(align), _i64p(offs), _i64p(total)))
+    return offs, int(total[0])
+
+
+def method_code(ns_method) -> int:
+    if isinstance(ns_method, str):
+        if ns_method not in NS_METHODS:
+            raise ValueError(f"ns_method must be one of {sorted(NS_METHODS)}")
+        return NS_METHODS[ns_method]
+    return int(ns_method)
+
+
+def workspace_bytes(shapes: Sequence[Tuple[int, int]], ns_method=NS_METHOD_DEFAULT,
+                    ns_steps: int = NS_STEPS_DEFAULT) -> int:
+    s = _shapes_array(shapes)
+    b = lib().muon_workspace_bytes(_i32p(s), s.shape[0], method_code(ns_method), int(ns_steps))
+    if b == 0:
+        raise NsmError(NSM_ERR_ARG, last_error())
+    return int(b)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def muon_step(grads, params, momentum, offsets, shapes, lr: float = MUON_LR_DEFAULT,
+              wd: float = 0.0, mu: float = MUON_MOMENTUM_DEFAULT,
+              ns_method=NS_METHOD_DEFAULT, ns_steps: int = NS_STEPS_DEFAULT,
+              nesterov: bool = True, workspace=None, stream=None) -> None:
+    """One owner-side Muon step on packed buffers (bf16 grads, fp32 params/momentum)."""
+    s = _shapes_array(shapes)
+    o = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+    ws_size = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().muon_step(_ptr(grads), _ptr(params), _ptr(momentum), _i64p(o), _i32p(s),
+                           s.shape[0], float(lr), float(wd), float(mu), method_code(ns_method),
+                           int(ns_steps), 1 if nesterov else 0, _ptr(workspace), ws_size,
+                           _stream_ptr(stream)))
+
+
+def muon_orthogonalize(inp, out, offsets, shapes, ns_method=NS_METHOD_DEFAULT,
+                       ns_steps: int = NS_STEPS_DEFAULT, workspace=None, stream=None) -> None:
+    """Newton-Schulz orthogonalisation of every matrix of a packed bf16 buffer."""
+    s = _shapes_array(shapes)
+    o = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+    ws_size = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().muon_orthogonalize(_ptr(inp), _ptr(out), _i64p(o), _i32p(s), s.shape[0],
+                                    method_code(ns_method), int(ns_steps), _ptr(workspace),
+                                    ws_size, _stream_ptr(stream)))
+
+
+def adamw_step(grads, params, exp_avg, exp_avg_sq, lr: float = ADAM_LR_DEFAULT,
+               beta1: float = ADAM_BETAS_DEFAULT[0], beta2: float = ADAM_BETAS_DEFAULT[1],
+               eps: float = ADAM_EPS_DEFAULT, wd: float = 0.0, step: int = 1,
+               stream=None) -> None:
+    """Fused AdamW on one flat group (bf16 grads, fp32 params and moments)."""
+    numel = 0 if params is None else params.numel()
+    _check(lib().adamw_step(_ptr(grads), _ptr(params), _ptr(exp_avg), _ptr(exp_avg_sq), numel,
+                            float(lr), float(beta1), float(beta2), float(eps), float(wd),
+                            int(step), _stream_ptr(stream)))
+
+
+def gemm(a, b, out, aux=None, b_mn_major: bool = False, alpha: float = 1.0, beta: float = 0.0,
+         diag: float = 0.0, scratch=None, stream=None) -> None:
+    """out = alpha * a @ op(b) + beta * aux + diag * I on the tensor-core engine.
+
+    ``a`` is M x K; ``b`` is N x K (op = transpose) or, with ``b_mn_major``, K x N.  All
+    tensors are 2D bf16 or all fp16, with unit column stride."""
+    import torch
+    M, K = a.shape
+    N = b.shape[1] if b_mn_major else b.shape[0]
+    fp16 = 1 if a.dtype == torch.float16 else 0
+    if scratch is None:
+        scratch = torch.empty(1024, dtype=torch.uint8, device=a.device)
+    _check(lib().nsm_gemm(_ptr(a), a.stride(0), _ptr(b), b.stride(0), _ptr(out), out.stride(0),
+                          _ptr(aux), 0 if aux is None else aux.stride(0), M, N, K,
+                          1 if b_mn_major else 0, fp16, float(alpha), float(beta), float(diag),
+                          _ptr(scratch), scratch.numel(), _stream_ptr(stream)))
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream; returns NSM_OK or NSM_ERR_TIMEOUT (and clears it)."""
+    v = ctypes.c_int(0)
+    _check(lib().nsm_device_status(_stream_ptr(stream), ctypes.byref(v)))
+    return v.value
+
+
+def timing_enable(on: bool = True) -> None:
+    lib().nsm_timing_enable(1 if on else 0)
+
+
+def timing_reset() -> None:
+    lib().nsm_timing_reset()
+
+
+def timing_read() -> Tuple[float, int, float]:
+    ms = ctypes.c_double(0)
+    n = ctypes.c_int64(0)
+    fl = ctypes.c_double(0)
+    lib().nsm_timing_read(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl))
+    return ms.value, n.value, fl.value
+
+
+# ---------------------------------------------------------------- optimizer wrapper
+
+class MuonAdamW:
+    """Hybrid optimizer state over named parameters, on one GPU.
+
+    Parameters tagged by :func:`route` go to one packed Muon group (fp32 master params,
+    fp32 momentum, a bf16 gradient buffer); the rest go to one flat AdamW group.  The
+    config keys mirror the pages: ``muon_lr`` / ``adam_lr`` override ``lr``, ``momentum``,
+    ``weight_decay``, ``betas``, ``eps`` and ``ns_method``.
+    """
+
+    def __init__(self, named_shapes: Iterable[Tuple[str, Tuple[int, ...]]], device="cuda",
+                 lr: Optional[float] = None, muon_lr: Optional[float] = None,
+                 adam_lr: Optional[float] = None, momentum: float = MUON_MOMENTUM_DEFAULT,
+                 weight_decay: float = 0.0, betas=ADAM_BETAS_DEFAULT,
+                 eps: float = ADAM_EPS_DEFAULT, ns_method: str = NS_METHOD_DEFAULT,
+                 ns_steps: int = NS_STEPS_DEFAULT, nesterov: bool = True):
+        import torch
+        named = list(named_shapes)
+        self.muon_names: List[str] = []
+        self.muon_shapes: List[Tuple[int, int]] = []
+        self.adam_names: List[str] = []
+        self.adam_sizes: List[int] = []
+        for name, shape in named:
+            shape = tuple(int(d) for d in shape)
+            if route(name, len(shape)):
+                cols = 1
+                for d in shape[1:]:
+                    cols *= d
+                self.muon_names.append(name)
+                self.muon_shapes.append((shape[0], cols))
+            else:
+                size = 1
+                for d in shape:
+                    size *= d
+                self.adam_names.append(name)
+                self.adam_sizes.append(size)
+        base_lr = lr
+        self.muon_lr = muon_lr if muon_lr is not None else (base_lr if base_lr is not None else MUON_LR_DEFAULT)
+        self.adam_lr = adam_lr if adam_lr is not None else (base_lr if base_lr is not None else ADAM_LR_DEFAULT)
+        self.momentum = momentum
+        self.weight_decay = weight_decay
+        self.betas = tuple(betas)
+        self.eps = eps
+        self.ns_method = ns_method
+        self.ns_steps = ns_steps
+        self.nesterov = nesterov
+        self.step_count = 0
+        dev = torch.device(device)
+        if self.muon_shapes:
+            self.offsets, total = pack(self.muon_shapes)
+            self.muon_params = torch.zeros(total, dtype=torch.float32, device=dev)
+            self.muon_momentum = torch.zeros(total, dtype=torch.float32, device=dev)
+            self.muon_grads = torch.zeros(total, dtype=torch.bfloat16, device=dev)
+            self.workspace = torch.empty(workspace_bytes(self.muon_shapes, ns_method, ns_steps),
+                                         dtype=torch.uint8, device=dev)
+        n_adam = sum(self.adam_sizes)
+        self.adam_params = torch.zeros(n_adam, dtype=torch.float32, device=dev)
+        self.adam_exp_avg = torch.zeros(n_adam, dtype=torch.float32, device=dev)
+        self.adam_exp_avg_sq = torch.zeros(n_adam, dtype=torch.float32, device=dev)
+        self.adam_grads = torch.zeros(n_adam, dtype=torch.bfloat16, device=dev)
+
+    def step(self, stream=None) -> None:
+        self.step_count += 1
+        if self.muon_shapes:
+            muon_step(self.muon_grads, self.muon_params, self.muon_momentum, self.offsets,
+                      self.muon_shapes, self.muon_lr, self.weight_decay, self.momentum,
+                      self.ns_method, self.ns_steps, self.nesterov, self.workspace, stream)
+        if self.adam_params.numel():
+            adamw_step(self.adam_grads, self.adam_params, self.adam_exp_avg, self.adam_exp_avg_sq,
+                       self.adam_lr, self.betas[0], self.betas[1], self.eps, self.weight_decay,
+                       self.step_count, stream)
+
+    def state_dict(self) -> Dict[str, object]:
+        """Optimizer state as plain tensors (the caller saves and restores them)."""
+        d: Dict[str, object] = {"step": self.step_count,
+                                "adam_exp_avg": self.adam_exp_avg, "adam_exp_avg_sq": self.adam_exp_avg_sq}
+        if self.muon_shapes:
+            d["muon_momentum"] = self.muon_momentum
+        return d
+
+    def load_state_dict(self, d: Dict[str, object]) -> None:
+        self.step_count = int(d["step"])
+        self.adam_exp_avg.copy_(d["adam_exp_avg"])
+        self.adam_exp_avg_sq.copy_(d["adam_exp_avg_sq"])
+        if self.muon_shapes:
+            self.muon_momentum.copy_(d["muon_momentum"])

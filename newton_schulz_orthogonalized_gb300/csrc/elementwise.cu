@@ -1,0 +1,516 @@
+// Memory-bound kernels of the Muon step and the fused AdamW step.
+//
+//   k_momentum_norm  M <- mu M + G; U = G + mu M (Nesterov) or M; U stored bf16 in the
+//                    matrix's workspace slot; per-chunk sums of U^2 (fixed order)
+//   k_norm_finalize  s_i = 1 / (sqrt(sum of matrix i's chunk sums) + eps), fixed order
+//   k_to_class       X = s U moved from the natural row-major layout into the matrix's
+//                    slot (transposed when rows > cols), bf16 or fp16
+//   k_apply          p <- p (1 - lr wd) - lr sqrt(max(1, rows/cols)) O, O read back from
+//                    the slot (transposed back when rows > cols)
+//   k_export         O copied back to a natural bf16 layout
+//   k_adamw          decoupled-weight-decay Adam on a flat group
+//
+// Sources ("DeepSpeed 集成 Muon 优化器实战" §什么是 Muon 优化器？, §核心算子,
+// §混合优化器的参数组构造).  Every reduction runs in a fixed order, so results are
+// bit-identical from run to run.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "nsm_internal.h"
+
+namespace nsm {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ int find_by_chunk(const MatInfo* __restrict__ mats, int nmats, int c) {
+  int lo = 0, hi = nmats - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (mats[mid].chunk_begin <= c) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int find_by_tile(const MatInfo* __restrict__ mats, int nmats,
+                                            int64_t t) {
+  int lo = 0, hi = nmats - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (mats[mid].tile_begin <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 t = __bfloat1622float2(h[j]);
+    f[2 * j] = t.x;
+    f[2 * j + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&f)[8]) {
+  uint4 raw;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+  return raw;
+}
+
+__device__ __forceinline__ uint4 pack_f16x8(const float (&f)[8]) {
+  uint4 raw;
+  __half2* h = reinterpret_cast<__half2*>(&raw);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+  return raw;
+}
+
+__device__ __forceinline__ void unpack_f16x8(const uint4& raw, float (&f)[8]) {
+  const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 t = __half22float2(h[j]);
+    f[2 * j] = t.x;
+    f[2 * j + 1] = t.y;
+  }
+}
+
+template <bool FP16>
+__device__ __forceinline__ float load_half(const void* base, int64_t i) {
+  if (FP16) return __half2float(reinterpret_cast<const __half*>(base)[i]);
+  return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+}
+
+template <bool FP16>
+__device__ __forceinline__ void store_half(void* base, int64_t i, float v) {
+  if (FP16) reinterpret_cast<__half*>(base)[i] = __float2half_rn(v);
+  else reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+}
+
+template <bool FP16>
+__device__ __forceinline__ void load8(const void* base, int64_t i, float (&f)[8]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(
+      reinterpret_cast<const uint16_t*>(base) + i);
+  if (FP16) unpack_f16x8(raw, f); else unpack_bf16x8(raw, f);
+}
+
+template <bool FP16>
+__device__ __forceinline__ void store8(void* base, int64_t i, const float (&f)[8]) {
+  *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + i) =
+      FP16 ? pack_f16x8(f) : pack_bf16x8(f);
+}
+
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) scratch[warp] = v;
+  __syncthreads();
+  float s = 0.f;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kThreads / 32; ++w) s += scratch[w];
+  }
+  __syncthreads();
+  return s;
+}
+
+// ---------------------------------------------------------------- momentum + norm
+
+template <bool HAS_M, bool NESTEROV>
+__global__ void __launch_bounds__(kThreads)
+    k_momentum_norm(const __nv_bfloat16* __restrict__ grads, float* __restrict__ mom,
+                    __nv_bfloat16* __restrict__ u_base, const MatInfo* __restrict__ mats,
+                    int nmats, int total_chunks, float* __restrict__ partials, float mu) {
+  __shared__ float scratch[kThreads / 32];
+  for (int chunk = blockIdx.x; chunk < total_chunks; chunk += gridDim.x) {
+    const MatInfo& mt = mats[find_by_chunk(mats, nmats, chunk)];
+    const int64_t len = static_cast<int64_t>(mt.rows) * mt.cols;
+    const int64_t start = static_cast<int64_t>(chunk - mt.chunk_begin) * kChunk;
+    const int64_t end = min(start + static_cast<int64_t>(kChunk), len);
+    const __nv_bfloat16* g = grads + mt.off;
+    float* m = HAS_M ? mom + mt.off : nullptr;
+    __nv_bfloat16* u = HAS_M ? u_base + mt.slot : nullptr;
+    float acc = 0.f;
+    const int64_t nvec = (end - start) >> 3;
+    for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
+      const int64_t i = start + v * 8;
+      float gf[8];
+      unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(g + i)), gf);
+      if (HAS_M) {
+        float4* mp = reinterpret_cast<float4*>(m + i);
+        const float4 m0 = mp[0], m1 = mp[1];
+        float mf[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        float uf[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float mn = fmaf(mu, mf[j], gf[j]);
+          mf[j] = mn;
+          uf[j] = NESTEROV ? fmaf(mu, mn, gf[j]) : mn;
+          acc = fmaf(uf[j], uf[j], acc);
+        }
+        mp[0] = make_float4(mf[0], mf[1], mf[2], mf[3]);
+        mp[1] = make_float4(mf[4], mf[5], mf[6], mf[7]);
+        *reinterpret_cast<uint4*>(u + i) = pack_bf16x8(uf);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc = fmaf(gf[j], gf[j], acc);
+      }
+    }
+    for (int64_t i = start + nvec * 8 + threadIdx.x; i < end; i += kThreads) {
+      const float gv = __bfloat162float(g[i]);
+      if (HAS_M) {
+        const float mn = fmaf(mu, m[i], gv);
+        m[i] = mn;
+        const float uv = NESTEROV ? fmaf(mu, mn, gv) : mn;
+        u[i] = __float2bfloat16_rn(uv);
+        acc = fmaf(uv, uv, acc);
+      } else {
+        acc = fmaf(gv, gv, acc);
+      }
+    }
+    const float s = block_sum(acc, scratch);
+    if (threadIdx.x == 0) partials[chunk] = s;
+  }
+}
+
+__global__ void k_norm_finalize(const MatInfo* __restrict__ mats, int nmats,
+                                const float* __restrict__ partials, float* __restrict__ scales,
+                                float eps) {
+  const int w = static_cast<int>((blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= nmats) return;
+  const MatInfo& mt = mats[w];
+  float s = 0.f;
+  for (int c = lane; c < mt.nchunks; c += 32) s += partials[mt.chunk_begin + c];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) scales[w] = 1.0f / (sqrtf(s) + eps);
+}
+
+// ---------------------------------------------------------------- layout moves
+
+struct TilePos {
+  int mi;
+  int r0, c0;
+};
+
+__device__ __forceinline__ TilePos tile_pos(const MatInfo* __restrict__ mats, int nmats, int64_t t) {
+  const int mi = find_by_tile(mats, nmats, t);
+  const MatInfo& mt = mats[mi];
+  const int64_t local = t - mt.tile_begin;
+  const int tiles_c = (mt.cols + kTile - 1) / kTile;
+  const int tr = static_cast<int>(local / tiles_c);
+  const int tc = static_cast<int>(local - static_cast<int64_t>(tr) * tiles_c);
+  return {mi, tr * kTile, tc * kTile};
+}
+
+// Natural bf16 U (row stride cols) -> slot X (row stride ld), scaled; transposed when tall.
+template <bool TO_FP16>
+__global__ void __launch_bounds__(kThreads)
+    k_to_class(const __nv_bfloat16* __restrict__ src, int src_is_slot, void* __restrict__ dst,
+               const MatInfo* __restrict__ mats, int nmats, int64_t total_tiles,
+               const float* __restrict__ scales) {
+  __shared__ float tile[kTile][kTile + 1];
+  for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+    const TilePos tp = tile_pos(mats, nmats, t);
+    const MatInfo& mt = mats[tp.mi];
+    const __nv_bfloat16* s = src + (src_is_slot ? mt.slot : mt.off);
+    const int64_t d0 = mt.slot;
+    const float sc = scales[tp.mi];
+    const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
+    if (!mt.transposed) {
+      if (mt.vec_ok) {
+        for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+          const int r = tp.r0 + (j >> 3), c = tp.c0 + (j & 7) * 8;
+          if (r < rows && c < cols) {
+            float f[8];
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(s + static_cast<int64_t>(r) * cols + c)), f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] *= sc;
+            store8<TO_FP16>(dst, d0 + static_cast<int64_t>(r) * ld + c, f);
+          }
+        }
+      } else {
+        for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
+          const int r = tp.r0 + (j >> 6), c = tp.c0 + (j & 63);
+          if (r < rows && c < cols) {
+            const float v = __bfloat162float(s[static_cast<int64_t>(r) * cols + c]) * sc;
+            store_half<TO_FP16>(dst, d0 + static_cast<int64_t>(r) * ld + c, v);
+          }
+        }
+      }
+    } else {
+      // slot row = natural column c, slot column = natural row r
+      if (mt.vec_ok) {
+        for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+          const int rr = j >> 3, cc = (j & 7) * 8;
+          const int r = tp.r0 + rr, c = tp.c0 + cc;
+          float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (r < rows && c < cols) {
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(s + static_cast<int64_t>(r) * cols + c)), f);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) tile[rr][cc + q] = f[q];
+        }
+        __syncthreads();
+        for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+          const int cr = j >> 3, rc = (j & 7) * 8;  // slot row c0+cr, slot cols r0+rc..+7
+          const int c = tp.c0 + cr, r = tp.r0 + rc;
+          if (c < cols && r < rows) {
+            float f[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] = tile[rc + q][cr] * sc;
+            store8<TO_FP16>(dst, d0 + static_cast<int64_t>(c) * ld + r, f);
+          }
+        }
+      } else {
+        for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
+          const int rr = j >> 6, cc = j & 63;
+          const int r = tp.r0 + rr, c = tp.c0 + cc;
+          tile[rr][cc] = (r < rows && c < cols) ? __bfloat162float(s[static_cast<int64_t>(r) * cols + c]) : 0.f;
+        }
+        __syncthreads();
+        for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
+          const int cr = j >> 6, rc = j & 63;
+          const int c = tp.c0 + cr, r = tp.r0 + rc;
+          if (c < cols && r < rows) {
+            store_half<TO_FP16>(dst, d0 + static_cast<int64_t>(c) * ld + r, tile[rc][cr] * sc);
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Slot O -> natural layout.  APPLY: p <- p*decay - lr*scale*O.  Otherwise out = bf16(O).
+template <bool O_FP16, bool APPLY>
+__global__ void __launch_bounds__(kThreads)
+    k_from_class(const void* __restrict__ o, float* __restrict__ params,
+                 __nv_bfloat16* __restrict__ out, const MatInfo* __restrict__ mats, int nmats,
+                 int64_t total_tiles, float lr, float decay) {
+  __shared__ float tile[kTile][kTile + 1];
+  for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+    const TilePos tp = tile_pos(mats, nmats, t);
+    const MatInfo& mt = mats[tp.mi];
+    const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
+    const int64_t s0 = mt.slot;
+    const float coef = lr * mt.scale;
+    float* p = APPLY ? params + mt.off : nullptr;
+    __nv_bfloat16* ob = APPLY ? nullptr : out + mt.off;
+    if (mt.transposed) {
+      // tile[rr][cc] = O^T[r0+rr][c0+cc] = slot[c0+cc][r0+rr]
+      if (mt.vec_ok) {
+        for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+          const int cc = j >> 3, rr = (j & 7) * 8;
+          const int c = tp.c0 + cc, r = tp.r0 + rr;
+          float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (c < cols && r < rows) load8<O_FP16>(o, s0 + static_cast<int64_t>(c) * ld + r, f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) tile[rr + q][cc] = f[q];
+        }
+      } else {
+        for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
+          const int cc = j >> 6, rr = j & 63;
+          const int c = tp.c0 + cc, r = tp.r0 + rr;
+          tile[rr][cc] = (c < cols && r < rows) ? load_half<O_FP16>(o, s0 + static_cast<int64_t>(c) * ld + r) : 0.f;
+        }
+      }
+      __syncthreads();
+    }
+    if (mt.vec_ok) {
+      for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+        const int rr = j >> 3, cc = (j & 7) * 8;
+        const int r = tp.r0 + rr, c = tp.c0 + cc;
+        if (r < rows && c < cols) {
+          float f[8];
+          if (mt.transposed) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] = tile[rr][cc + q];
+          } else {
+            load8<O_FP16>(o, s0 + static_cast<int64_t>(r) * ld + c, f);
+          }
+          const int64_t i = static_cast<int64_t>(r) * cols + c;
+          if (APPLY) {
+            float4* pp = reinterpret_cast<float4*>(p + i);
+            float4 a = pp[0], b = pp[1];
+            a.x = fmaf(-coef, f[0], a.x * decay);
+            a.y = fmaf(-coef, f[1], a.y * decay);
+            a.z = fmaf(-coef, f[2], a.z * decay);
+            a.w = fmaf(-coef, f[3], a.w * decay);
+            b.x = fmaf(-coef, f[4], b.x * decay);
+            b.y = fmaf(-coef, f[5], b.y * decay);
+            b.z = fmaf(-coef, f[6], b.z * decay);
+            b.w = fmaf(-coef, f[7], b.w * decay);
+            pp[0] = a;
+            pp[1] = b;
+          } else {
+            *reinterpret_cast<uint4*>(ob + i) = pack_bf16x8(f);
+          }
+        }
+      }
+    } else {
+      for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
+        const int rr = j >> 6, cc = j & 63;
+        const int r = tp.r0 + rr, c = tp.c0 + cc;
+        if (r < rows && c < cols) {
+          const float ov = mt.transposed ? tile[rr][cc]
+                                         : load_half<O_FP16>(o, s0 + static_cast<int64_t>(r) * ld + c);
+          const int64_t i = static_cast<int64_t>(r) * cols + c;
+          if (APPLY) p[i] = fmaf(-coef, ov, p[i] * decay);
+          else ob[i] = __float2bfloat16_rn(ov);
+        }
+      }
+    }
+    if (mt.transposed) __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- AdamW
+
+__device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v, float b1,
+                                           float b2, float eps, float decay, float step_size,
+                                           float bc2) {
+  m = fmaf(b1, m, (1.0f - b1) * g);
+  v = fmaf(b2, v, (1.0f - b2) * g * g);
+  const float denom = sqrtf(v / bc2) + eps;
+  p = p * decay - step_size * (m / denom);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_adamw(const __nv_bfloat16* __restrict__ grads, float* __restrict__ params,
+            float* __restrict__ mom1, float* __restrict__ mom2, int64_t numel, float b1,
+            float b2, float eps, float decay, float step_size, float bc2) {
+  const int64_t nvec = numel >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t v = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; v < nvec; v += stride) {
+    const int64_t i = v * 8;
+    float g[8];
+    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(grads + i)), g);
+    float4* pp = reinterpret_cast<float4*>(params + i);
+    float4* mp = reinterpret_cast<float4*>(mom1 + i);
+    float4* vp = reinterpret_cast<float4*>(mom2 + i);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float4 p = pp[h], m = mp[h], w = vp[h];
+      adamw_elem(g[4 * h + 0], p.x, m.x, w.x, b1, b2, eps, decay, step_size, bc2);
+      adamw_elem(g[4 * h + 1], p.y, m.y, w.y, b1, b2, eps, decay, step_size, bc2);
+      adamw_elem(g[4 * h + 2], p.z, m.z, w.z, b1, b2, eps, decay, step_size, bc2);
+      adamw_elem(g[4 * h + 3], p.w, m.w, w.w, b1, b2, eps, decay, step_size, bc2);
+      pp[h] = p;
+      mp[h] = m;
+      vp[h] = w;
+    }
+  }
+  for (int64_t i = nvec * 8 + blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < numel; i += stride) {
+    float p = params[i], m = mom1[i], w = mom2[i];
+    adamw_elem(__bfloat162float(grads[i]), p, m, w, b1, b2, eps, decay, step_size, bc2);
+    params[i] = p;
+    mom1[i] = m;
+    mom2[i] = w;
+  }
+}
+
+int g_num_sms_cache[64] = {0};
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && g_num_sms_cache[dev] > 0) return g_num_sms_cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) g_num_sms_cache[dev] = n;
+  return n;
+}
+
+int grid_for(int64_t items, int per_sm) {
+  const int64_t cap = static_cast<int64_t>(num_sms()) * per_sm;
+  const int64_t g = items < cap ? items : cap;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_momentum_norm(const void* grads, float* momentum, void* u_base,
+                                 const MatInfo* mats, int nmats, int total_chunks,
+                                 float* partials, float mu, int nesterov, int has_momentum,
+                                 cudaStream_t stream) {
+  const int grid = grid_for(total_chunks, 8);
+  const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
+  auto* u = reinterpret_cast<__nv_bfloat16*>(u_base);
+  if (!has_momentum) {
+    k_momentum_norm<false, false><<<grid, kThreads, 0, stream>>>(g, nullptr, nullptr, mats, nmats,
+                                                                 total_chunks, partials, mu);
+  } else if (nesterov) {
+    k_momentum_norm<true, true><<<grid, kThreads, 0, stream>>>(g, momentum, u, mats, nmats,
+                                                               total_chunks, partials, mu);
+  } else {
+    k_momentum_norm<true, false><<<grid, kThreads, 0, stream>>>(g, momentum, u, mats, nmats,
+                                                                total_chunks, partials, mu);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(const MatInfo* mats, int nmats, const float* partials,
+                                 float* scales, float eps, cudaStream_t stream) {
+  const int warps_per_block = kThreads / 32;
+  const int grid = (nmats + warps_per_block - 1) / warps_per_block;
+  k_norm_finalize<<<grid, kThreads, 0, stream>>>(mats, nmats, partials, scales, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_class(const void* src, int src_is_slot, void* dst, int to_fp16,
+                            const MatInfo* mats, int nmats, int64_t total_tiles,
+                            const float* scales, cudaStream_t stream) {
+  const int grid = grid_for(total_tiles, 8);
+  const auto* s = reinterpret_cast<const __nv_bfloat16*>(src);
+  if (to_fp16) {
+    k_to_class<true><<<grid, kThreads, 0, stream>>>(s, src_is_slot, dst, mats, nmats, total_tiles, scales);
+  } else {
+    k_to_class<false><<<grid, kThreads, 0, stream>>>(s, src_is_slot, dst, mats, nmats, total_tiles, scales);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply(const void* o, int o_fp16, float* params, const MatInfo* mats,
+                         int nmats, int64_t total_tiles, float lr, float wd,
+                         cudaStream_t stream) {
+  const int grid = grid_for(total_tiles, 8);
+  const float decay = 1.0f - lr * wd;
+  if (o_fp16) {
+    k_from_class<true, true><<<grid, kThreads, 0, stream>>>(o, params, nullptr, mats, nmats, total_tiles, lr, decay);
+  } else {
+    k_from_class<false, true><<<grid, kThreads, 0, stream>>>(o, params, nullptr, mats, nmats, total_tiles, lr, decay);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* mats, int nmats,
+                          int64_t total_tiles, cudaStream_t stream) {
+  const int grid = grid_for(total_tiles, 8);
+  auto* ob = reinterpret_cast<__nv_bfloat16*>(out);
+  if (o_fp16) {
+    k_from_class<true, false><<<grid, kThreads, 0, stream>>>(o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f);
+  } else {
+    k_from_class<false, false><<<grid, kThreads, 0, stream>>>(o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(const void* grads, float* params, float* m, float* v, int64_t numel,
+                         float lr, float beta1, float beta2, float eps, float wd, float bc1,
+                         float bc2, cudaStream_t stream) {
+  if (numel <= 0) return cudaSuccess;
+  const int64_t items = (numel + 7) / 8;
+  const int grid = grid_for((items + kThreads - 1) / kThreads, 8);
+  const float decay = 1.0f - lr * wd;
+  const float step_size = lr / bc1;
+  k_adamw<<<grid, kThreads, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(grads), params, m, v,
+                                         numel, beta1, beta2, eps, decay, step_size, bc2);
+  return cudaGetLastError();
+}
+
+}  // namespace nsm

@@ -1,0 +1,401 @@
+// Grouped GEMM engine of the Newton-Schulz chain on the 5th-generation tensor cores.
+//
+// One persistent launch runs one stage of the chain (for example A = X X^T) for every
+// matrix of a packed group.  Matrices of the same working shape form a group whose
+// operands sit back to back in the workspace, so one 3D tensor map per buffer covers
+// the whole group.  Each CTA owns one SM and walks the flat tile list with a fixed
+// stride, so the result of every tile is computed by exactly one CTA in a fixed order
+// (bit-identical run to run).
+//
+// Per CTA: warp 0 issues TMA loads (128B-swizzled 64x64 boxes) into a 4-stage ring,
+// warp 1 issues tcgen05.mma (M=128, N<=256, K=16, fp32 accumulation in TMEM, two
+// accumulator buffers of 256 columns), warps 2-5 drain TMEM with tcgen05.ld and apply
+// the fused epilogue  out = alpha*acc + beta*aux + diag*I  before storing bf16/fp16.
+//
+// The stages it serves ("DeepSpeed 集成 Muon 优化器实战" §核心算子):
+//   standard:  A = X X^T;  B = b A + c A A^T (A symmetric);  X' = a X + B X
+//   gram:      R = X X^T;  H = a I + b R + c R R^T;  Q' = H Q^T;  T = H R^T;
+//              R' = T H^T;  O = Q X      (H, Q, R are symmetric polynomials of R_0)
+// B X and Q X read X as a K x N operand with N contiguous ("MN-major").
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "nsm_internal.h"
+#include "ptx.cuh"
+
+namespace nsm {
+
+__device__ int g_device_status = 0;
+
+int* device_status_ptr() {
+  int* p = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_device_status) != cudaSuccess) {
+    return nullptr;
+  }
+  return p;
+}
+
+namespace {
+
+constexpr int BM = 128;                   // MMA M (TMEM lanes)
+constexpr int BN = 256;                   // widest MMA N per tile
+constexpr int BK = 64;                    // K per stage: 64 16-bit elements = 128 B rows
+constexpr int STAGES = 4;
+constexpr int BOX_BYTES = 64 * 64 * 2;    // one TMA box: 64 rows x 128 B
+constexpr int A_BYTES = BM * BK * 2;      // 16 KB
+constexpr int B_BYTES = BN * BK * 2;      // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;          // 6 warps
+constexpr uint32_t TMEM_COLS = 512;       // 2 x 256 fp32 accumulator columns
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+
+struct Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int never;  // stays 0: the flag the teardown waits poll, so they ignore `abort`
+};
+
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl);
+
+struct TileCoord {
+  int g, b, m0, n0;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const GemmGroup* __restrict__ groups, int ng,
+                                                 int64_t t) {
+  int lo = 0, hi = ng - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (groups[mid].tile_begin <= t) lo = mid; else hi = mid - 1;
+  }
+  const GemmGroup& G = groups[lo];
+  const int64_t local = t - G.tile_begin;
+  const int per = G.tiles_m * G.tiles_n;
+  const int b = static_cast<int>(local / per);
+  const int rem = static_cast<int>(local - static_cast<int64_t>(b) * per);
+  const int mt = rem / G.tiles_n;
+  const int nt = rem - mt * G.tiles_n;
+  return {lo, b, mt * BM, nt * BN};
+}
+
+template <bool FP16>
+struct Elem;
+template <>
+struct Elem<false> {
+  using T = __nv_bfloat16;
+  __device__ static __forceinline__ float to_f(T v) { return __bfloat162float(v); }
+  __device__ static __forceinline__ T from_f(float v) { return __float2bfloat16_rn(v); }
+};
+template <>
+struct Elem<true> {
+  using T = __half;
+  __device__ static __forceinline__ float to_f(T v) { return __half2float(v); }
+  __device__ static __forceinline__ T from_f(float v) { return __float2half_rn(v); }
+};
+
+__device__ __forceinline__ void signal_timeout(Ctrl* ctrl, int* status) {
+  ctrl->abort = 1;
+  atomicExch(status, kDevTimeout);
+}
+
+template <bool B_MN, bool FP16, bool HAS_AUX>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_ns_gemm(const GemmGroup* __restrict__ groups, int ng, int64_t total_tiles, float alpha,
+              float beta, float diag, int* status) {
+  using E = Elem<FP16>;
+  using T = typename E::T;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + size_t(STAGES) * STAGE_BYTES);
+  const uint32_t ring = ptx::smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  auto bar = [&](uint64_t* b) { return ptx::smem_u32(b); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar(&ctrl->full[s]), 1);
+      ptx::mbar_init(bar(&ctrl->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(bar(&ctrl->acc_full[a]), 1);
+      ptx::mbar_init(bar(&ctrl->acc_empty[a]), 4);
+    }
+    ptx::mbar_init(bar(&ctrl->drain), 1);
+    ctrl->abort = 0;
+    ctrl->never = 0;
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctrl->tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctrl->tmem_base;
+  volatile int* abort_flag = &ctrl->abort;
+  volatile int* never_flag = &ctrl->never;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fill_parity[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) fill_parity[s] = -1;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const TileCoord tc = decode_tile(groups, ng, t);
+        const GemmGroup& G = groups[tc.g];
+        const int kblocks = (G.K + BK - 1) / BK;
+        const int n_len = min(BN, G.N - tc.n0);
+        const int nb = (n_len + 63) >> 6;
+        const int a_boxes = (G.M - tc.m0 > 64) ? 2 : 1;
+        const uint32_t bytes = static_cast<uint32_t>((a_boxes + nb) * BOX_BYTES);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(bar(&ctrl->empty[stage]), phase ^ 1u, abort_flag,
+                                      WAIT_LIMIT_NS)) {
+            signal_timeout(ctrl, status);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar(&ctrl->full[stage]);
+          ptx::mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t a_dst = ring + stage * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          const int k0 = kb * BK;
+          ptx::tma_load_3d(a_dst, G.map_a, fb, k0, tc.m0, tc.b);
+          if (a_boxes == 2) ptx::tma_load_3d(a_dst + BOX_BYTES, G.map_a, fb, k0, tc.m0 + 64, tc.b);
+          for (int q = 0; q < nb; ++q) {
+            if (B_MN) {
+              ptx::tma_load_3d(b_dst + q * BOX_BYTES, G.map_b, fb, tc.n0 + 64 * q, k0, tc.b);
+            } else {
+              ptx::tma_load_3d(b_dst + q * BOX_BYTES, G.map_b, fb, k0, tc.n0 + 64 * q, tc.b);
+            }
+          }
+          fill_parity[stage] = static_cast<int>(phase);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let every copy already issued land before the block can exit.
+        for (int s = 0; s < STAGES; ++s) {
+          if (fill_parity[s] >= 0) {
+            ptx::mbar_wait_bounded(bar(&ctrl->full[s]), static_cast<uint32_t>(fill_parity[s]),
+                                   never_flag, WAIT_LIMIT_NS);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++local) {
+        const TileCoord tc = decode_tile(groups, ng, t);
+        const GemmGroup& G = groups[tc.g];
+        const int kblocks = (G.K + BK - 1) / BK;
+        const int n_len = min(BN, G.N - tc.n0);
+        const int nb = (n_len + 63) >> 6;
+        const int acc = local & 1;
+        const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
+        if (!ptx::mbar_wait_bounded(bar(&ctrl->acc_empty[acc]), acc_phase ^ 1u, abort_flag,
+                                    WAIT_LIMIT_NS)) {
+          signal_timeout(ctrl, status);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t idesc = ptx::idesc_f16(BM, nb * 64, !FP16, B_MN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(bar(&ctrl->full[stage]), phase, abort_flag,
+                                      WAIT_LIMIT_NS)) {
+            signal_timeout(ctrl, status);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ring + stage * STAGE_BYTES;
+          const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t a_desc = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t b_desc = B_MN ? ptx::smem_desc_sw128(b_addr + kk * 2048, BOX_BYTES, 1024)
+                                         : ptx::smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+            ptx::mma_f16(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(&ctrl->empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(&ctrl->acc_full[acc]));
+      }
+      // No MMA may still write TMEM when the block frees it.
+      ptx::mma_commit(bar(&ctrl->drain));
+      if (!ptx::mbar_wait_bounded(bar(&ctrl->drain), 0u, never_flag, WAIT_LIMIT_NS)) {
+        signal_timeout(ctrl, status);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;  // TMEM lanes this warp may access: 32*quarter + [0, 32)
+    int local = 0;
+    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
+      const TileCoord tc = decode_tile(groups, ng, t);
+      const GemmGroup& G = groups[tc.g];
+      const int acc = local & 1;
+      const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
+      bool ok = true;
+      if (lane == 0) {
+        ok = ptx::mbar_wait_bounded(bar(&ctrl->acc_full[acc]), acc_phase, abort_flag,
+                                    WAIT_LIMIT_NS);
+        if (!ok) signal_timeout(ctrl, status);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      ptx::tc_fence_after();
+
+      const int row = tc.m0 + quarter * 32 + lane;
+      const bool row_ok = row < G.M;
+      const int n_len = min(BN, G.N - tc.n0);
+      const int nchunks = (n_len + 31) >> 5;
+      T* out_row = reinterpret_cast<T*>(G.out) + static_cast<int64_t>(tc.b) * G.out_bstride +
+                   static_cast<int64_t>(row) * G.ld_out + tc.n0;
+      const T* aux_row = nullptr;
+      if (HAS_AUX) {
+        aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(tc.b) * G.aux_bstride +
+                  static_cast<int64_t>(row) * G.ld_aux + tc.n0;
+      }
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+      for (int c = 0; c < nchunks; ++c) {
+        uint32_t r[32];
+        __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
+        ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+        ptx::tmem_ld_wait();
+        if (row_ok) {
+        const int col0 = c * 32;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
+        const bool full = col0 + 32 <= n_len;
+        if (HAS_AUX) {
+          if (full) {
+            const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint4 pk = __ldg(src + w);
+              const T* e = reinterpret_cast<const T*>(&pk);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[w * 8 + j] += beta * E::to_f(e[j]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (col0 + j < n_len) v[j] += beta * E::to_f(aux_row[col0 + j]);
+            }
+          }
+        }
+        if (diag != 0.0f) {
+          const int d = row - (tc.n0 + col0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (d == j) v[j] += diag;
+          }
+        }
+        if (full) {
+          uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 pk;
+            T* e = reinterpret_cast<T*>(&pk);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) e[j] = E::from_f(v[w * 8 + j]);
+            dst[w] = pk;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (col0 + j < n_len) out_row[col0 + j] = E::from_f(v[j]);
+          }
+        }
+        }  // row_ok
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(&ctrl->acc_empty[acc]));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <bool B_MN, bool FP16, bool HAS_AUX>
+cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_done{0};  // one bit per device ordinal < 64
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!bit || !(attr_done.load() & bit)) {
+    e = cudaFuncSetAttribute(k_ns_gemm<B_MN, FP16, HAS_AUX>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit);
+  }
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
+  const int64_t grid64 = l.total_tiles < num_sms ? l.total_tiles : num_sms;
+  const int grid = static_cast<int>(grid64);
+  if (grid <= 0) return cudaSuccess;
+  k_ns_gemm<B_MN, FP16, HAS_AUX><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+      l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream) {
+  const int key = (l.b_mn_major ? 4 : 0) | (l.fp16 ? 2 : 0) | (l.has_aux ? 1 : 0);
+  switch (key) {
+    case 0: return launch_typed<false, false, false>(l, num_sms, stream);
+    case 1: return launch_typed<false, false, true>(l, num_sms, stream);
+    case 2: return launch_typed<false, true, false>(l, num_sms, stream);
+    case 3: return launch_typed<false, true, true>(l, num_sms, stream);
+    case 4: return launch_typed<true, false, false>(l, num_sms, stream);
+    case 5: return launch_typed<true, false, true>(l, num_sms, stream);
+    case 6: return launch_typed<true, true, false>(l, num_sms, stream);
+    default: return launch_typed<true, true, true>(l, num_sms, stream);
+  }
+}
+
+}  // namespace nsm

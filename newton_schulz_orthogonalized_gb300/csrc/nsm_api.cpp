@@ -1,0 +1,878 @@
+// C-ABI entry points of libnsmuon.so: argument validation, workspace layout, launch
+// plans (tensor maps and grouped work lists) and the launch sequence of the Muon step.
+//
+// Sources ("DeepSpeed 集成 Muon 优化器实战" §use_muon参数打标, §核心算子,
+// §混合优化器的参数组构造; "Z2 与 Z3 模式" §两种packed buffer生命周期).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <list>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/nsmuon.h"
+#include "nsm_internal.h"
+
+namespace nsm {
+namespace {
+
+// Quintic coefficients of "DeepSpeed 集成 Muon 优化器实战" §核心算子.
+constexpr float kA = 3.4445f;
+constexpr float kB = -4.7750f;
+constexpr float kC = 2.0315f;
+constexpr float kNormEps = 1e-7f;
+constexpr int kMaxSteps = 16;
+constexpr int kMaxMatrices = 1 << 22;
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+constexpr size_t kAlign = 1024;
+
+thread_local std::string t_last_error;
+thread_local int t_last_launches = 0;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(NSM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int64_t align_up64(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- layout
+
+struct ShapeClass {
+  int m, n;        // working shape, m <= n
+  int ldn, ldm;    // row strides of the X slots and of the m x m buffers (multiples of 64)
+  int count;
+  int64_t x_base;  // element offset of the class in an X-layout buffer
+  int64_t mm_base; // element offset of the class in an m x m buffer
+};
+
+struct Layout {
+  int n = 0;
+  int method = 0;
+  int steps = 0;
+  std::vector<ShapeClass> classes;
+  std::vector<int> cls_of;
+  std::vector<int> batch_of;
+  std::vector<int64_t> slot;
+  std::vector<int32_t> chunk_begin, nchunks;
+  std::vector<int64_t> tile_begin;
+  int64_t x_elems = 0, mm_elems = 0;
+  int total_chunks = 0;
+  int64_t total_tiles = 0;
+  size_t off_partials = 0, off_scales = 0, off_x[2] = {0, 0}, off_mm[4] = {0, 0, 0, 0};
+  int num_mm = 0;
+  size_t bytes = 0;
+};
+
+int validate_shapes(const int32_t* shapes, int n) {
+  if (!shapes) return fail(NSM_ERR_NULL, "shapes is NULL");
+  if (n <= 0 || n > kMaxMatrices) return fail(NSM_ERR_SHAPE, "n = %d out of range", n);
+  for (int i = 0; i < n; ++i) {
+    const int64_t r = shapes[2 * i], c = shapes[2 * i + 1];
+    if (r <= 0 || c <= 0) return fail(NSM_ERR_SHAPE, "matrix %d has shape %lldx%lld", i, (long long)r, (long long)c);
+    if (r > kMaxDim || c > kMaxDim || r * c > (int64_t(1) << 40))
+      return fail(NSM_ERR_SHAPE, "matrix %d is too large (%lldx%lld)", i, (long long)r, (long long)c);
+  }
+  return NSM_OK;
+}
+
+int validate_method(int method, int steps) {
+  if (method != NSM_NS_STANDARD && method != NSM_NS_GRAM)
+    return fail(NSM_ERR_METHOD, "unknown ns_method %d (0 = standard, 1 = gram)", method);
+  if (steps < 0 || steps > kMaxSteps) return fail(NSM_ERR_METHOD, "ns_steps = %d not in [0, %d]", steps, kMaxSteps);
+  return NSM_OK;
+}
+
+Layout make_layout(const int32_t* shapes, int n, int method, int steps) {
+  Layout L;
+  L.n = n;
+  L.method = method;
+  L.steps = steps;
+  L.cls_of.resize(n);
+  L.batch_of.resize(n);
+  L.slot.resize(n);
+  L.chunk_begin.resize(n);
+  L.nchunks.resize(n);
+  L.tile_begin.resize(n);
+  std::map<std::pair<int, int>, int> index;
+  for (int i = 0; i < n; ++i) {
+    const int r = shapes[2 * i], c = shapes[2 * i + 1];
+    const int m = std::min(r, c), nn = std::max(r, c);
+    auto it = index.find({m, nn});
+    int ci;
+    if (it == index.end()) {
+      ci = static_cast<int>(L.classes.size());
+      index[{m, nn}] = ci;
+      ShapeClass sc{};
+      sc.m = m;
+      sc.n = nn;
+      sc.ldn = static_cast<int>(align_up64(nn, 64));
+      sc.ldm = static_cast<int>(align_up64(m, 64));
+      sc.count = 0;
+      L.classes.push_back(sc);
+    } else {
+      ci = it->second;
+    }
+    L.cls_of[i] = ci;
+    L.batch_of[i] = L.classes[ci].count++;
+  }
+  for (auto& sc : L.classes) {
+    sc.x_base = L.x_elems;
+    L.x_elems += int64_t(sc.count) * sc.m * sc.ldn;
+    sc.mm_base = L.mm_elems;
+    L.mm_elems += int64_t(sc.count) * sc.m * sc.ldm;
+  }
+  int64_t chunks = 0, tiles = 0;
+  for (int i = 0; i < n; ++i) {
+    const ShapeClass& sc = L.classes[L.cls_of[i]];
+    L.slot[i] = sc.x_base + int64_t(L.batch_of[i]) * sc.m * sc.ldn;
+    const int64_t len = int64_t(shapes[2 * i]) * shapes[2 * i + 1];
+    L.chunk_begin[i] = static_cast<int32_t>(chunks);
+    L.nchunks[i] = static_cast<int32_t>((len + kChunk - 1) / kChunk);
+    chunks += L.nchunks[i];
+    L.tile_begin[i] = tiles;
+    tiles += int64_t((shapes[2 * i] + kTile - 1) / kTile) * ((shapes[2 * i + 1] + kTile - 1) / kTile);
+  }
+  L.total_chunks = static_cast<int>(std::min<int64_t>(chunks, INT32_MAX));
+  L.total_tiles = tiles;
+  L.num_mm = method == NSM_NS_GRAM ? 4 : 2;
+  size_t off = 0;
+  L.off_partials = off;
+  off = align_up(off + size_t(chunks) * 4, kAlign);
+  L.off_scales = off;
+  off = align_up(off + size_t(n) * 4, kAlign);
+  for (int k = 0; k < 2; ++k) {
+    L.off_x[k] = off;
+    off = align_up(off + size_t(L.x_elems) * 2, kAlign);
+  }
+  for (int k = 0; k < L.num_mm; ++k) {
+    L.off_mm[k] = off;
+    off = align_up(off + size_t(L.mm_elems) * 2, kAlign);
+  }
+  L.bytes = off;
+  return L;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+  });
+  return fn;
+}
+
+// 3D map over `count` back-to-back row-major matrices of rows x inner (row stride ld),
+// box 64 x 64 x 1, 128-byte swizzle, zero fill outside the matrix.
+int encode_map(CUtensorMap* map, void* base, bool fp16, int inner, int rows, int ld, int count,
+               const char* ws_begin, const char* ws_end) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(NSM_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const size_t row_bytes = size_t(ld) * 2;
+  const size_t mat_bytes = size_t(rows) * row_bytes;
+  const char* first = static_cast<const char*>(base);
+  const char* last = first + size_t(count - 1) * mat_bytes + size_t(rows - 1) * row_bytes + size_t(inner) * 2;
+  if (ws_begin && (first < ws_begin || last > ws_end))
+    return fail(NSM_ERR_WORKSPACE, "internal: tensor map exceeds the workspace");
+  cuuint64_t dims[3] = {cuuint64_t(inner), cuuint64_t(rows), cuuint64_t(count)};
+  cuuint64_t strides[2] = {cuuint64_t(row_bytes), cuuint64_t(mat_bytes)};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(NSM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return NSM_OK;
+}
+
+// ---------------------------------------------------------------- plans
+
+// Buffers the chain reads/writes, per class: X0, X1 (X layout) and MM0..MM3 (m x m).
+enum Buf { X0 = 0, X1 = 1, MM0 = 2 };
+
+struct Plan {
+  Layout L;
+  int device = 0;
+  char* ws = nullptr;
+  void* dmeta = nullptr;
+  MatInfo* d_mats = nullptr;
+  std::vector<GemmLaunch> launches;
+  int final_buf = X0;     // buffer holding O after the chain
+  bool final_fp16 = false;
+  bool x_fp16 = false;
+  ~Plan() {
+    if (dmeta) cudaFree(dmeta);
+  }
+};
+
+struct StageSpec {
+  int a_buf, b_buf, out_buf, aux_buf;  // aux_buf < 0: none
+  bool b_mn;                           // B operand is the X slot read K x N
+  bool k_is_n;                         // K = n (X X^T); otherwise K = m
+  bool n_is_n;                         // N = n (B X, Q X); otherwise N = m
+  float alpha, beta, diag;
+};
+
+int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, int method, int steps,
+               void* ws, size_t ws_bytes) {
+  P.L = make_layout(shapes, n, method, steps);
+  const Layout& L = P.L;
+  P.ws = static_cast<char*>(ws);
+  P.x_fp16 = method == NSM_NS_GRAM;
+  const int nclass = static_cast<int>(L.classes.size());
+  const int nbuf = 2 + L.num_mm;
+  auto buf_base = [&](int b, int c) -> char* {
+    const ShapeClass& sc = L.classes[c];
+    if (b < MM0) return P.ws + L.off_x[b] + size_t(sc.x_base) * 2;
+    return P.ws + L.off_mm[b - MM0] + size_t(sc.mm_base) * 2;
+  };
+
+  // Launch list of the chain.
+  std::vector<StageSpec> stages;
+  if (method == NSM_NS_STANDARD) {
+    for (int k = 0; k < steps; ++k) {
+      const int src = (k % 2 == 0) ? X0 : X1, dst = (k % 2 == 0) ? X1 : X0;
+      stages.push_back({src, src, MM0, -1, false, true, false, 1.f, 0.f, 0.f});            // A = X X^T
+      stages.push_back({MM0, MM0, MM0 + 1, MM0, false, false, false, kC, kB, 0.f});       // B = bA + cAA
+      stages.push_back({MM0 + 1, src, dst, src, true, false, true, 1.f, kA, 0.f});         // X' = aX + BX
+    }
+    P.final_buf = (steps % 2 == 0) ? X0 : X1;
+    P.final_fp16 = false;
+  } else {
+    if (steps == 0) {
+      P.final_buf = X0;
+    } else {
+      int rR = MM0, rQ = -1;
+      std::vector<int> freeb = {MM0 + 1, MM0 + 2, MM0 + 3};
+      stages.push_back({X0, X0, rR, -1, false, true, false, 1.f, 0.f, 0.f});                // R0 = X X^T
+      for (int k = 1; k <= steps; ++k) {
+        const int h = freeb[0];
+        stages.push_back({rR, rR, h, rR, false, false, false, kC, kB, kA});                  // H
+        if (k == 1) {
+          rQ = h;                                                                             // Q1 = H1
+          freeb = {freeb[1], freeb[2]};
+          if (k < steps) {
+            const int t = freeb[0];
+            stages.push_back({h, rR, t, -1, false, false, false, 1.f, 0.f, 0.f});            // T = H R
+            stages.push_back({t, h, rR, -1, false, false, false, 1.f, 0.f, 0.f});            // R = T H
+            // free: t and the remaining one
+          }
+        } else {
+          const int qn = freeb[1];
+          stages.push_back({h, rQ, qn, -1, false, false, false, 1.f, 0.f, 0.f});             // Q' = H Q
+          const int old_q = rQ;
+          if (k < steps) {
+            stages.push_back({h, rR, old_q, -1, false, false, false, 1.f, 0.f, 0.f});        // T = H R
+            stages.push_back({old_q, h, rR, -1, false, false, false, 1.f, 0.f, 0.f});        // R = T H
+          }
+          rQ = qn;
+          freeb = {h, old_q};
+        }
+        if (k == 1) {
+          // after step 1 the free list is {the buffer T used, the one never used}
+          freeb = {MM0 + 2, MM0 + 3};
+        }
+      }
+      stages.push_back({rQ, X0, X1, -1, true, false, true, 1.f, 0.f, 0.f});                 // O = Q X
+      P.final_buf = X1;
+    }
+    P.final_fp16 = true;
+  }
+
+  // Device metadata: MatInfo[n] | tensor maps [nclass][nbuf] | GemmGroup arrays.
+  const size_t mats_bytes = align_up(sizeof(MatInfo) * n, 128);
+  const size_t maps_off = mats_bytes;
+  const size_t maps_bytes = align_up(sizeof(CUtensorMap) * size_t(nclass) * nbuf, 128);
+  const size_t groups_off = maps_off + maps_bytes;
+  const size_t groups_bytes = sizeof(GemmGroup) * size_t(nclass) * stages.size();
+  const size_t total = groups_off + groups_bytes + 128;
+  std::vector<uint8_t> host(total, 0);
+
+  MatInfo* hm = reinterpret_cast<MatInfo*>(host.data());
+  for (int i = 0; i < n; ++i) {
+    const ShapeClass& sc = L.classes[L.cls_of[i]];
+    MatInfo mi{};
+    mi.off = offsets ? offsets[i] : 0;
+    mi.slot = L.slot[i];
+    mi.tile_begin = L.tile_begin[i];
+    mi.rows = shapes[2 * i];
+    mi.cols = shapes[2 * i + 1];
+    mi.m = sc.m;
+    mi.n = sc.n;
+    mi.ld = sc.ldn;
+    mi.transposed = mi.rows > mi.cols ? 1 : 0;
+    mi.chunk_begin = L.chunk_begin[i];
+    mi.nchunks = L.nchunks[i];
+    mi.scale = static_cast<float>(std::sqrt(std::max(1.0, double(mi.rows) / double(mi.cols))));
+    mi.vec_ok = (mi.rows % 8 == 0 && mi.cols % 8 == 0) ? 1 : 0;
+    hm[i] = mi;
+  }
+
+  cudaError_t e = cudaMalloc(&P.dmeta, total);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(plan metadata)");
+  char* dbase = static_cast<char*>(P.dmeta);
+  P.d_mats = reinterpret_cast<MatInfo*>(dbase);
+
+  const char* ws_begin = P.ws;
+  const char* ws_end = P.ws + L.bytes;
+  CUtensorMap* hmaps = reinterpret_cast<CUtensorMap*>(host.data() + maps_off);
+  for (int c = 0; c < nclass; ++c) {
+    const ShapeClass& sc = L.classes[c];
+    for (int b = 0; b < nbuf; ++b) {
+      CUtensorMap* map = &hmaps[size_t(c) * nbuf + b];
+      int rc;
+      if (b < MM0) rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.n, sc.m, sc.ldn, sc.count, ws_begin, ws_end);
+      else rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.m, sc.m, sc.ldm, sc.count, ws_begin, ws_end);
+      if (rc != NSM_OK) return rc;
+    }
+  }
+  auto dmap = [&](int c, int b) {
+    return reinterpret_cast<const CUtensorMap*>(dbase + maps_off) + size_t(c) * nbuf + b;
+  };
+
+  GemmGroup* hg = reinterpret_cast<GemmGroup*>(host.data() + groups_off);
+  for (size_t s = 0; s < stages.size(); ++s) {
+    const StageSpec& st = stages[s];
+    // heaviest tiles (largest K) first
+    std::vector<int> order(nclass);
+    for (int c = 0; c < nclass; ++c) order[c] = c;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+      const int kx = st.k_is_n ? L.classes[x].n : L.classes[x].m;
+      const int ky = st.k_is_n ? L.classes[y].n : L.classes[y].m;
+      return kx > ky;
+    });
+    GemmGroup* gs = hg + s * nclass;
+    int64_t tiles = 0;
+    double flops = 0;
+    for (int j = 0; j < nclass; ++j) {
+      const int c = order[j];
+      const ShapeClass& sc = L.classes[c];
+      GemmGroup g{};
+      g.map_a = dmap(c, st.a_buf);
+      g.map_b = dmap(c, st.b_buf);
+      const bool out_x = st.out_buf < MM0;
+      g.out = buf_base(st.out_buf, c);
+      g.ld_out = out_x ? sc.ldn : sc.ldm;
+      g.out_bstride = int64_t(sc.m) * g.ld_out;
+      if (st.aux_buf >= 0) {
+        const bool aux_x = st.aux_buf < MM0;
+        g.aux = buf_base(st.aux_buf, c);
+        g.ld_aux = aux_x ? sc.ldn : sc.ldm;
+        g.aux_bstride = int64_t(sc.m) * g.ld_aux;
+      }
+      g.M = sc.m;
+      g.N = st.n_is_n ? sc.n : sc.m;
+      g.K = st.k_is_n ? sc.n : sc.m;
+      g.count = sc.count;
+      g.tiles_m = (g.M + 127) / 128;
+      g.tiles_n = (g.N + 255) / 256;
+      g.tile_begin = tiles;
+      tiles += int64_t(g.count) * g.tiles_m * g.tiles_n;
+      flops += 2.0 * g.count * double(g.M) * g.N * g.K;
+      gs[j] = g;
+    }
+    GemmLaunch l{};
+    l.groups = reinterpret_cast<const GemmGroup*>(dbase + groups_off) + s * nclass;
+    l.num_groups = nclass;
+    l.b_mn_major = st.b_mn ? 1 : 0;
+    l.has_aux = st.aux_buf >= 0 ? 1 : 0;
+    l.fp16 = P.x_fp16 ? 1 : 0;
+    l.total_tiles = tiles;
+    l.alpha = st.alpha;
+    l.beta = st.beta;
+    l.diag = st.diag;
+    l.flops = flops;
+    P.launches.push_back(l);
+  }
+
+  e = cudaMemcpy(P.dmeta, host.data(), total, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpy(plan metadata)");
+  (void)ws_bytes;
+  return NSM_OK;
+}
+
+struct PlanCache {
+  std::mutex mu;
+  std::list<std::pair<std::string, std::unique_ptr<Plan>>> lru;  // front = most recent
+  static constexpr size_t kMax = 8;
+};
+
+PlanCache& cache() {
+  static PlanCache* c = new PlanCache();  // never destroyed: plans may outlive static teardown
+  return *c;
+}
+
+std::string plan_key(int device, const int32_t* shapes, const int64_t* offsets, int n, int method,
+                     int steps, const void* ws) {
+  std::string k;
+  k.reserve(64 + size_t(n) * 16);
+  auto put = [&](const void* p, size_t b) { k.append(static_cast<const char*>(p), b); };
+  put(&device, sizeof(device));
+  put(&method, sizeof(method));
+  put(&steps, sizeof(steps));
+  put(&n, sizeof(n));
+  put(&ws, sizeof(ws));
+  put(shapes, sizeof(int32_t) * 2 * size_t(n));
+  put(offsets, sizeof(int64_t) * size_t(n));
+  return k;
+}
+
+// Returns a plan (owned by the cache) or NULL with the error set.
+Plan* get_plan(const int32_t* shapes, const int64_t* offsets, int n, int method, int steps, void* ws,
+               size_t ws_bytes, int* rc) {
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) {
+    *rc = fail_cuda(e, "cudaGetDevice");
+    return nullptr;
+  }
+  const std::string key = plan_key(device, shapes, offsets, n, method, steps, ws);
+  PlanCache& C = cache();
+  std::lock_guard<std::mutex> lock(C.mu);
+  for (auto it = C.lru.begin(); it != C.lru.end(); ++it) {
+    if (it->first == key) {
+      C.lru.splice(C.lru.begin(), C.lru, it);
+      return C.lru.front().second.get();
+    }
+  }
+  std::unique_ptr<Plan> P(new Plan());
+  P->device = device;
+  *rc = build_plan(*P, shapes, offsets, n, method, steps, ws, ws_bytes);
+  if (*rc != NSM_OK) return nullptr;
+  if (C.lru.size() >= PlanCache::kMax) {
+    // the evicted plan's metadata may still be read by queued kernels
+    cudaDeviceSynchronize();
+    C.lru.pop_back();
+  }
+  C.lru.emplace_front(key, std::move(P));
+  return C.lru.front().second.get();
+}
+
+// ---------------------------------------------------------------- timing
+
+struct Timing {
+  std::mutex mu;
+  bool enabled = false;
+  struct Rec {
+    cudaEvent_t a, b;
+    double flops;
+  };
+  std::vector<Rec> pending;
+  std::vector<cudaEvent_t> pool;
+  double ms = 0, flops = 0;
+  int64_t launches = 0;
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  void collect() {
+    for (auto& r : pending) {
+      cudaEventSynchronize(r.b);
+      float t = 0.f;
+      cudaEventElapsedTime(&t, r.a, r.b);
+      ms += t;
+      flops += r.flops;
+      launches += 1;
+      pool.push_back(r.a);
+      pool.push_back(r.b);
+    }
+    pending.clear();
+  }
+};
+
+Timing& timing() {
+  static Timing* t = new Timing();
+  return *t;
+}
+
+// ---------------------------------------------------------------- validation helpers
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int validate_offsets(const int64_t* offsets, const int32_t* shapes, int n, int64_t* extent) {
+  if (!offsets) return fail(NSM_ERR_NULL, "offsets is NULL");
+  std::vector<int> order(n);
+  for (int i = 0; i < n; ++i) {
+    if (offsets[i] < 0) return fail(NSM_ERR_OFFSET, "offset %d is negative", i);
+    if (offsets[i] % 8 != 0) return fail(NSM_ERR_ALIGN, "offset %d (%lld) is not a multiple of 8 elements", i, (long long)offsets[i]);
+    order[i] = i;
+  }
+  std::sort(order.begin(), order.end(), [&](int a, int b) { return offsets[a] < offsets[b]; });
+  int64_t end_prev = 0;
+  int64_t ext = 0;
+  for (int k = 0; k < n; ++k) {
+    const int i = order[k];
+    const int64_t len = int64_t(shapes[2 * i]) * shapes[2 * i + 1];
+    if (k > 0 && offsets[i] < end_prev) return fail(NSM_ERR_OFFSET, "matrix %d overlaps the matrix before it", i);
+    end_prev = offsets[i] + len;
+    ext = std::max(ext, end_prev);
+  }
+  *extent = ext;
+  return NSM_OK;
+}
+
+bool ranges_overlap(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+int check_workspace(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return fail(NSM_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(NSM_ERR_ALIGN, "workspace is not 256-byte aligned");
+  if (ws_bytes < need) return fail(NSM_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", ws_bytes, need);
+  return NSM_OK;
+}
+
+int run_chain(Plan& P, cudaStream_t stream, int* launches) {
+  int num_sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, P.device);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+  Timing& T = timing();
+  bool timed;
+  {
+    std::lock_guard<std::mutex> lock(T.mu);
+    timed = T.enabled;
+  }
+  for (const GemmLaunch& l : P.launches) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (timed) {
+      std::lock_guard<std::mutex> lock(T.mu);
+      a = T.get();
+      b = T.get();
+      cudaEventRecord(a, stream);
+    }
+    e = launch_gemm(l, num_sms, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "Newton-Schulz GEMM launch");
+    ++*launches;
+    if (timed) {
+      std::lock_guard<std::mutex> lock(T.mu);
+      cudaEventRecord(b, stream);
+      T.pending.push_back({a, b, l.flops});
+    }
+  }
+  return NSM_OK;
+}
+
+}  // namespace
+}  // namespace nsm
+
+using namespace nsm;
+
+extern "C" {
+
+int nsm_version(void) { return 100; }
+
+const char* nsm_last_error(void) { return t_last_error.c_str(); }
+
+int nsm_last_launch_count(void) { return t_last_launches; }
+
+int nsm_route(const char* name, int ndim) {
+  if (!name) return fail(NSM_ERR_NULL, "name is NULL");
+  if (ndim < 2) return 0;
+  std::string s(name);
+  for (char& ch : s) {
+    if (ch >= 'A' && ch <= 'Z') ch = static_cast<char>(ch - 'A' + 'a');
+  }
+  if (s.find("embed") != std::string::npos) return 0;
+  if (s.find("lm_head") != std::string::npos) return 0;
+  return 1;
+}
+
+int nsm_pack(const int32_t* shapes, int n, int64_t align_elems, int64_t* offsets_out, int64_t* total_out) {
+  if (!offsets_out || !total_out) return fail(NSM_ERR_NULL, "output pointer is NULL");
+  int rc = validate_shapes(shapes, n);
+  if (rc != NSM_OK) return rc;
+  if (align_elems < 1) return fail(NSM_ERR_ARG, "align_elems must be >= 1");
+  int64_t cursor = 0;
+  for (int i = 0; i < n; ++i) {
+    offsets_out[i] = cursor;
+    const int64_t end = cursor + int64_t(shapes[2 * i]) * shapes[2 * i + 1];
+    cursor = (end + align_elems - 1) / align_elems * align_elems;
+  }
+  *total_out = cursor;
+  return NSM_OK;
+}
+
+size_t muon_workspace_bytes(const int32_t* shapes, int n, int ns_method, int ns_steps) {
+  if (validate_shapes(shapes, n) != NSM_OK) return 0;
+  if (validate_method(ns_method, ns_steps) != NSM_OK) return 0;
+  return make_layout(shapes, n, ns_method, ns_steps).bytes;
+}
+
+int muon_step(const void* packed_grads, float* packed_params, float* momentum, const int64_t* offsets,
+              const int32_t* shapes, int n, float lr, float wd, float mu, int ns_method, int ns_steps,
+              int nesterov, void* workspace, size_t workspace_bytes, nsm_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!packed_grads || !packed_params || !momentum) return fail(NSM_ERR_NULL, "a device buffer is NULL");
+  int rc = validate_shapes(shapes, n);
+  if (rc != NSM_OK) return rc;
+  rc = validate_method(ns_method, ns_steps);
+  if (rc != NSM_OK) return rc;
+  if (!std::isfinite(lr) || !std::isfinite(wd) || !std::isfinite(mu))
+    return fail(NSM_ERR_ARG, "lr, wd and mu must be finite");
+  int64_t extent = 0;
+  rc = validate_offsets(offsets, shapes, n, &extent);
+  if (rc != NSM_OK) return rc;
+  if (!aligned(packed_grads, 16) || !aligned(packed_params, 16) || !aligned(momentum, 16))
+    return fail(NSM_ERR_ALIGN, "device buffers must be 16-byte aligned");
+  if (ranges_overlap(packed_grads, size_t(extent) * 2, packed_params, size_t(extent) * 4) ||
+      ranges_overlap(packed_grads, size_t(extent) * 2, momentum, size_t(extent) * 4) ||
+      ranges_overlap(packed_params, size_t(extent) * 4, momentum, size_t(extent) * 4))
+    return fail(NSM_ERR_ARG, "grads, params and momentum must not overlap");
+  const Layout L = make_layout(shapes, n, ns_method, ns_steps);
+  rc = check_workspace(workspace, workspace_bytes, L.bytes);
+  if (rc != NSM_OK) return rc;
+
+  Plan* P = get_plan(shapes, offsets, n, ns_method, ns_steps, workspace, workspace_bytes, &rc);
+  if (!P) return rc;
+  char* ws = P->ws;
+  float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
+  float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
+  int launches = 0;
+  cudaError_t e = launch_momentum_norm(packed_grads, momentum, ws + P->L.off_x[1], P->d_mats, n,
+                                       P->L.total_chunks, partials, mu, nesterov, 1, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "momentum/norm launch");
+  ++launches;
+  e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
+  ++launches;
+  e = launch_to_class(ws + P->L.off_x[1], 1, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n,
+                      P->L.total_tiles, scales, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
+  ++launches;
+  rc = run_chain(*P, stream, &launches);
+  if (rc != NSM_OK) return rc;
+  e = launch_apply(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, packed_params, P->d_mats, n,
+                   P->L.total_tiles, lr, wd, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "apply launch");
+  ++launches;
+  t_last_launches = launches;
+  return NSM_OK;
+}
+
+int muon_orthogonalize(const void* in_bf16, void* out_bf16, const int64_t* offsets, const int32_t* shapes, int n,
+                       int ns_method, int ns_steps, void* workspace, size_t workspace_bytes, nsm_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!in_bf16 || !out_bf16) return fail(NSM_ERR_NULL, "a device buffer is NULL");
+  int rc = validate_shapes(shapes, n);
+  if (rc != NSM_OK) return rc;
+  rc = validate_method(ns_method, ns_steps);
+  if (rc != NSM_OK) return rc;
+  int64_t extent = 0;
+  rc = validate_offsets(offsets, shapes, n, &extent);
+  if (rc != NSM_OK) return rc;
+  if (!aligned(in_bf16, 16) || !aligned(out_bf16, 16)) return fail(NSM_ERR_ALIGN, "device buffers must be 16-byte aligned");
+  if (ranges_overlap(in_bf16, size_t(extent) * 2, out_bf16, size_t(extent) * 2))
+    return fail(NSM_ERR_ARG, "input and output must not overlap");
+  const Layout L = make_layout(shapes, n, ns_method, ns_steps);
+  rc = check_workspace(workspace, workspace_bytes, L.bytes);
+  if (rc != NSM_OK) return rc;
+
+  Plan* P = get_plan(shapes, offsets, n, ns_method, ns_steps, workspace, workspace_bytes, &rc);
+  if (!P) return rc;
+  char* ws = P->ws;
+  float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
+  float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
+  int launches = 0;
+  cudaError_t e = launch_momentum_norm(in_bf16, nullptr, nullptr, P->d_mats, n, P->L.total_chunks, partials, 0.f,
+                                       0, 0, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
+  ++launches;
+  e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
+  ++launches;
+  e = launch_to_class(in_bf16, 0, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n, P->L.total_tiles, scales,
+                      stream);
+  if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
+  ++launches;
+  rc = run_chain(*P, stream, &launches);
+  if (rc != NSM_OK) return rc;
+  e = launch_export(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, out_bf16, P->d_mats, n, P->L.total_tiles,
+                    stream);
+  if (e != cudaSuccess) return fail_cuda(e, "export launch");
+  ++launches;
+  t_last_launches = launches;
+  return NSM_OK;
+}
+
+int adamw_step(const void* grads, float* params, float* exp_avg, float* exp_avg_sq, int64_t numel, float lr,
+               float beta1, float beta2, float eps, float wd, int step, nsm_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (numel < 0) return fail(NSM_ERR_SHAPE, "numel is negative");
+  if (numel == 0) {
+    t_last_launches = 0;
+    return NSM_OK;
+  }
+  if (!grads || !params || !exp_avg || !exp_avg_sq) return fail(NSM_ERR_NULL, "a device buffer is NULL");
+  if (step < 1) return fail(NSM_ERR_ARG, "step counts from 1");
+  if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f))
+    return fail(NSM_ERR_ARG, "betas must lie in [0, 1)");
+  if (!std::isfinite(lr) || !std::isfinite(wd) || !(eps >= 0.f) || !std::isfinite(eps))
+    return fail(NSM_ERR_ARG, "lr, wd, eps must be finite (eps >= 0)");
+  if (!aligned(grads, 16) || !aligned(params, 16) || !aligned(exp_avg, 16) || !aligned(exp_avg_sq, 16))
+    return fail(NSM_ERR_ALIGN, "device buffers must be 16-byte aligned");
+  const size_t fb = size_t(numel) * 4;
+  if (ranges_overlap(params, fb, exp_avg, fb) || ranges_overlap(params, fb, exp_avg_sq, fb) ||
+      ranges_overlap(exp_avg, fb, exp_avg_sq, fb) || ranges_overlap(grads, size_t(numel) * 2, params, fb))
+    return fail(NSM_ERR_ARG, "AdamW buffers must not overlap");
+  const double bc1 = 1.0 - std::pow(double(beta1), double(step));
+  const double bc2 = 1.0 - std::pow(double(beta2), double(step));
+  cudaError_t e = launch_adamw(grads, params, exp_avg, exp_avg_sq, numel, lr, beta1, beta2, eps, wd,
+                               static_cast<float>(bc1), static_cast<float>(bc2), stream);
+  if (e != cudaSuccess) return fail_cuda(e, "AdamW launch");
+  t_last_launches = 1;
+  return NSM_OK;
+}
+
+int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo, const void* aux, int ldx, int M,
+             int N, int K, int b_mn_major, int fp16, float alpha, float beta, float diag, void* scratch,
+             size_t scratch_bytes, nsm_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!a || !b || !out || !scratch) return fail(NSM_ERR_NULL, "a, b, out and scratch must be non-NULL");
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return fail(NSM_ERR_SHAPE, "bad GEMM shape %dx%dx%d", M, N, K);
+  const int b_cols = b_mn_major ? N : K;
+  if (lda < K || ldb < b_cols || ldo < N || (aux && ldx < N))
+    return fail(NSM_ERR_SHAPE, "a row stride is shorter than its row");
+  if (lda % 8 || ldb % 8 || ldo % 8 || (aux && ldx % 8))
+    return fail(NSM_ERR_ALIGN, "row strides must be multiples of 8 elements");
+  if (!aligned(a, 16) || !aligned(b, 16) || !aligned(out, 16) || (aux && !aligned(aux, 16)))
+    return fail(NSM_ERR_ALIGN, "pointers must be 16-byte aligned");
+  if (!aligned(scratch, 128)) return fail(NSM_ERR_ALIGN, "scratch must be 128-byte aligned");
+  const size_t need = 2 * sizeof(CUtensorMap) + sizeof(GemmGroup);
+  if (scratch_bytes < need) return fail(NSM_ERR_WORKSPACE, "scratch needs %zu bytes", need);
+  if (aux && ranges_overlap(aux, size_t(M) * ldx * 2, out, size_t(M) * ldo * 2))
+    return fail(NSM_ERR_ARG, "aux must not overlap out");
+  struct Blob {
+    CUtensorMap ma, mb;
+    GemmGroup g;
+  };
+  static_assert(sizeof(Blob) <= 1024, "scratch blob");
+  Blob blob;
+  std::memset(&blob, 0, sizeof(blob));
+  int rc = encode_map(&blob.ma, const_cast<void*>(a), fp16 != 0, K, M, lda, 1, nullptr, nullptr);
+  if (rc != NSM_OK) return rc;
+  if (b_mn_major) rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, N, K, ldb, 1, nullptr, nullptr);
+  else rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, K, N, ldb, 1, nullptr, nullptr);
+  if (rc != NSM_OK) return rc;
+  Blob* d = static_cast<Blob*>(scratch);
+  GemmGroup& g = blob.g;
+  g.map_a = &d->ma;
+  g.map_b = &d->mb;
+  g.out = out;
+  g.aux = aux;
+  g.ld_out = ldo;
+  g.ld_aux = aux ? ldx : 0;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.count = 1;
+  g.tiles_m = (M + 127) / 128;
+  g.tiles_n = (N + 255) / 256;
+  g.tile_begin = 0;
+  cudaError_t e = cudaMemcpyAsync(scratch, &blob, sizeof(blob), cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "copy GEMM descriptors");
+  // the source is pageable host memory: the copy is staged before cudaMemcpyAsync returns
+  GemmLaunch l{};
+  l.groups = &d->g;
+  l.num_groups = 1;
+  l.b_mn_major = b_mn_major ? 1 : 0;
+  l.has_aux = aux ? 1 : 0;
+  l.fp16 = fp16 ? 1 : 0;
+  l.total_tiles = int64_t(g.tiles_m) * g.tiles_n;
+  l.alpha = alpha;
+  l.beta = aux ? beta : 0.f;
+  l.diag = diag;
+  l.flops = 2.0 * M * double(N) * K;
+  int dev = 0, num_sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail_cuda(e, "device query");
+  e = launch_gemm(l, num_sms, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "GEMM launch");
+  t_last_launches = 1;
+  return NSM_OK;
+}
+
+int nsm_device_status(nsm_stream_t stream_, int* status_out) {
+  if (!status_out) return fail(NSM_ERR_NULL, "status_out is NULL");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+  int* p = device_status_ptr();
+  if (!p) return fail(NSM_ERR_CUDA, "device status word unavailable");
+  int v = 0;
+  e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e, "read device status");
+  const int zero = 0;
+  e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail_cuda(e, "clear device status");
+  *status_out = (v == kDevTimeout) ? NSM_ERR_TIMEOUT : NSM_OK;
+  return NSM_OK;
+}
+
+int nsm_timing_enable(int enable) {
+  Timing& T = timing();
+  std::lock_guard<std::mutex> lock(T.mu);
+  T.enabled = enable != 0;
+  return NSM_OK;
+}
+
+int nsm_timing_read(double* gemm_ms, int64_t* gemm_launches, double* gemm_flops) {
+  Timing& T = timing();
+  std::lock_guard<std::mutex> lock(T.mu);
+  T.collect();
+  if (gemm_ms) *gemm_ms = T.ms;
+  if (gemm_launches) *gemm_launches = T.launches;
+  if (gemm_flops) *gemm_flops = T.flops;
+  return NSM_OK;
+}
+
+int nsm_timing_reset(void) {
+  Timing& T = timing();
+  std::lock_guard<std::mutex> lock(T.mu);
+  T.collect();
+  T.ms = 0;
+  T.flops = 0;
+  T.launches = 0;
+  return NSM_OK;
+}
+
+}  // extern "C"

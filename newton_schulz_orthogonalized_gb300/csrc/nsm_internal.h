@@ -1,0 +1,91 @@
+// Internal definitions shared by the host planner (nsm_api.cpp) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nsm {
+
+// Status word values kernels write when a bounded wait expires.
+constexpr int kDevOk = 0;
+constexpr int kDevTimeout = 1;
+
+// One matrix of a packed group, as the elementwise kernels see it.
+struct MatInfo {
+  int64_t off;        // element offset in the packed (natural, row-major) buffers
+  int64_t slot;       // element offset of the matrix's slot in the class-layout buffers
+  int64_t tile_begin; // prefix count of 64x64 natural tiles over the table
+  int32_t rows, cols; // shape of the parameter
+  int32_t m, n, ld;   // working shape (m = min, n = max) and row stride of the slot
+  int32_t transposed; // rows > cols: the slot holds the transpose
+  int32_t chunk_begin, nchunks;  // momentum/norm chunks of this matrix
+  float scale;        // sqrt(max(1, rows/cols))
+  int32_t vec_ok;     // rows % 8 == 0 && cols % 8 == 0 (16-byte vector paths usable)
+};
+static_assert(sizeof(MatInfo) == 64, "MatInfo layout");
+
+// Elements of one momentum/norm chunk (256 threads x 8 vectors of 8).
+constexpr int kChunk = 16384;
+// Natural tiles moved between layouts are kTile x kTile.
+constexpr int kTile = 64;
+
+// One group of same-shape problems of a grouped GEMM launch:
+//   out[b] = alpha * (A[b] . op(B[b])) + beta * aux[b] + diag * I     for b < count
+// A[b] is M x K (K contiguous).  B[b] is N x K (K contiguous, "K-major") or K x N
+// (N contiguous, "MN-major"), chosen per launch.  Output and aux are M x N with row
+// strides ld_out / ld_aux and batch strides out_bstride / aux_bstride (elements).
+struct GemmGroup {
+  const CUtensorMap* map_a;
+  const CUtensorMap* map_b;
+  void* out;
+  const void* aux;
+  int64_t out_bstride;
+  int64_t aux_bstride;
+  int64_t tile_begin;
+  int32_t ld_out, ld_aux;
+  int32_t M, N, K;
+  int32_t count;
+  int32_t tiles_m, tiles_n;
+  int32_t pad0, pad1;
+};
+static_assert(sizeof(GemmGroup) == 96, "GemmGroup layout");
+
+struct GemmLaunch {
+  const GemmGroup* groups;  // device array
+  int32_t num_groups;
+  int32_t b_mn_major;       // 1: B operand is K x N with N contiguous
+  int32_t has_aux;
+  int32_t fp16;             // 1: operands/outputs are fp16, else bf16
+  int64_t total_tiles;
+  float alpha, beta, diag;
+  double flops;             // canonical flops of this launch
+};
+
+// ---- launchers (defined in the .cu files) ---------------------------------------
+
+cudaError_t launch_momentum_norm(const void* grads, float* momentum, void* u_base,
+                                 const MatInfo* mats, int nmats, int total_chunks,
+                                 float* partials, float mu, int nesterov, int has_momentum,
+                                 cudaStream_t stream);
+cudaError_t launch_norm_finalize(const MatInfo* mats, int nmats, const float* partials,
+                                 float* scales, float eps, cudaStream_t stream);
+// natural (bf16) -> class layout, scaled by scales[i]; out fp16 when to_fp16
+cudaError_t launch_to_class(const void* src, int src_is_slot, void* dst, int to_fp16,
+                            const MatInfo* mats, int nmats, int64_t total_tiles,
+                            const float* scales, cudaStream_t stream);
+// class layout O -> p update in natural layout
+cudaError_t launch_apply(const void* o, int o_fp16, float* params, const MatInfo* mats,
+                         int nmats, int64_t total_tiles, float lr, float wd,
+                         cudaStream_t stream);
+// class layout O -> natural bf16 copy
+cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* mats,
+                          int nmats, int64_t total_tiles, cudaStream_t stream);
+cudaError_t launch_adamw(const void* grads, float* params, float* m, float* v,
+                         int64_t numel, float lr, float beta1, float beta2, float eps,
+                         float wd, float bc1, float bc2, cudaStream_t stream);
+cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream);
+
+int* device_status_ptr();
+
+}  // namespace nsm

@@ -1,0 +1,112 @@
+"""The tensor-core GEMM engine on single problems, every variant the chain uses.
+
+out = alpha * A op(B) + beta * aux + diag * I is compared with a float64 matmul of the
+same bf16/fp16 inputs.  The only rounding on the GPU side is the final cast of the fp32
+accumulator (plus the epilogue's fp32 arithmetic), so the bar is a few half-precision
+ulps: relative Frobenius error <= 4e-3 for bf16 outputs and 5e-4 for fp16 outputs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nsm():
+    import newton_schulz_orthogonalized_gb300 as m
+    m.lib()
+    return m
+
+
+def _rand(shape, dtype, seed):
+    """Random matrix whose row stride is rounded up to 8 elements (a view when padded)."""
+    rows, cols = shape
+    ld = (cols + 7) // 8 * 8
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    full = torch.randn(rows, ld, generator=g, device="cuda").to(dtype)
+    return full[:, :cols]
+
+
+def _ref(a, b, aux, b_mn, alpha, beta, diag):
+    A = a.double().cpu().numpy()
+    B = b.double().cpu().numpy()
+    prod = A @ (B if b_mn else B.T)
+    out = alpha * prod
+    if aux is not None:
+        out = out + beta * aux.double().cpu().numpy()
+    if diag:
+        k = min(out.shape)
+        out[np.arange(k), np.arange(k)] += diag
+    return out
+
+
+CASES = [
+    # M, N, K, b_mn, aux, diag
+    (128, 256, 64, False, False, 0.0),
+    (128, 128, 128, False, False, 0.0),
+    (256, 512, 1024, False, False, 0.0),
+    (200, 136, 72, False, False, 0.0),
+    (3, 5, 8, False, False, 0.0),
+    (128, 256, 128, True, True, 0.0),
+    (264, 328, 200, True, True, 0.0),
+    (64, 1000, 64, True, False, 0.0),
+    (192, 192, 192, False, True, 3.4445),
+    (384, 384, 4096, False, True, 0.0),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("M,N,K,b_mn,use_aux,diag", CASES)
+def test_gemm_variants(nsm, dtype, M, N, K, b_mn, use_aux, diag):
+    seed = M * 7 + N * 3 + K
+    a = _rand((M, K), dtype, seed)
+    b = _rand((K, N) if b_mn else (N, K), dtype, seed + 1)
+    aux = _rand((M, N), dtype, seed + 2) if use_aux else None
+    out = torch.full((M, (N + 7) // 8 * 8), float("nan"), dtype=dtype, device="cuda")[:, :N]
+    alpha, beta = 0.75, -1.25
+    nsm.gemm(a, b, out, aux, b_mn, alpha, beta, diag)
+    assert nsm.device_status() == nsm.NSM_OK
+    ref = _ref(a, b, aux, b_mn, alpha, beta if use_aux else 0.0, diag)
+    got = out.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    tol = 4e-3 if dtype == torch.bfloat16 else 5e-4
+    assert rel <= tol, rel
+
+
+def test_gemm_padded_leading_dimension(nsm):
+    # operands that are views into wider buffers (row stride > row length)
+    M, N, K = 160, 200, 96
+    a_full = _rand((M, K + 32), torch.bfloat16, 1)
+    b_full = _rand((N, K + 64), torch.bfloat16, 2)
+    out_full = torch.zeros((M, N + 56), dtype=torch.bfloat16, device="cuda")
+    a, b, out = a_full[:, :K], b_full[:, :K], out_full[:, :N]
+    nsm.gemm(a, b, out)
+    torch.cuda.synchronize()
+    ref = _ref(a, b, None, False, 1.0, 0.0, 0.0)
+    rel = np.linalg.norm(out.double().cpu().numpy() - ref) / np.linalg.norm(ref)
+    assert rel <= 4e-3
+    # columns beyond N untouched
+    assert torch.count_nonzero(out_full[:, N:]).item() == 0
+
+
+def test_gemm_deterministic(nsm):
+    a = _rand((512, 2048), torch.bfloat16, 5)
+    o1 = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
+    o2 = torch.empty_like(o1)
+    nsm.gemm(a, a, o1)
+    nsm.gemm(a, a, o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+
+
+def test_gemm_rejects_bad_arguments(nsm):
+    a = torch.zeros((16, 12), dtype=torch.bfloat16, device="cuda")  # row stride 12
+    b = torch.zeros((16, 12), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((16, 16), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(nsm.NsmError) as e:
+        nsm.gemm(a, b, out)
+    assert e.value.code == nsm.NSM_ERR_ALIGN

@@ -1,0 +1,299 @@
+"""Parity of the CUDA path with the float64 oracle, through the C ABI.
+
+Tolerances (relative Frobenius norms): orthogonalised output <= 2e-2 (bf16/fp16 NS),
+final parameter delta <= 1e-2, momentum and AdamW <= 1e-5.  Routing and offsets are
+bit-exact (tests/test_abi.py).  Inputs come from the seeded generators in ``synth``:
+the GPU draws them, the oracle reads the same bf16 values decoded exactly.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_NS = 2e-2
+TOL_DELTA = 1e-2
+TOL_FP32 = 1e-5
+
+
+@pytest.fixture(scope="module")
+def nsm():
+    import newton_schulz_orthogonalized_gb300 as m
+    m.lib()
+    return m
+
+
+def rel(a, b):
+    nb = np.linalg.norm(b)
+    return np.linalg.norm(a - b) / (nb if nb > 0 else 1.0)
+
+
+class Step:
+    """Runs muon_step on a workload and keeps host copies for the oracle."""
+
+    def __init__(self, nsm, wl, method, steps=5, nesterov=True, momentum_init=None,
+                 zero_grads=()):
+        self.wl = wl
+        self.method = method
+        self.steps = steps
+        self.nesterov = nesterov
+        self.offsets, total = nsm.pack(wl.muon_shapes)
+        dev = "cuda"
+        self.grads = torch.zeros(total, dtype=torch.bfloat16, device=dev)
+        synth.fill_packed_grads(wl, self.offsets, self.grads)
+        for i in zero_grads:
+            r, c = wl.muon_shapes[i]
+            o = int(self.offsets[i])
+            self.grads[o:o + r * c].zero_()
+        self.params = torch.zeros(total, dtype=torch.float32, device=dev)
+        synth.fill_packed_params(wl, self.offsets, self.params)
+        if momentum_init is None:
+            self.mom = torch.zeros(total, dtype=torch.float32, device=dev)
+        else:
+            self.mom = momentum_init.to(dev).clone()
+        self.p0 = self.params.double().cpu().numpy()
+        self.m0 = self.mom.double().cpu().numpy()
+        self.g = self.grads.double().cpu().numpy()
+        ws = torch.empty(nsm.workspace_bytes(wl.muon_shapes, method, steps), dtype=torch.uint8,
+                         device=dev)
+        nsm.muon_step(self.grads, self.params, self.mom, self.offsets, wl.muon_shapes, wl.lr,
+                      wl.wd, wl.mu, method, steps, nesterov, ws)
+        assert nsm.device_status() == nsm.NSM_OK
+        self.p1 = self.params.double().cpu().numpy()
+        self.m1 = self.mom.double().cpu().numpy()
+
+    def matrix(self, arr, i):
+        r, c = self.wl.muon_shapes[i]
+        o = int(self.offsets[i])
+        return arr[o:o + r * c].reshape(r, c)
+
+    def check(self, indices=None):
+        wl = self.wl
+        idx = range(len(wl.muon_shapes)) if indices is None else indices
+        worst = {"delta": 0.0, "mom": 0.0}
+        for i in idx:
+            g = self.matrix(self.g, i)
+            p = self.matrix(self.p0, i)
+            m = self.matrix(self.m0, i)
+            (pn,), (mn,), _ = oracle.muon_step([g], [p], [m], wl.lr, wl.wd, wl.mu, self.method,
+                                               self.steps, self.nesterov)
+            e_m = rel(self.matrix(self.m1, i), mn)
+            e_d = rel(self.matrix(self.p1, i) - p, pn - p)
+            worst["mom"] = max(worst["mom"], e_m)
+            worst["delta"] = max(worst["delta"], e_d)
+            assert e_m <= TOL_FP32, (i, e_m)
+            assert e_d <= TOL_DELTA, (i, wl.muon_shapes[i], e_d)
+        return worst
+
+
+def orthogonalize_gpu(nsm, wl, method, steps=5):
+    offsets, total = nsm.pack(wl.muon_shapes)
+    inp = torch.zeros(total, dtype=torch.bfloat16, device="cuda")
+    synth.fill_packed_grads(wl, offsets, inp)
+    out = torch.zeros_like(inp)
+    ws = torch.empty(nsm.workspace_bytes(wl.muon_shapes, method, steps), dtype=torch.uint8,
+                     device="cuda")
+    nsm.muon_orthogonalize(inp, out, offsets, wl.muon_shapes, method, steps, ws)
+    assert nsm.device_status() == nsm.NSM_OK
+    return offsets, inp.double().cpu().numpy(), out.double().cpu().numpy()
+
+
+RAGGED = [(130, 260), (3, 5), (257, 129), (64, 1000), (1, 8), (200, 200), (8, 8), (384, 96),
+          (136, 72)]
+
+
+# ------------------------------------------------------------------ orthogonalisation
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+@pytest.mark.parametrize("steps", [0, 1, 5])
+def test_orthogonalize_ragged(nsm, method, steps):
+    wl = synth.custom(RAGGED, seed=3, lowrank=False)
+    offsets, g, o = orthogonalize_gpu(nsm, wl, method, steps)
+    for i, (r, c) in enumerate(wl.muon_shapes):
+        off = int(offsets[i])
+        gi = g[off:off + r * c].reshape(r, c)
+        ref = oracle.orthogonalize(gi, method, steps)
+        got = o[off:off + r * c].reshape(r, c)
+        assert rel(got, ref) <= TOL_NS, ((r, c), rel(got, ref))
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_orthogonalize_layer1024(nsm, method):
+    wl = synth.workload("layer1024")
+    offsets, g, o = orthogonalize_gpu(nsm, wl, method)
+    for i, (r, c) in enumerate(wl.muon_shapes):
+        off = int(offsets[i])
+        ref = oracle.orthogonalize(g[off:off + r * c].reshape(r, c), method)
+        got = o[off:off + r * c].reshape(r, c)
+        assert rel(got, ref) <= TOL_NS, ((r, c), rel(got, ref))
+
+
+# ------------------------------------------------------------------ full step
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_step_tiny(nsm, method):
+    Step(nsm, synth.workload("tiny"), method).check()
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_step_ragged(nsm, method):
+    Step(nsm, synth.custom(RAGGED, seed=5), method).check()
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_step_layer1024(nsm, method):
+    Step(nsm, synth.workload("layer1024"), method).check()
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_step_gpt2small_one_per_shape(nsm, method):
+    wl = synth.workload("gpt2small")
+    s = Step(nsm, wl, method)
+    s.check(indices=[0, 1, 2, 3, 45, 46, 47])
+
+
+@pytest.mark.parametrize("nesterov", [True, False])
+@pytest.mark.parametrize("steps", [1, 2, 3])
+def test_step_variants(nsm, nesterov, steps):
+    wl = synth.custom([(256, 384), (384, 256), (128, 128)], seed=11)
+    for method in ("standard", "gram"):
+        Step(nsm, wl, method, steps=steps, nesterov=nesterov).check()
+
+
+def test_step_zero_grads_with_momentum(nsm):
+    # matrices whose gradient is zero still decay, and move along their momentum
+    wl = synth.custom([(128, 256), (256, 128), (192, 64)], seed=2)
+    _, total = nsm.pack(wl.muon_shapes)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(99)
+    m_init = 0.01 * torch.randn(total, generator=gen, device="cuda")
+    for method in ("standard", "gram"):
+        s = Step(nsm, wl, method, momentum_init=m_init, zero_grads=(0, 2))
+        s.check()
+
+
+def test_step_all_zero(nsm):
+    # G = 0 and M = 0: U = 0, the orthogonalised update is 0, only the decay acts
+    wl = synth.custom([(128, 256), (64, 64)], seed=0)
+    for method in ("standard", "gram"):
+        s = Step(nsm, wl, method, zero_grads=(0, 1))
+        lr, wd = wl.lr, wl.wd
+        np.testing.assert_allclose(s.p1, s.p0 * np.float32(1 - np.float32(lr) * np.float32(wd)),
+                                   rtol=1e-6, atol=0)
+        assert np.all(s.m1 == 0)
+
+
+def test_packed_equals_per_matrix_bitwise(nsm):
+    shapes = [(128, 256), (256, 128), (96, 320), (128, 256)]
+    wl = synth.custom(shapes, seed=21)
+    for method in ("standard", "gram"):
+        packed = Step(nsm, wl, method)
+        for i, sh in enumerate(shapes):
+            offs, total = nsm.pack([sh])
+            grads = torch.from_numpy(packed.matrix(packed.g, i).reshape(-1)).to("cuda", torch.bfloat16)
+            params = torch.from_numpy(packed.matrix(packed.p0, i).reshape(-1)).to("cuda", torch.float32)
+            mom = torch.zeros_like(params)
+            ws = torch.empty(nsm.workspace_bytes([sh], method), dtype=torch.uint8, device="cuda")
+            nsm.muon_step(grads, params, mom, offs, [sh], wl.lr, wl.wd, wl.mu, method, 5, True, ws)
+            torch.cuda.synchronize()
+            assert np.array_equal(params.double().cpu().numpy(), packed.matrix(packed.p1, i).reshape(-1)), i
+
+
+def test_deterministic_bitwise(nsm):
+    wl = synth.workload("layer1024")
+    for method in ("standard", "gram"):
+        a = Step(nsm, wl, method)
+        b = Step(nsm, wl, method)
+        assert np.array_equal(a.p1, b.p1) and np.array_equal(a.m1, b.m1)
+
+
+def test_two_steps_accumulate_momentum(nsm):
+    # second step with a new gradient: the momentum path through two calls
+    wl = synth.custom([(256, 512), (512, 256)], seed=7)
+    offsets, total = nsm.pack(wl.muon_shapes)
+    dev = "cuda"
+    grads = torch.zeros(total, dtype=torch.bfloat16, device=dev)
+    params = torch.zeros(total, dtype=torch.float32, device=dev)
+    mom = torch.zeros(total, dtype=torch.float32, device=dev)
+    synth.fill_packed_params(wl, offsets, params)
+    ws = torch.empty(nsm.workspace_bytes(wl.muon_shapes, "gram"), dtype=torch.uint8, device=dev)
+    p = [params.double().cpu().numpy()]
+    m = [mom.double().cpu().numpy()]
+    g = []
+    for k in range(2):
+        synth.fill_packed_grads(wl, offsets, grads, seed_offset=k)
+        g.append(grads.double().cpu().numpy())
+        nsm.muon_step(grads, params, mom, offsets, wl.muon_shapes, wl.lr, wl.wd, wl.mu, "gram", 5,
+                      True, ws)
+        torch.cuda.synchronize()
+        p.append(params.double().cpu().numpy())
+        m.append(mom.double().cpu().numpy())
+    for i, (r, c) in enumerate(wl.muon_shapes):
+        o = int(offsets[i])
+        sl = slice(o, o + r * c)
+        pr, mr = p[0][sl].reshape(r, c), m[0][sl].reshape(r, c)
+        for k in range(2):
+            (pr,), (mr,), _ = oracle.muon_step([g[k][sl].reshape(r, c)], [pr], [mr], wl.lr, wl.wd,
+                                               wl.mu, "gram")
+        assert rel(m[2][sl].reshape(r, c), mr) <= TOL_FP32
+        assert rel(p[2][sl].reshape(r, c) - p[0][sl].reshape(r, c), pr - p[0][sl].reshape(r, c)) <= TOL_DELTA
+
+
+# ------------------------------------------------------------------ AdamW
+
+@pytest.mark.parametrize("numel", [1, 7, 8, 1000, 1000003])
+def test_adamw(nsm, numel):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(numel)
+    g = (0.01 * torch.randn(numel, generator=gen, device="cuda")).to(torch.bfloat16)
+    p = 0.02 * torch.randn(numel, generator=gen, device="cuda")
+    m = 1e-3 * torch.randn(numel, generator=gen, device="cuda")
+    v = 1e-5 * torch.rand(numel, generator=gen, device="cuda")
+    host = [t.double().cpu().numpy() for t in (g, p, m, v)]
+    for step in (1, 2, 10):
+        nsm.adamw_step(g, p, m, v, 3e-4, 0.9, 0.95, 1e-8, 0.1, step)
+        torch.cuda.synchronize()
+        pr, mr, vr = oracle.adamw_step(host[0], host[1], host[2], host[3], 3e-4, 0.9, 0.95, 1e-8,
+                                       0.1, step)
+        host = [host[0], pr, mr, vr]
+        assert rel(p.double().cpu().numpy(), pr) <= TOL_FP32
+        assert rel(m.double().cpu().numpy(), mr) <= TOL_FP32
+        assert rel(v.double().cpu().numpy(), vr) <= TOL_FP32
+
+
+def test_adamw_group_of_workload(nsm):
+    wl = synth.workload("gpt2small")
+    g, p = synth.make_adam_group(wl, "cuda")
+    n = p.numel()
+    m = torch.zeros(n, device="cuda")
+    v = torch.zeros(n, device="cuda")
+    p0 = p.double().cpu().numpy()
+    nsm.adamw_step(g, p, m, v, 3e-4, 0.9, 0.95, 1e-10, wl.wd, 1)
+    torch.cuda.synchronize()
+    pr, mr, vr = oracle.adamw_step(g.double().cpu().numpy(), p0, np.zeros(n), np.zeros(n), 3e-4,
+                                   0.9, 0.95, 1e-10, wl.wd, 1)
+    assert rel(p.double().cpu().numpy() - p0, pr - p0) <= TOL_FP32 * 10
+    assert rel(m.double().cpu().numpy(), mr) <= TOL_FP32
+
+
+# ------------------------------------------------------------------ boundary on a GPU
+
+def test_errors_launch_nothing(nsm):
+    wl = synth.workload("tiny")
+    offsets, total = nsm.pack(wl.muon_shapes)
+    g = torch.zeros(total, dtype=torch.bfloat16, device="cuda")
+    p = torch.zeros(total, device="cuda")
+    m = torch.zeros(total, device="cuda")
+    small = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(nsm.NsmError) as e:
+        nsm.muon_step(g, p, m, offsets, wl.muon_shapes, workspace=small)
+    assert e.value.code == nsm.NSM_ERR_WORKSPACE
+    with pytest.raises(nsm.NsmError) as e:
+        nsm.muon_step(g, p, p, offsets, wl.muon_shapes, workspace=small)
+    assert e.value.code == nsm.NSM_ERR_ARG
+    torch.cuda.synchronize()
+    assert nsm.device_status() == nsm.NSM_OK
