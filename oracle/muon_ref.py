@@ -25,7 +25,10 @@ Readings taken where the pages are silent (each is listed again in the design no
   iterate always has ``m = min(rows, cols)`` rows.
 * the same (a, b, c) on every Newton-Schulz step.
 * gram form: iterate on ``R = X X^T`` and accumulate the left polynomial ``Q``
-  (derivation in :func:`ns_gram`); no restarts.
+  (derivation in :func:`ns_gram`), re-anchoring ``R`` from the explicit iterate every
+  two steps (exact-arithmetic no-op; keeps the fp16 iteration accurate).
+* storage precision: the pages fix bf16 for the standard form and fp16 for the gram
+  form; ``storage="method"`` rounds at exactly the points where the method stores.
 * update scale ``sqrt(max(1, rows/cols))`` of the original (untransposed) matrix.
 * AdamW: the textbook decoupled form with bias correction, eps outside the square
   root, step counter starting at 1.
@@ -65,6 +68,55 @@ NS_METHODS = ("standard", "gram")
 
 # Reading (pages silent): the epsilon added to the Frobenius norm.
 NORM_EPS = 1e-7
+
+
+# --- storage formats -------------------------------------------------------------------
+#
+# [DSM] §核心算子 fixes the precision the method stores its iterates in: the five-step
+# iteration runs in bf16 ("stable in bf16"), the gram variant in fp16 ("uses fp16 for
+# better half-precision accuracy").  With ``storage`` set, the routines below round every
+# intermediate the method stores to that format (round to nearest, ties to even) and
+# accumulate everything else in float64.  With ``storage=None`` they are the exact
+# float64 iteration.
+
+_FORMATS = {
+    # significant bits, smallest normal exponent, largest finite value
+    "bf16": (8, -126, float.fromhex("0x1.fep127")),
+    "fp16": (11, -14, 65504.0),
+}
+
+
+def round_to(x, fmt):
+    """Round float64 values to the nearest ``fmt`` value (ties to even), exactly.
+
+    The spacing of ``fmt`` values around ``x`` is ``2**(e - p + 1)`` for
+    ``2**e <= |x| < 2**(e+1)`` (``p`` significant bits), never finer than the subnormal
+    spacing ``2**(emin - p + 1)``; scaling by a power of two and ``np.rint`` (ties to
+    even) are exact in float64.  Values beyond the largest finite one become inf.
+    """
+    if fmt is None:
+        return np.asarray(x, dtype=np.float64)
+    p, emin, vmax = _FORMATS[fmt]
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x, dtype=np.float64, copy=True)
+    finite = np.isfinite(x) & (x != 0)
+    xf = x[finite]
+    _, e2 = np.frexp(np.abs(xf))          # |x| = f * 2**e2 with f in [0.5, 1)
+    e = np.maximum(e2 - 1, emin)           # exponent of the leading bit, clamped
+    ulp = np.ldexp(1.0, (e - (p - 1)).astype(np.int64))
+    r = np.rint(xf / ulp) * ulp
+    r[np.abs(r) > vmax] = np.inf * np.sign(r[np.abs(r) > vmax])
+    out[finite] = r
+    return out
+
+
+def method_storage(method):
+    """Storage format the pages give each ns_method: bf16 (standard), fp16 (gram)."""
+    return {"standard": "bf16", "gram": "fp16"}[method]
+
+
+def _store(x, storage):
+    return x if storage is None else round_to(x, storage)
 
 
 # --- a0: routing ---------------------------------------------------------------------
@@ -175,70 +227,92 @@ def ns_poly_iterated(x, steps: int = NS_STEPS, a: float = NS_A, b: float = NS_B,
 # --- a4: Newton-Schulz, standard form -----------------------------------------------
 
 def ns_standard(x: np.ndarray, steps: int = NS_STEPS, a: float = NS_A, b: float = NS_B,
-                c: float = NS_C) -> np.ndarray:
+                c: float = NS_C, storage=None) -> np.ndarray:
     """Standard quintic Newton-Schulz on an already normalised ``m x n`` iterate.
 
     [DSM] §核心算子 (``zeropower_via_newtonschulz5``): each step forms
-    ``A = X X^T``, ``B = b A + c A A`` and replaces ``X`` by ``a X + B X``.
+    ``A = X X^T``, ``B = b A + c A A`` and replaces ``X`` by ``a X + B X``.  With
+    ``storage`` the input, ``A``, ``B`` and every new ``X`` are rounded to that format.
     """
-    x = np.array(x, dtype=np.float64)
+    x = _store(np.array(x, dtype=np.float64), storage)
     for _ in range(steps):
-        gram_a = x @ x.T
-        poly_b = b * gram_a + c * (gram_a @ gram_a)
-        x = a * x + poly_b @ x
+        gram_a = _store(x @ x.T, storage)
+        poly_b = _store(b * gram_a + c * (gram_a @ gram_a), storage)
+        x = _store(a * x + poly_b @ x, storage)
     return x
 
 
 # --- a4': Newton-Schulz, gram form ----------------------------------------------------
 
 def ns_gram(x: np.ndarray, steps: int = NS_STEPS, a: float = NS_A, b: float = NS_B,
-            c: float = NS_C) -> np.ndarray:
-    """Gram-form Newton-Schulz: iterate only on the small square ``R = X X^T``.
+            c: float = NS_C, storage=None, restart_every: int = 2) -> np.ndarray:
+    """Gram-form Newton-Schulz: iterate on the small square ``R = X X^T``.
 
     [DSM] §核心算子 (``zeropower_via_gram_newtonschulz``) says the variant iterates on
-    the Gram matrix ``R = X @ X.T`` to save FLOPs on wide matrices.  Reading of the
-    steps: every iterate of the standard form is ``X_k = Q_k X_0`` with ``Q_k`` a
+    the Gram matrix ``R = X @ X.T`` to save FLOPs on wide matrices, in fp16.  Reading of
+    the steps: every iterate of the standard form is ``X_k = Q_k X_0`` with ``Q_k`` a
     polynomial in ``R_0 = X_0 X_0^T``, hence ``X_k X_k^T = Q_k R_0 Q_k``.  One step with
-    ``H = a I + b R + c R R`` sends ``Q -> H Q`` and ``R -> H R H``; the final result is
-    ``Q X_0``.  The last step does not need the ``R`` update.
+    ``H = a I + b R + c R R`` sends ``Q -> H Q`` and ``R -> H R H`` (formed as
+    ``T = H R``, ``R = T H``); the result is ``Q X``.  The last step needs no ``R``.
+
+    Re-anchoring: every ``restart_every`` steps (when more steps follow) the iterate is
+    formed explicitly, ``X <- Q X``, ``Q <- I`` and ``R <- X X^T``.  In exact arithmetic
+    this changes nothing (``X X^T = Q R Q``); in fp16 it keeps the small eigenvalues of
+    ``R`` from drowning in the rounding of the large ones.  ``restart_every=0`` never
+    re-anchors.  With ``storage`` every stored matrix (``X``, ``R``, ``H``, ``Q``,
+    ``T``, the result) is rounded to that format.
     """
-    x0 = np.array(x, dtype=np.float64)
-    m = x0.shape[0]
+    x = _store(np.array(x, dtype=np.float64), storage)
+    m = x.shape[0]
     eye = np.eye(m)
-    r = x0 @ x0.T
-    q = eye.copy()
-    for step in range(steps):
-        h = a * eye + b * r + c * (r @ r)
-        q = h @ q
-        if step + 1 < steps:
-            r = h @ r @ h
-    return q @ x0
+    r = _store(x @ x.T, storage)
+    q = None  # None stands for the identity
+    for step in range(1, steps + 1):
+        h = _store(a * eye + b * r + c * (r @ r), storage)
+        q = h if q is None else _store(h @ q, storage)
+        if step < steps:
+            if restart_every and step % restart_every == 0:
+                x = _store(q @ x, storage)
+                q = None
+                r = _store(x @ x.T, storage)
+            else:
+                t = _store(h @ r, storage)
+                r = _store(t @ h, storage)
+    return x if q is None else _store(q @ x, storage)
 
 
 def newton_schulz(x: np.ndarray, method: str = NS_METHOD_DEFAULT, steps: int = NS_STEPS,
-                  a: float = NS_A, b: float = NS_B, c: float = NS_C) -> np.ndarray:
+                  a: float = NS_A, b: float = NS_B, c: float = NS_C, storage=None) -> np.ndarray:
     """Dispatch on ``ns_method`` ([DSM] §核心算子: ``NS_METHODS = {standard, gram}``)."""
     if method == "standard":
-        return ns_standard(x, steps, a, b, c)
+        return ns_standard(x, steps, a, b, c, storage)
     if method == "gram":
-        return ns_gram(x, steps, a, b, c)
+        return ns_gram(x, steps, a, b, c, storage)
     raise ValueError(f"unknown ns_method {method!r}")
 
 
+def _resolve_storage(storage, method):
+    if storage == "method":
+        return method_storage(method)
+    return storage
+
+
 def orthogonalize(u: np.ndarray, method: str = NS_METHOD_DEFAULT, steps: int = NS_STEPS,
-                  eps: float = NORM_EPS) -> np.ndarray:
+                  eps: float = NORM_EPS, storage=None) -> np.ndarray:
     """Normalise, transpose when tall, run Newton-Schulz, transpose back.
 
-    Returns ``O`` with the shape of ``u``.
+    Returns ``O`` with the shape of ``u``.  ``storage="method"`` stores the iterates in
+    the format the pages give the method (bf16 standard, fp16 gram); ``None`` is exact.
     """
     u = np.asarray(u, dtype=np.float64)
     if u.ndim != 2:
         raise ValueError("orthogonalize takes a 2D matrix")
+    storage = _resolve_storage(storage, method)
     rows, cols = u.shape
     transposed = rows > cols
     x = u.T if transposed else u
     x = frobenius_normalize(x, eps)
-    o = newton_schulz(x, method, steps)
+    o = newton_schulz(x, method, steps, storage=storage)
     return o.T if transposed else o
 
 
@@ -261,7 +335,8 @@ def apply_update(param: np.ndarray, ortho: np.ndarray, lr: float, wd: float) -> 
 def muon_step(grads: Sequence[np.ndarray], params: Sequence[np.ndarray],
               momenta: Sequence[np.ndarray], lr: float, wd: float,
               mu: float = MUON_MOMENTUM_DEFAULT, method: str = NS_METHOD_DEFAULT,
-              steps: int = NS_STEPS, nesterov: bool = True, eps: float = NORM_EPS):
+              steps: int = NS_STEPS, nesterov: bool = True, eps: float = NORM_EPS,
+              storage=None):
     """The owner-side Muon step over a list of matrices.
 
     [DSM] §什么是 Muon 优化器？ — momentum, then Newton-Schulz orthogonalisation of the
@@ -272,7 +347,7 @@ def muon_step(grads: Sequence[np.ndarray], params: Sequence[np.ndarray],
     new_params, new_momenta, orthos = [], [], []
     for g, p, m in zip(grads, params, momenta):
         m_new, u = momentum_update(g, m, mu, nesterov)
-        o = orthogonalize(u, method, steps, eps)
+        o = orthogonalize(u, method, steps, eps, storage)
         new_params.append(apply_update(p, o, lr, wd))
         new_momenta.append(m_new)
         orthos.append(o)
@@ -318,11 +393,26 @@ def flops_standard(m: int, n: int, steps: int = NS_STEPS) -> int:
     return steps * (4 * m * m * n + 2 * m ** 3)
 
 
-def flops_gram(m: int, n: int, steps: int = NS_STEPS) -> int:
-    """Canonical flop count of the gram form: ``R_0`` and the final ``Q X_0``
-    (``2 m^2 n`` each) plus ``2 m^3`` for each of ``R R``, ``H Q`` (not on the first
-    step, where ``Q = H``) and the two products of ``H R H`` (not on the last step)."""
+def flops_gram(m: int, n: int, steps: int = NS_STEPS, restart_every: int = 2) -> int:
+    """Flop count of :func:`ns_gram` as written: ``2 m^2 n`` for each product with
+    ``X`` (``R_0``, every re-anchoring ``Q X`` and ``X X^T``, the final ``Q X``) and
+    ``2 m^3`` for each square product (``R R``; ``H Q`` unless ``Q`` is the identity;
+    the two products of ``H R H``)."""
     if steps <= 0:
         return 0
-    n_cubes = steps + (steps - 1) + 2 * (steps - 1)
-    return 4 * m * m * n + 2 * n_cubes * m ** 3
+    wide = 1          # R_0
+    cubes = 0
+    q_identity = True
+    for step in range(1, steps + 1):
+        cubes += 1                      # R R inside H
+        if not q_identity:
+            cubes += 1                  # H Q
+        q_identity = False
+        if step < steps:
+            if restart_every and step % restart_every == 0:
+                wide += 2               # X <- Q X, R <- X X^T
+                q_identity = True
+            else:
+                cubes += 2              # T = H R, R = T H
+    wide += 0 if q_identity else 1      # final Q X (skipped when Q is the identity)
+    return 2 * wide * m * m * n + 2 * cubes * m ** 3

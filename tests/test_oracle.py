@@ -340,9 +340,113 @@ def _count_macs_standard(m, n, steps):
 def test_flop_counts():
     for m, n in [(2, 3), (128, 4096), (4096, 11008)]:
         assert oracle.flops_standard(m, n) == _count_macs_standard(m, n, 5)
-    # gram, 5 steps: R0 and Q X0 (m^2 n MACs each); R R x5; H Q x4; H R H = 2 per step x4
+    # gram, 5 steps, never re-anchored: R0 and Q X0 (m^2 n MACs each); R R x5; H Q x4;
+    # H R H = 2 per step x4
     m, n = 7, 11
-    assert oracle.flops_gram(m, n) == 2 * (2 * m * m * n + (5 + 4 + 8) * m ** 3)
+    assert oracle.flops_gram(m, n, restart_every=0) == 2 * (2 * m * m * n + (5 + 4 + 8) * m ** 3)
+    # re-anchored after steps 2 and 4: products with X are R0, (Q X, X X^T) twice and the
+    # final Q X = 6; squares: step1 R R, T, R; step2 R R, H Q; step3 R R, T, R;
+    # step4 R R, H Q; step5 R R = 11
+    assert oracle.flops_gram(m, n) == 2 * (6 * m * m * n + 11 * m ** 3)
+    assert oracle.flops_gram(m, n, steps=1) == 2 * (2 * m * m * n + 1 * m ** 3)
+
+
+def _mac_count_gram(m, n, steps, restart_every):
+    """Counts MACs by running the gram iteration on shape placeholders."""
+    macs = m * m * n  # R0
+    q_identity = True
+    for step in range(1, steps + 1):
+        macs += m ** 3
+        if not q_identity:
+            macs += m ** 3
+        q_identity = False
+        if step < steps:
+            if restart_every and step % restart_every == 0:
+                macs += 2 * m * m * n
+                q_identity = True
+            else:
+                macs += 2 * m ** 3
+    if not q_identity:
+        macs += m * m * n
+    return 2 * macs
+
+
+def test_flop_counts_gram_schedules():
+    for steps in range(0, 8):
+        for every in (0, 1, 2, 3):
+            if steps == 0:
+                assert oracle.flops_gram(9, 13, steps, every) == 0
+            else:
+                assert oracle.flops_gram(9, 13, steps, every) == _mac_count_gram(9, 13, steps, every)
+
+
+# ---------------------------------------------------------------- storage rounding
+
+def test_round_to_ties_by_hand():
+    # bf16 keeps 8 significant bits: neighbours of 1 are 1 and 1 + 2^-7
+    assert oracle.round_to(1 + 2 ** -8, "bf16") == 1.0             # tie -> even
+    assert oracle.round_to(1 + 3 * 2 ** -8, "bf16") == 1 + 2 ** -6  # tie -> even
+    assert oracle.round_to(1 + 2 ** -8 + 2 ** -20, "bf16") == 1 + 2 ** -7
+    # fp16 keeps 11 significant bits, largest finite 65504, subnormal spacing 2^-24
+    assert oracle.round_to(1 + 2 ** -11, "fp16") == 1.0
+    assert oracle.round_to(65504.0, "fp16") == 65504.0
+    assert np.isinf(oracle.round_to(65520.0, "fp16"))              # ties away to inf
+    assert oracle.round_to(3 * 2 ** -25, "fp16") == 2 ** -23       # subnormal tie -> even
+    assert oracle.round_to(2 ** -26, "fp16") == 0.0
+    assert oracle.round_to(-0.0, "bf16") == 0.0
+
+
+def test_round_to_matches_library_conversions():
+    import torch
+    rng = np.random.default_rng(0)
+    # float32 inputs (exact in float64), spanning normal, subnormal and overflow ranges
+    for scale in (1.0, 1e-3, 1e-30, 1e-39, 1e30, 1e38):
+        x32 = (rng.standard_normal(20000) * scale).astype(np.float32)
+        x = x32.astype(np.float64)
+        bf = torch.from_numpy(x32).to(torch.bfloat16).double().numpy()
+        assert np.array_equal(oracle.round_to(x, "bf16"), bf), scale
+        f16 = x32.astype(np.float16).astype(np.float64)
+        assert np.array_equal(oracle.round_to(x, "fp16"), f16), scale
+
+
+def test_method_storage_formats():
+    g = _golden("pages_constants.json")
+    assert oracle.method_storage("standard") == "bf16"
+    assert oracle.method_storage("gram") == "fp16"
+
+
+@pytest.mark.parametrize("every", [0, 1, 2, 3])
+@pytest.mark.parametrize("steps", [1, 2, 5, 6])
+def test_gram_reanchoring_is_exact_noop(every, steps):
+    rng = np.random.default_rng(steps * 10 + every)
+    x = rng.standard_normal((12, 31))
+    x /= np.linalg.norm(x)
+    assert np.max(np.abs(oracle.ns_gram(x, steps, restart_every=every) -
+                         oracle.ns_standard(x, steps))) < 1e-10
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_storage_mode_close_on_well_conditioned_input(method):
+    # singular values of X in [0.2, 0.6]: the iteration is not in its steep region, so
+    # half-precision storage stays within a few units of its rounding of the exact map
+    m, n = 24, 40
+    uu, s, vv = _known_svd(m, n, np.linspace(1.0, 0.35, m), seed=4)
+    g = (uu * s) @ vv.T
+    exact = oracle.orthogonalize(g, method)
+    stored = oracle.orthogonalize(g, method, storage="method")
+    err = np.linalg.norm(stored - exact) / np.linalg.norm(exact)
+    assert 0 < err < 2e-2
+    # the result is a value of the storage format
+    fmt = oracle.method_storage(method)
+    assert np.array_equal(oracle.round_to(stored, fmt), stored)
+
+
+def test_storage_mode_none_is_exact():
+    rng = np.random.default_rng(8)
+    g = rng.standard_normal((6, 9))
+    for method in ("standard", "gram"):
+        assert np.array_equal(oracle.orthogonalize(g, method, storage=None),
+                              oracle.orthogonalize(g, method))
 
 
 # ---------------------------------------------------------------- page arithmetic

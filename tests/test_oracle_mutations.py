@@ -118,3 +118,28 @@ def test_adamw_mutants_fail():
     p, _, _ = oracle.adamw_step(np.array([2.0]), np.array([1.0]), np.array([0.0]),
                                 np.array([0.0]), 0.5, 0.5, 0.5, 0.0, 0.5, 1)
     assert p[0] == 0.25 and p_no_bc != 0.25
+
+
+def test_storage_mutants_fail():
+    # dropping the rounding of A (or of the input) changes the stored-precision result
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((16, 24))
+    x /= np.linalg.norm(x)
+    good = oracle.ns_standard(x, storage="bf16")
+
+    def no_round_a(x):
+        r = lambda v: oracle.round_to(v, "bf16")
+        x = r(x)
+        for _ in range(5):
+            a_ = x @ x.T
+            x = r(A * x + r(B * a_ + C * a_ @ a_) @ x)
+        return x
+
+    def unrounded_input(x):
+        r = lambda v: oracle.round_to(v, "bf16")
+        for _ in range(5):
+            a_ = r(x @ x.T)
+            x = r(A * x + r(B * a_ + C * a_ @ a_) @ x)
+        return x
+    assert not np.array_equal(no_round_a(x), good)
+    assert not np.array_equal(unrounded_input(x), good)
