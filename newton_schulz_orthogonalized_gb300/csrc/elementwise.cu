@@ -1,10 +1,11 @@
 // Memory-bound kernels of the Muon step and the fused AdamW step.
 //
-//   k_momentum_norm  M <- mu M + G; U = G + mu M (Nesterov) or M; U stored bf16 in the
-//                    matrix's workspace slot; per-chunk sums of U^2 (fixed order)
+//   k_momentum_norm  M <- mu M + G; per-chunk sums of U^2 with U = G + mu M (Nesterov)
+//                    or M, in fp32 (fixed order)
 //   k_norm_finalize  s_i = 1 / (sqrt(sum of matrix i's chunk sums) + eps), fixed order
-//   k_to_class       X = s U moved from the natural row-major layout into the matrix's
-//                    slot (transposed when rows > cols), bf16 or fp16
+//   k_to_class       X = s U with U recomputed in fp32 from G and the updated M, moved
+//                    from the natural row-major layout into the matrix's slot
+//                    (transposed when rows > cols) and rounded once to bf16 or fp16
 //   k_apply          p <- p (1 - lr wd) - lr sqrt(max(1, rows/cols)) O, O read back from
 //                    the slot (transposed back when rows > cols)
 //   k_export         O copied back to a natural bf16 layout
@@ -22,6 +23,9 @@ namespace nsm {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kUFromGrad = 0;   // U = G (orthogonalisation only)
+constexpr int kUMomentum = 1;   // U = M (momentum already updated)
+constexpr int kUNesterov = 2;   // U = G + mu M
 
 __device__ __forceinline__ int find_by_chunk(const MatInfo* __restrict__ mats, int nmats, int c) {
   int lo = 0, hi = nmats - 1;
@@ -122,8 +126,8 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
 template <bool HAS_M, bool NESTEROV>
 __global__ void __launch_bounds__(kThreads)
     k_momentum_norm(const __nv_bfloat16* __restrict__ grads, float* __restrict__ mom,
-                    __nv_bfloat16* __restrict__ u_base, const MatInfo* __restrict__ mats,
-                    int nmats, int total_chunks, float* __restrict__ partials, float mu) {
+                    const MatInfo* __restrict__ mats, int nmats, int total_chunks,
+                    float* __restrict__ partials, float mu) {
   __shared__ float scratch[kThreads / 32];
   for (int chunk = blockIdx.x; chunk < total_chunks; chunk += gridDim.x) {
     const MatInfo& mt = mats[find_by_chunk(mats, nmats, chunk)];
@@ -132,7 +136,6 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t end = min(start + static_cast<int64_t>(kChunk), len);
     const __nv_bfloat16* g = grads + mt.off;
     float* m = HAS_M ? mom + mt.off : nullptr;
-    __nv_bfloat16* u = HAS_M ? u_base + mt.slot : nullptr;
     float acc = 0.f;
     const int64_t nvec = (end - start) >> 3;
     for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
@@ -143,17 +146,15 @@ __global__ void __launch_bounds__(kThreads)
         float4* mp = reinterpret_cast<float4*>(m + i);
         const float4 m0 = mp[0], m1 = mp[1];
         float mf[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        float uf[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float mn = fmaf(mu, mf[j], gf[j]);
           mf[j] = mn;
-          uf[j] = NESTEROV ? fmaf(mu, mn, gf[j]) : mn;
-          acc = fmaf(uf[j], uf[j], acc);
+          const float u = NESTEROV ? fmaf(mu, mn, gf[j]) : mn;
+          acc = fmaf(u, u, acc);
         }
         mp[0] = make_float4(mf[0], mf[1], mf[2], mf[3]);
         mp[1] = make_float4(mf[4], mf[5], mf[6], mf[7]);
-        *reinterpret_cast<uint4*>(u + i) = pack_bf16x8(uf);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc = fmaf(gf[j], gf[j], acc);
@@ -165,7 +166,6 @@ __global__ void __launch_bounds__(kThreads)
         const float mn = fmaf(mu, m[i], gv);
         m[i] = mn;
         const float uv = NESTEROV ? fmaf(mu, mn, gv) : mn;
-        u[i] = __float2bfloat16_rn(uv);
         acc = fmaf(uv, uv, acc);
       } else {
         acc = fmaf(gv, gv, acc);
@@ -207,17 +207,41 @@ __device__ __forceinline__ TilePos tile_pos(const MatInfo* __restrict__ mats, in
   return {mi, tr * kTile, tc * kTile};
 }
 
-// Natural bf16 U (row stride cols) -> slot X (row stride ld), scaled; transposed when tall.
-template <bool TO_FP16>
+// U of eight consecutive natural elements: G (no momentum), M (plain momentum, already
+// updated) or G + mu M (Nesterov).
+template <int MODE>
+__device__ __forceinline__ void load_u8(const __nv_bfloat16* g, const float* m, int64_t i, float mu,
+                                        float (&u)[8]) {
+  unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(g + i)), u);
+  if (MODE != kUFromGrad) {
+    const float4 m0 = __ldg(reinterpret_cast<const float4*>(m + i));
+    const float4 m1 = __ldg(reinterpret_cast<const float4*>(m + i + 4));
+    const float mf[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) u[q] = (MODE == kUNesterov) ? fmaf(mu, mf[q], u[q]) : mf[q];
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ float load_u1(const __nv_bfloat16* g, const float* m, int64_t i, float mu) {
+  if (MODE == kUFromGrad) return __bfloat162float(g[i]);
+  if (MODE == kUMomentum) return m[i];
+  return fmaf(mu, m[i], __bfloat162float(g[i]));
+}
+
+// X = s U moved from the natural row-major layout (row stride cols) into the matrix's
+// slot (row stride ld), transposed when rows > cols, rounded once to bf16/fp16.
+template <bool TO_FP16, int MODE>
 __global__ void __launch_bounds__(kThreads)
-    k_to_class(const __nv_bfloat16* __restrict__ src, int src_is_slot, void* __restrict__ dst,
-               const MatInfo* __restrict__ mats, int nmats, int64_t total_tiles,
-               const float* __restrict__ scales) {
+    k_to_class(const __nv_bfloat16* __restrict__ grads, const float* __restrict__ mom, float mu,
+               void* __restrict__ dst, const MatInfo* __restrict__ mats, int nmats,
+               int64_t total_tiles, const float* __restrict__ scales) {
   __shared__ float tile[kTile][kTile + 1];
   for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
     const TilePos tp = tile_pos(mats, nmats, t);
     const MatInfo& mt = mats[tp.mi];
-    const __nv_bfloat16* s = src + (src_is_slot ? mt.slot : mt.off);
+    const __nv_bfloat16* g = grads + mt.off;
+    const float* m = (MODE == kUFromGrad) ? nullptr : mom + mt.off;
     const int64_t d0 = mt.slot;
     const float sc = scales[tp.mi];
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
@@ -227,7 +251,7 @@ __global__ void __launch_bounds__(kThreads)
           const int r = tp.r0 + (j >> 3), c = tp.c0 + (j & 7) * 8;
           if (r < rows && c < cols) {
             float f[8];
-            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(s + static_cast<int64_t>(r) * cols + c)), f);
+            load_u8<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu, f);
 #pragma unroll
             for (int q = 0; q < 8; ++q) f[q] *= sc;
             store8<TO_FP16>(dst, d0 + static_cast<int64_t>(r) * ld + c, f);
@@ -237,7 +261,7 @@ __global__ void __launch_bounds__(kThreads)
         for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
           const int r = tp.r0 + (j >> 6), c = tp.c0 + (j & 63);
           if (r < rows && c < cols) {
-            const float v = __bfloat162float(s[static_cast<int64_t>(r) * cols + c]) * sc;
+            const float v = load_u1<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu) * sc;
             store_half<TO_FP16>(dst, d0 + static_cast<int64_t>(r) * ld + c, v);
           }
         }
@@ -249,9 +273,7 @@ __global__ void __launch_bounds__(kThreads)
           const int rr = j >> 3, cc = (j & 7) * 8;
           const int r = tp.r0 + rr, c = tp.c0 + cc;
           float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (r < rows && c < cols) {
-            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(s + static_cast<int64_t>(r) * cols + c)), f);
-          }
+          if (r < rows && c < cols) load_u8<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu, f);
 #pragma unroll
           for (int q = 0; q < 8; ++q) tile[rr][cc + q] = f[q];
         }
@@ -270,7 +292,7 @@ __global__ void __launch_bounds__(kThreads)
         for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
           const int rr = j >> 6, cc = j & 63;
           const int r = tp.r0 + rr, c = tp.c0 + cc;
-          tile[rr][cc] = (r < rows && c < cols) ? __bfloat162float(s[static_cast<int64_t>(r) * cols + c]) : 0.f;
+          tile[rr][cc] = (r < rows && c < cols) ? load_u1<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu) : 0.f;
         }
         __syncthreads();
         for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
@@ -434,22 +456,20 @@ int grid_for(int64_t items, int per_sm) {
 
 }  // namespace
 
-cudaError_t launch_momentum_norm(const void* grads, float* momentum, void* u_base,
-                                 const MatInfo* mats, int nmats, int total_chunks,
-                                 float* partials, float mu, int nesterov, int has_momentum,
-                                 cudaStream_t stream) {
+cudaError_t launch_momentum_norm(const void* grads, float* momentum, const MatInfo* mats, int nmats,
+                                 int total_chunks, float* partials, float mu, int nesterov,
+                                 int has_momentum, cudaStream_t stream) {
   const int grid = grid_for(total_chunks, 8);
   const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
-  auto* u = reinterpret_cast<__nv_bfloat16*>(u_base);
   if (!has_momentum) {
-    k_momentum_norm<false, false><<<grid, kThreads, 0, stream>>>(g, nullptr, nullptr, mats, nmats,
-                                                                 total_chunks, partials, mu);
+    k_momentum_norm<false, false><<<grid, kThreads, 0, stream>>>(g, nullptr, mats, nmats, total_chunks,
+                                                                 partials, mu);
   } else if (nesterov) {
-    k_momentum_norm<true, true><<<grid, kThreads, 0, stream>>>(g, momentum, u, mats, nmats,
-                                                               total_chunks, partials, mu);
+    k_momentum_norm<true, true><<<grid, kThreads, 0, stream>>>(g, momentum, mats, nmats, total_chunks,
+                                                               partials, mu);
   } else {
-    k_momentum_norm<true, false><<<grid, kThreads, 0, stream>>>(g, momentum, u, mats, nmats,
-                                                                total_chunks, partials, mu);
+    k_momentum_norm<true, false><<<grid, kThreads, 0, stream>>>(g, momentum, mats, nmats, total_chunks,
+                                                                partials, mu);
   }
   return cudaGetLastError();
 }
@@ -462,16 +482,27 @@ cudaError_t launch_norm_finalize(const MatInfo* mats, int nmats, const float* pa
   return cudaGetLastError();
 }
 
-cudaError_t launch_to_class(const void* src, int src_is_slot, void* dst, int to_fp16,
-                            const MatInfo* mats, int nmats, int64_t total_tiles,
+template <bool TO_FP16>
+static void to_class_mode(int mode, int grid, const __nv_bfloat16* g, const float* m, float mu, void* dst,
+                          const MatInfo* mats, int nmats, int64_t total_tiles, const float* scales,
+                          cudaStream_t stream) {
+  if (mode == kUFromGrad) {
+    k_to_class<TO_FP16, kUFromGrad><<<grid, kThreads, 0, stream>>>(g, m, mu, dst, mats, nmats, total_tiles, scales);
+  } else if (mode == kUMomentum) {
+    k_to_class<TO_FP16, kUMomentum><<<grid, kThreads, 0, stream>>>(g, m, mu, dst, mats, nmats, total_tiles, scales);
+  } else {
+    k_to_class<TO_FP16, kUNesterov><<<grid, kThreads, 0, stream>>>(g, m, mu, dst, mats, nmats, total_tiles, scales);
+  }
+}
+
+cudaError_t launch_to_class(const void* grads, const float* momentum, int has_momentum, int nesterov, float mu,
+                            void* dst, int to_fp16, const MatInfo* mats, int nmats, int64_t total_tiles,
                             const float* scales, cudaStream_t stream) {
   const int grid = grid_for(total_tiles, 8);
-  const auto* s = reinterpret_cast<const __nv_bfloat16*>(src);
-  if (to_fp16) {
-    k_to_class<true><<<grid, kThreads, 0, stream>>>(s, src_is_slot, dst, mats, nmats, total_tiles, scales);
-  } else {
-    k_to_class<false><<<grid, kThreads, 0, stream>>>(s, src_is_slot, dst, mats, nmats, total_tiles, scales);
-  }
+  const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
+  const int mode = !has_momentum ? kUFromGrad : (nesterov ? kUNesterov : kUMomentum);
+  if (to_fp16) to_class_mode<true>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, stream);
+  else to_class_mode<false>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, stream);
   return cudaGetLastError();
 }
 

@@ -30,6 +30,7 @@ constexpr float kB = -4.7750f;
 constexpr float kC = 2.0315f;
 constexpr float kNormEps = 1e-7f;
 constexpr int kMaxSteps = 16;
+constexpr int kGramReanchor = 2;  // gram form: re-anchor R from the explicit iterate every 2 steps
 constexpr int kMaxMatrices = 1 << 22;
 constexpr int64_t kMaxDim = int64_t(1) << 30;
 constexpr size_t kAlign = 1024;
@@ -270,42 +271,57 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     P.final_buf = (steps % 2 == 0) ? X0 : X1;
     P.final_fp16 = false;
   } else {
-    if (steps == 0) {
-      P.final_buf = X0;
-    } else {
-      int rR = MM0, rQ = -1;
-      std::vector<int> freeb = {MM0 + 1, MM0 + 2, MM0 + 3};
-      stages.push_back({X0, X0, rR, -1, false, true, false, 1.f, 0.f, 0.f});                // R0 = X X^T
-      for (int k = 1; k <= steps; ++k) {
-        const int h = freeb[0];
-        stages.push_back({rR, rR, h, rR, false, false, false, kC, kB, kA});                  // H
-        if (k == 1) {
-          rQ = h;                                                                             // Q1 = H1
-          freeb = {freeb[1], freeb[2]};
-          if (k < steps) {
-            const int t = freeb[0];
-            stages.push_back({h, rR, t, -1, false, false, false, 1.f, 0.f, 0.f});            // T = H R
-            stages.push_back({t, h, rR, -1, false, false, false, 1.f, 0.f, 0.f});            // R = T H
-            // free: t and the remaining one
-          }
-        } else {
-          const int qn = freeb[1];
-          stages.push_back({h, rQ, qn, -1, false, false, false, 1.f, 0.f, 0.f});             // Q' = H Q
-          const int old_q = rQ;
-          if (k < steps) {
-            stages.push_back({h, rR, old_q, -1, false, false, false, 1.f, 0.f, 0.f});        // T = H R
-            stages.push_back({old_q, h, rR, -1, false, false, false, 1.f, 0.f, 0.f});        // R = T H
-          }
-          rQ = qn;
-          freeb = {h, old_q};
-        }
-        if (k == 1) {
-          // after step 1 the free list is {the buffer T used, the one never used}
-          freeb = {MM0 + 2, MM0 + 3};
-        }
+    // Gram form ("DeepSpeed 集成 Muon 优化器实战" §核心算子): iterate on R = X X^T in fp16,
+    // accumulate Q, re-anchor (X <- Q X, R <- X X^T, Q <- I) every kGramReanchor steps.
+    // Four m x m buffers suffice: R, Q, H and one temporary (T or the new Q).
+    int xb = X0;      // buffer holding the current anchor X
+    int rR = MM0;     // R
+    int q = -1;       // Q, -1 = identity
+    std::vector<int> freeb = {MM0 + 1, MM0 + 2, MM0 + 3};
+    auto pop = [&]() {
+      const int b = freeb.front();
+      freeb.erase(freeb.begin());
+      return b;
+    };
+    auto push = [&](int b) { freeb.push_back(b); };
+    if (steps > 0) stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f});       // R = X X^T
+    for (int k = 1; k <= steps; ++k) {
+      const int h = pop();
+      stages.push_back({rR, rR, h, rR, false, false, false, kC, kB, kA});                        // H
+      bool h_is_q = false;
+      if (q < 0) {
+        q = h;                                                                                    // Q = H
+        h_is_q = true;
+      } else {
+        const int qn = pop();
+        stages.push_back({h, q, qn, -1, false, false, false, 1.f, 0.f, 0.f});                    // Q' = H Q
+        push(q);
+        q = qn;
       }
-      stages.push_back({rQ, X0, X1, -1, true, false, true, 1.f, 0.f, 0.f});                 // O = Q X
-      P.final_buf = X1;
+      if (k < steps) {
+        if (k % kGramReanchor == 0) {
+          const int xn = (xb == X0) ? X1 : X0;
+          stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f});                   // X = Q X
+          xb = xn;
+          stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f});                 // R = X X^T
+          push(q);  // H is Q here or already released below
+          if (!h_is_q) push(h);
+          q = -1;
+          continue;
+        }
+        const int t = pop();
+        stages.push_back({h, rR, t, -1, false, false, false, 1.f, 0.f, 0.f});                    // T = H R
+        stages.push_back({t, h, rR, -1, false, false, false, 1.f, 0.f, 0.f});                    // R = T H
+        push(t);
+      }
+      if (!h_is_q) push(h);
+    }
+    if (q >= 0) {
+      const int xn = (xb == X0) ? X1 : X0;
+      stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f});                       // O = Q X
+      P.final_buf = xn;
+    } else {
+      P.final_buf = xb;
     }
     P.final_fp16 = true;
   }
@@ -666,15 +682,15 @@ int muon_step(const void* packed_grads, float* packed_params, float* momentum, c
   float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
   float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
   int launches = 0;
-  cudaError_t e = launch_momentum_norm(packed_grads, momentum, ws + P->L.off_x[1], P->d_mats, n,
-                                       P->L.total_chunks, partials, mu, nesterov, 1, stream);
+  cudaError_t e = launch_momentum_norm(packed_grads, momentum, P->d_mats, n, P->L.total_chunks, partials, mu,
+                                       nesterov, 1, stream);
   if (e != cudaSuccess) return fail_cuda(e, "momentum/norm launch");
   ++launches;
   e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
   if (e != cudaSuccess) return fail_cuda(e, "norm launch");
   ++launches;
-  e = launch_to_class(ws + P->L.off_x[1], 1, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n,
-                      P->L.total_tiles, scales, stream);
+  e = launch_to_class(packed_grads, momentum, 1, nesterov, mu, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats,
+                      n, P->L.total_tiles, scales, stream);
   if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
   ++launches;
   rc = run_chain(*P, stream, &launches);
@@ -711,15 +727,15 @@ int muon_orthogonalize(const void* in_bf16, void* out_bf16, const int64_t* offse
   float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
   float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
   int launches = 0;
-  cudaError_t e = launch_momentum_norm(in_bf16, nullptr, nullptr, P->d_mats, n, P->L.total_chunks, partials, 0.f,
-                                       0, 0, stream);
+  cudaError_t e = launch_momentum_norm(in_bf16, nullptr, P->d_mats, n, P->L.total_chunks, partials, 0.f, 0, 0,
+                                       stream);
   if (e != cudaSuccess) return fail_cuda(e, "norm launch");
   ++launches;
   e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
   if (e != cudaSuccess) return fail_cuda(e, "norm launch");
   ++launches;
-  e = launch_to_class(in_bf16, 0, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n, P->L.total_tiles, scales,
-                      stream);
+  e = launch_to_class(in_bf16, nullptr, 0, 0, 0.f, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n,
+                      P->L.total_tiles, scales, stream);
   if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
   ++launches;
   rc = run_chain(*P, stream, &launches);

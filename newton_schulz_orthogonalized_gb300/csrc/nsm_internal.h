@@ -64,16 +64,18 @@ struct GemmLaunch {
 
 // ---- launchers (defined in the .cu files) ---------------------------------------
 
-cudaError_t launch_momentum_norm(const void* grads, float* momentum, void* u_base,
-                                 const MatInfo* mats, int nmats, int total_chunks,
-                                 float* partials, float mu, int nesterov, int has_momentum,
-                                 cudaStream_t stream);
+// M <- mu M + G (when has_momentum) and per-chunk sums of U^2, U = G + mu M (Nesterov),
+// M (plain) or G (no momentum)
+cudaError_t launch_momentum_norm(const void* grads, float* momentum, const MatInfo* mats, int nmats,
+                                 int total_chunks, float* partials, float mu, int nesterov,
+                                 int has_momentum, cudaStream_t stream);
 cudaError_t launch_norm_finalize(const MatInfo* mats, int nmats, const float* partials,
                                  float* scales, float eps, cudaStream_t stream);
-// natural (bf16) -> class layout, scaled by scales[i]; out fp16 when to_fp16
-cudaError_t launch_to_class(const void* src, int src_is_slot, void* dst, int to_fp16,
-                            const MatInfo* mats, int nmats, int64_t total_tiles,
-                            const float* scales, cudaStream_t stream);
+// X = s U, U recomputed in fp32 from G and the updated M, into the class layout, rounded
+// once to bf16 (or fp16 when to_fp16)
+cudaError_t launch_to_class(const void* grads, const float* momentum, int has_momentum, int nesterov,
+                            float mu, void* dst, int to_fp16, const MatInfo* mats, int nmats,
+                            int64_t total_tiles, const float* scales, cudaStream_t stream);
 // class layout O -> p update in natural layout
 cudaError_t launch_apply(const void* o, int o_fp16, float* params, const MatInfo* mats,
                          int nmats, int64_t total_tiles, float lr, float wd,
