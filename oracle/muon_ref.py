@@ -27,8 +27,9 @@ Readings taken where the pages are silent (each is listed again in the design no
 * gram form: iterate on ``R = X X^T`` and accumulate the left polynomial ``Q``
   (derivation in :func:`ns_gram`), re-anchoring ``R`` from the explicit iterate every
   two steps (exact-arithmetic no-op; keeps the fp16 iteration accurate).
-* storage precision: the pages fix bf16 for the standard form and fp16 for the gram
-  form; ``storage="method"`` rounds at exactly the points where the method stores.
+* storage precision: fp16 for both forms (the page calls the standard form stable in
+  bf16 and gives fp16 to the gram form for accuracy); "standard_bf16" keeps bf16;
+  ``storage="method"`` rounds at exactly the points where the method stores.
 * update scale ``sqrt(max(1, rows/cols))`` of the original (untransposed) matrix.
 * AdamW: the textbook decoupled form with bias correction, eps outside the square
   root, step counter starting at 1.
@@ -65,6 +66,8 @@ ADAM_EPS_DEFAULT = 1e-10
 
 # [DSM] §核心算子 — the two methods the dispatcher accepts.
 NS_METHODS = ("standard", "gram")
+# The standard form stored in bf16, the precision the page calls stable.
+NS_METHOD_VARIANTS = ("standard_bf16",)
 
 # Reading (pages silent): the epsilon added to the Frobenius norm.
 NORM_EPS = 1e-7
@@ -72,12 +75,15 @@ NORM_EPS = 1e-7
 
 # --- storage formats -------------------------------------------------------------------
 #
-# [DSM] §核心算子 fixes the precision the method stores its iterates in: the five-step
-# iteration runs in bf16 ("stable in bf16"), the gram variant in fp16 ("uses fp16 for
-# better half-precision accuracy").  With ``storage`` set, the routines below round every
-# intermediate the method stores to that format (round to nearest, ties to even) and
-# accumulate everything else in float64.  With ``storage=None`` they are the exact
-# float64 iteration.
+# [DSM] §核心算子 describes the precision the method stores its iterates in: the
+# five-step iteration is stable in bf16, and the gram variant uses fp16 for better
+# half-precision accuracy.  Reading taken: both forms store in fp16 (the normalised
+# iterate, X X^T and the quintic's matrices stay within fp16's range, and fp16 carries
+# three more significant bits at the same tensor-core rate); the bf16 form of the
+# standard iteration is kept as the method "standard_bf16".  With ``storage`` set, the
+# routines below round every intermediate the method stores to that format (round to
+# nearest, ties to even) and accumulate everything else in float64.  With
+# ``storage=None`` they are the exact float64 iteration.
 
 _FORMATS = {
     # significant bits, smallest normal exponent, largest finite value
@@ -111,8 +117,8 @@ def round_to(x, fmt):
 
 
 def method_storage(method):
-    """Storage format the pages give each ns_method: bf16 (standard), fp16 (gram)."""
-    return {"standard": "bf16", "gram": "fp16"}[method]
+    """Storage format of each ns_method: fp16 (standard, gram), bf16 (standard_bf16)."""
+    return {"standard": "fp16", "gram": "fp16", "standard_bf16": "bf16"}[method]
 
 
 def _store(x, storage):
@@ -284,7 +290,7 @@ def ns_gram(x: np.ndarray, steps: int = NS_STEPS, a: float = NS_A, b: float = NS
 def newton_schulz(x: np.ndarray, method: str = NS_METHOD_DEFAULT, steps: int = NS_STEPS,
                   a: float = NS_A, b: float = NS_B, c: float = NS_C, storage=None) -> np.ndarray:
     """Dispatch on ``ns_method`` ([DSM] §核心算子: ``NS_METHODS = {standard, gram}``)."""
-    if method == "standard":
+    if method in ("standard", "standard_bf16"):
         return ns_standard(x, steps, a, b, c, storage)
     if method == "gram":
         return ns_gram(x, steps, a, b, c, storage)
@@ -302,7 +308,7 @@ def orthogonalize(u: np.ndarray, method: str = NS_METHOD_DEFAULT, steps: int = N
     """Normalise, transpose when tall, run Newton-Schulz, transpose back.
 
     Returns ``O`` with the shape of ``u``.  ``storage="method"`` stores the iterates in
-    the format the pages give the method (bf16 standard, fp16 gram); ``None`` is exact.
+    the method's format (:func:`method_storage`); ``None`` is exact.
     """
     u = np.asarray(u, dtype=np.float64)
     if u.ndim != 2:

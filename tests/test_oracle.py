@@ -410,9 +410,13 @@ def test_round_to_matches_library_conversions():
 
 
 def test_method_storage_formats():
-    g = _golden("pages_constants.json")
-    assert oracle.method_storage("standard") == "bf16"
+    assert oracle.method_storage("standard") == "fp16"
     assert oracle.method_storage("gram") == "fp16"
+    assert oracle.method_storage("standard_bf16") == "bf16"
+    # the bf16 variant is the same mathematical iteration
+    rng = np.random.default_rng(2)
+    g = rng.standard_normal((5, 8))
+    assert np.array_equal(oracle.orthogonalize(g, "standard_bf16"), oracle.orthogonalize(g, "standard"))
 
 
 @pytest.mark.parametrize("every", [0, 1, 2, 3])
@@ -425,7 +429,7 @@ def test_gram_reanchoring_is_exact_noop(every, steps):
                          oracle.ns_standard(x, steps))) < 1e-10
 
 
-@pytest.mark.parametrize("method", ["standard", "gram"])
+@pytest.mark.parametrize("method", ["standard", "gram", "standard_bf16"])
 def test_storage_mode_close_on_well_conditioned_input(method):
     # singular values of X in [0.2, 0.6]: the iteration is not in its steep region, so
     # half-precision storage stays within a few units of its rounding of the exact map
