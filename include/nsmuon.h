@@ -53,8 +53,11 @@ typedef struct CUstream_st* nsm_stream_t;
 #define NSM_ERR_TIMEOUT   -8  /* a bounded in-kernel wait expired (nsm_device_status) */
 #define NSM_ERR_ARG       -9  /* any other invalid argument */
 
-#define NSM_NS_STANDARD 0     /* quintic Newton-Schulz on X, bf16 storage  [DSM §核心算子] */
-#define NSM_NS_GRAM     1     /* gram form on R = X X^T, fp16 storage       [DSM §核心算子] */
+/* Newton-Schulz methods [DSM §核心算子].  Every form accumulates in fp32 on the tensor
+ * cores; they differ in the half precision the iterates are stored in. */
+#define NSM_NS_STANDARD      0  /* quintic steps on X, fp16 storage */
+#define NSM_NS_GRAM          1  /* gram form on R = X X^T, fp16, re-anchored every 2 steps */
+#define NSM_NS_STANDARD_BF16 2  /* quintic steps on X, bf16 storage (the page's stable form) */
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int nsm_version(void);
@@ -87,7 +90,7 @@ size_t muon_workspace_bytes(const int32_t* shapes, int n, int ns_method, int ns_
  *     M <- mu*M + G;   U = G + mu*M (nesterov != 0) or U = M (nesterov == 0)
  *     X = U / (||U||_F + 1e-7), working on U^T when rows > cols
  *     X <- ns_steps quintic Newton-Schulz steps (a, b, c) = (3.4445, -4.7750, 2.0315)
- *          in the standard or gram form
+ *          in the standard or gram form (ns_method: NSM_NS_*)
  *     p <- p*(1 - lr*wd) - lr*sqrt(max(1, rows/cols))*O      (O transposed back)
  *   packed_grads  device, bf16 bits, read only
  *   packed_params device, fp32, updated in place (the owner's master copy)

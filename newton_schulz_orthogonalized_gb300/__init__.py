@@ -33,7 +33,7 @@ NSM_ERR_CUDA = -7
 NSM_ERR_TIMEOUT = -8
 NSM_ERR_ARG = -9
 
-NS_METHODS = {"standard": 0, "gram": 1}
+NS_METHODS = {"standard": 0, "gram": 1, "standard_bf16": 2}
 NS_METHOD_DEFAULT = "gram"
 NS_STEPS_DEFAULT = 5
 MUON_LR_DEFAULT = 0.02

@@ -96,8 +96,8 @@ int validate_shapes(const int32_t* shapes, int n) {
 }
 
 int validate_method(int method, int steps) {
-  if (method != NSM_NS_STANDARD && method != NSM_NS_GRAM)
-    return fail(NSM_ERR_METHOD, "unknown ns_method %d (0 = standard, 1 = gram)", method);
+  if (method != NSM_NS_STANDARD && method != NSM_NS_GRAM && method != NSM_NS_STANDARD_BF16)
+    return fail(NSM_ERR_METHOD, "unknown ns_method %d (0 = standard, 1 = gram, 2 = standard_bf16)", method);
   if (steps < 0 || steps > kMaxSteps) return fail(NSM_ERR_METHOD, "ns_steps = %d not in [0, %d]", steps, kMaxSteps);
   return NSM_OK;
 }
@@ -250,7 +250,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   P.L = make_layout(shapes, n, method, steps);
   const Layout& L = P.L;
   P.ws = static_cast<char*>(ws);
-  P.x_fp16 = method == NSM_NS_GRAM;
+  P.x_fp16 = method != NSM_NS_STANDARD_BF16;
   const int nclass = static_cast<int>(L.classes.size());
   const int nbuf = 2 + L.num_mm;
   auto buf_base = [&](int b, int c) -> char* {
@@ -261,7 +261,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
 
   // Launch list of the chain.
   std::vector<StageSpec> stages;
-  if (method == NSM_NS_STANDARD) {
+  if (method == NSM_NS_STANDARD || method == NSM_NS_STANDARD_BF16) {
     for (int k = 0; k < steps; ++k) {
       const int src = (k % 2 == 0) ? X0 : X1, dst = (k % 2 == 0) ? X1 : X0;
       stages.push_back({src, src, MM0, -1, false, true, false, 1.f, 0.f, 0.f});            // A = X X^T
@@ -269,7 +269,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       stages.push_back({MM0 + 1, src, dst, src, true, false, true, 1.f, kA, 0.f});         // X' = aX + BX
     }
     P.final_buf = (steps % 2 == 0) ? X0 : X1;
-    P.final_fp16 = false;
+    P.final_fp16 = P.x_fp16;
   } else {
     // Gram form ("DeepSpeed 集成 Muon 优化器实战" §核心算子): iterate on R = X X^T in fp16,
     // accumulate Q, re-anchor (X <- Q X, R <- X X^T, Q <- I) every kGramReanchor steps.

@@ -109,7 +109,8 @@ def test_step_validation_errors_without_gpu(nsm):
     assert _call_step(nsm, shapes, grads=0) == nsm.NSM_ERR_NULL
     assert _call_step(nsm, [(128, 0)], offsets=[0]) == nsm.NSM_ERR_SHAPE
     assert _call_step(nsm, shapes, n=0) == nsm.NSM_ERR_SHAPE
-    assert _call_step(nsm, shapes, method=2) == nsm.NSM_ERR_METHOD
+    assert _call_step(nsm, shapes, method=3) == nsm.NSM_ERR_METHOD
+    assert _call_step(nsm, shapes, method=2) == nsm.NSM_ERR_WORKSPACE  # standard_bf16 is valid
     assert _call_step(nsm, shapes, steps=-1) == nsm.NSM_ERR_METHOD
     # overlapping matrices
     assert _call_step(nsm, shapes, offsets=[0, 64]) == nsm.NSM_ERR_OFFSET

@@ -75,7 +75,7 @@ class Step:
         o = int(self.offsets[i])
         return arr[o:o + r * c].reshape(r, c)
 
-    def check(self, indices=None):
+    def check(self, indices=None, tol_delta=TOL_DELTA):
         wl = self.wl
         idx = range(len(wl.muon_shapes)) if indices is None else indices
         worst = {"delta": 0.0, "mom": 0.0}
@@ -90,7 +90,7 @@ class Step:
             worst["mom"] = max(worst["mom"], e_m)
             worst["delta"] = max(worst["delta"], e_d)
             assert e_m <= TOL_FP32, (i, e_m)
-            assert e_d <= TOL_DELTA, (i, wl.muon_shapes[i], e_d)
+            assert e_d <= tol_delta, (i, wl.muon_shapes[i], e_d)
         return worst
 
 
@@ -166,19 +166,41 @@ def test_orthogonalize_well_conditioned_vs_exact(nsm, method):
         assert rel(o[sl].reshape(r, c), ref) <= TOL_NS
 
 
-def test_gram_close_to_exact_on_workload(nsm):
-    # the re-anchored fp16 gram form stays within 2.5e-2 of the exact iteration even on
-    # the near-low-rank inputs (the standard bf16 form does not: its own rounding is
-    # amplified in the small singular directions)
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_fp16_forms_close_to_exact_on_workload(nsm, method):
+    # both fp16 forms stay within 3e-2 of the exact float64 iteration even on the
+    # near-low-rank inputs (measured ~1.9% gram, ~2.3% standard: the floor set by
+    # rounding the normalised input to 11 significant bits); the bf16 form is ~18% away
     wl = synth.workload("layer1024")
-    offsets, g, o = orthogonalize_gpu(nsm, wl, "gram")
+    offsets, g, o = orthogonalize_gpu(nsm, wl, method)
     for i, (r, c) in enumerate(wl.muon_shapes):
         off = int(offsets[i])
-        ref = oracle.orthogonalize(g[off:off + r * c].reshape(r, c), "gram")
-        assert rel(o[off:off + r * c].reshape(r, c), ref) <= 2.5e-2
+        ref = oracle.orthogonalize(g[off:off + r * c].reshape(r, c), method)
+        assert rel(o[off:off + r * c].reshape(r, c), ref) <= 3e-2
 
 
 # ------------------------------------------------------------------ full step
+
+# The bf16 form of the standard iteration: two correct bf16 implementations that round at
+# the same points but accumulate differently differ by up to ~1.5% on near-low-rank
+# inputs (the iteration amplifies small singular directions ~487x), so its step delta is
+# held at the same 2e-2 as its output; the fp16 forms meet 1e-2.
+TOL_DELTA_BF16 = 2e-2
+
+
+@pytest.mark.parametrize("wl_name", ["tiny", "layer1024"])
+def test_step_standard_bf16(nsm, wl_name):
+    Step(nsm, synth.workload(wl_name), "standard_bf16").check(tol_delta=TOL_DELTA_BF16)
+
+
+def test_orthogonalize_standard_bf16(nsm):
+    wl = synth.custom(RAGGED + [(1024, 1024), (768, 3072)], seed=4)
+    offsets, g, o = orthogonalize_gpu(nsm, wl, "standard_bf16")
+    for i, (r, c) in enumerate(wl.muon_shapes):
+        off = int(offsets[i])
+        ref = oracle.orthogonalize(g[off:off + r * c].reshape(r, c), "standard_bf16", storage="method")
+        assert rel(o[off:off + r * c].reshape(r, c), ref) <= TOL_NS, ((r, c))
+
 
 @pytest.mark.parametrize("method", ["standard", "gram"])
 def test_step_tiny(nsm, method):
