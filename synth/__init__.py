@@ -14,7 +14,8 @@ Workloads (transformer-shaped gradient sets; no datasets or trained weights):
 * ``gpt2small`` — 12 layers of hidden 768: 2304x768 qkv, 768x768 proj, 3072x768 fc,
                   768x3072 out; AdamW on the embeddings, lm_head, norms and biases.
 * ``llama7b``   — 32 layers of hidden 4096: q/o 4096x4096, k/v 1024x4096 (GQA),
-                  gate/up 11008x4096, down 4096x11008.
+                  gate/up 11008x4096, down 4096x11008.  ``llama7b_layer`` is its first
+                  layer alone (for profiler captures).
 * ``split_moe`` — 16 layers, each with 32 per-head 128x4096 query blocks (Muon Split:
                   every head block is its own table entry) and 64 experts with gate/up
                   1408x2048 and down 2048x1408.
@@ -114,6 +115,13 @@ def _llama7b() -> Workload:
     return Workload("llama7b", 3, names, shapes, lr=1e-4)
 
 
+def _llama7b_layer() -> Workload:
+    """One layer of the Llama-7B-shaped set (7 matrices, 177M elements): small enough
+    for profiler captures, with operands larger than L2."""
+    full = _llama7b()
+    return Workload("llama7b_layer", 3, full.muon_names[:7], full.muon_shapes[:7], lr=1e-4)
+
+
 def _split_moe() -> Workload:
     names, shapes = [], []
     for l in range(16):
@@ -133,6 +141,7 @@ WORKLOADS = {
     "layer1024": _layer1024,
     "gpt2small": _gpt2small,
     "llama7b": _llama7b,
+    "llama7b_layer": _llama7b_layer,
     "split_moe": _split_moe,
 }
 
