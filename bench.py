@@ -301,7 +301,12 @@ def run_ours(args):
         torch.cuda.synchronize()
     nsm.timing_enable(False)
     ms = t0.elapsed_time(t1) / args.steps
-    gemm_ms, gemm_launches, gemm_flops = nsm.timing_read()
+    gemm_ms, gemm_launches, gemm_flops = nsm.timing_read(nsm.KIND_GEMM)
+    per_kind = {}
+    for kind, kname in nsm.KIND_NAMES.items():
+        k_ms, k_n, k_work = nsm.timing_read(kind)
+        if k_n:
+            per_kind[kname] = (k_ms, k_n, k_work)
     if nsm.device_status() != nsm.NSM_OK:
         raise RuntimeError("a bounded device wait expired in the timed region")
     if dist is not None:
@@ -380,6 +385,17 @@ def run_ours(args):
             "launches_timed": gemm_launches,
             "flops_per_launch": per_launch_flops,
             "ms_per_launch": per_launch_ms,
+        },
+        "kernels": {
+            kname: {
+                "launches": k_n,
+                "ms_per_step": k_ms / args.steps,
+                "achieved": (k_work / (k_ms * 1e-3) / (1e12 if kname == "k_ns_gemm" else 1e9)) if k_ms > 0 else None,
+                "unit": "TFLOP/s" if kname == "k_ns_gemm" else "GB/s",
+                "frac": ((k_work / (k_ms * 1e-3) / 1e12) / peak if kname == "k_ns_gemm"
+                         else (k_work / (k_ms * 1e-3) / 1e9) / peaks["hbm_gbs"]) if k_ms > 0 else None,
+            }
+            for kname, (k_ms, k_n, k_work) in per_kind.items()
         },
         "gpu_launches": launches,
         "clocks": clocks,

@@ -149,13 +149,22 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
  * NSM_ERR_CUDA if the synchronisation itself reports an error. */
 int nsm_device_status(nsm_stream_t stream, int* status_out);
 
-/* Kernel timing for profiling.  While enabled, every Newton-Schulz GEMM launch of
- * muon_step / muon_orthogonalize is bracketed by CUDA events on the caller's stream.
- * nsm_timing_read synchronises the recorded events and returns, summed since the last
- * reset: *gemm_ms (device time of those launches), *gemm_launches, *gemm_flops
- * (canonical flops they performed).  Any output pointer may be NULL. */
+/* Kernel timing for profiling.  While enabled, every kernel launch of muon_step,
+ * muon_orthogonalize, adamw_step and nsm_gemm is bracketed by CUDA events on the
+ * caller's stream.  nsm_timing_read_kind synchronises the recorded events and returns,
+ * summed since the last reset for one kind of kernel: *ms (device time), *launches and
+ * *work (the algorithmic work of those launches: flops for NSM_KIND_GEMM, bytes that
+ * must cross HBM for the other kinds).  nsm_timing_read is the GEMM kind.  Any output
+ * pointer may be NULL.  Not for use inside stream capture. */
+#define NSM_KIND_GEMM     0  /* Newton-Schulz GEMM stages (tensor cores) */
+#define NSM_KIND_MOMENTUM 1  /* momentum update + chunk sums of U^2 */
+#define NSM_KIND_NORM     2  /* per-matrix norm from the chunk sums */
+#define NSM_KIND_LAYOUT   3  /* X = s U into the working layout */
+#define NSM_KIND_APPLY    4  /* decay + apply (or the export of O) */
+#define NSM_KIND_ADAMW    5  /* AdamW */
 int nsm_timing_enable(int enable);
 int nsm_timing_read(double* gemm_ms, int64_t* gemm_launches, double* gemm_flops);
+int nsm_timing_read_kind(int kind, double* ms, int64_t* launches, double* work);
 int nsm_timing_reset(void);
 
 /* Number of kernel launches the last successful muon_step / muon_orthogonalize /

@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
     L.nsm_timing_enable.argtypes = [ctypes.c_int]
     L.nsm_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p,
                                   ctypes.POINTER(ctypes.c_double)]
+    L.nsm_timing_read_kind.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double), _c_i64p,
+                                       ctypes.POINTER(ctypes.c_double)]
     _lib = L
     return L
 
@@ -242,12 +244,18 @@ def timing_reset() -> None:
     lib().nsm_timing_reset()
 
 
-def timing_read() -> Tuple[float, int, float]:
+KIND_GEMM, KIND_MOMENTUM, KIND_NORM, KIND_LAYOUT, KIND_APPLY, KIND_ADAMW = range(6)
+KIND_NAMES = {KIND_GEMM: "k_ns_gemm", KIND_MOMENTUM: "k_momentum_norm", KIND_NORM: "k_norm_finalize",
+              KIND_LAYOUT: "k_to_class", KIND_APPLY: "k_from_class", KIND_ADAMW: "k_adamw"}
+
+
+def timing_read(kind: int = KIND_GEMM) -> Tuple[float, int, float]:
+    """(device ms, launches, algorithmic work) of one kernel kind since the last reset."""
     ms = ctypes.c_double(0)
     n = ctypes.c_int64(0)
-    fl = ctypes.c_double(0)
-    lib().nsm_timing_read(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl))
-    return ms.value, n.value, fl.value
+    w = ctypes.c_double(0)
+    _check(lib().nsm_timing_read_kind(int(kind), ctypes.byref(ms), ctypes.byref(n), ctypes.byref(w)))
+    return ms.value, n.value, w.value
 
 
 # ---------------------------------------------------------------- optimizer wrapper

@@ -229,6 +229,7 @@ struct Plan {
   void* dmeta = nullptr;
   MatInfo* d_mats = nullptr;
   std::vector<GemmLaunch> launches;
+  int64_t elems = 0;      // elements of the table (sum of rows x cols)
   int final_buf = X0;     // buffer holding O after the chain
   bool final_fp16 = false;
   bool x_fp16 = false;
@@ -249,6 +250,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
                void* ws, size_t ws_bytes) {
   P.L = make_layout(shapes, n, method, steps);
   const Layout& L = P.L;
+  for (int i = 0; i < n; ++i) P.elems += int64_t(shapes[2 * i]) * shapes[2 * i + 1];
   P.ws = static_cast<char*>(ws);
   P.x_fp16 = method != NSM_NS_STANDARD_BF16;
   const int nclass = static_cast<int>(L.classes.size());
@@ -497,17 +499,21 @@ Plan* get_plan(const int32_t* shapes, const int64_t* offsets, int n, int method,
 
 // ---------------------------------------------------------------- timing
 
+// Kernel kinds the timing hooks distinguish (NSM_KIND_* in the header).
+constexpr int kKinds = 6;
+
 struct Timing {
   std::mutex mu;
   bool enabled = false;
   struct Rec {
     cudaEvent_t a, b;
-    double flops;
+    int kind;
+    double work;
   };
   std::vector<Rec> pending;
   std::vector<cudaEvent_t> pool;
-  double ms = 0, flops = 0;
-  int64_t launches = 0;
+  double ms[kKinds] = {0}, work[kKinds] = {0};
+  int64_t launches[kKinds] = {0};
   cudaEvent_t get() {
     if (!pool.empty()) {
       cudaEvent_t e = pool.back();
@@ -523,9 +529,9 @@ struct Timing {
       cudaEventSynchronize(r.b);
       float t = 0.f;
       cudaEventElapsedTime(&t, r.a, r.b);
-      ms += t;
-      flops += r.flops;
-      launches += 1;
+      ms[r.kind] += t;
+      work[r.kind] += r.work;
+      launches[r.kind] += 1;
       pool.push_back(r.a);
       pool.push_back(r.b);
     }
@@ -537,6 +543,32 @@ Timing& timing() {
   static Timing* t = new Timing();
   return *t;
 }
+
+// Brackets one launch with events on `stream` while timing is enabled.
+class TimedLaunch {
+ public:
+  TimedLaunch(cudaStream_t stream, int kind, double work) : stream_(stream), kind_(kind), work_(work) {
+    Timing& T = timing();
+    std::lock_guard<std::mutex> lock(T.mu);
+    if (!T.enabled) return;
+    a_ = T.get();
+    b_ = T.get();
+    cudaEventRecord(a_, stream_);
+  }
+  ~TimedLaunch() {
+    if (!a_) return;
+    Timing& T = timing();
+    std::lock_guard<std::mutex> lock(T.mu);
+    cudaEventRecord(b_, stream_);
+    T.pending.push_back({a_, b_, kind_, work_});
+  }
+
+ private:
+  cudaStream_t stream_;
+  int kind_;
+  double work_;
+  cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
 
 // ---------------------------------------------------------------- validation helpers
 
@@ -580,28 +612,11 @@ int run_chain(Plan& P, cudaStream_t stream, int* launches) {
   int num_sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, P.device);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
-  Timing& T = timing();
-  bool timed;
-  {
-    std::lock_guard<std::mutex> lock(T.mu);
-    timed = T.enabled;
-  }
   for (const GemmLaunch& l : P.launches) {
-    cudaEvent_t a = nullptr, b = nullptr;
-    if (timed) {
-      std::lock_guard<std::mutex> lock(T.mu);
-      a = T.get();
-      b = T.get();
-      cudaEventRecord(a, stream);
-    }
+    TimedLaunch t(stream, NSM_KIND_GEMM, l.flops);
     e = launch_gemm(l, num_sms, stream);
     if (e != cudaSuccess) return fail_cuda(e, "Newton-Schulz GEMM launch");
     ++*launches;
-    if (timed) {
-      std::lock_guard<std::mutex> lock(T.mu);
-      cudaEventRecord(b, stream);
-      T.pending.push_back({a, b, l.flops});
-    }
   }
   return NSM_OK;
 }
@@ -682,21 +697,35 @@ int muon_step(const void* packed_grads, float* packed_params, float* momentum, c
   float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
   float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
   int launches = 0;
-  cudaError_t e = launch_momentum_norm(packed_grads, momentum, P->d_mats, n, P->L.total_chunks, partials, mu,
-                                       nesterov, 1, stream);
+  const double elems = double(P->elems);
+  cudaError_t e;
+  {
+    TimedLaunch t(stream, NSM_KIND_MOMENTUM, 10.0 * elems);
+    e = launch_momentum_norm(packed_grads, momentum, P->d_mats, n, P->L.total_chunks, partials, mu, nesterov, 1,
+                             stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "momentum/norm launch");
   ++launches;
-  e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
+  {
+    TimedLaunch t(stream, NSM_KIND_NORM, 4.0 * (P->L.total_chunks + n));
+    e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "norm launch");
   ++launches;
-  e = launch_to_class(packed_grads, momentum, 1, nesterov, mu, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats,
-                      n, P->L.total_tiles, scales, stream);
+  {
+    TimedLaunch t(stream, NSM_KIND_LAYOUT, 8.0 * elems);
+    e = launch_to_class(packed_grads, momentum, 1, nesterov, mu, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats,
+                        n, P->L.total_tiles, scales, stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
   ++launches;
   rc = run_chain(*P, stream, &launches);
   if (rc != NSM_OK) return rc;
-  e = launch_apply(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, packed_params, P->d_mats, n,
-                   P->L.total_tiles, lr, wd, stream);
+  {
+    TimedLaunch t(stream, NSM_KIND_APPLY, 10.0 * elems);
+    e = launch_apply(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, packed_params, P->d_mats, n,
+                     P->L.total_tiles, lr, wd, stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "apply launch");
   ++launches;
   t_last_launches = launches;
@@ -727,21 +756,34 @@ int muon_orthogonalize(const void* in_bf16, void* out_bf16, const int64_t* offse
   float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
   float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
   int launches = 0;
-  cudaError_t e = launch_momentum_norm(in_bf16, nullptr, P->d_mats, n, P->L.total_chunks, partials, 0.f, 0, 0,
-                                       stream);
+  const double elems = double(P->elems);
+  cudaError_t e;
+  {
+    TimedLaunch t(stream, NSM_KIND_MOMENTUM, 2.0 * elems);
+    e = launch_momentum_norm(in_bf16, nullptr, P->d_mats, n, P->L.total_chunks, partials, 0.f, 0, 0, stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "norm launch");
   ++launches;
-  e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
+  {
+    TimedLaunch t(stream, NSM_KIND_NORM, 4.0 * (P->L.total_chunks + n));
+    e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "norm launch");
   ++launches;
-  e = launch_to_class(in_bf16, nullptr, 0, 0, 0.f, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n,
-                      P->L.total_tiles, scales, stream);
+  {
+    TimedLaunch t(stream, NSM_KIND_LAYOUT, 4.0 * elems);
+    e = launch_to_class(in_bf16, nullptr, 0, 0, 0.f, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n,
+                        P->L.total_tiles, scales, stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
   ++launches;
   rc = run_chain(*P, stream, &launches);
   if (rc != NSM_OK) return rc;
-  e = launch_export(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, out_bf16, P->d_mats, n, P->L.total_tiles,
-                    stream);
+  {
+    TimedLaunch t(stream, NSM_KIND_APPLY, 4.0 * elems);
+    e = launch_export(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, out_bf16, P->d_mats, n,
+                      P->L.total_tiles, stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "export launch");
   ++launches;
   t_last_launches = launches;
@@ -770,8 +812,12 @@ int adamw_step(const void* grads, float* params, float* exp_avg, float* exp_avg_
     return fail(NSM_ERR_ARG, "AdamW buffers must not overlap");
   const double bc1 = 1.0 - std::pow(double(beta1), double(step));
   const double bc2 = 1.0 - std::pow(double(beta2), double(step));
-  cudaError_t e = launch_adamw(grads, params, exp_avg, exp_avg_sq, numel, lr, beta1, beta2, eps, wd,
-                               static_cast<float>(bc1), static_cast<float>(bc2), stream);
+  cudaError_t e;
+  {
+    TimedLaunch t(stream, NSM_KIND_ADAMW, 26.0 * double(numel));
+    e = launch_adamw(grads, params, exp_avg, exp_avg_sq, numel, lr, beta1, beta2, eps, wd, static_cast<float>(bc1),
+                     static_cast<float>(bc2), stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "AdamW launch");
   t_last_launches = 1;
   return NSM_OK;
@@ -841,7 +887,10 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return fail_cuda(e, "device query");
-  e = launch_gemm(l, num_sms, stream);
+  {
+    TimedLaunch t(stream, NSM_KIND_GEMM, l.flops);
+    e = launch_gemm(l, num_sms, stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "GEMM launch");
   t_last_launches = 1;
   return NSM_OK;
@@ -872,12 +921,17 @@ int nsm_timing_enable(int enable) {
 }
 
 int nsm_timing_read(double* gemm_ms, int64_t* gemm_launches, double* gemm_flops) {
+  return nsm_timing_read_kind(NSM_KIND_GEMM, gemm_ms, gemm_launches, gemm_flops);
+}
+
+int nsm_timing_read_kind(int kind, double* ms, int64_t* launches, double* work) {
+  if (kind < 0 || kind >= kKinds) return fail(NSM_ERR_ARG, "unknown timing kind %d", kind);
   Timing& T = timing();
   std::lock_guard<std::mutex> lock(T.mu);
   T.collect();
-  if (gemm_ms) *gemm_ms = T.ms;
-  if (gemm_launches) *gemm_launches = T.launches;
-  if (gemm_flops) *gemm_flops = T.flops;
+  if (ms) *ms = T.ms[kind];
+  if (launches) *launches = T.launches[kind];
+  if (work) *work = T.work[kind];
   return NSM_OK;
 }
 
@@ -885,9 +939,11 @@ int nsm_timing_reset(void) {
   Timing& T = timing();
   std::lock_guard<std::mutex> lock(T.mu);
   T.collect();
-  T.ms = 0;
-  T.flops = 0;
-  T.launches = 0;
+  for (int k = 0; k < kKinds; ++k) {
+    T.ms[k] = 0;
+    T.work[k] = 0;
+    T.launches[k] = 0;
+  }
   return NSM_OK;
 }
 
