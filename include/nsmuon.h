@@ -117,6 +117,28 @@ int muon_orthogonalize(const void* in_bf16, void* out_bf16,
                        int ns_method, int ns_steps,
                        void* workspace, size_t workspace_bytes, nsm_stream_t stream);
 
+/* Orthogonalisation that allocates no device memory, for callers that cannot call
+ * cudaMalloc: code recording a CUDA graph under a capture mode that forbids allocation,
+ * a host framework whose own pool owns every byte of device memory, or a latency-bound
+ * loop that cannot afford the device synchronisation an allocation may imply.  It
+ * computes what muon_orthogonalize computes, with the same kernels, but keeps its
+ * workspace and its launch plan in a 64 MiB array of device memory that is part of the
+ * library itself (a file-scope __device__ array: every GPU that loads the library holds
+ * it until the process exits).  The pages have no counterpart; this is a convenience of
+ * the library.
+ *   - Tables whose workspace and plan do not fit in the 64 MiB are rejected with
+ *     NSM_ERR_WORKSPACE and nothing is launched (about 8M elements of square matrices
+ *     fit; use muon_orthogonalize with a caller workspace for more).
+ *   - Every call shares the array and leaves its contents behind; each call rewrites
+ *     what it reads, so nothing needs to start at zero.  Calls that overlap on the GPU
+ *     (two streams, or two host threads) race on it: order them on one stream.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call outside stream capture.
+ * Arguments are those of muon_orthogonalize without the workspace. */
+int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16,
+                               const int64_t* offsets, const int32_t* shapes, int n,
+                               int ns_method, int ns_steps, nsm_stream_t stream);
+
 /* Fused AdamW step on one flat group ([DSM] §混合优化器的参数组构造: parameters without
  * use_muon go to AdamW; decoupled decay is the default mode):
  *     m <- b1*m + (1-b1)*g;  v <- b2*v + (1-b2)*g^2

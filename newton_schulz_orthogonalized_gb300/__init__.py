@@ -80,6 +80,9 @@ def lib() -> ctypes.CDLL:
     L.muon_orthogonalize.argtypes = [_vp, _vp, _c_i64p, _c_i32p, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, _vp, ctypes.c_size_t, _vp]
     L.muon_orthogonalize.restype = ctypes.c_int
+    L.muon_orthogonalize_noalloc.argtypes = [_vp, _vp, _c_i64p, _c_i32p, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, _vp]
+    L.muon_orthogonalize_noalloc.restype = ctypes.c_int
     L.adamw_step.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
                              ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_int, _vp]
     L.adamw_step.restype = ctypes.c_int
@@ -198,6 +201,18 @@ def muon_orthogonalize(inp, out, offsets, shapes, ns_method=NS_METHOD_DEFAULT,
     _check(lib().muon_orthogonalize(_ptr(inp), _ptr(out), _i64p(o), _i32p(s), s.shape[0],
                                     method_code(ns_method), int(ns_steps), _ptr(workspace),
                                     ws_size, _stream_ptr(stream)))
+
+
+def muon_orthogonalize_noalloc(inp, out, offsets, shapes, ns_method=NS_METHOD_DEFAULT,
+                               ns_steps: int = NS_STEPS_DEFAULT, stream=None) -> None:
+    """muon_orthogonalize without a workspace: for callers that cannot allocate device
+    memory.  Uses 64 MiB of device memory the library itself owns; tables that do not fit
+    raise NsmError(NSM_ERR_WORKSPACE).  Overlapping calls on different streams race."""
+    s = _shapes_array(shapes)
+    o = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+    _check(lib().muon_orthogonalize_noalloc(_ptr(inp), _ptr(out), _i64p(o), _i32p(s), s.shape[0],
+                                            method_code(ns_method), int(ns_steps),
+                                            _stream_ptr(stream)))
 
 
 def adamw_step(grads, params, exp_avg, exp_avg_sq, lr: float = ADAM_LR_DEFAULT,

@@ -233,9 +233,17 @@ struct Plan {
   int final_buf = X0;     // buffer holding O after the chain
   bool final_fp16 = false;
   bool x_fp16 = false;
+  bool owns_meta = true;  // false when the metadata lives in memory the plan does not own
   ~Plan() {
-    if (dmeta) cudaFree(dmeta);
+    if (dmeta && owns_meta) cudaFree(dmeta);
   }
+};
+
+// Device memory a caller provides for a plan's metadata instead of a fresh allocation.
+struct MetaSink {
+  char* dptr;
+  size_t capacity;
+  cudaStream_t stream;
 };
 
 struct StageSpec {
@@ -247,7 +255,7 @@ struct StageSpec {
 };
 
 int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, int method, int steps,
-               void* ws, size_t ws_bytes) {
+               void* ws, size_t ws_bytes, const MetaSink* sink = nullptr) {
   P.L = make_layout(shapes, n, method, steps);
   const Layout& L = P.L;
   for (int i = 0; i < n; ++i) P.elems += int64_t(shapes[2 * i]) * shapes[2 * i + 1];
@@ -357,8 +365,16 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     hm[i] = mi;
   }
 
-  cudaError_t e = cudaMalloc(&P.dmeta, total);
-  if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(plan metadata)");
+  cudaError_t e = cudaSuccess;
+  if (sink) {
+    if (total > sink->capacity)
+      return fail(NSM_ERR_WORKSPACE, "plan metadata needs %zu bytes, %zu available", total, sink->capacity);
+    P.dmeta = sink->dptr;
+    P.owns_meta = false;
+  } else {
+    e = cudaMalloc(&P.dmeta, total);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(plan metadata)");
+  }
   char* dbase = static_cast<char*>(P.dmeta);
   P.d_mats = reinterpret_cast<MatInfo*>(dbase);
 
@@ -434,8 +450,13 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     P.launches.push_back(l);
   }
 
-  e = cudaMemcpy(P.dmeta, host.data(), total, cudaMemcpyHostToDevice);
-  if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpy(plan metadata)");
+  if (sink) {
+    // pageable source: the copy is staged before cudaMemcpyAsync returns
+    e = cudaMemcpyAsync(P.dmeta, host.data(), total, cudaMemcpyHostToDevice, sink->stream);
+  } else {
+    e = cudaMemcpy(P.dmeta, host.data(), total, cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "copy plan metadata");
   (void)ws_bytes;
   return NSM_OK;
 }
@@ -619,6 +640,35 @@ int run_chain(Plan& P, cudaStream_t stream, int* launches) {
     ++*launches;
   }
   return NSM_OK;
+}
+
+// ---------------------------------------------------------------- allocation-free path
+
+// Device memory of the allocation-free orthogonalisation: its workspace and its launch
+// plan.  It is part of the library's module, so every GPU that loads the library holds
+// it until the process exits; no call ever allocates it.
+constexpr size_t kNoAllocBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device.
+char* noalloc_scratch(int device, int* rc) {
+  static std::mutex mu;
+  static char* ptr[64] = {nullptr};
+  if (device < 0 || device >= 64) {
+    *rc = fail(NSM_ERR_CUDA, "device ordinal %d out of range", device);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[device]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      *rc = fail_cuda(e, "cudaGetSymbolAddress(allocation-free scratch)");
+      return nullptr;
+    }
+    ptr[device] = static_cast<char*>(p);
+  }
+  return ptr[device];
 }
 
 }  // namespace
@@ -893,6 +943,63 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   }
   if (e != cudaSuccess) return fail_cuda(e, "GEMM launch");
   t_last_launches = 1;
+  return NSM_OK;
+}
+
+int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16, const int64_t* offsets, const int32_t* shapes,
+                               int n, int ns_method, int ns_steps, nsm_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!in_bf16 || !out_bf16) return fail(NSM_ERR_NULL, "a device buffer is NULL");
+  int rc = validate_shapes(shapes, n);
+  if (rc != NSM_OK) return rc;
+  rc = validate_method(ns_method, ns_steps);
+  if (rc != NSM_OK) return rc;
+  int64_t extent = 0;
+  rc = validate_offsets(offsets, shapes, n, &extent);
+  if (rc != NSM_OK) return rc;
+  if (!aligned(in_bf16, 16) || !aligned(out_bf16, 16)) return fail(NSM_ERR_ALIGN, "device buffers must be 16-byte aligned");
+  if (ranges_overlap(in_bf16, size_t(extent) * 2, out_bf16, size_t(extent) * 2))
+    return fail(NSM_ERR_ARG, "input and output must not overlap");
+  const size_t ws_bytes = make_layout(shapes, n, ns_method, ns_steps).bytes;
+  if (ws_bytes >= kNoAllocBytes)
+    return fail(NSM_ERR_WORKSPACE,
+                "the allocation-free path holds %zu bytes; this table needs %zu bytes of workspace (use "
+                "muon_orthogonalize with a caller workspace)",
+                kNoAllocBytes, ws_bytes);
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  char* scratch = noalloc_scratch(device, &rc);
+  if (!scratch) return rc;
+
+  // workspace at the start of the array, the plan's metadata after it
+  Plan P;
+  P.device = device;
+  const size_t meta_off = align_up(ws_bytes, kAlign);
+  MetaSink sink{scratch + meta_off, kNoAllocBytes - meta_off, stream};
+  rc = build_plan(P, shapes, offsets, n, ns_method, ns_steps, scratch, ws_bytes, &sink);
+  if (rc != NSM_OK) return rc;
+  char* ws = P.ws;
+  float* partials = reinterpret_cast<float*>(ws + P.L.off_partials);
+  float* scales = reinterpret_cast<float*>(ws + P.L.off_scales);
+  int launches = 0;
+  e = launch_momentum_norm(in_bf16, nullptr, P.d_mats, n, P.L.total_chunks, partials, 0.f, 0, 0, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
+  ++launches;
+  e = launch_norm_finalize(P.d_mats, n, partials, scales, kNormEps, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
+  ++launches;
+  e = launch_to_class(in_bf16, nullptr, 0, 0, 0.f, ws + P.L.off_x[0], P.x_fp16 ? 1 : 0, P.d_mats, n, P.L.total_tiles,
+                      scales, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
+  ++launches;
+  rc = run_chain(P, stream, &launches);
+  if (rc != NSM_OK) return rc;
+  e = launch_export(ws + P.L.off_x[P.final_buf], P.final_fp16 ? 1 : 0, out_bf16, P.d_mats, n, P.L.total_tiles,
+                    stream);
+  if (e != cudaSuccess) return fail_cuda(e, "export launch");
+  ++launches;
+  t_last_launches = launches;
   return NSM_OK;
 }
 
