@@ -62,7 +62,9 @@ struct Ctrl {
   int never;  // stays 0: the flag the teardown waits poll, so they ignore `abort`
 };
 
-constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl);
+constexpr int EPI_WARPS = 4;
+constexpr int XPOSE_BYTES = EPI_WARPS * 32 * 33 * 4;  // per-warp 32x32 fp32 transpose tiles
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + XPOSE_BYTES + sizeof(Ctrl);
 
 struct TileCoord {
   int g, b, m0, n0;
@@ -77,11 +79,18 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmGroup* __restrict__ g
   }
   const GemmGroup& G = groups[lo];
   const int64_t local = t - G.tile_begin;
-  const int per = G.tiles_m * G.tiles_n;
+  const int per = G.sym ? G.tiles_per_mat : G.tiles_m * G.tiles_n;
   const int b = static_cast<int>(local / per);
   const int rem = static_cast<int>(local - static_cast<int64_t>(b) * per);
-  const int mt = rem / G.tiles_n;
-  const int nt = rem - mt * G.tiles_n;
+  int mt, nt;
+  if (G.sym) {
+    const int packed = __ldg(G.tile_list + rem);
+    mt = packed >> 16;
+    nt = packed & 0xffff;
+  } else {
+    mt = rem / G.tiles_n;
+    nt = rem - mt * G.tiles_n;
+  }
   return {lo, b, mt * BM, nt * BN};
 }
 
@@ -114,7 +123,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + size_t(STAGES) * STAGE_BYTES);
+  float* xpose = reinterpret_cast<float*>(smem + size_t(STAGES) * STAGE_BYTES);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + size_t(STAGES) * STAGE_BYTES + XPOSE_BYTES);
   const uint32_t ring = ptx::smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -296,53 +306,92 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
         ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
         ptx::tmem_ld_wait();
-        if (row_ok) {
         const int col0 = c * 32;
+        const int gc0 = tc.n0 + col0;  // first column of this chunk in the matrix
+        const bool full = col0 + 32 <= n_len;
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
-        const bool full = col0 + 32 <= n_len;
-        if (HAS_AUX) {
-          if (full) {
-            const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
+        if (row_ok) {
+          if (HAS_AUX) {
+            if (full) {
+              const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                uint4 pk = __ldg(src + w);
+                const T* e = reinterpret_cast<const T*>(&pk);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[w * 8 + j] += beta * E::to_f(e[j]);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (col0 + j < n_len) v[j] += beta * E::to_f(aux_row[col0 + j]);
+              }
+            }
+          }
+          if (diag != 0.0f) {
+            const int d = row - gc0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (d == j) v[j] += diag;
+            }
+          }
+          // a symmetric output stores only its upper triangle (column >= row) directly
+          const int first_col = G.sym ? row : 0;
+          if (full && gc0 >= first_col) {
+            uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-              uint4 pk = __ldg(src + w);
-              const T* e = reinterpret_cast<const T*>(&pk);
+              uint4 pk;
+              T* e = reinterpret_cast<T*>(&pk);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) v[w * 8 + j] += beta * E::to_f(e[j]);
+              for (int j = 0; j < 8; ++j) e[j] = E::from_f(v[w * 8 + j]);
+              dst[w] = pk;
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              if (col0 + j < n_len) v[j] += beta * E::to_f(aux_row[col0 + j]);
+              if (col0 + j < n_len && gc0 + j >= first_col) out_row[col0 + j] = E::from_f(v[j]);
             }
           }
         }
-        if (diag != 0.0f) {
-          const int d = row - (tc.n0 + col0);
+        if (G.sym) {
+          // Mirror the strict upper triangle.  The warp's 32x32 block (rows rb.., columns
+          // gc0..) is transposed in shared memory, so lane l writes the contiguous piece
+          // of mirrored row gc0 + l.  Lanes whose row is out of range hold values that the
+          // row mask below never stores.
+          const int rb = tc.m0 + quarter * 32;
+          if (gc0 + 31 > rb) {
+            float* xt = xpose + (warp - 2) * (32 * 33);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (d == j) v[j] += diag;
+            for (int j = 0; j < 32; ++j) xt[lane * 33 + j] = v[j];
+            __syncwarp();
+            const int mr = gc0 + lane;
+            if (mr < G.N && col0 + lane < n_len) {
+              T* mrow = reinterpret_cast<T*>(G.out) + static_cast<int64_t>(tc.b) * G.out_bstride +
+                        static_cast<int64_t>(mr) * G.ld_out + rb;
+              if (gc0 >= rb + 32 && rb + 32 <= G.M) {
+                // block strictly above the diagonal: the whole mirrored piece is stored
+                uint4* dst = reinterpret_cast<uint4*>(mrow);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  uint4 pk;
+                  T* e = reinterpret_cast<T*>(&pk);
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) e[j] = E::from_f(xt[(w * 8 + j) * 33 + lane]);
+                  dst[w] = pk;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  if (rb + j < G.M && mr > rb + j) mrow[j] = E::from_f(xt[j * 33 + lane]);
+                }
+              }
+            }
+            __syncwarp();
           }
         }
-        if (full) {
-          uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint4 pk;
-            T* e = reinterpret_cast<T*>(&pk);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) e[j] = E::from_f(v[w * 8 + j]);
-            dst[w] = pk;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (col0 + j < n_len) out_row[col0 + j] = E::from_f(v[j]);
-          }
-        }
-        }  // row_ok
       }
       ptx::tc_fence_before();
       __syncwarp();

@@ -252,7 +252,28 @@ struct StageSpec {
   bool k_is_n;                         // K = n (X X^T); otherwise K = m
   bool n_is_n;                         // N = n (B X, Q X); otherwise N = m
   float alpha, beta, diag;
+  bool sym;                            // output symmetric: upper-triangle tiles + mirror
 };
+
+// Tiles (packed mt << 16 | nt) of an m x m output that touch its upper triangle.
+std::vector<int32_t> upper_tiles(int m) {
+  std::vector<int32_t> t;
+  const int tm = (m + 127) / 128, tn = (m + 255) / 256;
+  for (int mt = 0; mt < tm; ++mt)
+    for (int nt = 0; nt < tn; ++nt)
+      if (std::min(nt * 256 + 255, m - 1) >= mt * 128) t.push_back((mt << 16) | nt);
+  return t;
+}
+
+// Flops the tensor cores execute for the listed tiles of an m x m x K product.
+double tile_flops(const std::vector<int32_t>& tiles, int m, int K) {
+  double f = 0;
+  for (int32_t p : tiles) {
+    const int mt = p >> 16, nt = p & 0xffff;
+    f += 2.0 * K * std::min(128, m - mt * 128) * std::min(256, m - nt * 256);
+  }
+  return f;
+}
 
 int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, int method, int steps,
                void* ws, size_t ws_bytes, const MetaSink* sink = nullptr) {
@@ -274,9 +295,9 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   if (method == NSM_NS_STANDARD || method == NSM_NS_STANDARD_BF16) {
     for (int k = 0; k < steps; ++k) {
       const int src = (k % 2 == 0) ? X0 : X1, dst = (k % 2 == 0) ? X1 : X0;
-      stages.push_back({src, src, MM0, -1, false, true, false, 1.f, 0.f, 0.f});            // A = X X^T
-      stages.push_back({MM0, MM0, MM0 + 1, MM0, false, false, false, kC, kB, 0.f});       // B = bA + cAA
-      stages.push_back({MM0 + 1, src, dst, src, true, false, true, 1.f, kA, 0.f});         // X' = aX + BX
+      stages.push_back({src, src, MM0, -1, false, true, false, 1.f, 0.f, 0.f, true});            // A = X X^T
+      stages.push_back({MM0, MM0, MM0 + 1, MM0, false, false, false, kC, kB, 0.f, true});       // B = bA + cAA
+      stages.push_back({MM0 + 1, src, dst, src, true, false, true, 1.f, kA, 0.f, false});         // X' = aX + BX
     }
     P.final_buf = (steps % 2 == 0) ? X0 : X1;
     P.final_fp16 = P.x_fp16;
@@ -294,41 +315,41 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       return b;
     };
     auto push = [&](int b) { freeb.push_back(b); };
-    if (steps > 0) stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f});       // R = X X^T
+    if (steps > 0) stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f, true});       // R = X X^T
     for (int k = 1; k <= steps; ++k) {
       const int h = pop();
-      stages.push_back({rR, rR, h, rR, false, false, false, kC, kB, kA});                        // H
+      stages.push_back({rR, rR, h, rR, false, false, false, kC, kB, kA, true});                        // H
       bool h_is_q = false;
       if (q < 0) {
         q = h;                                                                                    // Q = H
         h_is_q = true;
       } else {
         const int qn = pop();
-        stages.push_back({h, q, qn, -1, false, false, false, 1.f, 0.f, 0.f});                    // Q' = H Q
+        stages.push_back({h, q, qn, -1, false, false, false, 1.f, 0.f, 0.f, true});                    // Q' = H Q
         push(q);
         q = qn;
       }
       if (k < steps) {
         if (k % kGramReanchor == 0) {
           const int xn = (xb == X0) ? X1 : X0;
-          stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f});                   // X = Q X
+          stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f, false});                   // X = Q X
           xb = xn;
-          stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f});                 // R = X X^T
+          stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f, true});                 // R = X X^T
           push(q);  // H is Q here or already released below
           if (!h_is_q) push(h);
           q = -1;
           continue;
         }
         const int t = pop();
-        stages.push_back({h, rR, t, -1, false, false, false, 1.f, 0.f, 0.f});                    // T = H R
-        stages.push_back({t, h, rR, -1, false, false, false, 1.f, 0.f, 0.f});                    // R = T H
+        stages.push_back({h, rR, t, -1, false, false, false, 1.f, 0.f, 0.f, true});                    // T = H R
+        stages.push_back({t, h, rR, -1, false, false, false, 1.f, 0.f, 0.f, true});                    // R = T H
         push(t);
       }
       if (!h_is_q) push(h);
     }
     if (q >= 0) {
       const int xn = (xb == X0) ? X1 : X0;
-      stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f});                       // O = Q X
+      stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f, false});                       // O = Q X
       P.final_buf = xn;
     } else {
       P.final_buf = xb;
@@ -336,13 +357,24 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     P.final_fp16 = true;
   }
 
-  // Device metadata: MatInfo[n] | tensor maps [nclass][nbuf] | GemmGroup arrays.
+  // Upper-triangle tile lists of the m x m products, one per class.
+  std::vector<std::vector<int32_t>> class_tiles(nclass);
+  std::vector<size_t> tiles_off(nclass);
+  size_t tile_ints = 0;
+  for (int c = 0; c < nclass; ++c) {
+    class_tiles[c] = upper_tiles(L.classes[c].m);
+    tiles_off[c] = tile_ints;
+    tile_ints += class_tiles[c].size();
+  }
+
+  // Device metadata: MatInfo[n] | tensor maps [nclass][nbuf] | GemmGroup arrays | tile lists.
   const size_t mats_bytes = align_up(sizeof(MatInfo) * n, 128);
   const size_t maps_off = mats_bytes;
   const size_t maps_bytes = align_up(sizeof(CUtensorMap) * size_t(nclass) * nbuf, 128);
   const size_t groups_off = maps_off + maps_bytes;
-  const size_t groups_bytes = sizeof(GemmGroup) * size_t(nclass) * stages.size();
-  const size_t total = groups_off + groups_bytes + 128;
+  const size_t groups_bytes = align_up(sizeof(GemmGroup) * size_t(nclass) * stages.size(), 128);
+  const size_t tiles_off_bytes = groups_off + groups_bytes;
+  const size_t total = tiles_off_bytes + tile_ints * sizeof(int32_t) + 128;
   std::vector<uint8_t> host(total, 0);
 
   MatInfo* hm = reinterpret_cast<MatInfo*>(host.data());
@@ -395,6 +427,11 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     return reinterpret_cast<const CUtensorMap*>(dbase + maps_off) + size_t(c) * nbuf + b;
   };
 
+  int32_t* htiles = reinterpret_cast<int32_t*>(host.data() + tiles_off_bytes);
+  for (int c = 0; c < nclass; ++c) {
+    std::copy(class_tiles[c].begin(), class_tiles[c].end(), htiles + tiles_off[c]);
+  }
+  const int32_t* dtiles = reinterpret_cast<const int32_t*>(dbase + tiles_off_bytes);
   GemmGroup* hg = reinterpret_cast<GemmGroup*>(host.data() + groups_off);
   for (size_t s = 0; s < stages.size(); ++s) {
     const StageSpec& st = stages[s];
@@ -408,7 +445,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     });
     GemmGroup* gs = hg + s * nclass;
     int64_t tiles = 0;
-    double flops = 0;
+    double flops = 0, canonical = 0;
     for (int j = 0; j < nclass; ++j) {
       const int c = order[j];
       const ShapeClass& sc = L.classes[c];
@@ -432,8 +469,17 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       g.tiles_m = (g.M + 127) / 128;
       g.tiles_n = (g.N + 255) / 256;
       g.tile_begin = tiles;
-      tiles += int64_t(g.count) * g.tiles_m * g.tiles_n;
-      flops += 2.0 * g.count * double(g.M) * g.N * g.K;
+      canonical += 2.0 * g.count * double(g.M) * g.N * g.K;
+      if (st.sym) {
+        g.sym = 1;
+        g.tile_list = dtiles + tiles_off[c];
+        g.tiles_per_mat = static_cast<int32_t>(class_tiles[c].size());
+        tiles += int64_t(g.count) * g.tiles_per_mat;
+        flops += g.count * tile_flops(class_tiles[c], g.M, g.K);
+      } else {
+        tiles += int64_t(g.count) * g.tiles_m * g.tiles_n;
+        flops += 2.0 * g.count * double(g.M) * g.N * g.K;
+      }
       gs[j] = g;
     }
     GemmLaunch l{};
@@ -447,6 +493,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     l.beta = st.beta;
     l.diag = st.diag;
     l.flops = flops;
+    l.canonical_flops = canonical;
     P.launches.push_back(l);
   }
 
@@ -874,8 +921,8 @@ int adamw_step(const void* grads, float* params, float* exp_avg, float* exp_avg_
 }
 
 int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo, const void* aux, int ldx, int M,
-             int N, int K, int b_mn_major, int fp16, float alpha, float beta, float diag, void* scratch,
-             size_t scratch_bytes, nsm_stream_t stream_) {
+             int N, int K, int b_mn_major, int fp16, int symmetric, float alpha, float beta, float diag,
+             void* scratch, size_t scratch_bytes, nsm_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (!a || !b || !out || !scratch) return fail(NSM_ERR_NULL, "a, b, out and scratch must be non-NULL");
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
@@ -888,7 +935,9 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   if (!aligned(a, 16) || !aligned(b, 16) || !aligned(out, 16) || (aux && !aligned(aux, 16)))
     return fail(NSM_ERR_ALIGN, "pointers must be 16-byte aligned");
   if (!aligned(scratch, 128)) return fail(NSM_ERR_ALIGN, "scratch must be 128-byte aligned");
-  const size_t need = 2 * sizeof(CUtensorMap) + sizeof(GemmGroup);
+  if (symmetric && M != N) return fail(NSM_ERR_SHAPE, "a symmetric output needs M == N");
+  const std::vector<int32_t> sym_tiles = symmetric ? upper_tiles(M) : std::vector<int32_t>();
+  const size_t need = nsm_gemm_scratch_bytes(M, N, symmetric);
   if (scratch_bytes < need) return fail(NSM_ERR_WORKSPACE, "scratch needs %zu bytes", need);
   if (aux && ranges_overlap(aux, size_t(M) * ldx * 2, out, size_t(M) * ldo * 2))
     return fail(NSM_ERR_ARG, "aux must not overlap out");
@@ -919,7 +968,15 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   g.tiles_m = (M + 127) / 128;
   g.tiles_n = (N + 255) / 256;
   g.tile_begin = 0;
-  cudaError_t e = cudaMemcpyAsync(scratch, &blob, sizeof(blob), cudaMemcpyHostToDevice, stream);
+  std::vector<uint8_t> host(sizeof(Blob) + sym_tiles.size() * sizeof(int32_t));
+  if (symmetric) {
+    g.sym = 1;
+    g.tiles_per_mat = static_cast<int32_t>(sym_tiles.size());
+    g.tile_list = reinterpret_cast<const int32_t*>(static_cast<char*>(scratch) + sizeof(Blob));
+    std::memcpy(host.data() + sizeof(Blob), sym_tiles.data(), sym_tiles.size() * sizeof(int32_t));
+  }
+  std::memcpy(host.data(), &blob, sizeof(Blob));
+  cudaError_t e = cudaMemcpyAsync(scratch, host.data(), host.size(), cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return fail_cuda(e, "copy GEMM descriptors");
   // the source is pageable host memory: the copy is staged before cudaMemcpyAsync returns
   GemmLaunch l{};
@@ -928,11 +985,12 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   l.b_mn_major = b_mn_major ? 1 : 0;
   l.has_aux = aux ? 1 : 0;
   l.fp16 = fp16 ? 1 : 0;
-  l.total_tiles = int64_t(g.tiles_m) * g.tiles_n;
+  l.total_tiles = symmetric ? int64_t(sym_tiles.size()) : int64_t(g.tiles_m) * g.tiles_n;
   l.alpha = alpha;
   l.beta = aux ? beta : 0.f;
   l.diag = diag;
-  l.flops = 2.0 * M * double(N) * K;
+  l.canonical_flops = 2.0 * M * double(N) * K;
+  l.flops = symmetric ? tile_flops(sym_tiles, M, K) : l.canonical_flops;
   int dev = 0, num_sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -944,6 +1002,12 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   if (e != cudaSuccess) return fail_cuda(e, "GEMM launch");
   t_last_launches = 1;
   return NSM_OK;
+}
+
+size_t nsm_gemm_scratch_bytes(int M, int N, int symmetric) {
+  size_t b = 2 * sizeof(CUtensorMap) + sizeof(GemmGroup);
+  if (symmetric && M > 0 && M == N) b += upper_tiles(M).size() * sizeof(int32_t);
+  return align_up(b, 128);
 }
 
 int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16, const int64_t* offsets, const int32_t* shapes,

@@ -35,11 +35,15 @@ constexpr int kTile = 64;
 // A[b] is M x K (K contiguous).  B[b] is N x K (K contiguous, "K-major") or K x N
 // (N contiguous, "MN-major"), chosen per launch.  Output and aux are M x N with row
 // strides ld_out / ld_aux and batch strides out_bstride / aux_bstride (elements).
+// sym != 0: the output is known to be symmetric (M == N, aux symmetric); only the tiles
+// in tile_list (packed mt << 16 | nt, tiles_per_mat of them) are computed, their upper
+// triangle is stored and mirrored into the lower one.
 struct GemmGroup {
   const CUtensorMap* map_a;
   const CUtensorMap* map_b;
   void* out;
   const void* aux;
+  const int32_t* tile_list;
   int64_t out_bstride;
   int64_t aux_bstride;
   int64_t tile_begin;
@@ -47,9 +51,10 @@ struct GemmGroup {
   int32_t M, N, K;
   int32_t count;
   int32_t tiles_m, tiles_n;
+  int32_t sym, tiles_per_mat;
   int32_t pad0, pad1;
 };
-static_assert(sizeof(GemmGroup) == 96, "GemmGroup layout");
+static_assert(sizeof(GemmGroup) == 112, "GemmGroup layout");
 
 struct GemmLaunch {
   const GemmGroup* groups;  // device array
@@ -59,7 +64,8 @@ struct GemmLaunch {
   int32_t fp16;             // 1: operands/outputs are fp16, else bf16
   int64_t total_tiles;
   float alpha, beta, diag;
-  double flops;             // canonical flops of this launch
+  double flops;             // flops the tensor cores execute (whole tiles)
+  double canonical_flops;   // 2 M N K per problem, as if no tile were skipped
 };
 
 // ---- launchers (defined in the .cu files) ---------------------------------------

@@ -110,3 +110,46 @@ def test_gemm_rejects_bad_arguments(nsm):
     with pytest.raises(nsm.NsmError) as e:
         nsm.gemm(a, b, out)
     assert e.value.code == nsm.NSM_ERR_ALIGN
+
+
+SYM_CASES = [(128, 64), (200, 72), (256, 256), (384, 1024), (1000, 136), (64, 64), (3, 8), (520, 4096)]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("M,K", SYM_CASES)
+@pytest.mark.parametrize("use_aux", [False, True])
+def test_gemm_symmetric_output(nsm, dtype, M, K, use_aux):
+    # A A^T (+ beta S + diag I with S symmetric) computed on the upper-triangle tiles only
+    seed = M * 11 + K
+    a = _rand((M, K), dtype, seed)
+    aux = None
+    if use_aux:
+        s = _rand((M, M), torch.float32, seed + 1)
+        s = (s + s.T).to(dtype)
+        ld = (M + 7) // 8 * 8
+        aux = torch.zeros((M, ld), dtype=dtype, device="cuda")[:, :M]
+        aux.copy_(s)
+    ld = (M + 7) // 8 * 8
+    out_full = torch.full((M, ld + 8), float("nan"), dtype=dtype, device="cuda")
+    out = out_full[:, :M]
+    alpha, beta, diag = 0.5, -1.5, (2.0 if use_aux else 0.0)
+    nsm.gemm(a, a, out, aux, False, alpha, beta, diag, symmetric=True)
+    assert nsm.device_status() == nsm.NSM_OK
+    got = out.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert np.array_equal(got, got.T)  # exactly symmetric
+    ref = _ref(a, a, aux, False, alpha, beta if use_aux else 0.0, diag)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= (4e-3 if dtype == torch.bfloat16 else 5e-4), rel
+    # nothing written past the M columns of the view
+    assert torch.isnan(out_full[:, M:ld].float()).all() if ld > M else True
+    assert torch.isnan(out_full[:, ld:].float()).all()
+
+
+def test_gemm_symmetric_rejects_rectangular(nsm):
+    a = _rand((64, 64), torch.bfloat16, 0)
+    b = _rand((128, 64), torch.bfloat16, 1)
+    out = torch.empty((64, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(nsm.NsmError) as e:
+        nsm.gemm(a, b, out, symmetric=True)
+    assert e.value.code == nsm.NSM_ERR_SHAPE
