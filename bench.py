@@ -150,6 +150,25 @@ def _dist_setup(args):
     return world, rank, local
 
 
+def rank_workload(name, rank):
+    """The owner group rank `rank` runs: the workload's shapes with its own seed (weak
+    scaling: every rank owns one group of the same size; no data crosses ranks)."""
+    import synth
+    wl = synth.workload(name)
+    wl.seed = wl.seed + 7919 * rank
+    return wl
+
+
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (the step time the job sees)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _traffic_record(method, workload):
     """Per-launch DRAM traffic of the dominant kernel from a committed ncu summary, if the
     kernel source is unchanged since the counters were taken."""
@@ -250,7 +269,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     nsm.lib()
-    wl = synth.workload(args.config)
+    wl = rank_workload(args.config, rank)
     shapes = wl.muon_shapes
     method = args.method
     offsets, total = nsm.pack(shapes)
@@ -309,10 +328,8 @@ def run_ours(args):
             per_kind[kname] = (k_ms, k_n, k_work)
     if nsm.device_status() != nsm.NSM_OK:
         raise RuntimeError("a bounded device wait expired in the timed region")
+    ms = max_over_ranks(ms, dist, dev)
     if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     clocks = clk.summary()
 

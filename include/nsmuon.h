@@ -80,6 +80,16 @@ int nsm_route(const char* name, int ndim);
 int nsm_pack(const int32_t* shapes, int n, int64_t align_elems,
              int64_t* offsets_out, int64_t* total_out);
 
+/* Dedicated ownership ([DMZ] §两种packed buffer生命周期 and §每步通信字节数: every
+ * Muon-target matrix has one owner, which alone runs its Newton-Schulz chain).  Assigns
+ * the n matrices of a table to `world` owners by longest-processing-time-first on the
+ * flops of each matrix's chain (ns_method/ns_steps as in muon_step): heaviest first, to
+ * the least-loaded owner, ties to the lower rank.  Deterministic: every rank computes
+ * the same plan.  owner_out: n int32 (host, caller-allocated); load_out: world int64
+ * flops per owner, or NULL.  Host-only. */
+int nsm_assign_owners(const int32_t* shapes, int n, int world, int ns_method, int ns_steps,
+                      int32_t* owner_out, int64_t* load_out);
+
 /* Bytes of device workspace muon_step / muon_orthogonalize need for this table and
  * method (independent of offsets).  Returns 0 when the arguments are invalid (the
  * reason is in nsm_last_error()).  Host-only. */

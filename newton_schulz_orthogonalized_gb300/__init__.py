@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
     L.nsm_route.restype = ctypes.c_int
     L.nsm_pack.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int64, _c_i64p, _c_i64p]
     L.nsm_pack.restype = ctypes.c_int
+    L.nsm_assign_owners.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, _c_i32p, _c_i64p]
+    L.nsm_assign_owners.restype = ctypes.c_int
     L.muon_workspace_bytes.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     L.muon_workspace_bytes.restype = ctypes.c_size_t
     L.muon_step.argtypes = [_vp, _vp, _vp, _c_i64p, _c_i32p, ctypes.c_int, ctypes.c_float,
@@ -148,6 +151,51 @@ def pack(shapes: Sequence[Tuple[int, int]], align: int = 64) -> Tuple[np.ndarray
     total = np.zeros(1, dtype=np.int64)
     _check(lib().nsm_pack(_i32p(s), n, int(align), _i64p(offs), _i64p(total)))
     return offs, int(total[0])
+
+
+def assign_owners(shapes: Sequence[Tuple[int, int]], world: int, ns_method=NS_METHOD_DEFAULT,
+                  ns_steps: int = NS_STEPS_DEFAULT) -> Tuple[np.ndarray, np.ndarray]:
+    """Owner rank of every matrix (LPT on Newton-Schulz flops) and the flops per owner."""
+    s = _shapes_array(shapes)
+    owner = np.zeros(s.shape[0], dtype=np.int32)
+    load = np.zeros(int(world), dtype=np.int64)
+    _check(lib().nsm_assign_owners(_i32p(s), s.shape[0], int(world), method_code(ns_method),
+                                   int(ns_steps), _i32p(owner), _i64p(load)))
+    return owner, load
+
+
+def owner_table(shapes: Sequence[Tuple[int, int]], owner: Sequence[int], rank: int,
+                align: int = 64):
+    """The packed table of one owner: (indices of its matrices, their shapes, offsets in its
+    own packed buffer, that buffer's length)."""
+    idx = [i for i, o in enumerate(owner) if int(o) == int(rank)]
+    sub = [tuple(shapes[i]) for i in idx]
+    if not sub:
+        return idx, sub, np.zeros(0, dtype=np.int64), 0
+    offs, total = pack(sub, align)
+    return idx, sub, offs, total
+
+
+# "Z2 与 Z3 模式" §每步通信字节数 and §显存开销: communication per step on a shard group of
+# N ranks, in elements of the Muon-target parameters P_M, and the steady-state memory of
+# the packed buffers.
+DMUON_COMM_FACTORS = {"naive_z2": 3, "dmuon_z2": 2, "naive_z3": 4, "dmuon_z3": 3}
+
+
+def dmuon_comm_elements(mode: str, world: int, p_m: float) -> float:
+    """Elements each step moves on the shard group: k (N-1)/N P_M (k per mode)."""
+    return DMUON_COMM_FACTORS[mode] * (world - 1) / world * p_m
+
+
+def dmuon_packed_memory_elements(mode: str, world: int, p_m: float,
+                                 max_layer_p_m: float = 0.0) -> float:
+    """Steady-state elements of owned packed buffers per rank: P_M / N under Z2 (all
+    resident), one layer's buffer (max_layer_P_M) under Z3."""
+    if mode == "dmuon_z2":
+        return p_m / world
+    if mode == "dmuon_z3":
+        return max_layer_p_m
+    raise ValueError(mode)
 
 
 def method_code(ns_method) -> int:

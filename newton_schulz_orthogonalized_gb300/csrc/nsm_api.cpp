@@ -758,6 +758,58 @@ int nsm_pack(const int32_t* shapes, int n, int64_t align_elems, int64_t* offsets
   return NSM_OK;
 }
 
+int nsm_assign_owners(const int32_t* shapes, int n, int world, int ns_method, int ns_steps, int32_t* owner_out,
+                      int64_t* load_out) {
+  if (!owner_out) return fail(NSM_ERR_NULL, "owner_out is NULL");
+  int rc = validate_shapes(shapes, n);
+  if (rc != NSM_OK) return rc;
+  rc = validate_method(ns_method, ns_steps);
+  if (rc != NSM_OK) return rc;
+  if (world < 1 || world > (1 << 20)) return fail(NSM_ERR_ARG, "world = %d out of range", world);
+  // cost of a matrix: flops of its Newton-Schulz chain (the step's dominant work)
+  std::vector<int64_t> cost(n);
+  for (int i = 0; i < n; ++i) {
+    const int64_t r = shapes[2 * i], c = shapes[2 * i + 1];
+    const int64_t m = std::min(r, c), nn = std::max(r, c);
+    if (ns_method == NSM_NS_GRAM) {
+      int64_t wide = ns_steps > 0 ? 1 : 0, cubes = 0;
+      bool q_identity = true;
+      for (int k = 1; k <= ns_steps; ++k) {
+        cubes += q_identity ? 1 : 2;
+        q_identity = false;
+        if (k < ns_steps) {
+          if (k % kGramReanchor == 0) {
+            wide += 2;
+            q_identity = true;
+          } else {
+            cubes += 2;
+          }
+        }
+      }
+      if (ns_steps > 0 && !q_identity) wide += 1;
+      cost[i] = 2 * wide * m * m * nn + 2 * cubes * m * m * m;
+    } else {
+      cost[i] = int64_t(ns_steps) * (4 * m * m * nn + 2 * m * m * m);
+    }
+  }
+  // longest processing time first: heaviest matrix to the least-loaded owner; ties go to
+  // the lower matrix index and the lower rank, so every rank computes the same plan
+  std::vector<int> order(n);
+  for (int i = 0; i < n; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+  std::vector<int64_t> load(world, 0);
+  for (int i : order) {
+    int best = 0;
+    for (int w = 1; w < world; ++w) {
+      if (load[w] < load[best]) best = w;
+    }
+    owner_out[i] = best;
+    load[best] += cost[i];
+  }
+  if (load_out) std::copy(load.begin(), load.end(), load_out);
+  return NSM_OK;
+}
+
 size_t muon_workspace_bytes(const int32_t* shapes, int n, int ns_method, int ns_steps) {
   if (validate_shapes(shapes, n) != NSM_OK) return 0;
   if (validate_method(ns_method, ns_steps) != NSM_OK) return 0;

@@ -11,5 +11,5 @@ from .muon_ref import (  # noqa: F401
     route, matrix_view_shape, pack_offsets, momentum_update, frobenius_normalize,
     ns_poly, ns_poly_iterated, ns_standard, ns_gram, newton_schulz, orthogonalize,
     update_scale, apply_update, muon_step, adamw_step, bf16_bits_to_f64,
-    flops_standard, flops_gram, round_to, method_storage,
+    flops_standard, flops_gram, round_to, method_storage, lpt_assign,
 )

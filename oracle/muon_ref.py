@@ -422,3 +422,24 @@ def flops_gram(m: int, n: int, steps: int = NS_STEPS, restart_every: int = 2) ->
                 cubes += 2              # T = H R, R = T H
     wide += 0 if q_identity else 1      # final Q X (skipped when Q is the identity)
     return 2 * wide * m * m * n + 2 * cubes * m ** 3
+
+
+# --- dedicated ownership (planner check) ------------------------------------------------
+
+def lpt_assign(costs: Sequence[int], world: int) -> Tuple[List[int], List[int]]:
+    """Longest processing time first, written out plainly.
+
+    [DMZ] §每步通信字节数 — under dedicated ownership each Muon-target matrix has one owner
+    that runs its Newton-Schulz chain once.  The build balances owners with LPT: take the
+    matrices from the heaviest down (equal costs in index order), give each to the owner
+    with the smallest load so far (equal loads: the lowest rank).  Returns the owner of
+    every matrix and the load of every owner.
+    """
+    order = sorted(range(len(costs)), key=lambda i: (-costs[i], i))
+    load = [0] * world
+    owner = [0] * len(costs)
+    for i in order:
+        best = min(range(world), key=lambda w: (load[w], w))
+        owner[i] = best
+        load[best] += costs[i]
+    return owner, load
