@@ -50,6 +50,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;          // 6 warps
 constexpr uint32_t TMEM_COLS = 512;       // 2 x 256 fp32 accumulator columns
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+constexpr int kPanel = 8;                 // column tiles per raster panel
 
 struct Ctrl {
   uint64_t full[STAGES];
@@ -88,8 +89,21 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmGroup* __restrict__ g
     mt = packed >> 16;
     nt = packed & 0xffff;
   } else {
-    mt = rem / G.tiles_n;
-    nt = rem - mt * G.tiles_n;
+    // panel raster: the grid is cut into panels of kPanel column tiles, walked row by
+    // row inside a panel, so the tiles in flight at once share few operand panels
+    const int full_panels = G.tiles_n / kPanel;
+    const int panel_tiles = G.tiles_m * kPanel;
+    const int p = rem / panel_tiles;
+    if (p < full_panels) {
+      const int within = rem - p * panel_tiles;
+      mt = within / kPanel;
+      nt = p * kPanel + (within - mt * kPanel);
+    } else {
+      const int w = G.tiles_n - full_panels * kPanel;
+      const int within = rem - full_panels * panel_tiles;
+      mt = within / w;
+      nt = full_panels * kPanel + (within - mt * w);
+    }
   }
   return {lo, b, mt * BM, nt * BN};
 }

@@ -255,13 +255,16 @@ struct StageSpec {
   bool sym;                            // output symmetric: upper-triangle tiles + mirror
 };
 
-// Tiles (packed mt << 16 | nt) of an m x m output that touch its upper triangle.
+// Tiles (packed mt << 16 | nt) of an m x m output that touch its upper triangle, in the
+// engine's panel raster (panels of 8 column tiles, rows inside a panel).
 std::vector<int32_t> upper_tiles(int m) {
   std::vector<int32_t> t;
   const int tm = (m + 127) / 128, tn = (m + 255) / 256;
-  for (int mt = 0; mt < tm; ++mt)
-    for (int nt = 0; nt < tn; ++nt)
-      if (std::min(nt * 256 + 255, m - 1) >= mt * 128) t.push_back((mt << 16) | nt);
+  constexpr int kPanel = 8;
+  for (int p0 = 0; p0 < tn; p0 += kPanel)
+    for (int mt = 0; mt < tm; ++mt)
+      for (int nt = p0; nt < std::min(p0 + kPanel, tn); ++nt)
+        if (std::min(nt * 256 + 255, m - 1) >= mt * 128) t.push_back((mt << 16) | nt);
   return t;
 }
 
