@@ -167,19 +167,23 @@ int adamw_step(const void* grads, float* params, float* exp_avg, float* exp_avg_
  *   out    device, M x N row-major, row stride ldo (written)
  *   aux    device, M x N row-major, row stride ldx, or NULL (then beta is ignored)
  *   fp16   0: every operand is bf16; 1: every operand is fp16.  fp32 accumulation.
- *   symmetric  non-zero when the result is known to be symmetric (M == N and aux, if
+ *   flags  NSM_GEMM_SYMMETRIC: the result is known to be symmetric (M == N and aux, if
  *          any, symmetric): only the tiles touching the upper triangle are computed and
- *          the strict upper triangle is mirrored into the lower one
- *   scratch device, >= nsm_gemm_scratch_bytes(M, N, symmetric) bytes, 128-byte aligned
+ *          the strict upper triangle is mirrored into the lower one.
+ *          NSM_GEMM_PAIR: run on the 2-SM kernel (clusters of two CTAs, 256 x 256 tiles)
+ *          instead of the 1-CTA kernel (128 x 256 tiles).
+ *   scratch device, >= nsm_gemm_scratch_bytes(M, N, flags) bytes, 128-byte aligned
  *          (holds the tensor maps and work list of the call)
  * Row strides must be multiples of 8 elements (>= the row length), pointers 16-byte
  * aligned, aux must not overlap out.  Exposed so the engine can be checked and timed
  * on its own; muon_step and muon_orthogonalize use the same kernel. */
+#define NSM_GEMM_SYMMETRIC 1
+#define NSM_GEMM_PAIR      2
 int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
              const void* aux, int ldx, int M, int N, int K, int b_mn_major, int fp16,
-             int symmetric, float alpha, float beta, float diag, void* scratch,
+             int flags, float alpha, float beta, float diag, void* scratch,
              size_t scratch_bytes, nsm_stream_t stream);
-size_t nsm_gemm_scratch_bytes(int M, int N, int symmetric);
+size_t nsm_gemm_scratch_bytes(int M, int N, int flags);
 
 /* Synchronises `stream`, then reads and clears the device status word that kernels set
  * when a bounded wait expires.  *status_out = NSM_OK or NSM_ERR_TIMEOUT.  Returns

@@ -276,25 +276,31 @@ def adamw_step(grads, params, exp_avg, exp_avg_sq, lr: float = ADAM_LR_DEFAULT,
                             int(step), _stream_ptr(stream)))
 
 
+GEMM_SYMMETRIC = 1
+GEMM_PAIR = 2
+
+
 def gemm(a, b, out, aux=None, b_mn_major: bool = False, alpha: float = 1.0, beta: float = 0.0,
-         diag: float = 0.0, symmetric: bool = False, scratch=None, stream=None) -> None:
+         diag: float = 0.0, symmetric: bool = False, pair: bool = False, scratch=None,
+         stream=None) -> None:
     """out = alpha * a @ op(b) + beta * aux + diag * I on the tensor-core engine.
 
     ``a`` is M x K; ``b`` is N x K (op = transpose) or, with ``b_mn_major``, K x N.  All
     tensors are 2D bf16 or all fp16, with unit column stride.  ``symmetric`` declares the
-    result symmetric: the upper triangle is computed and mirrored."""
+    result symmetric: the upper triangle is computed and mirrored.  ``pair`` runs the 2-SM
+    kernel (256 x 256 tiles on clusters of two CTAs)."""
     import torch
     M, K = a.shape
     N = b.shape[1] if b_mn_major else b.shape[0]
     fp16 = 1 if a.dtype == torch.float16 else 0
+    flags = (GEMM_SYMMETRIC if symmetric else 0) | (GEMM_PAIR if pair else 0)
     if scratch is None:
-        need = lib().nsm_gemm_scratch_bytes(M, N, 1 if symmetric else 0)
+        need = lib().nsm_gemm_scratch_bytes(M, N, flags)
         scratch = torch.empty(max(int(need), 1024), dtype=torch.uint8, device=a.device)
     _check(lib().nsm_gemm(_ptr(a), a.stride(0), _ptr(b), b.stride(0), _ptr(out), out.stride(0),
                           _ptr(aux), 0 if aux is None else aux.stride(0), M, N, K,
-                          1 if b_mn_major else 0, fp16, 1 if symmetric else 0, float(alpha),
-                          float(beta), float(diag), _ptr(scratch), scratch.numel(),
-                          _stream_ptr(stream)))
+                          1 if b_mn_major else 0, fp16, flags, float(alpha), float(beta),
+                          float(diag), _ptr(scratch), scratch.numel(), _stream_ptr(stream)))
 
 
 def device_status(stream=None) -> int:

@@ -3,19 +3,26 @@
 // One persistent launch runs one stage of the chain (for example A = X X^T) for every
 // matrix of a packed group.  Matrices of the same working shape form a group whose
 // operands sit back to back in the workspace, so one 3D tensor map per buffer covers
-// the whole group.  Each CTA owns one SM and walks the flat tile list with a fixed
-// stride, so the result of every tile is computed by exactly one CTA in a fixed order
-// (bit-identical run to run).
+// the whole group.  Work units walk the flat tile list with a fixed stride, so every
+// output tile is computed by exactly one unit in a fixed order (bit-identical run to run).
 //
-// Per CTA: warp 0 issues TMA loads (128B-swizzled 64x64 boxes) into a 4-stage ring,
-// warp 1 issues tcgen05.mma (M=128, N<=256, K=16, fp32 accumulation in TMEM, two
-// accumulator buffers of 256 columns), warps 2-5 drain TMEM with tcgen05.ld and apply
-// the fused epilogue  out = alpha*acc + beta*aux + diag*I  before storing bf16/fp16.
+// Two kernels share the tile decode and the epilogue:
+//   k_ns_gemm       one CTA per SM, 128 x 256 tiles (tcgen05.mma.cta_group::1, M = 128).
+//   k_ns_gemm_pair  a cluster of two CTAs on two SMs per 256 x 256 tile
+//                   (tcgen05.mma.cta_group::2, M = 256): each CTA stages half of A and half
+//                   of B, so each SM's shared memory carries two thirds of the operand
+//                   traffic of the 1-CTA tile for the same tensor-core work.
+// Roles inside a CTA: warp 0 issues TMA loads (128B-swizzled 64x64 boxes) into a ring of
+// stages, warp 1 issues the MMAs (the leader CTA's, in the pair kernel) into two TMEM
+// accumulators of 256 fp32 columns, warps 2-5 drain TMEM with tcgen05.ld and apply the
+// fused epilogue  out = alpha*acc + beta*aux + diag*I  before storing bf16/fp16.
+// A group flagged symmetric computes only the tiles that touch the upper triangle, stores
+// that triangle and mirrors it.
 //
 // The stages it serves ("DeepSpeed 集成 Muon 优化器实战" §核心算子):
 //   standard:  A = X X^T;  B = b A + c A A^T (A symmetric);  X' = a X + B X
 //   gram:      R = X X^T;  H = a I + b R + c R R^T;  Q' = H Q^T;  T = H R^T;
-//              R' = T H^T;  O = Q X      (H, Q, R are symmetric polynomials of R_0)
+//              R' = T H^T;  X = Q X;  O = Q X   (H, Q, R, T symmetric polynomials of R_0)
 // B X and Q X read X as a K x N operand with N contiguous ("MN-major").
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -39,19 +46,28 @@ int* device_status_ptr() {
 
 namespace {
 
-constexpr int BM = 128;                   // MMA M (TMEM lanes)
 constexpr int BN = 256;                   // widest MMA N per tile
 constexpr int BK = 64;                    // K per stage: 64 16-bit elements = 128 B rows
-constexpr int STAGES = 4;
 constexpr int BOX_BYTES = 64 * 64 * 2;    // one TMA box: 64 rows x 128 B
-constexpr int A_BYTES = BM * BK * 2;      // 16 KB
-constexpr int B_BYTES = BN * BK * 2;      // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;          // 6 warps
 constexpr uint32_t TMEM_COLS = 512;       // 2 x 256 fp32 accumulator columns
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 constexpr int kPanel = 8;                 // column tiles per raster panel
+constexpr int EPI_WARPS = 4;
+constexpr int XPOSE_BYTES = EPI_WARPS * 32 * 33 * 4;  // per-warp 32x32 fp32 transpose tiles
 
+// 1-CTA kernel: 128 x 256 tiles, 4 stages of A 16 KB + B 32 KB.
+constexpr int S1_STAGES = 4;
+constexpr int S1_A_BYTES = 128 * BK * 2;
+constexpr int S1_STAGE_BYTES = S1_A_BYTES + BN * BK * 2;
+
+// pair kernel: 256 x 256 tiles, each CTA stages A 128 x 64 and half of B (128 x 64):
+// 6 stages of 32 KB.
+constexpr int S2_STAGES = 6;
+constexpr int S2_A_BYTES = 128 * BK * 2;
+constexpr int S2_STAGE_BYTES = S2_A_BYTES + 128 * BK * 2;
+
+template <int STAGES>
 struct Ctrl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -63,14 +79,18 @@ struct Ctrl {
   int never;  // stays 0: the flag the teardown waits poll, so they ignore `abort`
 };
 
-constexpr int EPI_WARPS = 4;
-constexpr int XPOSE_BYTES = EPI_WARPS * 32 * 33 * 4;  // per-warp 32x32 fp32 transpose tiles
-constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + XPOSE_BYTES + sizeof(Ctrl);
+constexpr size_t S1_SMEM = 1024 + size_t(S1_STAGES) * S1_STAGE_BYTES + XPOSE_BYTES + sizeof(Ctrl<S1_STAGES>);
+constexpr size_t S2_SMEM = 1024 + size_t(S2_STAGES) * S2_STAGE_BYTES + XPOSE_BYTES + sizeof(Ctrl<S2_STAGES>);
+static_assert(S1_SMEM <= 232448 && S2_SMEM <= 232448, "shared memory per CTA");
 
 struct TileCoord {
   int g, b, m0, n0;
 };
 
+// Tile t of the launch: group, matrix within the group, first row and column.  Tiles are
+// TILE_M x 256; symmetric groups enumerate their precomputed list, the others the grid in
+// panels of kPanel column tiles (rows inside a panel).
+template <int TILE_M>
 __device__ __forceinline__ TileCoord decode_tile(const GemmGroup* __restrict__ groups, int ng,
                                                  int64_t t) {
   int lo = 0, hi = ng - 1;
@@ -89,8 +109,6 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmGroup* __restrict__ g
     mt = packed >> 16;
     nt = packed & 0xffff;
   } else {
-    // panel raster: the grid is cut into panels of kPanel column tiles, walked row by
-    // row inside a panel, so the tiles in flight at once share few operand panels
     const int full_panels = G.tiles_n / kPanel;
     const int panel_tiles = G.tiles_m * kPanel;
     const int p = rem / panel_tiles;
@@ -105,7 +123,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmGroup* __restrict__ g
       nt = full_panels * kPanel + (within - mt * w);
     }
   }
-  return {lo, b, mt * BM, nt * BN};
+  return {lo, b, mt * TILE_M, nt * BN};
 }
 
 template <bool FP16>
@@ -123,22 +141,132 @@ struct Elem<true> {
   __device__ static __forceinline__ T from_f(float v) { return __float2half_rn(v); }
 };
 
-__device__ __forceinline__ void signal_timeout(Ctrl* ctrl, int* status) {
+template <int STAGES>
+__device__ __forceinline__ void signal_timeout(Ctrl<STAGES>* ctrl, int* status) {
   ctrl->abort = 1;
   atomicExch(status, kDevTimeout);
 }
+
+// Epilogue of one accumulator: this warp's 32 rows (rows rb .. rb+31 of the matrix,
+// TMEM lanes 32*quarter ..), the tile's n_len columns from column n0.
+template <bool FP16, bool HAS_AUX>
+__device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
+                                              uint32_t t_row, float* xt, int lane, float alpha,
+                                              float beta, float diag) {
+  using E = Elem<FP16>;
+  using T = typename E::T;
+  const int row = rb + lane;
+  const bool row_ok = row < G.M;
+  const int nchunks = (n_len + 31) >> 5;
+  T* out_row = reinterpret_cast<T*>(G.out) + static_cast<int64_t>(b) * G.out_bstride +
+               static_cast<int64_t>(row) * G.ld_out + n0;
+  const T* aux_row = nullptr;
+  if (HAS_AUX) {
+    aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(b) * G.aux_bstride +
+              static_cast<int64_t>(row) * G.ld_aux + n0;
+  }
+  for (int c = 0; c < nchunks; ++c) {
+    uint32_t r[32];
+    __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
+    ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+    ptx::tmem_ld_wait();
+    const int col0 = c * 32;
+    const int gc0 = n0 + col0;  // first column of this chunk in the matrix
+    const bool full = col0 + 32 <= n_len;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
+    if (row_ok) {
+      if (HAS_AUX) {
+        if (full) {
+          const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 pk = __ldg(src + w);
+            const T* e = reinterpret_cast<const T*>(&pk);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[w * 8 + j] += beta * E::to_f(e[j]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (col0 + j < n_len) v[j] += beta * E::to_f(aux_row[col0 + j]);
+          }
+        }
+      }
+      if (diag != 0.0f) {
+        const int d = row - gc0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (d == j) v[j] += diag;
+        }
+      }
+      // a symmetric output stores only its upper triangle (column >= row) directly
+      const int first_col = G.sym ? row : 0;
+      if (full && gc0 >= first_col) {
+        uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint4 pk;
+          T* e = reinterpret_cast<T*>(&pk);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) e[j] = E::from_f(v[w * 8 + j]);
+          dst[w] = pk;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (col0 + j < n_len && gc0 + j >= first_col) out_row[col0 + j] = E::from_f(v[j]);
+        }
+      }
+    }
+    if (G.sym && gc0 + 31 > rb) {
+      // Mirror the strict upper triangle.  The warp's 32x32 block (rows rb.., columns
+      // gc0..) is transposed in shared memory, so lane l writes the contiguous piece of
+      // mirrored row gc0 + l.  Lanes whose row is out of range hold values that the row
+      // mask below never stores.
+#pragma unroll
+      for (int j = 0; j < 32; ++j) xt[lane * 33 + j] = v[j];
+      __syncwarp();
+      const int mr = gc0 + lane;
+      if (mr < G.N && col0 + lane < n_len) {
+        T* mrow = reinterpret_cast<T*>(G.out) + static_cast<int64_t>(b) * G.out_bstride +
+                  static_cast<int64_t>(mr) * G.ld_out + rb;
+        if (gc0 >= rb + 32 && rb + 32 <= G.M) {
+          // block strictly above the diagonal: the whole mirrored piece is stored
+          uint4* dst = reinterpret_cast<uint4*>(mrow);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 pk;
+            T* e = reinterpret_cast<T*>(&pk);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) e[j] = E::from_f(xt[(w * 8 + j) * 33 + lane]);
+            dst[w] = pk;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (rb + j < G.M && mr > rb + j) mrow[j] = E::from_f(xt[j * 33 + lane]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// ===================================================================== 1-CTA kernel
 
 template <bool B_MN, bool FP16, bool HAS_AUX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ns_gemm(const GemmGroup* __restrict__ groups, int ng, int64_t total_tiles, float alpha,
               float beta, float diag, int* status) {
-  using E = Elem<FP16>;
-  using T = typename E::T;
+  constexpr int STAGES = S1_STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* xpose = reinterpret_cast<float*>(smem + size_t(STAGES) * STAGE_BYTES);
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + size_t(STAGES) * STAGE_BYTES + XPOSE_BYTES);
+  float* xpose = reinterpret_cast<float*>(smem + size_t(STAGES) * S1_STAGE_BYTES);
+  auto* ctrl = reinterpret_cast<Ctrl<STAGES>*>(smem + size_t(STAGES) * S1_STAGE_BYTES + XPOSE_BYTES);
   const uint32_t ring = ptx::smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -152,7 +280,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar(&ctrl->acc_full[a]), 1);
-      ptx::mbar_init(bar(&ctrl->acc_empty[a]), 4);
+      ptx::mbar_init(bar(&ctrl->acc_empty[a]), EPI_WARPS);
     }
     ptx::mbar_init(bar(&ctrl->drain), 1);
     ctrl->abort = 0;
@@ -180,7 +308,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int s = 0; s < STAGES; ++s) fill_parity[s] = -1;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const TileCoord tc = decode_tile(groups, ng, t);
+        const TileCoord tc = decode_tile<128>(groups, ng, t);
         const GemmGroup& G = groups[tc.g];
         const int kblocks = (G.K + BK - 1) / BK;
         const int n_len = min(BN, G.N - tc.n0);
@@ -196,8 +324,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const uint32_t fb = bar(&ctrl->full[stage]);
           ptx::mbar_arrive_expect_tx(fb, bytes);
-          const uint32_t a_dst = ring + stage * STAGE_BYTES;
-          const uint32_t b_dst = a_dst + A_BYTES;
+          const uint32_t a_dst = ring + stage * S1_STAGE_BYTES;
+          const uint32_t b_dst = a_dst + S1_A_BYTES;
           const int k0 = kb * BK;
           ptx::tma_load_3d(a_dst, G.map_a, fb, k0, tc.m0, tc.b);
           if (a_boxes == 2) ptx::tma_load_3d(a_dst + BOX_BYTES, G.map_a, fb, k0, tc.m0 + 64, tc.b);
@@ -234,7 +362,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int local = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++local) {
-        const TileCoord tc = decode_tile(groups, ng, t);
+        const TileCoord tc = decode_tile<128>(groups, ng, t);
         const GemmGroup& G = groups[tc.g];
         const int kblocks = (G.K + BK - 1) / BK;
         const int n_len = min(BN, G.N - tc.n0);
@@ -249,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        const uint32_t idesc = ptx::idesc_f16(BM, nb * 64, !FP16, B_MN);
+        const uint32_t idesc = ptx::idesc_f16(128, nb * 64, !FP16, B_MN);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait_bounded(bar(&ctrl->full[stage]), phase, abort_flag,
                                       WAIT_LIMIT_NS)) {
@@ -258,8 +386,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a_addr = ring + stage * STAGE_BYTES;
-          const uint32_t b_addr = a_addr + A_BYTES;
+          const uint32_t a_addr = ring + stage * S1_STAGE_BYTES;
+          const uint32_t b_addr = a_addr + S1_A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t a_desc = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
@@ -286,9 +414,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int quarter = warp & 3;  // TMEM lanes this warp may access: 32*quarter + [0, 32)
+    float* xt = xpose + (warp - 2) * (32 * 33);
     int local = 0;
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
-      const TileCoord tc = decode_tile(groups, ng, t);
+      const TileCoord tc = decode_tile<128>(groups, ng, t);
       const GemmGroup& G = groups[tc.g];
       const int acc = local & 1;
       const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
@@ -301,112 +430,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       ptx::tc_fence_after();
-
-      const int row = tc.m0 + quarter * 32 + lane;
-      const bool row_ok = row < G.M;
-      const int n_len = min(BN, G.N - tc.n0);
-      const int nchunks = (n_len + 31) >> 5;
-      T* out_row = reinterpret_cast<T*>(G.out) + static_cast<int64_t>(tc.b) * G.out_bstride +
-                   static_cast<int64_t>(row) * G.ld_out + tc.n0;
-      const T* aux_row = nullptr;
-      if (HAS_AUX) {
-        aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(tc.b) * G.aux_bstride +
-                  static_cast<int64_t>(row) * G.ld_aux + tc.n0;
-      }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-      for (int c = 0; c < nchunks; ++c) {
-        uint32_t r[32];
-        __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
-        ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
-        ptx::tmem_ld_wait();
-        const int col0 = c * 32;
-        const int gc0 = tc.n0 + col0;  // first column of this chunk in the matrix
-        const bool full = col0 + 32 <= n_len;
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
-        if (row_ok) {
-          if (HAS_AUX) {
-            if (full) {
-              const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
-#pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                uint4 pk = __ldg(src + w);
-                const T* e = reinterpret_cast<const T*>(&pk);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[w * 8 + j] += beta * E::to_f(e[j]);
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                if (col0 + j < n_len) v[j] += beta * E::to_f(aux_row[col0 + j]);
-              }
-            }
-          }
-          if (diag != 0.0f) {
-            const int d = row - gc0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (d == j) v[j] += diag;
-            }
-          }
-          // a symmetric output stores only its upper triangle (column >= row) directly
-          const int first_col = G.sym ? row : 0;
-          if (full && gc0 >= first_col) {
-            uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              uint4 pk;
-              T* e = reinterpret_cast<T*>(&pk);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) e[j] = E::from_f(v[w * 8 + j]);
-              dst[w] = pk;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < n_len && gc0 + j >= first_col) out_row[col0 + j] = E::from_f(v[j]);
-            }
-          }
-        }
-        if (G.sym) {
-          // Mirror the strict upper triangle.  The warp's 32x32 block (rows rb.., columns
-          // gc0..) is transposed in shared memory, so lane l writes the contiguous piece
-          // of mirrored row gc0 + l.  Lanes whose row is out of range hold values that the
-          // row mask below never stores.
-          const int rb = tc.m0 + quarter * 32;
-          if (gc0 + 31 > rb) {
-            float* xt = xpose + (warp - 2) * (32 * 33);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) xt[lane * 33 + j] = v[j];
-            __syncwarp();
-            const int mr = gc0 + lane;
-            if (mr < G.N && col0 + lane < n_len) {
-              T* mrow = reinterpret_cast<T*>(G.out) + static_cast<int64_t>(tc.b) * G.out_bstride +
-                        static_cast<int64_t>(mr) * G.ld_out + rb;
-              if (gc0 >= rb + 32 && rb + 32 <= G.M) {
-                // block strictly above the diagonal: the whole mirrored piece is stored
-                uint4* dst = reinterpret_cast<uint4*>(mrow);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                  uint4 pk;
-                  T* e = reinterpret_cast<T*>(&pk);
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) e[j] = E::from_f(xt[(w * 8 + j) * 33 + lane]);
-                  dst[w] = pk;
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  if (rb + j < G.M && mr > rb + j) mrow[j] = E::from_f(xt[j * 33 + lane]);
-                }
-              }
-            }
-            __syncwarp();
-          }
-        }
-      }
+      epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
+                                   t_row, xt, lane, alpha, beta, diag);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(&ctrl->acc_empty[acc]));
@@ -421,26 +448,298 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ===================================================================== pair kernel
+//
+// A cluster of two CTAs (ranks 0 and 1, the leader is rank 0) owns one 256 x 256 output
+// tile at a time.  Rank r stages rows [m0 + 128r, +128) of A and rows (K-major B) or
+// columns (MN-major B) [n0 + 128r, +128) of B; its TMA loads count on the leader's full
+// barrier.  The leader issues tcgen05.mma.cta_group::2 (M = 256, N = 256) and commits to
+// both CTAs' empty / accumulator barriers with a multicast.  Each CTA's TMEM receives its
+// own 128 rows of D; the epilogue warps of both CTAs arrive on the leader's
+// accumulator-empty barrier.  Every wait is bounded; every path reaches the closing
+// cluster barrier.
+
+__device__ __forceinline__ int boxes_in(int start, int limit) {
+  // 64-wide boxes of the 128-wide half starting at `start` that hold any in-range index
+  const int left = limit - start;
+  return left <= 0 ? 0 : (left > 64 ? 2 : 1);
+}
+
 template <bool B_MN, bool FP16, bool HAS_AUX>
-cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream) {
-  static std::atomic<uint64_t> attr_done{0};  // one bit per device ordinal < 64
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    k_ns_gemm_pair(const GemmGroup* __restrict__ groups, int ng, int64_t total_tiles, float alpha,
+                   float beta, float diag, int* status) {
+  constexpr int STAGES = S2_STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* xpose = reinterpret_cast<float*>(smem + size_t(STAGES) * S2_STAGE_BYTES);
+  auto* ctrl = reinterpret_cast<Ctrl<STAGES>*>(smem + size_t(STAGES) * S2_STAGE_BYTES + XPOSE_BYTES);
+  const uint32_t ring = ptx::smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int64_t pair = blockIdx.x >> 1;
+  const int64_t npairs = gridDim.x >> 1;
+
+  auto bar = [&](uint64_t* b) { return ptx::smem_u32(b); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar(&ctrl->full[s]), 1);
+      ptx::mbar_init(bar(&ctrl->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(bar(&ctrl->acc_full[a]), 1);
+      ptx::mbar_init(bar(&ctrl->acc_empty[a]), 2 * EPI_WARPS);
+    }
+    ptx::mbar_init(bar(&ctrl->drain), 1);
+    ctrl->abort = 0;
+    ctrl->never = 0;
+    ptx::fence_mbarrier_init();
+  }
+  // both CTAs' barriers must exist before either CTA signals the other's
+  ptx::cluster_sync();
+  if (warp == 0) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(&ctrl->tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctrl->tmem_base;
+  volatile int* abort_flag = &ctrl->abort;
+  volatile int* never_flag = &ctrl->never;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fill_parity[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) fill_parity[s] = -1;
+      bool ok = true;
+      for (int64_t t = pair; t < total_tiles && ok; t += npairs) {
+        const TileCoord tc = decode_tile<256>(groups, ng, t);
+        const GemmGroup& G = groups[tc.g];
+        const int kblocks = (G.K + BK - 1) / BK;
+        // boxes each CTA loads; the leader expects both CTAs' bytes
+        const int a0 = boxes_in(tc.m0, G.M), a1 = boxes_in(tc.m0 + 128, G.M);
+        const int b0 = boxes_in(tc.n0, G.N), b1 = boxes_in(tc.n0 + 128, G.N);
+        const int my_a = rank ? a1 : a0, my_b = rank ? b1 : b0;
+        const uint32_t total_bytes = static_cast<uint32_t>((a0 + a1 + b0 + b1) * BOX_BYTES);
+        const int row0 = tc.m0 + 128 * static_cast<int>(rank);
+        const int col0 = tc.n0 + 128 * static_cast<int>(rank);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(bar(&ctrl->empty[stage]), phase ^ 1u, abort_flag,
+                                      WAIT_LIMIT_NS)) {
+            signal_timeout(ctrl, status);
+            ok = false;
+            break;
+          }
+          const uint32_t fb_local = bar(&ctrl->full[stage]);
+          const uint32_t fb_leader = ptx::mapa_shared(fb_local, 0);
+          if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, total_bytes);
+          const uint32_t a_dst = ring + stage * S2_STAGE_BYTES;
+          const uint32_t b_dst = a_dst + S2_A_BYTES;
+          const int k0 = kb * BK;
+          for (int q = 0; q < my_a; ++q) {
+            ptx::tma_load_3d_pair(a_dst + q * BOX_BYTES, G.map_a, fb_leader, k0, row0 + 64 * q, tc.b);
+          }
+          for (int q = 0; q < my_b; ++q) {
+            if (B_MN) {
+              ptx::tma_load_3d_pair(b_dst + q * BOX_BYTES, G.map_b, fb_leader, col0 + 64 * q, k0, tc.b);
+            } else {
+              ptx::tma_load_3d_pair(b_dst + q * BOX_BYTES, G.map_b, fb_leader, k0, col0 + 64 * q, tc.b);
+            }
+          }
+          fill_parity[stage] = static_cast<int>(phase);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        if (rank == 0) {
+          // the leader's full barriers count both CTAs' copies: wait for those in flight
+          for (int s = 0; s < STAGES; ++s) {
+            if (fill_parity[s] >= 0) {
+              ptx::mbar_wait_bounded(bar(&ctrl->full[s]), static_cast<uint32_t>(fill_parity[s]),
+                                     never_flag, WAIT_LIMIT_NS);
+            }
+          }
+        } else {
+          // the peer cannot observe the leader's barriers: give its copies time to land
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (ptx::globaltimer_ns() - t0 < 1000000ull) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      const uint32_t idesc = ptx::idesc_f16(256, 256, !FP16, B_MN);
+      for (int64_t t = pair; t < total_tiles && ok; t += npairs, ++local) {
+        const TileCoord tc = decode_tile<256>(groups, ng, t);
+        const GemmGroup& G = groups[tc.g];
+        const int kblocks = (G.K + BK - 1) / BK;
+        const int acc = local & 1;
+        const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
+        if (!ptx::mbar_wait_bounded(bar(&ctrl->acc_empty[acc]), acc_phase ^ 1u, abort_flag,
+                                    WAIT_LIMIT_NS)) {
+          signal_timeout(ctrl, status);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(bar(&ctrl->full[stage]), phase, abort_flag,
+                                      WAIT_LIMIT_NS)) {
+            signal_timeout(ctrl, status);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ring + stage * S2_STAGE_BYTES;
+          const uint32_t b_addr = a_addr + S2_A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t a_desc = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t b_desc = B_MN ? ptx::smem_desc_sw128(b_addr + kk * 2048, BOX_BYTES, 1024)
+                                         : ptx::smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+            ptx::mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit_pair(bar(&ctrl->empty[stage]), 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair(bar(&ctrl->acc_full[acc]), 0x3);
+      }
+      // both CTAs' drain barriers complete once every MMA of the pair has finished
+      ptx::mma_commit_pair(bar(&ctrl->drain), 0x3);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    float* xt = xpose + (warp - 2) * (32 * 33);
+    int local = 0;
+    for (int64_t t = pair; t < total_tiles; t += npairs, ++local) {
+      const TileCoord tc = decode_tile<256>(groups, ng, t);
+      const GemmGroup& G = groups[tc.g];
+      const int acc = local & 1;
+      const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
+      bool ok = true;
+      if (lane == 0) {
+        ok = ptx::mbar_wait_bounded(bar(&ctrl->acc_full[acc]), acc_phase, abort_flag,
+                                    WAIT_LIMIT_NS);
+        if (!ok) signal_timeout(ctrl, status);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+      const int rb = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
+      epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, xt, lane,
+                                   alpha, beta, diag);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(&ctrl->acc_empty[acc]), 0));
+    }
+  }
+
+  // no MMA of the pair may still write this CTA's TMEM when it is freed
+  if (threadIdx.x == 0) {
+    if (!ptx::mbar_wait_bounded(bar(&ctrl->drain), 0u, never_flag, WAIT_LIMIT_NS)) {
+      signal_timeout(ctrl, status);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  // neither CTA leaves while the other may still signal its barriers
+  ptx::cluster_sync();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+// ===================================================================== launchers
+
+template <typename K>
+cudaError_t set_smem_once(K kernel, size_t bytes, std::atomic<uint64_t>& done) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
-  if (!bit || !(attr_done.load() & bit)) {
-    e = cudaFuncSetAttribute(k_ns_gemm<B_MN, FP16, HAS_AUX>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(SMEM_BYTES));
+  if (!bit || !(done.load() & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
     if (e != cudaSuccess) return e;
-    attr_done.fetch_or(bit);
+    done.fetch_or(bit);
   }
+  return cudaSuccess;
+}
+
+template <bool B_MN, bool FP16, bool HAS_AUX>
+cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream) {
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
-  const int64_t grid64 = l.total_tiles < num_sms ? l.total_tiles : num_sms;
-  const int grid = static_cast<int>(grid64);
+  if (l.pair) {
+    static std::atomic<uint64_t> done{0};
+    static std::atomic<int> max_clusters[64];
+    cudaError_t e = set_smem_once(k_ns_gemm_pair<B_MN, FP16, HAS_AUX>, S2_SMEM, done);
+    if (e != cudaSuccess) return e;
+    // as many pairs as can be resident at once (a GPC with an odd number of free SMs
+    // cannot host a cluster of two)
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int resident = (dev >= 0 && dev < 64) ? max_clusters[dev].load() : 0;
+    if (resident <= 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
+      cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = S2_SMEM;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&resident, k_ns_gemm_pair<B_MN, FP16, HAS_AUX>, &cfg) != cudaSuccess ||
+          resident <= 0) {
+        cudaGetLastError();
+        resident = num_sms / 2;
+      }
+      if (dev >= 0 && dev < 64) max_clusters[dev].store(resident);
+    }
+    const int64_t cap = resident < num_sms / 2 ? resident : num_sms / 2;
+    const int64_t pairs = l.total_tiles < cap ? l.total_tiles : cap;
+    if (pairs <= 0) return cudaSuccess;
+    k_ns_gemm_pair<B_MN, FP16, HAS_AUX><<<static_cast<int>(2 * pairs), NUM_THREADS, S2_SMEM, stream>>>(
+        l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag, status);
+    return cudaGetLastError();
+  }
+  static std::atomic<uint64_t> done{0};
+  cudaError_t e = set_smem_once(k_ns_gemm<B_MN, FP16, HAS_AUX>, S1_SMEM, done);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = l.total_tiles < num_sms ? l.total_tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  k_ns_gemm<B_MN, FP16, HAS_AUX><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+  k_ns_gemm<B_MN, FP16, HAS_AUX><<<static_cast<int>(grid), NUM_THREADS, S1_SMEM, stream>>>(
       l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag, status);
   return cudaGetLastError();
 }

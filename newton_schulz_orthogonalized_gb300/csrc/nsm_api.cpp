@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <list>
 #include <map>
@@ -239,6 +240,16 @@ struct Plan {
   }
 };
 
+// The 2-SM kernel is used where it pays; NSM_PAIR_KERNELS=0 in the environment keeps every
+// launch on the 1-CTA kernel (for comparisons).
+bool pair_kernels_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("NSM_PAIR_KERNELS");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 // Device memory a caller provides for a plan's metadata instead of a fresh allocation.
 struct MetaSink {
   char* dptr;
@@ -255,33 +266,46 @@ struct StageSpec {
   bool sym;                            // output symmetric: upper-triangle tiles + mirror
 };
 
-// Tiles (packed mt << 16 | nt) of an m x m output that touch its upper triangle, in the
-// engine's panel raster (panels of 8 column tiles, rows inside a panel).
-std::vector<int32_t> upper_tiles(int m) {
+// Tiles (packed mt << 16 | nt) of an m x m output that touch its upper triangle, for
+// tiles of tile_m rows and 256 columns, in the engine's panel raster (panels of 8 column
+// tiles, rows inside a panel).
+std::vector<int32_t> upper_tiles(int m, int tile_m = 128) {
   std::vector<int32_t> t;
-  const int tm = (m + 127) / 128, tn = (m + 255) / 256;
+  const int tm = (m + tile_m - 1) / tile_m, tn = (m + 255) / 256;
   constexpr int kPanel = 8;
   for (int p0 = 0; p0 < tn; p0 += kPanel)
     for (int mt = 0; mt < tm; ++mt)
       for (int nt = p0; nt < std::min(p0 + kPanel, tn); ++nt)
-        if (std::min(nt * 256 + 255, m - 1) >= mt * 128) t.push_back((mt << 16) | nt);
+        if (std::min(nt * 256 + 255, m - 1) >= mt * tile_m) t.push_back((mt << 16) | nt);
   return t;
 }
 
 // Flops the tensor cores execute for the listed tiles of an m x m x K product.
-double tile_flops(const std::vector<int32_t>& tiles, int m, int K) {
+double tile_flops(const std::vector<int32_t>& tiles, int m, int K, int tile_m = 128) {
   double f = 0;
   for (int32_t p : tiles) {
     const int mt = p >> 16, nt = p & 0xffff;
-    f += 2.0 * K * std::min(128, m - mt * 128) * std::min(256, m - nt * 256);
+    f += 2.0 * K * std::min(tile_m, m - mt * tile_m) * std::min(256, m - nt * 256);
   }
   return f;
+}
+
+// The 2-SM kernel pays off when most of a launch's work has at least 256 rows per tile;
+// matrices with fewer rows would leave half of each pair idle.
+bool prefer_pair(const std::vector<std::pair<int, double>>& rows_and_flops) {
+  double big = 0, all = 0;
+  for (const auto& rf : rows_and_flops) {
+    all += rf.second;
+    if (rf.first >= 256) big += rf.second;
+  }
+  return all > 0 && big >= 0.75 * all;
 }
 
 int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, int method, int steps,
                void* ws, size_t ws_bytes, const MetaSink* sink = nullptr) {
   P.L = make_layout(shapes, n, method, steps);
   const Layout& L = P.L;
+  const bool use_pair_kernels = pair_kernels_enabled();
   for (int i = 0; i < n; ++i) P.elems += int64_t(shapes[2 * i]) * shapes[2 * i + 1];
   P.ws = static_cast<char*>(ws);
   P.x_fp16 = method != NSM_NS_STANDARD_BF16;
@@ -360,14 +384,19 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     P.final_fp16 = true;
   }
 
-  // Upper-triangle tile lists of the m x m products, one per class.
-  std::vector<std::vector<int32_t>> class_tiles(nclass);
-  std::vector<size_t> tiles_off(nclass);
+  // Upper-triangle tile lists of the m x m products, one per class and tile height
+  // (index 0: 128-row tiles of the 1-CTA kernel, 1: 256-row tiles of the pair kernel).
+  std::vector<std::vector<int32_t>> class_tiles[2];
+  std::vector<size_t> tiles_off[2];
   size_t tile_ints = 0;
-  for (int c = 0; c < nclass; ++c) {
-    class_tiles[c] = upper_tiles(L.classes[c].m);
-    tiles_off[c] = tile_ints;
-    tile_ints += class_tiles[c].size();
+  for (int k = 0; k < 2; ++k) {
+    class_tiles[k].resize(nclass);
+    tiles_off[k].resize(nclass);
+    for (int c = 0; c < nclass; ++c) {
+      class_tiles[k][c] = upper_tiles(L.classes[c].m, k ? 256 : 128);
+      tiles_off[k][c] = tile_ints;
+      tile_ints += class_tiles[k][c].size();
+    }
   }
 
   // Device metadata: MatInfo[n] | tensor maps [nclass][nbuf] | GemmGroup arrays | tile lists.
@@ -431,8 +460,10 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   };
 
   int32_t* htiles = reinterpret_cast<int32_t*>(host.data() + tiles_off_bytes);
-  for (int c = 0; c < nclass; ++c) {
-    std::copy(class_tiles[c].begin(), class_tiles[c].end(), htiles + tiles_off[c]);
+  for (int k = 0; k < 2; ++k) {
+    for (int c = 0; c < nclass; ++c) {
+      std::copy(class_tiles[k][c].begin(), class_tiles[k][c].end(), htiles + tiles_off[k][c]);
+    }
   }
   const int32_t* dtiles = reinterpret_cast<const int32_t*>(dbase + tiles_off_bytes);
   GemmGroup* hg = reinterpret_cast<GemmGroup*>(host.data() + groups_off);
@@ -449,6 +480,15 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     GemmGroup* gs = hg + s * nclass;
     int64_t tiles = 0;
     double flops = 0, canonical = 0;
+    std::vector<std::pair<int, double>> rows_and_flops;
+    for (int c = 0; c < nclass; ++c) {
+      const ShapeClass& sc = L.classes[c];
+      const double f = 2.0 * sc.count * double(sc.m) * (st.n_is_n ? sc.n : sc.m) * (st.k_is_n ? sc.n : sc.m);
+      rows_and_flops.push_back({sc.m, f});
+    }
+    const bool pair = use_pair_kernels && prefer_pair(rows_and_flops);
+    const int tile_m = pair ? 256 : 128;
+    const int tk = pair ? 1 : 0;
     for (int j = 0; j < nclass; ++j) {
       const int c = order[j];
       const ShapeClass& sc = L.classes[c];
@@ -469,16 +509,16 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       g.N = st.n_is_n ? sc.n : sc.m;
       g.K = st.k_is_n ? sc.n : sc.m;
       g.count = sc.count;
-      g.tiles_m = (g.M + 127) / 128;
+      g.tiles_m = (g.M + tile_m - 1) / tile_m;
       g.tiles_n = (g.N + 255) / 256;
       g.tile_begin = tiles;
       canonical += 2.0 * g.count * double(g.M) * g.N * g.K;
       if (st.sym) {
         g.sym = 1;
-        g.tile_list = dtiles + tiles_off[c];
-        g.tiles_per_mat = static_cast<int32_t>(class_tiles[c].size());
+        g.tile_list = dtiles + tiles_off[tk][c];
+        g.tiles_per_mat = static_cast<int32_t>(class_tiles[tk][c].size());
         tiles += int64_t(g.count) * g.tiles_per_mat;
-        flops += g.count * tile_flops(class_tiles[c], g.M, g.K);
+        flops += g.count * tile_flops(class_tiles[tk][c], g.M, g.K, tile_m);
       } else {
         tiles += int64_t(g.count) * g.tiles_m * g.tiles_n;
         flops += 2.0 * g.count * double(g.M) * g.N * g.K;
@@ -491,6 +531,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     l.b_mn_major = st.b_mn ? 1 : 0;
     l.has_aux = st.aux_buf >= 0 ? 1 : 0;
     l.fp16 = P.x_fp16 ? 1 : 0;
+    l.pair = pair ? 1 : 0;
     l.total_tiles = tiles;
     l.alpha = st.alpha;
     l.beta = st.beta;
@@ -976,8 +1017,11 @@ int adamw_step(const void* grads, float* params, float* exp_avg, float* exp_avg_
 }
 
 int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo, const void* aux, int ldx, int M,
-             int N, int K, int b_mn_major, int fp16, int symmetric, float alpha, float beta, float diag,
+             int N, int K, int b_mn_major, int fp16, int flags, float alpha, float beta, float diag,
              void* scratch, size_t scratch_bytes, nsm_stream_t stream_) {
+  const bool symmetric = (flags & NSM_GEMM_SYMMETRIC) != 0;
+  const bool pair = (flags & NSM_GEMM_PAIR) != 0;
+  const int tile_m = pair ? 256 : 128;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (!a || !b || !out || !scratch) return fail(NSM_ERR_NULL, "a, b, out and scratch must be non-NULL");
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
@@ -991,8 +1035,8 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
     return fail(NSM_ERR_ALIGN, "pointers must be 16-byte aligned");
   if (!aligned(scratch, 128)) return fail(NSM_ERR_ALIGN, "scratch must be 128-byte aligned");
   if (symmetric && M != N) return fail(NSM_ERR_SHAPE, "a symmetric output needs M == N");
-  const std::vector<int32_t> sym_tiles = symmetric ? upper_tiles(M) : std::vector<int32_t>();
-  const size_t need = nsm_gemm_scratch_bytes(M, N, symmetric);
+  const std::vector<int32_t> sym_tiles = symmetric ? upper_tiles(M, tile_m) : std::vector<int32_t>();
+  const size_t need = nsm_gemm_scratch_bytes(M, N, flags);
   if (scratch_bytes < need) return fail(NSM_ERR_WORKSPACE, "scratch needs %zu bytes", need);
   if (aux && ranges_overlap(aux, size_t(M) * ldx * 2, out, size_t(M) * ldo * 2))
     return fail(NSM_ERR_ARG, "aux must not overlap out");
@@ -1020,7 +1064,7 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   g.N = N;
   g.K = K;
   g.count = 1;
-  g.tiles_m = (M + 127) / 128;
+  g.tiles_m = (M + tile_m - 1) / tile_m;
   g.tiles_n = (N + 255) / 256;
   g.tile_begin = 0;
   std::vector<uint8_t> host(sizeof(Blob) + sym_tiles.size() * sizeof(int32_t));
@@ -1040,12 +1084,13 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   l.b_mn_major = b_mn_major ? 1 : 0;
   l.has_aux = aux ? 1 : 0;
   l.fp16 = fp16 ? 1 : 0;
+  l.pair = pair ? 1 : 0;
   l.total_tiles = symmetric ? int64_t(sym_tiles.size()) : int64_t(g.tiles_m) * g.tiles_n;
   l.alpha = alpha;
   l.beta = aux ? beta : 0.f;
   l.diag = diag;
   l.canonical_flops = 2.0 * M * double(N) * K;
-  l.flops = symmetric ? tile_flops(sym_tiles, M, K) : l.canonical_flops;
+  l.flops = symmetric ? tile_flops(sym_tiles, M, K, tile_m) : l.canonical_flops;
   int dev = 0, num_sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1059,9 +1104,10 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   return NSM_OK;
 }
 
-size_t nsm_gemm_scratch_bytes(int M, int N, int symmetric) {
+size_t nsm_gemm_scratch_bytes(int M, int N, int flags) {
   size_t b = 2 * sizeof(CUtensorMap) + sizeof(GemmGroup);
-  if (symmetric && M > 0 && M == N) b += upper_tiles(M).size() * sizeof(int32_t);
+  if ((flags & NSM_GEMM_SYMMETRIC) && M > 0 && M == N)
+    b += upper_tiles(M, (flags & NSM_GEMM_PAIR) ? 256 : 128).size() * sizeof(int32_t);
   return align_up(b, 128);
 }
 

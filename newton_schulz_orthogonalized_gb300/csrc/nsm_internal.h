@@ -62,6 +62,7 @@ struct GemmLaunch {
   int32_t b_mn_major;       // 1: B operand is K x N with N contiguous
   int32_t has_aux;
   int32_t fp16;             // 1: operands/outputs are fp16, else bf16
+  int32_t pair;             // 1: 2-SM kernel on 256 x 256 tiles (groups laid out for it)
   int64_t total_tiles;
   float alpha, beta, diag;
   double flops;             // flops the tensor cores execute (whole tiles)

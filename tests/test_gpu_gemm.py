@@ -58,16 +58,17 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("pair", [False, True])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("M,N,K,b_mn,use_aux,diag", CASES)
-def test_gemm_variants(nsm, dtype, M, N, K, b_mn, use_aux, diag):
+def test_gemm_variants(nsm, dtype, M, N, K, b_mn, use_aux, diag, pair):
     seed = M * 7 + N * 3 + K
     a = _rand((M, K), dtype, seed)
     b = _rand((K, N) if b_mn else (N, K), dtype, seed + 1)
     aux = _rand((M, N), dtype, seed + 2) if use_aux else None
     out = torch.full((M, (N + 7) // 8 * 8), float("nan"), dtype=dtype, device="cuda")[:, :N]
     alpha, beta = 0.75, -1.25
-    nsm.gemm(a, b, out, aux, b_mn, alpha, beta, diag)
+    nsm.gemm(a, b, out, aux, b_mn, alpha, beta, diag, pair=pair)
     assert nsm.device_status() == nsm.NSM_OK
     ref = _ref(a, b, aux, b_mn, alpha, beta if use_aux else 0.0, diag)
     got = out.double().cpu().numpy()
@@ -93,14 +94,28 @@ def test_gemm_padded_leading_dimension(nsm):
     assert torch.count_nonzero(out_full[:, N:]).item() == 0
 
 
-def test_gemm_deterministic(nsm):
+@pytest.mark.parametrize("pair", [False, True])
+def test_gemm_deterministic(nsm, pair):
     a = _rand((512, 2048), torch.bfloat16, 5)
     o1 = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
     o2 = torch.empty_like(o1)
-    nsm.gemm(a, a, o1)
-    nsm.gemm(a, a, o2)
+    nsm.gemm(a, a, o1, pair=pair)
+    nsm.gemm(a, a, o2, pair=pair)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
+
+
+def test_gemm_pair_matches_single_cta(nsm):
+    # the two kernels accumulate each output in the same K order: results are identical
+    a = _rand((768, 1536), torch.float16, 8)
+    b = _rand((1024, 1536), torch.float16, 9)
+    o1 = torch.empty((768, 1024), dtype=torch.float16, device="cuda")
+    o2 = torch.empty_like(o1)
+    nsm.gemm(a, b, o1, pair=False)
+    nsm.gemm(a, b, o2, pair=True)
+    torch.cuda.synchronize()
+    rel = (o1.double() - o2.double()).norm() / o1.double().norm()
+    assert rel.item() <= 1e-3
 
 
 def test_gemm_rejects_bad_arguments(nsm):
@@ -115,10 +130,11 @@ def test_gemm_rejects_bad_arguments(nsm):
 SYM_CASES = [(128, 64), (200, 72), (256, 256), (384, 1024), (1000, 136), (64, 64), (3, 8), (520, 4096)]
 
 
+@pytest.mark.parametrize("pair", [False, True])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("M,K", SYM_CASES)
 @pytest.mark.parametrize("use_aux", [False, True])
-def test_gemm_symmetric_output(nsm, dtype, M, K, use_aux):
+def test_gemm_symmetric_output(nsm, dtype, M, K, use_aux, pair):
     # A A^T (+ beta S + diag I with S symmetric) computed on the upper-triangle tiles only
     seed = M * 11 + K
     a = _rand((M, K), dtype, seed)
@@ -133,7 +149,7 @@ def test_gemm_symmetric_output(nsm, dtype, M, K, use_aux):
     out_full = torch.full((M, ld + 8), float("nan"), dtype=dtype, device="cuda")
     out = out_full[:, :M]
     alpha, beta, diag = 0.5, -1.5, (2.0 if use_aux else 0.0)
-    nsm.gemm(a, a, out, aux, False, alpha, beta, diag, symmetric=True)
+    nsm.gemm(a, a, out, aux, False, alpha, beta, diag, symmetric=True, pair=pair)
     assert nsm.device_status() == nsm.NSM_OK
     got = out.double().cpu().numpy()
     assert np.all(np.isfinite(got))
