@@ -313,8 +313,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int kblocks = (G.K + BK - 1) / BK;
         const int n_len = min(BN, G.N - tc.n0);
         const int nb = (n_len + 63) >> 6;
-        const int a_boxes = (G.M - tc.m0 > 64) ? 2 : 1;
-        const uint32_t bytes = static_cast<uint32_t>((a_boxes + nb) * BOX_BYTES);
+        // A: one box of a_box >= 128 rows, or 64-row boxes for the rows in range; B likewise
+        // (MN-major B: 64-column boxes of 64 K rows)
+        const int a_loads = G.a_box >= 128 ? 1 : ((G.M - tc.m0 > 64) ? 2 : 1);
+        const int a_rows = G.a_box >= 128 ? G.a_box : 64;
+        const int b_loads = (!B_MN && G.b_box >= 256) ? 1 : nb;
+        const int b_rows = (!B_MN && G.b_box >= 256) ? G.b_box : 64;
+        const uint32_t bytes = static_cast<uint32_t>((a_loads * a_rows + b_loads * b_rows) * 128);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait_bounded(bar(&ctrl->empty[stage]), phase ^ 1u, abort_flag,
                                       WAIT_LIMIT_NS)) {
@@ -327,9 +332,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t a_dst = ring + stage * S1_STAGE_BYTES;
           const uint32_t b_dst = a_dst + S1_A_BYTES;
           const int k0 = kb * BK;
-          ptx::tma_load_3d(a_dst, G.map_a, fb, k0, tc.m0, tc.b);
-          if (a_boxes == 2) ptx::tma_load_3d(a_dst + BOX_BYTES, G.map_a, fb, k0, tc.m0 + 64, tc.b);
-          for (int q = 0; q < nb; ++q) {
+          for (int q = 0; q < a_loads; ++q) {
+            ptx::tma_load_3d(a_dst + q * BOX_BYTES, G.map_a, fb, k0, tc.m0 + 64 * q, tc.b);
+          }
+          for (int q = 0; q < b_loads; ++q) {
             if (B_MN) {
               ptx::tma_load_3d(b_dst + q * BOX_BYTES, G.map_b, fb, tc.n0 + 64 * q, k0, tc.b);
             } else {
@@ -527,8 +533,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         // boxes each CTA loads; the leader expects both CTAs' bytes
         const int a0 = boxes_in(tc.m0, G.M), a1 = boxes_in(tc.m0 + 128, G.M);
         const int b0 = boxes_in(tc.n0, G.N), b1 = boxes_in(tc.n0 + 128, G.N);
-        const int my_a = rank ? a1 : a0, my_b = rank ? b1 : b0;
-        const uint32_t total_bytes = static_cast<uint32_t>((a0 + a1 + b0 + b1) * BOX_BYTES);
+        // a half with any row in range loads one box of a_box (b_box) rows when the map's box
+        // covers the half, otherwise one 64-row box per 64 rows in range
+        auto loads = [](int units, int box) { return box >= 128 ? (units ? 1 : 0) : units; };
+        auto rows = [](int box) { return box >= 128 ? box : 64; };
+        const int bbox = B_MN ? 64 : G.b_box;
+        const int my_a = loads(rank ? a1 : a0, G.a_box), my_b = loads(rank ? b1 : b0, bbox);
+        const uint32_t total_bytes = static_cast<uint32_t>(
+            ((loads(a0, G.a_box) + loads(a1, G.a_box)) * rows(G.a_box) +
+             (loads(b0, bbox) + loads(b1, bbox)) * rows(bbox)) * 128);
         const int row0 = tc.m0 + 128 * static_cast<int>(rank);
         const int col0 = tc.n0 + 128 * static_cast<int>(rank);
         for (int kb = 0; kb < kblocks; ++kb) {

@@ -196,9 +196,9 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // 3D map over `count` back-to-back row-major matrices of rows x inner (row stride ld),
-// box 64 x 64 x 1, 128-byte swizzle, zero fill outside the matrix.
+// box 64 x box_rows x 1, 128-byte swizzle, zero fill outside the matrix.
 int encode_map(CUtensorMap* map, void* base, bool fp16, int inner, int rows, int ld, int count,
-               const char* ws_begin, const char* ws_end) {
+               const char* ws_begin, const char* ws_end, int box_rows = 64) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return fail(NSM_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const size_t row_bytes = size_t(ld) * 2;
@@ -209,7 +209,7 @@ int encode_map(CUtensorMap* map, void* base, bool fp16, int inner, int rows, int
     return fail(NSM_ERR_WORKSPACE, "internal: tensor map exceeds the workspace");
   cuuint64_t dims[3] = {cuuint64_t(inner), cuuint64_t(rows), cuuint64_t(count)};
   cuuint64_t strides[2] = {cuuint64_t(row_bytes), cuuint64_t(mat_bytes)};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -402,7 +402,8 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   // Device metadata: MatInfo[n] | tensor maps [nclass][nbuf] | GemmGroup arrays | tile lists.
   const size_t mats_bytes = align_up(sizeof(MatInfo) * n, 128);
   const size_t maps_off = mats_bytes;
-  const size_t maps_bytes = align_up(sizeof(CUtensorMap) * size_t(nclass) * nbuf, 128);
+  constexpr int kBoxKinds = 3;  // box heights 64, 128, 256 rows
+  const size_t maps_bytes = align_up(sizeof(CUtensorMap) * size_t(nclass) * nbuf * kBoxKinds, 128);
   const size_t groups_off = maps_off + maps_bytes;
   const size_t groups_bytes = align_up(sizeof(GemmGroup) * size_t(nclass) * stages.size(), 128);
   const size_t tiles_off_bytes = groups_off + groups_bytes;
@@ -448,15 +449,20 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   for (int c = 0; c < nclass; ++c) {
     const ShapeClass& sc = L.classes[c];
     for (int b = 0; b < nbuf; ++b) {
-      CUtensorMap* map = &hmaps[size_t(c) * nbuf + b];
-      int rc;
-      if (b < MM0) rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.n, sc.m, sc.ldn, sc.count, ws_begin, ws_end);
-      else rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.m, sc.m, sc.ldm, sc.count, ws_begin, ws_end);
-      if (rc != NSM_OK) return rc;
+      for (int k = 0; k < kBoxKinds; ++k) {
+        CUtensorMap* map = &hmaps[(size_t(c) * nbuf + b) * kBoxKinds + k];
+        const int box = 64 << k;
+        int rc;
+        if (b < MM0) rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.n, sc.m, sc.ldn, sc.count, ws_begin, ws_end, box);
+        else rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.m, sc.m, sc.ldm, sc.count, ws_begin, ws_end, box);
+        if (rc != NSM_OK) return rc;
+      }
     }
   }
-  auto dmap = [&](int c, int b) {
-    return reinterpret_cast<const CUtensorMap*>(dbase + maps_off) + size_t(c) * nbuf + b;
+  // map of buffer b of class c with boxes of `box` rows
+  auto dmap = [&](int c, int b, int box) {
+    const int k = box >= 256 ? 2 : (box >= 128 ? 1 : 0);
+    return reinterpret_cast<const CUtensorMap*>(dbase + maps_off) + (size_t(c) * nbuf + b) * kBoxKinds + k;
   };
 
   int32_t* htiles = reinterpret_cast<int32_t*>(host.data() + tiles_off_bytes);
@@ -493,8 +499,12 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       const int c = order[j];
       const ShapeClass& sc = L.classes[c];
       GemmGroup g{};
-      g.map_a = dmap(c, st.a_buf);
-      g.map_b = dmap(c, st.b_buf);
+      // the largest boxes each kernel can use: A halves and K-major B halves of 128 rows
+      // (pair) or A 128 rows and K-major B 256 rows (1-CTA); MN-major B in 64 x 64 boxes
+      g.a_box = 128;
+      g.b_box = st.b_mn ? 64 : (pair ? 128 : 256);
+      g.map_a = dmap(c, st.a_buf, g.a_box);
+      g.map_b = dmap(c, st.b_buf, g.b_box);
       const bool out_x = st.out_buf < MM0;
       g.out = buf_base(st.out_buf, c);
       g.ld_out = out_x ? sc.ldn : sc.ldm;
@@ -1047,10 +1057,12 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   static_assert(sizeof(Blob) <= 1024, "scratch blob");
   Blob blob;
   std::memset(&blob, 0, sizeof(blob));
-  int rc = encode_map(&blob.ma, const_cast<void*>(a), fp16 != 0, K, M, lda, 1, nullptr, nullptr);
+  const int a_box = 128;
+  const int b_box = b_mn_major ? 64 : (pair ? 128 : 256);
+  int rc = encode_map(&blob.ma, const_cast<void*>(a), fp16 != 0, K, M, lda, 1, nullptr, nullptr, a_box);
   if (rc != NSM_OK) return rc;
-  if (b_mn_major) rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, N, K, ldb, 1, nullptr, nullptr);
-  else rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, K, N, ldb, 1, nullptr, nullptr);
+  if (b_mn_major) rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, N, K, ldb, 1, nullptr, nullptr, b_box);
+  else rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, K, N, ldb, 1, nullptr, nullptr, b_box);
   if (rc != NSM_OK) return rc;
   Blob* d = static_cast<Blob*>(scratch);
   GemmGroup& g = blob.g;
@@ -1067,6 +1079,8 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   g.tiles_m = (M + tile_m - 1) / tile_m;
   g.tiles_n = (N + 255) / 256;
   g.tile_begin = 0;
+  g.a_box = a_box;
+  g.b_box = b_box;
   std::vector<uint8_t> host(sizeof(Blob) + sym_tiles.size() * sizeof(int32_t));
   if (symmetric) {
     g.sym = 1;

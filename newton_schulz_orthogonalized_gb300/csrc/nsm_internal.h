@@ -52,7 +52,7 @@ struct GemmGroup {
   int32_t count;
   int32_t tiles_m, tiles_n;
   int32_t sym, tiles_per_mat;
-  int32_t pad0, pad1;
+  int32_t a_box, b_box;  // rows per TMA box of map_a / map_b (64, 128 or 256)
 };
 static_assert(sizeof(GemmGroup) == 112, "GemmGroup layout");
 
