@@ -61,11 +61,12 @@ constexpr int S1_STAGES = 4;
 constexpr int S1_A_BYTES = 128 * BK * 2;
 constexpr int S1_STAGE_BYTES = S1_A_BYTES + BN * BK * 2;
 
-// pair kernel: 256 x 256 tiles, each CTA stages A 128 x 64 and half of B (128 x 64):
-// 6 stages of 32 KB.
-constexpr int S2_STAGES = 6;
-constexpr int S2_A_BYTES = 128 * BK * 2;
-constexpr int S2_STAGE_BYTES = S2_A_BYTES + 128 * BK * 2;
+// pair kernel: 256 x 256 tiles, K 128 per stage; each CTA stages A 128 x 128 and half of
+// B (128 x 128) as two 128-byte-wide K boxes each: 3 stages of 64 KB.
+constexpr int BK2 = 128;
+constexpr int S2_STAGES = 3;
+constexpr int S2_A_BYTES = 128 * BK2 * 2;
+constexpr int S2_STAGE_BYTES = S2_A_BYTES + 128 * BK2 * 2;
 
 template <int STAGES>
 struct Ctrl {
@@ -529,19 +530,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       for (int64_t t = pair; t < total_tiles && ok; t += npairs) {
         const TileCoord tc = decode_tile<256>(groups, ng, t);
         const GemmGroup& G = groups[tc.g];
-        const int kblocks = (G.K + BK - 1) / BK;
+        const int kblocks = (G.K + BK2 - 1) / BK2;
         // boxes each CTA loads; the leader expects both CTAs' bytes
         const int a0 = boxes_in(tc.m0, G.M), a1 = boxes_in(tc.m0 + 128, G.M);
         const int b0 = boxes_in(tc.n0, G.N), b1 = boxes_in(tc.n0 + 128, G.N);
-        // a half with any row in range loads one box of a_box (b_box) rows when the map's box
-        // covers the half, otherwise one 64-row box per 64 rows in range
+        // Per 64-wide K box, a K-major half with any row in range loads one box of 128 rows
+        // (a_box / b_box >= 128) or one 64-row box per 64 rows in range.  An MN-major B half
+        // loads one box per 64 columns in range, each holding the stage's K rows (b_box =
+        // 128 K rows, or 64 with one box per K box).
         auto loads = [](int units, int box) { return box >= 128 ? (units ? 1 : 0) : units; };
         auto rows = [](int box) { return box >= 128 ? box : 64; };
-        const int bbox = B_MN ? 64 : G.b_box;
-        const int my_a = loads(rank ? a1 : a0, G.a_box), my_b = loads(rank ? b1 : b0, bbox);
-        const uint32_t total_bytes = static_cast<uint32_t>(
-            ((loads(a0, G.a_box) + loads(a1, G.a_box)) * rows(G.a_box) +
-             (loads(b0, bbox) + loads(b1, bbox)) * rows(bbox)) * 128);
+        const int my_a = loads(rank ? a1 : a0, G.a_box);
+        const int my_b = B_MN ? (rank ? b1 : b0) : loads(rank ? b1 : b0, G.b_box);
+        const uint32_t a_bytes_k = static_cast<uint32_t>((loads(a0, G.a_box) + loads(a1, G.a_box)) * rows(G.a_box) * 128);
+        const uint32_t b_bytes_k = static_cast<uint32_t>(
+            B_MN ? (b0 + b1) * 64 * 128 : (loads(b0, G.b_box) + loads(b1, G.b_box)) * rows(G.b_box) * 128);
         const int row0 = tc.m0 + 128 * static_cast<int>(rank);
         const int col0 = tc.n0 + 128 * static_cast<int>(rank);
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -553,18 +556,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
           const uint32_t fb_local = bar(&ctrl->full[stage]);
           const uint32_t fb_leader = ptx::mapa_shared(fb_local, 0);
-          if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, total_bytes);
+          const int k0 = kb * BK2;
+          const int nk = (G.K - k0 > 64) ? 2 : 1;  // 64-wide K boxes holding any K in range
+          // MN-major B boxes with 128 K rows load both K boxes at once
+          const int b_k_loads = (B_MN && G.b_box >= 128) ? 1 : nk;
+          const uint32_t bytes = a_bytes_k * nk + (B_MN && G.b_box >= 128 ? 2 * b_bytes_k : b_bytes_k * nk);
+          if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, bytes);
+          // stage layout: A [K box][128 rows]; K-major B [K box][128 rows];
+          // MN-major B [64-column block][128 K rows]
           const uint32_t a_dst = ring + stage * S2_STAGE_BYTES;
           const uint32_t b_dst = a_dst + S2_A_BYTES;
-          const int k0 = kb * BK;
-          for (int q = 0; q < my_a; ++q) {
-            ptx::tma_load_3d_pair(a_dst + q * BOX_BYTES, G.map_a, fb_leader, k0, row0 + 64 * q, tc.b);
+          for (int kq = 0; kq < nk; ++kq) {
+            for (int q = 0; q < my_a; ++q) {
+              ptx::tma_load_3d_pair(a_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, G.map_a, fb_leader,
+                                    k0 + 64 * kq, row0 + 64 * q, tc.b);
+            }
+            if (!B_MN) {
+              for (int q = 0; q < my_b; ++q) {
+                ptx::tma_load_3d_pair(b_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, G.map_b, fb_leader,
+                                      k0 + 64 * kq, col0 + 64 * q, tc.b);
+              }
+            }
           }
-          for (int q = 0; q < my_b; ++q) {
-            if (B_MN) {
-              ptx::tma_load_3d_pair(b_dst + q * BOX_BYTES, G.map_b, fb_leader, col0 + 64 * q, k0, tc.b);
-            } else {
-              ptx::tma_load_3d_pair(b_dst + q * BOX_BYTES, G.map_b, fb_leader, k0, col0 + 64 * q, tc.b);
+          if (B_MN) {
+            for (int kq = 0; kq < b_k_loads; ++kq) {
+              for (int q = 0; q < my_b; ++q) {
+                ptx::tma_load_3d_pair(b_dst + q * 2 * BOX_BYTES + kq * BOX_BYTES, G.map_b, fb_leader,
+                                      col0 + 64 * q, k0 + 64 * kq, tc.b);
+              }
             }
           }
           fill_parity[stage] = static_cast<int>(phase);
@@ -603,7 +622,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       for (int64_t t = pair; t < total_tiles && ok; t += npairs, ++local) {
         const TileCoord tc = decode_tile<256>(groups, ng, t);
         const GemmGroup& G = groups[tc.g];
-        const int kblocks = (G.K + BK - 1) / BK;
+        const int kblocks = (G.K + BK2 - 1) / BK2;
         const int acc = local & 1;
         const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
         if (!ptx::mbar_wait_bounded(bar(&ctrl->acc_empty[acc]), acc_phase ^ 1u, abort_flag,
@@ -624,11 +643,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           ptx::tc_fence_after();
           const uint32_t a_addr = ring + stage * S2_STAGE_BYTES;
           const uint32_t b_addr = a_addr + S2_A_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t a_desc = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t b_desc = B_MN ? ptx::smem_desc_sw128(b_addr + kk * 2048, BOX_BYTES, 1024)
-                                         : ptx::smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+          // K slices of 16 in range (the last stage may hold fewer than 8)
+          const int left = G.K - kb * BK2;
+          const int nslices = left >= BK2 ? BK2 / 16 : (left + 15) / 16;
+          for (int kk = 0; kk < nslices; ++kk) {
+            const uint32_t koff = static_cast<uint32_t>((kk >> 2) * 2 * BOX_BYTES + (kk & 3) * 32);
+            const uint64_t a_desc = ptx::smem_desc_sw128(a_addr + koff, 16, 1024);
+            const uint64_t b_desc = B_MN ? ptx::smem_desc_sw128(b_addr + kk * 2048, 2 * BOX_BYTES, 1024)
+                                         : ptx::smem_desc_sw128(b_addr + koff, 16, 1024);
             ptx::mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit_pair(bar(&ctrl->empty[stage]), 0x3);

@@ -502,7 +502,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       // the largest boxes each kernel can use: A halves and K-major B halves of 128 rows
       // (pair) or A 128 rows and K-major B 256 rows (1-CTA); MN-major B in 64 x 64 boxes
       g.a_box = 128;
-      g.b_box = st.b_mn ? 64 : (pair ? 128 : 256);
+      g.b_box = st.b_mn ? (pair ? 128 : 64) : (pair ? 128 : 256);
       g.map_a = dmap(c, st.a_buf, g.a_box);
       g.map_b = dmap(c, st.b_buf, g.b_box);
       const bool out_x = st.out_buf < MM0;
@@ -1058,7 +1058,7 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   Blob blob;
   std::memset(&blob, 0, sizeof(blob));
   const int a_box = 128;
-  const int b_box = b_mn_major ? 64 : (pair ? 128 : 256);
+  const int b_box = b_mn_major ? (pair ? 128 : 64) : (pair ? 128 : 256);
   int rc = encode_map(&blob.ma, const_cast<void*>(a), fp16 != 0, K, M, lda, 1, nullptr, nullptr, a_box);
   if (rc != NSM_OK) return rc;
   if (b_mn_major) rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, N, K, ldb, 1, nullptr, nullptr, b_box);
