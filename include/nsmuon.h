@@ -118,6 +118,17 @@ int muon_step(const void* packed_grads, float* packed_params, float* momentum,
               float lr, float wd, float mu, int ns_method, int ns_steps, int nesterov,
               void* workspace, size_t workspace_bytes, nsm_stream_t stream);
 
+/* muon_step that also writes the bf16 copy of every updated parameter into
+ * params_bf16 (device, bf16, same offsets; NULL behaves like muon_step).  That copy is the
+ * buffer an owner broadcasts to the other ranks and the next forward pass reads
+ * ([DMZ] §两种packed buffer生命周期: the owner keeps the authoritative copy and broadcasts
+ * the packed buffer); it is fused into the apply pass (2 more bytes per element).  It
+ * must be 16-byte aligned and not overlap the other buffers. */
+int muon_step_with_copy(const void* packed_grads, float* packed_params, float* momentum,
+                        void* params_bf16, const int64_t* offsets, const int32_t* shapes, int n,
+                        float lr, float wd, float mu, int ns_method, int ns_steps, int nesterov,
+                        void* workspace, size_t workspace_bytes, nsm_stream_t stream);
+
 /* Orthogonalisation only: out_i = NS(in_i / (||in_i||_F + 1e-7)) for every matrix of a
  * packed bf16 group (the same transpose rule and methods as muon_step).  in_bf16 and
  * out_bf16 are device bf16 buffers sharing the offsets table; they may not overlap.

@@ -80,6 +80,10 @@ def lib() -> ctypes.CDLL:
                             ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                             ctypes.c_int, _vp, ctypes.c_size_t, _vp]
     L.muon_step.restype = ctypes.c_int
+    L.muon_step_with_copy.argtypes = [_vp, _vp, _vp, _vp, _c_i64p, _c_i32p, ctypes.c_int,
+                                      ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+    L.muon_step_with_copy.restype = ctypes.c_int
     L.muon_orthogonalize.argtypes = [_vp, _vp, _c_i64p, _c_i32p, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, _vp, ctypes.c_size_t, _vp]
     L.muon_orthogonalize.restype = ctypes.c_int
@@ -231,15 +235,18 @@ def _stream_ptr(stream) -> int:
 def muon_step(grads, params, momentum, offsets, shapes, lr: float = MUON_LR_DEFAULT,
               wd: float = 0.0, mu: float = MUON_MOMENTUM_DEFAULT,
               ns_method=NS_METHOD_DEFAULT, ns_steps: int = NS_STEPS_DEFAULT,
-              nesterov: bool = True, workspace=None, stream=None) -> None:
-    """One owner-side Muon step on packed buffers (bf16 grads, fp32 params/momentum)."""
+              nesterov: bool = True, workspace=None, stream=None, params_bf16=None) -> None:
+    """One owner-side Muon step on packed buffers (bf16 grads, fp32 params/momentum).
+
+    With ``params_bf16`` (a bf16 buffer of the same length) the step also writes the bf16
+    copy of the updated parameters, the buffer an owner broadcasts."""
     s = _shapes_array(shapes)
     o = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
     ws_size = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().muon_step(_ptr(grads), _ptr(params), _ptr(momentum), _i64p(o), _i32p(s),
-                           s.shape[0], float(lr), float(wd), float(mu), method_code(ns_method),
-                           int(ns_steps), 1 if nesterov else 0, _ptr(workspace), ws_size,
-                           _stream_ptr(stream)))
+    _check(lib().muon_step_with_copy(_ptr(grads), _ptr(params), _ptr(momentum), _ptr(params_bf16),
+                                     _i64p(o), _i32p(s), s.shape[0], float(lr), float(wd), float(mu),
+                                     method_code(ns_method), int(ns_steps), 1 if nesterov else 0,
+                                     _ptr(workspace), ws_size, _stream_ptr(stream)))
 
 
 def muon_orthogonalize(inp, out, offsets, shapes, ns_method=NS_METHOD_DEFAULT,

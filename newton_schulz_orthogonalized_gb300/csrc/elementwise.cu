@@ -308,7 +308,8 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// Slot O -> natural layout.  APPLY: p <- p*decay - lr*scale*O.  Otherwise out = bf16(O).
+// Slot O -> natural layout.  APPLY: p <- p*decay - lr*scale*O, and out = bf16(p) when out is
+// not NULL (the parameters' bf16 copy).  Otherwise out = bf16(O).
 template <bool O_FP16, bool APPLY>
 __global__ void __launch_bounds__(kThreads)
     k_from_class(const void* __restrict__ o, float* __restrict__ params,
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t s0 = mt.slot;
     const float coef = lr * mt.scale;
     float* p = APPLY ? params + mt.off : nullptr;
-    __nv_bfloat16* ob = APPLY ? nullptr : out + mt.off;
+    __nv_bfloat16* ob = out ? out + mt.off : nullptr;
     if (mt.transposed) {
       // tile[rr][cc] = O^T[r0+rr][c0+cc] = slot[c0+cc][r0+rr]
       if (mt.vec_ok) {
@@ -369,6 +370,10 @@ __global__ void __launch_bounds__(kThreads)
             b.w = fmaf(-coef, f[7], b.w * decay);
             pp[0] = a;
             pp[1] = b;
+            if (ob) {
+              const float np[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+              *reinterpret_cast<uint4*>(ob + i) = pack_bf16x8(np);
+            }
           } else {
             *reinterpret_cast<uint4*>(ob + i) = pack_bf16x8(f);
           }
@@ -382,8 +387,13 @@ __global__ void __launch_bounds__(kThreads)
           const float ov = mt.transposed ? tile[rr][cc]
                                          : load_half<O_FP16>(o, s0 + static_cast<int64_t>(r) * ld + c);
           const int64_t i = static_cast<int64_t>(r) * cols + c;
-          if (APPLY) p[i] = fmaf(-coef, ov, p[i] * decay);
-          else ob[i] = __float2bfloat16_rn(ov);
+          if (APPLY) {
+            const float np = fmaf(-coef, ov, p[i] * decay);
+            p[i] = np;
+            if (ob) ob[i] = __float2bfloat16_rn(np);
+          } else {
+            ob[i] = __float2bfloat16_rn(ov);
+          }
         }
       }
     }
@@ -506,15 +516,16 @@ cudaError_t launch_to_class(const void* grads, const float* momentum, int has_mo
   return cudaGetLastError();
 }
 
-cudaError_t launch_apply(const void* o, int o_fp16, float* params, const MatInfo* mats,
-                         int nmats, int64_t total_tiles, float lr, float wd,
+cudaError_t launch_apply(const void* o, int o_fp16, float* params, void* params_bf16,
+                         const MatInfo* mats, int nmats, int64_t total_tiles, float lr, float wd,
                          cudaStream_t stream) {
   const int grid = grid_for(total_tiles, 8);
   const float decay = 1.0f - lr * wd;
+  auto* pb = reinterpret_cast<__nv_bfloat16*>(params_bf16);
   if (o_fp16) {
-    k_from_class<true, true><<<grid, kThreads, 0, stream>>>(o, params, nullptr, mats, nmats, total_tiles, lr, decay);
+    k_from_class<true, true><<<grid, kThreads, 0, stream>>>(o, params, pb, mats, nmats, total_tiles, lr, decay);
   } else {
-    k_from_class<false, true><<<grid, kThreads, 0, stream>>>(o, params, nullptr, mats, nmats, total_tiles, lr, decay);
+    k_from_class<false, true><<<grid, kThreads, 0, stream>>>(o, params, pb, mats, nmats, total_tiles, lr, decay);
   }
   return cudaGetLastError();
 }

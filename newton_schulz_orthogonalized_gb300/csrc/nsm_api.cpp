@@ -873,6 +873,14 @@ size_t muon_workspace_bytes(const int32_t* shapes, int n, int ns_method, int ns_
 int muon_step(const void* packed_grads, float* packed_params, float* momentum, const int64_t* offsets,
               const int32_t* shapes, int n, float lr, float wd, float mu, int ns_method, int ns_steps,
               int nesterov, void* workspace, size_t workspace_bytes, nsm_stream_t stream_) {
+  return muon_step_with_copy(packed_grads, packed_params, momentum, nullptr, offsets, shapes, n, lr, wd, mu,
+                             ns_method, ns_steps, nesterov, workspace, workspace_bytes, stream_);
+}
+
+int muon_step_with_copy(const void* packed_grads, float* packed_params, float* momentum, void* params_bf16,
+                        const int64_t* offsets, const int32_t* shapes, int n, float lr, float wd, float mu,
+                        int ns_method, int ns_steps, int nesterov, void* workspace, size_t workspace_bytes,
+                        nsm_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (!packed_grads || !packed_params || !momentum) return fail(NSM_ERR_NULL, "a device buffer is NULL");
   int rc = validate_shapes(shapes, n);
@@ -890,6 +898,13 @@ int muon_step(const void* packed_grads, float* packed_params, float* momentum, c
       ranges_overlap(packed_grads, size_t(extent) * 2, momentum, size_t(extent) * 4) ||
       ranges_overlap(packed_params, size_t(extent) * 4, momentum, size_t(extent) * 4))
     return fail(NSM_ERR_ARG, "grads, params and momentum must not overlap");
+  if (params_bf16) {
+    if (!aligned(params_bf16, 16)) return fail(NSM_ERR_ALIGN, "the bf16 copy must be 16-byte aligned");
+    if (ranges_overlap(params_bf16, size_t(extent) * 2, packed_grads, size_t(extent) * 2) ||
+        ranges_overlap(params_bf16, size_t(extent) * 2, packed_params, size_t(extent) * 4) ||
+        ranges_overlap(params_bf16, size_t(extent) * 2, momentum, size_t(extent) * 4))
+      return fail(NSM_ERR_ARG, "the bf16 copy must not overlap grads, params or momentum");
+  }
   const Layout L = make_layout(shapes, n, ns_method, ns_steps);
   rc = check_workspace(workspace, workspace_bytes, L.bytes);
   if (rc != NSM_OK) return rc;
@@ -925,9 +940,9 @@ int muon_step(const void* packed_grads, float* packed_params, float* momentum, c
   rc = run_chain(*P, stream, &launches);
   if (rc != NSM_OK) return rc;
   {
-    TimedLaunch t(stream, NSM_KIND_APPLY, 10.0 * elems);
-    e = launch_apply(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, packed_params, P->d_mats, n,
-                     P->L.total_tiles, lr, wd, stream);
+    TimedLaunch t(stream, NSM_KIND_APPLY, (params_bf16 ? 12.0 : 10.0) * elems);
+    e = launch_apply(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, packed_params, params_bf16,
+                     P->d_mats, n, P->L.total_tiles, lr, wd, stream);
   }
   if (e != cudaSuccess) return fail_cuda(e, "apply launch");
   ++launches;

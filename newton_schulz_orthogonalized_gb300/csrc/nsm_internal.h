@@ -83,9 +83,9 @@ cudaError_t launch_norm_finalize(const MatInfo* mats, int nmats, const float* pa
 cudaError_t launch_to_class(const void* grads, const float* momentum, int has_momentum, int nesterov,
                             float mu, void* dst, int to_fp16, const MatInfo* mats, int nmats,
                             int64_t total_tiles, const float* scales, cudaStream_t stream);
-// class layout O -> p update in natural layout
-cudaError_t launch_apply(const void* o, int o_fp16, float* params, const MatInfo* mats,
-                         int nmats, int64_t total_tiles, float lr, float wd,
+// class layout O -> p update in natural layout (and its bf16 copy when params_bf16 != NULL)
+cudaError_t launch_apply(const void* o, int o_fp16, float* params, void* params_bf16,
+                         const MatInfo* mats, int nmats, int64_t total_tiles, float lr, float wd,
                          cudaStream_t stream);
 // class layout O -> natural bf16 copy
 cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* mats,

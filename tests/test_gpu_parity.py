@@ -365,3 +365,29 @@ def test_errors_launch_nothing(nsm):
     assert e.value.code == nsm.NSM_ERR_ARG
     torch.cuda.synchronize()
     assert nsm.device_status() == nsm.NSM_OK
+
+
+def test_step_bf16_copy(nsm):
+    # the bf16 copy is the round-to-nearest-even bf16 of the updated fp32 parameters, and
+    # writing it changes nothing else
+    wl = synth.custom([(256, 384), (384, 256), (130, 260)], seed=13)
+    offsets, total = nsm.pack(wl.muon_shapes)
+    dev = "cuda"
+    grads = torch.zeros(total, dtype=torch.bfloat16, device=dev)
+    synth.fill_packed_grads(wl, offsets, grads)
+    p_a = torch.zeros(total, dtype=torch.float32, device=dev)
+    synth.fill_packed_params(wl, offsets, p_a)
+    p_b = p_a.clone()
+    m_a = torch.zeros(total, device=dev)
+    m_b = torch.zeros(total, device=dev)
+    copy = torch.full((total,), float("nan"), dtype=torch.bfloat16, device=dev)
+    for method in ("gram", "standard"):
+        ws = torch.empty(nsm.workspace_bytes(wl.muon_shapes, method), dtype=torch.uint8, device=dev)
+        nsm.muon_step(grads, p_a, m_a, offsets, wl.muon_shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws)
+        nsm.muon_step(grads, p_b, m_b, offsets, wl.muon_shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws,
+                      params_bf16=copy)
+        torch.cuda.synchronize()
+        assert torch.equal(p_a, p_b) and torch.equal(m_a, m_b)
+        for i, (r, c) in enumerate(wl.muon_shapes):
+            o = int(offsets[i])
+            assert torch.equal(copy[o:o + r * c], p_b[o:o + r * c].to(torch.bfloat16))
