@@ -391,3 +391,44 @@ def test_step_bf16_copy(nsm):
         for i, (r, c) in enumerate(wl.muon_shapes):
             o = int(offsets[i])
             assert torch.equal(copy[o:o + r * c], p_b[o:o + r * c].to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("method", ["gram", "standard"])
+def test_step_replays_in_cuda_graph(nsm, method):
+    # After a first call has built the plan, muon_step launches only kernels on the given
+    # stream: a CUDA graph of it replays bit-identically to direct calls (the remedy for
+    # launch-bound small tables).
+    wl = synth.workload("tiny")
+    offsets, total = nsm.pack(wl.muon_shapes)
+    dev = "cuda"
+    grads = torch.zeros(total, dtype=torch.bfloat16, device=dev)
+    synth.fill_packed_grads(wl, offsets, grads)
+    p0 = torch.zeros(total, device=dev)
+    synth.fill_packed_params(wl, offsets, p0)
+    ws = torch.empty(nsm.workspace_bytes(wl.muon_shapes, method), dtype=torch.uint8, device=dev)
+
+    def run(p, m, stream=None):
+        nsm.muon_step(grads, p, m, offsets, wl.muon_shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws,
+                      stream)
+
+    p_direct, m_direct = p0.clone(), torch.zeros(total, device=dev)
+    for _ in range(3):
+        run(p_direct, m_direct)
+    p_graph, m_graph = p0.clone(), torch.zeros(total, device=dev)
+    warm_p, warm_m = p0.clone(), torch.zeros(total, device=dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run(warm_p, warm_m, s)  # builds and caches the plan outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(p_graph, m_graph, torch.cuda.current_stream())
+    p_graph.copy_(p0)
+    m_graph.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert nsm.device_status() == nsm.NSM_OK
+    assert torch.equal(p_graph, p_direct) and torch.equal(m_graph, m_direct)
