@@ -432,3 +432,39 @@ def test_step_replays_in_cuda_graph(nsm, method):
     torch.cuda.synchronize()
     assert nsm.device_status() == nsm.NSM_OK
     assert torch.equal(p_graph, p_direct) and torch.equal(m_graph, m_direct)
+
+
+def test_checkpoint_resume_bitwise(nsm):
+    # the step's whole state is the fp32 params and momentum (plus the caller's step
+    # count): saving them mid-run and resuming gives bit-identical later steps
+    wl = synth.custom([(256, 384), (384, 256), (128, 128)], seed=23)
+    offsets, total = nsm.pack(wl.muon_shapes)
+    dev = "cuda"
+    grads = torch.zeros(total, dtype=torch.bfloat16, device=dev)
+    p = torch.zeros(total, device=dev)
+    synth.fill_packed_params(wl, offsets, p)
+    m = torch.zeros(total, device=dev)
+    ws = torch.empty(nsm.workspace_bytes(wl.muon_shapes, "gram"), dtype=torch.uint8, device=dev)
+
+    def step(k, p, m):
+        synth.fill_packed_grads(wl, offsets, grads, seed_offset=k)
+        nsm.muon_step(grads, p, m, offsets, wl.muon_shapes, wl.lr, wl.wd, wl.mu, "gram", 5, True, ws)
+
+    for k in range(2):
+        step(k, p, m)
+    saved = {"p": p.cpu().clone(), "m": m.cpu().clone()}
+    for k in range(2, 4):
+        step(k, p, m)
+    p2, m2 = saved["p"].to(dev), saved["m"].to(dev)
+    for k in range(2, 4):
+        step(k, p2, m2)
+    torch.cuda.synchronize()
+    assert torch.equal(p, p2) and torch.equal(m, m2)
+
+
+@pytest.mark.parametrize("method", ["gram", "standard"])
+def test_degenerate_and_extreme_shapes(nsm, method):
+    shapes = [(1, 1), (7, 1), (1, 8), (256, 262144)]
+    wl = synth.custom(shapes, seed=29, lowrank=False)
+    s = Step(nsm, wl, method)
+    s.check()
