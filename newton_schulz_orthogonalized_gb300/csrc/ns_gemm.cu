@@ -150,12 +150,78 @@ __device__ __forceinline__ void signal_timeout(Ctrl<STAGES>* ctrl, int* status) 
 
 // Epilogue of one accumulator: this warp's 32 rows (rows rb .. rb+31 of the matrix,
 // TMEM lanes 32*quarter ..), the tile's n_len columns from column n0.
+// O's apply at natural positions (see ApplyArgs): o[j] is the stored-precision O at
+// class (row, gc0 + j) of matrix mt.  Every load of the chunk is issued before its first
+// store, so the 32 read-modify-writes of a lane overlap instead of queueing behind one
+// another.
+__device__ __forceinline__ void apply_chunk(const ApplyArgs& ap, const MatInfo& mt, int row, int gc0,
+                                            int ncols, const float (&o)[32]) {
+  float* __restrict__ p = ap.params + mt.off;
+  __nv_bfloat16* __restrict__ pb =
+      ap.params_bf16 ? reinterpret_cast<__nv_bfloat16*>(ap.params_bf16) + mt.off : nullptr;
+  const float coef = ap.lr * mt.scale;
+  const float decay = ap.decay;
+  if (!mt.transposed && ncols == 32 && mt.vec_ok) {
+    // class row = natural row: 32 consecutive parameters of this lane
+    const int64_t i0 = static_cast<int64_t>(row) * mt.cols + gc0;
+    float4* pp = reinterpret_cast<float4*>(p + i0);
+    float4 a[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) a[w] = pp[w];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      a[w].x = fmaf(-coef, o[4 * w + 0], a[w].x * decay);
+      a[w].y = fmaf(-coef, o[4 * w + 1], a[w].y * decay);
+      a[w].z = fmaf(-coef, o[4 * w + 2], a[w].z * decay);
+      a[w].w = fmaf(-coef, o[4 * w + 3], a[w].w * decay);
+      pp[w] = a[w];
+    }
+    if (pb) {
+      uint4* q = reinterpret_cast<uint4*>(pb + i0);
+      const bool q16 = (reinterpret_cast<uintptr_t>(q) & 15) == 0;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        __nv_bfloat162 h[4] = {__floats2bfloat162_rn(a[2 * w].x, a[2 * w].y),
+                               __floats2bfloat162_rn(a[2 * w].z, a[2 * w].w),
+                               __floats2bfloat162_rn(a[2 * w + 1].x, a[2 * w + 1].y),
+                               __floats2bfloat162_rn(a[2 * w + 1].z, a[2 * w + 1].w)};
+        if (q16) {
+          q[w] = *reinterpret_cast<const uint4*>(h);
+        } else {
+          __nv_bfloat162* q2 = reinterpret_cast<__nv_bfloat162*>(pb + i0 + 8 * w);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) q2[k] = h[k];
+        }
+      }
+    }
+    return;
+  }
+  // general case: element (class row, gc0 + j) lives at natural (row, gc0 + j), or at
+  // (gc0 + j, row) when the matrix is stored transposed in its class (then the lanes of
+  // a warp cover consecutive natural columns)
+  const int64_t step = mt.transposed ? mt.cols : 1;
+  const int64_t i0 = mt.transposed ? static_cast<int64_t>(gc0) * mt.cols + row
+                                   : static_cast<int64_t>(row) * mt.cols + gc0;
+  float pv[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) pv[j] = j < ncols ? p[i0 + j * step] : 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j < ncols) {
+      const float np = fmaf(-coef, o[j], pv[j] * decay);
+      p[i0 + j * step] = np;
+      if (pb) pb[i0 + j * step] = __float2bfloat16_rn(np);
+    }
+  }
+}
+
 template <bool FP16, bool HAS_AUX>
 __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
                                               uint32_t t_row, float* xt, int lane, float alpha,
-                                              float beta, float diag) {
+                                              float beta, float diag, const ApplyArgs& ap) {
   using E = Elem<FP16>;
   using T = typename E::T;
+  const MatInfo* apply_mt = ap.params ? ap.mats + __ldg(G.mat_index + b) : nullptr;
   const int row = rb + lane;
   const bool row_ok = row < G.M;
   const int nchunks = (n_len + 31) >> 5;
@@ -201,6 +267,13 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
         for (int j = 0; j < 32; ++j) {
           if (d == j) v[j] += diag;
         }
+      }
+      if (apply_mt) {
+        // the step's last product: round O to its storage format, then apply it
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = E::to_f(E::from_f(v[j]));
+        apply_chunk(ap, *apply_mt, row, gc0, full ? 32 : n_len - col0, v);
+        continue;
       }
       // a symmetric output stores only its upper triangle (column >= row) directly
       const int first_col = G.sym ? row : 0;
@@ -261,7 +334,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
 template <bool B_MN, bool FP16, bool HAS_AUX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ns_gemm(const GemmGroup* __restrict__ groups, int ng, int64_t total_tiles, float alpha,
-              float beta, float diag, int* status) {
+              float beta, float diag, int* status, ApplyArgs ap) {
   constexpr int STAGES = S1_STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -440,7 +513,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
       epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                   t_row, xt, lane, alpha, beta, diag);
+                                   t_row, xt, lane, alpha, beta, diag, ap);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(&ctrl->acc_empty[acc]));
@@ -475,7 +548,7 @@ __device__ __forceinline__ int boxes_in(int start, int limit) {
 template <bool B_MN, bool FP16, bool HAS_AUX>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_ns_gemm_pair(const GemmGroup* __restrict__ groups, int ng, int64_t total_tiles, float alpha,
-                   float beta, float diag, int* status) {
+                   float beta, float diag, int* status, ApplyArgs ap) {
   constexpr int STAGES = S2_STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -689,7 +762,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                              static_cast<uint32_t>(acc * BN);
       const int rb = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
       epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, xt, lane,
-                                   alpha, beta, diag);
+                                   alpha, beta, diag, ap);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(&ctrl->acc_empty[acc]), 0));
@@ -729,7 +802,7 @@ cudaError_t set_smem_once(K kernel, size_t bytes, std::atomic<uint64_t>& done) {
 }
 
 template <bool B_MN, bool FP16, bool HAS_AUX>
-cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream) {
+cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream, const ApplyArgs& ap) {
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   if (l.pair) {
@@ -766,7 +839,7 @@ cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream) 
     const int64_t pairs = l.total_tiles < cap ? l.total_tiles : cap;
     if (pairs <= 0) return cudaSuccess;
     k_ns_gemm_pair<B_MN, FP16, HAS_AUX><<<static_cast<int>(2 * pairs), NUM_THREADS, S2_SMEM, stream>>>(
-        l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag, status);
+        l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag, status, ap);
     return cudaGetLastError();
   }
   static std::atomic<uint64_t> done{0};
@@ -775,23 +848,24 @@ cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream) 
   const int64_t grid = l.total_tiles < num_sms ? l.total_tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
   k_ns_gemm<B_MN, FP16, HAS_AUX><<<static_cast<int>(grid), NUM_THREADS, S1_SMEM, stream>>>(
-      l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag, status);
+      l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag, status, ap);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream, const ApplyArgs* apply) {
+  const ApplyArgs ap = apply ? *apply : ApplyArgs{nullptr, nullptr, nullptr, 0.f, 1.f};
   const int key = (l.b_mn_major ? 4 : 0) | (l.fp16 ? 2 : 0) | (l.has_aux ? 1 : 0);
   switch (key) {
-    case 0: return launch_typed<false, false, false>(l, num_sms, stream);
-    case 1: return launch_typed<false, false, true>(l, num_sms, stream);
-    case 2: return launch_typed<false, true, false>(l, num_sms, stream);
-    case 3: return launch_typed<false, true, true>(l, num_sms, stream);
-    case 4: return launch_typed<true, false, false>(l, num_sms, stream);
-    case 5: return launch_typed<true, false, true>(l, num_sms, stream);
-    case 6: return launch_typed<true, true, false>(l, num_sms, stream);
-    default: return launch_typed<true, true, true>(l, num_sms, stream);
+    case 0: return launch_typed<false, false, false>(l, num_sms, stream, ap);
+    case 1: return launch_typed<false, false, true>(l, num_sms, stream, ap);
+    case 2: return launch_typed<false, true, false>(l, num_sms, stream, ap);
+    case 3: return launch_typed<false, true, true>(l, num_sms, stream, ap);
+    case 4: return launch_typed<true, false, false>(l, num_sms, stream, ap);
+    case 5: return launch_typed<true, false, true>(l, num_sms, stream, ap);
+    case 6: return launch_typed<true, true, false>(l, num_sms, stream, ap);
+    default: return launch_typed<true, true, true>(l, num_sms, stream, ap);
   }
 }
 

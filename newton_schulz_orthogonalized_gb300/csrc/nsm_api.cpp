@@ -240,6 +240,17 @@ struct Plan {
   }
 };
 
+// The step's weight decay and update are applied in the epilogue of the chain's last
+// product; NSM_FUSED_APPLY=0 in the environment runs them as a separate pass instead (for
+// comparisons; both give the same bits).
+bool fused_apply_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("NSM_FUSED_APPLY");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 // The 2-SM kernel is used where it pays; NSM_PAIR_KERNELS=0 in the environment keeps every
 // launch on the 1-CTA kernel (for comparisons).
 bool pair_kernels_enabled() {
@@ -399,9 +410,13 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     }
   }
 
-  // Device metadata: MatInfo[n] | tensor maps [nclass][nbuf] | GemmGroup arrays | tile lists.
+  // Device metadata: MatInfo[n] | matrix of each (class, batch) | tensor maps [nclass][nbuf] |
+  // GemmGroup arrays | tile lists.
   const size_t mats_bytes = align_up(sizeof(MatInfo) * n, 128);
-  const size_t maps_off = mats_bytes;
+  std::vector<int32_t> class_first(nclass + 1, 0);
+  for (int c = 0; c < nclass; ++c) class_first[c + 1] = class_first[c] + L.classes[c].count;
+  const size_t matidx_off = mats_bytes;
+  const size_t maps_off = matidx_off + align_up(sizeof(int32_t) * size_t(n), 128);
   constexpr int kBoxKinds = 3;  // box heights 64, 128, 256 rows
   const size_t maps_bytes = align_up(sizeof(CUtensorMap) * size_t(nclass) * nbuf * kBoxKinds, 128);
   const size_t groups_off = maps_off + maps_bytes;
@@ -429,6 +444,8 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     mi.vec_ok = (mi.rows % 8 == 0 && mi.cols % 8 == 0) ? 1 : 0;
     hm[i] = mi;
   }
+  int32_t* hmatidx = reinterpret_cast<int32_t*>(host.data() + matidx_off);
+  for (int i = 0; i < n; ++i) hmatidx[class_first[L.cls_of[i]] + L.batch_of[i]] = i;
 
   cudaError_t e = cudaSuccess;
   if (sink) {
@@ -522,6 +539,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       g.tiles_m = (g.M + tile_m - 1) / tile_m;
       g.tiles_n = (g.N + 255) / 256;
       g.tile_begin = tiles;
+      g.mat_index = reinterpret_cast<const int32_t*>(dbase + matidx_off) + class_first[c];
       canonical += 2.0 * g.count * double(g.M) * g.N * g.K;
       if (st.sym) {
         g.sym = 1;
@@ -730,13 +748,17 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need) {
   return NSM_OK;
 }
 
-int run_chain(Plan& P, cudaStream_t stream, int* launches) {
+// Launches the chain's GEMMs.  With `apply_last`, the last product (which computes O)
+// applies the step to the parameters in its epilogue instead of storing O.
+int run_chain(Plan& P, cudaStream_t stream, int* launches, const ApplyArgs* apply_last = nullptr) {
   int num_sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, P.device);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
-  for (const GemmLaunch& l : P.launches) {
+  for (size_t k = 0; k < P.launches.size(); ++k) {
+    const GemmLaunch& l = P.launches[k];
+    const bool last = k + 1 == P.launches.size();
     TimedLaunch t(stream, NSM_KIND_GEMM, l.flops);
-    e = launch_gemm(l, num_sms, stream);
+    e = launch_gemm(l, num_sms, stream, last ? apply_last : nullptr);
     if (e != cudaSuccess) return fail_cuda(e, "Newton-Schulz GEMM launch");
     ++*launches;
   }
@@ -937,6 +959,15 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   }
   if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
   ++launches;
+  const float decay = 1.0f - lr * wd;
+  if (!P->launches.empty() && fused_apply_enabled()) {
+    // the last product writes the parameters (and their bf16 copy) directly
+    const ApplyArgs ap{P->d_mats, packed_params, params_bf16, lr, decay};
+    rc = run_chain(*P, stream, &launches, &ap);
+    if (rc != NSM_OK) return rc;
+    t_last_launches = launches;
+    return NSM_OK;
+  }
   rc = run_chain(*P, stream, &launches);
   if (rc != NSM_OK) return rc;
   {

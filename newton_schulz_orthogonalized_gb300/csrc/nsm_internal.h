@@ -53,8 +53,20 @@ struct GemmGroup {
   int32_t tiles_m, tiles_n;
   int32_t sym, tiles_per_mat;
   int32_t a_box, b_box;  // rows per TMA box of map_a / map_b (64, 128 or 256)
+  const int32_t* mat_index;  // matrix (MatInfo index) of each batch entry
+  int64_t pad;
 };
-static_assert(sizeof(GemmGroup) == 112, "GemmGroup layout");
+static_assert(sizeof(GemmGroup) == 128, "GemmGroup layout");
+
+// Epilogue that applies the step instead of storing O: for matrix mats[mat_index[b]],
+// p <- p * decay - lr * scale * O at O's natural position (transposed back when the
+// matrix is tall), and params_bf16 (if not NULL) <- bf16(p).  params == NULL: store O.
+struct ApplyArgs {
+  const MatInfo* mats;
+  float* params;
+  void* params_bf16;
+  float lr, decay;
+};
 
 struct GemmLaunch {
   const GemmGroup* groups;  // device array
@@ -93,7 +105,8 @@ cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* m
 cudaError_t launch_adamw(const void* grads, float* params, float* m, float* v,
                          int64_t numel, float lr, float beta1, float beta2, float eps,
                          float wd, float bc1, float bc2, cudaStream_t stream);
-cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream,
+                        const ApplyArgs* apply = nullptr);
 
 int* device_status_ptr();
 

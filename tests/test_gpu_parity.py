@@ -1,7 +1,7 @@
 """Parity of the CUDA path with the oracle, through the C ABI.
 
-The oracle runs the method in the storage precision the pages give it (bf16 for the
-standard form, fp16 for the gram form: it rounds where the method stores an iterate and
+The oracle runs the method in the storage precision of its form (fp16 for the standard
+and gram forms, bf16 for standard_bf16: it rounds where the method stores an iterate and
 accumulates in float64).  Tolerances (relative Frobenius norms): orthogonalised output
 <= 2e-2, final parameter delta <= 1e-2, momentum and AdamW <= 1e-5.  Routing and
 offsets are bit-exact (tests/test_abi.py).  Where the exact float64 iteration is within
@@ -9,6 +9,10 @@ reach of half-precision storage (well-conditioned inputs, and the re-anchored gr
 the GPU is also held to it.  Inputs come from the seeded generators in ``synth``: the GPU
 draws them, the oracle reads the same bf16 values decoded exactly.
 """
+
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -468,3 +472,45 @@ def test_degenerate_and_extreme_shapes(nsm, method):
     wl = synth.custom(shapes, seed=29, lowrank=False)
     s = Step(nsm, wl, method)
     s.check()
+
+
+_SEPARATE_APPLY = r"""
+import sys, torch
+import newton_schulz_orthogonalized_gb300 as nsm
+import synth
+wl = synth.custom([(256, 384), (384, 256), (130, 260), (96, 96)], seed=31)
+offsets, total = nsm.pack(wl.muon_shapes)
+out = {}
+for method in ("gram", "standard", "standard_bf16"):
+    grads = torch.zeros(total, dtype=torch.bfloat16, device="cuda")
+    synth.fill_packed_grads(wl, offsets, grads)
+    p = torch.zeros(total, device="cuda")
+    synth.fill_packed_params(wl, offsets, p)
+    m = torch.zeros(total, device="cuda")
+    copy = torch.zeros(total, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(nsm.workspace_bytes(wl.muon_shapes, method), dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        nsm.muon_step(grads, p, m, offsets, wl.muon_shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws,
+                      params_bf16=copy)
+    out[method] = (p.cpu(), m.cpu(), copy.cpu())
+torch.save(out, sys.argv[1])
+"""
+
+
+def test_fused_apply_matches_separate_pass_bitwise(nsm, tmp_path):
+    # The chain's last product applies the step in its epilogue; with NSM_FUSED_APPLY=0 a
+    # separate pass applies it from the stored O.  Both round O to the same storage format
+    # and evaluate the same fused multiply-add, so the results agree bit for bit.
+    path = tmp_path / "separate.pt"
+    env = dict(os.environ, NSM_FUSED_APPLY="0")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    subprocess.run([sys.executable, "-c", _SEPARATE_APPLY, str(path)], env=env, cwd=root, check=True,
+                   timeout=600)
+    ref = torch.load(path)
+    path2 = tmp_path / "fused.pt"
+    subprocess.run([sys.executable, "-c", _SEPARATE_APPLY, str(path2)], cwd=root, check=True, timeout=600,
+                   env={k: v for k, v in os.environ.items() if k != "NSM_FUSED_APPLY"})
+    got = torch.load(path2)
+    for method in ref:
+        for a, b in zip(got[method], ref[method]):
+            assert torch.equal(a, b), method
