@@ -214,6 +214,7 @@ int nsm_device_status(nsm_stream_t stream, int* status_out);
 #define NSM_KIND_LAYOUT   3  /* X = s U into the working layout */
 #define NSM_KIND_APPLY    4  /* decay + apply (or the export of O) */
 #define NSM_KIND_ADAMW    5  /* AdamW */
+#define NSM_KIND_SMALL    6  /* whole Newton-Schulz chains of matrices with m <= 128 (flops) */
 int nsm_timing_enable(int enable);
 int nsm_timing_read(double* gemm_ms, int64_t* gemm_launches, double* gemm_flops);
 int nsm_timing_read_kind(int kind, double* ms, int64_t* launches, double* work);

@@ -235,6 +235,12 @@ struct Plan {
   bool final_fp16 = false;
   bool x_fp16 = false;
   bool owns_meta = true;  // false when the metadata lives in memory the plan does not own
+  // matrices with m <= kSmallMaxM run their whole chain in the small-matrix kernel
+  const SmallJob* d_small_jobs = nullptr;
+  const SmallOp* d_small_ops = nullptr;
+  int n_small_jobs = 0;
+  int n_small_ops = 0;
+  double small_flops = 0;
   ~Plan() {
     if (dmeta && owns_meta) cudaFree(dmeta);
   }
@@ -259,6 +265,145 @@ bool pair_kernels_enabled() {
     return !(v && v[0] == '0');
   }();
   return on;
+}
+
+// Matrices with m <= 128 run in the small-matrix kernel; NSM_SMALL_KERNEL=0 in the
+// environment sends them through the grouped launches instead (for comparisons).
+bool small_kernel_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("NSM_SMALL_KERNEL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+// Flops of one matrix's Newton-Schulz chain (2 m n k per product, as if no tile were
+// skipped): standard 4 m^2 n + 2 m^3 per step; gram counts its m x n products (X X^T,
+// Q X) and m x m products step by step, with re-anchoring.
+int64_t chain_flops(int method, int steps, int64_t m, int64_t n) {
+  if (method == NSM_NS_GRAM) {
+    int64_t wide = steps > 0 ? 1 : 0, cubes = 0;
+    bool q_identity = true;
+    for (int k = 1; k <= steps; ++k) {
+      cubes += q_identity ? 1 : 2;
+      q_identity = false;
+      if (k < steps) {
+        if (k % kGramReanchor == 0) {
+          wide += 2;
+          q_identity = true;
+        } else {
+          cubes += 2;
+        }
+      }
+    }
+    if (steps > 0 && !q_identity) wide += 1;
+    return 2 * wide * m * m * n + 2 * cubes * m * m * m;
+  }
+  return int64_t(steps) * (4 * m * m * n + 2 * m * m * m);
+}
+
+// The chain of one matrix as the small-matrix kernel runs it: the products and storage
+// points of the grouped stages, with X X^T of each new iterate accumulated by the pass
+// that forms it.  S0..S2 are the kernel's shared-memory matrices.  Returns the X buffer
+// that receives O (the one the grouped stages end in).
+int small_schedule(int method, int steps, std::vector<SmallOp>& ops) {
+  auto make = [](int kind) {
+    SmallOp o{};
+    o.kind = kind;
+    o.aux = -1;
+    o.alpha = 1.f;
+    return o;
+  };
+  if (method == NSM_NS_GRAM) {
+    int xb = X0;
+    int q = -1;  // shared-memory matrix holding Q; -1 = identity
+    SmallOp g = make(kSmallGram);  // R = X X^T in S0
+    g.src_x = xb;
+    g.dst = 0;
+    ops.push_back(g);
+    for (int k = 1; k <= steps; ++k) {
+      const int h = q == 1 ? 2 : 1;
+      SmallOp hs = make(kSmallSquare);  // H = a I + b R + c R R
+      hs.a = 0;
+      hs.b = 0;
+      hs.dst = h;
+      hs.aux = 0;
+      hs.alpha = kC;
+      hs.beta = kB;
+      hs.diag = kA;
+      ops.push_back(hs);
+      if (q < 0) {
+        q = h;  // Q = H
+      } else {
+        SmallOp qs = make(kSmallSquare);  // Q = H Q, in place
+        qs.a = h;
+        qs.b = q;
+        qs.dst = q;
+        ops.push_back(qs);
+      }
+      if (k < steps) {
+        if (k % kGramReanchor == 0) {
+          const int xn = xb == X0 ? X1 : X0;
+          SmallOp ps = make(kSmallPass);  // X = Q X, and R = X X^T on the way
+          ps.a = q;
+          ps.src_x = xb;
+          ps.dst_x = xn;
+          ps.accumulate = 1;
+          ps.dst = 0;
+          ops.push_back(ps);
+          xb = xn;
+          q = -1;
+        } else {
+          SmallOp ts = make(kSmallSquare);  // T = H R, in R's place
+          ts.a = h;
+          ts.b = 0;
+          ts.dst = 0;
+          ops.push_back(ts);
+          SmallOp rs = make(kSmallSquare);  // R = T H
+          rs.a = 0;
+          rs.b = h;
+          rs.dst = 0;
+          ops.push_back(rs);
+        }
+      }
+    }
+    const int xn = xb == X0 ? X1 : X0;
+    SmallOp fs = make(kSmallPass);  // O = Q X
+    fs.a = q;
+    fs.src_x = xb;
+    fs.dst_x = xn;
+    fs.final_pass = 1;
+    ops.push_back(fs);
+    return xn;
+  }
+  SmallOp g = make(kSmallGram);  // A = X X^T in S0
+  g.src_x = X0;
+  g.dst = 0;
+  ops.push_back(g);
+  for (int k = 0; k < steps; ++k) {
+    const int src = (k % 2 == 0) ? X0 : X1, dst = (k % 2 == 0) ? X1 : X0;
+    SmallOp bs = make(kSmallSquare);  // B = b A + c A A in S1
+    bs.a = 0;
+    bs.b = 0;
+    bs.dst = 1;
+    bs.aux = 0;
+    bs.alpha = kC;
+    bs.beta = kB;
+    ops.push_back(bs);
+    SmallOp ps = make(kSmallPass);  // X' = a X + B X (and A = X' X'^T unless last)
+    ps.a = 1;
+    ps.src_x = src;
+    ps.dst_x = dst;
+    ps.beta = kA;
+    if (k + 1 < steps) {
+      ps.accumulate = 1;
+      ps.dst = 0;
+    } else {
+      ps.final_pass = 1;
+    }
+    ops.push_back(ps);
+  }
+  return steps % 2 == 0 ? X0 : X1;
 }
 
 // Device memory a caller provides for a plan's metadata instead of a fresh allocation.
@@ -410,8 +555,35 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     }
   }
 
+  // Classes whose whole chain runs in the small-matrix kernel; the grouped launches take
+  // the others.
+  std::vector<char> small(nclass, 0);
+  std::vector<int> big;
+  for (int c = 0; c < nclass; ++c) {
+    small[c] = steps > 0 && small_kernel_enabled() && L.classes[c].m <= kSmallMaxM;
+    if (!small[c]) big.push_back(c);
+  }
+  std::vector<SmallOp> small_ops;
+  std::vector<int> small_mats;
+  for (int i = 0; i < n; ++i) {
+    if (small[L.cls_of[i]]) small_mats.push_back(i);
+  }
+  if (!small_mats.empty()) {
+    const int final_x = small_schedule(method, steps, small_ops);
+    if (final_x != P.final_buf || small_ops.size() > size_t(kSmallMaxOps))
+      return fail(NSM_ERR_METHOD, "small-matrix schedule does not fit (%zu operations)", small_ops.size());
+    // heaviest first, for the persistent CTAs' balance
+    std::stable_sort(small_mats.begin(), small_mats.end(), [&](int x, int y) {
+      return int64_t(shapes[2 * x]) * shapes[2 * x + 1] > int64_t(shapes[2 * y]) * shapes[2 * y + 1];
+    });
+    for (int i : small_mats) {
+      const ShapeClass& sc = L.classes[L.cls_of[i]];
+      P.small_flops += double(chain_flops(method, steps, sc.m, sc.n));
+    }
+  }
+
   // Device metadata: MatInfo[n] | matrix of each (class, batch) | tensor maps [nclass][nbuf] |
-  // GemmGroup arrays | tile lists.
+  // GemmGroup arrays | tile lists | small-matrix jobs | small-matrix operations.
   const size_t mats_bytes = align_up(sizeof(MatInfo) * n, 128);
   std::vector<int32_t> class_first(nclass + 1, 0);
   for (int c = 0; c < nclass; ++c) class_first[c + 1] = class_first[c] + L.classes[c].count;
@@ -422,7 +594,9 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   const size_t groups_off = maps_off + maps_bytes;
   const size_t groups_bytes = align_up(sizeof(GemmGroup) * size_t(nclass) * stages.size(), 128);
   const size_t tiles_off_bytes = groups_off + groups_bytes;
-  const size_t total = tiles_off_bytes + tile_ints * sizeof(int32_t) + 128;
+  const size_t jobs_off = align_up(tiles_off_bytes + tile_ints * sizeof(int32_t), 128);
+  const size_t ops_off = align_up(jobs_off + sizeof(SmallJob) * small_mats.size(), 128);
+  const size_t total = ops_off + sizeof(SmallOp) * small_ops.size() + 128;
   std::vector<uint8_t> host(total, 0);
 
   MatInfo* hm = reinterpret_cast<MatInfo*>(host.data());
@@ -489,12 +663,32 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     }
   }
   const int32_t* dtiles = reinterpret_cast<const int32_t*>(dbase + tiles_off_bytes);
+  if (!small_mats.empty()) {
+    SmallJob* hj = reinterpret_cast<SmallJob*>(host.data() + jobs_off);
+    for (size_t k = 0; k < small_mats.size(); ++k) {
+      const int i = small_mats[k];
+      const int c = L.cls_of[i];
+      SmallJob jb{};
+      jb.map_x[0] = dmap(c, X0, 128);
+      jb.map_x[1] = dmap(c, X1, 128);
+      jb.mat = i;
+      jb.b = L.batch_of[i];
+      jb.m = L.classes[c].m;
+      jb.n = L.classes[c].n;
+      hj[k] = jb;
+    }
+    std::copy(small_ops.begin(), small_ops.end(), reinterpret_cast<SmallOp*>(host.data() + ops_off));
+    P.d_small_jobs = reinterpret_cast<const SmallJob*>(dbase + jobs_off);
+    P.d_small_ops = reinterpret_cast<const SmallOp*>(dbase + ops_off);
+    P.n_small_jobs = static_cast<int>(small_mats.size());
+    P.n_small_ops = static_cast<int>(small_ops.size());
+  }
   GemmGroup* hg = reinterpret_cast<GemmGroup*>(host.data() + groups_off);
-  for (size_t s = 0; s < stages.size(); ++s) {
+  const int nbig = static_cast<int>(big.size());
+  for (size_t s = 0; s < stages.size() && nbig > 0; ++s) {
     const StageSpec& st = stages[s];
     // heaviest tiles (largest K) first
-    std::vector<int> order(nclass);
-    for (int c = 0; c < nclass; ++c) order[c] = c;
+    std::vector<int> order = big;
     std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
       const int kx = st.k_is_n ? L.classes[x].n : L.classes[x].m;
       const int ky = st.k_is_n ? L.classes[y].n : L.classes[y].m;
@@ -504,7 +698,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     int64_t tiles = 0;
     double flops = 0, canonical = 0;
     std::vector<std::pair<int, double>> rows_and_flops;
-    for (int c = 0; c < nclass; ++c) {
+    for (int c : big) {
       const ShapeClass& sc = L.classes[c];
       const double f = 2.0 * sc.count * double(sc.m) * (st.n_is_n ? sc.n : sc.m) * (st.k_is_n ? sc.n : sc.m);
       rows_and_flops.push_back({sc.m, f});
@@ -512,7 +706,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     const bool pair = use_pair_kernels && prefer_pair(rows_and_flops);
     const int tile_m = pair ? 256 : 128;
     const int tk = pair ? 1 : 0;
-    for (int j = 0; j < nclass; ++j) {
+    for (int j = 0; j < nbig; ++j) {
       const int c = order[j];
       const ShapeClass& sc = L.classes[c];
       GemmGroup g{};
@@ -555,7 +749,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     }
     GemmLaunch l{};
     l.groups = reinterpret_cast<const GemmGroup*>(dbase + groups_off) + s * nclass;
-    l.num_groups = nclass;
+    l.num_groups = nbig;
     l.b_mn_major = st.b_mn ? 1 : 0;
     l.has_aux = st.aux_buf >= 0 ? 1 : 0;
     l.fp16 = P.x_fp16 ? 1 : 0;
@@ -640,7 +834,7 @@ Plan* get_plan(const int32_t* shapes, const int64_t* offsets, int n, int method,
 // ---------------------------------------------------------------- timing
 
 // Kernel kinds the timing hooks distinguish (NSM_KIND_* in the header).
-constexpr int kKinds = 6;
+constexpr int kKinds = 7;
 
 struct Timing {
   std::mutex mu;
@@ -748,12 +942,20 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need) {
   return NSM_OK;
 }
 
-// Launches the chain's GEMMs.  With `apply_last`, the last product (which computes O)
-// applies the step to the parameters in its epilogue instead of storing O.
+// Launches the chain: the small-matrix kernel, then the grouped GEMMs.  With
+// `apply_last`, the products that compute O apply the step to the parameters in their
+// epilogues instead of storing O.
 int run_chain(Plan& P, cudaStream_t stream, int* launches, const ApplyArgs* apply_last = nullptr) {
   int num_sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, P.device);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+  if (P.n_small_jobs > 0) {
+    TimedLaunch t(stream, NSM_KIND_SMALL, P.small_flops);
+    e = launch_ns_small(P.d_small_jobs, P.n_small_jobs, P.d_small_ops, P.n_small_ops, P.x_fp16 ? 1 : 0, num_sms,
+                        stream, apply_last);
+    if (e != cudaSuccess) return fail_cuda(e, "small-matrix Newton-Schulz launch");
+    ++*launches;
+  }
   for (size_t k = 0; k < P.launches.size(); ++k) {
     const GemmLaunch& l = P.launches[k];
     const bool last = k + 1 == P.launches.size();
@@ -846,27 +1048,7 @@ int nsm_assign_owners(const int32_t* shapes, int n, int world, int ns_method, in
   std::vector<int64_t> cost(n);
   for (int i = 0; i < n; ++i) {
     const int64_t r = shapes[2 * i], c = shapes[2 * i + 1];
-    const int64_t m = std::min(r, c), nn = std::max(r, c);
-    if (ns_method == NSM_NS_GRAM) {
-      int64_t wide = ns_steps > 0 ? 1 : 0, cubes = 0;
-      bool q_identity = true;
-      for (int k = 1; k <= ns_steps; ++k) {
-        cubes += q_identity ? 1 : 2;
-        q_identity = false;
-        if (k < ns_steps) {
-          if (k % kGramReanchor == 0) {
-            wide += 2;
-            q_identity = true;
-          } else {
-            cubes += 2;
-          }
-        }
-      }
-      if (ns_steps > 0 && !q_identity) wide += 1;
-      cost[i] = 2 * wide * m * m * nn + 2 * cubes * m * m * m;
-    } else {
-      cost[i] = int64_t(ns_steps) * (4 * m * m * nn + 2 * m * m * m);
-    }
+    cost[i] = chain_flops(ns_method, ns_steps, std::min(r, c), std::max(r, c));
   }
   // longest processing time first: heaviest matrix to the least-loaded owner; ties go to
   // the lower matrix index and the lower rank, so every rank computes the same plan
@@ -960,7 +1142,7 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
   ++launches;
   const float decay = 1.0f - lr * wd;
-  if (!P->launches.empty() && fused_apply_enabled()) {
+  if ((!P->launches.empty() || P->n_small_jobs > 0) && fused_apply_enabled()) {
     // the last product writes the parameters (and their bf16 copy) directly
     const ApplyArgs ap{P->d_mats, packed_params, params_bf16, lr, decay};
     rc = run_chain(*P, stream, &launches, &ap);

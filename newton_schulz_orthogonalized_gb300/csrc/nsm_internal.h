@@ -81,7 +81,43 @@ struct GemmLaunch {
   double canonical_flops;   // 2 M N K per problem, as if no tile were skipped
 };
 
+// ---- small-matrix kernel: the whole Newton-Schulz chain of one m <= 128 matrix per CTA
+
+// Working shapes the small-matrix kernel takes: m (rows of the working matrix) at most this.
+constexpr int kSmallMaxM = 128;
+
+// One matrix for the small-matrix kernel: its class tensor maps of the two X buffers
+// (128-row boxes), its batch index in the class and its MatInfo index.
+struct SmallJob {
+  const CUtensorMap* map_x[2];
+  int32_t mat, b, m, n;
+};
+static_assert(sizeof(SmallJob) == 32, "SmallJob layout");
+
+// Operations of the small-matrix chain (every matrix of the launch runs the same list).
+// S0..S2 are 128 x 128 matrices in shared memory, X0/X1 the class buffers in the workspace.
+enum SmallOpKind : int32_t {
+  kSmallGram = 0,    // S[dst] = X[src_x] X[src_x]^T
+  kSmallSquare = 1,  // S[dst] = alpha S[a] S[b]^T + beta S[aux] + diag I
+  kSmallPass = 2,    // X[dst_x] = alpha S[a] X[src_x] + beta X[src_x];
+                     //   accumulate: also S[dst] = X[dst_x] X[dst_x]^T;  final: it is O
+};
+struct SmallOp {
+  int32_t kind;
+  int32_t a, b, dst, aux;  // shared-memory matrices; aux < 0: none
+  int32_t src_x, dst_x;    // X buffers of Gram and pass operations
+  int32_t accumulate, final_pass;
+  float alpha, beta, diag;
+};
+static_assert(sizeof(SmallOp) == 48, "SmallOp layout");
+constexpr int kSmallMaxOps = 96;
+
 // ---- launchers (defined in the .cu files) ---------------------------------------
+
+// Runs `ops` for every job; with `apply` (params != NULL) the final pass applies the step
+// instead of storing O.
+cudaError_t launch_ns_small(const SmallJob* jobs, int njobs, const SmallOp* ops, int nops, int fp16,
+                            int num_sms, cudaStream_t stream, const ApplyArgs* apply);
 
 // M <- mu M + G (when has_momentum) and per-chunk sums of U^2, U = G + mu M (Nesterov),
 // M (plain) or G (no momentum)
