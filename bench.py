@@ -169,6 +169,10 @@ def max_over_ranks(value, dist, device):
     return float(t.item())
 
 
+# kernels whose timing work is flops (the others count bytes)
+FLOP_KERNELS = ("k_ns_gemm", "k_ns_small")
+
+
 def _traffic_record(method, workload):
     """Per-launch DRAM traffic of the dominant kernel from a committed ncu summary, if the
     kernel source is unchanged since the counters were taken."""
@@ -348,38 +352,48 @@ def run_ours(args):
         d_grads = [grads, torch.empty_like(grads)]
         d_out = [torch.empty(total, dtype=torch.bfloat16, device=dev) for _ in range(2)]
         ev = lambda: torch.cuda.Event()
-        h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(h2d)
-        with torch.cuda.stream(h2d):
-            d_grads[0].copy_(h_grads, non_blocking=True)
-            h2d_done[0].record(h2d)
-        for k in range(reps):
-            cur, nxt = k % 2, (k + 1) % 2
-            stream.wait_event(h2d_done[cur])
-            if k >= 2:
-                stream.wait_event(d2h_done[cur])  # step k-2's result has left d_out[cur]
-            nsm.muon_step(d_grads[cur], params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method,
-                          NS_STEPS, True, ws, stream, params_bf16=d_out[cur])
-            comp_done[cur].record(stream)
-            if k + 1 < reps:
-                with torch.cuda.stream(h2d):
-                    if k >= 1:
-                        h2d.wait_event(comp_done[nxt])  # step k-1 is done with d_grads[nxt]
-                    d_grads[nxt].copy_(h_grads, non_blocking=True)
-                    h2d_done[nxt].record(h2d)
-            with torch.cuda.stream(d2h):
-                d2h.wait_event(comp_done[cur])
-                h_out.copy_(d_out[cur], non_blocking=True)
-                d2h_done[cur].record(d2h)
-        h2d.wait_stream(d2h)
-        e1.record(h2d)
-        torch.cuda.synchronize()
-        e2e = {"value": e0.elapsed_time(e1) / reps, "unit": "ms",
+
+        def pipeline():
+            h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(h2d)
+            with torch.cuda.stream(h2d):
+                d_grads[0].copy_(h_grads, non_blocking=True)
+                h2d_done[0].record(h2d)
+            for k in range(reps):
+                cur, nxt = k % 2, (k + 1) % 2
+                stream.wait_event(h2d_done[cur])
+                if k >= 2:
+                    stream.wait_event(d2h_done[cur])  # step k-2's result has left d_out[cur]
+                nsm.muon_step(d_grads[cur], params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method,
+                              NS_STEPS, True, ws, stream, params_bf16=d_out[cur])
+                comp_done[cur].record(stream)
+                if k + 1 < reps:
+                    with torch.cuda.stream(h2d):
+                        if k >= 1:
+                            h2d.wait_event(comp_done[nxt])  # step k-1 is done with d_grads[nxt]
+                        d_grads[nxt].copy_(h_grads, non_blocking=True)
+                        h2d_done[nxt].record(h2d)
+                with torch.cuda.stream(d2h):
+                    d2h.wait_event(comp_done[cur])
+                    h_out.copy_(d_out[cur], non_blocking=True)
+                    d2h_done[cur].record(d2h)
+            h2d.wait_stream(d2h)
+            e1.record(h2d)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        # Host<->device copy speed on these machines varies from pass to pass while the
+        # GPU runs at its power cap, so one untimed pass warms the pinned buffers and the
+        # median of three timed passes is reported (all three are listed).
+        pipeline()
+        passes = [pipeline() for _ in range(3)]
+        e2e = {"value": sorted(passes)[1], "unit": "ms",
                "h2d_bytes_per_step": total * 2, "d2h_bytes_per_step": total * 2,
-               "steps": reps, "overlap": "copies on two streams, double-buffered"}
+               "steps": reps, "passes_ms": passes, "statistic": "median of 3 timed passes",
+               "overlap": "copies on two streams, double-buffered"}
         del h_grads, h_out, d_grads, d_out
     except Exception as exc:  # pinned memory may be unavailable on a host
         e2e = {"value": None, "unit": "ms", "h2d_bytes_per_step": total * 2,
@@ -435,9 +449,9 @@ def run_ours(args):
             kname: {
                 "launches": k_n,
                 "ms_per_step": k_ms / args.steps,
-                "achieved": (k_work / (k_ms * 1e-3) / (1e12 if kname == "k_ns_gemm" else 1e9)) if k_ms > 0 else None,
-                "unit": "TFLOP/s" if kname == "k_ns_gemm" else "GB/s",
-                "frac": ((k_work / (k_ms * 1e-3) / 1e12) / peak if kname == "k_ns_gemm"
+                "achieved": (k_work / (k_ms * 1e-3) / (1e12 if kname in FLOP_KERNELS else 1e9)) if k_ms > 0 else None,
+                "unit": "TFLOP/s" if kname in FLOP_KERNELS else "GB/s",
+                "frac": ((k_work / (k_ms * 1e-3) / 1e12) / peak if kname in FLOP_KERNELS
                          else (k_work / (k_ms * 1e-3) / 1e9) / peaks["hbm_gbs"]) if k_ms > 0 else None,
             }
             for kname, (k_ms, k_n, k_work) in per_kind.items()

@@ -18,7 +18,8 @@ Workloads (transformer-shaped gradient sets; no datasets or trained weights):
                   layer alone (for profiler captures).
 * ``split_moe`` — 16 layers, each with 32 per-head 128x4096 query blocks (Muon Split:
                   every head block is its own table entry) and 64 experts with gate/up
-                  1408x2048 and down 2048x1408.
+                  1408x2048 and down 2048x1408.  ``split_moe_heads`` is its 512 head
+                  blocks alone.
 
 Gradients other than ``tiny`` are near low-rank with a high condition number:
 ``G = sum_{i<32} 0.7^i u_i v_i^T + 0.01 N(0,1)`` with raw N(0,1) vectors ``u_i, v_i``,
@@ -136,6 +137,16 @@ def _split_moe() -> Workload:
     return Workload("split_moe", 4, names, shapes)
 
 
+def _split_moe_heads() -> Workload:
+    """The Split/MoE set's query head blocks alone (512 blocks of 128x4096, 268M
+    elements): the small-matrix kernel's share of that set, small enough for profiler
+    captures."""
+    full = _split_moe()
+    keep = [i for i, s in enumerate(full.muon_shapes) if s == (128, 4096)]
+    return Workload("split_moe_heads", 4, [full.muon_names[i] for i in keep],
+                    [full.muon_shapes[i] for i in keep])
+
+
 WORKLOADS = {
     "tiny": _tiny,
     "layer1024": _layer1024,
@@ -143,6 +154,7 @@ WORKLOADS = {
     "llama7b": _llama7b,
     "llama7b_layer": _llama7b_layer,
     "split_moe": _split_moe,
+    "split_moe_heads": _split_moe_heads,
 }
 
 
