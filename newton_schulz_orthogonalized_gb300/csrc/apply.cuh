@@ -11,61 +11,73 @@
 namespace nsm {
 namespace {
 
-// O's apply at natural positions (see ApplyArgs): o[j] is the stored-precision O at
-// class (row, gc0 + j) of matrix mt.  Every load of the chunk is issued before its first
-// store, so the 32 read-modify-writes of a lane overlap instead of queueing behind one
-// another.
-__device__ __forceinline__ void apply_chunk(const ApplyArgs& ap, const MatInfo& mt, int row, int gc0,
-                                            int ncols, const float (&o)[32]) {
+// O's apply at natural positions (see ApplyArgs).  A chunk is the 32 elements
+// (row, gc0 + j), j < ncols, of matrix mt's class layout.  They live at natural
+// (row, gc0 + j), or at (gc0 + j, row) when the matrix is stored transposed in its class;
+// then the lanes of a warp cover consecutive natural columns.  apply_load reads the
+// chunk's parameters and apply_store writes the updated ones, so a caller can issue the
+// loads of the next chunk before the stores of this one.
+
+// The 32 parameters of a wide matrix's row segment are 16-byte aligned and contiguous.
+__device__ __forceinline__ bool apply_vec(const MatInfo& mt, int ncols) {
+  return !mt.transposed && ncols == 32 && mt.vec_ok;
+}
+
+__device__ __forceinline__ void apply_load(const ApplyArgs& ap, const MatInfo& mt, int row, int gc0, int ncols,
+                                           float (&pv)[32]) {
+  const float* __restrict__ p = ap.params + mt.off;
+  if (apply_vec(mt, ncols)) {
+    const float4* pp = reinterpret_cast<const float4*>(p + static_cast<int64_t>(row) * mt.cols + gc0);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float4 a = pp[w];
+      pv[4 * w + 0] = a.x;
+      pv[4 * w + 1] = a.y;
+      pv[4 * w + 2] = a.z;
+      pv[4 * w + 3] = a.w;
+    }
+    return;
+  }
+  const int64_t step = mt.transposed ? mt.cols : 1;
+  const int64_t i0 = mt.transposed ? static_cast<int64_t>(gc0) * mt.cols + row
+                                   : static_cast<int64_t>(row) * mt.cols + gc0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) pv[j] = j < ncols ? p[i0 + j * step] : 0.f;
+}
+
+// p <- pv (1 - lr wd) - lr scale o, and its bf16 copy when requested.
+__device__ __forceinline__ void apply_store(const ApplyArgs& ap, const MatInfo& mt, int row, int gc0, int ncols,
+                                            const float (&o)[32], const float (&pv)[32]) {
   float* __restrict__ p = ap.params + mt.off;
   __nv_bfloat16* __restrict__ pb =
       ap.params_bf16 ? reinterpret_cast<__nv_bfloat16*>(ap.params_bf16) + mt.off : nullptr;
   const float coef = ap.lr * mt.scale;
   const float decay = ap.decay;
-  if (!mt.transposed && ncols == 32 && mt.vec_ok) {
-    // class row = natural row: 32 consecutive parameters of this lane
+  if (apply_vec(mt, ncols)) {
     const int64_t i0 = static_cast<int64_t>(row) * mt.cols + gc0;
     float4* pp = reinterpret_cast<float4*>(p + i0);
-    float4 a[8];
+    float np[32];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) a[w] = pp[w];
+    for (int j = 0; j < 32; ++j) np[j] = fmaf(-coef, o[j], pv[j] * decay);
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      a[w].x = fmaf(-coef, o[4 * w + 0], a[w].x * decay);
-      a[w].y = fmaf(-coef, o[4 * w + 1], a[w].y * decay);
-      a[w].z = fmaf(-coef, o[4 * w + 2], a[w].z * decay);
-      a[w].w = fmaf(-coef, o[4 * w + 3], a[w].w * decay);
-      pp[w] = a[w];
-    }
+    for (int w = 0; w < 8; ++w) pp[w] = make_float4(np[4 * w], np[4 * w + 1], np[4 * w + 2], np[4 * w + 3]);
     if (pb) {
+      // i0 is a multiple of 8 elements and the copy is 16-byte aligned
       uint4* q = reinterpret_cast<uint4*>(pb + i0);
-      const bool q16 = (reinterpret_cast<uintptr_t>(q) & 15) == 0;
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        __nv_bfloat162 h[4] = {__floats2bfloat162_rn(a[2 * w].x, a[2 * w].y),
-                               __floats2bfloat162_rn(a[2 * w].z, a[2 * w].w),
-                               __floats2bfloat162_rn(a[2 * w + 1].x, a[2 * w + 1].y),
-                               __floats2bfloat162_rn(a[2 * w + 1].z, a[2 * w + 1].w)};
-        if (q16) {
-          q[w] = *reinterpret_cast<const uint4*>(h);
-        } else {
-          __nv_bfloat162* q2 = reinterpret_cast<__nv_bfloat162*>(pb + i0 + 8 * w);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) q2[k] = h[k];
-        }
+        __nv_bfloat162 h[4] = {__floats2bfloat162_rn(np[8 * w + 0], np[8 * w + 1]),
+                               __floats2bfloat162_rn(np[8 * w + 2], np[8 * w + 3]),
+                               __floats2bfloat162_rn(np[8 * w + 4], np[8 * w + 5]),
+                               __floats2bfloat162_rn(np[8 * w + 6], np[8 * w + 7])};
+        q[w] = *reinterpret_cast<const uint4*>(h);
       }
     }
     return;
   }
-  // general case: element (class row, gc0 + j) lives at natural (row, gc0 + j), or at
-  // (gc0 + j, row) when the matrix is stored transposed in its class (then the lanes of
-  // a warp cover consecutive natural columns)
   const int64_t step = mt.transposed ? mt.cols : 1;
   const int64_t i0 = mt.transposed ? static_cast<int64_t>(gc0) * mt.cols + row
                                    : static_cast<int64_t>(row) * mt.cols + gc0;
-  float pv[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) pv[j] = j < ncols ? p[i0 + j * step] : 0.f;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     if (j < ncols) {
@@ -74,6 +86,13 @@ __device__ __forceinline__ void apply_chunk(const ApplyArgs& ap, const MatInfo& 
       if (pb) pb[i0 + j * step] = __float2bfloat16_rn(np);
     }
   }
+}
+
+__device__ __forceinline__ void apply_chunk(const ApplyArgs& ap, const MatInfo& mt, int row, int gc0,
+                                            int ncols, const float (&o)[32]) {
+  float pv[32];
+  apply_load(ap, mt, row, gc0, ncols, pv);
+  apply_store(ap, mt, row, gc0, ncols, o, pv);
 }
 
 }  // namespace

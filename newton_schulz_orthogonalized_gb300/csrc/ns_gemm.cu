@@ -151,13 +151,69 @@ __device__ __forceinline__ void signal_timeout(Ctrl<STAGES>* ctrl, int* status) 
 
 // Epilogue of one accumulator: this warp's 32 rows (rows rb .. rb+31 of the matrix,
 // TMEM lanes 32*quarter ..), the tile's n_len columns from column n0.
+// Epilogue of the product that forms O when the step is applied: out = alpha acc +
+// beta aux + diag I is rounded to O's storage format and applied to the parameters
+// (apply_store) instead of being stored.  The parameters of chunk c + 1 are loaded
+// before chunk c is drained and applied, so two chunks of load latency overlap with
+// the tensor-memory reads.
+template <bool FP16, bool HAS_AUX>
+__device__ __forceinline__ void epilogue_apply_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
+                                                    uint32_t t_row, int lane, float alpha, float beta,
+                                                    float diag, const ApplyArgs& ap) {
+  using E = Elem<FP16>;
+  using T = typename E::T;
+  const MatInfo& mt = ap.mats[__ldg(G.mat_index + b)];
+  const int row = rb + lane;
+  const bool row_ok = row < G.M;
+  const int nchunks = (n_len + 31) >> 5;
+  const T* aux_row = nullptr;
+  if (HAS_AUX) {
+    aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(b) * G.aux_bstride +
+              static_cast<int64_t>(row) * G.ld_aux + n0;
+  }
+  float cur[32], nxt[32];
+  if (row_ok) apply_load(ap, mt, row, n0, min(32, n_len), cur);
+#pragma unroll 1
+  for (int c = 0; c < nchunks; ++c) {
+    const int col0 = c * 32;
+    const int ncols = min(32, n_len - col0);
+    if (row_ok && c + 1 < nchunks) apply_load(ap, mt, row, n0 + col0 + 32, min(32, n_len - col0 - 32), nxt);
+    uint32_t r[32];
+    __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
+    ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(col0), r);
+    ptx::tmem_ld_wait();
+    if (row_ok) {
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
+      if (HAS_AUX) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < ncols) v[j] += beta * E::to_f(aux_row[col0 + j]);
+        }
+      }
+      if (diag != 0.0f) {
+        const int d = row - (n0 + col0);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (d == j) v[j] += diag;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = E::to_f(E::from_f(v[j]));  // O as stored
+      apply_store(ap, mt, row, n0 + col0, ncols, v, cur);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
+  }
+}
+
 template <bool FP16, bool HAS_AUX>
 __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
                                               uint32_t t_row, float* xt, int lane, float alpha,
-                                              float beta, float diag, const ApplyArgs& ap) {
+                                              float beta, float diag) {
   using E = Elem<FP16>;
   using T = typename E::T;
-  const MatInfo* apply_mt = ap.params ? ap.mats + __ldg(G.mat_index + b) : nullptr;
   const int row = rb + lane;
   const bool row_ok = row < G.M;
   const int nchunks = (n_len + 31) >> 5;
@@ -203,13 +259,6 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
         for (int j = 0; j < 32; ++j) {
           if (d == j) v[j] += diag;
         }
-      }
-      if (apply_mt) {
-        // the step's last product: round O to its storage format, then apply it
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = E::to_f(E::from_f(v[j]));
-        apply_chunk(ap, *apply_mt, row, gc0, full ? 32 : n_len - col0, v);
-        continue;
       }
       // a symmetric output stores only its upper triangle (column >= row) directly
       const int first_col = G.sym ? row : 0;
@@ -448,8 +497,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-      epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                   t_row, xt, lane, alpha, beta, diag, ap);
+      if (ap.params) {
+        epilogue_apply_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
+                                           t_row, lane, alpha, beta, diag, ap);
+      } else {
+        epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
+                                     t_row, xt, lane, alpha, beta, diag);
+      }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(&ctrl->acc_empty[acc]));
@@ -697,8 +751,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
       const int rb = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
-      epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, xt, lane,
-                                   alpha, beta, diag, ap);
+      if (ap.params) {
+        epilogue_apply_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, lane, alpha,
+                                           beta, diag, ap);
+      } else {
+        epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, xt, lane, alpha,
+                                     beta, diag);
+      }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(&ctrl->acc_empty[acc]), 0));
