@@ -14,8 +14,9 @@
 //                   traffic of the 1-CTA tile for the same tensor-core work.
 // Roles inside a CTA: warp 0 issues TMA loads (128B-swizzled 64x64 boxes) into a ring of
 // stages, warp 1 issues the MMAs (the leader CTA's, in the pair kernel) into two TMEM
-// accumulators of 256 fp32 columns, warps 2-5 drain TMEM with tcgen05.ld and apply the
-// fused epilogue  out = alpha*acc + beta*aux + diag*I  before storing bf16/fp16.
+// accumulators of 256 fp32 columns, warps 2-5 drain TMEM with tcgen05.ld, apply the
+// fused epilogue  out = alpha*acc + beta*aux + diag*I  and store fp16/bf16 32 x 32 blocks
+// through shared memory with TMA stores.
 // A group flagged symmetric computes only the tiles that touch the upper triangle, stores
 // that triangle and mirrors it.
 //
@@ -55,7 +56,7 @@ constexpr uint32_t TMEM_COLS = 512;       // 2 x 256 fp32 accumulator columns
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 constexpr int kPanel = 8;                 // column tiles per raster panel
 constexpr int EPI_WARPS = 4;
-constexpr int XPOSE_BYTES = EPI_WARPS * 32 * 33 * 4;  // per-warp 32x32 fp32 transpose tiles
+constexpr int EPI_STAGE_BYTES = EPI_WARPS * 8192;   // per epilogue warp: 2 slots of 2 x 2 KB staged blocks
 
 // 1-CTA kernel: 128 x 256 tiles, 4 stages of A 16 KB + B 32 KB.
 constexpr int S1_STAGES = 4;
@@ -81,8 +82,8 @@ struct Ctrl {
   int never;  // stays 0: the flag the teardown waits poll, so they ignore `abort`
 };
 
-constexpr size_t S1_SMEM = 1024 + size_t(S1_STAGES) * S1_STAGE_BYTES + XPOSE_BYTES + sizeof(Ctrl<S1_STAGES>);
-constexpr size_t S2_SMEM = 1024 + size_t(S2_STAGES) * S2_STAGE_BYTES + XPOSE_BYTES + sizeof(Ctrl<S2_STAGES>);
+constexpr size_t S1_SMEM = 1024 + size_t(S1_STAGES) * S1_STAGE_BYTES + EPI_STAGE_BYTES + sizeof(Ctrl<S1_STAGES>);
+constexpr size_t S2_SMEM = 1024 + size_t(S2_STAGES) * S2_STAGE_BYTES + EPI_STAGE_BYTES + sizeof(Ctrl<S2_STAGES>);
 static_assert(S1_SMEM <= 232448 && S2_SMEM <= 232448, "shared memory per CTA");
 
 struct TileCoord {
@@ -151,6 +152,66 @@ __device__ __forceinline__ void signal_timeout(Ctrl<STAGES>* ctrl, int* status) 
 
 // Epilogue of one accumulator: this warp's 32 rows (rows rb .. rb+31 of the matrix,
 // TMEM lanes 32*quarter ..), the tile's n_len columns from column n0.
+// Two values rounded to the storage format and packed into one 32-bit word (the first
+// in the low half), with one conversion instruction.
+template <bool FP16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<true>(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<false>(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 16-bit element j of a packed row (element 2i in the low half of word i).
+__device__ __forceinline__ uint16_t half_of(const uint32_t (&h)[16], int j) {
+  return static_cast<uint16_t>((j & 1) ? (h[j >> 1] >> 16) : (h[j >> 1] & 0xffffu));
+}
+
+// v = alpha acc (+ beta aux) (+ diag on the diagonal) for one 32-column chunk of this
+// lane's row.
+template <bool FP16, bool HAS_AUX>
+__device__ __forceinline__ void chunk_values(const uint32_t (&r)[32], const typename Elem<FP16>::T* aux_row,
+                                             bool row_ok, int col0, bool full, int n_len, int d, float alpha,
+                                             float beta, float diag, float (&v)[32]) {
+  using E = Elem<FP16>;
+  using T = typename E::T;
+  if (alpha == 1.0f) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
+  }
+  if (HAS_AUX && row_ok) {  // rows past M have no aux row
+    if (full) {
+      const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint4 pk = __ldg(src + w);
+        const T* e = reinterpret_cast<const T*>(&pk);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[w * 8 + j] += beta * E::to_f(e[j]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (col0 + j < n_len) v[j] += beta * E::to_f(aux_row[col0 + j]);
+      }
+    }
+  }
+  if (diag != 0.0f) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (d == j) v[j] += diag;
+    }
+  }
+}
+
 // Epilogue of the product that forms O when the step is applied: out = alpha acc +
 // beta aux + diag I is rounded to O's storage format and applied to the parameters
 // (apply_store) instead of being stored.  The parameters of chunk c + 1 are loaded
@@ -184,21 +245,8 @@ __device__ __forceinline__ void epilogue_apply_rows(const GemmGroup& G, int b, i
     ptx::tmem_ld_wait();
     if (row_ok) {
       float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
-      if (HAS_AUX) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j < ncols) v[j] += beta * E::to_f(aux_row[col0 + j]);
-        }
-      }
-      if (diag != 0.0f) {
-        const int d = row - (n0 + col0);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (d == j) v[j] += diag;
-        }
-      }
+      chunk_values<FP16, HAS_AUX>(r, aux_row, true, col0, ncols == 32, n_len, row - (n0 + col0), alpha, beta, diag,
+                                  v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = E::to_f(E::from_f(v[j]));  // O as stored
       apply_store(ap, mt, row, n0 + col0, ncols, v, cur);
@@ -208,10 +256,15 @@ __device__ __forceinline__ void epilogue_apply_rows(const GemmGroup& G, int b, i
   }
 }
 
+// Epilogue of a stored product whose rows are not a whole number of 16-byte units (the
+// TMA store path needs that): out = alpha acc + beta aux + diag I, rounded once and stored
+// by each lane for its row.  A symmetric output stores its upper triangle directly and
+// mirrors the strict upper triangle: the warp's 32 x 32 block is transposed through
+// shared memory (32 rows of 17 words) as packed 16-bit pairs.
 template <bool FP16, bool HAS_AUX>
-__device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
-                                              uint32_t t_row, float* xt, int lane, float alpha,
-                                              float beta, float diag) {
+__device__ __forceinline__ void epilogue_rows_direct(const GemmGroup& G, int b, int rb, int n0, int n_len,
+                                                     uint32_t t_row, uint32_t* xw, int lane, float alpha,
+                                                     float beta, float diag) {
   using E = Elem<FP16>;
   using T = typename E::T;
   const int row = rb + lane;
@@ -224,93 +277,130 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
     aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(b) * G.aux_bstride +
               static_cast<int64_t>(row) * G.ld_aux + n0;
   }
+  const int first_col = G.sym ? row : 0;  // a symmetric output stores columns >= row
   for (int c = 0; c < nchunks; ++c) {
     uint32_t r[32];
     __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
     ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
     ptx::tmem_ld_wait();
     const int col0 = c * 32;
-    const int gc0 = n0 + col0;  // first column of this chunk in the matrix
+    const int gc0 = n0 + col0;
     const bool full = col0 + 32 <= n_len;
-    float v[32];
+    uint32_t h[16];
+    {
+      float v[32];
+      chunk_values<FP16, HAS_AUX>(r, aux_row, row_ok, col0, full, n_len, row - gc0, alpha, beta, diag, v);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
+      for (int i = 0; i < 16; ++i) h[i] = pack2<FP16>(v[2 * i], v[2 * i + 1]);
+    }
     if (row_ok) {
-      if (HAS_AUX) {
-        if (full) {
-          const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
+      uint16_t* o16 = reinterpret_cast<uint16_t*>(out_row + col0);
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint4 pk = __ldg(src + w);
-            const T* e = reinterpret_cast<const T*>(&pk);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[w * 8 + j] += beta * E::to_f(e[j]);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (col0 + j < n_len) v[j] += beta * E::to_f(aux_row[col0 + j]);
-          }
-        }
-      }
-      if (diag != 0.0f) {
-        const int d = row - gc0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (d == j) v[j] += diag;
-        }
-      }
-      // a symmetric output stores only its upper triangle (column >= row) directly
-      const int first_col = G.sym ? row : 0;
-      if (full && gc0 >= first_col) {
-        uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint4 pk;
-          T* e = reinterpret_cast<T*>(&pk);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) e[j] = E::from_f(v[w * 8 + j]);
-          dst[w] = pk;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (col0 + j < n_len && gc0 + j >= first_col) out_row[col0 + j] = E::from_f(v[j]);
-        }
+      for (int j = 0; j < 32; ++j) {
+        if (col0 + j < n_len && gc0 + j >= first_col) o16[j] = half_of(h, j);
       }
     }
     if (G.sym && gc0 + 31 > rb) {
-      // Mirror the strict upper triangle.  The warp's 32x32 block (rows rb.., columns
-      // gc0..) is transposed in shared memory, so lane l writes the contiguous piece of
-      // mirrored row gc0 + l.  Lanes whose row is out of range hold values that the row
-      // mask below never stores.
+      // lanes whose row is out of range hold values that the row mask below never stores
 #pragma unroll
-      for (int j = 0; j < 32; ++j) xt[lane * 33 + j] = v[j];
+      for (int i = 0; i < 16; ++i) xw[lane * 17 + i] = h[i];
       __syncwarp();
+      // lane l gathers column gc0 + l: rows 2i and 2i + 1 from two words, its half of each
+      const int wc = lane >> 1;
+      const uint32_t sel = (lane & 1) ? 0x7632u : 0x5410u;
+      uint32_t m[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m[i] = __byte_perm(xw[(2 * i) * 17 + wc], xw[(2 * i + 1) * 17 + wc], sel);
       const int mr = gc0 + lane;
       if (mr < G.N && col0 + lane < n_len) {
-        T* mrow = reinterpret_cast<T*>(G.out) + static_cast<int64_t>(b) * G.out_bstride +
-                  static_cast<int64_t>(mr) * G.ld_out + rb;
-        if (gc0 >= rb + 32 && rb + 32 <= G.M) {
-          // block strictly above the diagonal: the whole mirrored piece is stored
-          uint4* dst = reinterpret_cast<uint4*>(mrow);
+        uint16_t* m16 = reinterpret_cast<uint16_t*>(reinterpret_cast<T*>(G.out) +
+                                                    static_cast<int64_t>(b) * G.out_bstride +
+                                                    static_cast<int64_t>(mr) * G.ld_out + rb);
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint4 pk;
-            T* e = reinterpret_cast<T*>(&pk);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) e[j] = E::from_f(xt[(w * 8 + j) * 33 + lane]);
-            dst[w] = pk;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (rb + j < G.M && mr > rb + j) mrow[j] = E::from_f(xt[j * 33 + lane]);
-          }
+        for (int j = 0; j < 32; ++j) {
+          if (rb + j < G.M && mr > rb + j) m16[j] = half_of(m, j);
         }
       }
       __syncwarp();
     }
+  }
+}
+
+// Byte offset of 16-bit element (row, col) of a 32 x 32 block staged for a TMA store
+// with 64-byte swizzle: 64-byte rows, the 16-byte unit index XOR (row / 2) mod 4.
+__device__ __forceinline__ uint32_t sw64(int row, int col) {
+  return static_cast<uint32_t>(row * 64 + ((((col >> 3) ^ (row >> 1)) & 3) << 4) + (col & 7) * 2);
+}
+
+// Epilogue of a stored product: out = alpha acc + beta aux + diag I, rounded once.  The
+// warp stages each 32 x 32 block of its rows in shared memory and one lane stores it
+// with a TMA store (full lines into L2, instead of 16-byte pieces of 32 rows per store
+// instruction).  A symmetric output stores the blocks on and above the diagonal: an
+// upper block is also staged transposed and stored at the mirrored position, and the
+// diagonal block is completed from its own upper triangle before its store.  Every
+// element is written once.  Two slots of 4 KB (block + transposed block) alternate;
+// `nst` counts the warp's store groups.
+template <bool FP16, bool HAS_AUX>
+__device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
+                                              uint32_t t_row, uint32_t stage, uint32_t& nst, int lane,
+                                              float alpha, float beta, float diag) {
+  using E = Elem<FP16>;
+  using T = typename E::T;
+  if (rb >= G.M) return;  // the warp's rows are past the matrix
+  const int row = rb + lane;
+  const bool row_ok = row < G.M;
+  const int nchunks = (n_len + 31) >> 5;
+  const T* aux_row = nullptr;
+  if (HAS_AUX) {
+    aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(b) * G.aux_bstride +
+              static_cast<int64_t>(row) * G.ld_aux + n0;
+  }
+  for (int c = 0; c < nchunks; ++c) {
+    const int col0 = c * 32;
+    const int gc0 = n0 + col0;  // first column of this block in the matrix
+    if (G.sym && gc0 < rb) continue;  // below the diagonal: written as the mirror of its upper block
+    const bool diag_blk = G.sym && gc0 == rb;
+    const bool upper_blk = G.sym && gc0 > rb;
+    uint32_t r[32];
+    __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
+    ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(col0), r);
+    ptx::tmem_ld_wait();
+    uint32_t h[16];
+    {
+      float v[32];
+      chunk_values<FP16, HAS_AUX>(r, aux_row, row_ok, col0, col0 + 32 <= n_len, n_len, row - gc0, alpha, beta,
+                                  diag, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) h[i] = pack2<FP16>(v[2 * i], v[2 * i + 1]);
+    }
+    const uint32_t slot = stage + (nst & 1u) * 4096u;
+    if (nst >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();  // the store two blocks back has read it
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      ptx::st_shared_v4(slot + static_cast<uint32_t>(lane * 64 + (((u ^ (lane >> 1)) & 3) << 4)), h[4 * u],
+                        h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
+    }
+    if (diag_blk) {
+      // strictly lower elements (j, lane), j > lane, are this lane's (lane, j)
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j > lane) ptx::st_shared_u16(slot + sw64(j, lane), half_of(h, j));
+      }
+    } else if (upper_blk) {
+      // transposed block: its row j is column j of this block
+#pragma unroll
+      for (int j = 0; j < 32; ++j) ptx::st_shared_u16(slot + 2048u + sw64(j, lane), half_of(h, j));
+    }
+    ptx::fence_proxy_async_smem();  // the TMA engine reads the staged blocks next
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_3d(G.map_out, slot, gc0, rb, b);
+      if (upper_blk) ptx::tma_store_3d(G.map_out, slot + 2048u, rb, gc0, b);
+      ptx::bulk_commit_group();
+    }
+    ++nst;
   }
 }
 
@@ -324,8 +414,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* xpose = reinterpret_cast<float*>(smem + size_t(STAGES) * S1_STAGE_BYTES);
-  auto* ctrl = reinterpret_cast<Ctrl<STAGES>*>(smem + size_t(STAGES) * S1_STAGE_BYTES + XPOSE_BYTES);
+  uint8_t* epi_base = smem + size_t(STAGES) * S1_STAGE_BYTES;
+  const uint32_t epi_stage = ptx::smem_u32(epi_base);
+  auto* ctrl = reinterpret_cast<Ctrl<STAGES>*>(smem + size_t(STAGES) * S1_STAGE_BYTES + EPI_STAGE_BYTES);
   const uint32_t ring = ptx::smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -479,7 +570,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int quarter = warp & 3;  // TMEM lanes this warp may access: 32*quarter + [0, 32)
-    float* xt = xpose + (warp - 2) * (32 * 33);
+    const uint32_t stage = epi_stage + static_cast<uint32_t>(warp - 2) * 8192u;  // 1024-byte aligned
+    uint32_t* stage_words = reinterpret_cast<uint32_t*>(epi_base + (warp - 2) * 8192);
+    uint32_t nst = 0;
     int local = 0;
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
       const TileCoord tc = decode_tile<128>(groups, ng, t);
@@ -501,13 +594,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         epilogue_apply_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
                                            t_row, lane, alpha, beta, diag, ap);
       } else {
-        epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                     t_row, xt, lane, alpha, beta, diag);
+        if (G.map_out) {
+          epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
+                                       t_row, stage, nst, lane, alpha, beta, diag);
+        } else {
+          epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
+                                              t_row, stage_words, lane, alpha, beta, diag);
+        }
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(&ctrl->acc_empty[acc]));
     }
+    // staged blocks must be read out by the TMA engine before the block exits
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -543,8 +644,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* xpose = reinterpret_cast<float*>(smem + size_t(STAGES) * S2_STAGE_BYTES);
-  auto* ctrl = reinterpret_cast<Ctrl<STAGES>*>(smem + size_t(STAGES) * S2_STAGE_BYTES + XPOSE_BYTES);
+  uint8_t* epi_base = smem + size_t(STAGES) * S2_STAGE_BYTES;
+  const uint32_t epi_stage = ptx::smem_u32(epi_base);
+  auto* ctrl = reinterpret_cast<Ctrl<STAGES>*>(smem + size_t(STAGES) * S2_STAGE_BYTES + EPI_STAGE_BYTES);
   const uint32_t ring = ptx::smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -732,7 +834,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int quarter = warp & 3;
-    float* xt = xpose + (warp - 2) * (32 * 33);
+    const uint32_t stage = epi_stage + static_cast<uint32_t>(warp - 2) * 8192u;  // 1024-byte aligned
+    uint32_t* stage_words = reinterpret_cast<uint32_t*>(epi_base + (warp - 2) * 8192);
+    uint32_t nst = 0;
     int local = 0;
     for (int64_t t = pair; t < total_tiles; t += npairs, ++local) {
       const TileCoord tc = decode_tile<256>(groups, ng, t);
@@ -755,13 +859,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         epilogue_apply_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, lane, alpha,
                                            beta, diag, ap);
       } else {
-        epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, xt, lane, alpha,
-                                     beta, diag);
+        if (G.map_out) {
+          epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage, nst, lane,
+                                       alpha, beta, diag);
+        } else {
+          epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage_words,
+                                              lane, alpha, beta, diag);
+        }
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(&ctrl->acc_empty[acc]), 0));
     }
+    // staged blocks must be read out by the TMA engine before the block exits
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
   }
 
   // no MMA of the pair may still write this CTA's TMEM when it is freed

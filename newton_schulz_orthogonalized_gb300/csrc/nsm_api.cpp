@@ -197,8 +197,11 @@ EncodeTiledFn get_encode_fn() {
 
 // 3D map over `count` back-to-back row-major matrices of rows x inner (row stride ld),
 // box 64 x box_rows x 1, 128-byte swizzle, zero fill outside the matrix.
+// 3D map {inner, rows, count} of 16-bit elements.  Load maps take 64-wide boxes of
+// box_rows rows with 128-byte swizzle; store maps (store = true) 32 x 32 boxes with
+// 64-byte swizzle.
 int encode_map(CUtensorMap* map, void* base, bool fp16, int inner, int rows, int ld, int count,
-               const char* ws_begin, const char* ws_end, int box_rows = 64) {
+               const char* ws_begin, const char* ws_end, int box_rows = 64, bool store = false) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return fail(NSM_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const size_t row_bytes = size_t(ld) * 2;
@@ -209,10 +212,11 @@ int encode_map(CUtensorMap* map, void* base, bool fp16, int inner, int rows, int
     return fail(NSM_ERR_WORKSPACE, "internal: tensor map exceeds the workspace");
   cuuint64_t dims[3] = {cuuint64_t(inner), cuuint64_t(rows), cuuint64_t(count)};
   cuuint64_t strides[2] = {cuuint64_t(row_bytes), cuuint64_t(mat_bytes)};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t box[3] = {store ? 32u : 64u, store ? 32u : static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
-                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  store ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(NSM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
   return NSM_OK;
@@ -589,7 +593,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   for (int c = 0; c < nclass; ++c) class_first[c + 1] = class_first[c] + L.classes[c].count;
   const size_t matidx_off = mats_bytes;
   const size_t maps_off = matidx_off + align_up(sizeof(int32_t) * size_t(n), 128);
-  constexpr int kBoxKinds = 3;  // box heights 64, 128, 256 rows
+  constexpr int kBoxKinds = 4;  // load boxes of 64, 128, 256 rows; 32 x 32 store boxes
   const size_t maps_bytes = align_up(sizeof(CUtensorMap) * size_t(nclass) * nbuf * kBoxKinds, 128);
   const size_t groups_off = maps_off + maps_bytes;
   const size_t groups_bytes = align_up(sizeof(GemmGroup) * size_t(nclass) * stages.size(), 128);
@@ -642,17 +646,20 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     for (int b = 0; b < nbuf; ++b) {
       for (int k = 0; k < kBoxKinds; ++k) {
         CUtensorMap* map = &hmaps[(size_t(c) * nbuf + b) * kBoxKinds + k];
-        const int box = 64 << k;
+        const int box = 64 << (k % 3);
+        const bool store = k == 3;
         int rc;
-        if (b < MM0) rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.n, sc.m, sc.ldn, sc.count, ws_begin, ws_end, box);
-        else rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.m, sc.m, sc.ldm, sc.count, ws_begin, ws_end, box);
+        if (b < MM0)
+          rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.n, sc.m, sc.ldn, sc.count, ws_begin, ws_end, box, store);
+        else
+          rc = encode_map(map, buf_base(b, c), P.x_fp16, sc.m, sc.m, sc.ldm, sc.count, ws_begin, ws_end, box, store);
         if (rc != NSM_OK) return rc;
       }
     }
   }
-  // map of buffer b of class c with boxes of `box` rows
+  // map of buffer b of class c with load boxes of `box` rows, or its store map (box 0)
   auto dmap = [&](int c, int b, int box) {
-    const int k = box >= 256 ? 2 : (box >= 128 ? 1 : 0);
+    const int k = box == 0 ? 3 : (box >= 256 ? 2 : (box >= 128 ? 1 : 0));
     return reinterpret_cast<const CUtensorMap*>(dbase + maps_off) + (size_t(c) * nbuf + b) * kBoxKinds + k;
   };
 
@@ -718,6 +725,8 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       g.map_b = dmap(c, st.b_buf, g.b_box);
       const bool out_x = st.out_buf < MM0;
       g.out = buf_base(st.out_buf, c);
+      // TMA stores write whole 16-byte units of a row: only for rows of a multiple of 8
+      g.map_out = ((st.n_is_n ? sc.n : sc.m) % 8 == 0) ? dmap(c, st.out_buf, 0) : nullptr;
       g.ld_out = out_x ? sc.ldn : sc.ldm;
       g.out_bstride = int64_t(sc.m) * g.ld_out;
       if (st.aux_buf >= 0) {
@@ -1279,7 +1288,7 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   if (aux && ranges_overlap(aux, size_t(M) * ldx * 2, out, size_t(M) * ldo * 2))
     return fail(NSM_ERR_ARG, "aux must not overlap out");
   struct Blob {
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mo;
     GemmGroup g;
   };
   static_assert(sizeof(Blob) <= 1024, "scratch blob");
@@ -1292,10 +1301,17 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   if (b_mn_major) rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, N, K, ldb, 1, nullptr, nullptr, b_box);
   else rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, K, N, ldb, 1, nullptr, nullptr, b_box);
   if (rc != NSM_OK) return rc;
+  // TMA stores write whole 16-byte units of a row: only for rows of a multiple of 8
+  const bool tma_store = N % 8 == 0;
+  if (tma_store) {
+    rc = encode_map(&blob.mo, out, fp16 != 0, N, M, ldo, 1, nullptr, nullptr, 64, true);
+    if (rc != NSM_OK) return rc;
+  }
   Blob* d = static_cast<Blob*>(scratch);
   GemmGroup& g = blob.g;
   g.map_a = &d->ma;
   g.map_b = &d->mb;
+  g.map_out = tma_store ? &d->mo : nullptr;
   g.out = out;
   g.aux = aux;
   g.ld_out = ldo;
@@ -1347,7 +1363,7 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
 }
 
 size_t nsm_gemm_scratch_bytes(int M, int N, int flags) {
-  size_t b = 2 * sizeof(CUtensorMap) + sizeof(GemmGroup);
+  size_t b = 3 * sizeof(CUtensorMap) + sizeof(GemmGroup);
   if ((flags & NSM_GEMM_SYMMETRIC) && M > 0 && M == N)
     b += upper_tiles(M, (flags & NSM_GEMM_PAIR) ? 256 : 128).size() * sizeof(int32_t);
   return align_up(b, 128);

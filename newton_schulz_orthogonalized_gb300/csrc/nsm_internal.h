@@ -54,7 +54,8 @@ struct GemmGroup {
   int32_t sym, tiles_per_mat;
   int32_t a_box, b_box;  // rows per TMA box of map_a / map_b (64, 128 or 256)
   const int32_t* mat_index;  // matrix (MatInfo index) of each batch entry
-  int64_t pad;
+  const CUtensorMap* map_out;  // the output in 32 x 32 boxes with 64-byte swizzle (TMA stores);
+                               // NULL when N is not a multiple of 8 (rows of whole 16-byte units)
 };
 static_assert(sizeof(GemmGroup) == 128, "GemmGroup layout");
 
