@@ -20,7 +20,7 @@ namespace {
 
 // The 32 parameters of a wide matrix's row segment are 16-byte aligned and contiguous.
 __device__ __forceinline__ bool apply_vec(const MatInfo& mt, int ncols) {
-  return !mt.transposed && ncols == 32 && mt.vec_ok;
+  return !mt.transposed && ncols == 32 && (mt.flags & kMatVec);
 }
 
 __device__ __forceinline__ void apply_load(const ApplyArgs& ap, const MatInfo& mt, int row, int gc0, int ncols,

@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads)
     const float sc = scales[tp.mi];
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
     if (!mt.transposed) {
-      if (mt.vec_ok) {
+      if (mt.flags & kMatVec) {
         for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
           const int r = tp.r0 + (j >> 3), c = tp.c0 + (j & 7) * 8;
           if (r < rows && c < cols) {
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     } else {
       // slot row = natural column c, slot column = natural row r
-      if (mt.vec_ok) {
+      if (mt.flags & kMatVec) {
         for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
           const int rr = j >> 3, cc = (j & 7) * 8;
           const int r = tp.r0 + rr, c = tp.c0 + cc;
@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(kThreads)
   for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
     const TilePos tp = tile_pos(mats, nmats, t);
     const MatInfo& mt = mats[tp.mi];
+    if (APPLY && (mt.flags & kMatInChain)) continue;  // already applied by the small-matrix kernel
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
     const int64_t s0 = mt.slot;
     const float coef = lr * mt.scale;
@@ -326,7 +327,7 @@ __global__ void __launch_bounds__(kThreads)
     __nv_bfloat16* ob = out ? out + mt.off : nullptr;
     if (mt.transposed) {
       // tile[rr][cc] = O^T[r0+rr][c0+cc] = slot[c0+cc][r0+rr]
-      if (mt.vec_ok) {
+      if (mt.flags & kMatVec) {
         for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
           const int cc = j >> 3, rr = (j & 7) * 8;
           const int c = tp.c0 + cc, r = tp.r0 + rr;
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kThreads)
       }
       __syncthreads();
     }
-    if (mt.vec_ok) {
+    if (mt.flags & kMatVec) {
       for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
         const int rr = j >> 3, cc = (j & 7) * 8;
         const int r = tp.r0 + rr, c = tp.c0 + cc;

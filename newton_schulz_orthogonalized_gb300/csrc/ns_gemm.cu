@@ -136,12 +136,14 @@ struct Elem<false> {
   using T = __nv_bfloat16;
   __device__ static __forceinline__ float to_f(T v) { return __bfloat162float(v); }
   __device__ static __forceinline__ T from_f(float v) { return __float2bfloat16_rn(v); }
+  __device__ static __forceinline__ float bits_to_f(uint16_t v) { return __bfloat162float(__ushort_as_bfloat16(v)); }
 };
 template <>
 struct Elem<true> {
   using T = __half;
   __device__ static __forceinline__ float to_f(T v) { return __half2float(v); }
   __device__ static __forceinline__ T from_f(float v) { return __float2half_rn(v); }
+  __device__ static __forceinline__ float bits_to_f(uint16_t v) { return __half2float(__ushort_as_half(v)); }
 };
 
 template <int STAGES>
@@ -212,17 +214,21 @@ __device__ __forceinline__ void chunk_values(const uint32_t (&r)[32], const type
   }
 }
 
-// Epilogue of the product that forms O when the step is applied: out = alpha acc +
+// Epilogue of the product that forms O when the step is applied ("DeepSpeed 集成 Muon
+// 优化器实战" §核心算子: p <- p (1 - lr wd) - lr sqrt(max(1, rows/cols)) O): out = alpha acc +
 // beta aux + diag I is rounded to O's storage format and applied to the parameters
-// (apply_store) instead of being stored.  The parameters of chunk c + 1 are loaded
-// before chunk c is drained and applied, so two chunks of load latency overlap with
-// the tensor-memory reads.
+// instead of being stored.  Each lane updates one natural column of a 32 x 32 block of
+// the parameter matrix, so every load and store of the warp is one 128-byte access.
+// A tall matrix sits transposed in its class, so lane l's class row already is natural
+// column l; for a wide one the block of O is transposed through shared memory first.
+// The parameters of block c + 1 are loaded before block c is applied.
 template <bool FP16, bool HAS_AUX>
 __device__ __forceinline__ void epilogue_apply_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
-                                                    uint32_t t_row, int lane, float alpha, float beta,
-                                                    float diag, const ApplyArgs& ap) {
+                                                    uint32_t t_row, uint32_t* xw, int lane, float alpha,
+                                                    float beta, float diag, const ApplyArgs& ap) {
   using E = Elem<FP16>;
   using T = typename E::T;
+  if (rb >= G.M) return;  // the warp's rows are past the matrix
   const MatInfo& mt = ap.mats[__ldg(G.mat_index + b)];
   const int row = rb + lane;
   const bool row_ok = row < G.M;
@@ -232,24 +238,74 @@ __device__ __forceinline__ void epilogue_apply_rows(const GemmGroup& G, int b, i
     aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(b) * G.aux_bstride +
               static_cast<int64_t>(row) * G.ld_aux + n0;
   }
+  float* p = ap.params + mt.off;
+  __nv_bfloat16* pb = ap.params_bf16 ? reinterpret_cast<__nv_bfloat16*>(ap.params_bf16) + mt.off : nullptr;
+  const float coef = ap.lr * mt.scale;
+  const float decay = ap.decay;
+  const int64_t cols = mt.cols;
+  // block c covers natural rows r0 + j (j < nr) and columns c0 + lane (lane < nc)
+  auto origin = [&](int c, int& r0, int& c0, int& nr, int& nc) {
+    const int gc0 = n0 + 32 * c;
+    const int in_class_cols = min(32, n_len - 32 * c), in_class_rows = min(32, G.M - rb);
+    if (mt.transposed) {
+      r0 = gc0;
+      c0 = rb;
+      nr = in_class_cols;
+      nc = in_class_rows;
+    } else {
+      r0 = rb;
+      c0 = gc0;
+      nr = in_class_rows;
+      nc = in_class_cols;
+    }
+  };
+  auto load = [&](int c, float (&pv)[32]) {
+    int r0, c0, nr, nc;
+    origin(c, r0, c0, nr, nc);
+    const float* src = p + static_cast<int64_t>(r0) * cols + c0 + lane;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) pv[j] = (j < nr && lane < nc) ? src[j * cols] : 0.f;
+  };
   float cur[32], nxt[32];
-  if (row_ok) apply_load(ap, mt, row, n0, min(32, n_len), cur);
+  load(0, cur);
 #pragma unroll 1
   for (int c = 0; c < nchunks; ++c) {
+    if (c + 1 < nchunks) load(c + 1, nxt);
     const int col0 = c * 32;
-    const int ncols = min(32, n_len - col0);
-    if (row_ok && c + 1 < nchunks) apply_load(ap, mt, row, n0 + col0 + 32, min(32, n_len - col0 - 32), nxt);
     uint32_t r[32];
     __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
     ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(col0), r);
     ptx::tmem_ld_wait();
-    if (row_ok) {
+    uint32_t o[16];  // O as stored, packed pairs along the lane's natural column
+    {
       float v[32];
-      chunk_values<FP16, HAS_AUX>(r, aux_row, true, col0, ncols == 32, n_len, row - (n0 + col0), alpha, beta, diag,
-                                  v);
+      chunk_values<FP16, HAS_AUX>(r, aux_row, row_ok, col0, col0 + 32 <= n_len, n_len, row - (n0 + col0), alpha,
+                                  beta, diag, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = E::to_f(E::from_f(v[j]));  // O as stored
-      apply_store(ap, mt, row, n0 + col0, ncols, v, cur);
+      for (int i = 0; i < 16; ++i) o[i] = pack2<FP16>(v[2 * i], v[2 * i + 1]);
+    }
+    if (!mt.transposed) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xw[lane * 17 + i] = o[i];
+      __syncwarp();
+      const int wc = lane >> 1;
+      const uint32_t sel = (lane & 1) ? 0x7632u : 0x5410u;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = __byte_perm(xw[(2 * i) * 17 + wc], xw[(2 * i + 1) * 17 + wc], sel);
+      __syncwarp();
+    }
+    int r0, c0, nr, nc;
+    origin(c, r0, c0, nr, nc);
+    float* dst = p + static_cast<int64_t>(r0) * cols + c0 + lane;
+    __nv_bfloat16* dst16 = pb ? pb + static_cast<int64_t>(r0) * cols + c0 + lane : nullptr;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < nr && lane < nc) {
+        const float ov = E::bits_to_f(half_of(o, j));
+        const float np = fmaf(-coef, ov, cur[j] * decay);
+        dst[j * cols] = np;
+        if (dst16) dst16[j * cols] = __float2bfloat16_rn(np);
+      }
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
@@ -592,7 +648,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              static_cast<uint32_t>(acc * BN);
       if (ap.params) {
         epilogue_apply_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                           t_row, lane, alpha, beta, diag, ap);
+                                           t_row, stage_words, lane, alpha, beta, diag, ap);
       } else {
         if (G.map_out) {
           epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
@@ -856,8 +912,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                              static_cast<uint32_t>(acc * BN);
       const int rb = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
       if (ap.params) {
-        epilogue_apply_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, lane, alpha,
-                                           beta, diag, ap);
+        epilogue_apply_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage_words, lane,
+                                           alpha, beta, diag, ap);
       } else {
         if (G.map_out) {
           epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage, nst, lane,

@@ -250,13 +250,15 @@ struct Plan {
   }
 };
 
-// The step's weight decay and update are applied in the epilogue of the chain's last
-// product; NSM_FUSED_APPLY=0 in the environment runs them as a separate pass instead (for
-// comparisons; both give the same bits).
+// The grouped launches leave the step's decay and update to a separate pass; with
+// NSM_FUSED_APPLY=1 in the environment the epilogue of the chain's last product applies
+// them instead (both give the same bits, and the same step time: the epilogue's
+// parameter traffic costs the GEMM about what the separate pass costs).  The small-
+// matrix kernel always applies its matrices in its final pass.
 bool fused_apply_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("NSM_FUSED_APPLY");
-    return !(v && v[0] == '0');
+    return v && v[0] == '1';
   }();
   return on;
 }
@@ -619,7 +621,8 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     mi.chunk_begin = L.chunk_begin[i];
     mi.nchunks = L.nchunks[i];
     mi.scale = static_cast<float>(std::sqrt(std::max(1.0, double(mi.rows) / double(mi.cols))));
-    mi.vec_ok = (mi.rows % 8 == 0 && mi.cols % 8 == 0) ? 1 : 0;
+    mi.flags = (mi.rows % 8 == 0 && mi.cols % 8 == 0) ? kMatVec : 0;
+    if (small[L.cls_of[i]]) mi.flags |= kMatInChain;
     hm[i] = mi;
   }
   int32_t* hmatidx = reinterpret_cast<int32_t*>(host.data() + matidx_off);
@@ -952,16 +955,17 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need) {
 }
 
 // Launches the chain: the small-matrix kernel, then the grouped GEMMs.  With
-// `apply_last`, the products that compute O apply the step to the parameters in their
-// epilogues instead of storing O.
-int run_chain(Plan& P, cudaStream_t stream, int* launches, const ApplyArgs* apply_last = nullptr) {
+// `apply_small`, the small-matrix kernel applies the step to its matrices instead of
+// storing O; with `apply_last`, so does the grouped launch that computes O.
+int run_chain(Plan& P, cudaStream_t stream, int* launches, const ApplyArgs* apply_small = nullptr,
+              const ApplyArgs* apply_last = nullptr) {
   int num_sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, P.device);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
   if (P.n_small_jobs > 0) {
     TimedLaunch t(stream, NSM_KIND_SMALL, P.small_flops);
     e = launch_ns_small(P.d_small_jobs, P.n_small_jobs, P.d_small_ops, P.n_small_ops, P.x_fp16 ? 1 : 0, num_sms,
-                        stream, apply_last);
+                        stream, apply_small);
     if (e != cudaSuccess) return fail_cuda(e, "small-matrix Newton-Schulz launch");
     ++*launches;
   }
@@ -1150,17 +1154,18 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   }
   if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
   ++launches;
+  // The small-matrix kernel applies its matrices itself; the grouped launches' matrices
+  // are applied by the last product's epilogue (NSM_FUSED_APPLY=1) or by the separate
+  // pass, which skips the matrices already applied.
   const float decay = 1.0f - lr * wd;
-  if ((!P->launches.empty() || P->n_small_jobs > 0) && fused_apply_enabled()) {
-    // the last product writes the parameters (and their bf16 copy) directly
-    const ApplyArgs ap{P->d_mats, packed_params, params_bf16, lr, decay};
-    rc = run_chain(*P, stream, &launches, &ap);
-    if (rc != NSM_OK) return rc;
+  const ApplyArgs ap{P->d_mats, packed_params, params_bf16, lr, decay};
+  const bool fused = fused_apply_enabled() && !P->launches.empty();
+  rc = run_chain(*P, stream, &launches, &ap, fused ? &ap : nullptr);
+  if (rc != NSM_OK) return rc;
+  if (fused || P->n_small_jobs == n) {
     t_last_launches = launches;
     return NSM_OK;
   }
-  rc = run_chain(*P, stream, &launches);
-  if (rc != NSM_OK) return rc;
   {
     TimedLaunch t(stream, NSM_KIND_APPLY, (params_bf16 ? 12.0 : 10.0) * elems);
     e = launch_apply(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, packed_params, params_bf16,

@@ -21,8 +21,13 @@ struct MatInfo {
   int32_t transposed; // rows > cols: the slot holds the transpose
   int32_t chunk_begin, nchunks;  // momentum/norm chunks of this matrix
   float scale;        // sqrt(max(1, rows/cols))
-  int32_t vec_ok;     // rows % 8 == 0 && cols % 8 == 0 (16-byte vector paths usable)
+  int32_t flags;      // kMatVec | kMatInChain
 };
+// MatInfo::flags: rows % 8 == 0 && cols % 8 == 0 (16-byte vector paths usable) ...
+constexpr int32_t kMatVec = 1;
+// ... and: the small-matrix kernel applies this matrix's step in its final pass, so the
+// separate apply pass leaves it alone
+constexpr int32_t kMatInChain = 2;
 static_assert(sizeof(MatInfo) == 64, "MatInfo layout");
 
 // Elements of one momentum/norm chunk (256 threads x 8 vectors of 8).

@@ -498,18 +498,17 @@ torch.save(out, sys.argv[1])
 
 
 def test_fused_apply_matches_separate_pass_bitwise(nsm, tmp_path):
-    # The chain's last product applies the step in its epilogue; with NSM_FUSED_APPLY=0 a
-    # separate pass applies it from the stored O.  Both round O to the same storage format
-    # and evaluate the same fused multiply-add, so the results agree bit for bit.
-    path = tmp_path / "separate.pt"
-    env = dict(os.environ, NSM_FUSED_APPLY="0")
+    # A separate pass applies the step from the stored O; with NSM_FUSED_APPLY=1 the
+    # chain's last product applies it in its epilogue.  Both round O to the same storage
+    # format and evaluate the same fused multiply-add, so the results agree bit for bit.
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    subprocess.run([sys.executable, "-c", _SEPARATE_APPLY, str(path)], env=env, cwd=root, check=True,
-                   timeout=600)
+    path = tmp_path / "separate.pt"
+    subprocess.run([sys.executable, "-c", _SEPARATE_APPLY, str(path)], cwd=root, check=True, timeout=600,
+                   env=dict(os.environ, NSM_FUSED_APPLY="0"))
     ref = torch.load(path)
     path2 = tmp_path / "fused.pt"
     subprocess.run([sys.executable, "-c", _SEPARATE_APPLY, str(path2)], cwd=root, check=True, timeout=600,
-                   env={k: v for k, v in os.environ.items() if k != "NSM_FUSED_APPLY"})
+                   env=dict(os.environ, NSM_FUSED_APPLY="1"))
     got = torch.load(path2)
     for method in ref:
         for a, b in zip(got[method], ref[method]):
