@@ -338,9 +338,11 @@ def run_ours(args):
     clocks = clk.summary()
 
     # ---- end to end through the public API with host buffers.  Every step copies its bf16
-    # grads host -> device (pinned) and reads its result back: the bf16 copy of the updated
-    # parameters that the step writes (the buffer an owner broadcasts).  Two copy streams
-    # and double-buffered device buffers let step k's copies overlap steps k-1 and k+1.
+    # grads (the Muon group's and the AdamW group's) host -> device from pinned memory, runs
+    # muon_step and adamw_step, and reads its result back: the bf16 copy of the updated
+    # Muon parameters that the step writes (the buffer an owner broadcasts).  Two copy
+    # streams and double-buffered device buffers let step k's copies overlap steps k-1 and
+    # k+1.
     e2e = None
     try:
         reps = max(2, min(args.steps, 5))
@@ -351,7 +353,18 @@ def run_ours(args):
         h_out = torch.empty(total, dtype=torch.bfloat16, pin_memory=True)
         d_grads = [grads, torch.empty_like(grads)]
         d_out = [torch.empty(total, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        # the AdamW group's gradients are inputs of the step too
+        h_agrads = d_agrads = None
+        if adam is not None:
+            h_agrads = torch.empty(adam[0].numel(), dtype=torch.bfloat16, pin_memory=True)
+            h_agrads.copy_(adam[0])
+            d_agrads = [adam[0], torch.empty_like(adam[0])]
         ev = lambda: torch.cuda.Event()
+
+        def upload(slot):
+            d_grads[slot].copy_(h_grads, non_blocking=True)
+            if d_agrads is not None:
+                d_agrads[slot].copy_(h_agrads, non_blocking=True)
 
         def pipeline():
             h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
@@ -360,7 +373,7 @@ def run_ours(args):
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(h2d)
             with torch.cuda.stream(h2d):
-                d_grads[0].copy_(h_grads, non_blocking=True)
+                upload(0)
                 h2d_done[0].record(h2d)
             for k in range(reps):
                 cur, nxt = k % 2, (k + 1) % 2
@@ -369,12 +382,16 @@ def run_ours(args):
                     stream.wait_event(d2h_done[cur])  # step k-2's result has left d_out[cur]
                 nsm.muon_step(d_grads[cur], params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method,
                               NS_STEPS, True, ws, stream, params_bf16=d_out[cur])
+                if adam is not None:
+                    adam_state["t"] += 1
+                    nsm.adamw_step(d_agrads[cur], adam[1], adam[2], adam[3], 3e-4, 0.9, 0.95, 1e-10, wl.wd,
+                                   adam_state["t"], stream)
                 comp_done[cur].record(stream)
                 if k + 1 < reps:
                     with torch.cuda.stream(h2d):
                         if k >= 1:
                             h2d.wait_event(comp_done[nxt])  # step k-1 is done with d_grads[nxt]
-                        d_grads[nxt].copy_(h_grads, non_blocking=True)
+                        upload(nxt)
                         h2d_done[nxt].record(h2d)
                 with torch.cuda.stream(d2h):
                     d2h.wait_event(comp_done[cur])
@@ -390,11 +407,12 @@ def run_ours(args):
         # median of three timed passes is reported (all three are listed).
         pipeline()
         passes = [pipeline() for _ in range(3)]
+        h2d_bytes = total * 2 + (adam[0].numel() * 2 if adam is not None else 0)
         e2e = {"value": sorted(passes)[1], "unit": "ms",
-               "h2d_bytes_per_step": total * 2, "d2h_bytes_per_step": total * 2,
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": total * 2,
                "steps": reps, "passes_ms": passes, "statistic": "median of 3 timed passes",
                "overlap": "copies on two streams, double-buffered"}
-        del h_grads, h_out, d_grads, d_out
+        del h_grads, h_out, d_grads, d_out, h_agrads, d_agrads
     except Exception as exc:  # pinned memory may be unavailable on a host
         e2e = {"value": None, "unit": "ms", "h2d_bytes_per_step": total * 2,
                "d2h_bytes_per_step": total * 2, "error": str(exc)[:200]}

@@ -406,10 +406,26 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
   const int row = rb + lane;
   const bool row_ok = row < G.M;
   const int nchunks = (n_len + 31) >> 5;
-  const T* aux_row = nullptr;
+  // aux block of a chunk, read coalesced: lane l holds 16-byte unit (l & 3) of row
+  // rb + 8w + (l >> 2) for w < 4, one chunk ahead of its use
+  const T* aux_blk = nullptr;
+  uint4 ax_next[4];
+  auto aux_load = [&](int c, uint4 (&ax)[4]) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int r = rb + 8 * w + (lane >> 2);
+      const int col = 32 * c + 8 * (lane & 3);
+      ax[w] = (r < G.M && col < n_len)
+                  ? __ldg(reinterpret_cast<const uint4*>(aux_blk + static_cast<int64_t>(8 * w + (lane >> 2)) * G.ld_aux + col))
+                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
   if (HAS_AUX) {
-    aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(b) * G.aux_bstride +
-              static_cast<int64_t>(row) * G.ld_aux + n0;
+    aux_blk = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(b) * G.aux_bstride +
+              static_cast<int64_t>(rb) * G.ld_aux + n0;
+    int c = 0;
+    while (c < nchunks && G.sym && n0 + 32 * c < rb) ++c;
+    if (c < nchunks) aux_load(c, ax_next);
   }
   for (int c = 0; c < nchunks; ++c) {
     const int col0 = c * 32;
@@ -417,6 +433,26 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
     if (G.sym && gc0 < rb) continue;  // below the diagonal: written as the mirror of its upper block
     const bool diag_blk = G.sym && gc0 == rb;
     const bool upper_blk = G.sym && gc0 > rb;
+    const uint32_t slot = stage + (nst & 1u) * 4096u;
+    if (nst >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();  // the store two blocks back has read it
+    __syncwarp();
+    uint4 ax_row[4];  // this lane's aux row of the block
+    if (HAS_AUX) {
+      uint4 ax[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) ax[w] = ax_next[w];
+      if (c + 1 < nchunks) aux_load(c + 1, ax_next);
+      // through the slot's first half: row r, unit u at sw64(r, 8u)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int r = 8 * w + (lane >> 2), u = lane & 3;
+        ptx::st_shared_v4(slot + sw64(r, 8 * u), ax[w].x, ax[w].y, ax[w].z, ax[w].w);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ax_row[u] = ptx::ld_shared_v4(slot + sw64(lane, 8 * u));
+      __syncwarp();  // the slot is rewritten with the output below
+    }
     uint32_t r[32];
     __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
     ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(col0), r);
@@ -424,14 +460,32 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
     uint32_t h[16];
     {
       float v[32];
-      chunk_values<FP16, HAS_AUX>(r, aux_row, row_ok, col0, col0 + 32 <= n_len, n_len, row - gc0, alpha, beta,
-                                  diag, v);
+      if (alpha == 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
+      }
+      if (HAS_AUX) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const T* e = reinterpret_cast<const T*>(&ax_row[u]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[u * 8 + j] += beta * E::to_f(e[j]);
+        }
+      }
+      if (diag != 0.0f) {
+        const int d = row - gc0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (d == j) v[j] += diag;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i) h[i] = pack2<FP16>(v[2 * i], v[2 * i + 1]);
     }
-    const uint32_t slot = stage + (nst & 1u) * 4096u;
-    if (nst >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();  // the store two blocks back has read it
-    __syncwarp();
+    (void)row_ok;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       ptx::st_shared_v4(slot + static_cast<uint32_t>(lane * 64 + (((u ^ (lane >> 1)) & 3) << 4)), h[4 * u],

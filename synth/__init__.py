@@ -19,7 +19,7 @@ Workloads (transformer-shaped gradient sets; no datasets or trained weights):
 * ``split_moe`` — 16 layers, each with 32 per-head 128x4096 query blocks (Muon Split:
                   every head block is its own table entry) and 64 experts with gate/up
                   1408x2048 and down 2048x1408.  ``split_moe_heads`` is its 512 head
-                  blocks alone.
+                  blocks alone, ``split_moe_layer`` its first layer.
 
 Gradients other than ``tiny`` are near low-rank with a high condition number:
 ``G = sum_{i<32} 0.7^i u_i v_i^T + 0.01 N(0,1)`` with raw N(0,1) vectors ``u_i, v_i``,
@@ -147,6 +147,14 @@ def _split_moe_heads() -> Workload:
                     [full.muon_shapes[i] for i in keep])
 
 
+def _split_moe_layer() -> Workload:
+    """The Split/MoE set's first layer (32 head blocks and 192 expert matrices, 570M
+    elements): a small case of the same launches, for profiler captures."""
+    full = _split_moe()
+    n = 32 + 64 * 3
+    return Workload("split_moe_layer", 4, full.muon_names[:n], full.muon_shapes[:n])
+
+
 WORKLOADS = {
     "tiny": _tiny,
     "layer1024": _layer1024,
@@ -155,6 +163,7 @@ WORKLOADS = {
     "llama7b_layer": _llama7b_layer,
     "split_moe": _split_moe,
     "split_moe_heads": _split_moe_heads,
+    "split_moe_layer": _split_moe_layer,
 }
 
 
