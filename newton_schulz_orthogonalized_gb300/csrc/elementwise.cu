@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "launch.cuh"
 #include "nsm_internal.h"
 
 namespace nsm {
@@ -128,6 +129,8 @@ __global__ void __launch_bounds__(kThreads)
     k_momentum_norm(const __nv_bfloat16* __restrict__ grads, float* __restrict__ mom,
                     const MatInfo* __restrict__ mats, int nmats, int total_chunks,
                     float* __restrict__ partials, float mu) {
+  grid_dependency_sync();  // inputs come from the previous kernel of the stream
+  release_dependents();
   __shared__ float scratch[kThreads / 32];
   for (int chunk = blockIdx.x; chunk < total_chunks; chunk += gridDim.x) {
     const MatInfo& mt = mats[find_by_chunk(mats, nmats, chunk)];
@@ -179,6 +182,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void k_norm_finalize(const MatInfo* __restrict__ mats, int nmats,
                                 const float* __restrict__ partials, float* __restrict__ scales,
                                 float eps) {
+  grid_dependency_sync();  // inputs come from the previous kernel of the stream
+  release_dependents();
   const int w = static_cast<int>((blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= nmats) return;
@@ -236,6 +241,8 @@ __global__ void __launch_bounds__(kThreads)
     k_to_class(const __nv_bfloat16* __restrict__ grads, const float* __restrict__ mom, float mu,
                void* __restrict__ dst, const MatInfo* __restrict__ mats, int nmats,
                int64_t total_tiles, const float* __restrict__ scales) {
+  grid_dependency_sync();  // inputs come from the previous kernel of the stream
+  release_dependents();
   __shared__ float tile[kTile][kTile + 1];
   for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
     const TilePos tp = tile_pos(mats, nmats, t);
@@ -315,6 +322,8 @@ __global__ void __launch_bounds__(kThreads)
     k_from_class(const void* __restrict__ o, float* __restrict__ params,
                  __nv_bfloat16* __restrict__ out, const MatInfo* __restrict__ mats, int nmats,
                  int64_t total_tiles, float lr, float decay) {
+  grid_dependency_sync();  // inputs come from the previous kernel of the stream
+  release_dependents();
   __shared__ float tile[kTile][kTile + 1];
   for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
     const TilePos tp = tile_pos(mats, nmats, t);
@@ -417,6 +426,8 @@ __global__ void __launch_bounds__(kThreads)
     k_adamw(const __nv_bfloat16* __restrict__ grads, float* __restrict__ params,
             float* __restrict__ mom1, float* __restrict__ mom2, int64_t numel, float b1,
             float b2, float eps, float decay, float step_size, float bc2) {
+  grid_dependency_sync();  // inputs come from the previous kernel of the stream
+  release_dependents();
   const int64_t nvec = numel >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   for (int64_t v = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; v < nvec; v += stride) {
@@ -473,14 +484,14 @@ cudaError_t launch_momentum_norm(const void* grads, float* momentum, const MatIn
   const int grid = grid_for(total_chunks, 8);
   const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
   if (!has_momentum) {
-    k_momentum_norm<false, false><<<grid, kThreads, 0, stream>>>(g, nullptr, mats, nmats, total_chunks,
-                                                                 partials, mu);
+    if (const cudaError_t e_launch = launch_pdl(k_momentum_norm<false, false>, dim3(grid), dim3(kThreads), 0, stream, g, nullptr, mats, nmats, total_chunks,
+                                                                 partials, mu)) return e_launch;
   } else if (nesterov) {
-    k_momentum_norm<true, true><<<grid, kThreads, 0, stream>>>(g, momentum, mats, nmats, total_chunks,
-                                                               partials, mu);
+    if (const cudaError_t e_launch = launch_pdl(k_momentum_norm<true, true>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mats, nmats, total_chunks,
+                                                               partials, mu)) return e_launch;
   } else {
-    k_momentum_norm<true, false><<<grid, kThreads, 0, stream>>>(g, momentum, mats, nmats, total_chunks,
-                                                                partials, mu);
+    if (const cudaError_t e_launch = launch_pdl(k_momentum_norm<true, false>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mats, nmats, total_chunks,
+                                                                partials, mu)) return e_launch;
   }
   return cudaGetLastError();
 }
@@ -489,21 +500,22 @@ cudaError_t launch_norm_finalize(const MatInfo* mats, int nmats, const float* pa
                                  float* scales, float eps, cudaStream_t stream) {
   const int warps_per_block = kThreads / 32;
   const int grid = (nmats + warps_per_block - 1) / warps_per_block;
-  k_norm_finalize<<<grid, kThreads, 0, stream>>>(mats, nmats, partials, scales, eps);
+  if (const cudaError_t e_launch = launch_pdl(k_norm_finalize, dim3(grid), dim3(kThreads), 0, stream, mats, nmats, partials, scales, eps)) return e_launch;
   return cudaGetLastError();
 }
 
 template <bool TO_FP16>
-static void to_class_mode(int mode, int grid, const __nv_bfloat16* g, const float* m, float mu, void* dst,
+static cudaError_t to_class_mode(int mode, int grid, const __nv_bfloat16* g, const float* m, float mu, void* dst,
                           const MatInfo* mats, int nmats, int64_t total_tiles, const float* scales,
                           cudaStream_t stream) {
   if (mode == kUFromGrad) {
-    k_to_class<TO_FP16, kUFromGrad><<<grid, kThreads, 0, stream>>>(g, m, mu, dst, mats, nmats, total_tiles, scales);
+    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUFromGrad>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales)) return e_launch;
   } else if (mode == kUMomentum) {
-    k_to_class<TO_FP16, kUMomentum><<<grid, kThreads, 0, stream>>>(g, m, mu, dst, mats, nmats, total_tiles, scales);
+    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUMomentum>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales)) return e_launch;
   } else {
-    k_to_class<TO_FP16, kUNesterov><<<grid, kThreads, 0, stream>>>(g, m, mu, dst, mats, nmats, total_tiles, scales);
+    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUNesterov>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales)) return e_launch;
   }
+  return cudaSuccess;
 }
 
 cudaError_t launch_to_class(const void* grads, const float* momentum, int has_momentum, int nesterov, float mu,
@@ -512,8 +524,9 @@ cudaError_t launch_to_class(const void* grads, const float* momentum, int has_mo
   const int grid = grid_for(total_tiles, 8);
   const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
   const int mode = !has_momentum ? kUFromGrad : (nesterov ? kUNesterov : kUMomentum);
-  if (to_fp16) to_class_mode<true>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, stream);
-  else to_class_mode<false>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, stream);
+  const cudaError_t e = to_fp16 ? to_class_mode<true>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, stream)
+                                : to_class_mode<false>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -524,9 +537,9 @@ cudaError_t launch_apply(const void* o, int o_fp16, float* params, void* params_
   const float decay = 1.0f - lr * wd;
   auto* pb = reinterpret_cast<__nv_bfloat16*>(params_bf16);
   if (o_fp16) {
-    k_from_class<true, true><<<grid, kThreads, 0, stream>>>(o, params, pb, mats, nmats, total_tiles, lr, decay);
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, true>, dim3(grid), dim3(kThreads), 0, stream, o, params, pb, mats, nmats, total_tiles, lr, decay)) return e_launch;
   } else {
-    k_from_class<false, true><<<grid, kThreads, 0, stream>>>(o, params, pb, mats, nmats, total_tiles, lr, decay);
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, true>, dim3(grid), dim3(kThreads), 0, stream, o, params, pb, mats, nmats, total_tiles, lr, decay)) return e_launch;
   }
   return cudaGetLastError();
 }
@@ -536,9 +549,9 @@ cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* m
   const int grid = grid_for(total_tiles, 8);
   auto* ob = reinterpret_cast<__nv_bfloat16*>(out);
   if (o_fp16) {
-    k_from_class<true, false><<<grid, kThreads, 0, stream>>>(o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f);
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, false>, dim3(grid), dim3(kThreads), 0, stream, o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f)) return e_launch;
   } else {
-    k_from_class<false, false><<<grid, kThreads, 0, stream>>>(o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f);
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, false>, dim3(grid), dim3(kThreads), 0, stream, o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f)) return e_launch;
   }
   return cudaGetLastError();
 }
@@ -551,8 +564,8 @@ cudaError_t launch_adamw(const void* grads, float* params, float* m, float* v, i
   const int grid = grid_for((items + kThreads - 1) / kThreads, 8);
   const float decay = 1.0f - lr * wd;
   const float step_size = lr / bc1;
-  k_adamw<<<grid, kThreads, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(grads), params, m, v,
-                                         numel, beta1, beta2, eps, decay, step_size, bc2);
+  if (const cudaError_t e_launch = launch_pdl(k_adamw, dim3(grid), dim3(kThreads), 0, stream, reinterpret_cast<const __nv_bfloat16*>(grads), params, m, v,
+                                         numel, beta1, beta2, eps, decay, step_size, bc2)) return e_launch;
   return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@
 #include <atomic>
 
 #include "apply.cuh"
+#include "launch.cuh"
 #include "nsm_internal.h"
 #include "ptx.cuh"
 
@@ -56,6 +57,9 @@ constexpr uint32_t TMEM_COLS = 512;       // 2 x 256 fp32 accumulator columns
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 constexpr int kPanel = 8;                 // column tiles per raster panel
 constexpr int EPI_WARPS = 4;
+// Whether the grouped launches may overlap their launch with the previous kernel when
+// programmatic dependent launch is on (NSM_PDL=1).
+constexpr bool kOverlapGemmLaunch = true;
 constexpr int EPI_STAGE_BYTES = EPI_WARPS * 8192;   // per epilogue warp: 2 slots of 2 x 2 KB staged blocks
 
 // 1-CTA kernel: 128 x 256 tiles, 4 stages of A 16 KB + B 32 KB.
@@ -554,6 +558,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // barriers and TMEM are set up; the operands come from the previous kernel of the stream
+  grid_dependency_sync();
+  release_dependents();
   const uint32_t tmem_base = ctrl->tmem_base;
   volatile int* abort_flag = &ctrl->abort;
   volatile int* never_flag = &ctrl->never;
@@ -789,6 +796,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // barriers and TMEM are set up; the operands come from the previous kernel of the stream
+  grid_dependency_sync();
+  release_dependents();
   const uint32_t tmem_base = ctrl->tmem_base;
   volatile int* abort_flag = &ctrl->abort;
   volatile int* never_flag = &ctrl->never;
@@ -1055,8 +1065,10 @@ cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream, 
     const int64_t cap = resident < num_sms / 2 ? resident : num_sms / 2;
     const int64_t pairs = l.total_tiles < cap ? l.total_tiles : cap;
     if (pairs <= 0) return cudaSuccess;
-    k_ns_gemm_pair<B_MN, FP16, HAS_AUX><<<static_cast<int>(2 * pairs), NUM_THREADS, S2_SMEM, stream>>>(
-        l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag, status, ap);
+    if (const cudaError_t e_launch = launch_ordered(kOverlapGemmLaunch, k_ns_gemm_pair<B_MN, FP16, HAS_AUX>, dim3(static_cast<unsigned>(2 * pairs)),
+                                                dim3(NUM_THREADS), S2_SMEM, stream, l.groups, l.num_groups,
+                                                l.total_tiles, l.alpha, l.beta, l.diag, status, ap))
+      return e_launch;
     return cudaGetLastError();
   }
   static std::atomic<uint64_t> done{0};
@@ -1064,8 +1076,10 @@ cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream, 
   if (e != cudaSuccess) return e;
   const int64_t grid = l.total_tiles < num_sms ? l.total_tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  k_ns_gemm<B_MN, FP16, HAS_AUX><<<static_cast<int>(grid), NUM_THREADS, S1_SMEM, stream>>>(
-      l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag, status, ap);
+  if (const cudaError_t e_launch = launch_ordered(kOverlapGemmLaunch, k_ns_gemm<B_MN, FP16, HAS_AUX>, dim3(static_cast<unsigned>(grid)),
+                                              dim3(NUM_THREADS), S1_SMEM, stream, l.groups, l.num_groups, l.total_tiles,
+                                              l.alpha, l.beta, l.diag, status, ap))
+    return e_launch;
   return cudaGetLastError();
 }
 

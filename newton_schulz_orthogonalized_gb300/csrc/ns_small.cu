@@ -29,6 +29,7 @@
 #include <atomic>
 
 #include "apply.cuh"
+#include "launch.cuh"
 #include "nsm_internal.h"
 #include "ptx.cuh"
 
@@ -501,6 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // barriers and TMEM are set up; X comes from the previous kernel of the stream
+  grid_dependency_sync();
+  release_dependents();
   const uint32_t tmem = ctrl->tmem_base;
 
   if (warp == 0) {
@@ -567,7 +571,7 @@ cudaError_t launch_typed(const SmallJob* jobs, int njobs, const SmallOp* ops, in
   if (e != cudaSuccess) return e;
   const int grid = njobs < num_sms ? njobs : num_sms;
   if (grid <= 0) return cudaSuccess;
-  k_ns_small<FP16><<<grid, kThreads, kSmem, stream>>>(jobs, njobs, ops, nops, status, ap);
+  if (const cudaError_t e_launch = launch_pdl(k_ns_small<FP16>, dim3(grid), dim3(kThreads), kSmem, stream, jobs, njobs, ops, nops, status, ap)) return e_launch;
   return cudaGetLastError();
 }
 

@@ -513,3 +513,18 @@ def test_fused_apply_matches_separate_pass_bitwise(nsm, tmp_path):
     for method in ref:
         for a, b in zip(got[method], ref[method]):
             assert torch.equal(a, b), method
+
+
+def test_overlapped_launches_match_plain_order_bitwise(nsm, tmp_path):
+    # NSM_PDL=1 launches every kernel with programmatic stream serialisation (each waits
+    # for the previous grid before touching its outputs): the results are the same bits
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = {}
+    for flag in ("0", "1"):
+        path = tmp_path / f"pdl{flag}.pt"
+        subprocess.run([sys.executable, "-c", _SEPARATE_APPLY, str(path)], cwd=root, check=True, timeout=600,
+                       env=dict(os.environ, NSM_PDL=flag))
+        res[flag] = torch.load(path)
+    for method in res["0"]:
+        for a, b in zip(res["1"][method], res["0"][method]):
+            assert torch.equal(a, b), method
