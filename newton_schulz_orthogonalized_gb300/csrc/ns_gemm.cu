@@ -242,45 +242,18 @@ __device__ __forceinline__ void epilogue_apply_rows(const GemmGroup& G, int b, i
     aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(b) * G.aux_bstride +
               static_cast<int64_t>(row) * G.ld_aux + n0;
   }
-  float* p = ap.params + mt.off;
-  __nv_bfloat16* pb = ap.params_bf16 ? reinterpret_cast<__nv_bfloat16*>(ap.params_bf16) + mt.off : nullptr;
-  const float coef = ap.lr * mt.scale;
-  const float decay = ap.decay;
-  const int64_t cols = mt.cols;
-  // block c covers natural rows r0 + j (j < nr) and columns c0 + lane (lane < nc)
-  auto origin = [&](int c, int& r0, int& c0, int& nr, int& nc) {
-    const int gc0 = n0 + 32 * c;
-    const int in_class_cols = min(32, n_len - 32 * c), in_class_rows = min(32, G.M - rb);
-    if (mt.transposed) {
-      r0 = gc0;
-      c0 = rb;
-      nr = in_class_cols;
-      nc = in_class_rows;
-    } else {
-      r0 = rb;
-      c0 = gc0;
-      nr = in_class_rows;
-      nc = in_class_cols;
-    }
-  };
-  auto load = [&](int c, float (&pv)[32]) {
-    int r0, c0, nr, nc;
-    origin(c, r0, c0, nr, nc);
-    const float* src = p + static_cast<int64_t>(r0) * cols + c0 + lane;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) pv[j] = (j < nr && lane < nc) ? src[j * cols] : 0.f;
-  };
   float cur[32], nxt[32];
-  load(0, cur);
+  apply_block_load(ap, mt, apply_block_at(mt, rb, n0, G.M, n0 + n_len), lane, cur);
 #pragma unroll 1
   for (int c = 0; c < nchunks; ++c) {
-    if (c + 1 < nchunks) load(c + 1, nxt);
     const int col0 = c * 32;
+    const ApplyBlock blk = apply_block_at(mt, rb, n0 + col0, G.M, n0 + n_len);
+    if (c + 1 < nchunks) apply_block_load(ap, mt, apply_block_at(mt, rb, n0 + col0 + 32, G.M, n0 + n_len), lane, nxt);
     uint32_t r[32];
     __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
     ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(col0), r);
     ptx::tmem_ld_wait();
-    uint32_t o[16];  // O as stored, packed pairs along the lane's natural column
+    uint32_t o[16];  // O as stored, packed pairs
     {
       float v[32];
       chunk_values<FP16, HAS_AUX>(r, aux_row, row_ok, col0, col0 + 32 <= n_len, n_len, row - (n0 + col0), alpha,
@@ -288,29 +261,8 @@ __device__ __forceinline__ void epilogue_apply_rows(const GemmGroup& G, int b, i
 #pragma unroll
       for (int i = 0; i < 16; ++i) o[i] = pack2<FP16>(v[2 * i], v[2 * i + 1]);
     }
-    if (!mt.transposed) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) xw[lane * 17 + i] = o[i];
-      __syncwarp();
-      const int wc = lane >> 1;
-      const uint32_t sel = (lane & 1) ? 0x7632u : 0x5410u;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) o[i] = __byte_perm(xw[(2 * i) * 17 + wc], xw[(2 * i + 1) * 17 + wc], sel);
-      __syncwarp();
-    }
-    int r0, c0, nr, nc;
-    origin(c, r0, c0, nr, nc);
-    float* dst = p + static_cast<int64_t>(r0) * cols + c0 + lane;
-    __nv_bfloat16* dst16 = pb ? pb + static_cast<int64_t>(r0) * cols + c0 + lane : nullptr;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j < nr && lane < nc) {
-        const float ov = E::bits_to_f(half_of(o, j));
-        const float np = fmaf(-coef, ov, cur[j] * decay);
-        dst[j * cols] = np;
-        if (dst16) dst16[j * cols] = __float2bfloat16_rn(np);
-      }
-    }
+    apply_block_columns(mt, o, xw, lane);
+    apply_block_store<FP16>(ap, mt, blk, lane, o, cur);
 #pragma unroll
     for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
   }

@@ -83,6 +83,20 @@ struct Store<true> {
   __device__ static __forceinline__ T from_f(float v) { return __float2half_rn(v); }
 };
 
+// Two values rounded to the storage format, packed into one word (the first in the low half).
+template <bool FP16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<true>(float lo, float hi) {
+  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<false>(float lo, float hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
 // Byte offset of 16-byte unit u (0..7) of row `row` in a 128-byte-swizzled panel.
 __device__ __forceinline__ uint32_t sw(int row, int u) {
   return static_cast<uint32_t>(row * 128 + ((u ^ (row & 7)) << 4));
@@ -261,10 +275,11 @@ struct Epilogue {
   int row;          // the accumulator row (= TMEM lane) this thread drains
   int lane;
   bool leader;      // first epilogue thread: issues the TMA stores
+  uint32_t* xw;     // this warp's 32 x 17 words of transpose scratch (in the X' staging area)
   uint32_t sq_cnt = 0;
 
-  __device__ Epilogue(const Roles& r, uint32_t tmem, int warp, int ln)
-      : R(r), lane(ln), leader(warp == 2 && ln == 0) {
+  __device__ Epilogue(const Roles& r, uint32_t tmem, int warp, int ln, uint32_t* scratch)
+      : R(r), lane(ln), leader(warp == 2 && ln == 0), xw(scratch) {
     const int quarter = warp & 3;
     row = quarter * 32 + ln;
     t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -390,21 +405,28 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
 #pragma unroll
         for (int k = 0; k < 64; ++k) v[k] = E::to_f(E::from_f(v[k]));  // X' (or O) as stored
         if (!stores) {
-          // final pass: apply the step at O's natural positions
+          // final pass: apply the step, one coalesced 32 x 32 block at a time (the X'
+          // staging slots are idle in this pass: every earlier store and MMA read of
+          // them has completed)
           if (reads_x) {
             ptx::named_sync(kEpiBar, kEpiThreads);  // every thread has read the panel
             if (ep.leader) ptx::mbar_arrive(R.bar(&R.ctrl->empty[stage]));
           }
-          if (ep.row < job.m) {
+          const int rb = ep.row - ep.lane;  // the warp's first row
+          if (rb < job.m) {
             const MatInfo& mt = ap.mats[job.mat];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int gc0 = c * 64 + h * 32;
               if (gc0 < job.n) {
-                float oh[32];
+                uint32_t o[16];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) oh[k] = v[h * 32 + k];
-                apply_chunk(ap, mt, ep.row, gc0, min(32, job.n - gc0), oh);
+                for (int i = 0; i < 16; ++i) o[i] = pack2<FP16>(v[h * 32 + 2 * i], v[h * 32 + 2 * i + 1]);
+                apply_block_columns(mt, o, ep.xw, ep.lane);
+                const ApplyBlock blk = apply_block_at(mt, rb, gc0, job.m, job.n);
+                float pv[32];
+                apply_block_load(ap, mt, blk, ep.lane, pv);
+                apply_block_store<FP16>(ap, mt, blk, ep.lane, o, pv);
               }
             }
           }
@@ -533,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    Epilogue<FP16> ep(R, tmem, warp, lane);
+    Epilogue<FP16> ep(R, tmem, warp, lane, reinterpret_cast<uint32_t*>(smem + kXtOff + (warp - 2) * 4096));
     drain<FP16>(ep, jobs, njobs, ops, nops, ap);
     // stores still reading shared memory must finish before the block exits
     if (ep.leader) ptx::bulk_wait_group<0>();
