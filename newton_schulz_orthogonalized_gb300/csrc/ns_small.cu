@@ -8,14 +8,14 @@
 //   * m x m products  S[dst] = alpha S[a] S[b]^T + beta S[aux] + diag I  read both operands
 //     from shared memory (8 MMAs of 128 x 128 x 16) and write the rounded result back
 //     there from the TMEM accumulator;
-//   * passes over X (m x n, n up to the tensor's width) stream 64-column panels of X
-//     through a 4-stage TMA ring:
-//       Gram:  S[dst] = X X^T, the panels being both operands (K-major);
-//       pass:  X' = alpha S[a] X + beta X, the panel being the MN-major B operand.  Each
-//              64-column panel of X' is rounded in the epilogue, written to shared
-//              memory and stored with a TMA store; when another Gram follows, the MMA
-//              warp also accumulates X' X'^T from that panel, so the next step needs no
-//              extra pass over X.  The final pass applies the step to the parameters
+//   * passes over X (m x n, n up to the tensor's width) stream 128-column chunks of X
+//     (two 64-column panels each) through a 2-slot TMA ring:
+//       Gram:  S[dst] = X X^T, each chunk being both operands (K-major);
+//       pass:  X' = alpha S[a] X + beta X, the chunk being the MN-major B operand
+//              (N = 128).  Each chunk of X' is rounded in the epilogue, written to
+//              shared memory and stored with TMA stores; when another Gram follows, the
+//              MMA warp also accumulates X' X'^T from that chunk, so the next step needs
+//              no extra pass over X.  The final pass applies the step to the parameters
 //              (or stores O).
 //
 // Roles: warp 0 issues the TMA loads, warp 1 (one thread) the MMAs, warps 2-5 drain TMEM
@@ -37,11 +37,13 @@ namespace nsm {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kRing = 4;
 constexpr int kPanel = 128 * 128;          // 128 rows x 64 16-bit columns, 128-byte swizzle
 constexpr int kSquare = 2 * kPanel;        // 128 x 128: two 64-column panels
 constexpr int kSquares = 3;
-constexpr uint32_t kTmemCols = 256;        // [0,128) m x m accumulator; [128,256) two pass panels
+constexpr int kChunk = 128;                // columns of X per pass step: two panels
+constexpr int kSlot = 2 * kPanel;          // one chunk in shared memory (the layout of a square)
+constexpr int kRing = 2;                   // chunk slots of the TMA ring
+constexpr uint32_t kTmemCols = 512;        // [0,128) m x m accumulator; [128,384) two chunk accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kEpiBar = 1;            // named barrier of the epilogue warps
 constexpr uint32_t kEpiThreads = 128;
@@ -63,8 +65,8 @@ struct Ctrl {
 };
 
 constexpr size_t kRingOff = size_t(kSquares) * kSquare;
-constexpr size_t kXtOff = kRingOff + size_t(kRing) * kPanel;
-constexpr size_t kCtrlOff = kXtOff + 2 * size_t(kPanel);
+constexpr size_t kXtOff = kRingOff + size_t(kRing) * kSlot;
+constexpr size_t kCtrlOff = kXtOff + 2 * size_t(kSlot);
 constexpr size_t kSmem = 1024 + kCtrlOff + sizeof(Ctrl);
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
@@ -143,7 +145,7 @@ __device__ bool produce(const Roles& R, const SmallJob* __restrict__ jobs, int n
   uint32_t stores_seen = 0;
   for (int j = blockIdx.x; j < njobs; j += gridDim.x) {
     const SmallJob job = jobs[j];
-    const int nck = (job.n + 63) >> 6;
+    const int nck = (job.n + kChunk - 1) / kChunk;
     bool first_pass = true;
     for (int o = 0; o < nops; ++o) {
       const SmallOp op = ops[o];
@@ -160,8 +162,11 @@ __device__ bool produce(const Roles& R, const SmallJob* __restrict__ jobs, int n
       for (int c = 0; c < nck; ++c) {
         if (!R.wait(&R.ctrl->empty[rp.stage], rp.phase ^ 1u)) return false;
         const uint32_t fb = R.bar(&R.ctrl->full[rp.stage]);
-        ptx::mbar_arrive_expect_tx(fb, kPanel);
-        ptx::tma_load_3d(R.ring + static_cast<uint32_t>(rp.stage * kPanel), map, fb, c * 64, 0, job.b);
+        ptx::mbar_arrive_expect_tx(fb, kSlot);
+        const uint32_t slot = R.ring + static_cast<uint32_t>(rp.stage * kSlot);
+        // the second panel may start past the matrix: it reads zeros
+        ptx::tma_load_3d(slot, map, fb, c * kChunk, 0, job.b);
+        ptx::tma_load_3d(slot + kPanel, map, fb, c * kChunk + 64, 0, job.b);
         fill_parity[rp.stage] = static_cast<int>(rp.phase);
         rp.advance();
       }
@@ -175,7 +180,7 @@ template <bool FP16>
 __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict__ jobs, int njobs,
                       const SmallOp* __restrict__ ops, int nops, bool store_final) {
   const uint32_t id_sq = ptx::idesc_f16(128, 128, !FP16, false);
-  const uint32_t id_pass = ptx::idesc_f16(128, 64, !FP16, true);
+  const uint32_t id_pass = ptx::idesc_f16(128, kChunk, !FP16, true);
   RingPos rp;
   uint32_t acc_cnt = 0, sq_cnt = 0, xs = 0;
   uint32_t hand[2] = {0u, 0u};
@@ -188,14 +193,14 @@ __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict_
     ptx::tc_fence_after();
     return true;
   };
-  // X' X'^T += panel of X' in shared-memory slot `slot`
+  // X' X'^T += chunk of X' in shared-memory slot `slot`
   auto accumulate_panel = [&](int c, uint32_t slot) -> bool {
     if (!R.wait(&R.ctrl->xt_full[slot], hand[slot] & 1u)) return false;
     ptx::tc_fence_after();
-    const uint32_t base = R.xt + slot * kPanel;
+    const uint32_t base = R.xt + slot * kSlot;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t d = ptx::smem_desc_sw128(base + kk * 32, 16, 1024);
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t d = square_desc(base, kk);
       ptx::mma_f16(tmem, d, d, id_sq, (c | kk) != 0 ? 1u : 0u);
     }
     ptx::mma_commit(R.bar(&R.ctrl->xt_empty[slot]));
@@ -204,17 +209,17 @@ __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict_
   };
   for (int j = blockIdx.x; j < njobs; j += gridDim.x) {
     const SmallJob job = jobs[j];
-    const int nck = (job.n + 63) >> 6;
+    const int nck = (job.n + kChunk - 1) / kChunk;
     for (int o = 0; o < nops; ++o) {
       const SmallOp op = ops[o];
       if (op.kind == kSmallGram) {
         for (int c = 0; c < nck; ++c) {
           if (!R.wait(&R.ctrl->full[rp.stage], rp.phase)) return false;
           ptx::tc_fence_after();
-          const uint32_t base = R.ring + static_cast<uint32_t>(rp.stage * kPanel);
+          const uint32_t base = R.ring + static_cast<uint32_t>(rp.stage * kSlot);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t d = ptx::smem_desc_sw128(base + kk * 32, 16, 1024);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t d = square_desc(base, kk);
             ptx::mma_f16(tmem, d, d, id_sq, (c | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit(R.bar(&R.ctrl->empty[rp.stage]));
@@ -238,14 +243,15 @@ __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict_
           ptx::tc_fence_after();
           if (!R.wait(&R.ctrl->full[rp.stage], rp.phase)) return false;
           ptx::tc_fence_after();
-          const uint32_t panel = R.ring + static_cast<uint32_t>(rp.stage * kPanel);
-          const uint32_t d_tmem = tmem + 128u + 64u * acc;
+          // B = the chunk read K x N (N contiguous): two 64-column blocks kPanel apart
+          const uint32_t chunk = R.ring + static_cast<uint32_t>(rp.stage * kSlot);
+          const uint32_t d_tmem = tmem + 128u + static_cast<uint32_t>(kChunk) * acc;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            ptx::mma_f16(d_tmem, square_desc(a, kk), ptx::smem_desc_sw128(panel + kk * 2048, kPanel, 1024),
+            ptx::mma_f16(d_tmem, square_desc(a, kk), ptx::smem_desc_sw128(chunk + kk * 2048, kPanel, 1024),
                          id_pass, kk != 0 ? 1u : 0u);
           }
-          // with beta != 0 the epilogue reads the panel too and releases it itself
+          // with beta != 0 the epilogue reads the chunk too and releases it itself
           if (op.beta == 0.f) ptx::mma_commit(R.bar(&R.ctrl->empty[rp.stage]));
           ptx::mma_commit(R.bar(&R.ctrl->acc_full[acc]));
           ++acc_cnt;
@@ -355,7 +361,7 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
   int pend[2] = {-1, -1};  // parity of the MMA's outstanding read of each X' slot
   for (int j = blockIdx.x; j < njobs; j += gridDim.x) {
     const SmallJob job = jobs[j];
-    const int nck = (job.n + 63) >> 6;
+    const int nck = (job.n + kChunk - 1) / kChunk;
     for (int o = 0; o < nops; ++o) {
       const SmallOp op = ops[o];
       if (op.kind == kSmallGram) {
@@ -370,6 +376,7 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
       const bool stores = !op.final_pass || store_final;
       const bool reads_x = op.beta != 0.f;
       const uint32_t xs0 = xs;
+      const int rb = ep.row - ep.lane;  // the warp's first row
       for (int c = 0; c < nck; ++c) {
         const uint32_t acc = acc_cnt & 1u;
         bool ok = R.wait(&R.ctrl->acc_full[acc], (acc_cnt >> 1) & 1u);
@@ -377,51 +384,68 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
         if (!ok) R.give_up();
         if (!ptx::named_all(kEpiBar, kEpiThreads, ok)) return false;
         ptx::tc_fence_after();
-        float v[64];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(ep.t_lane + 128u + 64u * acc + static_cast<uint32_t>(h * 32), r);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[h * 32 + k] = op.alpha * __uint_as_float(r[k]);
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (ep.lane == 0) ptx::mbar_arrive(R.bar(&R.ctrl->acc_empty[acc]));
-        ++acc_cnt;
         const int stage = rp.stage;
-        if (reads_x) {
-          const uint32_t panel = R.ring + static_cast<uint32_t>(stage * kPanel);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 pk = *reinterpret_cast<const uint4*>(__cvta_shared_to_generic(panel + sw(ep.row, u)));
-            const T* e = reinterpret_cast<const T*>(&pk);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[u * 8 + k] += op.beta * E::to_f(e[k]);
+        const uint32_t chunk = R.ring + static_cast<uint32_t>(stage * kSlot);
+        const uint32_t slot = (xs0 + static_cast<uint32_t>(c)) & 1u;
+        if (stores) {
+          // the X' slot must be free: read by its store two chunks back and by the MMA
+          if (ep.leader) ptx::bulk_wait_group_read<1>();
+          bool free_ok = true;
+          if (pend[slot] >= 0) {
+            free_ok = R.wait(&R.ctrl->xt_empty[slot], static_cast<uint32_t>(pend[slot]));
+            if (!free_ok) R.give_up();
+            pend[slot] = -1;
           }
+          if (!ptx::named_all(kEpiBar, kEpiThreads, free_ok)) return false;
         }
-        rp.advance();
+        const uint32_t xt = R.xt + slot * kSlot;
+        // the chunk's two 64-column halves, one panel each
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          float v[64];
 #pragma unroll
-        for (int k = 0; k < 64; ++k) v[k] = E::to_f(E::from_f(v[k]));  // X' (or O) as stored
-        if (!stores) {
-          // final pass: apply the step, one coalesced 32 x 32 block at a time (the X'
-          // staging slots are idle in this pass: every earlier store and MMA read of
-          // them has completed)
-          if (reads_x) {
-            ptx::named_sync(kEpiBar, kEpiThreads);  // every thread has read the panel
-            if (ep.leader) ptx::mbar_arrive(R.bar(&R.ctrl->empty[stage]));
+          for (int q = 0; q < 2; ++q) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(
+                ep.t_lane + 128u + static_cast<uint32_t>(kChunk) * acc + static_cast<uint32_t>(64 * h + 32 * q), r);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[q * 32 + k] = op.alpha * __uint_as_float(r[k]);
           }
-          const int rb = ep.row - ep.lane;  // the warp's first row
-          if (rb < job.m) {
+          if (reads_x) {
+            const uint32_t panel = chunk + static_cast<uint32_t>(h * kPanel);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint4 pk = *reinterpret_cast<const uint4*>(__cvta_shared_to_generic(panel + sw(ep.row, u)));
+              const T* e = reinterpret_cast<const T*>(&pk);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v[u * 8 + k] += op.beta * E::to_f(e[k]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 64; ++k) v[k] = E::to_f(E::from_f(v[k]));  // X' (or O) as stored
+          if (stores) {
+            const uint32_t dst = xt + static_cast<uint32_t>(h * kPanel);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              uint4 pk;
+              T* e = reinterpret_cast<T*>(&pk);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) e[k] = E::from_f(v[u * 8 + k]);
+              *reinterpret_cast<uint4*>(__cvta_shared_to_generic(dst + sw(ep.row, u))) = pk;
+            }
+          } else if (rb < job.m) {
+            // final pass: apply the step, one coalesced 32 x 32 block at a time (the X'
+            // staging area is idle in this pass: every earlier store and MMA read of it
+            // has completed)
             const MatInfo& mt = ap.mats[job.mat];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int gc0 = c * 64 + h * 32;
+            for (int q = 0; q < 2; ++q) {
+              const int gc0 = c * kChunk + 64 * h + 32 * q;
               if (gc0 < job.n) {
                 uint32_t o[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = pack2<FP16>(v[h * 32 + 2 * i], v[h * 32 + 2 * i + 1]);
+                for (int i = 0; i < 16; ++i) o[i] = pack2<FP16>(v[q * 32 + 2 * i], v[q * 32 + 2 * i + 1]);
                 apply_block_columns(mt, o, ep.xw, ep.lane);
                 const ApplyBlock blk = apply_block_at(mt, rb, gc0, job.m, job.n);
                 float pv[32];
@@ -430,32 +454,26 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
               }
             }
           }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (ep.lane == 0) ptx::mbar_arrive(R.bar(&R.ctrl->acc_empty[acc]));
+        ++acc_cnt;
+        rp.advance();
+        if (!stores) {
+          if (reads_x) {
+            ptx::named_sync(kEpiBar, kEpiThreads);  // every thread has read the chunk
+            if (ep.leader) ptx::mbar_arrive(R.bar(&R.ctrl->empty[stage]));
+          }
           continue;
         }
-        // X' panel -> shared-memory slot -> TMA store (and to the MMA when accumulating)
-        const uint32_t slot = (xs0 + static_cast<uint32_t>(c)) & 1u;
-        if (ep.leader) ptx::bulk_wait_group_read<1>();  // the store two panels back has read the slot
-        bool free_ok = true;
-        if (pend[slot] >= 0) {
-          free_ok = R.wait(&R.ctrl->xt_empty[slot], static_cast<uint32_t>(pend[slot]));
-          if (!free_ok) R.give_up();
-          pend[slot] = -1;
-        }
-        if (!ptx::named_all(kEpiBar, kEpiThreads, free_ok)) return false;
-        const uint32_t xt = R.xt + slot * kPanel;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint4 pk;
-          T* e = reinterpret_cast<T*>(&pk);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) e[k] = E::from_f(v[u * 8 + k]);
-          *reinterpret_cast<uint4*>(__cvta_shared_to_generic(xt + sw(ep.row, u))) = pk;
-        }
+        // X' chunk -> TMA stores (and to the MMA when accumulating)
         ptx::fence_proxy_async_smem();
         ptx::named_sync(kEpiBar, kEpiThreads);
         if (ep.leader) {
           if (reads_x) ptx::mbar_arrive(R.bar(&R.ctrl->empty[stage]));
-          ptx::tma_store_3d(job.map_x[op.dst_x], xt, c * 64, 0, job.b);
+          ptx::tma_store_3d(job.map_x[op.dst_x], xt, c * kChunk, 0, job.b);
+          if (c * kChunk + 64 < job.n) ptx::tma_store_3d(job.map_x[op.dst_x], xt + kPanel, c * kChunk + 64, 0, job.b);
           ptx::bulk_commit_group();
         }
         if (op.accumulate) {
