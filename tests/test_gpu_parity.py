@@ -373,8 +373,9 @@ def test_errors_launch_nothing(nsm):
 
 def test_step_bf16_copy(nsm):
     # the bf16 copy is the round-to-nearest-even bf16 of the updated fp32 parameters, and
-    # writing it changes nothing else
-    wl = synth.custom([(256, 384), (384, 256), (130, 260)], seed=13)
+    # writing it changes nothing else (grouped launches and the small-matrix kernel)
+    wl = synth.custom([(256, 384), (384, 256), (130, 260), (64, 192), (300, 100), (128, 128), (7, 1)],
+                      seed=13)
     offsets, total = nsm.pack(wl.muon_shapes)
     dev = "cuda"
     grads = torch.zeros(total, dtype=torch.bfloat16, device=dev)
@@ -392,9 +393,14 @@ def test_step_bf16_copy(nsm):
                       params_bf16=copy)
         torch.cuda.synchronize()
         assert torch.equal(p_a, p_b) and torch.equal(m_a, m_b)
+        inside = torch.zeros(total, dtype=torch.bool, device=dev)
         for i, (r, c) in enumerate(wl.muon_shapes):
             o = int(offsets[i])
             assert torch.equal(copy[o:o + r * c], p_b[o:o + r * c].to(torch.bfloat16))
+            inside[o:o + r * c] = True
+        # nothing written between the matrices (the packing's padding)
+        assert torch.isnan(copy[~inside].float()).all()
+        assert (p_b[~inside] == 0).all() and (m_b[~inside] == 0).all()
 
 
 @pytest.mark.parametrize("method", ["gram", "standard"])
