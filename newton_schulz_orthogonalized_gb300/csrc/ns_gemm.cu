@@ -12,13 +12,14 @@
 //                   (tcgen05.mma.cta_group::2, M = 256): each CTA stages half of A and half
 //                   of B, so each SM's shared memory carries two thirds of the operand
 //                   traffic of the 1-CTA tile for the same tensor-core work.
-// Roles inside a CTA: warp 0 issues TMA loads (128B-swizzled 64x64 boxes) into a ring of
-// stages, warp 1 issues the MMAs (the leader CTA's, in the pair kernel) into two TMEM
-// accumulators of 256 fp32 columns, warps 2-5 drain TMEM with tcgen05.ld, apply the
-// fused epilogue  out = alpha*acc + beta*aux + diag*I  and store fp16/bf16 32 x 32 blocks
-// through shared memory with TMA stores.
+// Roles inside a CTA: warp 0 issues TMA loads (128B-swizzled boxes of 64 columns and 64,
+// 128 or 256 rows) into a ring of stages, warp 1 issues the MMAs (the leader CTA's, in the
+// pair kernel) into two TMEM accumulators of 256 fp32 columns, warps 2-5 drain TMEM with
+// tcgen05.ld, apply the fused epilogue  out = alpha*acc + beta*aux + diag*I  and store
+// fp16/bf16 32 x 32 blocks through shared memory with TMA stores.  With ApplyArgs, the
+// product that forms O applies the optimizer step instead of storing O.
 // A group flagged symmetric computes only the tiles that touch the upper triangle, stores
-// that triangle and mirrors it.
+// the blocks on and above the diagonal and mirrors the upper ones.
 //
 // The stages it serves ("DeepSpeed 集成 Muon 优化器实战" §核心算子):
 //   standard:  A = X X^T;  B = b A + c A A^T (A symmetric);  X' = a X + B X
