@@ -56,7 +56,7 @@ constexpr int BOX_BYTES = 64 * 64 * 2;    // one TMA box: 64 rows x 128 B
 constexpr int NUM_THREADS = 192;          // 6 warps
 constexpr uint32_t TMEM_COLS = 512;       // 2 x 256 fp32 accumulator columns
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
-constexpr int kPanel = 8;                 // column tiles per raster panel
+constexpr int kPanel = 2;                 // column tiles per raster panel
 constexpr int EPI_WARPS = 4;
 // Whether the grouped launches may overlap their launch with the previous kernel when
 // programmatic dependent launch is on (NSM_PDL=1).

@@ -429,12 +429,12 @@ struct StageSpec {
 };
 
 // Tiles (packed mt << 16 | nt) of an m x m output that touch its upper triangle, for
-// tiles of tile_m rows and 256 columns, in the engine's panel raster (panels of 8 column
+// tiles of tile_m rows and 256 columns, in the engine's panel raster (panels of 2 column
 // tiles, rows inside a panel).
 std::vector<int32_t> upper_tiles(int m, int tile_m = 128) {
   std::vector<int32_t> t;
   const int tm = (m + tile_m - 1) / tile_m, tn = (m + 255) / 256;
-  constexpr int kPanel = 8;
+  constexpr int kPanel = 2;
   for (int p0 = 0; p0 < tn; p0 += kPanel)
     for (int mt = 0; mt < tm; ++mt)
       for (int nt = p0; nt < std::min(p0 + kPanel, tn); ++nt)
