@@ -430,23 +430,37 @@ __global__ void __launch_bounds__(kThreads)
   release_dependents();
   const int64_t nvec = numel >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t v = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; v < nvec; v += stride) {
-    const int64_t i = v * 8;
-    float g[8];
-    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(grads + i)), g);
-    float4* pp = reinterpret_cast<float4*>(params + i);
-    float4* mp = reinterpret_cast<float4*>(mom1 + i);
-    float4* vp = reinterpret_cast<float4*>(mom2 + i);
+  // two 8-element groups per iteration, every load issued before the first store
+  for (int64_t v = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; v < nvec; v += 2 * stride) {
+    const bool two = v + stride < nvec;
+    float g[2][8];
+    float4 p[2][2], m[2][2], w[2][2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float4 p = pp[h], m = mp[h], w = vp[h];
-      adamw_elem(g[4 * h + 0], p.x, m.x, w.x, b1, b2, eps, decay, step_size, bc2);
-      adamw_elem(g[4 * h + 1], p.y, m.y, w.y, b1, b2, eps, decay, step_size, bc2);
-      adamw_elem(g[4 * h + 2], p.z, m.z, w.z, b1, b2, eps, decay, step_size, bc2);
-      adamw_elem(g[4 * h + 3], p.w, m.w, w.w, b1, b2, eps, decay, step_size, bc2);
-      pp[h] = p;
-      mp[h] = m;
-      vp[h] = w;
+    for (int u = 0; u < 2; ++u) {
+      if (u == 1 && !two) break;
+      const int64_t i = (v + u * stride) * 8;
+      unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(grads + i)), g[u]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        p[u][h] = reinterpret_cast<const float4*>(params + i)[h];
+        m[u][h] = reinterpret_cast<const float4*>(mom1 + i)[h];
+        w[u][h] = reinterpret_cast<const float4*>(mom2 + i)[h];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u == 1 && !two) break;
+      const int64_t i = (v + u * stride) * 8;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        adamw_elem(g[u][4 * h + 0], p[u][h].x, m[u][h].x, w[u][h].x, b1, b2, eps, decay, step_size, bc2);
+        adamw_elem(g[u][4 * h + 1], p[u][h].y, m[u][h].y, w[u][h].y, b1, b2, eps, decay, step_size, bc2);
+        adamw_elem(g[u][4 * h + 2], p[u][h].z, m[u][h].z, w[u][h].z, b1, b2, eps, decay, step_size, bc2);
+        adamw_elem(g[u][4 * h + 3], p[u][h].w, m[u][h].w, w[u][h].w, b1, b2, eps, decay, step_size, bc2);
+        reinterpret_cast<float4*>(params + i)[h] = p[u][h];
+        reinterpret_cast<float4*>(mom1 + i)[h] = m[u][h];
+        reinterpret_cast<float4*>(mom2 + i)[h] = w[u][h];
+      }
     }
   }
   for (int64_t i = nvec * 8 + blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < numel; i += stride) {
