@@ -253,7 +253,22 @@ __global__ void __launch_bounds__(kThreads)
     const float sc = scales[tp.mi];
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
     if (!mt.transposed) {
-      if (mt.flags & kMatVec) {
+      if ((mt.flags & kMatVec) && ld == cols) {
+        // slot and natural layouts coincide: the matrix's k-th tile is its k-th run of
+        // kTile^2 consecutive elements, streamed contiguously
+        const int64_t base = (t - mt.tile_begin) * (kTile * kTile);
+        const int64_t len = static_cast<int64_t>(rows) * cols;
+        for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+          const int64_t i = base + static_cast<int64_t>(j) * 8;
+          if (i < len) {
+            float f[8];
+            load_u8<MODE>(g, m, i, mu, f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] *= sc;
+            store8<TO_FP16>(dst, d0 + i, f);
+          }
+        }
+      } else if (mt.flags & kMatVec) {
         for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
           const int r = tp.r0 + (j >> 3), c = tp.c0 + (j & 7) * 8;
           if (r < rows && c < cols) {
@@ -354,7 +369,39 @@ __global__ void __launch_bounds__(kThreads)
       }
       __syncthreads();
     }
-    if (mt.flags & kMatVec) {
+    if ((mt.flags & kMatVec) && !mt.transposed && ld == cols) {
+      // slot and natural layouts coincide: the k-th tile is the k-th run of kTile^2
+      // consecutive elements
+      const int64_t base = (t - mt.tile_begin) * (kTile * kTile);
+      const int64_t len = static_cast<int64_t>(rows) * cols;
+      for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+        const int64_t i = base + static_cast<int64_t>(j) * 8;
+        if (i < len) {
+          float f[8];
+          load8<O_FP16>(o, s0 + i, f);
+          if (APPLY) {
+            float4* pp = reinterpret_cast<float4*>(p + i);
+            float4 a = pp[0], b = pp[1];
+            a.x = fmaf(-coef, f[0], a.x * decay);
+            a.y = fmaf(-coef, f[1], a.y * decay);
+            a.z = fmaf(-coef, f[2], a.z * decay);
+            a.w = fmaf(-coef, f[3], a.w * decay);
+            b.x = fmaf(-coef, f[4], b.x * decay);
+            b.y = fmaf(-coef, f[5], b.y * decay);
+            b.z = fmaf(-coef, f[6], b.z * decay);
+            b.w = fmaf(-coef, f[7], b.w * decay);
+            pp[0] = a;
+            pp[1] = b;
+            if (ob) {
+              const float np[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+              *reinterpret_cast<uint4*>(ob + i) = pack_bf16x8(np);
+            }
+          } else {
+            *reinterpret_cast<uint4*>(ob + i) = pack_bf16x8(f);
+          }
+        }
+      }
+    } else if (mt.flags & kMatVec) {
       for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
         const int rr = j >> 3, cc = (j & 7) * 8;
         const int r = tp.r0 + rr, c = tp.c0 + cc;
