@@ -216,6 +216,28 @@ def test_step_ragged(nsm, method):
     Step(nsm, synth.custom(RAGGED, seed=5), method).check()
 
 
+# Direct matrices whose width is a multiple of 64 (slot stride = width) take flat
+# 4096-element runs in the layout and apply passes; other direct matrices keep 64 x 64
+# tiles, and tall ones the transposing tiles.  200x192 ends in a partial run; 256x1000 is
+# 8-aligned (vector accesses) but on tiles.
+FLAT = [(200, 192), (136, 4096), (4096, 136), (256, 1000), (192, 320), (1000, 256)]
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_step_flat_runs(nsm, method):
+    Step(nsm, synth.custom(FLAT, seed=71), method).check()
+
+
+def test_orthogonalize_flat_runs(nsm):
+    # the export of O to the natural layout takes the same runs and tiles
+    wl = synth.custom(FLAT, seed=73)
+    offsets, g, o = orthogonalize_gpu(nsm, wl, "gram")
+    for i, (r, c) in enumerate(wl.muon_shapes):
+        off = int(offsets[i])
+        ref = oracle.orthogonalize(g[off:off + r * c].reshape(r, c), "gram", storage="method")
+        assert rel(o[off:off + r * c].reshape(r, c), ref) <= TOL_NS, ((r, c))
+
+
 @pytest.mark.parametrize("method", ["standard", "gram"])
 def test_step_layer1024(nsm, method):
     Step(nsm, synth.workload("layer1024"), method).check()
@@ -374,8 +396,8 @@ def test_errors_launch_nothing(nsm):
 def test_step_bf16_copy(nsm):
     # the bf16 copy is the round-to-nearest-even bf16 of the updated fp32 parameters, and
     # writing it changes nothing else (grouped launches and the small-matrix kernel)
-    wl = synth.custom([(256, 384), (384, 256), (130, 260), (64, 192), (300, 100), (128, 128), (7, 1)],
-                      seed=13)
+    wl = synth.custom([(256, 384), (384, 256), (130, 260), (64, 192), (300, 100), (128, 128), (7, 1),
+                       (200, 192)], seed=13)
     offsets, total = nsm.pack(wl.muon_shapes)
     dev = "cuda"
     grads = torch.zeros(total, dtype=torch.bfloat16, device=dev)
