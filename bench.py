@@ -353,7 +353,9 @@ def run_ours(args):
     # k+1.
     e2e = None
     try:
-        reps = max(2, min(args.steps, 5))
+        # the same K steps as the device timing (at least 2, at most 20): the first
+        # upload and the last read-back are the pipeline's only unhidden copies
+        reps = max(2, min(args.steps, 20))
         h2d = torch.cuda.Stream()
         d2h = torch.cuda.Stream()
         h_grads = torch.empty(total, dtype=torch.bfloat16, pin_memory=True)
