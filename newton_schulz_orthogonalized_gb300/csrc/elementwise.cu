@@ -6,10 +6,16 @@
 //   k_to_class       X = s U with U recomputed in fp32 from G and the updated M, moved
 //                    from the natural row-major layout into the matrix's slot
 //                    (transposed when rows > cols) and rounded once to bf16 or fp16
-//   k_apply          p <- p (1 - lr wd) - lr sqrt(max(1, rows/cols)) O, O read back from
-//                    the slot (transposed back when rows > cols)
-//   k_export         O copied back to a natural bf16 layout
+//   k_from_class     APPLY: p <- p (1 - lr wd) - lr sqrt(max(1, rows/cols)) O, O read
+//                    back from the slot (transposed back when rows > cols), with the
+//                    bf16 copy of p when asked; otherwise O copied to a natural bf16
+//                    layout (the export of muon_orthogonalize)
 //   k_adamw          decoupled-weight-decay Adam on a flat group
+//
+// The layout kernels work in units of 64 x 64 natural tiles.  A tall matrix's tile is
+// transposed through shared memory; a direct matrix whose slot stride equals its width
+// has the same layout in both places, so its k-th unit is simply its k-th run of 4096
+// consecutive elements.
 //
 // Sources ("DeepSpeed 集成 Muon 优化器实战" §什么是 Muon 优化器？, §核心算子,
 // §混合优化器的参数组构造).  Every reduction runs in a fixed order, so results are
