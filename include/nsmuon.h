@@ -201,6 +201,14 @@ size_t nsm_gemm_scratch_bytes(int M, int N, int flags);
  * NSM_ERR_CUDA if the synchronisation itself reports an error. */
 int nsm_device_status(nsm_stream_t stream, int* status_out);
 
+/* Self-test of the bounded-wait status path: launches one CTA on `stream` whose bounded
+ * wait on an mbarrier that nothing completes expires after wait_us microseconds (1 to
+ * 2,000,000).  The kernel then records the timeout in the device status word, exactly as
+ * a Newton-Schulz kernel that gave up would, and returns; the context stays usable.  The
+ * next nsm_device_status reports NSM_ERR_TIMEOUT (and clears it).  Returns NSM_ERR_ARG,
+ * with nothing launched, for wait_us out of range. */
+int nsm_status_selftest(int wait_us, nsm_stream_t stream);
+
 /* Kernel timing for profiling.  While enabled, every kernel launch of muon_step,
  * muon_orthogonalize, adamw_step and nsm_gemm is bracketed by CUDA events on the
  * caller's stream.  nsm_timing_read_kind synchronises the recorded events and returns,

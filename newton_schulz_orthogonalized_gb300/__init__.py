@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
     L.nsm_gemm_scratch_bytes.restype = ctypes.c_size_t
     L.nsm_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
     L.nsm_device_status.restype = ctypes.c_int
+    L.nsm_status_selftest.argtypes = [ctypes.c_int, _vp]
+    L.nsm_status_selftest.restype = ctypes.c_int
     L.nsm_timing_enable.argtypes = [ctypes.c_int]
     L.nsm_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p,
                                   ctypes.POINTER(ctypes.c_double)]
@@ -315,6 +317,12 @@ def device_status(stream=None) -> int:
     v = ctypes.c_int(0)
     _check(lib().nsm_device_status(_stream_ptr(stream), ctypes.byref(v)))
     return v.value
+
+
+def status_selftest(wait_us: int = 20000, stream=None) -> None:
+    """Launches one CTA whose bounded wait expires after wait_us and records a timeout in
+    the device status word (read it with device_status)."""
+    _check(lib().nsm_status_selftest(int(wait_us), _stream_ptr(stream)))
 
 
 def timing_enable(on: bool = True) -> None:

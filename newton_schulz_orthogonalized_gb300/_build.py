@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
-SOURCES = ["nsm_api.cpp", "elementwise.cu", "ns_gemm.cu", "ns_small.cu"]
+SOURCES = ["nsm_api.cpp", "elementwise.cu", "ns_gemm.cu", "ns_small.cu", "status_check.cu"]
 
 
 def _nvcc() -> str:

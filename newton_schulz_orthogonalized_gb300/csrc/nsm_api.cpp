@@ -1448,6 +1448,13 @@ int nsm_device_status(nsm_stream_t stream_, int* status_out) {
   return NSM_OK;
 }
 
+int nsm_status_selftest(int wait_us, nsm_stream_t stream_) {
+  if (wait_us < 1 || wait_us > 2000000) return fail(NSM_ERR_ARG, "wait_us = %d not in [1, 2000000]", wait_us);
+  const cudaError_t e = launch_status_selftest(uint64_t(wait_us) * 1000u, reinterpret_cast<cudaStream_t>(stream_));
+  if (e != cudaSuccess) return fail_cuda(e, "status self-test launch");
+  return NSM_OK;
+}
+
 int nsm_timing_enable(int enable) {
   Timing& T = timing();
   std::lock_guard<std::mutex> lock(T.mu);

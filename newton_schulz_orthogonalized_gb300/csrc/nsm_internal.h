@@ -151,5 +151,7 @@ cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream,
                         const ApplyArgs* apply = nullptr);
 
 int* device_status_ptr();
+// One CTA whose bounded wait expires after limit_ns and records kDevTimeout.
+cudaError_t launch_status_selftest(uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace nsm

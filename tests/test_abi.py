@@ -159,3 +159,9 @@ def test_optimizer_wrapper_routing(nsm):
     muon = [n for n, s in named if nsm.route(n, len(s))]
     assert muon == ["layers.0.q_proj.weight", "conv.weight"]
     assert oracle.matrix_view_shape((8, 3, 3, 3)) == (8, 27)
+
+
+def test_status_selftest_validation_without_gpu(nsm):
+    L = nsm.lib()
+    assert L.nsm_status_selftest(0, None) == nsm.NSM_ERR_ARG
+    assert L.nsm_status_selftest(2000001, None) == nsm.NSM_ERR_ARG

@@ -466,6 +466,20 @@ def test_step_replays_in_cuda_graph(nsm, method):
     assert torch.equal(p_graph, p_direct) and torch.equal(m_graph, m_direct)
 
 
+def test_expired_wait_is_reported_and_context_survives(nsm):
+    # a bounded in-kernel wait on a barrier nothing completes runs out after 20 ms,
+    # records the timeout in the status word and returns: the status read reports it
+    # once, and the same context still computes a correct step
+    import time
+    assert nsm.device_status() == nsm.NSM_OK
+    t0 = time.perf_counter()
+    nsm.status_selftest(20000)
+    assert nsm.device_status() == nsm.NSM_ERR_TIMEOUT
+    assert time.perf_counter() - t0 >= 0.02
+    assert nsm.device_status() == nsm.NSM_OK
+    Step(nsm, synth.workload("tiny"), "gram").check()
+
+
 def test_checkpoint_resume_bitwise(nsm):
     # the step's whole state is the fp32 params and momentum (plus the caller's step
     # count): saving them mid-run and resuming gives bit-identical later steps
