@@ -191,24 +191,24 @@ def _traffic_record(method, workload):
     return None
 
 
-def cpu_oracle_sample(wl, method, budget_s=20.0, min_mats=1):
+def cpu_oracle_sample(wl, method, budget_s=20.0, max_flops=3e12):
     """Times the oracle on a bounded sample of the workload; returns (ms per full step
-    extrapolated by canonical flops, description)."""
+    extrapolated by canonical flops, description).  The sample is one matrix of each of
+    the smallest shapes, as many as fit in max_flops canonical NS flops (at least one)."""
     import numpy as np
     import oracle
     import synth
     import torch
 
     order = sorted(range(len(wl.muon_shapes)), key=lambda i: wl.muon_shapes[i][0] * wl.muon_shapes[i][1])
-    # one matrix of each of the smallest shapes until the estimated budget is used
     picked, seen = [], set()
     for i in order:
         if wl.muon_shapes[i] in seen:
             continue
         seen.add(wl.muon_shapes[i])
-        picked.append(i)
-        if len(picked) >= min_mats and _canonical_ns_flops([wl.muon_shapes[j] for j in picked], method) > 2e11:
+        if picked and _canonical_ns_flops([wl.muon_shapes[j] for j in picked + [i]], method) > max_flops:
             break
+        picked.append(i)
     t_total = 0.0
     flops = 0
     for i in picked:
@@ -240,7 +240,8 @@ def run_reference(args):
     vals = []
     desc = ""
     for k in range(args.warmup + args.steps):
-        ms, desc = cpu_oracle_sample(wl, args.method, budget_s=3.0)
+        # the cpu_baseline's sample, so that the two lines measure the same thing
+        ms, desc = cpu_oracle_sample(wl, args.method, budget_s=20.0)
         if k >= args.warmup:
             vals.append(ms)
     value = statistics.median(vals)
