@@ -323,6 +323,8 @@ def run_ours(args):
             launches += step()
         t1.record(stream)
         torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
     ms = t0.elapsed_time(t1) / args.steps
     # ---- the same number of steps again with an event pair around every launch: the
     # per-kernel times behind `kernels` and `roofline`
