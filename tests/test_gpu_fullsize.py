@@ -41,7 +41,9 @@ def _run_fullsize(nsm, name, method, sample_shapes, last_too=()):
     synth.fill_packed_params(wl, offsets, params)
     p0 = params.clone()
     ws = torch.empty(nsm.workspace_bytes(shapes, method), dtype=torch.uint8, device=dev)
-    nsm.muon_step(grads, params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws)
+    copy = torch.empty(total, dtype=torch.bfloat16, device=dev)
+    nsm.muon_step(grads, params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws,
+                  params_bf16=copy)
     assert nsm.device_status() == nsm.NSM_OK
     del ws
     # properties on every matrix: O = (p0 (1 - lr wd) - p1) / (lr scale)
@@ -61,6 +63,13 @@ def _run_fullsize(nsm, name, method, sample_shapes, last_too=()):
         picked.append(where[0])
         if len(where) > 1 and want in last_too:
             picked.append(where[-1])
+    # the bf16 copy (the owner's broadcast payload) is the rounding of the updated params,
+    # here on the sampled matrices and on the table's last one (the largest offsets)
+    for i in picked + [len(shapes) - 1]:
+        r, c = shapes[i]
+        o = int(offsets[i])
+        assert torch.equal(copy[o:o + r * c], params[o:o + r * c].to(torch.bfloat16)), i
+    del copy
     for i in picked:
         r, c = shapes[i]
         o = int(offsets[i])
