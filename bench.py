@@ -1,16 +1,20 @@
 """Benchmark of the owner-side Muon step on GB300: one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config llama7b]
-                    [--method gram|standard] [--impl ours|reference]
+                    [--method gram|standard] [--impl ours|reference] [--no-other-configs]
 
 A step is one muon_step over the whole packed group of the workload (momentum, norm,
 five Newton-Schulz steps, decoupled decay and apply), plus the AdamW step of the
 workload's routed-out parameters when it has any.  Inputs are synthetic (seeded,
 transformer-shaped; see ``synth``) and already resident in HBM when the timed region
 starts; the workload's state (tens of GB) is far larger than L2, so no flush is needed.
+The line also carries, for the other workloads, a few timed steps each
+(``other_configs``).
 
---impl reference times the float64 CPU oracle on a bounded sample of the same workload
-and extrapolates to a full step by canonical flop count.
+--impl reference times the float64 CPU oracle on a bounded sample of the same workload:
+every step times the oracle on one matrix of one of the workload's distinct shapes (the
+first step on all of them) and reports the full step that the latest time of every shape
+implies, weighting each shape by its count in the table.
 """
 
 from __future__ import annotations
@@ -30,6 +34,7 @@ if ROOT not in sys.path:
 
 METRIC = "Muon optimizer step ms & NS TFLOP/s (frac of bf16 peak) on 1 GB300 vs CPU oracle"
 NS_STEPS = 5
+OTHER_CONFIGS = ("tiny", "layer1024", "gpt2small", "split_moe")
 
 
 def _peaks():
@@ -46,13 +51,14 @@ def _peaks():
 
 
 def _gram_counts(steps=NS_STEPS, every=2):
-    """(products with X, square products) of the re-anchored gram form."""
+    """(products with X, square products) of the gram form re-anchored every `every`
+    steps (every = 0: never)."""
     wide, cubes, q_identity = 1, 0, True
     for step in range(1, steps + 1):
         cubes += 1 if q_identity else 2
         q_identity = False
         if step < steps:
-            if step % every == 0:
+            if every and step % every == 0:
                 wide += 2
                 q_identity = True
             else:
@@ -60,10 +66,9 @@ def _gram_counts(steps=NS_STEPS, every=2):
     return wide + (0 if q_identity else 1), cubes
 
 
-def _canonical_ns_flops(shapes, method):
-    """Flops of the Newton-Schulz chain as the library runs it."""
+def _chain_flops(shapes, method, every):
     tot = 0
-    wide, cubes = _gram_counts()
+    wide, cubes = _gram_counts(NS_STEPS, every)
     for r, c in shapes:
         m, n = min(r, c), max(r, c)
         if method == "standard":
@@ -71,6 +76,18 @@ def _canonical_ns_flops(shapes, method):
         else:
             tot += 2 * wide * m * m * n + 2 * cubes * m ** 3
     return tot
+
+
+def _canonical_ns_flops(shapes, method):
+    """The method's canonical flop count: 5 (4 m^2 n + 2 m^3) per matrix for the standard
+    form, 4 m^2 n + 34 m^3 for the gram form iterated on R without re-anchoring."""
+    return _chain_flops(shapes, method, every=0)
+
+
+def _dense_ns_flops(shapes, method):
+    """Flops of the chain as the library runs it (the gram form re-anchored every 2
+    steps), counted as if every tile of every product were computed."""
+    return _chain_flops(shapes, method, every=2)
 
 
 def _describe(wl):
@@ -191,44 +208,55 @@ def _traffic_record(method, workload):
     return None
 
 
-def cpu_oracle_sample(wl, method, budget_s=20.0, max_flops=3e12):
-    """Times the oracle on a bounded sample of the workload; returns (ms per full step
-    extrapolated by canonical flops, description).  The sample is one matrix of each of
-    the smallest shapes, as many as fit in max_flops canonical NS flops (at least one)."""
+# ---------------------------------------------------------------- the oracle on the host
+
+def _shape_counts(wl):
+    """Distinct shapes of the table, smallest first, with the index of their first matrix
+    and their count."""
+    counts, first = {}, {}
+    for i, sh in enumerate(wl.muon_shapes):
+        counts[sh] = counts.get(sh, 0) + 1
+        first.setdefault(sh, i)
+    order = sorted(counts, key=lambda s: s[0] * s[1])
+    return [(sh, first[sh], counts[sh]) for sh in order]
+
+
+def _time_oracle_matrix(wl, method, sh, index):
+    """Seconds the float64 oracle takes for one whole step of one matrix of shape sh."""
     import numpy as np
     import oracle
     import synth
-    import torch
+    r, c = sh
+    g = synth.make_grad(r, c, wl.seed, index, "cpu", wl.lowrank).double().numpy()
+    p = np.zeros((r, c))
+    m = np.zeros((r, c))
+    t0 = time.perf_counter()
+    oracle.muon_step([g], [p], [m], wl.lr, wl.wd, wl.mu, method)
+    return time.perf_counter() - t0
 
-    order = sorted(range(len(wl.muon_shapes)), key=lambda i: wl.muon_shapes[i][0] * wl.muon_shapes[i][1])
-    picked, seen = [], set()
-    for i in order:
-        if wl.muon_shapes[i] in seen:
-            continue
-        seen.add(wl.muon_shapes[i])
-        if picked and _canonical_ns_flops([wl.muon_shapes[j] for j in picked + [i]], method) > max_flops:
+
+def cpu_oracle_sample(wl, method, budget_s=30.0):
+    """Times the float64 oracle (the exact iteration) on one matrix of each distinct shape
+    of the workload, smallest shapes first, until the budget is spent (at least one); the
+    full step is the sum over shapes of count x time, scaled by the share of the table's
+    matrices whose shape was timed when the budget ran out.  Returns (ms per full step,
+    description)."""
+    shapes = _shape_counts(wl)
+    times = {}
+    spent = 0.0
+    for sh, idx, _ in shapes:
+        if times and spent > budget_s:
             break
-        picked.append(i)
-    t_total = 0.0
-    flops = 0
-    for i in picked:
-        r, c = wl.muon_shapes[i]
-        g = synth.make_grad(r, c, wl.seed, i, "cpu", wl.lowrank).double().numpy()
-        p = np.zeros((r, c))
-        m = np.zeros((r, c))
-        t0 = time.perf_counter()
-        oracle.muon_step([g], [p], [m], wl.lr, wl.wd, wl.mu, method, storage="method")
-        t_total += time.perf_counter() - t0
-        flops += _canonical_ns_flops([(r, c)], method)
-        if t_total > budget_s:
-            break
-    full = _canonical_ns_flops(wl.muon_shapes, method)
-    ms = t_total * 1e3 * full / flops
-    desc = (f"oracle.muon_step ({method}) on {len(picked)} matrices "
-            f"({', '.join(f'{wl.muon_shapes[i][0]}x{wl.muon_shapes[i][1]}' for i in picked)}), "
-            f"{t_total:.2f} s, extrapolated to the full {len(wl.muon_shapes)}-matrix step by canonical "
-            f"NS flops ({flops:.3e} of {full:.3e})")
-    return ms, desc
+        t = _time_oracle_matrix(wl, method, sh, idx)
+        times[sh] = t
+        spent += t
+    covered = sum(cnt for sh, _, cnt in shapes if sh in times)
+    est = sum(cnt * times[sh] for sh, _, cnt in shapes if sh in times) * len(wl.muon_shapes) / covered
+    desc = (f"oracle.muon_step ({method}, exact float64 iteration) on one matrix of each of "
+            f"{len(times)} of the {len(shapes)} distinct shapes "
+            f"({', '.join(f'{r}x{c} {times[(r, c)]:.2f} s' for (r, c) in times)}); the full "
+            f"{len(wl.muon_shapes)}-matrix step is extrapolated as the sum over shapes of count x time")
+    return est * 1e3, desc
 
 
 def run_reference(args):
@@ -237,32 +265,249 @@ def run_reference(args):
         return 0
     import synth
     wl = synth.workload(args.config)
+    shapes = _shape_counts(wl)
+    latest = {}
     vals = []
-    desc = ""
     for k in range(args.warmup + args.steps):
-        # the cpu_baseline's sample, so that the two lines measure the same thing
-        ms, desc = cpu_oracle_sample(wl, args.method, budget_s=20.0)
+        if k == 0:
+            for sh, idx, _ in shapes:
+                latest[sh] = _time_oracle_matrix(wl, args.method, sh, idx)
+        else:
+            sh, idx, _ = shapes[(k - 1) % len(shapes)]
+            latest[sh] = _time_oracle_matrix(wl, args.method, sh, idx)
+        ms = 1e3 * sum(cnt * latest[sh] for sh, _, cnt in shapes)
         if k >= args.warmup:
             vals.append(ms)
     value = statistics.median(vals)
     cores = os.cpu_count()
+    desc = (f"oracle.muon_step ({args.method}, exact float64 iteration): the first step times one "
+            f"matrix of each of the {len(shapes)} distinct shapes, every later step re-times one "
+            f"shape in turn; each step reports the sum over shapes of count x latest time "
+            f"(median of {args.steps} timed steps)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "ms", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "ms", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": dict(_describe(wl), ns_method=args.method, ns_steps=NS_STEPS),
-        "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle", "sample": desc,
+                         "extrapolated": True},
         "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
 
 
+# ---------------------------------------------------------------- the GPU path
+
+class Setup:
+    """Device buffers of one workload's step."""
+
+    def __init__(self, nsm, wl, method, dev):
+        import torch
+        import synth
+        self.wl, self.method, self.dev = wl, method, dev
+        self.shapes = wl.muon_shapes
+        self.offsets, self.total = nsm.pack(self.shapes)
+        self.grads = torch.empty(self.total, dtype=torch.bfloat16, device=dev)
+        self.params = torch.zeros(self.total, dtype=torch.float32, device=dev)
+        self.mom = torch.zeros(self.total, dtype=torch.float32, device=dev)
+        synth.fill_packed_grads(wl, self.offsets, self.grads)
+        synth.fill_packed_params(wl, self.offsets, self.params)
+        self.ws = torch.empty(nsm.workspace_bytes(self.shapes, method, NS_STEPS), dtype=torch.uint8, device=dev)
+        self.adam = None
+        if wl.adam_elements:
+            ag, ap = synth.make_adam_group(wl, dev)
+            self.adam = (ag, ap, torch.zeros_like(ap), torch.zeros_like(ap))
+        self.t = 0
+
+    def step(self, nsm, stream, grads=None, params_bf16=None, adam_grads=None):
+        nsm.muon_step(self.grads if grads is None else grads, self.params, self.mom, self.offsets, self.shapes,
+                      self.wl.lr, self.wl.wd, self.wl.mu, self.method, NS_STEPS, True, self.ws, stream,
+                      params_bf16=params_bf16)
+        launches = nsm.last_launch_count()
+        if self.adam is not None:
+            self.t += 1
+            nsm.adamw_step(self.adam[0] if adam_grads is None else adam_grads, self.adam[1], self.adam[2],
+                           self.adam[3], 3e-4, 0.9, 0.95, 1e-10, self.wl.wd, self.t, stream)
+            launches += nsm.last_launch_count()
+        return launches
+
+
+def _timed_steps(nsm, S, stream, steps):
+    """Device ms per step over `steps` uninstrumented steps (CUDA events on the stream)."""
+    import torch
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    launches = 0
+    t0.record(stream)
+    for _ in range(steps):
+        launches += S.step(nsm, stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps, launches
+
+
+def _kernel_times(nsm, S, stream, steps):
+    """Per kernel kind: (ms, launches, work) over `steps` steps with an event pair around
+    every launch."""
+    import torch
+    nsm.timing_reset()
+    nsm.timing_enable(True)
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        S.step(nsm, stream)
+    torch.cuda.synchronize()
+    nsm.timing_enable(False)
+    per_kind = {}
+    for kind, kname in nsm.KIND_NAMES.items():
+        k_ms, k_n, k_work = nsm.timing_read(kind)
+        if k_n:
+            per_kind[kname] = (k_ms, k_n, k_work)
+    return per_kind
+
+
+def _kernels_block(per_kind, steps, peaks):
+    peak_t = peaks["bf16_tflops_sustained"]
+    out = {}
+    for kname, (k_ms, k_n, k_work) in per_kind.items():
+        flops = kname in FLOP_KERNELS
+        ach = (k_work / (k_ms * 1e-3) / (1e12 if flops else 1e9)) if k_ms > 0 else None
+        out[kname] = {"launches": k_n, "ms_per_step": k_ms / steps, "achieved": ach,
+                      "unit": "TFLOP/s" if flops else "GB/s",
+                      "frac": (ach / (peak_t if flops else peaks["hbm_gbs"])) if ach else None}
+    return out
+
+
+def _e2e(nsm, S, stream, reps):
+    """The step end to end through the public API with host buffers: every step copies
+    its bf16 grads (and the AdamW group's) host -> device from pinned memory, runs the
+    step, and reads back the bf16 copy of the updated Muon parameters that the step
+    writes.  Two copy streams and double-buffered device buffers let step k's copies
+    overlap steps k-1 and k+1.  Every copy and every step is bracketed by events on its
+    own stream, so the line records where the time went."""
+    import torch
+    dev = S.dev
+    h2d = torch.cuda.Stream()
+    d2h = torch.cuda.Stream()
+    # the host copy of the grads is filled by the CPU (a device-to-host copy into pageable
+    # memory, then a host memcpy), as a data loader would leave it
+    h_grads = torch.empty(S.total, dtype=torch.bfloat16, pin_memory=True)
+    h_grads.copy_(S.grads.cpu())
+    h_out = torch.empty(S.total, dtype=torch.bfloat16, pin_memory=True)
+    d_grads = [S.grads, torch.empty_like(S.grads)]
+    d_out = [torch.empty(S.total, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    h_agrads = d_agrads = None
+    if S.adam is not None:
+        h_agrads = torch.empty(S.adam[0].numel(), dtype=torch.bfloat16, pin_memory=True)
+        h_agrads.copy_(S.adam[0].cpu())
+        d_agrads = [S.adam[0], torch.empty_like(S.adam[0])]
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def upload(slot):
+        d_grads[slot].copy_(h_grads, non_blocking=True)
+        if d_agrads is not None:
+            d_agrads[slot].copy_(h_agrads, non_blocking=True)
+
+    def pipeline():
+        up = [(ev(), ev()) for _ in range(reps)]
+        cp = [(ev(), ev()) for _ in range(reps)]
+        dn = [(ev(), ev()) for _ in range(reps)]
+        torch.cuda.synchronize()
+        e0, e1 = ev(), ev()
+        e0.record(h2d)
+        with torch.cuda.stream(h2d):
+            up[0][0].record(h2d)
+            upload(0)
+            up[0][1].record(h2d)
+        for k in range(reps):
+            cur, nxt = k % 2, (k + 1) % 2
+            stream.wait_event(up[k][1])
+            if k >= 2:
+                stream.wait_event(dn[k - 2][1])  # step k-2's result has left d_out[cur]
+            cp[k][0].record(stream)
+            S.step(nsm, stream, grads=d_grads[cur], params_bf16=d_out[cur],
+                   adam_grads=None if d_agrads is None else d_agrads[cur])
+            cp[k][1].record(stream)
+            if k + 1 < reps:
+                with torch.cuda.stream(h2d):
+                    if k >= 1:
+                        h2d.wait_event(cp[k - 1][1])  # step k-1 is done with d_grads[nxt]
+                    up[k + 1][0].record(h2d)
+                    upload(nxt)
+                    up[k + 1][1].record(h2d)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(cp[k][1])
+                dn[k][0].record(d2h)
+                h_out.copy_(d_out[cur], non_blocking=True)
+                dn[k][1].record(d2h)
+        h2d.wait_stream(d2h)
+        e1.record(h2d)
+        torch.cuda.synchronize()
+        dur = lambda p: p[0].elapsed_time(p[1])
+        return {"ms_per_step": e0.elapsed_time(e1) / reps,
+                "h2d_ms_per_step": statistics.mean(dur(p) for p in up),
+                "compute_ms_per_step": statistics.mean(dur(p) for p in cp),
+                "d2h_ms_per_step": statistics.mean(dur(p) for p in dn),
+                "first_upload_ms": dur(up[0]), "last_download_ms": dur(dn[-1])}
+
+    # Host<->device copy speed varies between machines of the pool (and, on some, from
+    # pass to pass), so one untimed pass warms the pinned buffers and the median of three
+    # timed passes is reported, with every pass's breakdown.
+    pipeline()
+    passes = [pipeline() for _ in range(3)]
+    med = sorted(passes, key=lambda p: p["ms_per_step"])[1]
+    h2d_bytes = S.total * 2 + (S.adam[0].numel() * 2 if S.adam is not None else 0)
+    res = {"value": med["ms_per_step"], "unit": "ms",
+           "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": S.total * 2,
+           "steps": reps, "statistic": "median of 3 timed passes",
+           "overlap": "copies on two streams, double-buffered",
+           "breakdown": {k: med[k] for k in med if k != "ms_per_step"},
+           "h2d_gbs": h2d_bytes / (med["h2d_ms_per_step"] * 1e-3) / 1e9,
+           "d2h_gbs": S.total * 2 / (med["d2h_ms_per_step"] * 1e-3) / 1e9,
+           "passes_ms": [p["ms_per_step"] for p in passes]}
+    # the bound: the slowest of the three streams per step
+    res["bound"] = max(("compute", med["compute_ms_per_step"]), ("h2d", med["h2d_ms_per_step"]),
+                       ("d2h", med["d2h_ms_per_step"]), key=lambda t: t[1])[0]
+    return res
+
+
+def _other_configs(nsm, names, method, dev, stream, peaks):
+    """A few timed steps of each other workload (device step ms, kernel rates)."""
+    import torch
+    out = {}
+    for name in names:
+        try:
+            import synth
+            wl = synth.workload(name)
+            S = Setup(nsm, wl, method, dev)
+            steps = 20 if wl.muon_elements < 1e9 else 5
+            for _ in range(3):
+                S.step(nsm, stream)
+            ms, launches = _timed_steps(nsm, S, stream, steps)
+            per_kind = _kernel_times(nsm, S, stream, steps)
+            if nsm.device_status() != nsm.NSM_OK:
+                raise RuntimeError("a bounded device wait expired")
+            kb = _kernels_block(per_kind, steps, peaks)
+            out[name] = {"ms_per_step": ms, "steps": steps, "matrices": len(wl.muon_shapes),
+                         "muon_elements": wl.muon_elements, "adam_elements": wl.adam_elements,
+                         "gpu_launches_per_step": launches / steps,
+                         "gemm_frac_executed": kb.get("k_ns_gemm", {}).get("frac"),
+                         "adamw_gbs": kb.get("k_adamw", {}).get("achieved"),
+                         "adamw_frac": kb.get("k_adamw", {}).get("frac"),
+                         "kernels": kb}
+            del S
+        except Exception as exc:
+            out[name] = {"error": str(exc)[:200]}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
     import newton_schulz_orthogonalized_gb300 as nsm
-    import synth
 
     world, rank, local = _dist_setup(args)
     if not torch.cuda.is_available():
@@ -275,72 +520,30 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     nsm.lib()
     wl = rank_workload(args.config, rank)
-    shapes = wl.muon_shapes
     method = args.method
-    offsets, total = nsm.pack(shapes)
-    grads = torch.empty(total, dtype=torch.bfloat16, device=dev)
-    params = torch.zeros(total, dtype=torch.float32, device=dev)
-    mom = torch.zeros(total, dtype=torch.float32, device=dev)
-    synth.fill_packed_grads(wl, offsets, grads)
-    synth.fill_packed_params(wl, offsets, params)
-    ws = torch.empty(nsm.workspace_bytes(shapes, method, NS_STEPS), dtype=torch.uint8, device=dev)
-    adam = None
-    if wl.adam_elements:
-        ag, ap = synth.make_adam_group(wl, dev)
-        adam = (ag, ap, torch.zeros_like(ap), torch.zeros_like(ap))
+    S = Setup(nsm, wl, method, dev)
+    shapes = S.shapes
     stream = torch.cuda.current_stream()
-    adam_state = {"t": 0}
-
-    def step():
-        nsm.muon_step(grads, params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method, NS_STEPS,
-                      True, ws, stream)
-        launches = nsm.last_launch_count()
-        if adam is not None:
-            adam_state["t"] += 1
-            nsm.adamw_step(adam[0], adam[1], adam[2], adam[3], 3e-4, 0.9, 0.95, 1e-10, wl.wd,
-                           adam_state["t"], stream)
-            launches += nsm.last_launch_count()
-        return launches
 
     for _ in range(args.warmup):
-        step()
+        S.step(nsm, stream)
     torch.cuda.synchronize()
     if nsm.device_status() != nsm.NSM_OK:
         raise RuntimeError("a bounded device wait expired during warm-up")
 
     # ---- timed region (device events on the launching stream).  The step time comes from
-    # an uninstrumented pass: events between the library's launches would serialise them
-    # and hide the overlap of one kernel's tail with the next kernel's launch.
+    # an uninstrumented pass: events between the library's launches would serialise them.
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    launches = 0
     with ClockSampler(local) as clk:
-        t0.record(stream)
-        for _ in range(args.steps):
-            launches += step()
-        t1.record(stream)
-        torch.cuda.synchronize()
+        ms, launches = _timed_steps(nsm, S, stream, args.steps)
         if dist is not None:
             dist.barrier()
-    ms = t0.elapsed_time(t1) / args.steps
     # ---- the same number of steps again with an event pair around every launch: the
     # per-kernel times behind `kernels` and `roofline`
-    nsm.timing_reset()
-    nsm.timing_enable(True)
-    torch.cuda.synchronize()
-    for _ in range(args.steps):
-        step()
-    torch.cuda.synchronize()
-    nsm.timing_enable(False)
-    gemm_ms, gemm_launches, gemm_flops = nsm.timing_read(nsm.KIND_GEMM)
-    per_kind = {}
-    for kind, kname in nsm.KIND_NAMES.items():
-        k_ms, k_n, k_work = nsm.timing_read(kind)
-        if k_n:
-            per_kind[kname] = (k_ms, k_n, k_work)
+    per_kind = _kernel_times(nsm, S, stream, args.steps)
+    gemm_ms, gemm_launches, gemm_flops = per_kind.get("k_ns_gemm", (0.0, 0, 0.0))
     if nsm.device_status() != nsm.NSM_OK:
         raise RuntimeError("a bounded device wait expired in the timed region")
     ms = max_over_ranks(ms, dist, dev)
@@ -348,154 +551,83 @@ def run_ours(args):
         dist.barrier()
     clocks = clk.summary()
 
-    # ---- end to end through the public API with host buffers.  Every step copies its bf16
-    # grads (the Muon group's and the AdamW group's) host -> device from pinned memory, runs
-    # muon_step and adamw_step, and reads its result back: the bf16 copy of the updated
-    # Muon parameters that the step writes (the buffer an owner broadcasts).  Two copy
-    # streams and double-buffered device buffers let step k's copies overlap steps k-1 and
-    # k+1.
-    e2e = None
+    # ---- end to end through the public API with host buffers
     try:
-        # the same K steps as the device timing (at least 2, at most 20): the first
-        # upload and the last read-back are the pipeline's only unhidden copies
-        reps = max(2, min(args.steps, 20))
-        h2d = torch.cuda.Stream()
-        d2h = torch.cuda.Stream()
-        h_grads = torch.empty(total, dtype=torch.bfloat16, pin_memory=True)
-        h_grads.copy_(grads)
-        h_out = torch.empty(total, dtype=torch.bfloat16, pin_memory=True)
-        d_grads = [grads, torch.empty_like(grads)]
-        d_out = [torch.empty(total, dtype=torch.bfloat16, device=dev) for _ in range(2)]
-        # the AdamW group's gradients are inputs of the step too
-        h_agrads = d_agrads = None
-        if adam is not None:
-            h_agrads = torch.empty(adam[0].numel(), dtype=torch.bfloat16, pin_memory=True)
-            h_agrads.copy_(adam[0])
-            d_agrads = [adam[0], torch.empty_like(adam[0])]
-        ev = lambda: torch.cuda.Event()
-
-        def upload(slot):
-            d_grads[slot].copy_(h_grads, non_blocking=True)
-            if d_agrads is not None:
-                d_agrads[slot].copy_(h_agrads, non_blocking=True)
-
-        def pipeline():
-            h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(h2d)
-            with torch.cuda.stream(h2d):
-                upload(0)
-                h2d_done[0].record(h2d)
-            for k in range(reps):
-                cur, nxt = k % 2, (k + 1) % 2
-                stream.wait_event(h2d_done[cur])
-                if k >= 2:
-                    stream.wait_event(d2h_done[cur])  # step k-2's result has left d_out[cur]
-                nsm.muon_step(d_grads[cur], params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method,
-                              NS_STEPS, True, ws, stream, params_bf16=d_out[cur])
-                if adam is not None:
-                    adam_state["t"] += 1
-                    nsm.adamw_step(d_agrads[cur], adam[1], adam[2], adam[3], 3e-4, 0.9, 0.95, 1e-10, wl.wd,
-                                   adam_state["t"], stream)
-                comp_done[cur].record(stream)
-                if k + 1 < reps:
-                    with torch.cuda.stream(h2d):
-                        if k >= 1:
-                            h2d.wait_event(comp_done[nxt])  # step k-1 is done with d_grads[nxt]
-                        upload(nxt)
-                        h2d_done[nxt].record(h2d)
-                with torch.cuda.stream(d2h):
-                    d2h.wait_event(comp_done[cur])
-                    h_out.copy_(d_out[cur], non_blocking=True)
-                    d2h_done[cur].record(d2h)
-            h2d.wait_stream(d2h)
-            e1.record(h2d)
-            torch.cuda.synchronize()
-            return e0.elapsed_time(e1) / reps
-
-        # Host<->device copy speed on these machines varies from pass to pass while the
-        # GPU runs at its power cap, so one untimed pass warms the pinned buffers and the
-        # median of three timed passes is reported (all three are listed).
-        pipeline()
-        passes = [pipeline() for _ in range(3)]
-        h2d_bytes = total * 2 + (adam[0].numel() * 2 if adam is not None else 0)
-        e2e = {"value": sorted(passes)[1], "unit": "ms",
-               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": total * 2,
-               "steps": reps, "passes_ms": passes, "statistic": "median of 3 timed passes",
-               "overlap": "copies on two streams, double-buffered"}
-        del h_grads, h_out, d_grads, d_out, h_agrads, d_agrads
+        e2e = _e2e(nsm, S, stream, max(2, min(args.steps, 20)))
     except Exception as exc:  # pinned memory may be unavailable on a host
-        e2e = {"value": None, "unit": "ms", "h2d_bytes_per_step": total * 2,
-               "d2h_bytes_per_step": total * 2, "error": str(exc)[:200]}
+        e2e = {"value": None, "unit": "ms", "h2d_bytes_per_step": S.total * 2,
+               "d2h_bytes_per_step": S.total * 2, "error": str(exc)[:200]}
+
+    peaks = _peaks()
+    kernels = _kernels_block(per_kind, args.steps, peaks)
+    del S
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    others = None
+    if rank == 0 and not args.no_other_configs:
+        others = _other_configs(nsm, [c for c in OTHER_CONFIGS if c != args.config], method, dev, stream, peaks)
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return 0
 
-    peaks = _peaks()
     per_launch_ms = gemm_ms / max(gemm_launches, 1)
     per_launch_flops = gemm_flops / max(gemm_launches, 1)
     achieved_tflops = per_launch_flops / (per_launch_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
     peak = peaks["bf16_tflops_sustained"]
-    ns_flops = _canonical_ns_flops(shapes, method)
     ns_ms_per_step = gemm_ms / args.steps
+    tflops = lambda f: f / (ns_ms_per_step * 1e-3) / 1e12 if ns_ms_per_step > 0 else None
     line = {
         "metric": METRIC,
         "value": ms * 1.0,
         "unit": "ms",
-        "n_gpus": args.gpus,
+        "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms,
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if method == "standard" else "f16",
+        "dtype": "f16",
         "data": "synthetic",
         "config": dict(_describe(wl), ns_method=method, ns_steps=NS_STEPS,
+                       storage="fp16 iterates, fp32 tensor-core accumulation; bf16 grads, fp32 params/momentum",
                        l2="inputs larger than L2 (no flush)",
-                       parallelism="replicas" if args.gpus > 1 else "single"),
+                       parallelism="replicas" if world > 1 else "single"),
         "ns_chain_ms_per_step": ns_ms_per_step,
-        "ns_tflops": ns_flops / (ns_ms_per_step * 1e-3) / 1e12 if ns_ms_per_step > 0 else None,
-        "ns_frac_of_peak": (ns_flops / (ns_ms_per_step * 1e-3) / 1e12) / peak if ns_ms_per_step > 0 else None,
-        "matrices_per_s": len(shapes) / (ms * 1e-3) * args.gpus,
+        # the chain's canonical flops (standard 5(4m^2n+2m^3), gram 4m^2n+34m^3 per matrix)
+        # and the dense flops of the chain as run (gram re-anchored), over the GEMM time
+        "ns_tflops_canonical": tflops(_canonical_ns_flops(shapes, method)),
+        "ns_tflops_dense": tflops(_dense_ns_flops(shapes, method)),
+        "ns_frac_executed": achieved_tflops / peak if achieved_tflops else None,
+        "matrices_per_s": len(shapes) * world / (ms * 1e-3),
         "roofline": {
             "kernel": "k_ns_gemm",
             "bound": "tensor",
             "achieved": achieved_tflops,
             "peak": peak,
-            "peak_kind": f"bf16 sustained ({peaks['source']}); fp16 nominal ratio 1:1" if method == "gram"
-                         else f"bf16 sustained ({peaks['source']})",
+            "peak_kind": f"bf16 sustained ({peaks['source']}); fp16 at the nominal 1:1 ratio",
             "unit": "TFLOP/s",
             "frac": achieved_tflops / peak if achieved_tflops else None,
             "traffic": _traffic_record(method, wl.name),
             "launches_timed": gemm_launches,
             "flops_per_launch": per_launch_flops,
+            "flops_counted": "executed: whole tiles, upper-triangle tiles of symmetric outputs",
             "ms_per_launch": per_launch_ms,
             "timing": "CUDA events around every launch, in a second timed pass of the same steps",
         },
-        "kernels": {
-            kname: {
-                "launches": k_n,
-                "ms_per_step": k_ms / args.steps,
-                "achieved": (k_work / (k_ms * 1e-3) / (1e12 if kname in FLOP_KERNELS else 1e9)) if k_ms > 0 else None,
-                "unit": "TFLOP/s" if kname in FLOP_KERNELS else "GB/s",
-                "frac": ((k_work / (k_ms * 1e-3) / 1e12) / peak if kname in FLOP_KERNELS
-                         else (k_work / (k_ms * 1e-3) / 1e9) / peaks["hbm_gbs"]) if k_ms > 0 else None,
-            }
-            for kname, (k_ms, k_n, k_work) in per_kind.items()
-        },
+        "kernels": kernels,
         "gpu_launches": launches,
         "clocks": clocks,
         "e2e": e2e,
     }
+    if others is not None:
+        line["other_configs"] = others
     if not args.no_cpu_baseline:
-        ms_cpu, desc = cpu_oracle_sample(wl, method, budget_s=20.0)
+        ms_cpu, desc = cpu_oracle_sample(wl, method)
         line["cpu_baseline"] = {"value": ms_cpu, "unit": "ms", "cores": os.cpu_count(),
-                                "kind": "oracle", "sample": desc}
+                                "kind": "oracle", "sample": desc, "extrapolated": True}
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
@@ -511,6 +643,7 @@ def main(argv=None):
     ap.add_argument("--method", default="gram", choices=["gram", "standard"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

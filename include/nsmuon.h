@@ -90,6 +90,19 @@ int nsm_pack(const int32_t* shapes, int n, int64_t align_elems,
 int nsm_assign_owners(const int32_t* shapes, int n, int world, int ns_method, int ns_steps,
                       int32_t* owner_out, int64_t* load_out);
 
+/* Layout query (host-only; for checks and debugging): where muon_step and
+ * muon_orthogonalize keep matrix i's m x m iterates in the workspace.  Every m x m iterate
+ * of the chain (A and B of the standard forms; R, H, Q and T of the gram form) is
+ * symmetric, and the library stores it exactly symmetric.  buf selects one of the m x m
+ * buffers: 0..1 for NSM_NS_STANDARD and NSM_NS_STANDARD_BF16, 0..3 for NSM_NS_GRAM.  On
+ * return, *offset_bytes is the byte offset of matrix i's block in that buffer, *m its
+ * order (m = min(rows, cols)) and *ld its row stride in 16-bit elements (fp16, or bf16
+ * for NSM_NS_STANDARD_BF16).  *m = 0 when matrix i's chain runs in the small-matrix
+ * kernel, whose iterates never leave shared memory.  Returns NSM_ERR_ARG for i or buf out
+ * of range. */
+int nsm_workspace_iterate(const int32_t* shapes, int n, int ns_method, int ns_steps, int i,
+                          int buf, size_t* offset_bytes, int* m, int* ld);
+
 /* Bytes of device workspace muon_step / muon_orthogonalize need for this table and
  * method (independent of offsets).  Returns 0 when the arguments are invalid (the
  * reason is in nsm_last_error()).  Host-only. */
@@ -139,22 +152,25 @@ int muon_orthogonalize(const void* in_bf16, void* out_bf16,
                        void* workspace, size_t workspace_bytes, nsm_stream_t stream);
 
 /* Orthogonalisation that allocates no device memory, for callers that cannot call
- * cudaMalloc: code recording a CUDA graph under a capture mode that forbids allocation,
- * a host framework whose own pool owns every byte of device memory, or a latency-bound
- * loop that cannot afford the device synchronisation an allocation may imply.  It
- * computes what muon_orthogonalize computes, with the same kernels, but keeps its
- * workspace and its launch plan in a 64 MiB array of device memory that is part of the
- * library itself (a file-scope __device__ array: every GPU that loads the library holds
- * it until the process exits).  The pages have no counterpart; this is a convenience of
- * the library.
+ * cudaMalloc: a host framework whose own caching pool owns every byte of device memory
+ * (an allocation outside the pool can fail or fragment it), or a latency-critical loop
+ * that cannot take the device synchronisation an allocation may imply.  It computes what
+ * muon_orthogonalize computes, with the same kernels and bit-identical results, but keeps
+ * its workspace and its launch plan in a 64 MiB array of device memory that is part of
+ * the library itself (a file-scope __device__ array: every GPU that loads the library
+ * holds it until the process exits).  The pages have no counterpart; this is a
+ * convenience of the library.
  *   - Tables whose workspace and plan do not fit in the 64 MiB are rejected with
  *     NSM_ERR_WORKSPACE and nothing is launched (about 8M elements of square matrices
  *     fit; use muon_orthogonalize with a caller workspace for more).
- *   - Every call shares the array and leaves its contents behind; each call rewrites
- *     what it reads, so nothing needs to start at zero.  Calls that overlap on the GPU
- *     (two streams, or two host threads) race on it: order them on one stream.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call outside stream capture.
+ *   - Every call shares the array, which keeps the last call's contents.  Each call
+ *     rewrites the workspace part before reading it, so nothing needs to start at zero;
+ *     the plan part holds the last table's plan, which a call on the same table reuses
+ *     without copying anything.  Calls that overlap on the GPU (two streams, or two host
+ *     threads) race on the array: order them on one stream.
+ *   - The first call on a device (and the first after its context was recreated, e.g.
+ *     by a device reset) looks up the array's device address with cudaGetSymbolAddress,
+ *     with that device current; make that first call before any stream capture.
  * Arguments are those of muon_orthogonalize without the workspace. */
 int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16,
                                const int64_t* offsets, const int32_t* shapes, int n,
@@ -201,6 +217,39 @@ size_t nsm_gemm_scratch_bytes(int M, int N, int flags);
  * NSM_ERR_CUDA if the synchronisation itself reports an error. */
 int nsm_device_status(nsm_stream_t stream, int* status_out);
 
+/* Where the first bounded wait that expired since the status word was last read gave up:
+ * which kernel, which role inside the kernel and which barrier it was waiting on.
+ * Every wait of the library's kernels is bounded (2 s of wall time); on expiry the
+ * kernel records this, stops issuing work, lets its copies and MMAs in flight finish
+ * and returns, so the context stays usable. */
+#define NSM_KERNEL_GEMM       1  /* k_ns_gemm: the 1-CTA grouped GEMM */
+#define NSM_KERNEL_GEMM_PAIR  2  /* k_ns_gemm_pair: the 2-SM grouped GEMM */
+#define NSM_KERNEL_SMALL      3  /* k_ns_small: whole chains of matrices with m <= 128 */
+#define NSM_KERNEL_SELFTEST   4  /* the kernel of nsm_status_selftest */
+#define NSM_ROLE_PRODUCER     1  /* the thread issuing TMA loads */
+#define NSM_ROLE_MMA          2  /* the thread issuing tensor-core MMAs */
+#define NSM_ROLE_EPILOGUE     3  /* the epilogue warps draining TMEM */
+#define NSM_ROLE_TEARDOWN     4  /* the end of the kernel: copies and MMAs still in flight */
+#define NSM_SITE_STAGE_FULL   1  /* the TMA bytes of an operand stage */
+#define NSM_SITE_STAGE_EMPTY  2  /* the MMAs that read an operand stage */
+#define NSM_SITE_ACC_FULL     3  /* the MMAs of a TMEM accumulator */
+#define NSM_SITE_ACC_EMPTY    4  /* the epilogue draining a TMEM accumulator */
+#define NSM_SITE_DRAIN        5  /* the last MMAs before TMEM is freed */
+#define NSM_SITE_SQUARE_FULL  6  /* the MMAs of an m x m product (k_ns_small) */
+#define NSM_SITE_SQUARE_DONE  7  /* the epilogue writing an m x m iterate back (k_ns_small) */
+#define NSM_SITE_XT_FULL      8  /* an X' chunk handed to the MMA thread (k_ns_small) */
+#define NSM_SITE_XT_EMPTY     9  /* the MMA thread releasing an X' chunk (k_ns_small) */
+#define NSM_SITE_STORES_DONE 10  /* the previous pass's X' stores landing (k_ns_small) */
+#define NSM_SITE_SELFTEST    11  /* the self-test's barrier that nothing completes */
+
+/* nsm_device_status with the location: synchronises `stream`, reads and clears the
+ * status word.  *status_out = NSM_OK or NSM_ERR_TIMEOUT; on a timeout *kernel_out,
+ * *role_out and *site_out are NSM_KERNEL_*, NSM_ROLE_* and NSM_SITE_* (0 otherwise; the
+ * self-test kernel reports role 0).
+ * Any of the three location pointers may be NULL. */
+int nsm_device_status_detail(nsm_stream_t stream, int* status_out, int* kernel_out,
+                             int* role_out, int* site_out);
+
 /* Self-test of the bounded-wait status path: launches one CTA on `stream` whose bounded
  * wait on an mbarrier that nothing completes expires after wait_us microseconds (1 to
  * 2,000,000).  The kernel then records the timeout in the device status word, exactly as
@@ -231,6 +280,20 @@ int nsm_timing_reset(void);
 /* Number of kernel launches the last successful muon_step / muon_orthogonalize /
  * adamw_step call made on this host thread. */
 int nsm_last_launch_count(void);
+
+/* Process-wide launch options.  They select between the library's own equivalent paths,
+ * so that the paths can be compared with one another; every value gives the same
+ * results.  A call made after a change uses the new value.  nsm_set_option returns
+ * NSM_ERR_ARG for an unknown option or value; nsm_get_option returns the current value
+ * (NSM_ERR_ARG for an unknown option).  Not to be changed while another host thread is
+ * inside a library call. */
+#define NSM_OPT_PAIR_KERNELS 1  /* 1 (default): 2-SM GEMM kernel where it pays; 0: 1-CTA kernel only */
+#define NSM_OPT_SMALL_KERNEL 2  /* 1 (default): chains of m <= 128 matrices in k_ns_small;
+                                   0: those matrices go through the grouped launches */
+#define NSM_OPT_PDL          3  /* 0 (default): plain stream order; 1: programmatic dependent
+                                   launch (a kernel's launch overlaps its predecessor's tail) */
+int nsm_set_option(int option, int value);
+int nsm_get_option(int option);
 
 #ifdef __cplusplus
 }

@@ -74,6 +74,10 @@ def lib() -> ctypes.CDLL:
     L.nsm_assign_owners.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, _c_i32p, _c_i64p]
     L.nsm_assign_owners.restype = ctypes.c_int
+    L.nsm_workspace_iterate.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.POINTER(ctypes.c_size_t),
+                                        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+    L.nsm_workspace_iterate.restype = ctypes.c_int
     L.muon_workspace_bytes.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     L.muon_workspace_bytes.restype = ctypes.c_size_t
     L.muon_step.argtypes = [_vp, _vp, _vp, _c_i64p, _c_i32p, ctypes.c_int, ctypes.c_float,
@@ -102,6 +106,13 @@ def lib() -> ctypes.CDLL:
     L.nsm_gemm_scratch_bytes.restype = ctypes.c_size_t
     L.nsm_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
     L.nsm_device_status.restype = ctypes.c_int
+    _ip = ctypes.POINTER(ctypes.c_int)
+    L.nsm_device_status_detail.argtypes = [_vp, _ip, _ip, _ip, _ip]
+    L.nsm_device_status_detail.restype = ctypes.c_int
+    L.nsm_set_option.argtypes = [ctypes.c_int, ctypes.c_int]
+    L.nsm_set_option.restype = ctypes.c_int
+    L.nsm_get_option.argtypes = [ctypes.c_int]
+    L.nsm_get_option.restype = ctypes.c_int
     L.nsm_status_selftest.argtypes = [ctypes.c_int, _vp]
     L.nsm_status_selftest.restype = ctypes.c_int
     L.nsm_timing_enable.argtypes = [ctypes.c_int]
@@ -221,6 +232,24 @@ def workspace_bytes(shapes: Sequence[Tuple[int, int]], ns_method=NS_METHOD_DEFAU
     return int(b)
 
 
+def workspace_iterate(shapes: Sequence[Tuple[int, int]], i: int, buf: int, ns_method=NS_METHOD_DEFAULT,
+                      ns_steps: int = NS_STEPS_DEFAULT) -> Tuple[int, int, int]:
+    """(byte offset, m, row stride) of matrix i's m x m buffer `buf` in the workspace;
+    m = 0 when its chain runs in the small-matrix kernel."""
+    s = _shapes_array(shapes)
+    off = ctypes.c_size_t(0)
+    m = ctypes.c_int(0)
+    ld = ctypes.c_int(0)
+    _check(lib().nsm_workspace_iterate(_i32p(s), s.shape[0], method_code(ns_method), int(ns_steps), int(i),
+                                       int(buf), ctypes.byref(off), ctypes.byref(m), ctypes.byref(ld)))
+    return off.value, m.value, ld.value
+
+
+def mm_buffers(ns_method=NS_METHOD_DEFAULT) -> int:
+    """Number of m x m workspace buffers of a method (2 standard forms, 4 gram)."""
+    return 4 if method_code(ns_method) == NS_METHODS["gram"] else 2
+
+
 def _ptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
 
@@ -264,9 +293,11 @@ def muon_orthogonalize(inp, out, offsets, shapes, ns_method=NS_METHOD_DEFAULT,
 
 def muon_orthogonalize_noalloc(inp, out, offsets, shapes, ns_method=NS_METHOD_DEFAULT,
                                ns_steps: int = NS_STEPS_DEFAULT, stream=None) -> None:
-    """muon_orthogonalize without a workspace: for callers that cannot allocate device
-    memory.  Uses 64 MiB of device memory the library itself owns; tables that do not fit
-    raise NsmError(NSM_ERR_WORKSPACE).  Overlapping calls on different streams race."""
+    """muon_orthogonalize without a workspace, for callers that cannot allocate device
+    memory (a framework pool that owns all of it, a loop that cannot take an allocation's
+    synchronisation).  Uses a 64 MiB array of device memory the library itself holds;
+    tables that do not fit raise NsmError(NSM_ERR_WORKSPACE).  Calls that overlap on the
+    GPU race on that array: keep them on one stream."""
     s = _shapes_array(shapes)
     o = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
     _check(lib().muon_orthogonalize_noalloc(_ptr(inp), _ptr(out), _i64p(o), _i32p(s), s.shape[0],
@@ -319,6 +350,31 @@ def device_status(stream=None) -> int:
     return v.value
 
 
+def device_status_detail(stream=None) -> Tuple[int, int, int, int]:
+    """Synchronises the stream; returns (status, kernel, role, site) of the first bounded
+    wait that expired since the last read (status NSM_OK and zeros when none), and clears
+    the record.  kernel/role/site are the NSM_KERNEL_* / NSM_ROLE_* / NSM_SITE_* codes."""
+    v = [ctypes.c_int(0) for _ in range(4)]
+    _check(lib().nsm_device_status_detail(_stream_ptr(stream), *[ctypes.byref(x) for x in v]))
+    return tuple(x.value for x in v)
+
+
+NSM_KERNEL_GEMM, NSM_KERNEL_GEMM_PAIR, NSM_KERNEL_SMALL, NSM_KERNEL_SELFTEST = 1, 2, 3, 4
+NSM_SITE_SELFTEST = 11
+
+OPT_PAIR_KERNELS, OPT_SMALL_KERNEL, OPT_PDL = 1, 2, 3
+
+
+def set_option(option: int, value: int) -> None:
+    """Process-wide choice between the library's equivalent paths (for comparisons):
+    OPT_PAIR_KERNELS, OPT_SMALL_KERNEL (default 1) and OPT_PDL (default 0)."""
+    _check(lib().nsm_set_option(int(option), int(value)))
+
+
+def get_option(option: int) -> int:
+    return _check(lib().nsm_get_option(int(option)))
+
+
 def status_selftest(wait_us: int = 20000, stream=None) -> None:
     """Launches one CTA whose bounded wait expires after wait_us and records a timeout in
     the device status word (read it with device_status)."""
@@ -354,9 +410,13 @@ class MuonAdamW:
     """Hybrid optimizer state over named parameters, on one GPU.
 
     Parameters tagged by :func:`route` go to one packed Muon group (fp32 master params,
-    fp32 momentum, a bf16 gradient buffer); the rest go to one flat AdamW group.  The
-    config keys mirror the pages: ``muon_lr`` / ``adam_lr`` override ``lr``, ``momentum``,
-    ``weight_decay``, ``betas``, ``eps`` and ``ns_method``.
+    fp32 momentum, a bf16 gradient buffer); the rest go to one flat AdamW group (fp32
+    master params and moments, bf16 gradients).  The config keys mirror the pages:
+    ``muon_lr`` / ``adam_lr`` override ``lr``, ``momentum``, ``weight_decay``, ``betas``,
+    ``eps`` and ``ns_method``.  The optimizer owns the fp32 master weights: callers write
+    initial weights and each step's gradients through :meth:`param` / :meth:`grad`, and
+    :meth:`state_dict` carries the master weights with the moments, so that a checkpoint
+    restores the whole state.
     """
 
     def __init__(self, named_shapes: Iterable[Tuple[str, Tuple[int, ...]]], device="cuda",
@@ -371,8 +431,12 @@ class MuonAdamW:
         self.muon_shapes: List[Tuple[int, int]] = []
         self.adam_names: List[str] = []
         self.adam_sizes: List[int] = []
+        self._shape_of: Dict[str, Tuple[int, ...]] = {}
         for name, shape in named:
             shape = tuple(int(d) for d in shape)
+            if name in self._shape_of:
+                raise ValueError(f"parameter {name!r} is listed twice")
+            self._shape_of[name] = shape
             if route(name, len(shape)):
                 cols = 1
                 for d in shape[1:]:
@@ -397,6 +461,12 @@ class MuonAdamW:
         self.nesterov = nesterov
         self.step_count = 0
         dev = torch.device(device)
+        self._muon_index = {n: i for i, n in enumerate(self.muon_names)}
+        self._adam_offset: Dict[str, int] = {}
+        off = 0
+        for n, size in zip(self.adam_names, self.adam_sizes):
+            self._adam_offset[n] = off
+            off += size
         if self.muon_shapes:
             self.offsets, total = pack(self.muon_shapes)
             self.muon_params = torch.zeros(total, dtype=torch.float32, device=dev)
@@ -410,6 +480,27 @@ class MuonAdamW:
         self.adam_exp_avg_sq = torch.zeros(n_adam, dtype=torch.float32, device=dev)
         self.adam_grads = torch.zeros(n_adam, dtype=torch.bfloat16, device=dev)
 
+    def _view(self, name: str, muon_buf, adam_buf):
+        shape = self._shape_of[name]
+        if name in self._muon_index:
+            i = self._muon_index[name]
+            r, c = self.muon_shapes[i]
+            o = int(self.offsets[i])
+            return muon_buf[o:o + r * c].view(shape)
+        o = self._adam_offset[name]
+        size = 1
+        for d in shape:
+            size *= d
+        return adam_buf[o:o + size].view(shape)
+
+    def param(self, name: str):
+        """The fp32 master weight of a parameter (a view into its group's buffer)."""
+        return self._view(name, getattr(self, "muon_params", None), self.adam_params)
+
+    def grad(self, name: str):
+        """The bf16 gradient slot of a parameter (a view; write each step's gradient here)."""
+        return self._view(name, getattr(self, "muon_grads", None), self.adam_grads)
+
     def step(self, stream=None) -> None:
         self.step_count += 1
         if self.muon_shapes:
@@ -422,16 +513,31 @@ class MuonAdamW:
                        self.step_count, stream)
 
     def state_dict(self) -> Dict[str, object]:
-        """Optimizer state as plain tensors (the caller saves and restores them)."""
+        """The whole optimizer state as plain tensors (the caller saves and restores them):
+        the step count, both groups' fp32 master weights, the Muon momentum and the AdamW
+        moments, with the names and shapes they were packed from."""
         d: Dict[str, object] = {"step": self.step_count,
-                                "adam_exp_avg": self.adam_exp_avg, "adam_exp_avg_sq": self.adam_exp_avg_sq}
+                                "muon_names": list(self.muon_names),
+                                "muon_shapes": list(self.muon_shapes),
+                                "adam_names": list(self.adam_names),
+                                "adam_sizes": list(self.adam_sizes),
+                                "adam_params": self.adam_params,
+                                "adam_exp_avg": self.adam_exp_avg,
+                                "adam_exp_avg_sq": self.adam_exp_avg_sq}
         if self.muon_shapes:
+            d["muon_params"] = self.muon_params
             d["muon_momentum"] = self.muon_momentum
         return d
 
     def load_state_dict(self, d: Dict[str, object]) -> None:
+        if (list(d["muon_names"]) != self.muon_names or list(d["adam_names"]) != self.adam_names
+                or [tuple(s) for s in d["muon_shapes"]] != self.muon_shapes
+                or list(d["adam_sizes"]) != self.adam_sizes):
+            raise ValueError("state_dict was saved for other parameters")
         self.step_count = int(d["step"])
+        self.adam_params.copy_(d["adam_params"])
         self.adam_exp_avg.copy_(d["adam_exp_avg"])
         self.adam_exp_avg_sq.copy_(d["adam_exp_avg_sq"])
         if self.muon_shapes:
+            self.muon_params.copy_(d["muon_params"])
             self.muon_momentum.copy_(d["muon_momentum"])

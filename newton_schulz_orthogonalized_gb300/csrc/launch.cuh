@@ -3,7 +3,7 @@
 // Every kernel of the library calls grid_dependency_sync() before it touches memory that
 // an earlier kernel of the stream writes (and before nothing else: barrier setup and
 // TMEM allocation may run early), then release_dependents().  Launched in plain stream
-// order (the default) both return at once.  With NSM_PDL=1 in the environment, kernels
+// order (the default) both return at once.  With the NSM_OPT_PDL option set, kernels
 // are launched with programmatic stream serialisation: the next kernel's launch and
 // prologue then overlap the tail of the current one, and its own grid_dependency_sync()
 // waits until this grid has completed and its writes are visible.  Measured on one
@@ -13,7 +13,7 @@
 
 #include <cuda_runtime.h>
 
-#include <cstdlib>
+#include "nsm_internal.h"
 
 namespace nsm {
 
@@ -25,13 +25,7 @@ __device__ __forceinline__ void release_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-inline bool pdl_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("NSM_PDL");
-    return v && v[0] == '1';
-  }();
-  return on;
-}
+inline bool pdl_enabled() { return option_value(NSM_OPT_PDL) != 0; }
 
 // `overlap` = false launches in plain stream order (the kernel's own dependency sync then
 // returns at once).

@@ -16,8 +16,7 @@
 // 128 or 256 rows) into a ring of stages, warp 1 issues the MMAs (the leader CTA's, in the
 // pair kernel) into two TMEM accumulators of 256 fp32 columns, warps 2-5 drain TMEM with
 // tcgen05.ld, apply the fused epilogue  out = alpha*acc + beta*aux + diag*I  and store
-// fp16/bf16 32 x 32 blocks through shared memory with TMA stores.  With ApplyArgs, the
-// product that forms O applies the optimizer step instead of storing O.
+// fp16/bf16 32 x 32 blocks through shared memory with TMA stores.
 // A group flagged symmetric computes only the tiles that touch the upper triangle, stores
 // the blocks on and above the diagonal and mirrors the upper ones.
 //
@@ -31,7 +30,6 @@
 
 #include <atomic>
 
-#include "apply.cuh"
 #include "launch.cuh"
 #include "nsm_internal.h"
 #include "ptx.cuh"
@@ -59,7 +57,7 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 constexpr int kPanel = 2;                 // column tiles per raster panel
 constexpr int EPI_WARPS = 4;
 // Whether the grouped launches may overlap their launch with the previous kernel when
-// programmatic dependent launch is on (NSM_PDL=1).
+// programmatic dependent launch is on (the NSM_OPT_PDL option).
 constexpr bool kOverlapGemmLaunch = true;
 constexpr int EPI_STAGE_BYTES = EPI_WARPS * 8192;   // per epilogue warp: 2 slots of 2 x 2 KB staged blocks
 
@@ -151,10 +149,13 @@ struct Elem<true> {
   __device__ static __forceinline__ float bits_to_f(uint16_t v) { return __half2float(__ushort_as_half(v)); }
 };
 
+// A bounded wait expired: the other roles of the CTA give up at their next wait, and the
+// status word records where (kernel, role, barrier) unless an earlier expiry is there.
 template <int STAGES>
-__device__ __forceinline__ void signal_timeout(Ctrl<STAGES>* ctrl, int* status) {
+__device__ __forceinline__ void signal_timeout(Ctrl<STAGES>* ctrl, int* status, int kernel, int role,
+                                               int site) {
   ctrl->abort = 1;
-  atomicExch(status, kDevTimeout);
+  record_timeout(status, kernel, role, site);
 }
 
 // Epilogue of one accumulator: this warp's 32 rows (rows rb .. rb+31 of the matrix,
@@ -216,56 +217,6 @@ __device__ __forceinline__ void chunk_values(const uint32_t (&r)[32], const type
     for (int j = 0; j < 32; ++j) {
       if (d == j) v[j] += diag;
     }
-  }
-}
-
-// Epilogue of the product that forms O when the step is applied ("DeepSpeed 集成 Muon
-// 优化器实战" §核心算子: p <- p (1 - lr wd) - lr sqrt(max(1, rows/cols)) O): out = alpha acc +
-// beta aux + diag I is rounded to O's storage format and applied to the parameters
-// instead of being stored.  Each lane updates one natural column of a 32 x 32 block of
-// the parameter matrix, so every load and store of the warp is one 128-byte access.
-// A tall matrix sits transposed in its class, so lane l's class row already is natural
-// column l; for a wide one the block of O is transposed through shared memory first.
-// The parameters of block c + 1 are loaded before block c is applied.
-template <bool FP16, bool HAS_AUX>
-__device__ __forceinline__ void epilogue_apply_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
-                                                    uint32_t t_row, uint32_t* xw, int lane, float alpha,
-                                                    float beta, float diag, const ApplyArgs& ap) {
-  using E = Elem<FP16>;
-  using T = typename E::T;
-  if (rb >= G.M) return;  // the warp's rows are past the matrix
-  const MatInfo& mt = ap.mats[__ldg(G.mat_index + b)];
-  const int row = rb + lane;
-  const bool row_ok = row < G.M;
-  const int nchunks = (n_len + 31) >> 5;
-  const T* aux_row = nullptr;
-  if (HAS_AUX) {
-    aux_row = reinterpret_cast<const T*>(G.aux) + static_cast<int64_t>(b) * G.aux_bstride +
-              static_cast<int64_t>(row) * G.ld_aux + n0;
-  }
-  float cur[32], nxt[32];
-  apply_block_load(ap, mt, apply_block_at(mt, rb, n0, G.M, n0 + n_len), lane, cur);
-#pragma unroll 1
-  for (int c = 0; c < nchunks; ++c) {
-    const int col0 = c * 32;
-    const ApplyBlock blk = apply_block_at(mt, rb, n0 + col0, G.M, n0 + n_len);
-    if (c + 1 < nchunks) apply_block_load(ap, mt, apply_block_at(mt, rb, n0 + col0 + 32, G.M, n0 + n_len), lane, nxt);
-    uint32_t r[32];
-    __syncwarp();  // tcgen05.ld is warp-aligned: all 32 lanes arrive together
-    ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(col0), r);
-    ptx::tmem_ld_wait();
-    uint32_t o[16];  // O as stored, packed pairs
-    {
-      float v[32];
-      chunk_values<FP16, HAS_AUX>(r, aux_row, row_ok, col0, col0 + 32 <= n_len, n_len, row - (n0 + col0), alpha,
-                                  beta, diag, v);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) o[i] = pack2<FP16>(v[2 * i], v[2 * i + 1]);
-    }
-    apply_block_columns(mt, o, xw, lane);
-    apply_block_store<FP16>(ap, mt, blk, lane, o, cur);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
   }
 }
 
@@ -476,7 +427,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
 template <bool B_MN, bool FP16, bool HAS_AUX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ns_gemm(const GemmGroup* __restrict__ groups, int ng, int64_t total_tiles, float alpha,
-              float beta, float diag, int* status, ApplyArgs ap) {
+              float beta, float diag, int* status) {
   constexpr int STAGES = S1_STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -543,7 +494,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait_bounded(bar(&ctrl->empty[stage]), phase ^ 1u, abort_flag,
                                       WAIT_LIMIT_NS)) {
-            signal_timeout(ctrl, status);
+            signal_timeout(ctrl, status, NSM_KERNEL_GEMM, NSM_ROLE_PRODUCER, NSM_SITE_STAGE_EMPTY);
             ok = false;
             break;
           }
@@ -597,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
         if (!ptx::mbar_wait_bounded(bar(&ctrl->acc_empty[acc]), acc_phase ^ 1u, abort_flag,
                                     WAIT_LIMIT_NS)) {
-          signal_timeout(ctrl, status);
+          signal_timeout(ctrl, status, NSM_KERNEL_GEMM, NSM_ROLE_MMA, NSM_SITE_ACC_EMPTY);
           ok = false;
           break;
         }
@@ -607,7 +558,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait_bounded(bar(&ctrl->full[stage]), phase, abort_flag,
                                       WAIT_LIMIT_NS)) {
-            signal_timeout(ctrl, status);
+            signal_timeout(ctrl, status, NSM_KERNEL_GEMM, NSM_ROLE_MMA, NSM_SITE_STAGE_FULL);
             ok = false;
             break;
           }
@@ -633,7 +584,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // No MMA may still write TMEM when the block frees it.
       ptx::mma_commit(bar(&ctrl->drain));
       if (!ptx::mbar_wait_bounded(bar(&ctrl->drain), 0u, never_flag, WAIT_LIMIT_NS)) {
-        signal_timeout(ctrl, status);
+        signal_timeout(ctrl, status, NSM_KERNEL_GEMM, NSM_ROLE_TEARDOWN, NSM_SITE_DRAIN);
       }
     }
     __syncwarp();
@@ -653,24 +604,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) {
         ok = ptx::mbar_wait_bounded(bar(&ctrl->acc_full[acc]), acc_phase, abort_flag,
                                     WAIT_LIMIT_NS);
-        if (!ok) signal_timeout(ctrl, status);
+        if (!ok) signal_timeout(ctrl, status, NSM_KERNEL_GEMM, NSM_ROLE_EPILOGUE, NSM_SITE_ACC_FULL);
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-      if (ap.params) {
-        epilogue_apply_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                           t_row, stage_words, lane, alpha, beta, diag, ap);
+      if (G.map_out) {
+        epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
+                                     t_row, stage, nst, lane, alpha, beta, diag);
       } else {
-        if (G.map_out) {
-          epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                       t_row, stage, nst, lane, alpha, beta, diag);
-        } else {
-          epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                              t_row, stage_words, lane, alpha, beta, diag);
-        }
+        epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
+                                            t_row, stage_words, lane, alpha, beta, diag);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -709,7 +655,7 @@ __device__ __forceinline__ int boxes_in(int start, int limit) {
 template <bool B_MN, bool FP16, bool HAS_AUX>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_ns_gemm_pair(const GemmGroup* __restrict__ groups, int ng, int64_t total_tiles, float alpha,
-                   float beta, float diag, int* status, ApplyArgs ap) {
+                   float beta, float diag, int* status) {
   constexpr int STAGES = S2_STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -788,7 +734,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait_bounded(bar(&ctrl->empty[stage]), phase ^ 1u, abort_flag,
                                       WAIT_LIMIT_NS)) {
-            signal_timeout(ctrl, status);
+            signal_timeout(ctrl, status, NSM_KERNEL_GEMM_PAIR, NSM_ROLE_PRODUCER, NSM_SITE_STAGE_EMPTY);
             ok = false;
             break;
           }
@@ -865,7 +811,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
         if (!ptx::mbar_wait_bounded(bar(&ctrl->acc_empty[acc]), acc_phase ^ 1u, abort_flag,
                                     WAIT_LIMIT_NS)) {
-          signal_timeout(ctrl, status);
+          signal_timeout(ctrl, status, NSM_KERNEL_GEMM_PAIR, NSM_ROLE_MMA, NSM_SITE_ACC_EMPTY);
           ok = false;
           break;
         }
@@ -874,7 +820,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait_bounded(bar(&ctrl->full[stage]), phase, abort_flag,
                                       WAIT_LIMIT_NS)) {
-            signal_timeout(ctrl, status);
+            signal_timeout(ctrl, status, NSM_KERNEL_GEMM_PAIR, NSM_ROLE_MMA, NSM_SITE_STAGE_FULL);
             ok = false;
             break;
           }
@@ -920,7 +866,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) {
         ok = ptx::mbar_wait_bounded(bar(&ctrl->acc_full[acc]), acc_phase, abort_flag,
                                     WAIT_LIMIT_NS);
-        if (!ok) signal_timeout(ctrl, status);
+        if (!ok) signal_timeout(ctrl, status, NSM_KERNEL_GEMM_PAIR, NSM_ROLE_EPILOGUE, NSM_SITE_ACC_FULL);
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
@@ -928,17 +874,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
       const int rb = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
-      if (ap.params) {
-        epilogue_apply_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage_words, lane,
-                                           alpha, beta, diag, ap);
+      if (G.map_out) {
+        epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage, nst, lane,
+                                     alpha, beta, diag);
       } else {
-        if (G.map_out) {
-          epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage, nst, lane,
-                                       alpha, beta, diag);
-        } else {
-          epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage_words,
-                                              lane, alpha, beta, diag);
-        }
+        epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage_words,
+                                            lane, alpha, beta, diag);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -952,7 +893,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   // no MMA of the pair may still write this CTA's TMEM when it is freed
   if (threadIdx.x == 0) {
     if (!ptx::mbar_wait_bounded(bar(&ctrl->drain), 0u, never_flag, WAIT_LIMIT_NS)) {
-      signal_timeout(ctrl, status);
+      signal_timeout(ctrl, status, NSM_KERNEL_GEMM_PAIR, NSM_ROLE_TEARDOWN, NSM_SITE_DRAIN);
     }
   }
   ptx::tc_fence_before();
@@ -982,7 +923,7 @@ cudaError_t set_smem_once(K kernel, size_t bytes, std::atomic<uint64_t>& done) {
 }
 
 template <bool B_MN, bool FP16, bool HAS_AUX>
-cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream, const ApplyArgs& ap) {
+cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream) {
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   if (l.pair) {
@@ -1020,7 +961,7 @@ cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream, 
     if (pairs <= 0) return cudaSuccess;
     if (const cudaError_t e_launch = launch_ordered(kOverlapGemmLaunch, k_ns_gemm_pair<B_MN, FP16, HAS_AUX>, dim3(static_cast<unsigned>(2 * pairs)),
                                                 dim3(NUM_THREADS), S2_SMEM, stream, l.groups, l.num_groups,
-                                                l.total_tiles, l.alpha, l.beta, l.diag, status, ap))
+                                                l.total_tiles, l.alpha, l.beta, l.diag, status))
       return e_launch;
     return cudaGetLastError();
   }
@@ -1031,25 +972,24 @@ cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream, 
   if (grid <= 0) return cudaSuccess;
   if (const cudaError_t e_launch = launch_ordered(kOverlapGemmLaunch, k_ns_gemm<B_MN, FP16, HAS_AUX>, dim3(static_cast<unsigned>(grid)),
                                               dim3(NUM_THREADS), S1_SMEM, stream, l.groups, l.num_groups, l.total_tiles,
-                                              l.alpha, l.beta, l.diag, status, ap))
+                                              l.alpha, l.beta, l.diag, status))
     return e_launch;
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream, const ApplyArgs* apply) {
-  const ApplyArgs ap = apply ? *apply : ApplyArgs{nullptr, nullptr, nullptr, 0.f, 1.f};
+cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream) {
   const int key = (l.b_mn_major ? 4 : 0) | (l.fp16 ? 2 : 0) | (l.has_aux ? 1 : 0);
   switch (key) {
-    case 0: return launch_typed<false, false, false>(l, num_sms, stream, ap);
-    case 1: return launch_typed<false, false, true>(l, num_sms, stream, ap);
-    case 2: return launch_typed<false, true, false>(l, num_sms, stream, ap);
-    case 3: return launch_typed<false, true, true>(l, num_sms, stream, ap);
-    case 4: return launch_typed<true, false, false>(l, num_sms, stream, ap);
-    case 5: return launch_typed<true, false, true>(l, num_sms, stream, ap);
-    case 6: return launch_typed<true, true, false>(l, num_sms, stream, ap);
-    default: return launch_typed<true, true, true>(l, num_sms, stream, ap);
+    case 0: return launch_typed<false, false, false>(l, num_sms, stream);
+    case 1: return launch_typed<false, false, true>(l, num_sms, stream);
+    case 2: return launch_typed<false, true, false>(l, num_sms, stream);
+    case 3: return launch_typed<false, true, true>(l, num_sms, stream);
+    case 4: return launch_typed<true, false, false>(l, num_sms, stream);
+    case 5: return launch_typed<true, false, true>(l, num_sms, stream);
+    case 6: return launch_typed<true, true, false>(l, num_sms, stream);
+    default: return launch_typed<true, true, true>(l, num_sms, stream);
   }
 }
 

@@ -118,13 +118,15 @@ struct Roles {
 
   __device__ uint32_t bar(uint64_t* b) const { return ptx::smem_u32(b); }
   __device__ uint32_t square(int i) const { return squares + static_cast<uint32_t>(i * kSquare); }
-  __device__ bool wait(uint64_t* b, uint32_t parity) const {
-    return ptx::mbar_wait_bounded(bar(b), parity, abort_flag, kWaitNs);
-  }
-  __device__ void give_up() const {
+  // Bounded wait; on expiry the status word records this role and barrier (unless an
+  // earlier expiry is there) and the other roles give up at their next wait.
+  __device__ bool wait(uint64_t* b, uint32_t parity, int role, int site) const {
+    if (ptx::mbar_wait_bounded(bar(b), parity, abort_flag, kWaitNs)) return true;
+    if (!*abort_flag) record_timeout(status, NSM_KERNEL_SMALL, role, site);
     ctrl->abort = 1;
-    atomicExch(status, kDevTimeout);
+    return false;
   }
+  __device__ void give_up() const { ctrl->abort = 1; }
 };
 
 struct RingPos {
@@ -153,14 +155,14 @@ __device__ bool produce(const Roles& R, const SmallJob* __restrict__ jobs, int n
       if (op.kind == kSmallPass) {
         // the source was stored by the previous pass of this matrix: wait until it landed
         if (!first_pass) {
-          if (!R.wait(&R.ctrl->stores_done, stores_seen & 1u)) return false;
+          if (!R.wait(&R.ctrl->stores_done, stores_seen & 1u, NSM_ROLE_PRODUCER, NSM_SITE_STORES_DONE)) return false;
           ++stores_seen;
         }
         first_pass = false;
       }
       const CUtensorMap* map = job.map_x[op.src_x];
       for (int c = 0; c < nck; ++c) {
-        if (!R.wait(&R.ctrl->empty[rp.stage], rp.phase ^ 1u)) return false;
+        if (!R.wait(&R.ctrl->empty[rp.stage], rp.phase ^ 1u, NSM_ROLE_PRODUCER, NSM_SITE_STAGE_EMPTY)) return false;
         const uint32_t fb = R.bar(&R.ctrl->full[rp.stage]);
         ptx::mbar_arrive_expect_tx(fb, kSlot);
         const uint32_t slot = R.ring + static_cast<uint32_t>(rp.stage * kSlot);
@@ -188,14 +190,14 @@ __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict_
   // the rounded result is in shared memory
   auto finish_square = [&]() -> bool {
     ptx::mma_commit(R.bar(&R.ctrl->sq_full));
-    if (!R.wait(&R.ctrl->sq_done, sq_cnt & 1u)) return false;
+    if (!R.wait(&R.ctrl->sq_done, sq_cnt & 1u, NSM_ROLE_MMA, NSM_SITE_SQUARE_DONE)) return false;
     ++sq_cnt;
     ptx::tc_fence_after();
     return true;
   };
   // X' X'^T += chunk of X' in shared-memory slot `slot`
   auto accumulate_panel = [&](int c, uint32_t slot) -> bool {
-    if (!R.wait(&R.ctrl->xt_full[slot], hand[slot] & 1u)) return false;
+    if (!R.wait(&R.ctrl->xt_full[slot], hand[slot] & 1u, NSM_ROLE_MMA, NSM_SITE_XT_FULL)) return false;
     ptx::tc_fence_after();
     const uint32_t base = R.xt + slot * kSlot;
 #pragma unroll
@@ -214,7 +216,7 @@ __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict_
       const SmallOp op = ops[o];
       if (op.kind == kSmallGram) {
         for (int c = 0; c < nck; ++c) {
-          if (!R.wait(&R.ctrl->full[rp.stage], rp.phase)) return false;
+          if (!R.wait(&R.ctrl->full[rp.stage], rp.phase, NSM_ROLE_MMA, NSM_SITE_STAGE_FULL)) return false;
           ptx::tc_fence_after();
           const uint32_t base = R.ring + static_cast<uint32_t>(rp.stage * kSlot);
 #pragma unroll
@@ -239,9 +241,9 @@ __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict_
         const uint32_t xs0 = xs;
         for (int c = 0; c < nck; ++c) {
           const uint32_t acc = acc_cnt & 1u;
-          if (!R.wait(&R.ctrl->acc_empty[acc], ((acc_cnt >> 1) & 1u) ^ 1u)) return false;
+          if (!R.wait(&R.ctrl->acc_empty[acc], ((acc_cnt >> 1) & 1u) ^ 1u, NSM_ROLE_MMA, NSM_SITE_ACC_EMPTY)) return false;
           ptx::tc_fence_after();
-          if (!R.wait(&R.ctrl->full[rp.stage], rp.phase)) return false;
+          if (!R.wait(&R.ctrl->full[rp.stage], rp.phase, NSM_ROLE_MMA, NSM_SITE_STAGE_FULL)) return false;
           ptx::tc_fence_after();
           // B = the chunk read K x N (N contiguous): two 64-column blocks kPanel apart
           const uint32_t chunk = R.ring + static_cast<uint32_t>(rp.stage * kSlot);
@@ -292,15 +294,14 @@ struct Epilogue {
   }
 
   // Every epilogue thread waits; all give up together if any of them timed out.
-  __device__ bool wait_all(uint64_t* b, uint32_t parity) {
-    const bool ok = R.wait(b, parity);
-    if (!ok) R.give_up();
+  __device__ bool wait_all(uint64_t* b, uint32_t parity, int site) {
+    const bool ok = R.wait(b, parity, NSM_ROLE_EPILOGUE, site);
     return ptx::named_all(kEpiBar, kEpiThreads, ok);
   }
 
   // S[dst] = alpha acc + beta S[aux] + diag I (rows < m on the diagonal)
   __device__ bool square(int dst, int aux, float alpha, float beta, float diag, int m) {
-    if (!wait_all(&R.ctrl->sq_full, sq_cnt & 1u)) return false;
+    if (!wait_all(&R.ctrl->sq_full, sq_cnt & 1u, NSM_SITE_SQUARE_FULL)) return false;
     ++sq_cnt;
     ptx::tc_fence_after();
     const uint32_t d = R.square(dst);
@@ -379,9 +380,8 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
       const int rb = ep.row - ep.lane;  // the warp's first row
       for (int c = 0; c < nck; ++c) {
         const uint32_t acc = acc_cnt & 1u;
-        bool ok = R.wait(&R.ctrl->acc_full[acc], (acc_cnt >> 1) & 1u);
-        if (ok && reads_x) ok = R.wait(&R.ctrl->full[rp.stage], rp.phase);
-        if (!ok) R.give_up();
+        bool ok = R.wait(&R.ctrl->acc_full[acc], (acc_cnt >> 1) & 1u, NSM_ROLE_EPILOGUE, NSM_SITE_ACC_FULL);
+        if (ok && reads_x) ok = R.wait(&R.ctrl->full[rp.stage], rp.phase, NSM_ROLE_EPILOGUE, NSM_SITE_STAGE_FULL);
         if (!ptx::named_all(kEpiBar, kEpiThreads, ok)) return false;
         ptx::tc_fence_after();
         const int stage = rp.stage;
@@ -392,8 +392,8 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
           if (ep.leader) ptx::bulk_wait_group_read<1>();
           bool free_ok = true;
           if (pend[slot] >= 0) {
-            free_ok = R.wait(&R.ctrl->xt_empty[slot], static_cast<uint32_t>(pend[slot]));
-            if (!free_ok) R.give_up();
+            free_ok = R.wait(&R.ctrl->xt_empty[slot], static_cast<uint32_t>(pend[slot]), NSM_ROLE_EPILOGUE,
+                             NSM_SITE_XT_EMPTY);
             pend[slot] = -1;
           }
           if (!ptx::named_all(kEpiBar, kEpiThreads, free_ok)) return false;
@@ -569,7 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!issue<FP16>(R, tmem, jobs, njobs, ops, nops, ap.params == nullptr)) R.give_up();
       // no MMA may still write TMEM when the block frees it
       ptx::mma_commit(R.bar(&ctrl->drain));
-      if (!ptx::mbar_wait_bounded(R.bar(&ctrl->drain), 0u, R.never_flag, kWaitNs)) R.give_up();
+      if (!ptx::mbar_wait_bounded(R.bar(&ctrl->drain), 0u, R.never_flag, kWaitNs)) {
+        record_timeout(R.status, NSM_KERNEL_SMALL, NSM_ROLE_TEARDOWN, NSM_SITE_DRAIN);
+        R.give_up();
+      }
     }
     __syncwarp();
   } else {

@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <list>
+#include <atomic>
 #include <map>
 #include <memory>
 #include <mutex>
@@ -250,38 +251,13 @@ struct Plan {
   }
 };
 
-// The grouped launches leave the step's decay and update to a separate pass; with
-// NSM_FUSED_APPLY=1 in the environment the epilogue of the chain's last product applies
-// them instead (both give the same bits, and the same step time: the epilogue's
-// parameter traffic costs the GEMM about what the separate pass costs).  The small-
-// matrix kernel always applies its matrices in its final pass.
-bool fused_apply_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("NSM_FUSED_APPLY");
-    return v && v[0] == '1';
-  }();
-  return on;
-}
+// Process-wide launch options (nsm_set_option).  The 2-SM kernel is used where it pays
+// and matrices with m <= 128 run in the small-matrix kernel unless an option says
+// otherwise (for comparisons); programmatic dependent launch is off by default.
+std::atomic<int> g_opt_pair{1}, g_opt_small{1}, g_opt_pdl{0};
 
-// The 2-SM kernel is used where it pays; NSM_PAIR_KERNELS=0 in the environment keeps every
-// launch on the 1-CTA kernel (for comparisons).
-bool pair_kernels_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("NSM_PAIR_KERNELS");
-    return !(v && v[0] == '0');
-  }();
-  return on;
-}
-
-// Matrices with m <= 128 run in the small-matrix kernel; NSM_SMALL_KERNEL=0 in the
-// environment sends them through the grouped launches instead (for comparisons).
-bool small_kernel_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("NSM_SMALL_KERNEL");
-    return !(v && v[0] == '0');
-  }();
-  return on;
-}
+bool pair_kernels_enabled() { return g_opt_pair.load() != 0; }
+bool small_kernel_enabled() { return g_opt_small.load() != 0; }
 
 // Flops of one matrix's Newton-Schulz chain (2 m n k per product, as if no tile were
 // skipped): standard 4 m^2 n + 2 m^3 per step; gram counts its m x n products (X X^T,
@@ -588,13 +564,10 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     }
   }
 
-  // Device metadata: MatInfo[n] | matrix of each (class, batch) | tensor maps [nclass][nbuf] |
-  // GemmGroup arrays | tile lists | small-matrix jobs | small-matrix operations.
+  // Device metadata: MatInfo[n] | tensor maps [nclass][nbuf] | GemmGroup arrays | tile
+  // lists | small-matrix jobs | small-matrix operations.
   const size_t mats_bytes = align_up(sizeof(MatInfo) * n, 128);
-  std::vector<int32_t> class_first(nclass + 1, 0);
-  for (int c = 0; c < nclass; ++c) class_first[c + 1] = class_first[c] + L.classes[c].count;
-  const size_t matidx_off = mats_bytes;
-  const size_t maps_off = matidx_off + align_up(sizeof(int32_t) * size_t(n), 128);
+  const size_t maps_off = mats_bytes;
   constexpr int kBoxKinds = 4;  // load boxes of 64, 128, 256 rows; 32 x 32 store boxes
   const size_t maps_bytes = align_up(sizeof(CUtensorMap) * size_t(nclass) * nbuf * kBoxKinds, 128);
   const size_t groups_off = maps_off + maps_bytes;
@@ -625,8 +598,6 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     if (small[L.cls_of[i]]) mi.flags |= kMatInChain;
     hm[i] = mi;
   }
-  int32_t* hmatidx = reinterpret_cast<int32_t*>(host.data() + matidx_off);
-  for (int i = 0; i < n; ++i) hmatidx[class_first[L.cls_of[i]] + L.batch_of[i]] = i;
 
   cudaError_t e = cudaSuccess;
   if (sink) {
@@ -745,7 +716,6 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       g.tiles_m = (g.M + tile_m - 1) / tile_m;
       g.tiles_n = (g.N + 255) / 256;
       g.tile_begin = tiles;
-      g.mat_index = reinterpret_cast<const int32_t*>(dbase + matidx_off) + class_first[c];
       canonical += 2.0 * g.count * double(g.M) * g.N * g.K;
       if (st.sym) {
         g.sym = 1;
@@ -802,7 +772,9 @@ std::string plan_key(int device, const int32_t* shapes, const int64_t* offsets, 
   std::string k;
   k.reserve(64 + size_t(n) * 16);
   auto put = [&](const void* p, size_t b) { k.append(static_cast<const char*>(p), b); };
+  const int opts = (pair_kernels_enabled() ? 1 : 0) | (small_kernel_enabled() ? 2 : 0);
   put(&device, sizeof(device));
+  put(&opts, sizeof(opts));
   put(&method, sizeof(method));
   put(&steps, sizeof(steps));
   put(&n, sizeof(n));
@@ -956,9 +928,8 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need) {
 
 // Launches the chain: the small-matrix kernel, then the grouped GEMMs.  With
 // `apply_small`, the small-matrix kernel applies the step to its matrices instead of
-// storing O; with `apply_last`, so does the grouped launch that computes O.
-int run_chain(Plan& P, cudaStream_t stream, int* launches, const ApplyArgs* apply_small = nullptr,
-              const ApplyArgs* apply_last = nullptr) {
+// storing O.
+int run_chain(Plan& P, cudaStream_t stream, int* launches, const ApplyArgs* apply_small = nullptr) {
   int num_sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, P.device);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
@@ -971,9 +942,8 @@ int run_chain(Plan& P, cudaStream_t stream, int* launches, const ApplyArgs* appl
   }
   for (size_t k = 0; k < P.launches.size(); ++k) {
     const GemmLaunch& l = P.launches[k];
-    const bool last = k + 1 == P.launches.size();
     TimedLaunch t(stream, NSM_KIND_GEMM, l.flops);
-    e = launch_gemm(l, num_sms, stream, last ? apply_last : nullptr);
+    e = launch_gemm(l, num_sms, stream);
     if (e != cudaSuccess) return fail_cuda(e, "Newton-Schulz GEMM launch");
     ++*launches;
   }
@@ -988,28 +958,93 @@ int run_chain(Plan& P, cudaStream_t stream, int* launches, const ApplyArgs* appl
 constexpr size_t kNoAllocBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-// Device address of g_noalloc_scratch on the current device, looked up once per device.
-char* noalloc_scratch(int device, int* rc) {
-  static std::mutex mu;
-  static char* ptr[64] = {nullptr};
+// What the allocation-free path keeps per device: the context it belongs to, the array's
+// device address in that context, and the plan whose metadata the array holds now (with
+// the key it was built for), so that a call on the same table uploads nothing.
+struct NoAllocState {
+  unsigned long long ctx_id = 0;
+  char* scratch = nullptr;
+  std::string key;
+  std::unique_ptr<Plan> plan;
+};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the context current on this thread for `device` (a context created after
+// a device reset gets a new id, so nothing looked up in the old one is used again).
+int current_context_id(int device, unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return fail(NSM_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId are unavailable");
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return fail(NSM_ERR_CUDA, "cuCtxGetCurrent failed");
+  if (!ctx) {
+    // this thread has not used the device yet: make its primary context current
+    const cudaError_t e = cudaSetDevice(device);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaSetDevice");
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return fail(NSM_ERR_CUDA, "no current CUDA context");
+  }
+  if (get_id(ctx, id) != CUDA_SUCCESS) return fail(NSM_ERR_CUDA, "cuCtxGetId failed");
+  return NSM_OK;
+}
+
+// The state of the current device, with the array's device address looked up (once per
+// device and context, with that device current).  Called with noalloc_mutex() held.
+NoAllocState* noalloc_state(int device, int* rc) {
+  static NoAllocState states[64];
   if (device < 0 || device >= 64) {
     *rc = fail(NSM_ERR_CUDA, "device ordinal %d out of range", device);
     return nullptr;
   }
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptr[device]) {
+  unsigned long long id = 0;
+  *rc = current_context_id(device, &id);
+  if (*rc != NSM_OK) return nullptr;
+  NoAllocState& st = states[device];
+  if (!st.scratch || st.ctx_id != id) {
+    st.plan.reset();
+    st.key.clear();
+    st.scratch = nullptr;
     void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) {
       *rc = fail_cuda(e, "cudaGetSymbolAddress(allocation-free scratch)");
       return nullptr;
     }
-    ptr[device] = static_cast<char*>(p);
+    st.scratch = static_cast<char*>(p);
+    st.ctx_id = id;
   }
-  return ptr[device];
+  return &st;
+}
+
+std::mutex& noalloc_mutex() {
+  static std::mutex* mu = new std::mutex();
+  return *mu;
 }
 
 }  // namespace
+
+int option_value(int option) {
+  switch (option) {
+    case NSM_OPT_PAIR_KERNELS: return g_opt_pair.load();
+    case NSM_OPT_SMALL_KERNEL: return g_opt_small.load();
+    case NSM_OPT_PDL: return g_opt_pdl.load();
+    default: return -1;
+  }
+}
+
 }  // namespace nsm
 
 using namespace nsm;
@@ -1078,6 +1113,24 @@ int nsm_assign_owners(const int32_t* shapes, int n, int world, int ns_method, in
     load[best] += cost[i];
   }
   if (load_out) std::copy(load.begin(), load.end(), load_out);
+  return NSM_OK;
+}
+
+int nsm_workspace_iterate(const int32_t* shapes, int n, int ns_method, int ns_steps, int i, int buf,
+                          size_t* offset_bytes, int* m_out, int* ld_out) {
+  if (!offset_bytes || !m_out || !ld_out) return fail(NSM_ERR_NULL, "output pointer is NULL");
+  int rc = validate_shapes(shapes, n);
+  if (rc != NSM_OK) return rc;
+  rc = validate_method(ns_method, ns_steps);
+  if (rc != NSM_OK) return rc;
+  if (i < 0 || i >= n) return fail(NSM_ERR_ARG, "matrix %d not in [0, %d)", i, n);
+  const Layout L = make_layout(shapes, n, ns_method, ns_steps);
+  if (buf < 0 || buf >= L.num_mm) return fail(NSM_ERR_ARG, "buffer %d not in [0, %d)", buf, L.num_mm);
+  const ShapeClass& sc = L.classes[L.cls_of[i]];
+  const bool small = ns_steps > 0 && small_kernel_enabled() && sc.m <= kSmallMaxM;
+  *m_out = small ? 0 : sc.m;
+  *ld_out = sc.ldm;
+  *offset_bytes = L.off_mm[buf] + (size_t(sc.mm_base) + size_t(L.batch_of[i]) * sc.m * sc.ldm) * 2;
   return NSM_OK;
 }
 
@@ -1155,14 +1208,12 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
   ++launches;
   // The small-matrix kernel applies its matrices itself; the grouped launches' matrices
-  // are applied by the last product's epilogue (NSM_FUSED_APPLY=1) or by the separate
-  // pass, which skips the matrices already applied.
+  // are applied by the separate pass, which skips the matrices already applied.
   const float decay = 1.0f - lr * wd;
   const ApplyArgs ap{P->d_mats, packed_params, params_bf16, lr, decay};
-  const bool fused = fused_apply_enabled() && !P->launches.empty();
-  rc = run_chain(*P, stream, &launches, &ap, fused ? &ap : nullptr);
+  rc = run_chain(*P, stream, &launches, &ap);
   if (rc != NSM_OK) return rc;
-  if (fused || P->n_small_jobs == n) {
+  if (P->n_small_jobs == n) {
     t_last_launches = launches;
     return NSM_OK;
   }
@@ -1397,16 +1448,28 @@ int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16, const int64_
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
-  char* scratch = noalloc_scratch(device, &rc);
-  if (!scratch) return rc;
+  std::lock_guard<std::mutex> lock(noalloc_mutex());
+  NoAllocState* st = noalloc_state(device, &rc);
+  if (!st) return rc;
+  char* scratch = st->scratch;
 
-  // workspace at the start of the array, the plan's metadata after it
-  Plan P;
-  P.device = device;
-  const size_t meta_off = align_up(ws_bytes, kAlign);
-  MetaSink sink{scratch + meta_off, kNoAllocBytes - meta_off, stream};
-  rc = build_plan(P, shapes, offsets, n, ns_method, ns_steps, scratch, ws_bytes, &sink);
-  if (rc != NSM_OK) return rc;
+  // Workspace at the start of the array, the plan's metadata after it.  The kernels write
+  // only the workspace, so the metadata of the last plan uploaded stays valid, and a call
+  // on the same table (same key) reuses it without copying anything.
+  const std::string key = plan_key(device, shapes, offsets, n, ns_method, ns_steps, scratch);
+  if (!st->plan || st->key != key) {
+    st->plan.reset();
+    st->key.clear();
+    std::unique_ptr<Plan> P(new Plan());
+    P->device = device;
+    const size_t meta_off = align_up(ws_bytes, kAlign);
+    MetaSink sink{scratch + meta_off, kNoAllocBytes - meta_off, stream};
+    rc = build_plan(*P, shapes, offsets, n, ns_method, ns_steps, scratch, ws_bytes, &sink);
+    if (rc != NSM_OK) return rc;
+    st->plan = std::move(P);
+    st->key = key;
+  }
+  Plan& P = *st->plan;
   char* ws = P.ws;
   float* partials = reinterpret_cast<float*>(ws + P.L.off_partials);
   float* scales = reinterpret_cast<float*>(ws + P.L.off_scales);
@@ -1431,7 +1494,12 @@ int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16, const int64_
   return NSM_OK;
 }
 
-int nsm_device_status(nsm_stream_t stream_, int* status_out) {
+int nsm_device_status(nsm_stream_t stream, int* status_out) {
+  return nsm_device_status_detail(stream, status_out, nullptr, nullptr, nullptr);
+}
+
+int nsm_device_status_detail(nsm_stream_t stream_, int* status_out, int* kernel_out, int* role_out,
+                             int* site_out) {
   if (!status_out) return fail(NSM_ERR_NULL, "status_out is NULL");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   cudaError_t e = cudaStreamSynchronize(stream);
@@ -1444,8 +1512,27 @@ int nsm_device_status(nsm_stream_t stream_, int* status_out) {
   const int zero = 0;
   e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return fail_cuda(e, "clear device status");
-  *status_out = (v == kDevTimeout) ? NSM_ERR_TIMEOUT : NSM_OK;
+  const bool timeout = (v & 0xff) == kDevTimeout;
+  *status_out = timeout ? NSM_ERR_TIMEOUT : NSM_OK;
+  if (kernel_out) *kernel_out = timeout ? (v >> 8) & 0xff : 0;
+  if (role_out) *role_out = timeout ? (v >> 16) & 0xff : 0;
+  if (site_out) *site_out = timeout ? (v >> 24) & 0xff : 0;
   return NSM_OK;
+}
+
+int nsm_set_option(int option, int value) {
+  if (value != 0 && value != 1) return fail(NSM_ERR_ARG, "option value %d is not 0 or 1", value);
+  switch (option) {
+    case NSM_OPT_PAIR_KERNELS: g_opt_pair.store(value); return NSM_OK;
+    case NSM_OPT_SMALL_KERNEL: g_opt_small.store(value); return NSM_OK;
+    case NSM_OPT_PDL: g_opt_pdl.store(value); return NSM_OK;
+    default: return fail(NSM_ERR_ARG, "unknown option %d", option);
+  }
+}
+
+int nsm_get_option(int option) {
+  const int v = nsm::option_value(option);
+  return v >= 0 ? v : fail(NSM_ERR_ARG, "unknown option %d", option);
 }
 
 int nsm_status_selftest(int wait_us, nsm_stream_t stream_) {

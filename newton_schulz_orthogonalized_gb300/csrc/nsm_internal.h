@@ -5,11 +5,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "nsmuon.h"
+
 namespace nsm {
 
-// Status word values kernels write when a bounded wait expires.
+// Status word kernels write when a bounded wait expires: kDevTimeout in the low byte,
+// then which kernel, which role inside it and which barrier gave up (NSM_KERNEL_*,
+// NSM_ROLE_*, NSM_SITE_* of the public header).  Only the first expiry since the word
+// was last read is kept.
 constexpr int kDevOk = 0;
 constexpr int kDevTimeout = 1;
+__host__ __device__ constexpr int status_word(int kernel, int role, int site) {
+  return kDevTimeout | (kernel << 8) | (role << 16) | (site << 24);
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ void record_timeout(int* status, int kernel, int role, int site) {
+  atomicCAS(status, kDevOk, status_word(kernel, role, site));
+}
+#endif
+
+// Values of the process-wide launch options (NSM_OPT_* of the public header).
+int option_value(int option);
 
 // One matrix of a packed group, as the elementwise kernels see it.
 struct MatInfo {
@@ -58,15 +74,15 @@ struct GemmGroup {
   int32_t tiles_m, tiles_n;
   int32_t sym, tiles_per_mat;
   int32_t a_box, b_box;  // rows per TMA box of map_a / map_b (64, 128 or 256)
-  const int32_t* mat_index;  // matrix (MatInfo index) of each batch entry
   const CUtensorMap* map_out;  // the output in 32 x 32 boxes with 64-byte swizzle (TMA stores);
                                // NULL when N is not a multiple of 8 (rows of whole 16-byte units)
 };
-static_assert(sizeof(GemmGroup) == 128, "GemmGroup layout");
+static_assert(sizeof(GemmGroup) == 120, "GemmGroup layout");
 
-// Epilogue that applies the step instead of storing O: for matrix mats[mat_index[b]],
-// p <- p * decay - lr * scale * O at O's natural position (transposed back when the
-// matrix is tall), and params_bf16 (if not NULL) <- bf16(p).  params == NULL: store O.
+// The small-matrix kernel's final pass applies the step instead of storing O: for
+// matrix mats[job.mat], p <- p * decay - lr * scale * O at O's natural position
+// (transposed back when the matrix is tall), and params_bf16 (if not NULL) <- bf16(p).
+// params == NULL: store O.
 struct ApplyArgs {
   const MatInfo* mats;
   float* params;
@@ -147,8 +163,7 @@ cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* m
 cudaError_t launch_adamw(const void* grads, float* params, float* m, float* v,
                          int64_t numel, float lr, float beta1, float beta2, float eps,
                          float wd, float bc1, float bc2, cudaStream_t stream);
-cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream,
-                        const ApplyArgs* apply = nullptr);
+cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream);
 
 int* device_status_ptr();
 // One CTA whose bounded wait expires after limit_ns and records kDevTimeout.

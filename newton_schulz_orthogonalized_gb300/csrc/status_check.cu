@@ -1,7 +1,8 @@
 // Self-test of the device status path.  One CTA waits, with the bounded mbarrier wait the
 // Newton-Schulz kernels use, on a barrier that nothing completes.  When the limit runs
 // out it records a timeout in the device status word, as a stalled chain kernel would,
-// and returns; the context stays usable.  nsm_device_status then reports it.
+// and returns; the context stays usable.  nsm_device_status then reports it, and
+// nsm_device_status_detail names this kernel and its barrier (role 0).
 #include <cuda_runtime.h>
 
 #include "nsm_internal.h"
@@ -21,7 +22,9 @@ __global__ void k_status_selftest(int* status, uint64_t limit_ns) {
   __syncthreads();
   if (threadIdx.x == 0) {
     // no thread ever arrives: phase 0 of the barrier does not complete
-    if (!ptx::mbar_wait_bounded(ptx::smem_u32(&bar), 0u, &never, limit_ns)) atomicExch(status, kDevTimeout);
+    if (!ptx::mbar_wait_bounded(ptx::smem_u32(&bar), 0u, &never, limit_ns)) {
+      record_timeout(status, NSM_KERNEL_SELFTEST, 0, NSM_SITE_SELFTEST);
+    }
   }
 }
 

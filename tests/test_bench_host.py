@@ -1,9 +1,10 @@
 """Host-side arithmetic of bench.py, checked without a GPU.
 
-The canonical Newton-Schulz flop count behind the reported NS TFLOP/s and the CPU
-baseline's extrapolation is counted in bench.py independently of the oracle; here it
-must equal the oracle's counts (which the oracle tests pin).  The oracle sample behind
-cpu_baseline must stay inside its flop budget.
+The Newton-Schulz flop counts behind the reported TFLOP/s are counted in bench.py
+independently of the oracle; here they must equal the oracle's counts (which the oracle
+tests pin): the canonical count is the gram form without re-anchoring, the dense count
+the chain as the library runs it.  The oracle sample behind cpu_baseline covers the
+distinct shapes of the table and scales each by its count.
 """
 
 import bench
@@ -14,16 +15,28 @@ SHAPES = [(128, 256), (4096, 11008), (11008, 4096), (768, 768), (1408, 2048), (1
 
 
 def test_canonical_flops_match_oracle():
-    for method, count in (("gram", oracle.flops_gram), ("standard", oracle.flops_standard)):
-        want = sum(count(min(r, c), max(r, c), 5) for r, c in SHAPES)
-        assert bench._canonical_ns_flops(SHAPES, method) == want, method
+    for m, n in [(min(r, c), max(r, c)) for r, c in SHAPES]:
+        assert oracle.flops_gram(m, n, 5, restart_every=0) == 4 * m * m * n + 34 * m ** 3
+    want = sum(oracle.flops_gram(min(r, c), max(r, c), 5, restart_every=0) for r, c in SHAPES)
+    assert bench._canonical_ns_flops(SHAPES, "gram") == want
+    want = sum(oracle.flops_standard(min(r, c), max(r, c), 5) for r, c in SHAPES)
+    assert bench._canonical_ns_flops(SHAPES, "standard") == want
+    assert bench._dense_ns_flops(SHAPES, "standard") == want
 
 
-def test_oracle_sample_keeps_to_its_flop_budget():
-    wl = synth.workload("tiny")  # four 128 x 256 matrices: one shape, one sampled matrix
-    ms, desc = bench.cpu_oracle_sample(wl, "gram", budget_s=5.0, max_flops=1e9)
+def test_dense_flops_match_oracle():
+    want = sum(oracle.flops_gram(min(r, c), max(r, c), 5) for r, c in SHAPES)
+    assert bench._dense_ns_flops(SHAPES, "gram") == want
+
+
+def test_oracle_sample_covers_shapes_and_scales_by_count():
+    wl = synth.custom([(16, 32), (16, 32), (16, 32), (24, 8)], seed=1)
+    shapes = bench._shape_counts(wl)
+    assert [(sh, cnt) for sh, _, cnt in shapes] == [((24, 8), 1), ((16, 32), 3)]
+    ms, desc = bench.cpu_oracle_sample(wl, "gram", budget_s=30.0)
     assert ms > 0
-    assert "on 1 matrices (128x256)" in desc
-    # a budget below the smallest matrix still samples that one matrix
-    ms, desc = bench.cpu_oracle_sample(wl, "gram", budget_s=5.0, max_flops=1.0)
-    assert ms > 0 and "on 1 matrices" in desc
+    assert "2 of the 2 distinct shapes" in desc
+    # a budget below the smallest matrix still times that one shape, and scales it to
+    # the whole table by the matrix count
+    ms1, desc1 = bench.cpu_oracle_sample(wl, "gram", budget_s=0.0)
+    assert ms1 > 0 and "1 of the 2 distinct shapes" in desc1

@@ -1,11 +1,21 @@
 """Parity at the full workload sizes, in the launch configuration the benchmark times.
 
 One muon_step runs over the whole packed group (224 matrices / 5.67B elements for the
-Llama-7B-shaped set, 3584 matrices / 9.13B elements for the Split/MoE set).  A sample of
-matrices (one of each working shape) is then checked against the oracle in the method's
-storage precision.  On every matrix the properties that hold at any size are checked:
-the update is finite, and ||O||_F <= 1.2 sqrt(m), because every singular value of the
-five-step output lies in [0, 1.2].
+Llama-7B-shaped set, 3584 matrices / 9.13B elements for the Split/MoE set); then one
+muon_orthogonalize runs over the same table, with the same grouped launches.
+
+* On every matrix: the update is finite, ||O||_F <= 1.2 sqrt(m) (every singular value of
+  the five-step output lies in [0, 1.2]), and every m x m iterate the chain left in the
+  workspace is exactly symmetric (the workspace starts as NaN, so each block is either
+  untouched or finite and symmetric).
+* On a sample that covers every working shape, the first and the last matrix of the large
+  classes (the far ends of the packed buffers and of the class slots, where 64-bit offsets
+  matter): the momentum at 1e-5 and the parameter delta at 1e-2 against the oracle in the
+  method's storage precision, and the orthogonalised output at 2e-2 against it, each with
+  the element-wise bounds of the parity tests.  The same outputs are compared with the
+  exact float64 iteration too: the measured distance is recorded, and held to 2.5e-2
+  (gram) / 3e-2 (standard), the distance that rounding the normalised input to fp16
+  alone produces on these near-low-rank inputs.
 """
 
 import numpy as np
@@ -13,9 +23,13 @@ import pytest
 import torch
 
 import oracle
+import parity_log
 import synth
+from test_gpu_parity import TOL_DELTA, TOL_FP32, TOL_NS, compare, elementwise, rel
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+TOL_EXACT = {"gram": 2.5e-2, "standard": 3e-2}
 
 
 @pytest.fixture(scope="module")
@@ -25,11 +39,42 @@ def nsm():
     return m
 
 
-def rel(a, b):
-    return np.linalg.norm(a - b) / np.linalg.norm(b)
+def _pick(shapes, picks):
+    """Indices: for each (shape, which) in picks, its first ('first') or last ('last')
+    occurrence in the table."""
+    out = []
+    for want, which in picks:
+        where = [i for i, sh in enumerate(shapes) if sh == want]
+        i = where[0] if which == "first" else where[-1]
+        if i not in out:
+            out.append(i)
+    return out
 
 
-def _run_fullsize(nsm, name, method, sample_shapes, last_too=()):
+def _iterates_symmetric(nsm, shapes, method, ws):
+    """Every m x m block of the workspace is untouched (NaN bits) or finite and exactly
+    symmetric; at least one block of every grouped-launch matrix was written."""
+    bits = ws.view(torch.int16)
+    vals = ws.view(torch.float16 if method != "standard_bf16" else torch.bfloat16)
+    for i in range(len(shapes)):
+        written = 0
+        for b in range(nsm.mm_buffers(method)):
+            off, m, ld = nsm.workspace_iterate(shapes, i, b, method)
+            if m == 0:
+                break
+            e0 = off // 2
+            blk = bits[e0:e0 + m * ld].view(m, ld)[:, :m]
+            if bool((blk == -1).all()):
+                continue
+            v = vals[e0:e0 + m * ld].view(m, ld)[:, :m]
+            assert bool(torch.isfinite(v).all()), (i, b)
+            assert torch.equal(blk, blk.t()), (i, shapes[i], b)
+            written += 1
+        off, m, _ = nsm.workspace_iterate(shapes, i, 0, method)
+        assert m == 0 or written > 0, i
+
+
+def _fullsize(nsm, name, method, step_picks, ortho_picks):
     wl = synth.workload(name)
     shapes = wl.muon_shapes
     offsets, total = nsm.pack(shapes)
@@ -40,12 +85,12 @@ def _run_fullsize(nsm, name, method, sample_shapes, last_too=()):
     synth.fill_packed_grads(wl, offsets, grads)
     synth.fill_packed_params(wl, offsets, params)
     p0 = params.clone()
-    ws = torch.empty(nsm.workspace_bytes(shapes, method), dtype=torch.uint8, device=dev)
+    ws = torch.full((nsm.workspace_bytes(shapes, method),), 255, dtype=torch.uint8, device=dev)
     copy = torch.empty(total, dtype=torch.bfloat16, device=dev)
     nsm.muon_step(grads, params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws,
                   params_bf16=copy)
     assert nsm.device_status() == nsm.NSM_OK
-    del ws
+    _iterates_symmetric(nsm, shapes, method, ws)
     # properties on every matrix: O = (p0 (1 - lr wd) - p1) / (lr scale)
     decay = np.float32(1.0) - np.float32(wl.lr) * np.float32(wl.wd)
     for i, (r, c) in enumerate(shapes):
@@ -54,23 +99,15 @@ def _run_fullsize(nsm, name, method, sample_shapes, last_too=()):
         assert torch.isfinite(d).all()
         onorm = float(d.double().norm()) / (wl.lr * oracle.update_scale(r, c))
         assert onorm <= 1.2 * np.sqrt(min(r, c)) * 1.01, (i, onorm)
-    # sampled matrices against the oracle: each shape's first occurrence and, where asked,
-    # its last (at the far end of the packed buffers and of the class slots, where 64-bit
-    # offsets matter)
-    picked = []
-    for want in sample_shapes:
-        where = [i for i, sh in enumerate(shapes) if sh == want]
-        picked.append(where[0])
-        if len(where) > 1 and want in last_too:
-            picked.append(where[-1])
+    step_idx = _pick(shapes, step_picks)
     # the bf16 copy (the owner's broadcast payload) is the rounding of the updated params,
-    # here on the sampled matrices and on the table's last one (the largest offsets)
-    for i in picked + [len(shapes) - 1]:
+    # on the sampled matrices and on the table's last one (the largest offsets)
+    for i in step_idx + [len(shapes) - 1]:
         r, c = shapes[i]
         o = int(offsets[i])
         assert torch.equal(copy[o:o + r * c], params[o:o + r * c].to(torch.bfloat16)), i
     del copy
-    for i in picked:
+    for i in step_idx:
         r, c = shapes[i]
         o = int(offsets[i])
         g = grads[o:o + r * c].double().cpu().numpy().reshape(r, c)
@@ -79,16 +116,46 @@ def _run_fullsize(nsm, name, method, sample_shapes, last_too=()):
                                            storage="method")
         got_p = params[o:o + r * c].double().cpu().numpy().reshape(r, c)
         got_m = mom[o:o + r * c].double().cpu().numpy().reshape(r, c)
-        assert rel(got_m, mn) <= 1e-5
-        assert rel(got_p - p, pn - p) <= 1e-2, ((r, c), rel(got_p - p, pn - p))
+        assert rel(got_m, mn) <= TOL_FP32
+        compare(got_p - p, pn - p, TOL_DELTA, f"fullsize/{name}/{method}/step/{(r, c)}/{i}")
+    del params, mom, p0
+
+    # the orthogonalisation alone over the same table: O as the chain computes it
+    out = torch.empty_like(grads)
+    ws.fill_(255)
+    nsm.muon_orthogonalize(grads, out, offsets, shapes, method, 5, ws)
+    assert nsm.device_status() == nsm.NSM_OK
+    _iterates_symmetric(nsm, shapes, method, ws)
+    del ws
+    for i in _pick(shapes, ortho_picks):
+        r, c = shapes[i]
+        o = int(offsets[i])
+        g = grads[o:o + r * c].double().cpu().numpy().reshape(r, c)
+        got = out[o:o + r * c].double().cpu().numpy().reshape(r, c)
+        ref = oracle.orthogonalize(g, method, storage="method")
+        compare(got, ref, TOL_NS, f"fullsize/{name}/{method}/ortho/{(r, c)}/{i}")
+        exact = oracle.orthogonalize(g, method)
+        e = rel(got, exact)
+        emax, ep = elementwise(got, exact)
+        parity_log.record(f"fullsize/{name}/{method}/ortho_vs_exact/{(r, c)}/{i}", rel=e, max_over_rms=emax,
+                          p999_over_rms=ep, tol=TOL_EXACT[method])
+        assert e <= TOL_EXACT[method], ((r, c), i, e)
+
+
+LLAMA_STEP = [((1024, 4096), "first"), ((1024, 4096), "last"), ((4096, 4096), "first"),
+              ((11008, 4096), "first"), ((11008, 4096), "last"), ((4096, 11008), "last")]
+LLAMA_ORTHO = [((11008, 4096), "first"), ((4096, 11008), "first"), ((4096, 4096), "last"),
+               ((1024, 4096), "last")]
 
 
 @pytest.mark.parametrize("method", ["gram", "standard"])
 def test_llama7b_fullsize(nsm, method):
-    _run_fullsize(nsm, "llama7b", method, [(1024, 4096), (4096, 4096)], last_too=[(1024, 4096)])
+    _fullsize(nsm, "llama7b", method, LLAMA_STEP, LLAMA_ORTHO)
 
 
 @pytest.mark.parametrize("method", ["gram"])
 def test_split_moe_fullsize(nsm, method):
-    _run_fullsize(nsm, "split_moe", method, [(128, 4096), (1408, 2048), (2048, 1408)],
-                  last_too=[(1408, 2048)])
+    picks = [((128, 4096), "first"), ((128, 4096), "last"), ((1408, 2048), "first"),
+             ((1408, 2048), "last"), ((2048, 1408), "last")]
+    _fullsize(nsm, "split_moe", method, picks, [((2048, 1408), "first"), ((1408, 2048), "last"),
+                                                ((128, 4096), "last")])

@@ -105,17 +105,27 @@ def test_gemm_deterministic(nsm, pair):
     assert torch.equal(o1, o2)
 
 
-def test_gemm_pair_matches_single_cta(nsm):
-    # the two kernels accumulate each output in the same K order: results are identical
-    a = _rand((768, 1536), torch.float16, 8)
-    b = _rand((1024, 1536), torch.float16, 9)
-    o1 = torch.empty((768, 1024), dtype=torch.float16, device="cuda")
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("b_mn", [False, True])
+def test_gemm_pair_matches_single_cta(nsm, dtype, b_mn):
+    # the two kernels accumulate each output over K in the same order of 16-wide MMAs
+    # into fp32 TMEM and round once in the same epilogue: the results are the same bits
+    a = _rand((768, 1536), dtype, 8)
+    b = _rand((1536, 1016) if b_mn else (1016, 1536), dtype, 9)
+    aux = _rand((768, 1016), dtype, 10)
+    o1 = torch.empty((768, 1016), dtype=dtype, device="cuda")
     o2 = torch.empty_like(o1)
-    nsm.gemm(a, b, o1, pair=False)
-    nsm.gemm(a, b, o2, pair=True)
+    nsm.gemm(a, b, o1, aux=aux, b_mn_major=b_mn, alpha=0.75, beta=-1.5, pair=False)
+    nsm.gemm(a, b, o2, aux=aux, b_mn_major=b_mn, alpha=0.75, beta=-1.5, pair=True)
     torch.cuda.synchronize()
-    rel = (o1.double() - o2.double()).norm() / o1.double().norm()
-    assert rel.item() <= 1e-3
+    assert torch.equal(o1, o2)
+    # and a symmetric output, upper tiles mirrored
+    s1 = torch.empty((768, 768), dtype=dtype, device="cuda")
+    s2 = torch.empty_like(s1)
+    nsm.gemm(a, a, s1, symmetric=True, pair=False)
+    nsm.gemm(a, a, s2, symmetric=True, pair=True)
+    torch.cuda.synchronize()
+    assert torch.equal(s1, s2)
 
 
 def test_gemm_rejects_bad_arguments(nsm):

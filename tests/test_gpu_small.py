@@ -7,10 +7,6 @@ GPU has SMs (each CTA runs several chains), at every step count the interface al
 and to the grouped path, which computes the same products in other launches.
 """
 
-import os
-import subprocess
-import sys
-
 import numpy as np
 import pytest
 import torch
@@ -18,7 +14,7 @@ import torch
 import oracle
 import synth
 
-from test_gpu_parity import TOL_NS, Step, orthogonalize_gpu, rel
+from test_gpu_parity import TOL_NS, Step, compare, orthogonalize_gpu, rel
 
 pytestmark = pytest.mark.gpu
 
@@ -90,39 +86,34 @@ def test_orthogonalize_small_vs_exact(nsm, method):
         x = inp[o:o + r * c].reshape(r, c)
         got = out[o:o + r * c].reshape(r, c)
         want = oracle.orthogonalize(x, method)
-        assert rel(got, want) <= TOL_NS, (i, rel(got, want))
+        compare(got, want, TOL_NS, f"small/vs_exact/{method}/{(r, c)}")
 
 
-_GROUPED = r"""
-import sys, torch
-import newton_schulz_orthogonalized_gb300 as nsm
-import synth
-wl = synth.custom([(128, 1024), (96, 333), (128, 128), (700, 64)], seed=59, lowrank=False)
-offsets, total = nsm.pack(wl.muon_shapes)
-res = {}
-for method in ("gram", "standard"):
-    inp = torch.zeros(total, dtype=torch.bfloat16, device="cuda")
-    synth.fill_packed_grads(wl, offsets, inp)
-    out = torch.zeros_like(inp)
-    ws = torch.empty(nsm.workspace_bytes(wl.muon_shapes, method), dtype=torch.uint8, device="cuda")
-    nsm.muon_orthogonalize(inp, out, offsets, wl.muon_shapes, method, 5, ws)
-    assert nsm.device_status() == 0
-    res[method] = out.cpu()
-torch.save(res, sys.argv[1])
-"""
+def _orthogonalize_both_forms(nsm):
+    wl = synth.custom([(128, 1024), (96, 333), (128, 128), (700, 64)], seed=59, lowrank=False)
+    offsets, total = nsm.pack(wl.muon_shapes)
+    res = {}
+    for method in ("gram", "standard"):
+        inp = torch.zeros(total, dtype=torch.bfloat16, device="cuda")
+        synth.fill_packed_grads(wl, offsets, inp)
+        out = torch.zeros_like(inp)
+        ws = torch.empty(nsm.workspace_bytes(wl.muon_shapes, method), dtype=torch.uint8, device="cuda")
+        nsm.muon_orthogonalize(inp, out, offsets, wl.muon_shapes, method, 5, ws)
+        assert nsm.device_status() == nsm.NSM_OK
+        res[method] = out.cpu()
+    return res
 
 
-def test_small_kernel_agrees_with_grouped_path(nsm, tmp_path):
-    # NSM_SMALL_KERNEL=0 sends the same matrices through the grouped launches: the same
-    # products and storage points, summed in another order
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    paths = {}
-    for flag in ("1", "0"):
-        paths[flag] = tmp_path / f"small{flag}.pt"
-        env = dict(os.environ, NSM_SMALL_KERNEL=flag)
-        subprocess.run([sys.executable, "-c", _GROUPED, str(paths[flag])], env=env, cwd=root, check=True,
-                       timeout=600)
-    a, b = torch.load(paths["1"]), torch.load(paths["0"])
+def test_small_kernel_agrees_with_grouped_path(nsm):
+    # The option that turns the small-matrix kernel off sends the same matrices through
+    # the grouped launches: the same products and storage points, summed in another order
+    assert nsm.get_option(nsm.OPT_SMALL_KERNEL) == 1
+    a = _orthogonalize_both_forms(nsm)
+    nsm.set_option(nsm.OPT_SMALL_KERNEL, 0)
+    try:
+        b = _orthogonalize_both_forms(nsm)
+    finally:
+        nsm.set_option(nsm.OPT_SMALL_KERNEL, 1)
     for method in a:
         x, y = a[method].double().numpy(), b[method].double().numpy()
         assert rel(x, y) <= 5e-3, (method, rel(x, y))

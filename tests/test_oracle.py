@@ -465,3 +465,58 @@ def test_page_memory_arithmetic():
     assert (2 + 2 + 4 + 4 + 4) / w == mem["zero3"]
     d = g["dmuon_z2_example"]
     assert d["params_muon"] * d["bytes_per_elem"] / d["shards"] / 1e6 == d["per_rank_mb"]
+
+
+# ---------------------------------------------------------------- storage-point placement
+#
+# tests/golden/storage_points.json holds a 3x5 case worked in exact rational arithmetic
+# with its own fp16 rounding (tests/golden/make_storage_points.py: no numpy, no oracle):
+# the expected fp16 results of 1-2 standard steps and 1-3 gram steps (the third covers a
+# re-anchoring), and the results with any one rounding point dropped or one plausible
+# extra rounding point added, each of which differs from the expected one.  The oracle
+# must give the expected bits, round exactly as many times, and change its result when
+# any one of its own rounding points is skipped.
+
+def _hexmat(rows):
+    return np.array([[float.fromhex(v) for v in r] for r in rows])
+
+
+_SP = _golden("storage_points.json")
+
+
+def _ns_fp16(method, x, steps):
+    if method == "standard":
+        return oracle.ns_standard(x, steps, storage="fp16")
+    return oracle.ns_gram(x, steps, storage="fp16")
+
+
+@pytest.mark.parametrize("case", _SP["cases"], ids=lambda c: f"{c['method']}{c['steps']}")
+def test_storage_points_give_the_worked_bits(case):
+    x = _hexmat(_SP["x"])
+    want = _hexmat(case["expected"])
+    assert np.array_equal(_ns_fp16(case["method"], x, case["steps"]), want)
+    for alt in case["dropped"] + list(case["added"].values()):
+        assert not np.array_equal(_hexmat(alt), want)
+
+
+@pytest.mark.parametrize("case", _SP["cases"], ids=lambda c: f"{c['method']}{c['steps']}")
+def test_storage_points_count_and_each_matters(case, monkeypatch):
+    x = _hexmat(_SP["x"])
+    want = _hexmat(case["expected"])
+    from oracle import muon_ref
+    real_store = muon_ref._store
+    calls = {"n": 0, "skip": None}
+
+    def counting_store(v, storage):
+        k = calls["n"]
+        calls["n"] += 1
+        if storage is not None and k == calls["skip"]:
+            return np.asarray(v, dtype=np.float64)
+        return real_store(v, storage)
+
+    monkeypatch.setattr(muon_ref, "_store", counting_store)
+    _ns_fp16(case["method"], x, case["steps"])
+    assert calls["n"] == case["rounding_points"]
+    for k in range(1, case["rounding_points"]):
+        calls["n"], calls["skip"] = 0, k
+        assert not np.array_equal(_ns_fp16(case["method"], x, case["steps"]), want), k

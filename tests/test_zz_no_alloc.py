@@ -1,14 +1,17 @@
 """The allocation-free orthogonalisation against the regular one.
 
-muon_orthogonalize_noalloc serves callers that cannot allocate device memory (graph
-capture under a mode that forbids it, a framework pool that owns all device memory, a
-loop that cannot take an allocation's implicit synchronisation).  It must give the
-output of muon_orthogonalize with a caller workspace.  The two run the same kernels on
-the same plan, so the outputs are expected to be identical; the check uses the parity
-tolerance of the other tests (2e-2 relative Frobenius error).  Two calls in a row, on
-different tables, show that the shared array carries nothing over from one call to the
-next.  This file is collected last so that a failure here leaves every other result
-standing.
+muon_orthogonalize_noalloc is for callers that cannot call cudaMalloc: a framework whose
+own caching pool owns all device memory (an allocation outside it can fail or fragment
+the pool), or a latency-critical loop that cannot take the device synchronisation an
+allocation may imply.  It keeps its workspace and launch plan in a fixed array of device
+memory that belongs to the library.
+
+It runs the same kernels on the same plan as muon_orthogonalize with a caller workspace,
+so the outputs must be identical bit for bit.  The calls in a row use different tables,
+then the first table again: the shared array keeps the last call's contents, and neither
+a stale workspace nor a stale plan may leak into the next result.  This file is
+collected last so that a failure here leaves every other result standing; it passes on
+its own in a fresh process too.
 """
 
 import ctypes
@@ -20,8 +23,6 @@ import torch
 import synth
 
 pytestmark = pytest.mark.gpu
-
-TOL_NS = 2e-2
 
 
 @pytest.fixture(scope="module")
@@ -47,6 +48,7 @@ def _regular(nsm, wl, offsets, inp, method):
 
 
 def _noalloc(nsm, wl, offsets, inp, method):
+    # straight through the C ABI
     out = torch.full_like(inp, float("nan"))
     L = nsm.lib()
     s = np.ascontiguousarray(np.asarray(wl.muon_shapes, dtype=np.int32).reshape(-1, 2))
@@ -61,26 +63,26 @@ def _noalloc(nsm, wl, offsets, inp, method):
     return out
 
 
-def _compare(nsm, wl, offsets, a, b):
-    a = a.double().cpu().numpy()
-    b = b.double().cpu().numpy()
+def _same_bits(nsm, wl, offsets, got, ref):
     for i, (r, c) in enumerate(wl.muon_shapes):
         o = int(offsets[i])
-        x, y = a[o:o + r * c], b[o:o + r * c]
-        assert np.all(np.isfinite(x))
-        err = np.linalg.norm(x - y) / np.linalg.norm(y)
-        assert err <= TOL_NS, (i, (r, c), err)
+        x, y = got[o:o + r * c], ref[o:o + r * c]
+        assert torch.isfinite(x.float()).all(), (i, (r, c))
+        assert torch.equal(x, y), (i, (r, c))
 
 
 @pytest.mark.parametrize("method", ["gram", "standard"])
 def test_noalloc_matches_regular_two_calls(nsm, method):
     first = synth.custom([(256, 512), (512, 256), (130, 260), (64, 64)], seed=31)
     second = synth.custom([(1024, 1024), (384, 96), (3, 5)], seed=32)
-    for wl in (first, second):
+    for wl in (first, second, first):
         offsets, inp = _inputs(nsm, wl)
         ref = _regular(nsm, wl, offsets, inp, method)
         got = _noalloc(nsm, wl, offsets, inp, method)
-        _compare(nsm, wl, offsets, got, ref)
+        _same_bits(nsm, wl, offsets, got, ref)
+        # the same table again: the plan already in the array is reused as it stands
+        again = _noalloc(nsm, wl, offsets, inp, method)
+        _same_bits(nsm, wl, offsets, again, ref)
     assert nsm.device_status() == nsm.NSM_OK
 
 
@@ -92,4 +94,4 @@ def test_noalloc_rejects_tables_beyond_its_array(nsm):
     with pytest.raises(nsm.NsmError) as e:
         nsm.muon_orthogonalize_noalloc(inp, out, offsets, wl.muon_shapes, "gram")
     assert e.value.code == nsm.NSM_ERR_WORKSPACE
-    assert "64" in nsm.last_error() or "bytes" in nsm.last_error()
+    assert "bytes" in nsm.last_error()
