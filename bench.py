@@ -187,7 +187,7 @@ def max_over_ranks(value, dist, device):
 
 
 # kernels whose timing work is flops (the others count bytes)
-FLOP_KERNELS = ("k_ns_gemm", "k_ns_small")
+FLOP_KERNELS = ("k_ns_gemm",)
 
 
 def _traffic_record(method, workload):

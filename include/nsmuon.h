@@ -271,7 +271,8 @@ int nsm_status_selftest(int wait_us, nsm_stream_t stream);
 #define NSM_KIND_LAYOUT   3  /* X = s U into the working layout */
 #define NSM_KIND_APPLY    4  /* decay + apply (or the export of O) */
 #define NSM_KIND_ADAMW    5  /* AdamW */
-#define NSM_KIND_SMALL    6  /* whole Newton-Schulz chains of matrices with m <= 128 (flops) */
+#define NSM_KIND_SMALL    6  /* whole Newton-Schulz chains of matrices with m <= 128 (bytes:
+                                 every read and write of X; the kernel is HBM-bound) */
 int nsm_timing_enable(int enable);
 int nsm_timing_read(double* gemm_ms, int64_t* gemm_launches, double* gemm_flops);
 int nsm_timing_read_kind(int kind, double* ms, int64_t* launches, double* work);

@@ -349,7 +349,6 @@ __global__ void __launch_bounds__(kThreads)
   for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
     const TilePos tp = tile_pos(mats, nmats, t);
     const MatInfo& mt = mats[tp.mi];
-    if (APPLY && (mt.flags & kMatInChain)) continue;  // already applied by the small-matrix kernel
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
     const int64_t s0 = mt.slot;
     const float coef = lr * mt.scale;

@@ -15,8 +15,10 @@
 //              (N = 128).  Each chunk of X' is rounded in the epilogue, written to
 //              shared memory and stored with TMA stores; when another Gram follows, the
 //              MMA warp also accumulates X' X'^T from that chunk, so the next step needs
-//              no extra pass over X.  The final pass applies the step to the parameters
-//              (or stores O).
+//              no extra pass over X.  The final pass stores O the same way; the step's
+//              separate apply pass then updates the parameters (the four epilogue warps
+//              of a CTA cannot keep enough parameter loads in flight to apply it here:
+//              measured, that took 62% of this kernel's time on the Split/MoE head blocks).
 //
 // Roles: warp 0 issues the TMA loads, warp 1 (one thread) the MMAs, warps 2-5 drain TMEM
 // (each thread one row).  Every wait is bounded; the epilogue warps take every decision
@@ -28,7 +30,6 @@
 
 #include <atomic>
 
-#include "apply.cuh"
 #include "launch.cuh"
 #include "nsm_internal.h"
 #include "ptx.cuh"
@@ -180,7 +181,7 @@ __device__ bool produce(const Roles& R, const SmallJob* __restrict__ jobs, int n
 // ------------------------------------------------------------------ MMA issuer
 template <bool FP16>
 __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict__ jobs, int njobs,
-                      const SmallOp* __restrict__ ops, int nops, bool store_final) {
+                      const SmallOp* __restrict__ ops, int nops) {
   const uint32_t id_sq = ptx::idesc_f16(128, 128, !FP16, false);
   const uint32_t id_pass = ptx::idesc_f16(128, kChunk, !FP16, true);
   RingPos rp;
@@ -236,7 +237,6 @@ __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict_
         }
         if (!finish_square()) return false;
       } else {
-        const bool stores = !op.final_pass || store_final;
         const uint32_t a = R.square(op.a);
         const uint32_t xs0 = xs;
         for (int c = 0; c < nck; ++c) {
@@ -266,7 +266,7 @@ __device__ bool issue(const Roles& R, uint32_t tmem, const SmallJob* __restrict_
           if (!accumulate_panel(nck - 1, (xs0 + nck - 1) & 1u)) return false;
           if (!finish_square()) return false;
         }
-        if (stores) xs += static_cast<uint32_t>(nck);
+        xs += static_cast<uint32_t>(nck);
       }
     }
   }
@@ -283,11 +283,10 @@ struct Epilogue {
   int row;          // the accumulator row (= TMEM lane) this thread drains
   int lane;
   bool leader;      // first epilogue thread: issues the TMA stores
-  uint32_t* xw;     // this warp's 32 x 17 words of transpose scratch (in the X' staging area)
   uint32_t sq_cnt = 0;
 
-  __device__ Epilogue(const Roles& r, uint32_t tmem, int warp, int ln, uint32_t* scratch)
-      : R(r), lane(ln), leader(warp == 2 && ln == 0), xw(scratch) {
+  __device__ Epilogue(const Roles& r, uint32_t tmem, int warp, int ln)
+      : R(r), lane(ln), leader(warp == 2 && ln == 0) {
     const int quarter = warp & 3;
     row = quarter * 32 + ln;
     t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -351,11 +350,10 @@ struct Epilogue {
 
 template <bool FP16>
 __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int njobs,
-                      const SmallOp* __restrict__ ops, int nops, const ApplyArgs& ap) {
+                      const SmallOp* __restrict__ ops, int nops) {
   using E = Store<FP16>;
   using T = typename E::T;
   const Roles& R = ep.R;
-  const bool store_final = ap.params == nullptr;
   RingPos rp;
   uint32_t acc_cnt = 0, xs = 0;
   uint32_t hand[2] = {0u, 0u};
@@ -374,10 +372,8 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
         if (!ep.square(op.dst, op.aux, op.alpha, op.beta, op.diag, job.m)) return false;
         continue;
       }
-      const bool stores = !op.final_pass || store_final;
       const bool reads_x = op.beta != 0.f;
       const uint32_t xs0 = xs;
-      const int rb = ep.row - ep.lane;  // the warp's first row
       for (int c = 0; c < nck; ++c) {
         const uint32_t acc = acc_cnt & 1u;
         bool ok = R.wait(&R.ctrl->acc_full[acc], (acc_cnt >> 1) & 1u, NSM_ROLE_EPILOGUE, NSM_SITE_ACC_FULL);
@@ -387,7 +383,7 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
         const int stage = rp.stage;
         const uint32_t chunk = R.ring + static_cast<uint32_t>(stage * kSlot);
         const uint32_t slot = (xs0 + static_cast<uint32_t>(c)) & 1u;
-        if (stores) {
+        {
           // the X' slot must be free: read by its store two chunks back and by the MMA
           if (ep.leader) ptx::bulk_wait_group_read<1>();
           bool free_ok = true;
@@ -424,35 +420,14 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
           }
 #pragma unroll
           for (int k = 0; k < 64; ++k) v[k] = E::to_f(E::from_f(v[k]));  // X' (or O) as stored
-          if (stores) {
-            const uint32_t dst = xt + static_cast<uint32_t>(h * kPanel);
+          const uint32_t dst = xt + static_cast<uint32_t>(h * kPanel);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              uint4 pk;
-              T* e = reinterpret_cast<T*>(&pk);
+          for (int u = 0; u < 8; ++u) {
+            uint4 pk;
+            T* e = reinterpret_cast<T*>(&pk);
 #pragma unroll
-              for (int k = 0; k < 8; ++k) e[k] = E::from_f(v[u * 8 + k]);
-              *reinterpret_cast<uint4*>(__cvta_shared_to_generic(dst + sw(ep.row, u))) = pk;
-            }
-          } else if (rb < job.m) {
-            // final pass: apply the step, one coalesced 32 x 32 block at a time (the X'
-            // staging area is idle in this pass: every earlier store and MMA read of it
-            // has completed)
-            const MatInfo& mt = ap.mats[job.mat];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int gc0 = c * kChunk + 64 * h + 32 * q;
-              if (gc0 < job.n) {
-                uint32_t o[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = pack2<FP16>(v[q * 32 + 2 * i], v[q * 32 + 2 * i + 1]);
-                apply_block_columns(mt, o, ep.xw, ep.lane);
-                const ApplyBlock blk = apply_block_at(mt, rb, gc0, job.m, job.n);
-                float pv[32];
-                apply_block_load(ap, mt, blk, ep.lane, pv);
-                apply_block_store<FP16>(ap, mt, blk, ep.lane, o, pv);
-              }
-            }
+            for (int k = 0; k < 8; ++k) e[k] = E::from_f(v[u * 8 + k]);
+            *reinterpret_cast<uint4*>(__cvta_shared_to_generic(dst + sw(ep.row, u))) = pk;
           }
         }
         ptx::tc_fence_before();
@@ -460,14 +435,7 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
         if (ep.lane == 0) ptx::mbar_arrive(R.bar(&R.ctrl->acc_empty[acc]));
         ++acc_cnt;
         rp.advance();
-        if (!stores) {
-          if (reads_x) {
-            ptx::named_sync(kEpiBar, kEpiThreads);  // every thread has read the chunk
-            if (ep.leader) ptx::mbar_arrive(R.bar(&R.ctrl->empty[stage]));
-          }
-          continue;
-        }
-        // X' chunk -> TMA stores (and to the MMA when accumulating)
+        // X' (or O) chunk -> TMA stores (and to the MMA when accumulating)
         ptx::fence_proxy_async_smem();
         ptx::named_sync(kEpiBar, kEpiThreads);
         if (ep.leader) {
@@ -482,7 +450,7 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
           ++hand[slot];
         }
       }
-      if (stores) xs += static_cast<uint32_t>(nck);
+      xs += static_cast<uint32_t>(nck);
       if (!op.final_pass && ep.leader) {
         // the next pass loads this X': every store must have landed
         ptx::bulk_wait_group<0>();
@@ -500,7 +468,7 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
 template <bool FP16>
 __global__ void __launch_bounds__(kThreads, 1)
     k_ns_small(const SmallJob* __restrict__ jobs, int njobs, const SmallOp* __restrict__ ops, int nops,
-               int* status, ApplyArgs ap) {
+               int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -566,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      if (!issue<FP16>(R, tmem, jobs, njobs, ops, nops, ap.params == nullptr)) R.give_up();
+      if (!issue<FP16>(R, tmem, jobs, njobs, ops, nops)) R.give_up();
       // no MMA may still write TMEM when the block frees it
       ptx::mma_commit(R.bar(&ctrl->drain));
       if (!ptx::mbar_wait_bounded(R.bar(&ctrl->drain), 0u, R.never_flag, kWaitNs)) {
@@ -576,8 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    Epilogue<FP16> ep(R, tmem, warp, lane, reinterpret_cast<uint32_t*>(smem + kXtOff + (warp - 2) * 4096));
-    drain<FP16>(ep, jobs, njobs, ops, nops, ap);
+    Epilogue<FP16> ep(R, tmem, warp, lane);
+    drain<FP16>(ep, jobs, njobs, ops, nops);
     // stores still reading shared memory must finish before the block exits
     if (ep.leader) ptx::bulk_wait_group<0>();
   }
@@ -606,7 +574,7 @@ cudaError_t set_smem_once(K kernel, size_t bytes, std::atomic<uint64_t>& done) {
 
 template <bool FP16>
 cudaError_t launch_typed(const SmallJob* jobs, int njobs, const SmallOp* ops, int nops, int num_sms,
-                         cudaStream_t stream, const ApplyArgs& ap) {
+                         cudaStream_t stream) {
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   static std::atomic<uint64_t> done{0};
@@ -614,18 +582,17 @@ cudaError_t launch_typed(const SmallJob* jobs, int njobs, const SmallOp* ops, in
   if (e != cudaSuccess) return e;
   const int grid = njobs < num_sms ? njobs : num_sms;
   if (grid <= 0) return cudaSuccess;
-  if (const cudaError_t e_launch = launch_pdl(k_ns_small<FP16>, dim3(grid), dim3(kThreads), kSmem, stream, jobs, njobs, ops, nops, status, ap)) return e_launch;
+  if (const cudaError_t e_launch = launch_pdl(k_ns_small<FP16>, dim3(grid), dim3(kThreads), kSmem, stream, jobs, njobs, ops, nops, status)) return e_launch;
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_ns_small(const SmallJob* jobs, int njobs, const SmallOp* ops, int nops, int fp16,
-                            int num_sms, cudaStream_t stream, const ApplyArgs* apply) {
-  const ApplyArgs ap = apply ? *apply : ApplyArgs{nullptr, nullptr, nullptr, 0.f, 1.f};
+                            int num_sms, cudaStream_t stream) {
   if (nops <= 0 || nops > kSmallMaxOps) return cudaErrorInvalidValue;
-  return fp16 ? launch_typed<true>(jobs, njobs, ops, nops, num_sms, stream, ap)
-              : launch_typed<false>(jobs, njobs, ops, nops, num_sms, stream, ap);
+  return fp16 ? launch_typed<true>(jobs, njobs, ops, nops, num_sms, stream)
+              : launch_typed<false>(jobs, njobs, ops, nops, num_sms, stream);
 }
 
 }  // namespace nsm

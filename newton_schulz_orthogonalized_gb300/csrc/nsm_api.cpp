@@ -245,7 +245,7 @@ struct Plan {
   const SmallOp* d_small_ops = nullptr;
   int n_small_jobs = 0;
   int n_small_ops = 0;
-  double small_flops = 0;
+  double small_bytes = 0;  // HBM bytes the small-matrix kernel must move (its roofline)
   ~Plan() {
     if (dmeta && owns_meta) cudaFree(dmeta);
   }
@@ -558,9 +558,15 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     std::stable_sort(small_mats.begin(), small_mats.end(), [&](int x, int y) {
       return int64_t(shapes[2 * x]) * shapes[2 * x + 1] > int64_t(shapes[2 * y]) * shapes[2 * y + 1];
     });
+    // every Gram and pass operation reads X once, every pass writes X' (or O) once
+    int x_reads = 0, x_writes = 0;
+    for (const SmallOp& o : small_ops) {
+      if (o.kind != kSmallSquare) ++x_reads;
+      if (o.kind == kSmallPass) ++x_writes;
+    }
     for (int i : small_mats) {
       const ShapeClass& sc = L.classes[L.cls_of[i]];
-      P.small_flops += double(chain_flops(method, steps, sc.m, sc.n));
+      P.small_bytes += 2.0 * double(sc.m) * double(sc.n) * (x_reads + x_writes);
     }
   }
 
@@ -595,7 +601,6 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     mi.nchunks = L.nchunks[i];
     mi.scale = static_cast<float>(std::sqrt(std::max(1.0, double(mi.rows) / double(mi.cols))));
     mi.flags = (mi.rows % 8 == 0 && mi.cols % 8 == 0) ? kMatVec : 0;
-    if (small[L.cls_of[i]]) mi.flags |= kMatInChain;
     hm[i] = mi;
   }
 
@@ -926,17 +931,16 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need) {
   return NSM_OK;
 }
 
-// Launches the chain: the small-matrix kernel, then the grouped GEMMs.  With
-// `apply_small`, the small-matrix kernel applies the step to its matrices instead of
-// storing O.
-int run_chain(Plan& P, cudaStream_t stream, int* launches, const ApplyArgs* apply_small = nullptr) {
+// Launches the chain: the small-matrix kernel, then the grouped GEMMs.  Both leave O in
+// the X buffer P.final_buf.
+int run_chain(Plan& P, cudaStream_t stream, int* launches) {
   int num_sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, P.device);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
   if (P.n_small_jobs > 0) {
-    TimedLaunch t(stream, NSM_KIND_SMALL, P.small_flops);
+    TimedLaunch t(stream, NSM_KIND_SMALL, P.small_bytes);
     e = launch_ns_small(P.d_small_jobs, P.n_small_jobs, P.d_small_ops, P.n_small_ops, P.x_fp16 ? 1 : 0, num_sms,
-                        stream, apply_small);
+                        stream);
     if (e != cudaSuccess) return fail_cuda(e, "small-matrix Newton-Schulz launch");
     ++*launches;
   }
@@ -1207,16 +1211,9 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   }
   if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
   ++launches;
-  // The small-matrix kernel applies its matrices itself; the grouped launches' matrices
-  // are applied by the separate pass, which skips the matrices already applied.
-  const float decay = 1.0f - lr * wd;
-  const ApplyArgs ap{P->d_mats, packed_params, params_bf16, lr, decay};
-  rc = run_chain(*P, stream, &launches, &ap);
+  // The chain leaves O in the workspace; the apply pass updates every matrix from it.
+  rc = run_chain(*P, stream, &launches);
   if (rc != NSM_OK) return rc;
-  if (P->n_small_jobs == n) {
-    t_last_launches = launches;
-    return NSM_OK;
-  }
   {
     TimedLaunch t(stream, NSM_KIND_APPLY, (params_bf16 ? 12.0 : 10.0) * elems);
     e = launch_apply(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, packed_params, params_bf16,

@@ -37,13 +37,10 @@ struct MatInfo {
   int32_t transposed; // rows > cols: the slot holds the transpose
   int32_t chunk_begin, nchunks;  // momentum/norm chunks of this matrix
   float scale;        // sqrt(max(1, rows/cols))
-  int32_t flags;      // kMatVec | kMatInChain
+  int32_t flags;      // kMatVec
 };
-// MatInfo::flags: rows % 8 == 0 && cols % 8 == 0 (16-byte vector paths usable) ...
+// MatInfo::flags: rows % 8 == 0 && cols % 8 == 0 (16-byte vector paths usable)
 constexpr int32_t kMatVec = 1;
-// ... and: the small-matrix kernel applies this matrix's step in its final pass, so the
-// separate apply pass leaves it alone
-constexpr int32_t kMatInChain = 2;
 static_assert(sizeof(MatInfo) == 64, "MatInfo layout");
 
 // Elements of one momentum/norm chunk (256 threads x 8 vectors of 8).
@@ -78,17 +75,6 @@ struct GemmGroup {
                                // NULL when N is not a multiple of 8 (rows of whole 16-byte units)
 };
 static_assert(sizeof(GemmGroup) == 120, "GemmGroup layout");
-
-// The small-matrix kernel's final pass applies the step instead of storing O: for
-// matrix mats[job.mat], p <- p * decay - lr * scale * O at O's natural position
-// (transposed back when the matrix is tall), and params_bf16 (if not NULL) <- bf16(p).
-// params == NULL: store O.
-struct ApplyArgs {
-  const MatInfo* mats;
-  float* params;
-  void* params_bf16;
-  float lr, decay;
-};
 
 struct GemmLaunch {
   const GemmGroup* groups;  // device array
@@ -136,10 +122,9 @@ constexpr int kSmallMaxOps = 96;
 
 // ---- launchers (defined in the .cu files) ---------------------------------------
 
-// Runs `ops` for every job; with `apply` (params != NULL) the final pass applies the step
-// instead of storing O.
+// Runs `ops` for every job; the final pass stores O into its X buffer.
 cudaError_t launch_ns_small(const SmallJob* jobs, int njobs, const SmallOp* ops, int nops, int fp16,
-                            int num_sms, cudaStream_t stream, const ApplyArgs* apply);
+                            int num_sms, cudaStream_t stream);
 
 // M <- mu M + G (when has_momentum) and per-chunk sums of U^2, U = G + mu M (Nesterov),
 // M (plain) or G (no momentum)
