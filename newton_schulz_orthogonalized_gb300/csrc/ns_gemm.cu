@@ -717,7 +717,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int kblocks = (G.K + BK2 - 1) / BK2;
         // boxes each CTA loads; the leader expects both CTAs' bytes
         const int a0 = boxes_in(tc.m0, G.M), a1 = boxes_in(tc.m0 + 128, G.M);
-        const int b0 = boxes_in(tc.n0, G.N), b1 = boxes_in(tc.n0 + 128, G.N);
+        // A tile with at most 128 columns in range runs N = 128 MMAs: each CTA then stages
+        // 64 columns of B (rank r: [n0 + 64r, +64)), one 64-wide box, instead of 128.
+        const bool narrow = G.N - tc.n0 <= 128;
+        const int b0 = narrow ? 1 : boxes_in(tc.n0, G.N);
+        const int b1 = narrow ? (tc.n0 + 64 < G.N ? 1 : 0) : boxes_in(tc.n0 + 128, G.N);
         // Per 64-wide K box, a K-major half with any row in range loads one box of 128 rows
         // (a_box / b_box >= 128) or one 64-row box per 64 rows in range.  An MN-major B half
         // loads one box per 64 columns in range, each holding the stage's K rows (b_box =
@@ -725,12 +729,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         auto loads = [](int units, int box) { return box >= 128 ? (units ? 1 : 0) : units; };
         auto rows = [](int box) { return box >= 128 ? box : 64; };
         const int my_a = loads(rank ? a1 : a0, G.a_box);
-        const int my_b = B_MN ? (rank ? b1 : b0) : loads(rank ? b1 : b0, G.b_box);
+        const int my_b = (B_MN || narrow) ? (rank ? b1 : b0) : loads(rank ? b1 : b0, G.b_box);
         const uint32_t a_bytes_k = static_cast<uint32_t>((loads(a0, G.a_box) + loads(a1, G.a_box)) * rows(G.a_box) * 128);
         const uint32_t b_bytes_k = static_cast<uint32_t>(
-            B_MN ? (b0 + b1) * 64 * 128 : (loads(b0, G.b_box) + loads(b1, G.b_box)) * rows(G.b_box) * 128);
+            (B_MN || narrow) ? (b0 + b1) * 64 * 128 : (loads(b0, G.b_box) + loads(b1, G.b_box)) * rows(G.b_box) * 128);
         const int row0 = tc.m0 + 128 * static_cast<int>(rank);
-        const int col0 = tc.n0 + 128 * static_cast<int>(rank);
+        const int col0 = tc.n0 + (narrow ? 64 : 128) * static_cast<int>(rank);
+        const CUtensorMap* map_b = narrow ? G.map_b_narrow : G.map_b;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait_bounded(bar(&ctrl->empty[stage]), phase ^ 1u, abort_flag,
                                       WAIT_LIMIT_NS)) {
@@ -757,7 +762,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             }
             if (!B_MN) {
               for (int q = 0; q < my_b; ++q) {
-                ptx::tma_load_3d_pair(b_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, G.map_b, fb_leader,
+                ptx::tma_load_3d_pair(b_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, map_b, fb_leader,
                                       k0 + 64 * kq, col0 + 64 * q, tc.b);
               }
             }
@@ -765,7 +770,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if (B_MN) {
             for (int kq = 0; kq < b_k_loads; ++kq) {
               for (int q = 0; q < my_b; ++q) {
-                ptx::tma_load_3d_pair(b_dst + q * 2 * BOX_BYTES + kq * BOX_BYTES, G.map_b, fb_leader,
+                ptx::tma_load_3d_pair(b_dst + q * 2 * BOX_BYTES + kq * BOX_BYTES, map_b, fb_leader,
                                       col0 + 64 * q, k0 + 64 * kq, tc.b);
               }
             }
@@ -802,11 +807,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      const uint32_t idesc = ptx::idesc_f16(256, 256, !FP16, B_MN);
+      const uint32_t idesc_wide = ptx::idesc_f16(256, 256, !FP16, B_MN);
+      const uint32_t idesc_narrow = ptx::idesc_f16(256, 128, !FP16, B_MN);
       for (int64_t t = pair; t < total_tiles && ok; t += npairs, ++local) {
         const TileCoord tc = decode_tile<256>(groups, ng, t);
         const GemmGroup& G = groups[tc.g];
         const int kblocks = (G.K + BK2 - 1) / BK2;
+        // at most 128 columns in range: N = 128, each CTA's B holds 64 of them
+        const uint32_t idesc = G.N - tc.n0 <= 128 ? idesc_narrow : idesc_wide;
         const int acc = local & 1;
         const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
         if (!ptx::mbar_wait_bounded(bar(&ctrl->acc_empty[acc]), acc_phase ^ 1u, abort_flag,

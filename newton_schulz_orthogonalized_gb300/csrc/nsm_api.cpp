@@ -702,6 +702,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       g.b_box = st.b_mn ? (pair ? 128 : 64) : (pair ? 128 : 256);
       g.map_a = dmap(c, st.a_buf, g.a_box);
       g.map_b = dmap(c, st.b_buf, g.b_box);
+      g.map_b_narrow = st.b_mn ? g.map_b : dmap(c, st.b_buf, 64);
       const bool out_x = st.out_buf < MM0;
       g.out = buf_base(st.out_buf, c);
       // TMA stores write whole 16-byte units of a row: only for rows of a multiple of 8
@@ -1341,7 +1342,7 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   if (aux && ranges_overlap(aux, size_t(M) * ldx * 2, out, size_t(M) * ldo * 2))
     return fail(NSM_ERR_ARG, "aux must not overlap out");
   struct Blob {
-    CUtensorMap ma, mb, mo;
+    CUtensorMap ma, mb, mo, mbn;
     GemmGroup g;
   };
   static_assert(sizeof(Blob) <= 1024, "scratch blob");
@@ -1354,6 +1355,10 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   if (b_mn_major) rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, N, K, ldb, 1, nullptr, nullptr, b_box);
   else rc = encode_map(&blob.mb, const_cast<void*>(b), fp16 != 0, K, N, ldb, 1, nullptr, nullptr, b_box);
   if (rc != NSM_OK) return rc;
+  if (!b_mn_major) {
+    rc = encode_map(&blob.mbn, const_cast<void*>(b), fp16 != 0, K, N, ldb, 1, nullptr, nullptr, 64);
+    if (rc != NSM_OK) return rc;
+  }
   // TMA stores write whole 16-byte units of a row: only for rows of a multiple of 8
   const bool tma_store = N % 8 == 0;
   if (tma_store) {
@@ -1364,6 +1369,7 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   GemmGroup& g = blob.g;
   g.map_a = &d->ma;
   g.map_b = &d->mb;
+  g.map_b_narrow = b_mn_major ? &d->mb : &d->mbn;
   g.map_out = tma_store ? &d->mo : nullptr;
   g.out = out;
   g.aux = aux;
@@ -1416,7 +1422,7 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
 }
 
 size_t nsm_gemm_scratch_bytes(int M, int N, int flags) {
-  size_t b = 3 * sizeof(CUtensorMap) + sizeof(GemmGroup);
+  size_t b = 4 * sizeof(CUtensorMap) + sizeof(GemmGroup);
   if ((flags & NSM_GEMM_SYMMETRIC) && M > 0 && M == N)
     b += upper_tiles(M, (flags & NSM_GEMM_PAIR) ? 256 : 128).size() * sizeof(int32_t);
   return align_up(b, 128);

@@ -73,8 +73,10 @@ struct GemmGroup {
   int32_t a_box, b_box;  // rows per TMA box of map_a / map_b (64, 128 or 256)
   const CUtensorMap* map_out;  // the output in 32 x 32 boxes with 64-byte swizzle (TMA stores);
                                // NULL when N is not a multiple of 8 (rows of whole 16-byte units)
+  const CUtensorMap* map_b_narrow;  // B in 64-row boxes (K-major B; MN-major: map_b): the 2-SM
+                                    // kernel's tiles with at most 128 columns in range
 };
-static_assert(sizeof(GemmGroup) == 120, "GemmGroup layout");
+static_assert(sizeof(GemmGroup) == 128, "GemmGroup layout");
 
 struct GemmLaunch {
   const GemmGroup* groups;  // device array

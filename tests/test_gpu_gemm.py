@@ -55,6 +55,11 @@ CASES = [
     (64, 1000, 64, True, False, 0.0),
     (192, 192, 192, False, True, 3.4445),
     (384, 384, 4096, False, True, 0.0),
+    # the expert order of the Split/MoE table: the last column tile holds 128 of 256
+    # columns, and the 2-SM kernel runs it as N = 128 MMAs (64 columns of B per CTA)
+    (1408, 1408, 704, False, False, 0.0),
+    (256, 1408, 512, True, True, 0.0),
+    (272, 72, 136, True, False, 0.0),
 ]
 
 
@@ -137,7 +142,8 @@ def test_gemm_rejects_bad_arguments(nsm):
     assert e.value.code == nsm.NSM_ERR_ALIGN
 
 
-SYM_CASES = [(128, 64), (200, 72), (256, 256), (384, 1024), (1000, 136), (64, 64), (3, 8), (520, 4096)]
+SYM_CASES = [(128, 64), (200, 72), (256, 256), (384, 1024), (1000, 136), (64, 64), (3, 8), (520, 4096),
+             (1408, 2048)]
 
 
 @pytest.mark.parametrize("pair", [False, True])
