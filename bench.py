@@ -383,8 +383,9 @@ def _e2e(nsm, S, stream, reps):
     """The step end to end through the public API with host buffers: every step copies
     its bf16 grads (and the AdamW group's) host -> device from pinned memory, runs the
     step, and reads back the bf16 copy of the updated Muon parameters that the step
-    writes.  Two copy streams and double-buffered device buffers let step k's copies
-    overlap steps k-1 and k+1.  Every copy and every step is bracketed by events on its
+    writes.  Two copy streams and triple-buffered device buffers let the uploads run up
+    to two steps ahead of the compute and the read-back one step behind it, so a slow
+    copy has a step of slack.  Every copy and every step is bracketed by events on its
     own stream, so the line records where the time went."""
     import torch
     dev = S.dev
@@ -395,13 +396,14 @@ def _e2e(nsm, S, stream, reps):
     h_grads = torch.empty(S.total, dtype=torch.bfloat16, pin_memory=True)
     h_grads.copy_(S.grads.cpu())
     h_out = torch.empty(S.total, dtype=torch.bfloat16, pin_memory=True)
-    d_grads = [S.grads, torch.empty_like(S.grads)]
-    d_out = [torch.empty(S.total, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    nbuf = 3
+    d_grads = [S.grads] + [torch.empty_like(S.grads) for _ in range(nbuf - 1)]
+    d_out = [torch.empty(S.total, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
     h_agrads = d_agrads = None
     if S.adam is not None:
         h_agrads = torch.empty(S.adam[0].numel(), dtype=torch.bfloat16, pin_memory=True)
         h_agrads.copy_(S.adam[0].cpu())
-        d_agrads = [S.adam[0], torch.empty_like(S.adam[0])]
+        d_agrads = [S.adam[0]] + [torch.empty_like(S.adam[0]) for _ in range(nbuf - 1)]
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     def upload(slot):
@@ -416,26 +418,28 @@ def _e2e(nsm, S, stream, reps):
         torch.cuda.synchronize()
         e0, e1 = ev(), ev()
         e0.record(h2d)
-        with torch.cuda.stream(h2d):
-            up[0][0].record(h2d)
-            upload(0)
-            up[0][1].record(h2d)
+
+        def issue_upload(j):
+            with torch.cuda.stream(h2d):
+                if j >= nbuf:
+                    h2d.wait_event(cp[j - nbuf][1])  # step j - nbuf is done with the slot
+                up[j][0].record(h2d)
+                upload(j % nbuf)
+                up[j][1].record(h2d)
+
+        for j in range(min(nbuf - 1, reps)):
+            issue_upload(j)
         for k in range(reps):
-            cur, nxt = k % 2, (k + 1) % 2
+            cur = k % nbuf
             stream.wait_event(up[k][1])
-            if k >= 2:
-                stream.wait_event(dn[k - 2][1])  # step k-2's result has left d_out[cur]
+            if k >= nbuf:
+                stream.wait_event(dn[k - nbuf][1])  # step k - nbuf's result has left d_out[cur]
             cp[k][0].record(stream)
             S.step(nsm, stream, grads=d_grads[cur], params_bf16=d_out[cur],
                    adam_grads=None if d_agrads is None else d_agrads[cur])
             cp[k][1].record(stream)
-            if k + 1 < reps:
-                with torch.cuda.stream(h2d):
-                    if k >= 1:
-                        h2d.wait_event(cp[k - 1][1])  # step k-1 is done with d_grads[nxt]
-                    up[k + 1][0].record(h2d)
-                    upload(nxt)
-                    up[k + 1][1].record(h2d)
+            if k + nbuf - 1 < reps:
+                issue_upload(k + nbuf - 1)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(cp[k][1])
                 dn[k][0].record(d2h)
@@ -461,7 +465,7 @@ def _e2e(nsm, S, stream, reps):
     res = {"value": med["ms_per_step"], "unit": "ms",
            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": S.total * 2,
            "steps": reps, "statistic": "median of 3 timed passes",
-           "overlap": "copies on two streams, double-buffered",
+           "overlap": "copies on two streams, triple-buffered (uploads up to two steps ahead)",
            "breakdown": {k: med[k] for k in med if k != "ms_per_step"},
            "h2d_gbs": h2d_bytes / (med["h2d_ms_per_step"] * 1e-3) / 1e9,
            "d2h_gbs": S.total * 2 / (med["d2h_ms_per_step"] * 1e-3) / 1e9,
@@ -470,6 +474,33 @@ def _e2e(nsm, S, stream, reps):
     res["bound"] = max(("compute", med["compute_ms_per_step"]), ("h2d", med["h2d_ms_per_step"]),
                        ("d2h", med["d2h_ms_per_step"]), key=lambda t: t[1])[0]
     return res
+
+
+def _graph_steps(nsm, S, steps):
+    """Device ms per step of the step captured in a CUDA graph (10 steps per graph) and
+    replayed: the launch-bound small tables' remedy (the plan is cached first, so a
+    captured step launches kernels only)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        S.step(nsm, side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(10):
+            S.step(nsm, side)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // 10)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (10 * reps)
 
 
 def _other_configs(nsm, names, method, dev, stream, peaks):
@@ -489,7 +520,9 @@ def _other_configs(nsm, names, method, dev, stream, peaks):
             if nsm.device_status() != nsm.NSM_OK:
                 raise RuntimeError("a bounded device wait expired")
             kb = _kernels_block(per_kind, steps, peaks)
+            graph_ms = _graph_steps(nsm, S, 50) if wl.muon_elements < 1e9 else None
             out[name] = {"ms_per_step": ms, "steps": steps, "matrices": len(wl.muon_shapes),
+                         "graph_ms_per_step": graph_ms,
                          "muon_elements": wl.muon_elements, "adam_elements": wl.adam_elements,
                          "gpu_launches_per_step": launches / steps,
                          "gemm_frac_executed": kb.get("k_ns_gemm", {}).get("frac"),
