@@ -165,3 +165,49 @@ def test_status_selftest_validation_without_gpu(nsm):
     L = nsm.lib()
     assert L.nsm_status_selftest(0, None) == nsm.NSM_ERR_ARG
     assert L.nsm_status_selftest(2000001, None) == nsm.NSM_ERR_ARG
+
+
+def test_options_set_get_and_reject(nsm):
+    # host-only: the defaults, a round trip, and validation (no GPU call is made)
+    assert nsm.get_option(nsm.OPT_PAIR_KERNELS) == 1
+    assert nsm.get_option(nsm.OPT_SMALL_KERNEL) == 1
+    assert nsm.get_option(nsm.OPT_PDL) == 0
+    nsm.set_option(nsm.OPT_PDL, 1)
+    try:
+        assert nsm.get_option(nsm.OPT_PDL) == 1
+    finally:
+        nsm.set_option(nsm.OPT_PDL, 0)
+    with pytest.raises(nsm.NsmError) as e:
+        nsm.set_option(nsm.OPT_PDL, 2)
+    assert e.value.code == nsm.NSM_ERR_ARG
+    with pytest.raises(nsm.NsmError):
+        nsm.set_option(99, 1)
+    with pytest.raises(nsm.NsmError):
+        nsm.get_option(99)
+
+
+@pytest.mark.parametrize("method", ["gram", "standard", "standard_bf16"])
+def test_workspace_iterate_layout(nsm, method):
+    # every m x m block lies inside the workspace, blocks of one buffer do not overlap,
+    # matrices of the same working shape share the block size, and the small-matrix
+    # kernel's matrices report m = 0 (their iterates stay in shared memory)
+    shapes = [(256, 512), (512, 256), (130, 260), (64, 1000), (1024, 1024), (300, 520), (520, 300)]
+    total = nsm.workspace_bytes(shapes, method)
+    nbuf = nsm.mm_buffers(method)
+    for b in range(nbuf):
+        spans = []
+        for i, (r, c) in enumerate(shapes):
+            off, m, ld = nsm.workspace_iterate(shapes, i, b, method)
+            if min(r, c) <= 128:
+                assert m == 0
+                continue
+            assert m == min(r, c) and ld >= m and ld % 64 == 0
+            assert off % 2 == 0 and off + m * ld * 2 <= total
+            spans.append((off, off + m * ld * 2))
+        spans.sort()
+        for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+            assert a1 <= b0
+    with pytest.raises(nsm.NsmError):
+        nsm.workspace_iterate(shapes, 0, nbuf, method)
+    with pytest.raises(nsm.NsmError):
+        nsm.workspace_iterate(shapes, len(shapes), 0, method)
