@@ -652,7 +652,7 @@ __device__ __forceinline__ int boxes_in(int start, int limit) {
   return left <= 0 ? 0 : (left > 64 ? 2 : 1);
 }
 
-template <bool B_MN, bool FP16, bool HAS_AUX>
+template <bool B_MN, bool FP16, bool HAS_AUX, bool NARROW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_ns_gemm_pair(const GemmGroup* __restrict__ groups, int ng, int64_t total_tiles, float alpha,
                    float beta, float diag, int* status) {
@@ -718,8 +718,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         // boxes each CTA loads; the leader expects both CTAs' bytes
         const int a0 = boxes_in(tc.m0, G.M), a1 = boxes_in(tc.m0 + 128, G.M);
         // A tile with at most 128 columns in range runs N = 128 MMAs: each CTA then stages
-        // 64 columns of B (rank r: [n0 + 64r, +64)), one 64-wide box, instead of 128.
-        const bool narrow = G.N - tc.n0 <= 128;
+        // 64 columns of B (rank r: [n0 + 64r, +64)), one 64-wide box, instead of 128.  Only
+        // the instance for launches that have such tiles (NARROW) tests for them.
+        const bool narrow = NARROW && G.N - tc.n0 <= 128;
         const int b0 = narrow ? 1 : boxes_in(tc.n0, G.N);
         const int b1 = narrow ? (tc.n0 + 64 < G.N ? 1 : 0) : boxes_in(tc.n0 + 128, G.N);
         // Per 64-wide K box, a K-major half with any row in range loads one box of 128 rows
@@ -814,7 +815,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const GemmGroup& G = groups[tc.g];
         const int kblocks = (G.K + BK2 - 1) / BK2;
         // at most 128 columns in range: N = 128, each CTA's B holds 64 of them
-        const uint32_t idesc = G.N - tc.n0 <= 128 ? idesc_narrow : idesc_wide;
+        const uint32_t idesc = (NARROW && G.N - tc.n0 <= 128) ? idesc_narrow : idesc_wide;
         const int acc = local & 1;
         const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
         if (!ptx::mbar_wait_bounded(bar(&ctrl->acc_empty[acc]), acc_phase ^ 1u, abort_flag,
@@ -930,48 +931,55 @@ cudaError_t set_smem_once(K kernel, size_t bytes, std::atomic<uint64_t>& done) {
   return cudaSuccess;
 }
 
+template <bool B_MN, bool FP16, bool HAS_AUX, bool NARROW>
+cudaError_t launch_pair(const GemmLaunch& l, int num_sms, cudaStream_t stream, int* status) {
+  static std::atomic<uint64_t> done{0};
+  static std::atomic<int> max_clusters[64];
+  cudaError_t e = set_smem_once(k_ns_gemm_pair<B_MN, FP16, HAS_AUX, NARROW>, S2_SMEM, done);
+  if (e != cudaSuccess) return e;
+  // as many pairs as can be resident at once (a GPC with an odd number of free SMs
+  // cannot host a cluster of two)
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int resident = (dev >= 0 && dev < 64) ? max_clusters[dev].load() : 0;
+  if (resident <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = S2_SMEM;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&resident, k_ns_gemm_pair<B_MN, FP16, HAS_AUX, NARROW>, &cfg) != cudaSuccess ||
+        resident <= 0) {
+      cudaGetLastError();
+      resident = num_sms / 2;
+    }
+    if (dev >= 0 && dev < 64) max_clusters[dev].store(resident);
+  }
+  const int64_t cap = resident < num_sms / 2 ? resident : num_sms / 2;
+  const int64_t pairs = l.total_tiles < cap ? l.total_tiles : cap;
+  if (pairs <= 0) return cudaSuccess;
+  if (const cudaError_t e_launch = launch_ordered(kOverlapGemmLaunch, k_ns_gemm_pair<B_MN, FP16, HAS_AUX, NARROW>,
+                                              dim3(static_cast<unsigned>(2 * pairs)), dim3(NUM_THREADS), S2_SMEM,
+                                              stream, l.groups, l.num_groups, l.total_tiles, l.alpha, l.beta, l.diag,
+                                              status))
+    return e_launch;
+  return cudaGetLastError();
+}
+
 template <bool B_MN, bool FP16, bool HAS_AUX>
 cudaError_t launch_typed(const GemmLaunch& l, int num_sms, cudaStream_t stream) {
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   if (l.pair) {
-    static std::atomic<uint64_t> done{0};
-    static std::atomic<int> max_clusters[64];
-    cudaError_t e = set_smem_once(k_ns_gemm_pair<B_MN, FP16, HAS_AUX>, S2_SMEM, done);
-    if (e != cudaSuccess) return e;
-    // as many pairs as can be resident at once (a GPC with an odd number of free SMs
-    // cannot host a cluster of two)
-    int dev = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    int resident = (dev >= 0 && dev < 64) ? max_clusters[dev].load() : 0;
-    if (resident <= 0) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
-      cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-      cfg.dynamicSmemBytes = S2_SMEM;
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = 2;
-      attr.val.clusterDim.y = 1;
-      attr.val.clusterDim.z = 1;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&resident, k_ns_gemm_pair<B_MN, FP16, HAS_AUX>, &cfg) != cudaSuccess ||
-          resident <= 0) {
-        cudaGetLastError();
-        resident = num_sms / 2;
-      }
-      if (dev >= 0 && dev < 64) max_clusters[dev].store(resident);
-    }
-    const int64_t cap = resident < num_sms / 2 ? resident : num_sms / 2;
-    const int64_t pairs = l.total_tiles < cap ? l.total_tiles : cap;
-    if (pairs <= 0) return cudaSuccess;
-    if (const cudaError_t e_launch = launch_ordered(kOverlapGemmLaunch, k_ns_gemm_pair<B_MN, FP16, HAS_AUX>, dim3(static_cast<unsigned>(2 * pairs)),
-                                                dim3(NUM_THREADS), S2_SMEM, stream, l.groups, l.num_groups,
-                                                l.total_tiles, l.alpha, l.beta, l.diag, status))
-      return e_launch;
-    return cudaGetLastError();
+    return l.narrow ? launch_pair<B_MN, FP16, HAS_AUX, true>(l, num_sms, stream, status)
+                    : launch_pair<B_MN, FP16, HAS_AUX, false>(l, num_sms, stream, status);
   }
   static std::atomic<uint64_t> done{0};
   cudaError_t e = set_smem_once(k_ns_gemm<B_MN, FP16, HAS_AUX>, S1_SMEM, done);

@@ -742,6 +742,10 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     l.has_aux = st.aux_buf >= 0 ? 1 : 0;
     l.fp16 = P.x_fp16 ? 1 : 0;
     l.pair = pair ? 1 : 0;
+    for (int j = 0; j < nbig && pair; ++j) {
+      const int r = gs[j].N % 256;
+      if (r != 0 && r <= 128) l.narrow = 1;
+    }
     l.total_tiles = tiles;
     l.alpha = st.alpha;
     l.beta = st.beta;
@@ -1402,6 +1406,7 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   l.has_aux = aux ? 1 : 0;
   l.fp16 = fp16 ? 1 : 0;
   l.pair = pair ? 1 : 0;
+  l.narrow = (pair && N % 256 != 0 && N % 256 <= 128) ? 1 : 0;
   l.total_tiles = symmetric ? int64_t(sym_tiles.size()) : int64_t(g.tiles_m) * g.tiles_n;
   l.alpha = alpha;
   l.beta = aux ? beta : 0.f;

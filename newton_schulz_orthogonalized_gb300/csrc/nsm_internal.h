@@ -85,6 +85,7 @@ struct GemmLaunch {
   int32_t has_aux;
   int32_t fp16;             // 1: operands/outputs are fp16, else bf16
   int32_t pair;             // 1: 2-SM kernel on 256 x 256 tiles (groups laid out for it)
+  int32_t narrow;           // 1 (pair only): some tile has at most 128 columns in range
   int64_t total_tiles;
   float alpha, beta, diag;
   double flops;             // flops the tensor cores execute (whole tiles)
