@@ -235,6 +235,25 @@ def _time_oracle_matrix(wl, method, sh, index):
     return time.perf_counter() - t0
 
 
+def _time_oracle_adamw(wl, max_elems=16 * 1024 * 1024):
+    """Seconds the oracle's AdamW takes on the workload's whole AdamW group, timed on up to
+    max_elems of it and scaled linearly (every element costs the same); 0 without one."""
+    import numpy as np
+    import oracle
+    import synth
+    n = wl.adam_elements
+    if not n:
+        return 0.0
+    k = min(n, max_elems)
+    g16, p = synth.make_adam_group(wl, "cpu")
+    g = g16[:k].double().numpy()
+    pp = p[:k].double().numpy()
+    z = np.zeros(k)
+    t0 = time.perf_counter()
+    oracle.adamw_step(g, pp, z, z, 3e-4, 0.9, 0.95, 1e-10, wl.wd, 1)
+    return (time.perf_counter() - t0) * n / k
+
+
 def cpu_oracle_sample(wl, method, budget_s=30.0):
     """Times the float64 oracle (the exact iteration) on one matrix of each distinct shape
     of the workload, smallest shapes first, until the budget is spent (at least one); the
@@ -252,11 +271,14 @@ def cpu_oracle_sample(wl, method, budget_s=30.0):
         spent += t
     covered = sum(cnt for sh, _, cnt in shapes if sh in times)
     est = sum(cnt * times[sh] for sh, _, cnt in shapes if sh in times) * len(wl.muon_shapes) / covered
+    adam = _time_oracle_adamw(wl)
     desc = (f"oracle.muon_step ({method}, exact float64 iteration) on one matrix of each of "
             f"{len(times)} of the {len(shapes)} distinct shapes "
             f"({', '.join(f'{r}x{c} {times[(r, c)]:.2f} s' for (r, c) in times)}); the full "
-            f"{len(wl.muon_shapes)}-matrix step is extrapolated as the sum over shapes of count x time")
-    return est * 1e3, desc
+            f"{len(wl.muon_shapes)}-matrix step is extrapolated as the sum over shapes of count x time"
+            + (f"; plus oracle.adamw_step on the {wl.adam_elements}-element AdamW group ({adam:.2f} s, "
+               f"timed on up to 16M elements and scaled)" if wl.adam_elements else ""))
+    return (est + adam) * 1e3, desc
 
 
 def run_reference(args):
@@ -268,14 +290,16 @@ def run_reference(args):
     shapes = _shape_counts(wl)
     latest = {}
     vals = []
+    adam = 0.0
     for k in range(args.warmup + args.steps):
         if k == 0:
             for sh, idx, _ in shapes:
                 latest[sh] = _time_oracle_matrix(wl, args.method, sh, idx)
+            adam = _time_oracle_adamw(wl)
         else:
             sh, idx, _ = shapes[(k - 1) % len(shapes)]
             latest[sh] = _time_oracle_matrix(wl, args.method, sh, idx)
-        ms = 1e3 * sum(cnt * latest[sh] for sh, _, cnt in shapes)
+        ms = 1e3 * (sum(cnt * latest[sh] for sh, _, cnt in shapes) + adam)
         if k >= args.warmup:
             vals.append(ms)
     value = statistics.median(vals)
@@ -283,7 +307,9 @@ def run_reference(args):
     desc = (f"oracle.muon_step ({args.method}, exact float64 iteration): the first step times one "
             f"matrix of each of the {len(shapes)} distinct shapes, every later step re-times one "
             f"shape in turn; each step reports the sum over shapes of count x latest time "
-            f"(median of {args.steps} timed steps)")
+            f"(median of {args.steps} timed steps)"
+            + (f", plus oracle.adamw_step on the {wl.adam_elements}-element AdamW group timed once "
+               f"({adam:.2f} s)" if wl.adam_elements else ""))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "ms", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value,
