@@ -284,15 +284,17 @@ int nsm_last_launch_count(void);
 
 /* Process-wide launch options.  They select between the library's own equivalent paths,
  * so that the paths can be compared with one another; every value gives the same
- * results.  A call made after a change uses the new value.  nsm_set_option returns
- * NSM_ERR_ARG for an unknown option or value; nsm_get_option returns the current value
- * (NSM_ERR_ARG for an unknown option).  Not to be changed while another host thread is
- * inside a library call. */
+ * results.  A call made after a change uses the new value.  Values are 0 or 1 (0 to 2
+ * for NSM_OPT_PDL); nsm_set_option returns NSM_ERR_ARG for an unknown option or value;
+ * nsm_get_option returns the current value (NSM_ERR_ARG for an unknown option).  Not to
+ * be changed while another host thread is inside a library call. */
 #define NSM_OPT_PAIR_KERNELS 1  /* 1 (default): 2-SM GEMM kernel where it pays; 0: 1-CTA kernel only */
 #define NSM_OPT_SMALL_KERNEL 2  /* 1 (default): chains of m <= 128 matrices in k_ns_small;
                                    0: those matrices go through the grouped launches */
-#define NSM_OPT_PDL          3  /* 0 (default): plain stream order; 1: programmatic dependent
-                                   launch (a kernel's launch overlaps its predecessor's tail) */
+#define NSM_OPT_PDL          3  /* 0: plain stream order; 1: programmatic dependent launch (a
+                                   kernel's launch overlaps its predecessor's tail); 2 (default):
+                                   auto, the latter for tables of at most 2^25 elements, where
+                                   kernels are short enough for the launch latency to show */
 int nsm_set_option(int option, int value);
 int nsm_get_option(int option);
 

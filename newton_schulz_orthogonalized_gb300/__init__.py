@@ -367,7 +367,8 @@ OPT_PAIR_KERNELS, OPT_SMALL_KERNEL, OPT_PDL = 1, 2, 3
 
 def set_option(option: int, value: int) -> None:
     """Process-wide choice between the library's equivalent paths (for comparisons):
-    OPT_PAIR_KERNELS, OPT_SMALL_KERNEL (default 1) and OPT_PDL (default 0)."""
+    OPT_PAIR_KERNELS, OPT_SMALL_KERNEL (default 1) and OPT_PDL (0 off, 1 on, default 2:
+    on for tables of at most 2^25 elements)."""
     _check(lib().nsm_set_option(int(option), int(value)))
 
 

@@ -3,12 +3,13 @@
 // Every kernel of the library calls grid_dependency_sync() before it touches memory that
 // an earlier kernel of the stream writes (and before nothing else: barrier setup and
 // TMEM allocation may run early), then release_dependents().  Launched in plain stream
-// order (the default) both return at once.  With the NSM_OPT_PDL option set, kernels
-// are launched with programmatic stream serialisation: the next kernel's launch and
-// prologue then overlap the tail of the current one, and its own grid_dependency_sync()
-// waits until this grid has completed and its writes are visible.  Measured on one
-// GB300, the overlap made the 4-matrix table 13% faster (0.066 -> 0.058 ms) but the
-// GPT-2-small and Llama-7B tables 6-9% and 1.5% slower, so it is off by default.
+// order both return at once.  With programmatic dependent launch (the NSM_OPT_PDL
+// option), kernels are launched with programmatic stream serialisation: the next
+// kernel's launch and prologue then overlap the tail of the current one, and its own
+// grid_dependency_sync() waits until this grid has completed and its writes are visible.
+// Measured on one GB300, the overlap made the 4-matrix table 19% and the one-layer table
+// 8% faster, but the GPT-2-small and Llama-7B tables 4.5% and 1.5% slower, so by
+// default (auto) a call uses it only for tables of at most 2^25 elements.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -25,7 +26,7 @@ __device__ __forceinline__ void release_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-inline bool pdl_enabled() { return option_value(NSM_OPT_PDL) != 0; }
+inline bool pdl_enabled() { return pdl_for_launches(); }
 
 // `overlap` = false launches in plain stream order (the kernel's own dependency sync then
 // returns at once).

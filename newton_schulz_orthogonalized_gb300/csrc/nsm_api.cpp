@@ -254,7 +254,21 @@ struct Plan {
 // Process-wide launch options (nsm_set_option).  The 2-SM kernel is used where it pays
 // and matrices with m <= 128 run in the small-matrix kernel unless an option says
 // otherwise (for comparisons); programmatic dependent launch is off by default.
-std::atomic<int> g_opt_pair{1}, g_opt_small{1}, g_opt_pdl{0};
+std::atomic<int> g_opt_pair{1}, g_opt_small{1}, g_opt_pdl{2};
+
+// Programmatic dependent launch for the current call: on (1), off (0), or, in the auto
+// mode (2), on for tables of at most kPdlAutoElems elements, where each kernel is short
+// and the launch latency it hides is a visible share of the step.
+constexpr int64_t kPdlAutoElems = int64_t(1) << 25;
+thread_local bool t_pdl = false;
+
+struct PdlScope {
+  explicit PdlScope(int64_t elems) {
+    const int o = g_opt_pdl.load();
+    t_pdl = o == 1 || (o == 2 && elems <= kPdlAutoElems);
+  }
+  ~PdlScope() { t_pdl = false; }
+};
 
 bool pair_kernels_enabled() { return g_opt_pair.load() != 0; }
 bool small_kernel_enabled() { return g_opt_small.load() != 0; }
@@ -1045,6 +1059,8 @@ std::mutex& noalloc_mutex() {
 
 }  // namespace
 
+bool pdl_for_launches() { return t_pdl; }
+
 int option_value(int option) {
   switch (option) {
     case NSM_OPT_PAIR_KERNELS: return g_opt_pair.load();
@@ -1190,6 +1206,7 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
 
   Plan* P = get_plan(shapes, offsets, n, ns_method, ns_steps, workspace, workspace_bytes, &rc);
   if (!P) return rc;
+  const PdlScope pdl(P->elems);
   char* ws = P->ws;
   float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
   float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
@@ -1250,6 +1267,7 @@ int muon_orthogonalize(const void* in_bf16, void* out_bf16, const int64_t* offse
 
   Plan* P = get_plan(shapes, offsets, n, ns_method, ns_steps, workspace, workspace_bytes, &rc);
   if (!P) return rc;
+  const PdlScope pdl(P->elems);
   char* ws = P->ws;
   float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
   float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
@@ -1308,6 +1326,7 @@ int adamw_step(const void* grads, float* params, float* exp_avg, float* exp_avg_
   if (ranges_overlap(params, fb, exp_avg, fb) || ranges_overlap(params, fb, exp_avg_sq, fb) ||
       ranges_overlap(exp_avg, fb, exp_avg_sq, fb) || ranges_overlap(grads, size_t(numel) * 2, params, fb))
     return fail(NSM_ERR_ARG, "AdamW buffers must not overlap");
+  const PdlScope pdl(numel);
   const double bc1 = 1.0 - std::pow(double(beta1), double(step));
   const double bc2 = 1.0 - std::pow(double(beta2), double(step));
   cudaError_t e;
@@ -1417,6 +1436,7 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return fail_cuda(e, "device query");
+  const PdlScope pdl(int64_t(M) * N);
   {
     TimedLaunch t(stream, NSM_KIND_GEMM, l.flops);
     e = launch_gemm(l, num_sms, stream);
@@ -1478,6 +1498,7 @@ int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16, const int64_
     st->key = key;
   }
   Plan& P = *st->plan;
+  const PdlScope pdl(P.elems);
   char* ws = P.ws;
   float* partials = reinterpret_cast<float*>(ws + P.L.off_partials);
   float* scales = reinterpret_cast<float*>(ws + P.L.off_scales);
@@ -1529,7 +1550,8 @@ int nsm_device_status_detail(nsm_stream_t stream_, int* status_out, int* kernel_
 }
 
 int nsm_set_option(int option, int value) {
-  if (value != 0 && value != 1) return fail(NSM_ERR_ARG, "option value %d is not 0 or 1", value);
+  const int max_value = option == NSM_OPT_PDL ? 2 : 1;
+  if (value < 0 || value > max_value) return fail(NSM_ERR_ARG, "option value %d is not in [0, %d]", value, max_value);
   switch (option) {
     case NSM_OPT_PAIR_KERNELS: g_opt_pair.store(value); return NSM_OK;
     case NSM_OPT_SMALL_KERNEL: g_opt_small.store(value); return NSM_OK;

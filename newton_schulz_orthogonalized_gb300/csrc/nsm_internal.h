@@ -26,6 +26,9 @@ __device__ __forceinline__ void record_timeout(int* status, int kernel, int role
 
 // Values of the process-wide launch options (NSM_OPT_* of the public header).
 int option_value(int option);
+// Whether the launches of the current library call use programmatic dependent launch
+// (set per call from the NSM_OPT_PDL option and the size of the call's table).
+bool pdl_for_launches();
 
 // One matrix of a packed group, as the elementwise kernels see it.
 struct MatInfo {

@@ -171,15 +171,17 @@ def test_options_set_get_and_reject(nsm):
     # host-only: the defaults, a round trip, and validation (no GPU call is made)
     assert nsm.get_option(nsm.OPT_PAIR_KERNELS) == 1
     assert nsm.get_option(nsm.OPT_SMALL_KERNEL) == 1
-    assert nsm.get_option(nsm.OPT_PDL) == 0
+    assert nsm.get_option(nsm.OPT_PDL) == 2  # auto
     nsm.set_option(nsm.OPT_PDL, 1)
     try:
         assert nsm.get_option(nsm.OPT_PDL) == 1
     finally:
-        nsm.set_option(nsm.OPT_PDL, 0)
-    with pytest.raises(nsm.NsmError) as e:
         nsm.set_option(nsm.OPT_PDL, 2)
+    with pytest.raises(nsm.NsmError) as e:
+        nsm.set_option(nsm.OPT_PDL, 3)
     assert e.value.code == nsm.NSM_ERR_ARG
+    with pytest.raises(nsm.NsmError):
+        nsm.set_option(nsm.OPT_SMALL_KERNEL, 2)
     with pytest.raises(nsm.NsmError):
         nsm.set_option(99, 1)
     with pytest.raises(nsm.NsmError):

@@ -599,13 +599,14 @@ def _two_steps_each_form(nsm):
 def test_overlapped_launches_match_plain_order_bitwise(nsm):
     # With the PDL option every kernel is launched with programmatic stream serialisation
     # (each waits for the previous grid before touching its outputs): the same bits
-    assert nsm.get_option(nsm.OPT_PDL) == 0
-    plain = _two_steps_each_form(nsm)
-    nsm.set_option(nsm.OPT_PDL, 1)
+    default = nsm.get_option(nsm.OPT_PDL)
+    nsm.set_option(nsm.OPT_PDL, 0)
     try:
+        plain = _two_steps_each_form(nsm)
+        nsm.set_option(nsm.OPT_PDL, 1)
         overlapped = _two_steps_each_form(nsm)
     finally:
-        nsm.set_option(nsm.OPT_PDL, 0)
+        nsm.set_option(nsm.OPT_PDL, default)
     for method in plain:
         for a, b in zip(overlapped[method], plain[method]):
             assert torch.equal(a, b), method
