@@ -672,7 +672,7 @@ def run_ours(args):
             "traffic": _traffic_record(method, wl.name),
             "launches_timed": gemm_launches,
             "flops_per_launch": per_launch_flops,
-            "flops_counted": "executed: whole tiles, upper-triangle tiles of symmetric outputs",
+            "flops_counted": "executed: the tiles launched, clipped to the matrix edges; upper-triangle tiles of symmetric outputs",
             "ms_per_launch": per_launch_ms,
             "timing": "CUDA events around every launch, in a second timed pass of the same steps",
         },
