@@ -52,6 +52,8 @@ typedef struct CUstream_st* nsm_stream_t;
 #define NSM_ERR_CUDA      -7  /* a CUDA runtime/driver call failed */
 #define NSM_ERR_TIMEOUT   -8  /* a bounded in-kernel wait expired (nsm_device_status) */
 #define NSM_ERR_ARG       -9  /* any other invalid argument */
+#define NSM_ERR_BOUNDS   -10  /* (checked build) a kernel's bounds check failed and the
+                                 access was skipped (nsm_device_status) */
 
 /* Newton-Schulz methods [DSM §核心算子].  Every form accumulates in fp32 on the tensor
  * cores; they differ in the half precision the iterates are stored in. */
@@ -213,8 +215,9 @@ int nsm_gemm(const void* a, int lda, const void* b, int ldb, void* out, int ldo,
 size_t nsm_gemm_scratch_bytes(int M, int N, int flags);
 
 /* Synchronises `stream`, then reads and clears the device status word that kernels set
- * when a bounded wait expires.  *status_out = NSM_OK or NSM_ERR_TIMEOUT.  Returns
- * NSM_ERR_CUDA if the synchronisation itself reports an error. */
+ * when a bounded wait expires (or, in the checked build, when a bounds check fails).
+ * *status_out = NSM_OK, NSM_ERR_TIMEOUT or NSM_ERR_BOUNDS.  Returns NSM_ERR_CUDA if the
+ * synchronisation itself reports an error. */
 int nsm_device_status(nsm_stream_t stream, int* status_out);
 
 /* Where the first bounded wait that expired since the status word was last read gave up:
@@ -225,7 +228,11 @@ int nsm_device_status(nsm_stream_t stream, int* status_out);
 #define NSM_KERNEL_GEMM       1  /* k_ns_gemm: the 1-CTA grouped GEMM */
 #define NSM_KERNEL_GEMM_PAIR  2  /* k_ns_gemm_pair: the 2-SM grouped GEMM */
 #define NSM_KERNEL_SMALL      3  /* k_ns_small: whole chains of matrices with m <= 128 */
-#define NSM_KERNEL_SELFTEST   4  /* the kernel of nsm_status_selftest */
+#define NSM_KERNEL_SELFTEST   4  /* the kernels of nsm_status_selftest / nsm_bounds_selftest */
+#define NSM_KERNEL_MOMENTUM   5  /* k_momentum_norm (bounds checks only) */
+#define NSM_KERNEL_TO_CLASS   6  /* k_to_class (bounds checks only) */
+#define NSM_KERNEL_FROM_CLASS 7  /* k_from_class: apply or export (bounds checks only) */
+#define NSM_KERNEL_ADAMW      8  /* k_adamw (bounds checks only) */
 #define NSM_ROLE_PRODUCER     1  /* the thread issuing TMA loads */
 #define NSM_ROLE_MMA          2  /* the thread issuing tensor-core MMAs */
 #define NSM_ROLE_EPILOGUE     3  /* the epilogue warps draining TMEM */
@@ -241,11 +248,30 @@ int nsm_device_status(nsm_stream_t stream, int* status_out);
 #define NSM_SITE_XT_EMPTY     9  /* the MMA thread releasing an X' chunk (k_ns_small) */
 #define NSM_SITE_STORES_DONE 10  /* the previous pass's X' stores landing (k_ns_small) */
 #define NSM_SITE_SELFTEST    11  /* the self-test's barrier that nothing completes */
+/* Sites of the checked build's bounds checks (status NSM_ERR_BOUNDS).  A TMA box is in
+ * bounds when its first element lies inside the operand's matrix, its innermost
+ * coordinate is a whole number of 16-byte units and its batch index is one of the
+ * group's matrices; a plain access when every element it touches lies inside its
+ * matrix (in the natural layout, the slot or the flat AdamW group), 16-byte vectors on
+ * 16-byte boundaries. */
+#define NSM_SITE_TMA_A          12  /* TMA load of the A operand (GEMM kernels) */
+#define NSM_SITE_TMA_B          13  /* TMA load of the B operand (GEMM kernels) */
+#define NSM_SITE_AUX            14  /* epilogue load of the aux operand (GEMM kernels) */
+#define NSM_SITE_OUT            15  /* epilogue store of the output: TMA box or plain store */
+#define NSM_SITE_TMA_X_LOAD     16  /* TMA load of an X chunk (k_ns_small) */
+#define NSM_SITE_TMA_X_STORE    17  /* TMA store of an X' or O chunk (k_ns_small) */
+#define NSM_SITE_NATURAL_LOAD   18  /* load from the packed natural layout (G, M, p) */
+#define NSM_SITE_NATURAL_STORE  19  /* store to the packed natural layout (M, p, bf16 copy) */
+#define NSM_SITE_SLOT_LOAD      20  /* load from a matrix's slot in the working layout */
+#define NSM_SITE_SLOT_STORE     21  /* store to a matrix's slot in the working layout */
+#define NSM_SITE_FLAT           22  /* AdamW's access to its flat group */
+#define NSM_SITE_SELFTEST_BOUNDS 23 /* nsm_bounds_selftest's check of an index past its range */
 
 /* nsm_device_status with the location: synchronises `stream`, reads and clears the
- * status word.  *status_out = NSM_OK or NSM_ERR_TIMEOUT; on a timeout *kernel_out,
- * *role_out and *site_out are NSM_KERNEL_*, NSM_ROLE_* and NSM_SITE_* (0 otherwise; the
- * self-test kernel reports role 0).
+ * status word.  *status_out = NSM_OK, NSM_ERR_TIMEOUT or NSM_ERR_BOUNDS; then *kernel_out,
+ * *role_out and *site_out are NSM_KERNEL_*, NSM_ROLE_* and NSM_SITE_* (0 with NSM_OK; the
+ * self-test kernels and the elementwise kernels report role 0).  Only the first record
+ * since the word was last read is kept.
  * Any of the three location pointers may be NULL. */
 int nsm_device_status_detail(nsm_stream_t stream, int* status_out, int* kernel_out,
                              int* role_out, int* site_out);
@@ -257,6 +283,14 @@ int nsm_device_status_detail(nsm_stream_t stream, int* status_out, int* kernel_o
  * next nsm_device_status reports NSM_ERR_TIMEOUT (and clears it).  Returns NSM_ERR_ARG,
  * with nothing launched, for wait_us out of range. */
 int nsm_status_selftest(int wait_us, nsm_stream_t stream);
+
+/* Self-test of the checked build's bounds checks: launches one thread on `stream` that
+ * runs the bounds check the kernels use on the index one past the end of a one-element
+ * range, and makes no access at all.  In the checked build (NSM_OPT_BOUNDS_CHECKS = 1)
+ * the check fails and records NSM_ERR_BOUNDS with NSM_KERNEL_SELFTEST, role 0 and
+ * NSM_SITE_SELFTEST_BOUNDS; in the regular build the checks are compiled out and nothing
+ * is recorded.  Returns NSM_ERR_CUDA if the launch fails. */
+int nsm_bounds_selftest(nsm_stream_t stream);
 
 /* Kernel timing for profiling.  While enabled, every kernel launch of muon_step,
  * muon_orthogonalize, adamw_step and nsm_gemm is bracketed by CUDA events on the
@@ -295,6 +329,11 @@ int nsm_last_launch_count(void);
                                    kernel's launch overlaps its predecessor's tail); 2 (default):
                                    auto, the latter for tables of at most 2^25 elements, where
                                    kernels are short enough for the launch latency to show */
+#define NSM_OPT_BOUNDS_CHECKS 4 /* read only: 1 in the checked build (libnsmuon_checked.so),
+                                   whose kernels check every global access and TMA box
+                                   against its matrix before making it, record a failure
+                                   (NSM_ERR_BOUNDS) and skip the access; 0 in the regular
+                                   build.  nsm_set_option rejects it. */
 int nsm_set_option(int option, int value);
 int nsm_get_option(int option);
 

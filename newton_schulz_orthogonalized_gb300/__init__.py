@@ -20,7 +20,12 @@ from typing import Dict, Iterable, List, Optional, Sequence, Tuple
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libnsmuon.so")
+LIB_REGULAR = os.path.join(_HERE, "libnsmuon.so")
+# the bounds-checked build: every kernel tests each access to a matrix's elements before
+# making it, records a failure (NSM_ERR_BOUNDS) and skips the access
+LIB_CHECKED = os.path.join(_HERE, "libnsmuon_checked.so")
+# NSM_CHECKED=1 in the environment makes this process load the checked build
+LIB_PATH = LIB_CHECKED if os.environ.get("NSM_CHECKED") == "1" else LIB_REGULAR
 
 NSM_OK = 0
 NSM_ERR_NULL = -1
@@ -32,6 +37,7 @@ NSM_ERR_WORKSPACE = -6
 NSM_ERR_CUDA = -7
 NSM_ERR_TIMEOUT = -8
 NSM_ERR_ARG = -9
+NSM_ERR_BOUNDS = -10
 
 NS_METHODS = {"standard": 0, "gram": 1, "standard_bf16": 2}
 NS_METHOD_DEFAULT = "gram"
@@ -56,7 +62,8 @@ class NsmError(RuntimeError):
 
 
 def lib() -> ctypes.CDLL:
-    """Loads libnsmuon.so (built in-tree by ``__graft_entry__.build()``)."""
+    """Loads libnsmuon.so, or libnsmuon_checked.so when NSM_CHECKED=1 (both built in-tree
+    by ``__graft_entry__.build()``)."""
     global _lib
     if _lib is not None:
         return _lib
@@ -115,6 +122,8 @@ def lib() -> ctypes.CDLL:
     L.nsm_get_option.restype = ctypes.c_int
     L.nsm_status_selftest.argtypes = [ctypes.c_int, _vp]
     L.nsm_status_selftest.restype = ctypes.c_int
+    L.nsm_bounds_selftest.argtypes = [_vp]
+    L.nsm_bounds_selftest.restype = ctypes.c_int
     L.nsm_timing_enable.argtypes = [ctypes.c_int]
     L.nsm_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p,
                                   ctypes.POINTER(ctypes.c_double)]
@@ -344,7 +353,8 @@ def gemm(a, b, out, aux=None, b_mn_major: bool = False, alpha: float = 1.0, beta
 
 
 def device_status(stream=None) -> int:
-    """Synchronises the stream; returns NSM_OK or NSM_ERR_TIMEOUT (and clears it)."""
+    """Synchronises the stream; returns NSM_OK, NSM_ERR_TIMEOUT or (checked build)
+    NSM_ERR_BOUNDS, and clears the record."""
     v = ctypes.c_int(0)
     _check(lib().nsm_device_status(_stream_ptr(stream), ctypes.byref(v)))
     return v.value
@@ -352,8 +362,9 @@ def device_status(stream=None) -> int:
 
 def device_status_detail(stream=None) -> Tuple[int, int, int, int]:
     """Synchronises the stream; returns (status, kernel, role, site) of the first bounded
-    wait that expired since the last read (status NSM_OK and zeros when none), and clears
-    the record.  kernel/role/site are the NSM_KERNEL_* / NSM_ROLE_* / NSM_SITE_* codes."""
+    wait that expired, or (checked build) bounds test that failed, since the last read
+    (status NSM_OK and zeros when none), and clears the record.  kernel/role/site are the
+    NSM_KERNEL_* / NSM_ROLE_* / NSM_SITE_* codes of the C header."""
     v = [ctypes.c_int(0) for _ in range(4)]
     _check(lib().nsm_device_status_detail(_stream_ptr(stream), *[ctypes.byref(x) for x in v]))
     return tuple(x.value for x in v)
@@ -361,8 +372,9 @@ def device_status_detail(stream=None) -> Tuple[int, int, int, int]:
 
 NSM_KERNEL_GEMM, NSM_KERNEL_GEMM_PAIR, NSM_KERNEL_SMALL, NSM_KERNEL_SELFTEST = 1, 2, 3, 4
 NSM_SITE_SELFTEST = 11
+NSM_SITE_SELFTEST_BOUNDS = 23
 
-OPT_PAIR_KERNELS, OPT_SMALL_KERNEL, OPT_PDL = 1, 2, 3
+OPT_PAIR_KERNELS, OPT_SMALL_KERNEL, OPT_PDL, OPT_BOUNDS_CHECKS = 1, 2, 3, 4
 
 
 def set_option(option: int, value: int) -> None:
@@ -380,6 +392,18 @@ def status_selftest(wait_us: int = 20000, stream=None) -> None:
     """Launches one CTA whose bounded wait expires after wait_us and records a timeout in
     the device status word (read it with device_status)."""
     _check(lib().nsm_status_selftest(int(wait_us), _stream_ptr(stream)))
+
+
+def bounds_selftest(stream=None) -> None:
+    """Launches one thread that runs the kernels' bounds test on an index past its range
+    and makes no access: the checked build records NSM_ERR_BOUNDS (read it with
+    device_status_detail), the regular build nothing."""
+    _check(lib().nsm_bounds_selftest(_stream_ptr(stream)))
+
+
+def checked_build() -> bool:
+    """Whether the loaded library is the bounds-checked build."""
+    return get_option(OPT_BOUNDS_CHECKS) == 1
 
 
 def timing_enable(on: bool = True) -> None:

@@ -1,7 +1,10 @@
 """Builds libnsmuon.so in-tree with nvcc for sm_103a (no torch extension machinery).
 
 Each translation unit compiles in its own nvcc process (in parallel), then one link
-step makes the shared library next to this file.
+step makes the shared library next to this file.  The checked build,
+libnsmuon_checked.so, is the same sources compiled with NSM_CHECKED=1: its kernels test
+every access to a matrix's elements (global loads and stores, TMA boxes) against that
+matrix before making it, record a failure in the device status word and skip the access.
 """
 
 from __future__ import annotations
@@ -16,6 +19,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libnsmuon.so")
+LIB_CHECKED = os.path.join(HERE, "libnsmuon_checked.so")
 BUILD = os.path.join(ROOT, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -37,32 +41,50 @@ def _run(cmd):
     return proc.stdout
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
+def _jobs(checked: bool, ptxas_info: bool):
+    """(compile commands, objects, link command pieces, output) of one library."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    objs = []
-    cmds = []
+    out_dir = os.path.join(BUILD, "checked") if checked else BUILD
+    os.makedirs(out_dir, exist_ok=True)
+    defs = ["-DNSM_CHECKED=1"] if checked else []
+    objs, cmds = [], []
     for src in SOURCES:
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
-        cmd = [nvcc] + ARCH + COMMON + ["-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc] + ARCH + COMMON + defs + ["-c", os.path.join(CSRC, src), "-o", obj]
         if src.endswith(".cpp"):
             cmd += ["-x", "cu"]
         if ptxas_info and src.endswith(".cu"):
             cmd += ["-Xptxas", "-v"]
         cmds.append(cmd)
+    return cmds, objs, LIB_CHECKED if checked else LIB
+
+
+def _link(objs, lib):
+    tmp = lib + ".tmp"
+    _run([_nvcc()] + ARCH + ["-shared", "-o", tmp] + objs)
+    os.replace(tmp, lib)
+
+
+def build(verbose: bool = False, ptxas_info: bool = False, checked: bool = False,
+          both: bool = False) -> str:
+    """Builds libnsmuon.so (or, with checked, libnsmuon_checked.so; with both, the two
+    at once, their translation units compiled in parallel).  Returns the regular
+    library's path (the checked one's when only it is built)."""
+    variants = [False, True] if both else [checked]
+    jobs = [_jobs(c, ptxas_info) for c in variants]
+    cmds = [c for j in jobs for c in j[0]]
     with ThreadPoolExecutor(max_workers=len(cmds)) as ex:
         outs = list(ex.map(_run, cmds))
     if verbose:
         for o in outs:
             if o.strip():
                 print(o)
-    tmp = LIB + ".tmp"
-    _run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs)
-    os.replace(tmp, LIB)
-    return LIB
+    for _, objs, lib in jobs:
+        _link(objs, lib)
+    return jobs[0][2]
 
 
 if __name__ == "__main__":
-    build(verbose=True, ptxas_info="--ptxas" in sys.argv)
-    print(LIB)
+    print(build(verbose=True, ptxas_info="--ptxas" in sys.argv, checked="--checked" in sys.argv,
+                both="--both" in sys.argv))

@@ -128,13 +128,30 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
   return s;
 }
 
+// ---------------------------------------------------------------- bounds checks
+
+// Tests of the checked build (bounds_ok; compiled out otherwise).  natural_run: w
+// elements from element i of a matrix of len elements in the packed natural layout, whose
+// first element is element `base` of the buffer.  slot_run: w elements from (row, col) of
+// a matrix's slot (m rows of n elements, row stride ld).  Runs of 8 are 16-byte vectors
+// (8 x 16-bit, or 2 x 4 fp32 at the same index) and must start on a multiple of 8
+// elements.
+__device__ __forceinline__ bool natural_run(int64_t base, int64_t i, int w, int64_t len) {
+  return i >= 0 && i + w <= len && (w == 1 || ((base + i) & 7) == 0);
+}
+
+__device__ __forceinline__ bool slot_run(const MatInfo& mt, int row, int col, int w) {
+  return row >= 0 && row < mt.m && col >= 0 && col + w <= mt.n &&
+         (w == 1 || ((mt.slot + static_cast<int64_t>(row) * mt.ld + col) & 7) == 0);
+}
+
 // ---------------------------------------------------------------- momentum + norm
 
 template <bool HAS_M, bool NESTEROV>
 __global__ void __launch_bounds__(kThreads)
     k_momentum_norm(const __nv_bfloat16* __restrict__ grads, float* __restrict__ mom,
                     const MatInfo* __restrict__ mats, int nmats, int total_chunks,
-                    float* __restrict__ partials, float mu) {
+                    float* __restrict__ partials, float mu, int* status) {
   grid_dependency_sync();  // inputs come from the previous kernel of the stream
   release_dependents();
   __shared__ float scratch[kThreads / 32];
@@ -149,6 +166,8 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t nvec = (end - start) >> 3;
     for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
       const int64_t i = start + v * 8;
+      // G is read and M read and written at the same 8 elements
+      if (!bounds_ok(natural_run(mt.off, i, 8, len), status, NSM_KERNEL_MOMENTUM, 0, NSM_SITE_NATURAL_LOAD)) continue;
       float gf[8];
       unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(g + i)), gf);
       if (HAS_M) {
@@ -170,6 +189,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     for (int64_t i = start + nvec * 8 + threadIdx.x; i < end; i += kThreads) {
+      if (!bounds_ok(natural_run(mt.off, i, 1, len), status, NSM_KERNEL_MOMENTUM, 0, NSM_SITE_NATURAL_LOAD)) continue;
       const float gv = __bfloat162float(g[i]);
       if (HAS_M) {
         const float mn = fmaf(mu, m[i], gv);
@@ -246,7 +266,7 @@ template <bool TO_FP16, int MODE>
 __global__ void __launch_bounds__(kThreads)
     k_to_class(const __nv_bfloat16* __restrict__ grads, const float* __restrict__ mom, float mu,
                void* __restrict__ dst, const MatInfo* __restrict__ mats, int nmats,
-               int64_t total_tiles, const float* __restrict__ scales) {
+               int64_t total_tiles, const float* __restrict__ scales, int* status) {
   grid_dependency_sync();  // inputs come from the previous kernel of the stream
   release_dependents();
   __shared__ float tile[kTile][kTile + 1];
@@ -258,19 +278,23 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t d0 = mt.slot;
     const float sc = scales[tp.mi];
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
+    const int64_t len = static_cast<int64_t>(rows) * cols;
+    constexpr int K = NSM_KERNEL_TO_CLASS;
     if (!mt.transposed) {
       if ((mt.flags & kMatVec) && ld == cols) {
         // slot and natural layouts coincide: the matrix's k-th tile is its k-th run of
         // kTile^2 consecutive elements, streamed contiguously
         const int64_t base = (t - mt.tile_begin) * (kTile * kTile);
-        const int64_t len = static_cast<int64_t>(rows) * cols;
         for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
           const int64_t i = base + static_cast<int64_t>(j) * 8;
           if (i < len) {
             float f[8];
+            if (!bounds_ok(natural_run(mt.off, i, 8, len), status, K, 0, NSM_SITE_NATURAL_LOAD)) continue;
             load_u8<MODE>(g, m, i, mu, f);
 #pragma unroll
             for (int q = 0; q < 8; ++q) f[q] *= sc;
+            if (!bounds_ok(slot_run(mt, static_cast<int>(i / ld), static_cast<int>(i % ld), 8), status, K, 0,
+                           NSM_SITE_SLOT_STORE)) continue;
             store8<TO_FP16>(dst, d0 + i, f);
           }
         }
@@ -279,9 +303,12 @@ __global__ void __launch_bounds__(kThreads)
           const int r = tp.r0 + (j >> 3), c = tp.c0 + (j & 7) * 8;
           if (r < rows && c < cols) {
             float f[8];
-            load_u8<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu, f);
+            const int64_t i = static_cast<int64_t>(r) * cols + c;
+            if (!bounds_ok(natural_run(mt.off, i, 8, len), status, K, 0, NSM_SITE_NATURAL_LOAD)) continue;
+            load_u8<MODE>(g, m, i, mu, f);
 #pragma unroll
             for (int q = 0; q < 8; ++q) f[q] *= sc;
+            if (!bounds_ok(slot_run(mt, r, c, 8), status, K, 0, NSM_SITE_SLOT_STORE)) continue;
             store8<TO_FP16>(dst, d0 + static_cast<int64_t>(r) * ld + c, f);
           }
         }
@@ -289,7 +316,10 @@ __global__ void __launch_bounds__(kThreads)
         for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
           const int r = tp.r0 + (j >> 6), c = tp.c0 + (j & 63);
           if (r < rows && c < cols) {
-            const float v = load_u1<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu) * sc;
+            const int64_t i = static_cast<int64_t>(r) * cols + c;
+            if (!bounds_ok(natural_run(mt.off, i, 1, len), status, K, 0, NSM_SITE_NATURAL_LOAD)) continue;
+            const float v = load_u1<MODE>(g, m, i, mu) * sc;
+            if (!bounds_ok(slot_run(mt, r, c, 1), status, K, 0, NSM_SITE_SLOT_STORE)) continue;
             store_half<TO_FP16>(dst, d0 + static_cast<int64_t>(r) * ld + c, v);
           }
         }
@@ -301,7 +331,11 @@ __global__ void __launch_bounds__(kThreads)
           const int rr = j >> 3, cc = (j & 7) * 8;
           const int r = tp.r0 + rr, c = tp.c0 + cc;
           float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (r < rows && c < cols) load_u8<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu, f);
+          if (r < rows && c < cols &&
+              bounds_ok(natural_run(mt.off, static_cast<int64_t>(r) * cols + c, 8, len), status, K, 0,
+                        NSM_SITE_NATURAL_LOAD)) {
+            load_u8<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu, f);
+          }
 #pragma unroll
           for (int q = 0; q < 8; ++q) tile[rr][cc + q] = f[q];
         }
@@ -309,7 +343,7 @@ __global__ void __launch_bounds__(kThreads)
         for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
           const int cr = j >> 3, rc = (j & 7) * 8;  // slot row c0+cr, slot cols r0+rc..+7
           const int c = tp.c0 + cr, r = tp.r0 + rc;
-          if (c < cols && r < rows) {
+          if (c < cols && r < rows && bounds_ok(slot_run(mt, c, r, 8), status, K, 0, NSM_SITE_SLOT_STORE)) {
             float f[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) f[q] = tile[rc + q][cr] * sc;
@@ -320,13 +354,16 @@ __global__ void __launch_bounds__(kThreads)
         for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
           const int rr = j >> 6, cc = j & 63;
           const int r = tp.r0 + rr, c = tp.c0 + cc;
-          tile[rr][cc] = (r < rows && c < cols) ? load_u1<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu) : 0.f;
+          const bool in = r < rows && c < cols &&
+                          bounds_ok(natural_run(mt.off, static_cast<int64_t>(r) * cols + c, 1, len), status, K, 0,
+                                    NSM_SITE_NATURAL_LOAD);
+          tile[rr][cc] = in ? load_u1<MODE>(g, m, static_cast<int64_t>(r) * cols + c, mu) : 0.f;
         }
         __syncthreads();
         for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
           const int cr = j >> 6, rc = j & 63;
           const int c = tp.c0 + cr, r = tp.r0 + rc;
-          if (c < cols && r < rows) {
+          if (c < cols && r < rows && bounds_ok(slot_run(mt, c, r, 1), status, K, 0, NSM_SITE_SLOT_STORE)) {
             store_half<TO_FP16>(dst, d0 + static_cast<int64_t>(c) * ld + r, tile[rc][cr] * sc);
           }
         }
@@ -342,14 +379,19 @@ template <bool O_FP16, bool APPLY>
 __global__ void __launch_bounds__(kThreads)
     k_from_class(const void* __restrict__ o, float* __restrict__ params,
                  __nv_bfloat16* __restrict__ out, const MatInfo* __restrict__ mats, int nmats,
-                 int64_t total_tiles, float lr, float decay) {
+                 int64_t total_tiles, float lr, float decay, int* status) {
   grid_dependency_sync();  // inputs come from the previous kernel of the stream
   release_dependents();
   __shared__ float tile[kTile][kTile + 1];
+  constexpr int K = NSM_KERNEL_FROM_CLASS;
+  // p is read and written (and its bf16 copy written) at the same elements; the export
+  // only writes its bf16 output there
+  constexpr int kNatural = APPLY ? NSM_SITE_NATURAL_LOAD : NSM_SITE_NATURAL_STORE;
   for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
     const TilePos tp = tile_pos(mats, nmats, t);
     const MatInfo& mt = mats[tp.mi];
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
+    const int64_t len = static_cast<int64_t>(rows) * cols;
     const int64_t s0 = mt.slot;
     const float coef = lr * mt.scale;
     float* p = APPLY ? params + mt.off : nullptr;
@@ -361,7 +403,9 @@ __global__ void __launch_bounds__(kThreads)
           const int cc = j >> 3, rr = (j & 7) * 8;
           const int c = tp.c0 + cc, r = tp.r0 + rr;
           float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (c < cols && r < rows) load8<O_FP16>(o, s0 + static_cast<int64_t>(c) * ld + r, f);
+          if (c < cols && r < rows && bounds_ok(slot_run(mt, c, r, 8), status, K, 0, NSM_SITE_SLOT_LOAD)) {
+            load8<O_FP16>(o, s0 + static_cast<int64_t>(c) * ld + r, f);
+          }
 #pragma unroll
           for (int q = 0; q < 8; ++q) tile[rr + q][cc] = f[q];
         }
@@ -369,7 +413,8 @@ __global__ void __launch_bounds__(kThreads)
         for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
           const int cc = j >> 6, rr = j & 63;
           const int c = tp.c0 + cc, r = tp.r0 + rr;
-          tile[rr][cc] = (c < cols && r < rows) ? load_half<O_FP16>(o, s0 + static_cast<int64_t>(c) * ld + r) : 0.f;
+          const bool in = c < cols && r < rows && bounds_ok(slot_run(mt, c, r, 1), status, K, 0, NSM_SITE_SLOT_LOAD);
+          tile[rr][cc] = in ? load_half<O_FP16>(o, s0 + static_cast<int64_t>(c) * ld + r) : 0.f;
         }
       }
       __syncthreads();
@@ -378,11 +423,13 @@ __global__ void __launch_bounds__(kThreads)
       // slot and natural layouts coincide: the k-th tile is the k-th run of kTile^2
       // consecutive elements
       const int64_t base = (t - mt.tile_begin) * (kTile * kTile);
-      const int64_t len = static_cast<int64_t>(rows) * cols;
       for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
         const int64_t i = base + static_cast<int64_t>(j) * 8;
         if (i < len) {
           float f[8];
+          if (!bounds_ok(slot_run(mt, static_cast<int>(i / ld), static_cast<int>(i % ld), 8), status, K, 0,
+                         NSM_SITE_SLOT_LOAD)) continue;
+          if (!bounds_ok(natural_run(mt.off, i, 8, len), status, K, 0, kNatural)) continue;
           load8<O_FP16>(o, s0 + i, f);
           if (APPLY) {
             float4* pp = reinterpret_cast<float4*>(p + i);
@@ -412,13 +459,15 @@ __global__ void __launch_bounds__(kThreads)
         const int r = tp.r0 + rr, c = tp.c0 + cc;
         if (r < rows && c < cols) {
           float f[8];
+          const int64_t i = static_cast<int64_t>(r) * cols + c;
+          if (!bounds_ok(natural_run(mt.off, i, 8, len), status, K, 0, kNatural)) continue;
           if (mt.transposed) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) f[q] = tile[rr][cc + q];
           } else {
+            if (!bounds_ok(slot_run(mt, r, c, 8), status, K, 0, NSM_SITE_SLOT_LOAD)) continue;
             load8<O_FP16>(o, s0 + static_cast<int64_t>(r) * ld + c, f);
           }
-          const int64_t i = static_cast<int64_t>(r) * cols + c;
           if (APPLY) {
             float4* pp = reinterpret_cast<float4*>(p + i);
             float4 a = pp[0], b = pp[1];
@@ -446,9 +495,11 @@ __global__ void __launch_bounds__(kThreads)
         const int rr = j >> 6, cc = j & 63;
         const int r = tp.r0 + rr, c = tp.c0 + cc;
         if (r < rows && c < cols) {
+          const int64_t i = static_cast<int64_t>(r) * cols + c;
+          if (!bounds_ok(natural_run(mt.off, i, 1, len), status, K, 0, kNatural)) continue;
+          if (!mt.transposed && !bounds_ok(slot_run(mt, r, c, 1), status, K, 0, NSM_SITE_SLOT_LOAD)) continue;
           const float ov = mt.transposed ? tile[rr][cc]
                                          : load_half<O_FP16>(o, s0 + static_cast<int64_t>(r) * ld + c);
-          const int64_t i = static_cast<int64_t>(r) * cols + c;
           if (APPLY) {
             const float np = fmaf(-coef, ov, p[i] * decay);
             p[i] = np;
@@ -477,14 +528,17 @@ __device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v
 __global__ void __launch_bounds__(kThreads)
     k_adamw(const __nv_bfloat16* __restrict__ grads, float* __restrict__ params,
             float* __restrict__ mom1, float* __restrict__ mom2, int64_t numel, float b1,
-            float b2, float eps, float decay, float step_size, float bc2) {
+            float b2, float eps, float decay, float step_size, float bc2, int* status) {
   grid_dependency_sync();  // inputs come from the previous kernel of the stream
   release_dependents();
   const int64_t nvec = numel >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   // two 8-element groups per iteration, every load issued before the first store
   for (int64_t v = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; v < nvec; v += 2 * stride) {
-    const bool two = v + stride < nvec;
+    // g, p, m and v are read and written at the same 8 elements of the group
+    if (!bounds_ok(natural_run(0, v * 8, 8, numel), status, NSM_KERNEL_ADAMW, 0, NSM_SITE_FLAT)) continue;
+    const bool two = v + stride < nvec &&
+                     bounds_ok(natural_run(0, (v + stride) * 8, 8, numel), status, NSM_KERNEL_ADAMW, 0, NSM_SITE_FLAT);
     float g[2][8];
     float4 p[2][2], m[2][2], w[2][2];
 #pragma unroll
@@ -516,6 +570,7 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
   for (int64_t i = nvec * 8 + blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < numel; i += stride) {
+    if (!bounds_ok(natural_run(0, i, 1, numel), status, NSM_KERNEL_ADAMW, 0, NSM_SITE_FLAT)) continue;
     float p = params[i], m = mom1[i], w = mom2[i];
     adamw_elem(__bfloat162float(grads[i]), p, m, w, b1, b2, eps, decay, step_size, bc2);
     params[i] = p;
@@ -548,16 +603,18 @@ cudaError_t launch_momentum_norm(const void* grads, float* momentum, const MatIn
                                  int total_chunks, float* partials, float mu, int nesterov,
                                  int has_momentum, cudaStream_t stream) {
   const int grid = grid_for(total_chunks, 8);
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
   const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
   if (!has_momentum) {
     if (const cudaError_t e_launch = launch_pdl(k_momentum_norm<false, false>, dim3(grid), dim3(kThreads), 0, stream, g, nullptr, mats, nmats, total_chunks,
-                                                                 partials, mu)) return e_launch;
+                                                                 partials, mu, status)) return e_launch;
   } else if (nesterov) {
     if (const cudaError_t e_launch = launch_pdl(k_momentum_norm<true, true>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mats, nmats, total_chunks,
-                                                               partials, mu)) return e_launch;
+                                                               partials, mu, status)) return e_launch;
   } else {
     if (const cudaError_t e_launch = launch_pdl(k_momentum_norm<true, false>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mats, nmats, total_chunks,
-                                                                partials, mu)) return e_launch;
+                                                                partials, mu, status)) return e_launch;
   }
   return cudaGetLastError();
 }
@@ -573,13 +630,13 @@ cudaError_t launch_norm_finalize(const MatInfo* mats, int nmats, const float* pa
 template <bool TO_FP16>
 static cudaError_t to_class_mode(int mode, int grid, const __nv_bfloat16* g, const float* m, float mu, void* dst,
                           const MatInfo* mats, int nmats, int64_t total_tiles, const float* scales,
-                          cudaStream_t stream) {
+                          int* status, cudaStream_t stream) {
   if (mode == kUFromGrad) {
-    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUFromGrad>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUFromGrad>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales, status)) return e_launch;
   } else if (mode == kUMomentum) {
-    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUMomentum>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUMomentum>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales, status)) return e_launch;
   } else {
-    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUNesterov>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUNesterov>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales, status)) return e_launch;
   }
   return cudaSuccess;
 }
@@ -590,8 +647,10 @@ cudaError_t launch_to_class(const void* grads, const float* momentum, int has_mo
   const int grid = grid_for(total_tiles, 8);
   const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
   const int mode = !has_momentum ? kUFromGrad : (nesterov ? kUNesterov : kUMomentum);
-  const cudaError_t e = to_fp16 ? to_class_mode<true>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, stream)
-                                : to_class_mode<false>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, stream);
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
+  const cudaError_t e = to_fp16 ? to_class_mode<true>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, status, stream)
+                                : to_class_mode<false>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, status, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -602,10 +661,12 @@ cudaError_t launch_apply(const void* o, int o_fp16, float* params, void* params_
   const int grid = grid_for(total_tiles, 8);
   const float decay = 1.0f - lr * wd;
   auto* pb = reinterpret_cast<__nv_bfloat16*>(params_bf16);
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
   if (o_fp16) {
-    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, true>, dim3(grid), dim3(kThreads), 0, stream, o, params, pb, mats, nmats, total_tiles, lr, decay)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, true>, dim3(grid), dim3(kThreads), 0, stream, o, params, pb, mats, nmats, total_tiles, lr, decay, status)) return e_launch;
   } else {
-    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, true>, dim3(grid), dim3(kThreads), 0, stream, o, params, pb, mats, nmats, total_tiles, lr, decay)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, true>, dim3(grid), dim3(kThreads), 0, stream, o, params, pb, mats, nmats, total_tiles, lr, decay, status)) return e_launch;
   }
   return cudaGetLastError();
 }
@@ -614,10 +675,12 @@ cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* m
                           int64_t total_tiles, cudaStream_t stream) {
   const int grid = grid_for(total_tiles, 8);
   auto* ob = reinterpret_cast<__nv_bfloat16*>(out);
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
   if (o_fp16) {
-    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, false>, dim3(grid), dim3(kThreads), 0, stream, o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, false>, dim3(grid), dim3(kThreads), 0, stream, o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f, status)) return e_launch;
   } else {
-    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, false>, dim3(grid), dim3(kThreads), 0, stream, o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, false>, dim3(grid), dim3(kThreads), 0, stream, o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f, status)) return e_launch;
   }
   return cudaGetLastError();
 }
@@ -630,8 +693,10 @@ cudaError_t launch_adamw(const void* grads, float* params, float* m, float* v, i
   const int grid = grid_for((items + kThreads - 1) / kThreads, 8);
   const float decay = 1.0f - lr * wd;
   const float step_size = lr / bc1;
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
   if (const cudaError_t e_launch = launch_pdl(k_adamw, dim3(grid), dim3(kThreads), 0, stream, reinterpret_cast<const __nv_bfloat16*>(grads), params, m, v,
-                                         numel, beta1, beta2, eps, decay, step_size, bc2)) return e_launch;
+                                         numel, beta1, beta2, eps, decay, step_size, bc2, status)) return e_launch;
   return cudaGetLastError();
 }
 

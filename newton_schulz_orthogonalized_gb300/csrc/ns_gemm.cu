@@ -220,6 +220,28 @@ __device__ __forceinline__ void chunk_values(const uint32_t (&r)[32], const type
   }
 }
 
+// Bounds tests of the checked build (bounds_ok; compiled out otherwise).  box_in: a TMA
+// box whose first element (x innermost, y, batch b) lies inside an x_ext x y_ext matrix of
+// a group of `count`, x on a 16-byte boundary.  A is M x K (x = k, y = row), K-major B is
+// N x K (x = k, y = column of the product), MN-major B is K x N (x = column, y = k), the
+// output M x N (x = column, y = row).  elem_in: a run of w elements from (row, col) of an
+// M x N matrix; a run read or written as 16-byte vectors (vec) must also start on a
+// 16-byte boundary (`at` is its first element's index in its buffer).
+__device__ __forceinline__ bool box_in(int x, int x_ext, int y, int y_ext, int b, int count) {
+  return x >= 0 && x < x_ext && (x & 7) == 0 && y >= 0 && y < y_ext && b >= 0 && b < count;
+}
+
+__device__ __forceinline__ bool elem_in(int row, int col, int w, int M, int N, int b, int count, int64_t at,
+                                        bool vec) {
+  return row >= 0 && row < M && col >= 0 && col + w <= N && b >= 0 && b < count && (!vec || (at & 7) == 0);
+}
+
+// Where the epilogue records a failed bounds test: the status word and the kernel.
+struct Chk {
+  int* status;
+  int kernel;
+};
+
 // Epilogue of a stored product whose rows are not a whole number of 16-byte units (the
 // TMA store path needs that): out = alpha acc + beta aux + diag I, rounded once and stored
 // by each lane for its row.  A symmetric output stores its upper triangle directly and
@@ -228,7 +250,7 @@ __device__ __forceinline__ void chunk_values(const uint32_t (&r)[32], const type
 template <bool FP16, bool HAS_AUX>
 __device__ __forceinline__ void epilogue_rows_direct(const GemmGroup& G, int b, int rb, int n0, int n_len,
                                                      uint32_t t_row, uint32_t* xw, int lane, float alpha,
-                                                     float beta, float diag) {
+                                                     float beta, float diag, Chk chk) {
   using E = Elem<FP16>;
   using T = typename E::T;
   const int row = rb + lane;
@@ -253,7 +275,13 @@ __device__ __forceinline__ void epilogue_rows_direct(const GemmGroup& G, int b, 
     uint32_t h[16];
     {
       float v[32];
-      chunk_values<FP16, HAS_AUX>(r, aux_row, row_ok, col0, full, n_len, row - gc0, alpha, beta, diag, v);
+      // the aux row's elements of this chunk: 32 as four 16-byte vectors, or the ones in range
+      const bool aux_ok =
+          !HAS_AUX || !row_ok ||
+          bounds_ok(elem_in(row, gc0, full ? 32 : min(32, n_len - col0), G.M, G.N, b, G.count,
+                            static_cast<int64_t>(b) * G.aux_bstride + static_cast<int64_t>(row) * G.ld_aux + gc0, full),
+                    chk.status, chk.kernel, NSM_ROLE_EPILOGUE, NSM_SITE_AUX);
+      chunk_values<FP16, HAS_AUX>(r, aux_row, row_ok && aux_ok, col0, full, n_len, row - gc0, alpha, beta, diag, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) h[i] = pack2<FP16>(v[2 * i], v[2 * i + 1]);
     }
@@ -261,7 +289,11 @@ __device__ __forceinline__ void epilogue_rows_direct(const GemmGroup& G, int b, 
       uint16_t* o16 = reinterpret_cast<uint16_t*>(out_row + col0);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        if (col0 + j < n_len && gc0 + j >= first_col) o16[j] = half_of(h, j);
+        if (col0 + j < n_len && gc0 + j >= first_col &&
+            bounds_ok(elem_in(row, gc0 + j, 1, G.M, G.N, b, G.count, 0, false), chk.status, chk.kernel, NSM_ROLE_EPILOGUE,
+                      NSM_SITE_OUT)) {
+          o16[j] = half_of(h, j);
+        }
       }
     }
     if (G.sym && gc0 + 31 > rb) {
@@ -282,7 +314,11 @@ __device__ __forceinline__ void epilogue_rows_direct(const GemmGroup& G, int b, 
                                                     static_cast<int64_t>(mr) * G.ld_out + rb);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          if (rb + j < G.M && mr > rb + j) m16[j] = half_of(m, j);
+          if (rb + j < G.M && mr > rb + j &&
+              bounds_ok(elem_in(mr, rb + j, 1, G.M, G.N, b, G.count, 0, false), chk.status, chk.kernel, NSM_ROLE_EPILOGUE,
+                        NSM_SITE_OUT)) {
+            m16[j] = half_of(m, j);
+          }
         }
       }
       __syncwarp();
@@ -307,7 +343,7 @@ __device__ __forceinline__ uint32_t sw64(int row, int col) {
 template <bool FP16, bool HAS_AUX>
 __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
                                               uint32_t t_row, uint32_t stage, uint32_t& nst, int lane,
-                                              float alpha, float beta, float diag) {
+                                              float alpha, float beta, float diag, Chk chk) {
   using E = Elem<FP16>;
   using T = typename E::T;
   if (rb >= G.M) return;  // the warp's rows are past the matrix
@@ -323,9 +359,14 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
     for (int w = 0; w < 4; ++w) {
       const int r = rb + 8 * w + (lane >> 2);
       const int col = 32 * c + 8 * (lane & 3);
-      ax[w] = (r < G.M && col < n_len)
-                  ? __ldg(reinterpret_cast<const uint4*>(aux_blk + static_cast<int64_t>(8 * w + (lane >> 2)) * G.ld_aux + col))
-                  : make_uint4(0u, 0u, 0u, 0u);
+      const bool in = r < G.M && col < n_len &&
+                      bounds_ok(elem_in(r, n0 + col, 8, G.M, G.N, b, G.count,
+                                        static_cast<int64_t>(b) * G.aux_bstride + static_cast<int64_t>(r) * G.ld_aux +
+                                            n0 + col,
+                                        true),
+                                chk.status, chk.kernel, NSM_ROLE_EPILOGUE, NSM_SITE_AUX);
+      ax[w] = in ? __ldg(reinterpret_cast<const uint4*>(aux_blk + static_cast<int64_t>(8 * w + (lane >> 2)) * G.ld_aux + col))
+                 : make_uint4(0u, 0u, 0u, 0u);
     }
   };
   if (HAS_AUX) {
@@ -414,8 +455,13 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
     ptx::fence_proxy_async_smem();  // the TMA engine reads the staged blocks next
     __syncwarp();
     if (lane == 0) {
-      ptx::tma_store_3d(G.map_out, slot, gc0, rb, b);
-      if (upper_blk) ptx::tma_store_3d(G.map_out, slot + 2048u, rb, gc0, b);
+      if (bounds_ok(box_in(gc0, G.N, rb, G.M, b, G.count), chk.status, chk.kernel, NSM_ROLE_EPILOGUE, NSM_SITE_OUT)) {
+        ptx::tma_store_3d(G.map_out, slot, gc0, rb, b);
+      }
+      if (upper_blk &&
+          bounds_ok(box_in(rb, G.N, gc0, G.M, b, G.count), chk.status, chk.kernel, NSM_ROLE_EPILOGUE, NSM_SITE_OUT)) {
+        ptx::tma_store_3d(G.map_out, slot + 2048u, rb, gc0, b);
+      }
       ptx::bulk_commit_group();
     }
     ++nst;
@@ -503,14 +549,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t a_dst = ring + stage * S1_STAGE_BYTES;
           const uint32_t b_dst = a_dst + S1_A_BYTES;
           const int k0 = kb * BK;
+          constexpr int K1 = NSM_KERNEL_GEMM, RP = NSM_ROLE_PRODUCER;
           for (int q = 0; q < a_loads; ++q) {
-            ptx::tma_load_3d(a_dst + q * BOX_BYTES, G.map_a, fb, k0, tc.m0 + 64 * q, tc.b);
+            if (bounds_ok(box_in(k0, G.K, tc.m0 + 64 * q, G.M, tc.b, G.count), status, K1, RP, NSM_SITE_TMA_A)) {
+              ptx::tma_load_3d(a_dst + q * BOX_BYTES, G.map_a, fb, k0, tc.m0 + 64 * q, tc.b);
+            }
           }
           for (int q = 0; q < b_loads; ++q) {
             if (B_MN) {
-              ptx::tma_load_3d(b_dst + q * BOX_BYTES, G.map_b, fb, tc.n0 + 64 * q, k0, tc.b);
+              if (bounds_ok(box_in(tc.n0 + 64 * q, G.N, k0, G.K, tc.b, G.count), status, K1, RP, NSM_SITE_TMA_B)) {
+                ptx::tma_load_3d(b_dst + q * BOX_BYTES, G.map_b, fb, tc.n0 + 64 * q, k0, tc.b);
+              }
             } else {
-              ptx::tma_load_3d(b_dst + q * BOX_BYTES, G.map_b, fb, k0, tc.n0 + 64 * q, tc.b);
+              if (bounds_ok(box_in(k0, G.K, tc.n0 + 64 * q, G.N, tc.b, G.count), status, K1, RP, NSM_SITE_TMA_B)) {
+                ptx::tma_load_3d(b_dst + q * BOX_BYTES, G.map_b, fb, k0, tc.n0 + 64 * q, tc.b);
+              }
             }
           }
           fill_parity[stage] = static_cast<int>(phase);
@@ -613,10 +666,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              static_cast<uint32_t>(acc * BN);
       if (G.map_out) {
         epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                     t_row, stage, nst, lane, alpha, beta, diag);
+                                     t_row, stage, nst, lane, alpha, beta, diag, Chk{status, NSM_KERNEL_GEMM});
       } else {
         epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                            t_row, stage_words, lane, alpha, beta, diag);
+                                            t_row, stage_words, lane, alpha, beta, diag,
+                                            Chk{status, NSM_KERNEL_GEMM});
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -756,23 +810,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           // MN-major B [64-column block][128 K rows]
           const uint32_t a_dst = ring + stage * S2_STAGE_BYTES;
           const uint32_t b_dst = a_dst + S2_A_BYTES;
+          constexpr int K2 = NSM_KERNEL_GEMM_PAIR, RP = NSM_ROLE_PRODUCER;
           for (int kq = 0; kq < nk; ++kq) {
             for (int q = 0; q < my_a; ++q) {
-              ptx::tma_load_3d_pair(a_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, G.map_a, fb_leader,
-                                    k0 + 64 * kq, row0 + 64 * q, tc.b);
+              if (bounds_ok(box_in(k0 + 64 * kq, G.K, row0 + 64 * q, G.M, tc.b, G.count), status, K2, RP,
+                            NSM_SITE_TMA_A)) {
+                ptx::tma_load_3d_pair(a_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, G.map_a, fb_leader,
+                                      k0 + 64 * kq, row0 + 64 * q, tc.b);
+              }
             }
             if (!B_MN) {
               for (int q = 0; q < my_b; ++q) {
-                ptx::tma_load_3d_pair(b_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, map_b, fb_leader,
-                                      k0 + 64 * kq, col0 + 64 * q, tc.b);
+                if (bounds_ok(box_in(k0 + 64 * kq, G.K, col0 + 64 * q, G.N, tc.b, G.count), status, K2, RP,
+                              NSM_SITE_TMA_B)) {
+                  ptx::tma_load_3d_pair(b_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, map_b, fb_leader,
+                                        k0 + 64 * kq, col0 + 64 * q, tc.b);
+                }
               }
             }
           }
           if (B_MN) {
             for (int kq = 0; kq < b_k_loads; ++kq) {
               for (int q = 0; q < my_b; ++q) {
-                ptx::tma_load_3d_pair(b_dst + q * 2 * BOX_BYTES + kq * BOX_BYTES, map_b, fb_leader,
-                                      col0 + 64 * q, k0 + 64 * kq, tc.b);
+                if (bounds_ok(box_in(col0 + 64 * q, G.N, k0 + 64 * kq, G.K, tc.b, G.count), status, K2, RP,
+                              NSM_SITE_TMA_B)) {
+                  ptx::tma_load_3d_pair(b_dst + q * 2 * BOX_BYTES + kq * BOX_BYTES, map_b, fb_leader,
+                                        col0 + 64 * q, k0 + 64 * kq, tc.b);
+                }
               }
             }
           }
@@ -885,10 +949,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int rb = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
       if (G.map_out) {
         epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage, nst, lane,
-                                     alpha, beta, diag);
+                                     alpha, beta, diag, Chk{status, NSM_KERNEL_GEMM_PAIR});
       } else {
         epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage_words,
-                                            lane, alpha, beta, diag);
+                                            lane, alpha, beta, diag, Chk{status, NSM_KERNEL_GEMM_PAIR});
       }
       ptx::tc_fence_before();
       __syncwarp();

@@ -168,8 +168,15 @@ __device__ bool produce(const Roles& R, const SmallJob* __restrict__ jobs, int n
         ptx::mbar_arrive_expect_tx(fb, kSlot);
         const uint32_t slot = R.ring + static_cast<uint32_t>(rp.stage * kSlot);
         // the second panel may start past the matrix: it reads zeros
-        ptx::tma_load_3d(slot, map, fb, c * kChunk, 0, job.b);
-        ptx::tma_load_3d(slot + kPanel, map, fb, c * kChunk + 64, 0, job.b);
+        const int x0 = c * kChunk, x1 = x0 + 64;
+        if (bounds_ok(x0 >= 0 && x0 < job.n && (x0 & 7) == 0 && job.b >= 0, R.status, NSM_KERNEL_SMALL,
+                      NSM_ROLE_PRODUCER, NSM_SITE_TMA_X_LOAD)) {
+          ptx::tma_load_3d(slot, map, fb, x0, 0, job.b);
+        }
+        if (bounds_ok(x1 >= 0 && (x1 & 7) == 0 && job.b >= 0, R.status, NSM_KERNEL_SMALL, NSM_ROLE_PRODUCER,
+                      NSM_SITE_TMA_X_LOAD)) {
+          ptx::tma_load_3d(slot + kPanel, map, fb, x1, 0, job.b);
+        }
         fill_parity[rp.stage] = static_cast<int>(rp.phase);
         rp.advance();
       }
@@ -440,8 +447,15 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
         ptx::named_sync(kEpiBar, kEpiThreads);
         if (ep.leader) {
           if (reads_x) ptx::mbar_arrive(R.bar(&R.ctrl->empty[stage]));
-          ptx::tma_store_3d(job.map_x[op.dst_x], xt, c * kChunk, 0, job.b);
-          if (c * kChunk + 64 < job.n) ptx::tma_store_3d(job.map_x[op.dst_x], xt + kPanel, c * kChunk + 64, 0, job.b);
+          const int x0 = c * kChunk, x1 = x0 + 64;
+          if (bounds_ok(x0 >= 0 && x0 < job.n && (x0 & 7) == 0 && job.b >= 0, R.status, NSM_KERNEL_SMALL,
+                        NSM_ROLE_EPILOGUE, NSM_SITE_TMA_X_STORE)) {
+            ptx::tma_store_3d(job.map_x[op.dst_x], xt, x0, 0, job.b);
+          }
+          if (x1 < job.n && bounds_ok((x1 & 7) == 0, R.status, NSM_KERNEL_SMALL, NSM_ROLE_EPILOGUE,
+                                      NSM_SITE_TMA_X_STORE)) {
+            ptx::tma_store_3d(job.map_x[op.dst_x], xt + kPanel, x1, 0, job.b);
+          }
           ptx::bulk_commit_group();
         }
         if (op.accumulate) {

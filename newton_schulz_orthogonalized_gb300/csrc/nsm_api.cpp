@@ -1066,6 +1066,7 @@ int option_value(int option) {
     case NSM_OPT_PAIR_KERNELS: return g_opt_pair.load();
     case NSM_OPT_SMALL_KERNEL: return g_opt_small.load();
     case NSM_OPT_PDL: return g_opt_pdl.load();
+    case NSM_OPT_BOUNDS_CHECKS: return kChecked ? 1 : 0;
     default: return -1;
   }
 }
@@ -1541,15 +1542,17 @@ int nsm_device_status_detail(nsm_stream_t stream_, int* status_out, int* kernel_
   const int zero = 0;
   e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return fail_cuda(e, "clear device status");
-  const bool timeout = (v & 0xff) == kDevTimeout;
-  *status_out = timeout ? NSM_ERR_TIMEOUT : NSM_OK;
-  if (kernel_out) *kernel_out = timeout ? (v >> 8) & 0xff : 0;
-  if (role_out) *role_out = timeout ? (v >> 16) & 0xff : 0;
-  if (site_out) *site_out = timeout ? (v >> 24) & 0xff : 0;
+  const int kind = v & 0xff;
+  const bool set = kind == kDevTimeout || kind == kDevBounds;
+  *status_out = kind == kDevTimeout ? NSM_ERR_TIMEOUT : (kind == kDevBounds ? NSM_ERR_BOUNDS : NSM_OK);
+  if (kernel_out) *kernel_out = set ? (v >> 8) & 0xff : 0;
+  if (role_out) *role_out = set ? (v >> 16) & 0xff : 0;
+  if (site_out) *site_out = set ? (v >> 24) & 0xff : 0;
   return NSM_OK;
 }
 
 int nsm_set_option(int option, int value) {
+  if (option == NSM_OPT_BOUNDS_CHECKS) return fail(NSM_ERR_ARG, "NSM_OPT_BOUNDS_CHECKS is read only");
   const int max_value = option == NSM_OPT_PDL ? 2 : 1;
   if (value < 0 || value > max_value) return fail(NSM_ERR_ARG, "option value %d is not in [0, %d]", value, max_value);
   switch (option) {
@@ -1569,6 +1572,12 @@ int nsm_status_selftest(int wait_us, nsm_stream_t stream_) {
   if (wait_us < 1 || wait_us > 2000000) return fail(NSM_ERR_ARG, "wait_us = %d not in [1, 2000000]", wait_us);
   const cudaError_t e = launch_status_selftest(uint64_t(wait_us) * 1000u, reinterpret_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return fail_cuda(e, "status self-test launch");
+  return NSM_OK;
+}
+
+int nsm_bounds_selftest(nsm_stream_t stream_) {
+  const cudaError_t e = launch_bounds_selftest(reinterpret_cast<cudaStream_t>(stream_));
+  if (e != cudaSuccess) return fail_cuda(e, "bounds self-test launch");
   return NSM_OK;
 }
 

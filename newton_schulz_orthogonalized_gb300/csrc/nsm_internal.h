@@ -9,18 +9,41 @@
 
 namespace nsm {
 
-// Status word kernels write when a bounded wait expires: kDevTimeout in the low byte,
-// then which kernel, which role inside it and which barrier gave up (NSM_KERNEL_*,
-// NSM_ROLE_*, NSM_SITE_* of the public header).  Only the first expiry since the word
-// was last read is kept.
+// Status word kernels write when a bounded wait expires (kDevTimeout in the low byte)
+// or, in the checked build, when a bounds check fails (kDevBounds); then which kernel,
+// which role inside it and which barrier or access site (NSM_KERNEL_*, NSM_ROLE_*,
+// NSM_SITE_* of the public header).  Only the first record since the word was last read
+// is kept.
 constexpr int kDevOk = 0;
 constexpr int kDevTimeout = 1;
-__host__ __device__ constexpr int status_word(int kernel, int role, int site) {
-  return kDevTimeout | (kernel << 8) | (role << 16) | (site << 24);
+constexpr int kDevBounds = 2;
+__host__ __device__ constexpr int status_word(int kernel, int role, int site, int kind = kDevTimeout) {
+  return kind | (kernel << 8) | (role << 16) | (site << 24);
 }
+
+// The checked build (compiled with NSM_CHECKED=1) tests every global access and TMA box of
+// its kernels against the matrix it belongs to before making it.
+#if defined(NSM_CHECKED) && NSM_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
 #ifdef __CUDACC__
 __device__ __forceinline__ void record_timeout(int* status, int kernel, int role, int site) {
   atomicCAS(status, kDevOk, status_word(kernel, role, site));
+}
+
+// Whether an access may be made.  The regular build always says yes and the test
+// compiles away; the checked build records a failed test (kDevBounds, kernel, role,
+// site) and the caller skips the access.
+__device__ __forceinline__ bool bounds_ok(bool ok, int* status, int kernel, int role, int site) {
+  if constexpr (kChecked) {
+    if (!ok) atomicCAS(status, kDevOk, status_word(kernel, role, site, kDevBounds));
+    return ok;
+  } else {
+    return true;
+  }
 }
 #endif
 
@@ -159,5 +182,7 @@ cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream);
 int* device_status_ptr();
 // One CTA whose bounded wait expires after limit_ns and records kDevTimeout.
 cudaError_t launch_status_selftest(uint64_t limit_ns, cudaStream_t stream);
+// One thread that runs bounds_ok on an index past its range, making no access.
+cudaError_t launch_bounds_selftest(cudaStream_t stream);
 
 }  // namespace nsm

@@ -213,3 +213,20 @@ def test_workspace_iterate_layout(nsm, method):
         nsm.workspace_iterate(shapes, 0, nbuf, method)
     with pytest.raises(nsm.NsmError):
         nsm.workspace_iterate(shapes, len(shapes), 0, method)
+
+
+def test_checked_build_exports_the_same_symbols_and_reports_itself(nsm):
+    # the bounds-checked twin library: same ABI; NSM_OPT_BOUNDS_CHECKS reads 1 there and
+    # 0 in the regular build, and is read only in both (host-only calls, no GPU)
+    if not os.path.exists(nsm.LIB_CHECKED):
+        from newton_schulz_orthogonalized_gb300 import _build
+        _build.build(checked=True)
+    C = ctypes.CDLL(nsm.LIB_CHECKED)
+    for name in _declared_functions():
+        assert hasattr(C, name), name
+    assert C.nsm_get_option(nsm.OPT_BOUNDS_CHECKS) == 1
+    assert C.nsm_set_option(nsm.OPT_BOUNDS_CHECKS, 0) == nsm.NSM_ERR_ARG
+    assert nsm.get_option(nsm.OPT_BOUNDS_CHECKS) == 0
+    assert not nsm.checked_build()
+    with pytest.raises(nsm.NsmError):
+        nsm.set_option(nsm.OPT_BOUNDS_CHECKS, 1)
