@@ -7,7 +7,8 @@ forms and their half precision; the rounding points are the reading written in t
 oracle's docstrings).  This script computes the same steps independently of the oracle
 and of numpy: Python fractions hold every value exactly, and each stored value is rounded
 to the nearest fp16 number (ties to even) by its own exact routine.  It writes the input,
-the expected results for 1-2 standard steps and 1-3 gram steps, and, for every case, the
+the expected results for 1-2 standard steps and 1-4 gram steps (re-anchored every 3
+steps, so the fourth covers a re-anchoring), and, for every case, the
 results with one rounding point dropped or one extra rounding point added; the input is
 chosen (first seed that works) so that every one of those variants differs from the
 expected result, so a test that demands the expected bits pins the placement.
@@ -97,7 +98,11 @@ def standard(x, steps, st):
     return x
 
 
-def gram(x, steps, st, every=2):
+# gram form: R is re-anchored from the explicit iterate every EVERY steps
+EVERY = 3
+
+
+def gram(x, steps, st, every=EVERY):
     x = st(x)
     m = len(x)
     r = st(matmul(x, transpose(x)))
@@ -119,7 +124,7 @@ def gram(x, steps, st, every=2):
     return st(matmul(q, x))
 
 
-CASES = [("standard", 1), ("standard", 2), ("gram", 1), ("gram", 2), ("gram", 3)]
+CASES = [("standard", 1), ("standard", 2), ("gram", 1), ("gram", 2), ("gram", 3), ("gram", 4)]
 # extra rounding points a slip could add: A A or B X rounded before they are combined
 # (standard), R R rounded before H is formed (gram)
 EXTRAS = {"standard": ["AA", "BX"], "gram": ["RR"]}
@@ -174,6 +179,7 @@ def main():
                     "coefficients are those of \"DeepSpeed 集成 Muon 优化器实战\" §核心算子; the "
                     "rounding points are the storage-precision reading of the oracle."),
         "seed": seed,
+        "gram_restart_every": EVERY,
         "x": hexs(x),
         "cases": cases,
     }

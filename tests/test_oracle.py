@@ -344,10 +344,15 @@ def test_flop_counts():
     # H R H = 2 per step x4
     m, n = 7, 11
     assert oracle.flops_gram(m, n, restart_every=0) == 2 * (2 * m * m * n + (5 + 4 + 8) * m ** 3)
+    # re-anchored after step 3 (the default): products with X are R0, Q X and X X^T,
+    # and the final Q X = 4; squares: step1 R R, T, R; step2 R R, H Q, T, R; step3 R R,
+    # H Q; step4 R R, T, R; step5 R R, H Q = 14
+    assert oracle.GRAM_RESTART_EVERY == 3
+    assert oracle.flops_gram(m, n) == 2 * (4 * m * m * n + 14 * m ** 3)
     # re-anchored after steps 2 and 4: products with X are R0, (Q X, X X^T) twice and the
     # final Q X = 6; squares: step1 R R, T, R; step2 R R, H Q; step3 R R, T, R;
     # step4 R R, H Q; step5 R R = 11
-    assert oracle.flops_gram(m, n) == 2 * (6 * m * m * n + 11 * m ** 3)
+    assert oracle.flops_gram(m, n, restart_every=2) == 2 * (6 * m * m * n + 11 * m ** 3)
     assert oracle.flops_gram(m, n, steps=1) == 2 * (2 * m * m * n + 1 * m ** 3)
 
 
@@ -471,8 +476,8 @@ def test_page_memory_arithmetic():
 #
 # tests/golden/storage_points.json holds a 3x5 case worked in exact rational arithmetic
 # with its own fp16 rounding (tests/golden/make_storage_points.py: no numpy, no oracle):
-# the expected fp16 results of 1-2 standard steps and 1-3 gram steps (the third covers a
-# re-anchoring), and the results with any one rounding point dropped or one plausible
+# the expected fp16 results of 1-2 standard steps and 1-4 gram steps (re-anchored every 3
+# steps: the fourth covers a re-anchoring), and the results with any one rounding point dropped or one plausible
 # extra rounding point added, each of which differs from the expected one.  The oracle
 # must give the expected bits, round exactly as many times, and change its result when
 # any one of its own rounding points is skipped.
@@ -482,6 +487,10 @@ def _hexmat(rows):
 
 
 _SP = _golden("storage_points.json")
+
+
+def test_storage_points_use_the_oracles_reanchoring_interval():
+    assert _SP["gram_restart_every"] == oracle.GRAM_RESTART_EVERY
 
 
 def _ns_fp16(method, x, steps):
