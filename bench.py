@@ -50,7 +50,11 @@ def _peaks():
                 "source": "fallback"}
 
 
-def _gram_counts(steps=NS_STEPS, every=2):
+# the library re-anchors the gram form's R from the explicit iterate every 3 steps
+GRAM_REANCHOR_EVERY = 3
+
+
+def _gram_counts(steps=NS_STEPS, every=GRAM_REANCHOR_EVERY):
     """(products with X, square products) of the gram form re-anchored every `every`
     steps (every = 0: never)."""
     wide, cubes, q_identity = 1, 0, True
@@ -85,9 +89,9 @@ def _canonical_ns_flops(shapes, method):
 
 
 def _dense_ns_flops(shapes, method):
-    """Flops of the chain as the library runs it (the gram form re-anchored every 2
+    """Flops of the chain as the library runs it (the gram form re-anchored every 3
     steps), counted as if every tile of every product were computed."""
-    return _chain_flops(shapes, method, every=2)
+    return _chain_flops(shapes, method, every=GRAM_REANCHOR_EVERY)
 
 
 def _describe(wl):

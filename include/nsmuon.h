@@ -58,7 +58,7 @@ typedef struct CUstream_st* nsm_stream_t;
 /* Newton-Schulz methods [DSM §核心算子].  Every form accumulates in fp32 on the tensor
  * cores; they differ in the half precision the iterates are stored in. */
 #define NSM_NS_STANDARD      0  /* quintic steps on X, fp16 storage */
-#define NSM_NS_GRAM          1  /* gram form on R = X X^T, fp16, re-anchored every 2 steps */
+#define NSM_NS_GRAM          1  /* gram form on R = X X^T, fp16, re-anchored every 3 steps */
 #define NSM_NS_STANDARD_BF16 2  /* quintic steps on X, bf16 storage (the page's stable form) */
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */

@@ -32,7 +32,11 @@ constexpr float kB = -4.7750f;
 constexpr float kC = 2.0315f;
 constexpr float kNormEps = 1e-7f;
 constexpr int kMaxSteps = 16;
-constexpr int kGramReanchor = 2;  // gram form: re-anchor R from the explicit iterate every 2 steps
+// Gram form: R is re-anchored from the explicit iterate every 3 steps.  In fp16 storage
+// that keeps the iteration as close to the exact one as every 2 steps does (about 2% on
+// near-low-rank inputs; every 4: 2.5%, never: 10-47%), with 3 m^2 (n - m) fewer executed
+// flops per five-step chain (symmetric products on half their tiles).
+constexpr int kGramReanchor = 3;
 constexpr int kMaxMatrices = 1 << 22;
 constexpr int64_t kMaxDim = int64_t(1) << 30;
 constexpr size_t kAlign = 1024;

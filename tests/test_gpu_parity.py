@@ -645,3 +645,21 @@ def test_stored_iterates_exactly_symmetric(nsm, method):
     nsm.muon_step(grads, params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws)
     assert nsm.device_status() == nsm.NSM_OK
     _iterates_symmetric(nsm, shapes, method, ws)
+
+
+@pytest.mark.parametrize("steps", [1, 2, 3, 4, 5, 7])
+def test_grouped_gram_chain_runs_one_launch_per_product_of_the_oracle(nsm, steps):
+    # The library's gram chain and the oracle's take the same re-anchoring schedule:
+    # one grouped GEMM launch per product the oracle's chain forms (flops_gram counts
+    # 2 m^2 n per product with X and 2 m^3 per square product, so at m = n = 1 it is
+    # twice the number of products), and the same executed work in flops.
+    wl = synth.custom([(256, 512), (512, 256)], seed=71, name="pair")
+    nsm.timing_reset()
+    nsm.timing_enable(True)
+    try:
+        Step(nsm, wl, "gram", steps=steps)
+        torch.cuda.synchronize()
+        _, n_gemm, _ = nsm.timing_read(nsm.KIND_GEMM)
+    finally:
+        nsm.timing_enable(False)
+    assert n_gemm == oracle.flops_gram(1, 1, steps) // 2

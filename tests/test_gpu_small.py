@@ -73,9 +73,10 @@ def test_small_table_is_one_chain_launch(nsm):
         nsm.timing_enable(False)
     assert launches == 5
     assert n_small == 1 and n_gemm == 0
-    # bytes: the re-anchored gram chain reads X in R0 = X X^T, in both re-anchoring
-    # passes and in the final pass, and writes it in those three passes (2 bytes each)
-    assert flops == pytest.approx(4 * 128 * 256 * 2 * (4 + 3))
+    # bytes: the re-anchored gram chain (re-anchored after step 3) reads X in R0 = X X^T,
+    # in the re-anchoring pass and in the final pass, and writes it in those two passes
+    # (2 bytes each)
+    assert flops == pytest.approx(4 * 128 * 256 * 2 * (3 + 2))
 
 
 @pytest.mark.parametrize("method", ["gram", "standard"])
