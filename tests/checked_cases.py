@@ -13,9 +13,14 @@ has:
 - nsm_gemm with aux, MN-major B, a symmetric output of odd order and the 2-SM kernel;
 - adamw_step on a group whose length is not a multiple of 8.
 
+`fullsize_digest(nsm, name)` runs one muon_step (gram, with the bf16 parameter copy) over
+a whole benchmark table (llama7b: 5.67B elements; split_moe: 9.13B) and returns exact
+integer digests of the updated parameters, momentum and copy, and the device status.
+
 Run as a script (`python tests/checked_cases.py OUT.npz`), it writes the outputs and the
-statuses to OUT.npz / OUT.json; with NSM_CHECKED=1 in the environment the binding loads
-the bounds-checked build.
+statuses to OUT.npz / OUT.json (`python tests/checked_cases.py --fullsize NAME OUT.json`:
+the digests); with NSM_CHECKED=1 in the environment the binding loads the bounds-checked
+build.
 """
 
 from __future__ import annotations
@@ -142,9 +147,57 @@ def run(nsm):
     return out, status
 
 
+def _digest(t):
+    """Exact digest of a tensor's bits: per chunk of 2^26 elements, the sum of its 16- or
+    32-bit words and their sum weighted by position (int64 arithmetic on the device)."""
+    import torch
+    words = t.view(torch.int32) if t.element_size() == 4 else t.view(torch.int16)
+    out = []
+    chunk = 1 << 26
+    for i in range(0, words.numel(), chunk):
+        w = words[i:i + chunk].to(torch.int64)
+        pos = torch.arange(1, w.numel() + 1, device=w.device, dtype=torch.int64) % 65521 + 1
+        out.append([int(w.sum()), int((w * pos).sum())])
+        del w, pos
+    return out
+
+
+def fullsize_digest(nsm, name):
+    import torch
+
+    import synth
+
+    nsm.lib()
+    wl = synth.workload(name)
+    shapes = wl.muon_shapes
+    offsets, total = nsm.pack(shapes)
+    grads = torch.zeros(total, dtype=torch.bfloat16, device="cuda")
+    params = torch.zeros(total, dtype=torch.float32, device="cuda")
+    mom = torch.zeros(total, dtype=torch.float32, device="cuda")
+    copy = torch.zeros(total, dtype=torch.bfloat16, device="cuda")
+    synth.fill_packed_grads(wl, offsets, grads)
+    synth.fill_packed_params(wl, offsets, params)
+    ws = torch.empty(nsm.workspace_bytes(shapes, "gram"), dtype=torch.uint8, device="cuda")
+    nsm.muon_step(grads, params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, "gram", 5, True, ws,
+                  params_bf16=copy)
+    torch.cuda.synchronize()
+    status = _status(nsm)
+    del ws, grads
+    res = {"status": status, "params": _digest(params), "momentum": _digest(mom), "copy": _digest(copy)}
+    del params, mom, copy
+    torch.cuda.empty_cache()
+    return res
+
+
 if __name__ == "__main__":
     import newton_schulz_orthogonalized_gb300 as nsm_mod
 
+    if sys.argv[1] == "--fullsize":
+        res = fullsize_digest(nsm_mod, sys.argv[2])
+        res.update(checked=nsm_mod.checked_build(), lib=nsm_mod.LIB_PATH)
+        with open(sys.argv[3], "w") as f:
+            json.dump(res, f)
+        sys.exit(0)
     path = sys.argv[1]
     outs, stats = run(nsm_mod)
     np.savez(path, **outs)

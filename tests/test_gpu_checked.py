@@ -9,7 +9,9 @@ which this GPU pool does not offer.
 The cases of tests/checked_cases.py (every kernel and access path of the library, on
 odd and ragged shapes) run in a child process that loads the checked build.  No test
 may fail there, and every output must equal, bit for bit, the regular build's output
-on the same inputs: the checks sit beside the arithmetic and change none of it.
+on the same inputs: the checks sit beside the arithmetic and change none of it.  The
+same holds for one step over each whole benchmark table (llama7b, split_moe), compared
+through exact digests of the updated buffers.
 """
 
 import json
@@ -92,3 +94,26 @@ def test_checked_build_matches_regular_bitwise(nsm, checked_run):
         assert got.shape == want.shape, name
         same = got.view(np.uint8) == want.view(np.uint8)
         assert same.all(), f"{name}: {int((~same).sum())} bytes differ"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["llama7b", "split_moe"])
+def test_checked_build_full_table_matches_regular(nsm, tmp_path, name):
+    import torch
+
+    import checked_cases
+    torch.cuda.empty_cache()  # the child needs the device memory this process has cached
+    path = str(tmp_path / "digest.json")
+    env = dict(os.environ, NSM_CHECKED="1")
+    proc = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "checked_cases.py"), "--fullsize",
+                           name, path], env=env, cwd=ROOT, stdout=subprocess.PIPE,
+                          stderr=subprocess.STDOUT, text=True, timeout=1200)
+    assert proc.returncode == 0, proc.stdout[-4000:]
+    with open(path) as f:
+        checked = json.load(f)
+    assert checked["checked"] is True
+    assert tuple(checked["status"]) == (0, 0, 0, 0), checked["status"]
+    regular = checked_cases.fullsize_digest(nsm, name)
+    assert tuple(regular["status"]) == (0, 0, 0, 0)
+    for key in ("params", "momentum", "copy"):
+        assert checked[key] == regular[key], key
