@@ -378,6 +378,35 @@ def _timed_steps(nsm, S, stream, steps):
     return t0.elapsed_time(t1) / steps, launches
 
 
+def _orthogonalize_block(nsm, S, stream, calls, executed_per_call, peak):
+    """muon_orthogonalize alone over the step's table (the Newton-Schulz-only number):
+    device ms per call over `calls` uninstrumented calls after one warm call (CUDA events
+    on the stream), and its rates on the chain's canonical and executed flops."""
+    import torch
+    out = torch.empty_like(S.grads)
+
+    def call():
+        nsm.muon_orthogonalize(S.grads, out, S.offsets, S.shapes, S.method, NS_STEPS, S.ws, stream)
+
+    call()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(calls):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / calls
+    del out
+    executed = executed_per_call / (ms * 1e-3) / 1e12 if executed_per_call else None
+    return {"ms": ms, "calls": calls,
+            "tflops_canonical": _canonical_ns_flops(S.shapes, S.method) / (ms * 1e-3) / 1e12,
+            "tflops_executed": executed,
+            "frac_executed": executed / peak if executed else None,
+            "includes": "the layout pass from the bf16 input, the whole chain and the export of O as bf16"}
+
+
 def _kernel_times(nsm, S, stream, steps):
     """Per kernel kind: (ms, launches, work) over `steps` steps with an event pair around
     every launch."""
@@ -623,6 +652,12 @@ def run_ours(args):
 
     peaks = _peaks()
     kernels = _kernels_block(per_kind, args.steps, peaks)
+    # ---- the orthogonalisation alone (muon_orthogonalize) over the same table
+    try:
+        ortho = _orthogonalize_block(nsm, S, stream, max(2, min(args.steps, 5)),
+                                     gemm_flops / max(args.steps, 1), peaks["bf16_tflops_sustained"])
+    except Exception as exc:
+        ortho = {"error": str(exc)[:200]}
     del S
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -681,6 +716,7 @@ def run_ours(args):
             "timing": "CUDA events around every launch, in a second timed pass of the same steps",
         },
         "kernels": kernels,
+        "orthogonalize": ortho,
         "gpu_launches": launches,
         "clocks": clocks,
         "e2e": e2e,
