@@ -334,6 +334,11 @@ int nsm_last_launch_count(void);
                                    against its matrix before making it, record a failure
                                    (NSM_ERR_BOUNDS) and skip the access; 0 in the regular
                                    build.  nsm_set_option rejects it. */
+#define NSM_OPT_SYM_STORAGE  5  /* 1 (default): where every grouped launch of a chain runs on the
+                                   2-SM kernel, its symmetric m x m iterates are stored as their
+                                   upper 256 x 256 tiles only, and a product reads a block below
+                                   the diagonal from its mirror image; 0: every symmetric iterate
+                                   is stored whole (each upper tile mirrored) */
 int nsm_set_option(int option, int value);
 int nsm_get_option(int option);
 

@@ -374,13 +374,14 @@ NSM_KERNEL_GEMM, NSM_KERNEL_GEMM_PAIR, NSM_KERNEL_SMALL, NSM_KERNEL_SELFTEST = 1
 NSM_SITE_SELFTEST = 11
 NSM_SITE_SELFTEST_BOUNDS = 23
 
-OPT_PAIR_KERNELS, OPT_SMALL_KERNEL, OPT_PDL, OPT_BOUNDS_CHECKS = 1, 2, 3, 4
+OPT_PAIR_KERNELS, OPT_SMALL_KERNEL, OPT_PDL, OPT_BOUNDS_CHECKS, OPT_SYM_STORAGE = 1, 2, 3, 4, 5
 
 
 def set_option(option: int, value: int) -> None:
     """Process-wide choice between the library's equivalent paths (for comparisons):
-    OPT_PAIR_KERNELS, OPT_SMALL_KERNEL (default 1) and OPT_PDL (0 off, 1 on, default 2:
-    on for tables of at most 2^25 elements)."""
+    OPT_PAIR_KERNELS, OPT_SMALL_KERNEL, OPT_SYM_STORAGE (default 1: symmetric iterates
+    kept as their upper 256 x 256 tiles where every launch is on the 2-SM kernel) and
+    OPT_PDL (0 off, 1 on, default 2: on for tables of at most 2^25 elements)."""
     _check(lib().nsm_set_option(int(option), int(value)))
 
 

@@ -250,7 +250,7 @@ struct Chk {
 template <bool FP16, bool HAS_AUX>
 __device__ __forceinline__ void epilogue_rows_direct(const GemmGroup& G, int b, int rb, int n0, int n_len,
                                                      uint32_t t_row, uint32_t* xw, int lane, float alpha,
-                                                     float beta, float diag, Chk chk) {
+                                                     float beta, float diag, bool mirror, Chk chk) {
   using E = Elem<FP16>;
   using T = typename E::T;
   const int row = rb + lane;
@@ -296,7 +296,7 @@ __device__ __forceinline__ void epilogue_rows_direct(const GemmGroup& G, int b, 
         }
       }
     }
-    if (G.sym && gc0 + 31 > rb) {
+    if (G.sym && mirror && gc0 + 31 > rb) {
       // lanes whose row is out of range hold values that the row mask below never stores
 #pragma unroll
       for (int i = 0; i < 16; ++i) xw[lane * 17 + i] = h[i];
@@ -343,7 +343,7 @@ __device__ __forceinline__ uint32_t sw64(int row, int col) {
 template <bool FP16, bool HAS_AUX>
 __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb, int n0, int n_len,
                                               uint32_t t_row, uint32_t stage, uint32_t& nst, int lane,
-                                              float alpha, float beta, float diag, Chk chk) {
+                                              float alpha, float beta, float diag, bool mirror, Chk chk) {
   using E = Elem<FP16>;
   using T = typename E::T;
   if (rb >= G.M) return;  // the warp's rows are past the matrix
@@ -381,7 +381,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmGroup& G, int b, int rb,
     const int gc0 = n0 + col0;  // first column of this block in the matrix
     if (G.sym && gc0 < rb) continue;  // below the diagonal: written as the mirror of its upper block
     const bool diag_blk = G.sym && gc0 == rb;
-    const bool upper_blk = G.sym && gc0 > rb;
+    const bool upper_blk = G.sym && mirror && gc0 > rb;  // stored again at its mirror image
     const uint32_t slot = stage + (nst & 1u) * 4096u;
     if (nst >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();  // the store two blocks back has read it
     __syncwarp();
@@ -666,10 +666,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              static_cast<uint32_t>(acc * BN);
       if (G.map_out) {
         epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                     t_row, stage, nst, lane, alpha, beta, diag, Chk{status, NSM_KERNEL_GEMM});
+                                     t_row, stage, nst, lane, alpha, beta, diag, true,
+                                     Chk{status, NSM_KERNEL_GEMM});
       } else {
         epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                            t_row, stage_words, lane, alpha, beta, diag,
+                                            t_row, stage_words, lane, alpha, beta, diag, true,
                                             Chk{status, NSM_KERNEL_GEMM});
       }
       ptx::tc_fence_before();
@@ -791,6 +792,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int row0 = tc.m0 + 128 * static_cast<int>(rank);
         const int col0 = tc.n0 + (narrow ? 64 : 128) * static_cast<int>(rank);
         const CUtensorMap* map_b = narrow ? G.map_b_narrow : G.map_b;
+        // Operands stored as upper 256 x 256 tiles: a K block before the operand's own tile
+        // (mt for A, nt for B) lies below the diagonal, and is loaded from its mirror image
+        // as an MN-major operand: one 64-column box of 128 K rows per 64 rows (A) or
+        // columns (B) in range, through the same maps (boxes of 64 x 128).
+        const int mt = tc.m0 >> 8, nt = tc.n0 >> 8;
+        const bool lean_a = (G.lean & kLeanA) != 0;
+        const bool lean_b = !B_MN && (G.lean & kLeanB) != 0;
+        const int my_at = rank ? a1 : a0;
+        const int my_bt = rank ? b1 : b0;
+        const uint32_t a_bytes_t = static_cast<uint32_t>((a0 + a1) * 2 * BOX_BYTES);
+        const uint32_t b_bytes_t = static_cast<uint32_t>((b0 + b1) * 2 * BOX_BYTES);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait_bounded(bar(&ctrl->empty[stage]), phase ^ 1u, abort_flag,
                                       WAIT_LIMIT_NS)) {
@@ -804,22 +816,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const int nk = (G.K - k0 > 64) ? 2 : 1;  // 64-wide K boxes holding any K in range
           // MN-major B boxes with 128 K rows load both K boxes at once
           const int b_k_loads = (B_MN && G.b_box >= 128) ? 1 : nk;
-          const uint32_t bytes = a_bytes_k * nk + (B_MN && G.b_box >= 128 ? 2 * b_bytes_k : b_bytes_k * nk);
+          const bool at = lean_a && (kb >> 1) < mt;  // this stage's 256-wide K tile is kb / 2
+          const bool bt = lean_b && (kb >> 1) < nt;
+          const uint32_t bytes = (at ? a_bytes_t : a_bytes_k * nk) +
+                                 (B_MN ? (G.b_box >= 128 ? 2 * b_bytes_k : b_bytes_k * nk)
+                                       : (bt ? b_bytes_t : b_bytes_k * nk));
           if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, bytes);
           // stage layout: A [K box][128 rows]; K-major B [K box][128 rows];
-          // MN-major B [64-column block][128 K rows]
+          // MN-major A or B [64-column block][128 K rows]
           const uint32_t a_dst = ring + stage * S2_STAGE_BYTES;
           const uint32_t b_dst = a_dst + S2_A_BYTES;
           constexpr int K2 = NSM_KERNEL_GEMM_PAIR, RP = NSM_ROLE_PRODUCER;
-          for (int kq = 0; kq < nk; ++kq) {
-            for (int q = 0; q < my_a; ++q) {
-              if (bounds_ok(box_in(k0 + 64 * kq, G.K, row0 + 64 * q, G.M, tc.b, G.count), status, K2, RP,
-                            NSM_SITE_TMA_A)) {
-                ptx::tma_load_3d_pair(a_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, G.map_a, fb_leader,
-                                      k0 + 64 * kq, row0 + 64 * q, tc.b);
+          if (at) {
+            for (int q = 0; q < my_at; ++q) {
+              if (bounds_ok(box_in(row0 + 64 * q, G.M, k0, G.K, tc.b, G.count), status, K2, RP, NSM_SITE_TMA_A)) {
+                ptx::tma_load_3d_pair(a_dst + q * 2 * BOX_BYTES, G.map_a, fb_leader, row0 + 64 * q, k0, tc.b);
               }
             }
-            if (!B_MN) {
+          } else {
+            for (int kq = 0; kq < nk; ++kq) {
+              for (int q = 0; q < my_a; ++q) {
+                if (bounds_ok(box_in(k0 + 64 * kq, G.K, row0 + 64 * q, G.M, tc.b, G.count), status, K2, RP,
+                              NSM_SITE_TMA_A)) {
+                  ptx::tma_load_3d_pair(a_dst + kq * 2 * BOX_BYTES + q * BOX_BYTES, G.map_a, fb_leader,
+                                        k0 + 64 * kq, row0 + 64 * q, tc.b);
+                }
+              }
+            }
+          }
+          if (!B_MN && bt) {
+            for (int q = 0; q < my_bt; ++q) {
+              if (bounds_ok(box_in(col0 + 64 * q, G.N, k0, G.K, tc.b, G.count), status, K2, RP, NSM_SITE_TMA_B)) {
+                ptx::tma_load_3d_pair(b_dst + q * 2 * BOX_BYTES, G.map_b, fb_leader, col0 + 64 * q, k0, tc.b);
+              }
+            }
+          } else if (!B_MN) {
+            for (int kq = 0; kq < nk; ++kq) {
               for (int q = 0; q < my_b; ++q) {
                 if (bounds_ok(box_in(k0 + 64 * kq, G.K, col0 + 64 * q, G.N, tc.b, G.count), status, K2, RP,
                               NSM_SITE_TMA_B)) {
@@ -880,6 +912,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int kblocks = (G.K + BK2 - 1) / BK2;
         // at most 128 columns in range: N = 128, each CTA's B holds 64 of them
         const uint32_t idesc = (NARROW && G.N - tc.n0 <= 128) ? idesc_narrow : idesc_wide;
+        // K blocks below the diagonal of an operand stored as upper tiles arrive MN-major
+        const int mt = tc.m0 >> 8, nt = tc.n0 >> 8;
+        const bool lean_a = (G.lean & kLeanA) != 0;
+        const bool lean_b = !B_MN && (G.lean & kLeanB) != 0;
         const int acc = local & 1;
         const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
         if (!ptx::mbar_wait_bounded(bar(&ctrl->acc_empty[acc]), acc_phase ^ 1u, abort_flag,
@@ -903,12 +939,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           // K slices of 16 in range (the last stage may hold fewer than 8)
           const int left = G.K - kb * BK2;
           const int nslices = left >= BK2 ? BK2 / 16 : (left + 15) / 16;
+          const bool at = lean_a && (kb >> 1) < mt;
+          const bool bt = B_MN || (lean_b && (kb >> 1) < nt);
+          const uint32_t id = idesc | (at ? ptx::kIdescAMajorMN : 0u) | (bt ? ptx::kIdescBMajorMN : 0u);
           for (int kk = 0; kk < nslices; ++kk) {
             const uint32_t koff = static_cast<uint32_t>((kk >> 2) * 2 * BOX_BYTES + (kk & 3) * 32);
-            const uint64_t a_desc = ptx::smem_desc_sw128(a_addr + koff, 16, 1024);
-            const uint64_t b_desc = B_MN ? ptx::smem_desc_sw128(b_addr + kk * 2048, 2 * BOX_BYTES, 1024)
-                                         : ptx::smem_desc_sw128(b_addr + koff, 16, 1024);
-            ptx::mma_f16_pair(d_tmem, a_desc, b_desc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            // K-major: 64-wide K boxes of 128 rows, a slice 32 bytes into a row; MN-major:
+            // 64-wide row (A) or column (B) blocks 16 KB apart, a slice 16 K rows down
+            const uint64_t a_desc = at ? ptx::smem_desc_sw128(a_addr + kk * 2048, 2 * BOX_BYTES, 1024)
+                                       : ptx::smem_desc_sw128(a_addr + koff, 16, 1024);
+            const uint64_t b_desc = bt ? ptx::smem_desc_sw128(b_addr + kk * 2048, 2 * BOX_BYTES, 1024)
+                                       : ptx::smem_desc_sw128(b_addr + koff, 16, 1024);
+            ptx::mma_f16_pair(d_tmem, a_desc, b_desc, id, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit_pair(bar(&ctrl->empty[stage]), 0x3);
           if (++stage == STAGES) {
@@ -947,12 +989,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
       const int rb = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
+      // an output stored as upper 256 x 256 tiles mirrors blocks only inside diagonal tiles
+      const bool mirror = !(G.lean & kLeanOut) || tc.m0 == tc.n0;
       if (G.map_out) {
         epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage, nst, lane,
-                                     alpha, beta, diag, Chk{status, NSM_KERNEL_GEMM_PAIR});
+                                     alpha, beta, diag, mirror, Chk{status, NSM_KERNEL_GEMM_PAIR});
       } else {
         epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage_words,
-                                            lane, alpha, beta, diag, Chk{status, NSM_KERNEL_GEMM_PAIR});
+                                            lane, alpha, beta, diag, mirror, Chk{status, NSM_KERNEL_GEMM_PAIR});
       }
       ptx::tc_fence_before();
       __syncwarp();

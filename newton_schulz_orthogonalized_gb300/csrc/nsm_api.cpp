@@ -250,15 +250,17 @@ struct Plan {
   int n_small_jobs = 0;
   int n_small_ops = 0;
   double small_bytes = 0;  // HBM bytes the small-matrix kernel must move (its roofline)
+  bool lean = false;       // symmetric iterates stored as their upper 256 x 256 tiles
   ~Plan() {
     if (dmeta && owns_meta) cudaFree(dmeta);
   }
 };
 
-// Process-wide launch options (nsm_set_option).  The 2-SM kernel is used where it pays
-// and matrices with m <= 128 run in the small-matrix kernel unless an option says
-// otherwise (for comparisons); programmatic dependent launch is off by default.
-std::atomic<int> g_opt_pair{1}, g_opt_small{1}, g_opt_pdl{2};
+// Process-wide launch options (nsm_set_option).  The 2-SM kernel is used where it pays,
+// matrices with m <= 128 run in the small-matrix kernel and symmetric iterates are stored
+// as their upper tiles where the chain allows it, unless an option says otherwise (for
+// comparisons); programmatic dependent launch is automatic (on for small tables).
+std::atomic<int> g_opt_pair{1}, g_opt_small{1}, g_opt_pdl{2}, g_opt_lean{1};
 
 // Programmatic dependent launch for the current call: on (1), off (0), or, in the auto
 // mode (2), on for tables of at most kPdlAutoElems elements, where each kernel is short
@@ -276,6 +278,7 @@ struct PdlScope {
 
 bool pair_kernels_enabled() { return g_opt_pair.load() != 0; }
 bool small_kernel_enabled() { return g_opt_small.load() != 0; }
+bool lean_storage_enabled() { return g_opt_lean.load() != 0; }
 
 // Flops of one matrix's Newton-Schulz chain (2 m n k per product, as if no tile were
 // skipped): standard 4 m^2 n + 2 m^3 per step; gram counts its m x n products (X X^T,
@@ -689,6 +692,22 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   }
   GemmGroup* hg = reinterpret_cast<GemmGroup*>(host.data() + groups_off);
   const int nbig = static_cast<int>(big.size());
+  // The 2-SM kernel where most of a launch's work has at least 256 rows per tile.
+  auto stage_pair = [&](const StageSpec& st) {
+    std::vector<std::pair<int, double>> rows_and_flops;
+    for (int c : big) {
+      const ShapeClass& sc = L.classes[c];
+      const double f = 2.0 * sc.count * double(sc.m) * (st.n_is_n ? sc.n : sc.m) * (st.k_is_n ? sc.n : sc.m);
+      rows_and_flops.push_back({sc.m, f});
+    }
+    return use_pair_kernels && prefer_pair(rows_and_flops);
+  };
+  // Symmetric iterates stored as their upper 256 x 256 tiles: only where every launch of
+  // the chain is on the 2-SM kernel (its tiles are 256 x 256; the 1-CTA kernel reads and
+  // writes whole matrices).
+  bool lean = lean_storage_enabled() && nbig > 0;
+  for (const StageSpec& st : stages) lean = lean && stage_pair(st);
+  P.lean = lean;
   for (size_t s = 0; s < stages.size() && nbig > 0; ++s) {
     const StageSpec& st = stages[s];
     // heaviest tiles (largest K) first
@@ -701,13 +720,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     GemmGroup* gs = hg + s * nclass;
     int64_t tiles = 0;
     double flops = 0, canonical = 0;
-    std::vector<std::pair<int, double>> rows_and_flops;
-    for (int c : big) {
-      const ShapeClass& sc = L.classes[c];
-      const double f = 2.0 * sc.count * double(sc.m) * (st.n_is_n ? sc.n : sc.m) * (st.k_is_n ? sc.n : sc.m);
-      rows_and_flops.push_back({sc.m, f});
-    }
-    const bool pair = use_pair_kernels && prefer_pair(rows_and_flops);
+    const bool pair = stage_pair(st);
     const int tile_m = pair ? 256 : 128;
     const int tk = pair ? 1 : 0;
     for (int j = 0; j < nbig; ++j) {
@@ -741,6 +754,12 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       g.tiles_n = (g.N + 255) / 256;
       g.tile_begin = tiles;
       canonical += 2.0 * g.count * double(g.M) * g.N * g.K;
+      if (lean) {
+        // every m x m buffer holds a symmetric iterate
+        if (st.sym && st.out_buf >= MM0) g.lean |= kLeanOut;
+        if (st.a_buf >= MM0) g.lean |= kLeanA;
+        if (!st.b_mn && st.b_buf >= MM0) g.lean |= kLeanB;
+      }
       if (st.sym) {
         g.sym = 1;
         g.tile_list = dtiles + tiles_off[tk][c];
@@ -800,7 +819,8 @@ std::string plan_key(int device, const int32_t* shapes, const int64_t* offsets, 
   std::string k;
   k.reserve(64 + size_t(n) * 16);
   auto put = [&](const void* p, size_t b) { k.append(static_cast<const char*>(p), b); };
-  const int opts = (pair_kernels_enabled() ? 1 : 0) | (small_kernel_enabled() ? 2 : 0);
+  const int opts = (pair_kernels_enabled() ? 1 : 0) | (small_kernel_enabled() ? 2 : 0) |
+                   (lean_storage_enabled() ? 4 : 0);
   put(&device, sizeof(device));
   put(&opts, sizeof(opts));
   put(&method, sizeof(method));
@@ -1070,6 +1090,7 @@ int option_value(int option) {
     case NSM_OPT_PAIR_KERNELS: return g_opt_pair.load();
     case NSM_OPT_SMALL_KERNEL: return g_opt_small.load();
     case NSM_OPT_PDL: return g_opt_pdl.load();
+    case NSM_OPT_SYM_STORAGE: return g_opt_lean.load();
     case NSM_OPT_BOUNDS_CHECKS: return kChecked ? 1 : 0;
     default: return -1;
   }
@@ -1563,6 +1584,7 @@ int nsm_set_option(int option, int value) {
     case NSM_OPT_PAIR_KERNELS: g_opt_pair.store(value); return NSM_OK;
     case NSM_OPT_SMALL_KERNEL: g_opt_small.store(value); return NSM_OK;
     case NSM_OPT_PDL: g_opt_pdl.store(value); return NSM_OK;
+    case NSM_OPT_SYM_STORAGE: g_opt_lean.store(value); return NSM_OK;
     default: return fail(NSM_ERR_ARG, "unknown option %d", option);
   }
 }

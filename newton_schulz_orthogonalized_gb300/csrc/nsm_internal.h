@@ -82,6 +82,11 @@ constexpr int kTile = 64;
 // sym != 0: the output is known to be symmetric (M == N, aux symmetric); only the tiles
 // in tile_list (packed mt << 16 | nt, tiles_per_mat of them) are computed, their upper
 // triangle is stored and mirrored into the lower one.
+// lean (2-SM kernel only, whose tiles are 256 x 256): symmetric m x m buffers stored as
+// their upper 256 x 256 tiles.  kLeanOut: the output keeps only the tiles it computes
+// (the diagonal tiles whole, no mirror of the others); kLeanA / kLeanB: the A / K-major B
+// operand is such a buffer, so a 256-wide block below the diagonal (K block before the
+// operand's own tile) is read from its mirror image above it, as an MN-major operand.
 struct GemmGroup {
   const CUtensorMap* map_a;
   const CUtensorMap* map_b;
@@ -101,8 +106,13 @@ struct GemmGroup {
                                // NULL when N is not a multiple of 8 (rows of whole 16-byte units)
   const CUtensorMap* map_b_narrow;  // B in 64-row boxes (K-major B; MN-major: map_b): the 2-SM
                                     // kernel's tiles with at most 128 columns in range
+  int32_t lean;                     // kLeanOut | kLeanA | kLeanB (2-SM kernel only)
+  int32_t lean_pad;
 };
-static_assert(sizeof(GemmGroup) == 128, "GemmGroup layout");
+static_assert(sizeof(GemmGroup) == 136, "GemmGroup layout");
+constexpr int32_t kLeanOut = 1;
+constexpr int32_t kLeanA = 2;
+constexpr int32_t kLeanB = 4;
 
 struct GemmLaunch {
   const GemmGroup* groups;  // device array

@@ -316,6 +316,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_
 // Instruction descriptor of kind::f16 with an f32 accumulator.
 //   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (0 = f16, 1 = bf16);
 //   15 A major, 16 B major (0 = K, 1 = MN); 17-22 N >> 3; 24-28 M >> 4.
+constexpr uint32_t kIdescAMajorMN = 1u << 15;
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
 __host__ __device__ __forceinline__ uint32_t idesc_f16(int m, int n, bool bf16, bool b_mn_major) {
   uint32_t d = 0;
   d |= 1u << 4;

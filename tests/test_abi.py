@@ -172,6 +172,12 @@ def test_options_set_get_and_reject(nsm):
     assert nsm.get_option(nsm.OPT_PAIR_KERNELS) == 1
     assert nsm.get_option(nsm.OPT_SMALL_KERNEL) == 1
     assert nsm.get_option(nsm.OPT_PDL) == 2  # auto
+    assert nsm.get_option(nsm.OPT_SYM_STORAGE) == 1
+    nsm.set_option(nsm.OPT_SYM_STORAGE, 0)
+    try:
+        assert nsm.get_option(nsm.OPT_SYM_STORAGE) == 0
+    finally:
+        nsm.set_option(nsm.OPT_SYM_STORAGE, 1)
     nsm.set_option(nsm.OPT_PDL, 1)
     try:
         assert nsm.get_option(nsm.OPT_PDL) == 1

@@ -576,8 +576,9 @@ def test_degenerate_and_extreme_shapes(nsm, method):
     s.check()
 
 
-def _two_steps_each_form(nsm):
-    wl = synth.custom([(256, 384), (384, 256), (130, 260), (96, 96)], seed=31)
+def _two_steps_each_form(nsm, wl=None):
+    if wl is None:
+        wl = synth.custom([(256, 384), (384, 256), (130, 260), (96, 96)], seed=31)
     offsets, total = nsm.pack(wl.muon_shapes)
     out = {}
     for method in ("gram", "standard", "standard_bf16"):
@@ -627,24 +628,66 @@ def test_one_cta_kernel_matches_pair_kernel_bitwise(nsm):
             assert torch.equal(a, b), method
 
 
-@pytest.mark.parametrize("method", ["gram", "standard", "standard_bf16"])
-def test_stored_iterates_exactly_symmetric(nsm, method):
-    # Every m x m iterate of the chain (A, B; R, H, Q, T) is a polynomial in X X^T, and
-    # the engine computes only its upper-triangle tiles and mirrors them: what it stores
-    # must be symmetric bit for bit, for ragged orders too.  The workspace starts as NaN,
-    # so a block the chain never wrote shows as untouched rather than as symmetric.
+# tables on which every grouped launch takes the 2-SM kernel (every order >= 256,
+# ragged orders, and the narrow last tiles of order 1408)
+PAIR_TABLE = [(256, 384), (384, 256), (300, 520), (520, 300), (1408, 2048), (700, 700)]
+
+
+def _stored_iterates(nsm, shapes, method, store_whole):
     from test_gpu_fullsize import _iterates_symmetric
-    wl = synth.custom([(130, 260), (257, 129), (200, 200), (300, 520), (520, 300), (96, 500)], seed=83)
-    shapes = wl.muon_shapes
+    wl = synth.custom(shapes, seed=83)
     offsets, total = nsm.pack(shapes)
     grads = torch.zeros(total, dtype=torch.bfloat16, device="cuda")
     synth.fill_packed_grads(wl, offsets, grads)
     params = torch.zeros(total, device="cuda")
     mom = torch.zeros(total, device="cuda")
     ws = torch.full((nsm.workspace_bytes(shapes, method),), 255, dtype=torch.uint8, device="cuda")
-    nsm.muon_step(grads, params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws)
+    if store_whole:
+        nsm.set_option(nsm.OPT_SYM_STORAGE, 0)
+    try:
+        nsm.muon_step(grads, params, mom, offsets, shapes, wl.lr, wl.wd, wl.mu, method, 5, True, ws)
+    finally:
+        nsm.set_option(nsm.OPT_SYM_STORAGE, 1)
     assert nsm.device_status() == nsm.NSM_OK
-    _iterates_symmetric(nsm, shapes, method, ws)
+    _iterates_symmetric(nsm, shapes, method, ws, upper_tiles=not store_whole)
+
+
+@pytest.mark.parametrize("method", ["gram", "standard", "standard_bf16"])
+def test_stored_iterates_exactly_symmetric(nsm, method):
+    # Every m x m iterate of the chain (A, B; R, H, Q, T) is a polynomial in X X^T, and
+    # the engine computes only its upper-triangle tiles and mirrors them: what it stores
+    # must be symmetric bit for bit, for ragged orders too.  The workspace starts as NaN,
+    # so a block the chain never wrote shows as untouched rather than as symmetric.  This
+    # table mixes orders below 256, so its launches run on the 1-CTA kernel and store whole
+    # iterates; PAIR_TABLE with whole storage forced covers the 2-SM kernel's mirror.
+    _stored_iterates(nsm, [(130, 260), (257, 129), (200, 200), (300, 520), (520, 300), (96, 500)], method,
+                     store_whole=False)
+    _stored_iterates(nsm, PAIR_TABLE, method, store_whole=True)
+
+
+@pytest.mark.parametrize("method", ["gram", "standard", "standard_bf16"])
+def test_upper_tile_storage_layout(nsm, method):
+    # With every launch on the 2-SM kernel the iterates are kept as their upper 256 x 256
+    # tiles: those are finite, the diagonal tiles exactly symmetric, and no tile below the
+    # diagonal is ever written (it keeps the NaN the workspace started with).
+    _stored_iterates(nsm, PAIR_TABLE, method, store_whole=False)
+
+
+def test_upper_tile_storage_matches_whole_storage_bitwise(nsm):
+    # A product reads a block below the diagonal of an operand from its mirror image above
+    # it (an MN-major operand): the same values in the same order of 16-wide MMAs, so the
+    # same bits as with whole iterates, for every form.
+    wl = synth.custom(PAIR_TABLE, seed=37)
+    assert nsm.get_option(nsm.OPT_SYM_STORAGE) == 1
+    upper = _two_steps_each_form(nsm, wl)
+    nsm.set_option(nsm.OPT_SYM_STORAGE, 0)
+    try:
+        whole = _two_steps_each_form(nsm, wl)
+    finally:
+        nsm.set_option(nsm.OPT_SYM_STORAGE, 1)
+    for method in upper:
+        for a, b in zip(upper[method], whole[method]):
+            assert torch.equal(a, b), method
 
 
 @pytest.mark.parametrize("steps", [1, 2, 3, 4, 5, 7])
