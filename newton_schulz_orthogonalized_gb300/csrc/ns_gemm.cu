@@ -18,7 +18,11 @@
 // tcgen05.ld, apply the fused epilogue  out = alpha*acc + beta*aux + diag*I  and store
 // fp16/bf16 32 x 32 blocks through shared memory with TMA stores.
 // A group flagged symmetric computes only the tiles that touch the upper triangle, stores
-// the blocks on and above the diagonal and mirrors the upper ones.
+// the blocks on and above the diagonal and mirrors the upper ones.  In the pair kernel a
+// group may instead keep its symmetric m x m buffers as their upper 256 x 256 tiles
+// (GemmGroup::lean): the output tiles off the diagonal are stored without a mirror, and a
+// K block below an operand's diagonal is loaded from its mirror image as an MN-major
+// operand (the A or B major bit of that block's instruction descriptor).
 //
 // The stages it serves ("DeepSpeed 集成 Muon 优化器实战" §核心算子):
 //   standard:  A = X X^T;  B = b A + c A A^T (A symmetric);  X' = a X + B X
