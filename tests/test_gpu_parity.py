@@ -481,12 +481,14 @@ def test_step_bf16_copy(nsm):
         assert (p_b[~inside] == 0).all() and (m_b[~inside] == 0).all()
 
 
+@pytest.mark.parametrize("table", ["tiny", "pair"])
 @pytest.mark.parametrize("method", ["gram", "standard"])
-def test_step_replays_in_cuda_graph(nsm, method):
+def test_step_replays_in_cuda_graph(nsm, method, table):
     # After a first call has built the plan, muon_step launches only kernels on the given
     # stream: a CUDA graph of it replays bit-identically to direct calls (the remedy for
-    # launch-bound small tables).
-    wl = synth.workload("tiny")
+    # launch-bound small tables).  "tiny" runs the small-matrix kernel, "pair" the grouped
+    # launches on the 2-SM kernel with upper-tile iterates.
+    wl = synth.workload("tiny") if table == "tiny" else synth.custom(PAIR_TABLE, seed=41, name="pair")
     offsets, total = nsm.pack(wl.muon_shapes)
     dev = "cuda"
     grads = torch.zeros(total, dtype=torch.bfloat16, device=dev)
