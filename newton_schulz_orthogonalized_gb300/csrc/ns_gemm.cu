@@ -73,6 +73,8 @@ constexpr int S1_STAGE_BYTES = S1_A_BYTES + BN * BK * 2;
 // pair kernel: 256 x 256 tiles, K 128 per stage; each CTA stages A 128 x 128 and half of
 // B (128 x 128) as two 128-byte-wide K boxes each: 3 stages of 64 KB.
 constexpr int BK2 = 128;
+// upper-tile storage (GemmGroup::lean) finds a stage's 256-wide K tile as kb / 2
+static_assert(2 * BK2 == BN, "two pair-kernel K stages per 256-wide tile");
 constexpr int S2_STAGES = 3;
 constexpr int S2_A_BYTES = 128 * BK2 * 2;
 constexpr int S2_STAGE_BYTES = S2_A_BYTES + 128 * BK2 * 2;
