@@ -95,7 +95,10 @@ int nsm_assign_owners(const int32_t* shapes, int n, int world, int ns_method, in
 /* Layout query (host-only; for checks and debugging): where muon_step and
  * muon_orthogonalize keep matrix i's m x m iterates in the workspace.  Every m x m iterate
  * of the chain (A and B of the standard forms; R, H, Q and T of the gram form) is
- * symmetric, and the library stores it exactly symmetric.  buf selects one of the m x m
+ * symmetric, and the library stores it exactly symmetric: whole, or (NSM_OPT_SYM_STORAGE,
+ * where every grouped launch runs on the 2-SM kernel) as its 256 x 256 tiles on and above
+ * the diagonal, the diagonal tiles exactly symmetric and the rest of the block never
+ * written.  buf selects one of the m x m
  * buffers: 0..1 for NSM_NS_STANDARD and NSM_NS_STANDARD_BF16, 0..3 for NSM_NS_GRAM.  On
  * return, *offset_bytes is the byte offset of matrix i's block in that buffer, *m its
  * order (m = min(rows, cols)) and *ld its row stride in 16-bit elements (fp16, or bf16
