@@ -180,6 +180,28 @@ def rank_workload(name, rank):
     return wl
 
 
+def owner_workload(nsm, name, rank, world, method):
+    """The matrices rank `rank` owns when one table is split by dedicated ownership
+    (DMuon: LPT on Newton-Schulz flops, `nsm_assign_owners`): strong scaling, every matrix
+    on exactly one rank, the AdamW group on rank 0.  Matrix names, shapes and the
+    workload's hyperparameters are kept; the seed is the table's."""
+    import dataclasses
+
+    import synth
+    wl = synth.workload(name)
+    owner, _ = nsm.assign_owners(wl.muon_shapes, world, method)
+    idx = [i for i, o in enumerate(owner) if int(o) == rank]
+    return dataclasses.replace(
+        wl, name=f"{wl.name}/owner{rank}of{world}",
+        muon_names=[wl.muon_names[i] for i in idx], muon_shapes=[wl.muon_shapes[i] for i in idx],
+        adam_names=wl.adam_names if rank == 0 else [], adam_shapes=wl.adam_shapes if rank == 0 else [])
+
+
+def synth_table(name):
+    import synth
+    return synth.workload(name).muon_shapes
+
+
 def max_over_ranks(value, dist, device):
     """The largest of every rank's value (the step time the job sees)."""
     if dist is None:
@@ -611,7 +633,10 @@ def run_ours(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     nsm.lib()
-    wl = rank_workload(args.config, rank)
+    owners = args.split == "owners"
+    wl = owner_workload(nsm, args.config, rank, world, args.method) if owners else rank_workload(args.config, rank)
+    if not wl.muon_shapes:
+        raise RuntimeError(f"rank {rank} owns no matrix of {args.config} at {world} ranks")
     method = args.method
     S = Setup(nsm, wl, method, dev)
     shapes = S.shapes
@@ -685,21 +710,23 @@ def run_ours(args):
         "warmup": args.warmup,
         "ms_per_step": ms,
         "higher_is_better": False,
-        "scaling": "weak",
+        "scaling": "strong" if owners else "weak",
         "vs_baseline": None,
         "dtype": "f16",
         "data": "synthetic",
         "config": dict(_describe(wl), ns_method=method, ns_steps=NS_STEPS,
                        storage="fp16 iterates, fp32 tensor-core accumulation; bf16 grads, fp32 params/momentum",
                        l2="inputs larger than L2 (no flush)",
-                       parallelism="replicas" if world > 1 else "single"),
+                       parallelism=(f"dmuon-owners{world}" if owners else "replicas") if world > 1 else "single"),
         "ns_chain_ms_per_step": ns_ms_per_step,
         # the chain's canonical flops (standard 5(4m^2n+2m^3), gram 4m^2n+34m^3 per matrix)
         # and the dense flops of the chain as run (gram re-anchored), over the GEMM time
         "ns_tflops_canonical": tflops(_canonical_ns_flops(shapes, method)),
         "ns_tflops_dense": tflops(_dense_ns_flops(shapes, method)),
         "ns_frac_executed": achieved_tflops / peak if achieved_tflops else None,
-        "matrices_per_s": len(shapes) * world / (ms * 1e-3),
+        # matrices of the whole job per second: every rank's table (replicas), or the one
+        # table the ranks share (owners)
+        "matrices_per_s": (len(synth_table(args.config)) if owners else len(shapes) * world) / (ms * 1e-3),
         "roofline": {
             "kernel": "k_ns_gemm",
             "bound": "tensor",
@@ -743,6 +770,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true")
+    ap.add_argument("--split", default="replicas", choices=["replicas", "owners"],
+                    help="N > 1: every rank runs its own copy of the table (replicas, weak scaling), "
+                         "or one table is split among the ranks by dedicated ownership (owners, "
+                         "strong scaling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

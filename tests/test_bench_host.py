@@ -40,3 +40,22 @@ def test_oracle_sample_covers_shapes_and_scales_by_count():
     # the whole table by the matrix count
     ms1, desc1 = bench.cpu_oracle_sample(wl, "gram", budget_s=0.0)
     assert ms1 > 0 and "1 of the 2 distinct shapes" in desc1
+
+
+def test_owner_split_covers_the_table_once():
+    # bench.py --split owners: every matrix of the table on exactly one rank (the library's
+    # LPT owner plan), the AdamW group on rank 0 only, the hyperparameters kept
+    import newton_schulz_orthogonalized_gb300 as nsm
+    nsm.lib()
+    full = synth.workload("gpt2small")
+    for world in (1, 2, 3, 8):
+        parts = [bench.owner_workload(nsm, "gpt2small", r, world, "gram") for r in range(world)]
+        names = sorted(n for p in parts for n in p.muon_names)
+        assert names == sorted(full.muon_names)
+        for p in parts:
+            assert [full.muon_shapes[full.muon_names.index(n)] for n in p.muon_names] == p.muon_shapes
+            assert (p.lr, p.wd, p.mu) == (full.lr, full.wd, full.mu)
+        assert parts[0].adam_elements == full.adam_elements
+        assert all(p.adam_elements == 0 for p in parts[1:])
+        owner, load = nsm.assign_owners(full.muon_shapes, world, "gram")
+        assert [len(p.muon_shapes) for p in parts] == [int((owner == r).sum()) for r in range(world)]
