@@ -460,7 +460,7 @@ def _kernels_block(per_kind, steps, peaks):
     return out
 
 
-def _e2e(nsm, S, stream, reps):
+def _e2e(nsm, S, stream, reps, upload_by="engine", sm_ctas=16):
     """The step end to end through the public API with host buffers: every step copies
     its bf16 grads (and the AdamW group's) host -> device from pinned memory, runs the
     step, and reads back the bf16 copy of the updated Muon parameters that the step
@@ -488,9 +488,15 @@ def _e2e(nsm, S, stream, reps):
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     def upload(slot):
-        d_grads[slot].copy_(h_grads, non_blocking=True)
-        if d_agrads is not None:
-            d_agrads[slot].copy_(h_agrads, non_blocking=True)
+        # the library's SM-load upload (nsm_copy_to_device) or the copy engine
+        if upload_by == "sm":
+            nsm.copy_to_device(d_grads[slot], h_grads, h2d, sm_ctas)
+            if d_agrads is not None:
+                nsm.copy_to_device(d_agrads[slot], h_agrads, h2d, sm_ctas)
+        else:
+            d_grads[slot].copy_(h_grads, non_blocking=True)
+            if d_agrads is not None:
+                d_agrads[slot].copy_(h_agrads, non_blocking=True)
 
     def pipeline():
         up = [(ev(), ev()) for _ in range(reps)]
@@ -547,6 +553,9 @@ def _e2e(nsm, S, stream, reps):
            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": S.total * 2,
            "steps": reps, "statistic": "median of 3 timed passes",
            "overlap": "copies on two streams, triple-buffered (uploads up to two steps ahead)",
+           "upload": (f"SM loads over the host link (nsm_copy_to_device, {sm_ctas} CTAs)" if upload_by == "sm"
+                      else "copy engine (cudaMemcpyAsync)"),
+           "download": "copy engine (cudaMemcpyAsync)",
            "breakdown": {k: med[k] for k in med if k != "ms_per_step"},
            "h2d_gbs": h2d_bytes / (med["h2d_ms_per_step"] * 1e-3) / 1e9,
            "d2h_gbs": S.total * 2 / (med["d2h_ms_per_step"] * 1e-3) / 1e9,
@@ -670,7 +679,7 @@ def run_ours(args):
 
     # ---- end to end through the public API with host buffers
     try:
-        e2e = _e2e(nsm, S, stream, max(2, min(args.steps, 20)))
+        e2e = _e2e(nsm, S, stream, max(2, min(args.steps, 20)), args.upload)
     except Exception as exc:  # pinned memory may be unavailable on a host
         e2e = {"value": None, "unit": "ms", "h2d_bytes_per_step": S.total * 2,
                "d2h_bytes_per_step": S.total * 2, "error": str(exc)[:200]}
@@ -770,6 +779,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true")
+    ap.add_argument("--upload", default="engine", choices=["engine", "sm"],
+                    help="e2e: grads uploaded by the copy engine (default) or by SM loads (nsm_copy_to_device)")
     ap.add_argument("--split", default="replicas", choices=["replicas", "owners"],
                     help="N > 1: every rank runs its own copy of the table (replicas, weak scaling), "
                          "or one table is split among the ranks by dedicated ownership (owners, "

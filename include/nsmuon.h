@@ -295,6 +295,19 @@ int nsm_status_selftest(int wait_us, nsm_stream_t stream);
  * is recorded.  Returns NSM_ERR_CUDA if the launch fails. */
 int nsm_bounds_selftest(nsm_stream_t stream);
 
+/* Host-to-device copy by the SMs, for uploading a step's inputs: `ctas` CTAs (0: 16) on
+ * `stream` read `bytes` from page-locked host memory `src` (cudaHostAlloc /
+ * cudaMallocHost, or registered with cudaHostRegister) through its device mapping, and
+ * write them to device memory `dst`.  On the GB300 machines measured, 16 CTAs loading
+ * over the host link sustained about 125-177 GB/s next to a running step, where the copy
+ * engine's rate varied from about 40 to 207 GB/s, but they slowed the step itself by
+ * 5-25%; with nothing else running both reach about 210 GB/s.  dst and src 16-byte aligned; any byte count.  Returns
+ * NSM_ERR_NULL / NSM_ERR_ALIGN, NSM_ERR_ARG for ctas outside [0, 1024] or a src that is
+ * not page-locked host memory with a device mapping (checked with cudaPointerGetAttributes
+ * before anything is launched), NSM_ERR_CUDA if that query or the launch fails.  The
+ * pages have no counterpart: it moves data only. */
+int nsm_copy_to_device(void* dst, const void* src, size_t bytes, int ctas, nsm_stream_t stream);
+
 /* Kernel timing for profiling.  While enabled, every kernel launch of muon_step,
  * muon_orthogonalize, adamw_step and nsm_gemm is bracketed by CUDA events on the
  * caller's stream.  nsm_timing_read_kind synchronises the recorded events and returns,

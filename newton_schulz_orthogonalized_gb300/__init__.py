@@ -124,6 +124,8 @@ def lib() -> ctypes.CDLL:
     L.nsm_status_selftest.restype = ctypes.c_int
     L.nsm_bounds_selftest.argtypes = [_vp]
     L.nsm_bounds_selftest.restype = ctypes.c_int
+    L.nsm_copy_to_device.argtypes = [_vp, _vp, ctypes.c_size_t, ctypes.c_int, _vp]
+    L.nsm_copy_to_device.restype = ctypes.c_int
     L.nsm_timing_enable.argtypes = [ctypes.c_int]
     L.nsm_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p,
                                   ctypes.POINTER(ctypes.c_double)]
@@ -400,6 +402,15 @@ def bounds_selftest(stream=None) -> None:
     and makes no access: the checked build records NSM_ERR_BOUNDS (read it with
     device_status_detail), the regular build nothing."""
     _check(lib().nsm_bounds_selftest(_stream_ptr(stream)))
+
+
+def copy_to_device(dst, src, stream=None, ctas: int = 0) -> None:
+    """dst (device tensor) <- src (pinned host tensor of the same byte size) by SM loads
+    over the host link (nsm_copy_to_device); asynchronous on `stream`."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src differ in size")
+    _check(lib().nsm_copy_to_device(_ptr(dst), _ptr(src), nbytes, int(ctas), _stream_ptr(stream)))
 
 
 def checked_build() -> bool:

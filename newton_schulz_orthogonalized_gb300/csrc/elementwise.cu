@@ -579,6 +579,26 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// ---------------------------------------------------------------- host -> device copy
+
+// Copy from page-locked host memory (through its device mapping) into device memory with
+// SM loads: 16-byte units, four in flight per thread, then the trailing bytes.
+__global__ void __launch_bounds__(kThreads)
+    k_copy_h2d(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t units,
+               const uint8_t* __restrict__ src_tail, uint8_t* __restrict__ dst_tail, int tail) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+  size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x;
+  for (; i + 3 * stride < units; i += 4 * stride) {
+    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+    dst[i] = a;
+    dst[i + stride] = b;
+    dst[i + 2 * stride] = c;
+    dst[i + 3 * stride] = d;
+  }
+  for (; i < units; i += stride) dst[i] = src[i];
+  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail) dst_tail[threadIdx.x] = src_tail[threadIdx.x];
+}
+
 int g_num_sms_cache[64] = {0};
 
 int num_sms() {
@@ -682,6 +702,16 @@ cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* m
   } else {
     if (const cudaError_t e_launch = launch_pdl(k_from_class<false, false>, dim3(grid), dim3(kThreads), 0, stream, o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f, status)) return e_launch;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_h2d(void* dst, const void* src_mapped, size_t bytes, int ctas, cudaStream_t stream) {
+  const size_t units = bytes / 16;
+  const int tail = static_cast<int>(bytes % 16);
+  const auto* s = static_cast<const uint8_t*>(src_mapped);
+  auto* d = static_cast<uint8_t*>(dst);
+  k_copy_h2d<<<ctas, kThreads, 0, stream>>>(reinterpret_cast<const uint4*>(s), reinterpret_cast<uint4*>(d), units,
+                                            s + units * 16, d + units * 16, tail);
   return cudaGetLastError();
 }
 

@@ -1601,6 +1601,27 @@ int nsm_status_selftest(int wait_us, nsm_stream_t stream_) {
   return NSM_OK;
 }
 
+int nsm_copy_to_device(void* dst, const void* src, size_t bytes, int ctas, nsm_stream_t stream_) {
+  if (!dst || !src) return fail(NSM_ERR_NULL, "dst or src is NULL");
+  if (!aligned(dst, 16) || !aligned(src, 16)) return fail(NSM_ERR_ALIGN, "dst and src must be 16-byte aligned");
+  if (ctas < 0 || ctas > 1024) return fail(NSM_ERR_ARG, "ctas = %d not in [0, 1024]", ctas);
+  if (bytes == 0) return NSM_OK;
+  // only page-locked host memory with a device mapping: anything else is refused before
+  // a launch
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, src);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail_cuda(e, "cudaPointerGetAttributes(src)");
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr)
+    return fail(NSM_ERR_ARG, "src is not page-locked host memory with a device mapping");
+  if (!aligned(attr.devicePointer, 16)) return fail(NSM_ERR_ALIGN, "src's device mapping is not 16-byte aligned");
+  e = launch_copy_h2d(dst, attr.devicePointer, bytes, ctas ? ctas : 16, reinterpret_cast<cudaStream_t>(stream_));
+  if (e != cudaSuccess) return fail_cuda(e, "copy launch");
+  return NSM_OK;
+}
+
 int nsm_bounds_selftest(nsm_stream_t stream_) {
   const cudaError_t e = launch_bounds_selftest(reinterpret_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return fail_cuda(e, "bounds self-test launch");

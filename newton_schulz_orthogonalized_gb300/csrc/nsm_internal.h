@@ -188,6 +188,9 @@ cudaError_t launch_adamw(const void* grads, float* params, float* m, float* v,
                          int64_t numel, float lr, float beta1, float beta2, float eps,
                          float wd, float bc1, float bc2, cudaStream_t stream);
 cudaError_t launch_gemm(const GemmLaunch& l, int num_sms, cudaStream_t stream);
+// bytes from page-locked host memory (src_mapped: its device mapping) to device memory, by
+// `ctas` CTAs of SM loads
+cudaError_t launch_copy_h2d(void* dst, const void* src_mapped, size_t bytes, int ctas, cudaStream_t stream);
 
 int* device_status_ptr();
 // One CTA whose bounded wait expires after limit_ns and records kDevTimeout.

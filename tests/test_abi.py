@@ -236,3 +236,16 @@ def test_checked_build_exports_the_same_symbols_and_reports_itself(nsm):
     assert not nsm.checked_build()
     with pytest.raises(nsm.NsmError):
         nsm.set_option(nsm.OPT_BOUNDS_CHECKS, 1)
+
+
+def test_copy_to_device_validation_without_gpu(nsm):
+    L = nsm.lib()
+    buf = ctypes.create_string_buffer(64)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert L.nsm_copy_to_device(None, base, 16, 0, None) == nsm.NSM_ERR_NULL
+    assert L.nsm_copy_to_device(base, None, 16, 0, None) == nsm.NSM_ERR_NULL
+    assert L.nsm_copy_to_device(base + 8, base, 16, 0, None) == nsm.NSM_ERR_ALIGN
+    assert L.nsm_copy_to_device(base, base + 4, 16, 0, None) == nsm.NSM_ERR_ALIGN
+    assert L.nsm_copy_to_device(base, base, 16, -1, None) == nsm.NSM_ERR_ARG
+    assert L.nsm_copy_to_device(base, base, 16, 1025, None) == nsm.NSM_ERR_ARG
+    assert L.nsm_copy_to_device(base, base, 0, 0, None) == nsm.NSM_OK  # nothing to copy
