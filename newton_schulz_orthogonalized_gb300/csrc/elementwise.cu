@@ -706,6 +706,12 @@ cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* m
 }
 
 cudaError_t launch_copy_h2d(void* dst, const void* src_mapped, size_t bytes, int ctas, cudaStream_t stream) {
+  // The copy runs beside the step's kernels, whose persistent GEMM CTAs take nearly all of
+  // an SM's shared memory: the copy asks for the same (largest) shared-memory carveout, so
+  // that its CTAs do not keep an SM in another configuration.
+  const cudaError_t carveout =
+      cudaFuncSetAttribute(k_copy_h2d, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (carveout != cudaSuccess) return carveout;
   const size_t units = bytes / 16;
   const int tail = static_cast<int>(bytes % 16);
   const auto* s = static_cast<const uint8_t*>(src_mapped);
