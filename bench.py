@@ -611,8 +611,13 @@ def _other_configs(nsm, names, method, dev, stream, peaks):
                 raise RuntimeError("a bounded device wait expired")
             kb = _kernels_block(per_kind, steps, peaks)
             graph_ms = _graph_steps(nsm, S, 50) if wl.muon_elements < 1e9 else None
+            g_ms, g_launches, g_flops = per_kind.get("k_ns_gemm", (0.0, 0, 0.0))
+            ortho = _orthogonalize_block(nsm, S, stream, max(2, min(steps, 10)), g_flops / steps,
+                                         peaks["bf16_tflops_sustained"]) if wl.muon_shapes else None
             out[name] = {"ms_per_step": ms, "steps": steps, "matrices": len(wl.muon_shapes),
                          "graph_ms_per_step": graph_ms,
+                         "orthogonalize_ms": ortho["ms"] if ortho else None,
+                         "ns_tflops_canonical": ortho["tflops_canonical"] if ortho else None,
                          "muon_elements": wl.muon_elements, "adam_elements": wl.adam_elements,
                          "gpu_launches_per_step": launches / steps,
                          "gemm_frac_executed": kb.get("k_ns_gemm", {}).get("frac"),
