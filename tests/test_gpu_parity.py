@@ -271,6 +271,30 @@ def test_step_ragged(nsm, method):
     Step(nsm, synth.custom(RAGGED, seed=5), method).check()
 
 
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_orthogonalize_extreme_aspect_ratios(nsm, method):
+    # Rows or columns past 2^16 (257 column tiles of 256, more than 1024 natural 64-wide
+    # tiles in a row), the tall transpose included: every tile index and coordinate of the
+    # layout and GEMM paths must stay exact.  With K = n of 65600 to 70000 in X X^T, the
+    # GPU's fp32 sums and the oracle's float64 sums round to different fp16 values often
+    # enough that the two fp16 iterations drift apart (about 1.4% for the standard form,
+    # 0.7-0.9% for gram), and each is as close to the exact iteration as the other: that,
+    # not the storage-oracle distance, is what is held here for the standard form.
+    shapes = [(130, 65600), (65600, 130), (260, 70000)]
+    wl = synth.custom(shapes, seed=19)
+    offsets, g, o = orthogonalize_gpu(nsm, wl, method)
+    for i, (r, c) in enumerate(shapes):
+        off = int(offsets[i])
+        gi = g[off:off + r * c].reshape(r, c)
+        got = o[off:off + r * c].reshape(r, c)
+        ref = oracle.orthogonalize(gi, method, 5, storage="method")
+        exact = oracle.orthogonalize(gi, method, 5)
+        name = f"ortho/extreme/{method}/{(r, c)}"
+        parity_log.record(name + "/vs_exact", rel=rel(got, exact), tol=rel(ref, exact))
+        assert rel(got, exact) <= 1.05 * rel(ref, exact) + 1e-3, (name, rel(got, exact), rel(ref, exact))
+        compare(got, ref, TOL_NS, name)
+
+
 # Direct matrices whose width is a multiple of 64 (slot stride = width) take flat
 # 4096-element runs in the layout and apply passes; other direct matrices keep 64 x 64
 # tiles, and tall ones the transposing tiles.  200x192 ends in a partial run; 256x1000 is
