@@ -168,8 +168,8 @@ def pack_offsets(shapes: Sequence[Tuple[int, int]], align: int = 64) -> Tuple[Li
     """Element offsets of each matrix inside one contiguous packed buffer.
 
     [DMZ] §两种packed buffer生命周期 — all Muon-target parameters of one owner are packed
-    into one contiguous buffer.  The layout is this build's choice: matrices in table
-    order, each starting on a multiple of ``align`` elements.  Returns the offsets and
+    into one contiguous buffer.  The page fixes no layout; the reading taken: matrices in
+    table order, each starting on a multiple of ``align`` elements.  Returns the offsets and
     the total number of elements (the end of the last matrix, rounded up likewise).
     """
     if align <= 0:
