@@ -30,6 +30,9 @@ Readings taken where the pages are silent (each is listed again in the design no
 * storage precision: fp16 for both forms (the page calls the standard form stable in
   bf16 and gives fp16 to the gram form for accuracy); "standard_bf16" keeps bf16;
   ``storage="method"`` rounds at exactly the points where the method stores.
+* the normalised input in storage precision: ``X = s * rnd(U)``, with ``s = 1/(||U||_F +
+  eps)`` and ``rnd`` rounding U to the format's significant bits at any exponent; the
+  scalar s multiplies the products that read X, unrounded (:func:`round_significand`).
 * update scale ``sqrt(max(1, rows/cols))`` of the original (untransposed) matrix.
 * AdamW: the textbook decoupled form with bias correction, eps outside the square
   root, step counter starting at 1.
@@ -115,6 +118,27 @@ def round_to(x, fmt):
     r = np.rint(xf / ulp) * ulp
     r[np.abs(r) > vmax] = np.inf * np.sign(r[np.abs(r) > vmax])
     out[finite] = r
+    return out
+
+
+def round_significand(x, fmt):
+    """Round float64 values to ``fmt``'s significant bits (ties to even) at any exponent.
+
+    This is :func:`round_to` without the format's exponent range: no subnormal spacing,
+    no overflow.  It is what storing ``2**k x`` in ``fmt`` and scaling back by ``2**-k``
+    gives whenever ``2**k x`` lies in the format's normal range, since a power of two
+    commutes with the rounding there.
+    """
+    if fmt is None:
+        return np.asarray(x, dtype=np.float64)
+    p = _FORMATS[fmt][0]
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x, dtype=np.float64, copy=True)
+    finite = np.isfinite(x) & (x != 0)
+    xf = x[finite]
+    _, e2 = np.frexp(np.abs(xf))           # |x| = f * 2**e2 with f in [0.5, 1)
+    ulp = np.ldexp(1.0, (e2 - p).astype(np.int64))
+    out[finite] = np.rint(xf / ulp) * ulp
     return out
 
 
@@ -235,14 +259,17 @@ def ns_poly_iterated(x, steps: int = NS_STEPS, a: float = NS_A, b: float = NS_B,
 # --- a4: Newton-Schulz, standard form -----------------------------------------------
 
 def ns_standard(x: np.ndarray, steps: int = NS_STEPS, a: float = NS_A, b: float = NS_B,
-                c: float = NS_C, storage=None) -> np.ndarray:
+                c: float = NS_C, storage=None, input_stored: bool = False) -> np.ndarray:
     """Standard quintic Newton-Schulz on an already normalised ``m x n`` iterate.
 
     [DSM] §核心算子 (``zeropower_via_newtonschulz5``): each step forms
     ``A = X X^T``, ``B = b A + c A A`` and replaces ``X`` by ``a X + B X``.  With
-    ``storage`` the input, ``A``, ``B`` and every new ``X`` are rounded to that format.
+    ``storage`` the input (unless ``input_stored``: the caller has stored it already),
+    ``A``, ``B`` and every new ``X`` are rounded to that format.
     """
-    x = _store(np.array(x, dtype=np.float64), storage)
+    x = np.array(x, dtype=np.float64)
+    if not input_stored:
+        x = _store(x, storage)
     for _ in range(steps):
         gram_a = _store(x @ x.T, storage)
         poly_b = _store(b * gram_a + c * (gram_a @ gram_a), storage)
@@ -253,7 +280,8 @@ def ns_standard(x: np.ndarray, steps: int = NS_STEPS, a: float = NS_A, b: float 
 # --- a4': Newton-Schulz, gram form ----------------------------------------------------
 
 def ns_gram(x: np.ndarray, steps: int = NS_STEPS, a: float = NS_A, b: float = NS_B,
-            c: float = NS_C, storage=None, restart_every: int = GRAM_RESTART_EVERY) -> np.ndarray:
+            c: float = NS_C, storage=None, restart_every: int = GRAM_RESTART_EVERY,
+            input_stored: bool = False) -> np.ndarray:
     """Gram-form Newton-Schulz: iterate on the small square ``R = X X^T``.
 
     [DSM] §核心算子 (``zeropower_via_gram_newtonschulz``) says the variant iterates on
@@ -278,7 +306,9 @@ def ns_gram(x: np.ndarray, steps: int = NS_STEPS, a: float = NS_A, b: float = NS
     triangle determines it, a five-step chain costs ``3 m^2 (n - m)`` flops less with
     every 3 than with every 2.
     """
-    x = _store(np.array(x, dtype=np.float64), storage)
+    x = np.array(x, dtype=np.float64)
+    if not input_stored:
+        x = _store(x, storage)
     m = x.shape[0]
     eye = np.eye(m)
     r = _store(x @ x.T, storage)
@@ -298,12 +328,13 @@ def ns_gram(x: np.ndarray, steps: int = NS_STEPS, a: float = NS_A, b: float = NS
 
 
 def newton_schulz(x: np.ndarray, method: str = NS_METHOD_DEFAULT, steps: int = NS_STEPS,
-                  a: float = NS_A, b: float = NS_B, c: float = NS_C, storage=None) -> np.ndarray:
+                  a: float = NS_A, b: float = NS_B, c: float = NS_C, storage=None,
+                  input_stored: bool = False) -> np.ndarray:
     """Dispatch on ``ns_method`` ([DSM] §核心算子: ``NS_METHODS = {standard, gram}``)."""
     if method in ("standard", "standard_bf16"):
-        return ns_standard(x, steps, a, b, c, storage)
+        return ns_standard(x, steps, a, b, c, storage, input_stored=input_stored)
     if method == "gram":
-        return ns_gram(x, steps, a, b, c, storage)
+        return ns_gram(x, steps, a, b, c, storage, input_stored=input_stored)
     raise ValueError(f"unknown ns_method {method!r}")
 
 
@@ -319,6 +350,11 @@ def orthogonalize(u: np.ndarray, method: str = NS_METHOD_DEFAULT, steps: int = N
 
     Returns ``O`` with the shape of ``u``.  ``storage="method"`` stores the iterates in
     the method's format (:func:`method_storage`); ``None`` is exact.
+
+    In storage precision the normalised input ``X = U / (||U||_F + eps)`` ([DSM]
+    §核心算子: the normalisation before the iteration) is held as ``s * rnd(U)``: U
+    rounded once to the format's significant bits (:func:`round_significand`) and the
+    scalar ``s = 1/(||U||_F + eps)``, of the unrounded U, multiplying it in float64.
     """
     u = np.asarray(u, dtype=np.float64)
     if u.ndim != 2:
@@ -327,8 +363,12 @@ def orthogonalize(u: np.ndarray, method: str = NS_METHOD_DEFAULT, steps: int = N
     rows, cols = u.shape
     transposed = rows > cols
     x = u.T if transposed else u
-    x = frobenius_normalize(x, eps)
-    o = newton_schulz(x, method, steps, storage=storage)
+    if storage is None:
+        o = newton_schulz(frobenius_normalize(x, eps), method, steps)
+    else:
+        scale = 1.0 / (math.sqrt(float(np.sum(x * x))) + eps)
+        o = newton_schulz(scale * round_significand(x, storage), method, steps, storage=storage,
+                          input_stored=True)
     return o.T if transposed else o
 
 

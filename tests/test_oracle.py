@@ -414,6 +414,68 @@ def test_round_to_matches_library_conversions():
         assert np.array_equal(oracle.round_to(x, "fp16"), f16), scale
 
 
+def test_round_significand_by_hand():
+    # the format's significant bits, at any exponent: no subnormal spacing, no overflow
+    for e in (-60, -30, 0, 20, 70):
+        two = 2.0 ** e
+        assert oracle.round_significand(two * (1 + 2 ** -11), "fp16") == two            # tie -> even
+        assert oracle.round_significand(two * (1 + 3 * 2 ** -11), "fp16") == two * (1 + 2 ** -9)
+        assert oracle.round_significand(two * (1 + 2 ** -8), "bf16") == two             # tie -> even
+        assert oracle.round_significand(-two * (1 + 2 ** -8 + 2 ** -20), "bf16") == -two * (1 + 2 ** -7)
+    assert oracle.round_significand(65520.0, "fp16") == 65536.0   # halfway to 2^16, no overflow
+    assert oracle.round_significand(3 * 2 ** -40, "fp16") == 3 * 2 ** -40
+    assert oracle.round_significand(0.0, "fp16") == 0.0
+
+
+def test_round_significand_is_power_of_two_scaled_library_rounding():
+    import torch
+    rng = np.random.default_rng(3)
+    for scale in (1e-30, 1e-3, 1.0, 1e4, 1e30):
+        x32 = (rng.standard_normal(20000) * scale).astype(np.float32)
+        x = x32.astype(np.float64)
+        # a power of two that puts the largest magnitude in [2^11, 2^12): the library's
+        # fp16 rounding of 2^k x, scaled back, wherever 2^k x is a normal fp16 number
+        _, e = np.frexp(np.max(np.abs(x)))
+        k = 12 - int(e)
+        y = np.ldexp(x, k)
+        normal = np.abs(y) >= 2.0 ** -14
+        f16 = np.ldexp(y.astype(np.float16).astype(np.float64), -k)
+        got = oracle.round_significand(x, "fp16")
+        assert np.array_equal(got[normal], f16[normal]), scale
+        assert normal.mean() > 0.999
+        bf = np.ldexp(torch.from_numpy(y.astype(np.float32)).to(torch.bfloat16).double().numpy(), -k)
+        assert np.array_equal(oracle.round_significand(x, "bf16"), bf), scale
+
+
+def test_orthogonalize_stores_the_input_as_rounded_u_times_its_scale():
+    # with no Newton-Schulz step the result is the stored input itself: U rounded to
+    # fp16's 11 significant bits, times s = 1/(||U||_F + eps) of the unrounded U.  Entries
+    # far below fp16's normal range after normalisation keep their 11 bits.
+    u = np.array([[1.0 + 2 ** -12, 2.0 ** -30, -3.0],
+                  [0.5, -(2.0 ** -36) * (1 + 2 ** -9), 0.0]])
+    s = 1.0 / (math.sqrt(float(np.sum(u * u))) + 1e-7)
+    want = s * np.array([[1.0, 2.0 ** -30, -3.0],
+                         [0.5, -(2.0 ** -36) * (1 + 2 ** -9), 0.0]])
+    got = oracle.orthogonalize(u, "standard", 0, storage="fp16")
+    assert np.array_equal(got, want)
+    # the entry of magnitude 2^-30 s (about 1e-9) is below fp16's smallest subnormal:
+    # rounding after the scale would have flushed it
+    assert got[0, 1] != 0 and oracle.round_to(s * u[0, 1], "fp16") == 0.0
+    # tall matrices are stored transposed, then transposed back
+    assert np.array_equal(oracle.orthogonalize(u.T, "gram", 0, storage="fp16"), want.T)
+
+
+@pytest.mark.parametrize("method", ["standard", "gram", "standard_bf16"])
+def test_storage_mode_invariant_under_power_of_two_scale(method):
+    # eps = 0: s scales inversely with U, and rounding U to its significand commutes with
+    # a power of two, so the stored iteration gives the same bits at any magnitude
+    rng = np.random.default_rng(5)
+    u = rng.standard_normal((6, 11))
+    want = oracle.orthogonalize(u, method, eps=0.0, storage="method")
+    for j in (-70, -20, 15, 60):
+        assert np.array_equal(oracle.orthogonalize(np.ldexp(u, j), method, eps=0.0, storage="method"), want), j
+
+
 def test_method_storage_formats():
     assert oracle.method_storage("standard") == "fp16"
     assert oracle.method_storage("gram") == "fp16"
