@@ -453,7 +453,9 @@ def _kernels_block(per_kind, steps, peaks):
     out = {}
     for kname, (k_ms, k_n, k_work) in per_kind.items():
         flops = kname in FLOP_KERNELS
-        ach = (k_work / (k_ms * 1e-3) / (1e12 if flops else 1e9)) if k_ms > 0 else None
+        # work 0: a pass whose bytes depend on the data (the step's second layout pass,
+        # which rewrites only matrices whose exponent was out of range)
+        ach = (k_work / (k_ms * 1e-3) / (1e12 if flops else 1e9)) if k_ms > 0 and k_work > 0 else None
         out[kname] = {"launches": k_n, "ms_per_step": k_ms / steps, "achieved": ach,
                       "unit": "TFLOP/s" if flops else "GB/s",
                       "frac": (ach / (peak_t if flops else peaks["hbm_gbs"])) if ach else None}

@@ -126,11 +126,23 @@ size_t muon_workspace_bytes(const int32_t* shapes, int n, int ns_method, int ns_
  *   offsets       host, n int64 element offsets (shared by the three buffers)
  *   shapes        host, n {rows, cols}
  *   workspace     device, >= muon_workspace_bytes(shapes, n, ns_method, ns_steps)
- *                 bytes, 256-byte aligned; overwritten; contents not needed between calls
+ *                 bytes, 256-byte aligned; overwritten, except that its first 4n bytes
+ *                 carry one exponent per matrix from one call to the next (below)
  *   stream        stream to launch on
- * Grads must not alias params or momentum.  Deterministic: identical inputs give
- * bit-identical outputs, and a matrix's result does not depend on the other matrices
- * in the table. */
+ * Grads must not alias params or momentum.
+ * Storage of X: the chain's input is held as U 2^k rounded once to the storage format,
+ * k a per-matrix power of two, and s 2^-k (s = 1/(||U||_F + 1e-7)) multiplies the
+ * products that read it; X is therefore s times U rounded to the format's significant
+ * bits, with no range limit.  The norm is known only after the pass over U, so the step
+ * stores U 2^k with the exponent the previous call on this table and workspace chose
+ * (the first 4n bytes of the workspace) and makes a second pass over G and M only for
+ * the matrices where that k put max|U| 2^k outside [2^4, 2^15): on the first call, or
+ * after the gradients' magnitude jumps by a factor of about 16 or more.  Any content of
+ * those bytes is safe.
+ * Deterministic: identical inputs give bit-identical outputs whatever those bytes hold
+ * (a power of two commutes with the rounding; only entries of U more than 2^18 below
+ * their matrix's largest, which fp16 keeps as subnormals, can round differently), and a
+ * matrix's result does not depend on the other matrices in the table. */
 int muon_step(const void* packed_grads, float* packed_params, float* momentum,
               const int64_t* offsets, const int32_t* shapes, int n,
               float lr, float wd, float mu, int ns_method, int ns_steps, int nesterov,
@@ -150,7 +162,9 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
 /* Orthogonalisation only: out_i = NS(in_i / (||in_i||_F + 1e-7)) for every matrix of a
  * packed bf16 group (the same transpose rule and methods as muon_step).  in_bf16 and
  * out_bf16 are device bf16 buffers sharing the offsets table; they may not overlap.
- * Used to check and time the Newton-Schulz chain on its own. */
+ * The input is held as in_i 2^k with k from a first pass over in_i (its sums and
+ * largest entry), exact in the storage format for bf16 entries within 2^26 of the
+ * largest.  Used to check and time the Newton-Schulz chain on its own. */
 int muon_orthogonalize(const void* in_bf16, void* out_bf16,
                        const int64_t* offsets, const int32_t* shapes, int n,
                        int ns_method, int ns_steps,
@@ -232,7 +246,7 @@ int nsm_device_status(nsm_stream_t stream, int* status_out);
 #define NSM_KERNEL_GEMM_PAIR  2  /* k_ns_gemm_pair: the 2-SM grouped GEMM */
 #define NSM_KERNEL_SMALL      3  /* k_ns_small: whole chains of matrices with m <= 128 */
 #define NSM_KERNEL_SELFTEST   4  /* the kernels of nsm_status_selftest / nsm_bounds_selftest */
-#define NSM_KERNEL_MOMENTUM   5  /* k_momentum_norm (bounds checks only) */
+#define NSM_KERNEL_MOMENTUM   5  /* k_momentum_class, k_grad_norm (bounds checks only) */
 #define NSM_KERNEL_TO_CLASS   6  /* k_to_class (bounds checks only) */
 #define NSM_KERNEL_FROM_CLASS 7  /* k_from_class: apply or export (bounds checks only) */
 #define NSM_KERNEL_ADAMW      8  /* k_adamw (bounds checks only) */
@@ -315,14 +329,18 @@ int nsm_copy_to_device(void* dst, const void* src, size_t bytes, int ctas, nsm_s
  * *work (the algorithmic work of those launches: flops for NSM_KIND_GEMM, bytes that
  * must cross HBM for the other kinds).  nsm_timing_read is the GEMM kind.  Any output
  * pointer may be NULL.  Not for use inside stream capture. */
-#define NSM_KIND_GEMM     0  /* Newton-Schulz GEMM stages (tensor cores) */
-#define NSM_KIND_MOMENTUM 1  /* momentum update + chunk sums of U^2 */
-#define NSM_KIND_NORM     2  /* per-matrix norm from the chunk sums */
-#define NSM_KIND_LAYOUT   3  /* X = s U into the working layout */
-#define NSM_KIND_APPLY    4  /* decay + apply (or the export of O) */
-#define NSM_KIND_ADAMW    5  /* AdamW */
-#define NSM_KIND_SMALL    6  /* whole Newton-Schulz chains of matrices with m <= 128 (bytes:
-                                 every read and write of X; the kernel is HBM-bound) */
+#define NSM_KIND_GEMM      0  /* Newton-Schulz GEMM stages (tensor cores) */
+#define NSM_KIND_MOMENTUM  1  /* the step's pass: momentum update, U 2^k into the working
+                                  layout, per-tile sums of U^2 and largest |U| */
+#define NSM_KIND_NORM      2  /* per-matrix norm, exponent and input factor */
+#define NSM_KIND_LAYOUT    3  /* U 2^k into the working layout: the orthogonalisation's pass,
+                                  and the step's second pass (work 0: it rewrites only the
+                                  matrices whose exponent was out of range, usually none) */
+#define NSM_KIND_APPLY     4  /* decay + apply (or the export of O) */
+#define NSM_KIND_ADAMW     5  /* AdamW */
+#define NSM_KIND_SMALL     6  /* whole Newton-Schulz chains of matrices with m <= 128 (bytes:
+                                  every read and write of X; the kernel is HBM-bound) */
+#define NSM_KIND_GRAD_NORM 7  /* the orthogonalisation's pass: sums of G^2, largest |G| */
 int nsm_timing_enable(int enable);
 int nsm_timing_read(double* gemm_ms, int64_t* gemm_launches, double* gemm_flops);
 int nsm_timing_read_kind(int kind, double* ms, int64_t* launches, double* work);

@@ -426,10 +426,10 @@ def timing_reset() -> None:
     lib().nsm_timing_reset()
 
 
-KIND_GEMM, KIND_MOMENTUM, KIND_NORM, KIND_LAYOUT, KIND_APPLY, KIND_ADAMW, KIND_SMALL = range(7)
-KIND_NAMES = {KIND_GEMM: "k_ns_gemm", KIND_MOMENTUM: "k_momentum_norm", KIND_NORM: "k_norm_finalize",
+KIND_GEMM, KIND_MOMENTUM, KIND_NORM, KIND_LAYOUT, KIND_APPLY, KIND_ADAMW, KIND_SMALL, KIND_GRAD_NORM = range(8)
+KIND_NAMES = {KIND_GEMM: "k_ns_gemm", KIND_MOMENTUM: "k_momentum_class", KIND_NORM: "k_scale_finalize",
               KIND_LAYOUT: "k_to_class", KIND_APPLY: "k_from_class", KIND_ADAMW: "k_adamw",
-              KIND_SMALL: "k_ns_small"}
+              KIND_SMALL: "k_ns_small", KIND_GRAD_NORM: "k_grad_norm"}
 
 
 def timing_read(kind: int = KIND_GEMM) -> Tuple[float, int, float]:

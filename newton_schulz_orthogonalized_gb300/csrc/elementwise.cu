@@ -1,16 +1,30 @@
 // Memory-bound kernels of the Muon step and the fused AdamW step.
 //
-//   k_momentum_norm  M <- mu M + G; per-chunk sums of U^2 with U = G + mu M (Nesterov)
-//                    or M, in fp32 (fixed order)
-//   k_norm_finalize  s_i = 1 / (sqrt(sum of matrix i's chunk sums) + eps), fixed order
-//   k_to_class       X = s U with U recomputed in fp32 from G and the updated M, moved
-//                    from the natural row-major layout into the matrix's slot
-//                    (transposed when rows > cols) and rounded once to bf16 or fp16
-//   k_from_class     APPLY: p <- p (1 - lr wd) - lr sqrt(max(1, rows/cols)) O, O read
-//                    back from the slot (transposed back when rows > cols), with the
-//                    bf16 copy of p when asked; otherwise O copied to a natural bf16
-//                    layout (the export of muon_orthogonalize)
-//   k_adamw          decoupled-weight-decay Adam on a flat group
+//   k_momentum_class  M <- mu M + G and U = G + mu M (Nesterov) or M, in one pass: M
+//                     written back, U 2^k (k from the matrix's exponent hint) moved from
+//                     the natural row-major layout into the matrix's slot (transposed
+//                     when rows > cols) and rounded once to bf16 or fp16; per-tile sums of
+//                     U^2 and largest |U|, in fp32 (fixed order)
+//   k_grad_norm       per-chunk sums of G^2 and largest |G| (the orthogonalisation)
+//   k_scale_finalize  s_i = 1 / (sqrt(sum of matrix i's partial sums) + eps), fixed order;
+//                     the exponent k_i that puts max|U| 2^k in [2^11, 2^12); the input
+//                     factor s_i 2^-k_i of the chain's products that read X
+//   k_to_class        U 2^k (U recomputed in fp32 from G and the updated M, or U = G) into
+//                     the slot: the orthogonalisation's layout pass, and the step's second
+//                     pass over the matrices whose hint was out of range
+//   k_from_class      APPLY: p <- p (1 - lr wd) - lr sqrt(max(1, rows/cols)) O, O read
+//                     back from the slot (transposed back when rows > cols), with the
+//                     bf16 copy of p when asked; otherwise O copied to a natural bf16
+//                     layout (the export of muon_orthogonalize)
+//   k_adamw           decoupled-weight-decay Adam on a flat group
+//
+// The normalised input X = s U is stored as U 2^k: a power of two commutes with the
+// rounding wherever U 2^k is a normal value of the format, so the stored X is s times U
+// rounded to the format's significant bits, whichever k was used, and s 2^-k enters the
+// products that read it in fp32.  A step knows each matrix's norm only after its pass
+// over U, so it stores U with the exponent the previous step chose (kept in the
+// workspace) and stores it again, in a second pass, only where that exponent put max|U|
+// 2^k outside [2^4, 2^15).
 //
 // The layout kernels work in units of 64 x 64 natural tiles.  A tall matrix's tile is
 // transposed through shared memory; a direct matrix whose slot stride equals its width
@@ -114,18 +128,37 @@ __device__ __forceinline__ void store8(void* base, int64_t i, const float (&f)[8
       FP16 ? pack_f16x8(f) : pack_bf16x8(f);
 }
 
-__device__ __forceinline__ float block_sum(float v, float* scratch) {
+// Sum and largest value over the block, in a fixed order; valid in thread 0.  One barrier:
+// a caller that reduces again alternates between two scratch buffers.
+__device__ __forceinline__ void block_sum_max(float& sum, float& mx, float (*scratch)[kThreads / 32]) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
   const int warp = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) scratch[warp] = v;
-  __syncthreads();
-  float s = 0.f;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < kThreads / 32; ++w) s += scratch[w];
+  if ((threadIdx.x & 31) == 0) {
+    scratch[0][warp] = sum;
+    scratch[1][warp] = mx;
   }
   __syncthreads();
-  return s;
+  if (threadIdx.x == 0) {
+    sum = 0.f;
+    mx = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      sum += scratch[0][w];
+      mx = fmaxf(mx, scratch[1][w]);
+    }
+  }
+}
+
+// 2^k for k in [-126, 127] (built from its bits: exact)
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((k + 127) << 23); }
+__device__ __forceinline__ int clamp_exp(int k) { return max(-kInExpClamp, min(kInExpClamp, k)); }
+// e with x = f 2^e, f in [0.5, 1), of a positive finite x (subnormals count as 2^-126)
+__device__ __forceinline__ int frexp_exponent(float x) {
+  const int biased = (__float_as_int(x) >> 23) & 0xff;
+  return (biased == 0 ? 1 : biased) - 126;
 }
 
 // ---------------------------------------------------------------- bounds checks
@@ -145,80 +178,96 @@ __device__ __forceinline__ bool slot_run(const MatInfo& mt, int row, int col, in
          (w == 1 || ((mt.slot + static_cast<int64_t>(row) * mt.ld + col) & 7) == 0);
 }
 
-// ---------------------------------------------------------------- momentum + norm
+// ---------------------------------------------------------------- norms
 
-template <bool HAS_M, bool NESTEROV>
+// Per chunk of kChunk natural elements: sum of G^2 and largest |G|.
 __global__ void __launch_bounds__(kThreads)
-    k_momentum_norm(const __nv_bfloat16* __restrict__ grads, float* __restrict__ mom,
-                    const MatInfo* __restrict__ mats, int nmats, int total_chunks,
-                    float* __restrict__ partials, float mu, int* status) {
+    k_grad_norm(const __nv_bfloat16* __restrict__ grads, const MatInfo* __restrict__ mats, int nmats,
+                int total_chunks, float* __restrict__ partials, int* status) {
   grid_dependency_sync();  // inputs come from the previous kernel of the stream
   release_dependents();
-  __shared__ float scratch[kThreads / 32];
+  __shared__ float scratch[2][2][kThreads / 32];
+  constexpr int K = NSM_KERNEL_MOMENTUM;
+  int rb = 0;
   for (int chunk = blockIdx.x; chunk < total_chunks; chunk += gridDim.x) {
     const MatInfo& mt = mats[find_by_chunk(mats, nmats, chunk)];
     const int64_t len = static_cast<int64_t>(mt.rows) * mt.cols;
     const int64_t start = static_cast<int64_t>(chunk - mt.chunk_begin) * kChunk;
     const int64_t end = min(start + static_cast<int64_t>(kChunk), len);
     const __nv_bfloat16* g = grads + mt.off;
-    float* m = HAS_M ? mom + mt.off : nullptr;
-    float acc = 0.f;
+    float acc = 0.f, mx = 0.f;
     const int64_t nvec = (end - start) >> 3;
     for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
       const int64_t i = start + v * 8;
-      // G is read and M read and written at the same 8 elements
-      if (!bounds_ok(natural_run(mt.off, i, 8, len), status, NSM_KERNEL_MOMENTUM, 0, NSM_SITE_NATURAL_LOAD)) continue;
+      if (!bounds_ok(natural_run(mt.off, i, 8, len), status, K, 0, NSM_SITE_NATURAL_LOAD)) continue;
       float gf[8];
       unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(g + i)), gf);
-      if (HAS_M) {
-        float4* mp = reinterpret_cast<float4*>(m + i);
-        const float4 m0 = mp[0], m1 = mp[1];
-        float mf[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float mn = fmaf(mu, mf[j], gf[j]);
-          mf[j] = mn;
-          const float u = NESTEROV ? fmaf(mu, mn, gf[j]) : mn;
-          acc = fmaf(u, u, acc);
-        }
-        mp[0] = make_float4(mf[0], mf[1], mf[2], mf[3]);
-        mp[1] = make_float4(mf[4], mf[5], mf[6], mf[7]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc = fmaf(gf[j], gf[j], acc);
+      for (int j = 0; j < 8; ++j) {
+        acc = fmaf(gf[j], gf[j], acc);
+        mx = fmaxf(mx, fabsf(gf[j]));
       }
     }
     for (int64_t i = start + nvec * 8 + threadIdx.x; i < end; i += kThreads) {
-      if (!bounds_ok(natural_run(mt.off, i, 1, len), status, NSM_KERNEL_MOMENTUM, 0, NSM_SITE_NATURAL_LOAD)) continue;
+      if (!bounds_ok(natural_run(mt.off, i, 1, len), status, K, 0, NSM_SITE_NATURAL_LOAD)) continue;
       const float gv = __bfloat162float(g[i]);
-      if (HAS_M) {
-        const float mn = fmaf(mu, m[i], gv);
-        m[i] = mn;
-        const float uv = NESTEROV ? fmaf(mu, mn, gv) : mn;
-        acc = fmaf(uv, uv, acc);
-      } else {
-        acc = fmaf(gv, gv, acc);
-      }
+      acc = fmaf(gv, gv, acc);
+      mx = fmaxf(mx, fabsf(gv));
     }
-    const float s = block_sum(acc, scratch);
-    if (threadIdx.x == 0) partials[chunk] = s;
+    block_sum_max(acc, mx, scratch[rb]);
+    if (threadIdx.x == 0) {
+      partials[chunk] = acc;
+      partials[total_chunks + chunk] = mx;
+    }
+    rb ^= 1;
   }
 }
 
-__global__ void k_norm_finalize(const MatInfo* __restrict__ mats, int nmats,
-                                const float* __restrict__ partials, float* __restrict__ scales,
-                                float eps) {
+// One block per matrix: sums and maxima of its partials (parts[begin + c] and
+// parts[nparts + begin + c]), then s, the exponent and the input factor.
+__global__ void __launch_bounds__(kThreads)
+    k_scale_finalize(const MatInfo* __restrict__ mats, int nmats, const float* __restrict__ parts,
+                     int64_t nparts, int by_tile, int* __restrict__ hints, float* __restrict__ layout_scale,
+                     int* __restrict__ redo, float* __restrict__ xs, float* __restrict__ xs_cls, float eps) {
   grid_dependency_sync();  // inputs come from the previous kernel of the stream
   release_dependents();
-  const int w = static_cast<int>((blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (w >= nmats) return;
-  const MatInfo& mt = mats[w];
-  float s = 0.f;
-  for (int c = lane; c < mt.nchunks; c += 32) s += partials[mt.chunk_begin + c];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) scales[w] = 1.0f / (sqrtf(s) + eps);
+  __shared__ float scratch[2][2][kThreads / 32];
+  int rb = 0;
+  for (int i = blockIdx.x; i < nmats; i += gridDim.x) {
+    const MatInfo& mt = mats[i];
+    const int per = by_tile ? kTileParts : 1;  // partials per unit
+    const int64_t begin = (by_tile ? mt.tile_begin : mt.chunk_begin) * per;
+    const int64_t count = (by_tile ? static_cast<int64_t>((mt.rows + kTile - 1) / kTile) * ((mt.cols + kTile - 1) / kTile)
+                                   : mt.nchunks) * per;
+    float sum = 0.f, mx = 0.f;
+    for (int64_t c = threadIdx.x; c < count; c += kThreads) {
+      sum += parts[begin + c];
+      mx = fmaxf(mx, parts[nparts * per + begin + c]);
+    }
+    block_sum_max(sum, mx, scratch[rb]);
+    rb ^= 1;
+    if (threadIdx.x != 0) continue;
+    const float s = 1.0f / (sqrtf(sum) + eps);
+    // no exponent follows from an all-zero or non-finite matrix: its hint stands
+    const bool has_max = mx > 0.f && mx < INFINITY;
+    const int e = has_max ? frexp_exponent(mx) : 0;
+    int k;
+    if (hints) {
+      const int used = clamp_exp(hints[i]);
+      const bool ok = !has_max || (e + used >= kInMinExp && e + used <= kInMaxExp);
+      const int next = has_max ? clamp_exp(kInTargetExp - e) : used;
+      k = ok ? used : next;
+      layout_scale[i] = ok ? 0.f : pow2f(k);
+      if (!ok) *redo = 1;
+      hints[i] = next;
+    } else {
+      k = has_max ? clamp_exp(kInTargetExp - e) : 0;
+      layout_scale[i] = pow2f(k);
+    }
+    const float f = s * pow2f(-k);
+    xs[i] = f;
+    xs_cls[mt.cls_pos] = f;
+  }
 }
 
 // ---------------------------------------------------------------- layout moves
@@ -260,23 +309,196 @@ __device__ __forceinline__ float load_u1(const __nv_bfloat16* g, const float* m,
   return fmaf(mu, m[i], __bfloat162float(g[i]));
 }
 
-// X = s U moved from the natural row-major layout (row stride cols) into the matrix's
-// slot (row stride ld), transposed when rows > cols, rounded once to bf16/fp16.
-template <bool TO_FP16, int MODE>
+// The step's pass over G and M: M <- mu M + G written back in place, U = G + mu M
+// (Nesterov) or M stored as U 2^k (k = the matrix's hint) into the slot (row stride ld),
+// transposed when rows > cols, rounded once to bf16/fp16; per tile the sum of U^2 and the
+// largest |U| (tparts[t], tparts[total_tiles + t]).
+template <bool TO_FP16, bool NESTEROV>
 __global__ void __launch_bounds__(kThreads)
-    k_to_class(const __nv_bfloat16* __restrict__ grads, const float* __restrict__ mom, float mu,
-               void* __restrict__ dst, const MatInfo* __restrict__ mats, int nmats,
-               int64_t total_tiles, const float* __restrict__ scales, int* status) {
+    k_momentum_class(const __nv_bfloat16* __restrict__ grads, float* __restrict__ mom, float mu,
+                     void* __restrict__ dst, const MatInfo* __restrict__ mats, int nmats,
+                     int64_t total_tiles, const int* __restrict__ hints, float* __restrict__ tparts,
+                     int* __restrict__ redo, int* status) {
   grid_dependency_sync();  // inputs come from the previous kernel of the stream
   release_dependents();
   __shared__ float tile[kTile][kTile + 1];
+  __shared__ float scratch[2][2][kThreads / 32];
+  static_assert(kTileParts == 1 || kTileParts == kThreads / 32, "one partial per tile, or one per warp");
+  constexpr int K = NSM_KERNEL_MOMENTUM;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *redo = 0;  // the finalize kernel sets it
+  int rb = 0;
   for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
     const TilePos tp = tile_pos(mats, nmats, t);
     const MatInfo& mt = mats[tp.mi];
     const __nv_bfloat16* g = grads + mt.off;
+    float* m = mom + mt.off;
+    const int64_t d0 = mt.slot;
+    const float sc = pow2f(clamp_exp(hints[tp.mi]));
+    const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
+    const int64_t len = static_cast<int64_t>(rows) * cols;
+    float acc = 0.f, mx = 0.f;
+    // G read, M read and written at the eight natural elements from i; U into u
+    auto step8 = [&](int64_t i, float (&u)[8]) {
+      float gf[8];
+      unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(g + i)), gf);
+      float4* mp = reinterpret_cast<float4*>(m + i);
+      const float4 m0 = mp[0], m1 = mp[1];
+      float mf[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float mn = fmaf(mu, mf[j], gf[j]);
+        mf[j] = mn;
+        u[j] = NESTEROV ? fmaf(mu, mn, gf[j]) : mn;
+        acc = fmaf(u[j], u[j], acc);
+        mx = fmaxf(mx, fabsf(u[j]));
+      }
+      mp[0] = make_float4(mf[0], mf[1], mf[2], mf[3]);
+      mp[1] = make_float4(mf[4], mf[5], mf[6], mf[7]);
+    };
+    auto step1 = [&](int64_t i) {
+      const float gv = __bfloat162float(g[i]);
+      const float mn = fmaf(mu, m[i], gv);
+      m[i] = mn;
+      const float uv = NESTEROV ? fmaf(mu, mn, gv) : mn;
+      acc = fmaf(uv, uv, acc);
+      mx = fmaxf(mx, fabsf(uv));
+      return uv;
+    };
+    if (!mt.transposed) {
+      if ((mt.flags & kMatVec) && ld == cols) {
+        // slot and natural layouts coincide: the matrix's k-th tile is its k-th run of
+        // kTile^2 consecutive elements, streamed contiguously
+        const int64_t base = (t - mt.tile_begin) * (kTile * kTile);
+        for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+          const int64_t i = base + static_cast<int64_t>(j) * 8;
+          if (i < len) {
+            if (!bounds_ok(natural_run(mt.off, i, 8, len), status, K, 0, NSM_SITE_NATURAL_LOAD)) continue;
+            float u[8];
+            step8(i, u);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) u[q] *= sc;
+            if (!bounds_ok(slot_run(mt, static_cast<int>(i / ld), static_cast<int>(i % ld), 8), status, K, 0,
+                           NSM_SITE_SLOT_STORE)) continue;
+            store8<TO_FP16>(dst, d0 + i, u);
+          }
+        }
+      } else if (mt.flags & kMatVec) {
+        for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+          const int r = tp.r0 + (j >> 3), c = tp.c0 + (j & 7) * 8;
+          if (r < rows && c < cols) {
+            const int64_t i = static_cast<int64_t>(r) * cols + c;
+            if (!bounds_ok(natural_run(mt.off, i, 8, len), status, K, 0, NSM_SITE_NATURAL_LOAD)) continue;
+            float u[8];
+            step8(i, u);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) u[q] *= sc;
+            if (!bounds_ok(slot_run(mt, r, c, 8), status, K, 0, NSM_SITE_SLOT_STORE)) continue;
+            store8<TO_FP16>(dst, d0 + static_cast<int64_t>(r) * ld + c, u);
+          }
+        }
+      } else {
+        for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
+          const int r = tp.r0 + (j >> 6), c = tp.c0 + (j & 63);
+          if (r < rows && c < cols) {
+            const int64_t i = static_cast<int64_t>(r) * cols + c;
+            if (!bounds_ok(natural_run(mt.off, i, 1, len), status, K, 0, NSM_SITE_NATURAL_LOAD)) continue;
+            const float v = step1(i) * sc;
+            if (!bounds_ok(slot_run(mt, r, c, 1), status, K, 0, NSM_SITE_SLOT_STORE)) continue;
+            store_half<TO_FP16>(dst, d0 + static_cast<int64_t>(r) * ld + c, v);
+          }
+        }
+      }
+    } else {
+      // slot row = natural column c, slot column = natural row r
+      if (mt.flags & kMatVec) {
+        for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+          const int rr = j >> 3, cc = (j & 7) * 8;
+          const int r = tp.r0 + rr, c = tp.c0 + cc;
+          float u[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (r < rows && c < cols &&
+              bounds_ok(natural_run(mt.off, static_cast<int64_t>(r) * cols + c, 8, len), status, K, 0,
+                        NSM_SITE_NATURAL_LOAD)) {
+            step8(static_cast<int64_t>(r) * cols + c, u);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) tile[rr][cc + q] = u[q];
+        }
+        __syncthreads();
+        for (int j = threadIdx.x; j < kTile * kTile / 8; j += kThreads) {
+          const int cr = j >> 3, rc = (j & 7) * 8;  // slot row c0+cr, slot cols r0+rc..+7
+          const int c = tp.c0 + cr, r = tp.r0 + rc;
+          if (c < cols && r < rows && bounds_ok(slot_run(mt, c, r, 8), status, K, 0, NSM_SITE_SLOT_STORE)) {
+            float f[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] = tile[rc + q][cr] * sc;
+            store8<TO_FP16>(dst, d0 + static_cast<int64_t>(c) * ld + r, f);
+          }
+        }
+      } else {
+        for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
+          const int rr = j >> 6, cc = j & 63;
+          const int r = tp.r0 + rr, c = tp.c0 + cc;
+          const bool in = r < rows && c < cols &&
+                          bounds_ok(natural_run(mt.off, static_cast<int64_t>(r) * cols + c, 1, len), status, K, 0,
+                                    NSM_SITE_NATURAL_LOAD);
+          tile[rr][cc] = in ? step1(static_cast<int64_t>(r) * cols + c) : 0.f;
+        }
+        __syncthreads();
+        for (int j = threadIdx.x; j < kTile * kTile; j += kThreads) {
+          const int cr = j >> 6, rc = j & 63;
+          const int c = tp.c0 + cr, r = tp.r0 + rc;
+          if (c < cols && r < rows && bounds_ok(slot_run(mt, c, r, 1), status, K, 0, NSM_SITE_SLOT_STORE)) {
+            store_half<TO_FP16>(dst, d0 + static_cast<int64_t>(c) * ld + r, tile[rc][cr] * sc);
+          }
+        }
+      }
+      __syncthreads();
+    }
+    if (kTileParts == 1) {
+      block_sum_max(acc, mx, scratch[rb]);
+      rb ^= 1;
+    } else {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+    }
+    const int part = kTileParts == 1 ? 0 : static_cast<int>(threadIdx.x >> 5);
+    if ((kTileParts == 1 && threadIdx.x == 0) || (kTileParts > 1 && (threadIdx.x & 31) == 0)) {
+      tparts[t * kTileParts + part] = acc;
+      tparts[(total_tiles + t) * kTileParts + part] = mx;
+    }
+  }
+}
+
+// X = U 2^k (scales[i] = 2^k) moved from the natural row-major layout (row stride cols)
+// into the matrix's slot (row stride ld), transposed when rows > cols, rounded once to
+// bf16/fp16.  redo != NULL (the step's second pass): nothing is done when *redo is 0, and
+// matrices whose scale is 0 keep what their slot holds.
+template <bool TO_FP16, int MODE>
+__global__ void __launch_bounds__(kThreads)
+    k_to_class(const __nv_bfloat16* __restrict__ grads, const float* __restrict__ mom, float mu,
+               void* __restrict__ dst, const MatInfo* __restrict__ mats, int nmats,
+               int64_t total_tiles, const float* __restrict__ scales, const int* __restrict__ redo,
+               int* status) {
+  grid_dependency_sync();  // inputs come from the previous kernel of the stream
+  release_dependents();
+  __shared__ float tile[kTile][kTile + 1];
+  if (redo && *redo == 0) return;  // the step's second pass: nothing to store again
+  for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+    const TilePos tp = tile_pos(mats, nmats, t);
+    const MatInfo& mt = mats[tp.mi];
+    const float sc = scales[tp.mi];
+    if (redo && sc == 0.f) {
+      // on to this block's first tile of a later matrix (the same for all threads)
+      const int64_t end = tp.mi + 1 < nmats ? mats[tp.mi + 1].tile_begin : total_tiles;
+      t += (end - 1 - t) / gridDim.x * gridDim.x;
+      continue;
+    }
+    const __nv_bfloat16* g = grads + mt.off;
     const float* m = (MODE == kUFromGrad) ? nullptr : mom + mt.off;
     const int64_t d0 = mt.slot;
-    const float sc = scales[tp.mi];
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
     const int64_t len = static_cast<int64_t>(rows) * cols;
     constexpr int K = NSM_KERNEL_TO_CLASS;
@@ -373,11 +595,12 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// Slot O -> natural layout.  APPLY: p <- p*decay - lr*scale*O, and out = bf16(p) when out is
-// not NULL (the parameters' bf16 copy).  Otherwise out = bf16(O).
+// Slot O -> natural layout, O being the stored values times oscale[i] (NULL: 1).  APPLY:
+// p <- p*decay - lr*scale*O, and out = bf16(p) when out is not NULL (the parameters' bf16
+// copy).  Otherwise out = bf16(O).
 template <bool O_FP16, bool APPLY>
 __global__ void __launch_bounds__(kThreads)
-    k_from_class(const void* __restrict__ o, float* __restrict__ params,
+    k_from_class(const void* __restrict__ o, const float* __restrict__ oscale, float* __restrict__ params,
                  __nv_bfloat16* __restrict__ out, const MatInfo* __restrict__ mats, int nmats,
                  int64_t total_tiles, float lr, float decay, int* status) {
   grid_dependency_sync();  // inputs come from the previous kernel of the stream
@@ -393,7 +616,8 @@ __global__ void __launch_bounds__(kThreads)
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
     const int64_t len = static_cast<int64_t>(rows) * cols;
     const int64_t s0 = mt.slot;
-    const float coef = lr * mt.scale;
+    const float os = oscale ? oscale[tp.mi] : 1.f;  // times 1 leaves every value as it is
+    const float coef = lr * mt.scale * os;
     float* p = APPLY ? params + mt.off : nullptr;
     __nv_bfloat16* ob = out ? out + mt.off : nullptr;
     if (mt.transposed) {
@@ -449,6 +673,8 @@ __global__ void __launch_bounds__(kThreads)
               *reinterpret_cast<uint4*>(ob + i) = pack_bf16x8(np);
             }
           } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] *= os;
             *reinterpret_cast<uint4*>(ob + i) = pack_bf16x8(f);
           }
         }
@@ -486,6 +712,8 @@ __global__ void __launch_bounds__(kThreads)
               *reinterpret_cast<uint4*>(ob + i) = pack_bf16x8(np);
             }
           } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] *= os;
             *reinterpret_cast<uint4*>(ob + i) = pack_bf16x8(f);
           }
         }
@@ -505,7 +733,7 @@ __global__ void __launch_bounds__(kThreads)
             p[i] = np;
             if (ob) ob[i] = __float2bfloat16_rn(np);
           } else {
-            ob[i] = __float2bfloat16_rn(ov);
+            ob[i] = __float2bfloat16_rn(ov * os);
           }
         }
       }
@@ -619,63 +847,79 @@ int grid_for(int64_t items, int per_sm) {
 
 }  // namespace
 
-cudaError_t launch_momentum_norm(const void* grads, float* momentum, const MatInfo* mats, int nmats,
-                                 int total_chunks, float* partials, float mu, int nesterov,
-                                 int has_momentum, cudaStream_t stream) {
+cudaError_t launch_grad_norm(const void* grads, const MatInfo* mats, int nmats, int total_chunks,
+                             float* partials, cudaStream_t stream) {
   const int grid = grid_for(total_chunks, 8);
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
-  if (!has_momentum) {
-    if (const cudaError_t e_launch = launch_pdl(k_momentum_norm<false, false>, dim3(grid), dim3(kThreads), 0, stream, g, nullptr, mats, nmats, total_chunks,
-                                                                 partials, mu, status)) return e_launch;
-  } else if (nesterov) {
-    if (const cudaError_t e_launch = launch_pdl(k_momentum_norm<true, true>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mats, nmats, total_chunks,
-                                                               partials, mu, status)) return e_launch;
-  } else {
-    if (const cudaError_t e_launch = launch_pdl(k_momentum_norm<true, false>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mats, nmats, total_chunks,
-                                                                partials, mu, status)) return e_launch;
-  }
+  if (const cudaError_t e_launch = launch_pdl(k_grad_norm, dim3(grid), dim3(kThreads), 0, stream, g, mats, nmats,
+                                              total_chunks, partials, status)) return e_launch;
   return cudaGetLastError();
 }
 
-cudaError_t launch_norm_finalize(const MatInfo* mats, int nmats, const float* partials,
-                                 float* scales, float eps, cudaStream_t stream) {
-  const int warps_per_block = kThreads / 32;
-  const int grid = (nmats + warps_per_block - 1) / warps_per_block;
-  if (const cudaError_t e_launch = launch_pdl(k_norm_finalize, dim3(grid), dim3(kThreads), 0, stream, mats, nmats, partials, scales, eps)) return e_launch;
+cudaError_t launch_momentum_class(const void* grads, float* momentum, int nesterov, float mu, void* dst,
+                                  int to_fp16, const MatInfo* mats, int nmats, int64_t total_tiles,
+                                  const int* hints, float* tparts, int* redo, cudaStream_t stream) {
+  const int grid = grid_for(total_tiles, 8);
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidSymbol;
+  const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
+  cudaError_t e;
+  if (to_fp16) {
+    e = nesterov ? launch_pdl(k_momentum_class<true, true>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mu,
+                              dst, mats, nmats, total_tiles, hints, tparts, redo, status)
+                 : launch_pdl(k_momentum_class<true, false>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mu,
+                              dst, mats, nmats, total_tiles, hints, tparts, redo, status);
+  } else {
+    e = nesterov ? launch_pdl(k_momentum_class<false, true>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mu,
+                              dst, mats, nmats, total_tiles, hints, tparts, redo, status)
+                 : launch_pdl(k_momentum_class<false, false>, dim3(grid), dim3(kThreads), 0, stream, g, momentum, mu,
+                              dst, mats, nmats, total_tiles, hints, tparts, redo, status);
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_finalize(const MatInfo* mats, int nmats, const float* parts, int64_t nparts,
+                                  int by_tile, int* hints, float* layout_scale, int* redo, float* xs,
+                                  float* xs_cls, float eps, cudaStream_t stream) {
+  const int grid = nmats < 65535 ? nmats : 65535;
+  if (const cudaError_t e_launch = launch_pdl(k_scale_finalize, dim3(grid), dim3(kThreads), 0, stream, mats, nmats,
+                                              parts, nparts, by_tile, hints, layout_scale, redo, xs, xs_cls, eps))
+    return e_launch;
   return cudaGetLastError();
 }
 
 template <bool TO_FP16>
 static cudaError_t to_class_mode(int mode, int grid, const __nv_bfloat16* g, const float* m, float mu, void* dst,
                           const MatInfo* mats, int nmats, int64_t total_tiles, const float* scales,
-                          int* status, cudaStream_t stream) {
+                          const int* redo, int* status, cudaStream_t stream) {
   if (mode == kUFromGrad) {
-    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUFromGrad>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales, status)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUFromGrad>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales, redo, status)) return e_launch;
   } else if (mode == kUMomentum) {
-    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUMomentum>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales, status)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUMomentum>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales, redo, status)) return e_launch;
   } else {
-    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUNesterov>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales, status)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_to_class<TO_FP16, kUNesterov>, dim3(grid), dim3(kThreads), 0, stream, g, m, mu, dst, mats, nmats, total_tiles, scales, redo, status)) return e_launch;
   }
   return cudaSuccess;
 }
 
 cudaError_t launch_to_class(const void* grads, const float* momentum, int has_momentum, int nesterov, float mu,
                             void* dst, int to_fp16, const MatInfo* mats, int nmats, int64_t total_tiles,
-                            const float* scales, cudaStream_t stream) {
+                            const float* scales, const int* redo, cudaStream_t stream) {
   const int grid = grid_for(total_tiles, 8);
   const auto* g = reinterpret_cast<const __nv_bfloat16*>(grads);
   const int mode = !has_momentum ? kUFromGrad : (nesterov ? kUNesterov : kUMomentum);
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
-  const cudaError_t e = to_fp16 ? to_class_mode<true>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, status, stream)
-                                : to_class_mode<false>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, status, stream);
+  const cudaError_t e = to_fp16 ? to_class_mode<true>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, redo, status, stream)
+                                : to_class_mode<false>(mode, grid, g, momentum, mu, dst, mats, nmats, total_tiles, scales, redo, status, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-cudaError_t launch_apply(const void* o, int o_fp16, float* params, void* params_bf16,
+cudaError_t launch_apply(const void* o, int o_fp16, const float* o_scale, float* params, void* params_bf16,
                          const MatInfo* mats, int nmats, int64_t total_tiles, float lr, float wd,
                          cudaStream_t stream) {
   const int grid = grid_for(total_tiles, 8);
@@ -684,23 +928,23 @@ cudaError_t launch_apply(const void* o, int o_fp16, float* params, void* params_
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   if (o_fp16) {
-    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, true>, dim3(grid), dim3(kThreads), 0, stream, o, params, pb, mats, nmats, total_tiles, lr, decay, status)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, true>, dim3(grid), dim3(kThreads), 0, stream, o, o_scale, params, pb, mats, nmats, total_tiles, lr, decay, status)) return e_launch;
   } else {
-    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, true>, dim3(grid), dim3(kThreads), 0, stream, o, params, pb, mats, nmats, total_tiles, lr, decay, status)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, true>, dim3(grid), dim3(kThreads), 0, stream, o, o_scale, params, pb, mats, nmats, total_tiles, lr, decay, status)) return e_launch;
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* mats, int nmats,
+cudaError_t launch_export(const void* o, int o_fp16, const float* o_scale, void* out, const MatInfo* mats, int nmats,
                           int64_t total_tiles, cudaStream_t stream) {
   const int grid = grid_for(total_tiles, 8);
   auto* ob = reinterpret_cast<__nv_bfloat16*>(out);
   int* status = device_status_ptr();
   if (!status) return cudaErrorInvalidSymbol;
   if (o_fp16) {
-    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, false>, dim3(grid), dim3(kThreads), 0, stream, o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f, status)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<true, false>, dim3(grid), dim3(kThreads), 0, stream, o, o_scale, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f, status)) return e_launch;
   } else {
-    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, false>, dim3(grid), dim3(kThreads), 0, stream, o, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f, status)) return e_launch;
+    if (const cudaError_t e_launch = launch_pdl(k_from_class<false, false>, dim3(grid), dim3(kThreads), 0, stream, o, o_scale, nullptr, ob, mats, nmats, total_tiles, 0.f, 1.f, status)) return e_launch;
   }
   return cudaGetLastError();
 }

@@ -16,7 +16,9 @@
 // 128 or 256 rows) into a ring of stages, warp 1 issues the MMAs (the leader CTA's, in the
 // pair kernel) into two TMEM accumulators of 256 fp32 columns, warps 2-5 drain TMEM with
 // tcgen05.ld, apply the fused epilogue  out = alpha*acc + beta*aux + diag*I  and store
-// fp16/bf16 32 x 32 blocks through shared memory with TMA stores.
+// fp16/bf16 32 x 32 blocks through shared memory with TMA stores.  A product that reads
+// the chain's input, stored as U 2^k, scales alpha and beta by that problem's s 2^-k
+// (squared for X X^T), so that it computes with X = s U.
 // A group flagged symmetric computes only the tiles that touch the upper triangle, stores
 // the blocks on and above the diagonal and mirrors the upper ones.  In the pair kernel a
 // group may instead keep its symmetric m x m buffers as their upper 256 x 256 tiles
@@ -184,6 +186,15 @@ __device__ __forceinline__ uint32_t pack2<false>(float lo, float hi) {
 // 16-bit element j of a packed row (element 2i in the low half of word i).
 __device__ __forceinline__ uint16_t half_of(const uint32_t (&h)[16], int j) {
   return static_cast<uint16_t>((j & 1) ? (h[j >> 1] >> 16) : (h[j >> 1] & 0xffffu));
+}
+
+// Factor of a product that reads the chain's stored input X = s U, kept as U 2^k: the
+// matrix's s 2^-k (squared for X X^T) multiplies alpha and beta; 1 for every other product
+// (times 1 leaves every value as it is).
+__device__ __forceinline__ float input_factor(const GemmGroup& G, int b) {
+  if (G.in_pow == 0) return 1.f;
+  const float x = G.in_scale[b];
+  return G.in_pow == 2 ? x * x : x;
 }
 
 // v = alpha acc (+ beta aux) (+ diag on the diagonal) for one 32-column chunk of this
@@ -670,13 +681,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
+      const float f = input_factor(G, tc.b);
       if (G.map_out) {
         epilogue_rows<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                     t_row, stage, nst, lane, alpha, beta, diag, true,
+                                     t_row, stage, nst, lane, alpha * f, beta * f, diag, true,
                                      Chk{status, NSM_KERNEL_GEMM});
       } else {
         epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, tc.m0 + quarter * 32, tc.n0, min(BN, G.N - tc.n0),
-                                            t_row, stage_words, lane, alpha, beta, diag, true,
+                                            t_row, stage_words, lane, alpha * f, beta * f, diag, true,
                                             Chk{status, NSM_KERNEL_GEMM});
       }
       ptx::tc_fence_before();
@@ -997,12 +1009,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int rb = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
       // an output stored as upper 256 x 256 tiles mirrors blocks only inside diagonal tiles
       const bool mirror = !(G.lean & kLeanOut) || tc.m0 == tc.n0;
+      const float f = input_factor(G, tc.b);
       if (G.map_out) {
         epilogue_rows<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage, nst, lane,
-                                     alpha, beta, diag, mirror, Chk{status, NSM_KERNEL_GEMM_PAIR});
+                                     alpha * f, beta * f, diag, mirror, Chk{status, NSM_KERNEL_GEMM_PAIR});
       } else {
         epilogue_rows_direct<FP16, HAS_AUX>(G, tc.b, rb, tc.n0, min(BN, G.N - tc.n0), t_row, stage_words,
-                                            lane, alpha, beta, diag, mirror, Chk{status, NSM_KERNEL_GEMM_PAIR});
+                                            lane, alpha * f, beta * f, diag, mirror, Chk{status, NSM_KERNEL_GEMM_PAIR});
       }
       ptx::tc_fence_before();
       __syncwarp();

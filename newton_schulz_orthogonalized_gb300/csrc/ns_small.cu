@@ -24,7 +24,9 @@
 // (each thread one row).  Every wait is bounded; the epilogue warps take every decision
 // to give up together (a barrier reduction), so no warp is left at a named barrier.
 // Every m x m iterate is symmetric (a polynomial in X X^T), which is why S[b]^T serves
-// for S[b] and one K-major layout serves every use.
+// for S[b] and one K-major layout serves every use.  The chain's input is stored as U 2^k;
+// the Gram and pass operations that read it take the matrix's s 2^-k into alpha and beta
+// (squared for the Gram), so that they compute with X = s U.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -370,9 +372,11 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
     const int nck = (job.n + kChunk - 1) / kChunk;
     for (int o = 0; o < nops; ++o) {
       const SmallOp op = ops[o];
+      // an operation on the stored input (U 2^k) multiplies by s 2^-k, squared for X X^T
+      const float f = op.in_pow == 0 ? 1.f : (op.in_pow == 2 ? job.in_scale[0] * job.in_scale[0] : job.in_scale[0]);
       if (op.kind == kSmallGram) {
         for (int c = 0; c < nck; ++c) rp.advance();
-        if (!ep.square(op.dst, -1, 1.f, 0.f, 0.f, job.m)) return false;
+        if (!ep.square(op.dst, -1, f, 0.f, 0.f, job.m)) return false;
         continue;
       }
       if (op.kind == kSmallSquare) {
@@ -380,6 +384,7 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
         continue;
       }
       const bool reads_x = op.beta != 0.f;
+      const float alpha = op.alpha * f, beta = op.beta * f;
       const uint32_t xs0 = xs;
       for (int c = 0; c < nck; ++c) {
         const uint32_t acc = acc_cnt & 1u;
@@ -413,7 +418,7 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
                 ep.t_lane + 128u + static_cast<uint32_t>(kChunk) * acc + static_cast<uint32_t>(64 * h + 32 * q), r);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[q * 32 + k] = op.alpha * __uint_as_float(r[k]);
+            for (int k = 0; k < 32; ++k) v[q * 32 + k] = alpha * __uint_as_float(r[k]);
           }
           if (reads_x) {
             const uint32_t panel = chunk + static_cast<uint32_t>(h * kPanel);
@@ -422,7 +427,7 @@ __device__ bool drain(Epilogue<FP16>& ep, const SmallJob* __restrict__ jobs, int
               const uint4 pk = *reinterpret_cast<const uint4*>(__cvta_shared_to_generic(panel + sw(ep.row, u)));
               const T* e = reinterpret_cast<const T*>(&pk);
 #pragma unroll
-              for (int k = 0; k < 8; ++k) v[u * 8 + k] += op.beta * E::to_f(e[k]);
+              for (int k = 0; k < 8; ++k) v[u * 8 + k] += beta * E::to_f(e[k]);
             }
           }
 #pragma unroll

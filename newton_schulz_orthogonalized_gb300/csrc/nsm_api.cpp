@@ -84,7 +84,16 @@ struct Layout {
   int64_t x_elems = 0, mm_elems = 0;
   int total_chunks = 0;
   int64_t total_tiles = 0;
-  size_t off_partials = 0, off_scales = 0, off_x[2] = {0, 0}, off_mm[4] = {0, 0, 0, 0};
+  // partials: per chunk sums and maxima (2 x chunks) of the orthogonalisation's norm pass;
+  // tparts: per tile sums and maxima (2 x kTileParts x tiles) of the step's pass; scales: the layout
+  // pass's 2^k per matrix (0: nothing to store again); xs / xs_cls: the input factor
+  // s 2^-k in matrix and class order; hints: the step's exponent per matrix, kept from one
+  // call to the next
+  size_t off_partials = 0, off_tparts = 0, off_scales = 0, off_xs = 0, off_xs_cls = 0, off_hints = 0;
+  size_t off_redo = 0;  // one int: set when some matrix must be stored again
+  size_t off_x[2] = {0, 0}, off_mm[4] = {0, 0, 0, 0};
+  std::vector<int32_t> cls_pos;  // each matrix's position in class order
+  std::vector<int32_t> cls_first;  // class order position of each class's first matrix
   int num_mm = 0;
   size_t bytes = 0;
 };
@@ -147,6 +156,13 @@ Layout make_layout(const int32_t* shapes, int n, int method, int steps) {
     sc.mm_base = L.mm_elems;
     L.mm_elems += int64_t(sc.count) * sc.m * sc.ldm;
   }
+  L.cls_first.resize(L.classes.size());
+  for (size_t c = 0, pos = 0; c < L.classes.size(); ++c) {
+    L.cls_first[c] = static_cast<int32_t>(pos);
+    pos += size_t(L.classes[c].count);
+  }
+  L.cls_pos.resize(n);
+  for (int i = 0; i < n; ++i) L.cls_pos[i] = L.cls_first[L.cls_of[i]] + L.batch_of[i];
   int64_t chunks = 0, tiles = 0;
   for (int i = 0; i < n; ++i) {
     const ShapeClass& sc = L.classes[L.cls_of[i]];
@@ -162,9 +178,19 @@ Layout make_layout(const int32_t* shapes, int n, int method, int steps) {
   L.total_tiles = tiles;
   L.num_mm = method == NSM_NS_GRAM ? 4 : 2;
   size_t off = 0;
+  L.off_hints = off;  // first, so that the same table finds them at the same place
+  off = align_up(off + size_t(n) * 4, kAlign);
   L.off_partials = off;
-  off = align_up(off + size_t(chunks) * 4, kAlign);
+  off = align_up(off + size_t(chunks) * 8, kAlign);
+  L.off_tparts = off;
+  off = align_up(off + size_t(tiles) * 8 * kTileParts, kAlign);
+  L.off_redo = off;
+  off = align_up(off + 4, kAlign);
   L.off_scales = off;
+  off = align_up(off + size_t(n) * 4, kAlign);
+  L.off_xs = off;
+  off = align_up(off + size_t(n) * 4, kAlign);
+  L.off_xs_cls = off;
   off = align_up(off + size_t(n) * 4, kAlign);
   for (int k = 0; k < 2; ++k) {
     L.off_x[k] = off;
@@ -241,6 +267,7 @@ struct Plan {
   std::vector<GemmLaunch> launches;
   int64_t elems = 0;      // elements of the table (sum of rows x cols)
   int final_buf = X0;     // buffer holding O after the chain
+  bool final_is_input = false;  // no step: O is the stored input (U 2^k, factor s 2^-k)
   bool final_fp16 = false;
   bool x_fp16 = false;
   bool owns_meta = true;  // false when the metadata lives in memory the plan does not own
@@ -319,10 +346,12 @@ int small_schedule(int method, int steps, std::vector<SmallOp>& ops) {
   };
   if (method == NSM_NS_GRAM) {
     int xb = X0;
+    bool xb_input = true;  // X[xb] is still the stored input
     int q = -1;  // shared-memory matrix holding Q; -1 = identity
     SmallOp g = make(kSmallGram);  // R = X X^T in S0
     g.src_x = xb;
     g.dst = 0;
+    g.in_pow = 2;
     ops.push_back(g);
     for (int k = 1; k <= steps; ++k) {
       const int h = q == 1 ? 2 : 1;
@@ -353,8 +382,10 @@ int small_schedule(int method, int steps, std::vector<SmallOp>& ops) {
           ps.dst_x = xn;
           ps.accumulate = 1;
           ps.dst = 0;
+          ps.in_pow = xb_input ? 1 : 0;
           ops.push_back(ps);
           xb = xn;
+          xb_input = false;
           q = -1;
         } else {
           SmallOp ts = make(kSmallSquare);  // T = H R, in R's place
@@ -376,12 +407,14 @@ int small_schedule(int method, int steps, std::vector<SmallOp>& ops) {
     fs.src_x = xb;
     fs.dst_x = xn;
     fs.final_pass = 1;
+    fs.in_pow = xb_input ? 1 : 0;
     ops.push_back(fs);
     return xn;
   }
   SmallOp g = make(kSmallGram);  // A = X X^T in S0
   g.src_x = X0;
   g.dst = 0;
+  g.in_pow = 2;
   ops.push_back(g);
   for (int k = 0; k < steps; ++k) {
     const int src = (k % 2 == 0) ? X0 : X1, dst = (k % 2 == 0) ? X1 : X0;
@@ -398,6 +431,7 @@ int small_schedule(int method, int steps, std::vector<SmallOp>& ops) {
     ps.src_x = src;
     ps.dst_x = dst;
     ps.beta = kA;
+    ps.in_pow = k == 0 ? 1 : 0;
     if (k + 1 < steps) {
       ps.accumulate = 1;
       ps.dst = 0;
@@ -423,6 +457,7 @@ struct StageSpec {
   bool n_is_n;                         // N = n (B X, Q X); otherwise N = m
   float alpha, beta, diag;
   bool sym;                            // output symmetric: upper-triangle tiles + mirror
+  int in_pow;                          // reads the stored input: 1, or 2 for X X^T; else 0
 };
 
 // Tiles (packed mt << 16 | nt) of an m x m output that touch its upper triangle, for
@@ -468,6 +503,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   for (int i = 0; i < n; ++i) P.elems += int64_t(shapes[2 * i]) * shapes[2 * i + 1];
   P.ws = static_cast<char*>(ws);
   P.x_fp16 = method != NSM_NS_STANDARD_BF16;
+  P.final_is_input = steps == 0;
   const int nclass = static_cast<int>(L.classes.size());
   const int nbuf = 2 + L.num_mm;
   auto buf_base = [&](int b, int c) -> char* {
@@ -481,9 +517,10 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
   if (method == NSM_NS_STANDARD || method == NSM_NS_STANDARD_BF16) {
     for (int k = 0; k < steps; ++k) {
       const int src = (k % 2 == 0) ? X0 : X1, dst = (k % 2 == 0) ? X1 : X0;
-      stages.push_back({src, src, MM0, -1, false, true, false, 1.f, 0.f, 0.f, true});            // A = X X^T
-      stages.push_back({MM0, MM0, MM0 + 1, MM0, false, false, false, kC, kB, 0.f, true});       // B = bA + cAA
-      stages.push_back({MM0 + 1, src, dst, src, true, false, true, 1.f, kA, 0.f, false});         // X' = aX + BX
+      const int first = k == 0 ? 1 : 0;  // the first step reads the stored input
+      stages.push_back({src, src, MM0, -1, false, true, false, 1.f, 0.f, 0.f, true, 2 * first});   // A = X X^T
+      stages.push_back({MM0, MM0, MM0 + 1, MM0, false, false, false, kC, kB, 0.f, true, 0});        // B = bA + cAA
+      stages.push_back({MM0 + 1, src, dst, src, true, false, true, 1.f, kA, 0.f, false, first});     // X' = aX + BX
     }
     P.final_buf = (steps % 2 == 0) ? X0 : X1;
     P.final_fp16 = P.x_fp16;
@@ -501,7 +538,8 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       return b;
     };
     auto push = [&](int b) { freeb.push_back(b); };
-    if (steps > 0) stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f, true});       // R = X X^T
+    bool xb_input = true;  // the anchor X is still the stored input
+    if (steps > 0) stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f, true, 2});    // R = X X^T
     for (int k = 1; k <= steps; ++k) {
       const int h = pop();
       stages.push_back({rR, rR, h, rR, false, false, false, kC, kB, kA, true});                        // H
@@ -518,9 +556,10 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       if (k < steps) {
         if (k % kGramReanchor == 0) {
           const int xn = (xb == X0) ? X1 : X0;
-          stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f, false});                   // X = Q X
+          stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f, false, xb_input ? 1 : 0});  // X = Q X
           xb = xn;
-          stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f, true});                 // R = X X^T
+          xb_input = false;
+          stages.push_back({xb, xb, rR, -1, false, true, false, 1.f, 0.f, 0.f, true, 0});              // R = X X^T
           push(q);  // H is Q here or already released below
           if (!h_is_q) push(h);
           q = -1;
@@ -535,7 +574,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     }
     if (q >= 0) {
       const int xn = (xb == X0) ? X1 : X0;
-      stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f, false});                       // O = Q X
+      stages.push_back({q, xb, xn, -1, true, false, true, 1.f, 0.f, 0.f, false, xb_input ? 1 : 0});    // O = Q X
       P.final_buf = xn;
     } else {
       P.final_buf = xb;
@@ -622,6 +661,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
     mi.nchunks = L.nchunks[i];
     mi.scale = static_cast<float>(std::sqrt(std::max(1.0, double(mi.rows) / double(mi.cols))));
     mi.flags = (mi.rows % 8 == 0 && mi.cols % 8 == 0) ? kMatVec : 0;
+    mi.cls_pos = L.cls_pos[i];
     hm[i] = mi;
   }
 
@@ -682,6 +722,7 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
       jb.b = L.batch_of[i];
       jb.m = L.classes[c].m;
       jb.n = L.classes[c].n;
+      jb.in_scale = reinterpret_cast<const float*>(P.ws + L.off_xs) + i;
       hj[k] = jb;
     }
     std::copy(small_ops.begin(), small_ops.end(), reinterpret_cast<SmallOp*>(host.data() + ops_off));
@@ -745,6 +786,10 @@ int build_plan(Plan& P, const int32_t* shapes, const int64_t* offsets, int n, in
         g.aux = buf_base(st.aux_buf, c);
         g.ld_aux = aux_x ? sc.ldn : sc.ldm;
         g.aux_bstride = int64_t(sc.m) * g.ld_aux;
+      }
+      if (st.in_pow) {
+        g.in_pow = st.in_pow;
+        g.in_scale = reinterpret_cast<const float*>(P.ws + L.off_xs_cls) + L.cls_first[c];
       }
       g.M = sc.m;
       g.N = st.n_is_n ? sc.n : sc.m;
@@ -866,7 +911,7 @@ Plan* get_plan(const int32_t* shapes, const int64_t* offsets, int n, int method,
 // ---------------------------------------------------------------- timing
 
 // Kernel kinds the timing hooks distinguish (NSM_KIND_* in the header).
-constexpr int kKinds = 7;
+constexpr int kKinds = 8;
 
 struct Timing {
   std::mutex mu;
@@ -994,6 +1039,49 @@ int run_chain(Plan& P, cudaStream_t stream, int* launches) {
     if (e != cudaSuccess) return fail_cuda(e, "Newton-Schulz GEMM launch");
     ++*launches;
   }
+  return NSM_OK;
+}
+
+// The orthogonalisation of a plan's table: the sums and maxima of G per chunk, each
+// matrix's s and exponent k, U = G stored as G 2^k, the chain, and the export of O.
+int run_orthogonalize(Plan& P, const void* in_bf16, void* out_bf16, int n, cudaStream_t stream, int* launches) {
+  char* ws = P.ws;
+  const Layout& L = P.L;
+  float* partials = reinterpret_cast<float*>(ws + L.off_partials);
+  float* scales = reinterpret_cast<float*>(ws + L.off_scales);
+  float* xs = reinterpret_cast<float*>(ws + L.off_xs);
+  float* xs_cls = reinterpret_cast<float*>(ws + L.off_xs_cls);
+  const double elems = double(P.elems);
+  cudaError_t e;
+  {
+    TimedLaunch t(stream, NSM_KIND_GRAD_NORM, 2.0 * elems);
+    e = launch_grad_norm(in_bf16, P.d_mats, n, L.total_chunks, partials, stream);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
+  ++*launches;
+  {
+    TimedLaunch t(stream, NSM_KIND_NORM, 8.0 * double(L.total_chunks) + 12.0 * n);
+    e = launch_scale_finalize(P.d_mats, n, partials, L.total_chunks, 0, nullptr, scales, nullptr, xs, xs_cls,
+                              kNormEps, stream);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
+  ++*launches;
+  {
+    TimedLaunch t(stream, NSM_KIND_LAYOUT, 4.0 * elems);
+    e = launch_to_class(in_bf16, nullptr, 0, 0, 0.f, ws + L.off_x[0], P.x_fp16 ? 1 : 0, P.d_mats, n, L.total_tiles,
+                        scales, nullptr, stream);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "layout launch");
+  ++*launches;
+  const int rc = run_chain(P, stream, launches);
+  if (rc != NSM_OK) return rc;
+  {
+    TimedLaunch t(stream, NSM_KIND_APPLY, 4.0 * elems);
+    e = launch_export(ws + L.off_x[P.final_buf], P.final_fp16 ? 1 : 0, P.final_is_input ? xs : nullptr, out_bf16,
+                      P.d_mats, n, L.total_tiles, stream);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "export launch");
+  ++*launches;
   return NSM_OK;
 }
 
@@ -1233,39 +1321,50 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   Plan* P = get_plan(shapes, offsets, n, ns_method, ns_steps, workspace, workspace_bytes, &rc);
   if (!P) return rc;
   const PdlScope pdl(P->elems);
-  char* ws = P->ws;
-  float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
-  float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
+  char* ws = P->ws;  // L (above) is the plan's layout
+  float* tparts = reinterpret_cast<float*>(ws + L.off_tparts);
+  float* scales = reinterpret_cast<float*>(ws + L.off_scales);
+  float* xs = reinterpret_cast<float*>(ws + L.off_xs);
+  float* xs_cls = reinterpret_cast<float*>(ws + L.off_xs_cls);
+  int* hints = reinterpret_cast<int*>(ws + L.off_hints);
+  int* redo = reinterpret_cast<int*>(ws + L.off_redo);
   int launches = 0;
   const double elems = double(P->elems);
   cudaError_t e;
+  // One pass over G and M: M updated, U stored as U 2^k with each matrix's exponent hint
+  // (the one the previous step on this table chose), per-tile sums and maxima of U.
   {
-    TimedLaunch t(stream, NSM_KIND_MOMENTUM, 10.0 * elems);
-    e = launch_momentum_norm(packed_grads, momentum, P->d_mats, n, P->L.total_chunks, partials, mu, nesterov, 1,
-                             stream);
+    TimedLaunch t(stream, NSM_KIND_MOMENTUM, 12.0 * elems);
+    e = launch_momentum_class(packed_grads, momentum, nesterov, mu, ws + L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats,
+                              n, L.total_tiles, hints, tparts, redo, stream);
   }
-  if (e != cudaSuccess) return fail_cuda(e, "momentum/norm launch");
+  if (e != cudaSuccess) return fail_cuda(e, "momentum/layout launch");
   ++launches;
+  // s and the exponent of each matrix; a hint that put max|U| 2^k outside the accepted
+  // range marks its matrix for the layout pass below
   {
-    TimedLaunch t(stream, NSM_KIND_NORM, 4.0 * (P->L.total_chunks + n));
-    e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
+    TimedLaunch t(stream, NSM_KIND_NORM, 8.0 * kTileParts * double(L.total_tiles) + 16.0 * n);
+    e = launch_scale_finalize(P->d_mats, n, tparts, L.total_tiles, 1, hints, scales, redo, xs, xs_cls, kNormEps,
+                              stream);
   }
   if (e != cudaSuccess) return fail_cuda(e, "norm launch");
   ++launches;
+  // U stored again where its hint was out of range (the first step on a table, or a jump
+  // of the gradients' magnitude); every other matrix is skipped
   {
-    TimedLaunch t(stream, NSM_KIND_LAYOUT, 8.0 * elems);
-    e = launch_to_class(packed_grads, momentum, 1, nesterov, mu, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats,
-                        n, P->L.total_tiles, scales, stream);
+    TimedLaunch t(stream, NSM_KIND_LAYOUT, 0.0);
+    e = launch_to_class(packed_grads, momentum, 1, nesterov, mu, ws + L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats,
+                        n, L.total_tiles, scales, redo, stream);
   }
-  if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
+  if (e != cudaSuccess) return fail_cuda(e, "layout launch");
   ++launches;
   // The chain leaves O in the workspace; the apply pass updates every matrix from it.
   rc = run_chain(*P, stream, &launches);
   if (rc != NSM_OK) return rc;
   {
     TimedLaunch t(stream, NSM_KIND_APPLY, (params_bf16 ? 12.0 : 10.0) * elems);
-    e = launch_apply(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, packed_params, params_bf16,
-                     P->d_mats, n, P->L.total_tiles, lr, wd, stream);
+    e = launch_apply(ws + L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, P->final_is_input ? xs : nullptr,
+                     packed_params, params_bf16, P->d_mats, n, L.total_tiles, lr, wd, stream);
   }
   if (e != cudaSuccess) return fail_cuda(e, "apply launch");
   ++launches;
@@ -1294,40 +1393,9 @@ int muon_orthogonalize(const void* in_bf16, void* out_bf16, const int64_t* offse
   Plan* P = get_plan(shapes, offsets, n, ns_method, ns_steps, workspace, workspace_bytes, &rc);
   if (!P) return rc;
   const PdlScope pdl(P->elems);
-  char* ws = P->ws;
-  float* partials = reinterpret_cast<float*>(ws + P->L.off_partials);
-  float* scales = reinterpret_cast<float*>(ws + P->L.off_scales);
   int launches = 0;
-  const double elems = double(P->elems);
-  cudaError_t e;
-  {
-    TimedLaunch t(stream, NSM_KIND_MOMENTUM, 2.0 * elems);
-    e = launch_momentum_norm(in_bf16, nullptr, P->d_mats, n, P->L.total_chunks, partials, 0.f, 0, 0, stream);
-  }
-  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
-  ++launches;
-  {
-    TimedLaunch t(stream, NSM_KIND_NORM, 4.0 * (P->L.total_chunks + n));
-    e = launch_norm_finalize(P->d_mats, n, partials, scales, kNormEps, stream);
-  }
-  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
-  ++launches;
-  {
-    TimedLaunch t(stream, NSM_KIND_LAYOUT, 4.0 * elems);
-    e = launch_to_class(in_bf16, nullptr, 0, 0, 0.f, ws + P->L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n,
-                        P->L.total_tiles, scales, stream);
-  }
-  if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
-  ++launches;
-  rc = run_chain(*P, stream, &launches);
+  rc = run_orthogonalize(*P, in_bf16, out_bf16, n, stream, &launches);
   if (rc != NSM_OK) return rc;
-  {
-    TimedLaunch t(stream, NSM_KIND_APPLY, 4.0 * elems);
-    e = launch_export(ws + P->L.off_x[P->final_buf], P->final_fp16 ? 1 : 0, out_bf16, P->d_mats, n,
-                      P->L.total_tiles, stream);
-  }
-  if (e != cudaSuccess) return fail_cuda(e, "export launch");
-  ++launches;
   t_last_launches = launches;
   return NSM_OK;
 }
@@ -1525,26 +1593,9 @@ int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16, const int64_
   }
   Plan& P = *st->plan;
   const PdlScope pdl(P.elems);
-  char* ws = P.ws;
-  float* partials = reinterpret_cast<float*>(ws + P.L.off_partials);
-  float* scales = reinterpret_cast<float*>(ws + P.L.off_scales);
   int launches = 0;
-  e = launch_momentum_norm(in_bf16, nullptr, P.d_mats, n, P.L.total_chunks, partials, 0.f, 0, 0, stream);
-  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
-  ++launches;
-  e = launch_norm_finalize(P.d_mats, n, partials, scales, kNormEps, stream);
-  if (e != cudaSuccess) return fail_cuda(e, "norm launch");
-  ++launches;
-  e = launch_to_class(in_bf16, nullptr, 0, 0, 0.f, ws + P.L.off_x[0], P.x_fp16 ? 1 : 0, P.d_mats, n, P.L.total_tiles,
-                      scales, stream);
-  if (e != cudaSuccess) return fail_cuda(e, "normalise launch");
-  ++launches;
-  rc = run_chain(P, stream, &launches);
+  rc = run_orthogonalize(P, in_bf16, out_bf16, n, stream, &launches);
   if (rc != NSM_OK) return rc;
-  e = launch_export(ws + P.L.off_x[P.final_buf], P.final_fp16 ? 1 : 0, out_bf16, P.d_mats, n, P.L.total_tiles,
-                    stream);
-  if (e != cudaSuccess) return fail_cuda(e, "export launch");
-  ++launches;
   t_last_launches = launches;
   return NSM_OK;
 }

@@ -64,10 +64,25 @@ struct MatInfo {
   int32_t chunk_begin, nchunks;  // momentum/norm chunks of this matrix
   float scale;        // sqrt(max(1, rows/cols))
   int32_t flags;      // kMatVec
+  int32_t cls_pos;    // position among the matrices in class order (class by class, batch index)
+  int32_t pad;
 };
 // MatInfo::flags: rows % 8 == 0 && cols % 8 == 0 (16-byte vector paths usable)
 constexpr int32_t kMatVec = 1;
-static_assert(sizeof(MatInfo) == 64, "MatInfo layout");
+static_assert(sizeof(MatInfo) == 72, "MatInfo layout");
+
+// The normalised input X = s U of the chain is stored as U 2^k rounded once to the
+// storage format, with a power-of-two k per matrix that puts its largest |U| in the
+// format's normal range; the products that read it multiply by s 2^-k (the matrix's
+// input factor, 'xs').  k is chosen so that the largest |U| 2^k lies in [2^11, 2^12); a
+// stored value is accepted when it lies in [2^4, 2^15).
+constexpr int kInTargetExp = 12;  // frexp exponent of max|U| 2^k after choosing k
+constexpr int kInMinExp = 5;      // accepted: frexp exponent of max|U| 2^k in [5, 15]
+constexpr int kInMaxExp = 15;
+constexpr int kInExpClamp = 120;  // |k| at most this (2^k and 2^-k are normal floats)
+// Partial sums (and maxima) the step's pass writes per 64 x 64 tile: one per warp of its
+// 256-thread blocks, so that no block-wide barrier is needed to combine them.
+constexpr int kTileParts = 8;
 
 // Elements of one momentum/norm chunk (256 threads x 8 vectors of 8).
 constexpr int kChunk = 16384;
@@ -107,9 +122,11 @@ struct GemmGroup {
   const CUtensorMap* map_b_narrow;  // B in 64-row boxes (K-major B; MN-major: map_b): the 2-SM
                                     // kernel's tiles with at most 128 columns in range
   int32_t lean;                     // kLeanOut | kLeanA | kLeanB (2-SM kernel only)
-  int32_t lean_pad;
+  int32_t in_pow;                   // 0, or 1 / 2: the product reads the chain's stored input
+  const float* in_scale;            // in_pow != 0: input factor of problem b at in_scale[b];
+                                    // the epilogue takes alpha, beta times in_scale[b]^in_pow
 };
-static_assert(sizeof(GemmGroup) == 136, "GemmGroup layout");
+static_assert(sizeof(GemmGroup) == 144, "GemmGroup layout");
 constexpr int32_t kLeanOut = 1;
 constexpr int32_t kLeanA = 2;
 constexpr int32_t kLeanB = 4;
@@ -138,8 +155,9 @@ constexpr int kSmallMaxM = 128;
 struct SmallJob {
   const CUtensorMap* map_x[2];
   int32_t mat, b, m, n;
+  const float* in_scale;  // the matrix's input factor (operations with in_pow read it)
 };
-static_assert(sizeof(SmallJob) == 32, "SmallJob layout");
+static_assert(sizeof(SmallJob) == 40, "SmallJob layout");
 
 // Operations of the small-matrix chain (every matrix of the launch runs the same list).
 // S0..S2 are 128 x 128 matrices in shared memory, X0/X1 the class buffers in the workspace.
@@ -155,8 +173,9 @@ struct SmallOp {
   int32_t src_x, dst_x;    // X buffers of Gram and pass operations
   int32_t accumulate, final_pass;
   float alpha, beta, diag;
+  int32_t in_pow;          // reads the stored input: alpha, beta times the input factor^in_pow
 };
-static_assert(sizeof(SmallOp) == 48, "SmallOp layout");
+static_assert(sizeof(SmallOp) == 52, "SmallOp layout");
 constexpr int kSmallMaxOps = 96;
 
 // ---- launchers (defined in the .cu files) ---------------------------------------
@@ -165,24 +184,40 @@ constexpr int kSmallMaxOps = 96;
 cudaError_t launch_ns_small(const SmallJob* jobs, int njobs, const SmallOp* ops, int nops, int fp16,
                             int num_sms, cudaStream_t stream);
 
-// M <- mu M + G (when has_momentum) and per-chunk sums of U^2, U = G + mu M (Nesterov),
-// M (plain) or G (no momentum)
-cudaError_t launch_momentum_norm(const void* grads, float* momentum, const MatInfo* mats, int nmats,
-                                 int total_chunks, float* partials, float mu, int nesterov,
-                                 int has_momentum, cudaStream_t stream);
-cudaError_t launch_norm_finalize(const MatInfo* mats, int nmats, const float* partials,
-                                 float* scales, float eps, cudaStream_t stream);
-// X = s U, U recomputed in fp32 from G and the updated M, into the class layout, rounded
-// once to bf16 (or fp16 when to_fp16)
+// Per-chunk sum of G^2 (partials[c]) and largest |G| (partials[total_chunks + c])
+cudaError_t launch_grad_norm(const void* grads, const MatInfo* mats, int nmats, int total_chunks,
+                             float* partials, cudaStream_t stream);
+// M <- mu M + G and U = G + mu M (Nesterov) or M, stored as U 2^k (k = the matrix's
+// hint) into the class layout, rounded once to bf16 (or fp16 when to_fp16); per tile t,
+// kTileParts partial sums of U^2 (tparts[t kTileParts + w]) and largest |U| (the same
+// index plus total_tiles kTileParts).  Clears *redo.
+cudaError_t launch_momentum_class(const void* grads, float* momentum, int nesterov, float mu, void* dst,
+                                  int to_fp16, const MatInfo* mats, int nmats, int64_t total_tiles,
+                                  const int* hints, float* tparts, int* redo, cudaStream_t stream);
+// Per matrix, from its partials (per chunk, or kTileParts per tile when by_tile; the
+// maxima nparts entries after the sums): s = 1/(sqrt(sum) + eps) and the exponent k.
+// With hints (the step): the stored U 2^hint is accepted or, with layout_scale = 2^k and
+// *redo = 1, marked for the layout pass to store again (layout_scale 0 when accepted);
+// hints receive the exponent for the next step.  Without: layout_scale = 2^k for the
+// layout pass.  xs (matrix order) and xs_cls (class order) receive the input factor
+// s 2^-k.
+cudaError_t launch_scale_finalize(const MatInfo* mats, int nmats, const float* parts, int64_t nparts,
+                                  int by_tile, int* hints, float* layout_scale, int* redo, float* xs,
+                                  float* xs_cls, float eps, cudaStream_t stream);
+// X = U 2^k (scales[i] = 2^k), U recomputed in fp32 from G and the updated M (or U = G),
+// into the class layout, rounded once to bf16 (or fp16 when to_fp16).  redo != NULL: the
+// step's second pass, which returns at once when *redo is 0 and otherwise leaves the
+// matrices whose scale is 0 as they are.
 cudaError_t launch_to_class(const void* grads, const float* momentum, int has_momentum, int nesterov,
                             float mu, void* dst, int to_fp16, const MatInfo* mats, int nmats,
-                            int64_t total_tiles, const float* scales, cudaStream_t stream);
-// class layout O -> p update in natural layout (and its bf16 copy when params_bf16 != NULL)
-cudaError_t launch_apply(const void* o, int o_fp16, float* params, void* params_bf16,
+                            int64_t total_tiles, const float* scales, const int* redo, cudaStream_t stream);
+// class layout O -> p update in natural layout (and its bf16 copy when params_bf16 != NULL);
+// o_scale (matrix order, may be NULL = 1): factor of each matrix's stored O
+cudaError_t launch_apply(const void* o, int o_fp16, const float* o_scale, float* params, void* params_bf16,
                          const MatInfo* mats, int nmats, int64_t total_tiles, float lr, float wd,
                          cudaStream_t stream);
-// class layout O -> natural bf16 copy
-cudaError_t launch_export(const void* o, int o_fp16, void* out, const MatInfo* mats,
+// class layout O -> natural bf16 copy (times o_scale, as for the apply)
+cudaError_t launch_export(const void* o, int o_fp16, const float* o_scale, void* out, const MatInfo* mats,
                           int nmats, int64_t total_tiles, cudaStream_t stream);
 cudaError_t launch_adamw(const void* grads, float* params, float* m, float* v,
                          int64_t numel, float lr, float beta1, float beta2, float eps,

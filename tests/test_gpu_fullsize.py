@@ -14,9 +14,7 @@ muon_orthogonalize runs over the same table, with the same grouped launches.
   matter): the momentum at 1e-5 and the parameter delta at 1e-2 against the oracle in the
   method's storage precision, and the orthogonalised output at 2e-2 against it, each with
   the element-wise bounds of the parity tests.  The same outputs are compared with the
-  exact float64 iteration too: the measured distance is recorded, and held to 2.5e-2
-  (gram) / 3e-2 (standard), the distance that rounding the normalised input to fp16
-  alone produces on these near-low-rank inputs.
+  exact float64 iteration too: the measured distance is recorded, and held to 2e-2.
 """
 
 import numpy as np
@@ -30,7 +28,7 @@ from test_gpu_parity import TOL_DELTA, TOL_FP32, TOL_NS, compare, elementwise, r
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-TOL_EXACT = {"gram": 2.5e-2, "standard": 3e-2}
+TOL_EXACT = {"gram": TOL_NS, "standard": TOL_NS}
 
 
 @pytest.fixture(scope="module")
