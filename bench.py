@@ -462,14 +462,16 @@ def _kernels_block(per_kind, steps, peaks):
     return out
 
 
-def _e2e(nsm, S, stream, reps, upload_by="engine", sm_ctas=16):
-    """The step end to end through the public API with host buffers: every step copies
-    its bf16 grads (and the AdamW group's) host -> device from pinned memory, runs the
+def _e2e(nsm, S, stream, reps, upload_by="mapped", sm_ctas=16):
+    """The step end to end through the public API with host buffers: every step moves
+    its bf16 grads (and the AdamW group's) from pinned host memory to the GPU, runs the
     step, and reads back the bf16 copy of the updated Muon parameters that the step
-    writes.  Two copy streams and triple-buffered device buffers let the uploads run up
-    to two steps ahead of the compute and the read-back one step behind it, so a slow
-    copy has a step of slack.  Every copy and every step is bracketed by events on its
-    own stream, so the line records where the time went."""
+    writes.  upload_by "mapped" (the default): the step's first pass reads the pinned
+    grads in place, over the host link, once; "engine" / "sm": a copy before the step, by
+    the copy engine or by SM loads, on its own stream, triple-buffered so that uploads run
+    up to two steps ahead of the compute.  The read-back runs one step behind the compute
+    on a second copy stream.  Every copy and every step is bracketed by events on its own
+    stream, so the line records where the time went."""
     import torch
     dev = S.dev
     h2d = torch.cuda.Stream()
@@ -489,8 +491,13 @@ def _e2e(nsm, S, stream, reps, upload_by="engine", sm_ctas=16):
         d_agrads = [S.adam[0]] + [torch.empty_like(S.adam[0]) for _ in range(nbuf - 1)]
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
+    mapped = upload_by == "mapped"
+
     def upload(slot):
-        # the library's SM-load upload (nsm_copy_to_device) or the copy engine
+        # the library's SM-load upload (nsm_copy_to_device) or the copy engine; mapped:
+        # nothing to copy, the step's first pass reads the page-locked grads in place
+        if mapped:
+            return
         if upload_by == "sm":
             nsm.copy_to_device(d_grads[slot], h_grads, h2d, sm_ctas)
             if d_agrads is not None:
@@ -524,8 +531,8 @@ def _e2e(nsm, S, stream, reps, upload_by="engine", sm_ctas=16):
             if k >= nbuf:
                 stream.wait_event(dn[k - nbuf][1])  # step k - nbuf's result has left d_out[cur]
             cp[k][0].record(stream)
-            S.step(nsm, stream, grads=d_grads[cur], params_bf16=d_out[cur],
-                   adam_grads=None if d_agrads is None else d_agrads[cur])
+            S.step(nsm, stream, grads=h_grads if mapped else d_grads[cur], params_bf16=d_out[cur],
+                   adam_grads=None if d_agrads is None else (h_agrads if mapped else d_agrads[cur]))
             cp[k][1].record(stream)
             if k + nbuf - 1 < reps:
                 issue_upload(k + nbuf - 1)
@@ -556,10 +563,11 @@ def _e2e(nsm, S, stream, reps, upload_by="engine", sm_ctas=16):
            "steps": reps, "statistic": "median of 3 timed passes",
            "overlap": "copies on two streams, triple-buffered (uploads up to two steps ahead)",
            "upload": (f"SM loads over the host link (nsm_copy_to_device, {sm_ctas} CTAs)" if upload_by == "sm"
-                      else "copy engine (cudaMemcpyAsync)"),
+                      else "read in place from page-locked host memory by the step's first pass (inside compute)"
+                      if mapped else "copy engine (cudaMemcpyAsync)"),
            "download": "copy engine (cudaMemcpyAsync)",
            "breakdown": {k: med[k] for k in med if k != "ms_per_step"},
-           "h2d_gbs": h2d_bytes / (med["h2d_ms_per_step"] * 1e-3) / 1e9,
+           "h2d_gbs": None if mapped else h2d_bytes / (med["h2d_ms_per_step"] * 1e-3) / 1e9,
            "d2h_gbs": S.total * 2 / (med["d2h_ms_per_step"] * 1e-3) / 1e9,
            "passes_ms": [p["ms_per_step"] for p in passes]}
     # the bound: the slowest of the three streams per step
@@ -786,8 +794,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true")
-    ap.add_argument("--upload", default="engine", choices=["engine", "sm"],
-                    help="e2e: grads uploaded by the copy engine (default) or by SM loads (nsm_copy_to_device)")
+    ap.add_argument("--upload", default="mapped", choices=["mapped", "engine", "sm"],
+                    help="e2e: grads read in place from page-locked host memory by the step's first pass "
+                         "(mapped, the default), or uploaded before the step by the copy engine or by SM "
+                         "loads (nsm_copy_to_device)")
     ap.add_argument("--split", default="replicas", choices=["replicas", "owners"],
                     help="N > 1: every rank runs its own copy of the table (replicas, weak scaling), "
                          "or one table is split among the ranks by dedicated ownership (owners, "

@@ -120,7 +120,10 @@ size_t muon_workspace_bytes(const int32_t* shapes, int n, int ns_method, int ns_
  *     X <- ns_steps quintic Newton-Schulz steps (a, b, c) = (3.4445, -4.7750, 2.0315)
  *          in the standard or gram form (ns_method: NSM_NS_*)
  *     p <- p*(1 - lr*wd) - lr*sqrt(max(1, rows/cols))*O      (O transposed back)
- *   packed_grads  device, bf16 bits, read only
+ *   packed_grads  bf16 bits, read only: device memory, or page-locked host memory with a
+ *                 device mapping (cudaHostAlloc / cudaMallocHost, or cudaHostRegister with
+ *                 a mapping), which the step's first pass then reads in place over the host
+ *                 link, once, with no copy; pageable host memory is refused (NSM_ERR_ARG)
  *   packed_params device, fp32, updated in place (the owner's master copy)
  *   momentum      device, fp32, updated in place
  *   offsets       host, n int64 element offsets (shared by the three buffers)

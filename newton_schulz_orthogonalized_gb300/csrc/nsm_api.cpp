@@ -1012,6 +1012,27 @@ bool ranges_overlap(const void* a, size_t an, const void* b, size_t bn) {
   return a0 < b0 + bn && b0 < a0 + an;
 }
 
+// The address the kernels use for a buffer they read: device (or managed) memory as it
+// is, page-locked host memory through its device mapping (read in place over the host
+// link).  Pageable host memory is refused here instead of faulting a kernel.
+int readable_view(const void* p, const char* what, const void** out) {
+  cudaPointerAttributes a{};
+  const cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(NSM_ERR_ARG, "%s: cudaPointerGetAttributes failed (%s)", what, cudaGetErrorString(e));
+  }
+  if (a.type == cudaMemoryTypeUnregistered)
+    return fail(NSM_ERR_ARG, "%s is neither device memory nor page-locked host memory", what);
+  if (a.type == cudaMemoryTypeHost) {
+    if (!a.devicePointer) return fail(NSM_ERR_ARG, "%s is page-locked host memory without a device mapping", what);
+    *out = a.devicePointer;
+  } else {
+    *out = p;
+  }
+  return NSM_OK;
+}
+
 int check_workspace(void* ws, size_t ws_bytes, size_t need) {
   if (!ws) return fail(NSM_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(ws, 256)) return fail(NSM_ERR_ALIGN, "workspace is not 256-byte aligned");
@@ -1317,6 +1338,10 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   const Layout L = make_layout(shapes, n, ns_method, ns_steps);
   rc = check_workspace(workspace, workspace_bytes, L.bytes);
   if (rc != NSM_OK) return rc;
+  const void* grads = nullptr;  // the address the kernels read G at
+  rc = readable_view(packed_grads, "packed_grads", &grads);
+  if (rc != NSM_OK) return rc;
+  if (!aligned(grads, 16)) return fail(NSM_ERR_ALIGN, "packed_grads' device mapping is not 16-byte aligned");
 
   Plan* P = get_plan(shapes, offsets, n, ns_method, ns_steps, workspace, workspace_bytes, &rc);
   if (!P) return rc;
@@ -1335,8 +1360,8 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   // (the one the previous step on this table chose), per-tile sums and maxima of U.
   {
     TimedLaunch t(stream, NSM_KIND_MOMENTUM, 12.0 * elems);
-    e = launch_momentum_class(packed_grads, momentum, nesterov, mu, ws + L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats,
-                              n, L.total_tiles, hints, tparts, redo, stream);
+    e = launch_momentum_class(grads, momentum, nesterov, mu, ws + L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n,
+                              L.total_tiles, hints, tparts, redo, stream);
   }
   if (e != cudaSuccess) return fail_cuda(e, "momentum/layout launch");
   ++launches;
@@ -1353,8 +1378,8 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   // of the gradients' magnitude); every other matrix is skipped
   {
     TimedLaunch t(stream, NSM_KIND_LAYOUT, 0.0);
-    e = launch_to_class(packed_grads, momentum, 1, nesterov, mu, ws + L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats,
-                        n, L.total_tiles, scales, redo, stream);
+    e = launch_to_class(grads, momentum, 1, nesterov, mu, ws + L.off_x[0], P->x_fp16 ? 1 : 0, P->d_mats, n,
+                        L.total_tiles, scales, redo, stream);
   }
   if (e != cudaSuccess) return fail_cuda(e, "layout launch");
   ++launches;
