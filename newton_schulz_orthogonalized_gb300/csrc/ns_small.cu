@@ -88,20 +88,6 @@ struct Store<true> {
   __device__ static __forceinline__ T from_f(float v) { return __float2half_rn(v); }
 };
 
-// Two values rounded to the storage format, packed into one word (the first in the low half).
-template <bool FP16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi);
-template <>
-__device__ __forceinline__ uint32_t pack2<true>(float lo, float hi) {
-  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
-         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
-}
-template <>
-__device__ __forceinline__ uint32_t pack2<false>(float lo, float hi) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-}
-
 // Byte offset of 16-byte unit u (0..7) of row `row` in a 128-byte-swizzled panel.
 __device__ __forceinline__ uint32_t sw(int row, int u) {
   return static_cast<uint32_t>(row * 128 + ((u ^ (row & 7)) << 4));
