@@ -143,3 +143,25 @@ def test_storage_mutants_fail():
         return x
     assert not np.array_equal(no_round_a(x), good)
     assert not np.array_equal(unrounded_input(x), good)
+
+
+def test_input_storage_mutants_fail():
+    # the stored normalised input is s * rnd(U): U rounded to the format's significant
+    # bits at any exponent, s applied unrounded.  Two slips a rewrite could make -- rounding
+    # s U into fp16's range (the earlier reading), or rounding U inside fp16's range
+    # (subnormals and all) -- both fail the pin of
+    # test_oracle.py::test_orthogonalize_stores_the_input_as_rounded_u_times_its_scale.
+    import math
+    u = np.array([[1.0 + 2 ** -12, 2.0 ** -30, -3.0],
+                  [0.5, -(2.0 ** -36) * (1 + 2 ** -9), 0.0]])
+    s = 1.0 / (math.sqrt(float(np.sum(u * u))) + 1e-7)
+    good = oracle.orthogonalize(u, "standard", 0, storage="fp16")
+
+    def rounded_after_scale(u):
+        return oracle.round_to(s * u, "fp16")
+
+    def rounded_in_range(u):
+        return s * oracle.round_to(u, "fp16")
+
+    for mutant in (rounded_after_scale, rounded_in_range):
+        assert not np.array_equal(mutant(u), good), mutant.__name__
