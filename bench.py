@@ -492,6 +492,16 @@ def _e2e(nsm, S, stream, reps, upload_by="mapped", sm_ctas=16):
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     mapped = upload_by == "mapped"
+    if mapped:
+        # the step reads the pinned grads through their device mapping; where the host
+        # memory has none (nsm_copy_to_device checks the same thing), the copy engine
+        # uploads them instead and the line says so
+        try:
+            probe = torch.empty(8, dtype=torch.bfloat16, device=dev)
+            nsm.copy_to_device(probe, h_grads[:8], stream)
+            torch.cuda.synchronize()
+        except nsm.NsmError:
+            mapped, upload_by = False, "engine"
 
     def upload(slot):
         # the library's SM-load upload (nsm_copy_to_device) or the copy engine; mapped:
