@@ -322,11 +322,9 @@ __global__ void __launch_bounds__(kThreads)
   grid_dependency_sync();  // inputs come from the previous kernel of the stream
   release_dependents();
   __shared__ float tile[kTile][kTile + 1];
-  __shared__ float scratch[2][2][kThreads / 32];
-  static_assert(kTileParts == 1 || kTileParts == kThreads / 32, "one partial per tile, or one per warp");
+  static_assert(kTileParts == kThreads / 32, "one partial sum and maximum per warp and tile");
   constexpr int K = NSM_KERNEL_MOMENTUM;
   if (blockIdx.x == 0 && threadIdx.x == 0) *redo = 0;  // the finalize kernel sets it
-  int rb = 0;
   for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
     const TilePos tp = tile_pos(mats, nmats, t);
     const MatInfo& mt = mats[tp.mi];
@@ -454,18 +452,14 @@ __global__ void __launch_bounds__(kThreads)
       }
       __syncthreads();
     }
-    if (kTileParts == 1) {
-      block_sum_max(acc, mx, scratch[rb]);
-      rb ^= 1;
-    } else {
+    // each warp's sum and maximum over its elements of the tile, in a fixed order
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      }
+    for (int o = 16; o > 0; o >>= 1) {
+      acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
-    const int part = kTileParts == 1 ? 0 : static_cast<int>(threadIdx.x >> 5);
-    if ((kTileParts == 1 && threadIdx.x == 0) || (kTileParts > 1 && (threadIdx.x & 31) == 0)) {
+    if ((threadIdx.x & 31) == 0) {
+      const int part = static_cast<int>(threadIdx.x >> 5);
       tparts[t * kTileParts + part] = acc;
       tparts[(total_tiles + t) * kTileParts + part] = mx;
     }
