@@ -82,6 +82,18 @@ int nsm_route(const char* name, int ndim);
 int nsm_pack(const int32_t* shapes, int n, int64_t align_elems,
              int64_t* offsets_out, int64_t* total_out);
 
+/* The exponent rule of muon_step's stored input (host-only; the kernels apply the same
+ * function).  A matrix's normalised input is held as U 2^k rounded once to the storage
+ * format; max_abs is its largest |U|.  With has_hint != 0 (the step), U was stored with
+ * 2^hint (hint clamped to [-120, 120]): *store_out = 0 and *k_out = hint when
+ * max_abs 2^hint lies in [2^4, 2^15), else *store_out = 1 and *k_out the exponent that
+ * puts max_abs 2^k in [2^11, 2^12).  With has_hint == 0 (the orthogonalisation) *k_out
+ * is that exponent and *store_out = 1.  *next_out is the hint the step leaves for its
+ * next call: that exponent, or the hint when max_abs is 0, infinite or NaN (no exponent
+ * follows from it; *k_out is then the hint, or 0).  Returns NSM_ERR_NULL for a NULL
+ * output. */
+int nsm_input_exponent(float max_abs, int has_hint, int hint, int* k_out, int* next_out, int* store_out);
+
 /* Dedicated ownership ([DMZ] §两种packed buffer生命周期 and §每步通信字节数: every
  * Muon-target matrix has one owner, which alone runs its Newton-Schulz chain).  Assigns
  * the n matrices of a table to `world` owners by longest-processing-time-first on the

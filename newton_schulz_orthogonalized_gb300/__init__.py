@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
     L.nsm_route.restype = ctypes.c_int
     L.nsm_pack.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int64, _c_i64p, _c_i64p]
     L.nsm_pack.restype = ctypes.c_int
+    _c_ip = ctypes.POINTER(ctypes.c_int)
+    L.nsm_input_exponent.argtypes = [ctypes.c_float, ctypes.c_int, ctypes.c_int, _c_ip, _c_ip, _c_ip]
+    L.nsm_input_exponent.restype = ctypes.c_int
     L.nsm_assign_owners.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, _c_i32p, _c_i64p]
     L.nsm_assign_owners.restype = ctypes.c_int
@@ -156,6 +159,15 @@ def last_launch_count() -> int:
 def route(name: str, ndim: int) -> bool:
     """Muon (True) or AdamW (False) for a named parameter of ``ndim`` dimensions."""
     return bool(_check(lib().nsm_route(name.encode("utf-8"), int(ndim))))
+
+
+def input_exponent(max_abs: float, hint=None) -> Tuple[int, int, bool]:
+    """(k, next hint, store again) of the stored input's exponent rule for a matrix whose
+    largest |U| is ``max_abs`` (a float32 value), with the step's hint or without one."""
+    k, nxt, store = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().nsm_input_exponent(float(max_abs), 0 if hint is None else 1, 0 if hint is None else int(hint),
+                                    ctypes.byref(k), ctypes.byref(nxt), ctypes.byref(store)))
+    return k.value, nxt.value, bool(store.value)
 
 
 def _shapes_array(shapes: Sequence[Tuple[int, int]]) -> np.ndarray:

@@ -154,12 +154,6 @@ __device__ __forceinline__ void block_sum_max(float& sum, float& mx, float (*scr
 
 // 2^k for k in [-126, 127] (built from its bits: exact)
 __device__ __forceinline__ float pow2f(int k) { return __int_as_float((k + 127) << 23); }
-__device__ __forceinline__ int clamp_exp(int k) { return max(-kInExpClamp, min(kInExpClamp, k)); }
-// e with x = f 2^e, f in [0.5, 1), of a positive finite x (subnormals count as 2^-126)
-__device__ __forceinline__ int frexp_exponent(float x) {
-  const int biased = (__float_as_int(x) >> 23) & 0xff;
-  return (biased == 0 ? 1 : biased) - 126;
-}
 
 // ---------------------------------------------------------------- bounds checks
 
@@ -248,23 +242,13 @@ __global__ void __launch_bounds__(kThreads)
     rb ^= 1;
     if (threadIdx.x != 0) continue;
     const float s = 1.0f / (sqrtf(sum) + eps);
-    // no exponent follows from an all-zero or non-finite matrix: its hint stands
-    const bool has_max = mx > 0.f && mx < INFINITY;
-    const int e = has_max ? frexp_exponent(mx) : 0;
-    int k;
+    const InExponent r = in_exponent(mx, hints != nullptr, hints ? hints[i] : 0);
+    layout_scale[i] = r.store ? pow2f(r.k) : 0.f;
     if (hints) {
-      const int used = clamp_exp(hints[i]);
-      const bool ok = !has_max || (e + used >= kInMinExp && e + used <= kInMaxExp);
-      const int next = has_max ? clamp_exp(kInTargetExp - e) : used;
-      k = ok ? used : next;
-      layout_scale[i] = ok ? 0.f : pow2f(k);
-      if (!ok) *redo = 1;
-      hints[i] = next;
-    } else {
-      k = has_max ? clamp_exp(kInTargetExp - e) : 0;
-      layout_scale[i] = pow2f(k);
+      if (r.store) *redo = 1;
+      hints[i] = r.next;
     }
-    const float f = s * pow2f(-k);
+    const float f = s * pow2f(-r.k);
     xs[i] = f;
     xs_cls[mt.cls_pos] = f;
   }
@@ -331,7 +315,7 @@ __global__ void __launch_bounds__(kThreads)
     const __nv_bfloat16* g = grads + mt.off;
     float* m = mom + mt.off;
     const int64_t d0 = mt.slot;
-    const float sc = pow2f(clamp_exp(hints[tp.mi]));
+    const float sc = pow2f(in_clamp_exp(hints[tp.mi]));
     const int rows = mt.rows, cols = mt.cols, ld = mt.ld;
     const int64_t len = static_cast<int64_t>(rows) * cols;
     float acc = 0.f, mx = 0.f;

@@ -1229,6 +1229,15 @@ int nsm_route(const char* name, int ndim) {
   return 1;
 }
 
+int nsm_input_exponent(float max_abs, int has_hint, int hint, int* k_out, int* next_out, int* store_out) {
+  if (!k_out || !next_out || !store_out) return fail(NSM_ERR_NULL, "an output pointer is NULL");
+  const InExponent r = in_exponent(max_abs, has_hint != 0, hint);
+  *k_out = r.k;
+  *next_out = r.next;
+  *store_out = r.store;
+  return NSM_OK;
+}
+
 int nsm_pack(const int32_t* shapes, int n, int64_t align_elems, int64_t* offsets_out, int64_t* total_out) {
   if (!offsets_out || !total_out) return fail(NSM_ERR_NULL, "output pointer is NULL");
   int rc = validate_shapes(shapes, n);

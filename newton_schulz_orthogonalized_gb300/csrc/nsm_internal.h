@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "nsmuon.h"
 
@@ -83,6 +84,49 @@ constexpr int kInExpClamp = 120;  // |k| at most this (2^k and 2^-k are normal f
 // Partial sums (and maxima) the step's pass writes per 64 x 64 tile: one per warp of its
 // 256-thread blocks, so that no block-wide barrier is needed to combine them.
 constexpr int kTileParts = 8;
+
+// e with x = f 2^e, f in [0.5, 1), of a positive finite float (subnormals count as 2^-126)
+__host__ __device__ inline int in_frexp_exponent(float x) {
+  uint32_t b;
+  memcpy(&b, &x, sizeof b);
+  const int biased = static_cast<int>((b >> 23) & 0xffu);
+  return (biased == 0 ? 1 : biased) - 126;
+}
+
+__host__ __device__ inline int in_clamp_exp(int k) {
+  return k < -kInExpClamp ? -kInExpClamp : (k > kInExpClamp ? kInExpClamp : k);
+}
+
+// The exponent of one matrix's stored input, from its largest |U| (max_abs), on the host
+// and in k_scale_finalize alike.
+struct InExponent {
+  int k;      // U is (or is to be) stored as U 2^k
+  int next;   // the hint for the next call on the table
+  int store;  // 1: U must be stored with 2^k by the layout pass (0: what is stored stands)
+};
+
+// With a hint (the step), U was stored with 2^hint (clamped): that stands when
+// max_abs 2^hint lies in [2^4, 2^15), and otherwise U is stored again with the exponent
+// that puts max_abs 2^k in [2^11, 2^12), which is also the next hint.  Without a hint
+// (the orthogonalisation) that exponent is the one used.  A matrix whose max_abs is 0,
+// infinite or NaN yields no exponent: its hint (or 0) stands.
+__host__ __device__ inline InExponent in_exponent(float max_abs, bool has_hint, int hint) {
+  const bool has_max = max_abs > 0.f && max_abs <= 3.40282347e38f;
+  const int e = has_max ? in_frexp_exponent(max_abs) : 0;
+  InExponent r;
+  if (has_hint) {
+    const int used = in_clamp_exp(hint);
+    const bool ok = !has_max || (e + used >= kInMinExp && e + used <= kInMaxExp);
+    r.next = has_max ? in_clamp_exp(kInTargetExp - e) : used;
+    r.k = ok ? used : r.next;
+    r.store = ok ? 0 : 1;
+  } else {
+    r.k = has_max ? in_clamp_exp(kInTargetExp - e) : 0;
+    r.next = r.k;
+    r.store = 1;
+  }
+  return r;
+}
 
 // Elements of one momentum/norm chunk (256 threads x 8 vectors of 8).
 constexpr int kChunk = 16384;
