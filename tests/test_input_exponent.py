@@ -89,3 +89,31 @@ def test_null_outputs_refused(lib):
     import ctypes
     k = ctypes.c_int(0)
     assert lib.nsm_input_exponent(1.0, 0, 0, None, ctypes.byref(k), ctypes.byref(k)) == nsm.NSM_ERR_NULL
+
+
+def test_stored_input_is_the_oracles_rounding_for_every_accepted_exponent(lib):
+    # The step stores U as fp16(U 2^k) and multiplies by 2^-k (inside s 2^-k).  For every
+    # k the rule accepts, that is the oracle's rnd(U) -- U rounded to fp16's 11
+    # significant bits at any exponent -- on every entry within 2^18 of the matrix's
+    # largest (numpy's float16 conversion is the rounding here, not the oracle's code);
+    # smaller entries may land in fp16's subnormals.  bf16 storage has no such range.
+    import torch
+
+    import oracle
+    rng = np.random.default_rng(7)
+    for scale in (1e-30, 1e-6, 1.0, 3e4, 1e30):
+        u = (rng.standard_normal(4096) * scale * np.exp(rng.uniform(-8, 0, size=4096))).astype(np.float32)
+        u = u.astype(np.float64)
+        m = float(np.max(np.abs(u)))
+        want16 = oracle.round_significand(u, "fp16")
+        want_bf = oracle.round_significand(u, "bf16")
+        k0 = nsm.input_exponent(m)[0]
+        accepted = [k for k in range(k0 - 12, k0 + 12) if not nsm.input_exponent(m, k)[2]]
+        assert accepted and k0 in accepted, (scale, k0, accepted)
+        big = np.abs(u) >= m * 2.0 ** -18
+        for k in accepted:
+            stored = np.ldexp(np.ldexp(u, k).astype(np.float16).astype(np.float64), -k)
+            assert np.all(np.isfinite(stored)), (scale, k)
+            assert np.array_equal(stored[big], want16[big]), (scale, k)
+            y = torch.from_numpy(np.ldexp(u, k).astype(np.float32)).to(torch.bfloat16).double().numpy()
+            assert np.array_equal(np.ldexp(y, -k), want_bf), (scale, k)
