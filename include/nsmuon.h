@@ -176,7 +176,9 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
 
 /* Orthogonalisation only: out_i = NS(in_i / (||in_i||_F + 1e-7)) for every matrix of a
  * packed bf16 group (the same transpose rule and methods as muon_step).  in_bf16 and
- * out_bf16 are device bf16 buffers sharing the offsets table; they may not overlap.
+ * out_bf16 are bf16 buffers sharing the offsets table, in device memory or in page-locked
+ * host memory with a device mapping (then read or written in place over the host link);
+ * they may not overlap, and pageable host memory is refused (NSM_ERR_ARG).
  * The input is held as in_i 2^k with k from a first pass over in_i (its sums and
  * largest entry), exact in the storage format for bf16 entries within 2^26 of the
  * largest.  Used to check and time the Newton-Schulz chain on its own. */

@@ -1012,10 +1012,10 @@ bool ranges_overlap(const void* a, size_t an, const void* b, size_t bn) {
   return a0 < b0 + bn && b0 < a0 + an;
 }
 
-// The address the kernels use for a buffer they read: device (or managed) memory as it
-// is, page-locked host memory through its device mapping (read in place over the host
-// link).  Pageable host memory is refused here instead of faulting a kernel.
-int readable_view(const void* p, const char* what, const void** out) {
+// The address the kernels use for a buffer: device (or managed) memory as it is,
+// page-locked host memory through its device mapping (read or written in place over the
+// host link).  Pageable host memory is refused here instead of faulting a kernel.
+int device_view(const void* p, const char* what, const void** out) {
   cudaPointerAttributes a{};
   const cudaError_t e = cudaPointerGetAttributes(&a, p);
   if (e != cudaSuccess) {
@@ -1030,6 +1030,16 @@ int readable_view(const void* p, const char* what, const void** out) {
   } else {
     *out = p;
   }
+  return NSM_OK;
+}
+
+// The orthogonalisation's input and output, as device_view gives them, 16-byte aligned.
+int device_views(const void* in_bf16, const void* out_bf16, const void** in, const void** out) {
+  int rc = device_view(in_bf16, "in_bf16", in);
+  if (rc != NSM_OK) return rc;
+  rc = device_view(out_bf16, "out_bf16", out);
+  if (rc != NSM_OK) return rc;
+  if (!aligned(*in, 16) || !aligned(*out, 16)) return fail(NSM_ERR_ALIGN, "a device mapping is not 16-byte aligned");
   return NSM_OK;
 }
 
@@ -1348,7 +1358,7 @@ int muon_step_with_copy(const void* packed_grads, float* packed_params, float* m
   rc = check_workspace(workspace, workspace_bytes, L.bytes);
   if (rc != NSM_OK) return rc;
   const void* grads = nullptr;  // the address the kernels read G at
-  rc = readable_view(packed_grads, "packed_grads", &grads);
+  rc = device_view(packed_grads, "packed_grads", &grads);
   if (rc != NSM_OK) return rc;
   if (!aligned(grads, 16)) return fail(NSM_ERR_ALIGN, "packed_grads' device mapping is not 16-byte aligned");
 
@@ -1423,12 +1433,16 @@ int muon_orthogonalize(const void* in_bf16, void* out_bf16, const int64_t* offse
   const Layout L = make_layout(shapes, n, ns_method, ns_steps);
   rc = check_workspace(workspace, workspace_bytes, L.bytes);
   if (rc != NSM_OK) return rc;
+  const void* in = nullptr;
+  const void* out = nullptr;
+  rc = device_views(in_bf16, out_bf16, &in, &out);
+  if (rc != NSM_OK) return rc;
 
   Plan* P = get_plan(shapes, offsets, n, ns_method, ns_steps, workspace, workspace_bytes, &rc);
   if (!P) return rc;
   const PdlScope pdl(P->elems);
   int launches = 0;
-  rc = run_orthogonalize(*P, in_bf16, out_bf16, n, stream, &launches);
+  rc = run_orthogonalize(*P, in, const_cast<void*>(out), n, stream, &launches);
   if (rc != NSM_OK) return rc;
   t_last_launches = launches;
   return NSM_OK;
@@ -1601,6 +1615,10 @@ int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16, const int64_
                 "the allocation-free path holds %zu bytes; this table needs %zu bytes of workspace (use "
                 "muon_orthogonalize with a caller workspace)",
                 kNoAllocBytes, ws_bytes);
+  const void* in = nullptr;
+  const void* out = nullptr;
+  rc = device_views(in_bf16, out_bf16, &in, &out);
+  if (rc != NSM_OK) return rc;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
@@ -1628,7 +1646,7 @@ int muon_orthogonalize_noalloc(const void* in_bf16, void* out_bf16, const int64_
   Plan& P = *st->plan;
   const PdlScope pdl(P.elems);
   int launches = 0;
-  rc = run_orthogonalize(P, in_bf16, out_bf16, n, stream, &launches);
+  rc = run_orthogonalize(P, in, const_cast<void*>(out), n, stream, &launches);
   if (rc != NSM_OK) return rc;
   t_last_launches = launches;
   return NSM_OK;
