@@ -3,8 +3,8 @@
 //   k_momentum_class  M <- mu M + G and U = G + mu M (Nesterov) or M, in one pass: M
 //                     written back, U 2^k (k from the matrix's exponent hint) moved from
 //                     the natural row-major layout into the matrix's slot (transposed
-//                     when rows > cols) and rounded once to bf16 or fp16; per-tile sums of
-//                     U^2 and largest |U|, in fp32 (fixed order)
+//                     when rows > cols) and rounded once to bf16 or fp16; for each warp of
+//                     each tile the sum of U^2 and the largest |U|, in fp32 (fixed order)
 //   k_grad_norm       per-chunk sums of G^2 and largest |G| (the orthogonalisation)
 //   k_scale_finalize  s_i = 1 / (sqrt(sum of matrix i's partial sums) + eps), fixed order;
 //                     the exponent k_i that puts max|U| 2^k in [2^11, 2^12); the input
@@ -217,8 +217,9 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// One block per matrix: sums and maxima of its partials (parts[begin + c] and
-// parts[nparts + begin + c]), then s, the exponent and the input factor.
+// One block per matrix: sums and maxima of its partials (per unit: one per chunk, or
+// kTileParts per tile when by_tile; the maxima nparts units after the sums), then s, the
+// exponent and the input factor.
 __global__ void __launch_bounds__(kThreads)
     k_scale_finalize(const MatInfo* __restrict__ mats, int nmats, const float* __restrict__ parts,
                      int64_t nparts, int by_tile, int* __restrict__ hints, float* __restrict__ layout_scale,
@@ -295,8 +296,9 @@ __device__ __forceinline__ float load_u1(const __nv_bfloat16* g, const float* m,
 
 // The step's pass over G and M: M <- mu M + G written back in place, U = G + mu M
 // (Nesterov) or M stored as U 2^k (k = the matrix's hint) into the slot (row stride ld),
-// transposed when rows > cols, rounded once to bf16/fp16; per tile the sum of U^2 and the
-// largest |U| (tparts[t], tparts[total_tiles + t]).
+// transposed when rows > cols, rounded once to bf16/fp16; for each warp w of tile t the
+// sum of U^2 and the largest |U| over its elements (tparts[t kTileParts + w], and
+// kTileParts total_tiles entries later).
 template <bool TO_FP16, bool NESTEROV>
 __global__ void __launch_bounds__(kThreads)
     k_momentum_class(const __nv_bfloat16* __restrict__ grads, float* __restrict__ mom, float mu,
